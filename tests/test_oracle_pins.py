@@ -1,0 +1,393 @@
+"""Pins of the CPU oracle to facts outside itself (no GPU).
+
+Each test ties one oracle function to a closed form, an invariant, a brute-force
+enumeration or a library routine, chosen so that a plausible mistake (a dropped
+relu, a swapped head weight, a transposed operand, a wrong slot mapping, a
+reversed tie-break, a misplaced fp8 scale, a sink multiplied by the scale) makes
+at least one of them fail.
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from deepseek_sparse_attention_dsa_gb300 import workloads as W
+from tests.dsa_cases import bf16, make_case, phys_rows, tiny_shape
+
+
+# ----------------------------------------------------------------------------
+# fp8 e4m3 (OCP FP8 "E4M3FN")
+# ----------------------------------------------------------------------------
+def test_e4m3_all_codes_match_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_values(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert set(np.nonzero(nan)[0]) == {0x7F, 0xFF}
+
+
+def test_e4m3_spec_points():
+    v = oracle.e4m3_values([0x7E, 0x01, 0x08, 0x38, 0xB8, 0x80, 0x07])
+    assert v[0] == 448.0                 # largest finite: 1.75 * 2^8
+    assert v[1] == 2.0 ** -9             # smallest subnormal: 1/8 * 2^-6
+    assert v[2] == 2.0 ** -6             # smallest normal
+    assert v[3] == 1.0 and v[4] == -1.0
+    assert v[5] == 0.0 and math.copysign(1.0, v[5]) < 0
+    assert v[6] == 7.0 / 8.0 * 2.0 ** -6  # largest subnormal
+
+
+# ----------------------------------------------------------------------------
+# slot mapping (DSASpan: page_start is the first token's offset in the pages)
+# ----------------------------------------------------------------------------
+def test_store_keys_slot_mapping_literal():
+    # page_size 2, pages [3, 1], page_start 1: positions 0, 1, 2 sit at slots 1, 2, 3,
+    # i.e. (page 3, slot 1), (page 1, slot 0), (page 1, slot 1) -> physical rows 7, 2, 3.
+    sh = tiny_shape(index_dim=2, page_size=2)
+    case = make_case(sh, [(0, 3)], pages=[[3, 1]], page_start=1, num_pages=4)
+    keys = bf16([[1, 2], [3, 4], [5, 6]])
+    cache = torch.zeros(4, 2, 2, dtype=torch.bfloat16)
+    out = oracle.store_keys(sh, case.spans, 4, keys, cache).view(np.uint16)
+    flat = torch.from_numpy(out.reshape(8, 2).astype(np.int16)).view(torch.bfloat16).float().numpy()
+    expect = np.zeros((8, 2))
+    expect[7] = [1, 2]
+    expect[2] = [3, 4]
+    expect[3] = [5, 6]
+    assert np.array_equal(flat, expect)
+
+
+def test_store_keys_fp8_page_blocked_literal():
+    # fp8 index rows: each page = [page_size x 128 codes][page_size x fp32 scale]
+    sh = tiny_shape(index_dim=128, page_size=2, index_fmt=W.INDEX_FP8_132)
+    case = make_case(sh, [(0, 3)], pages=[[1, 0]], page_start=0, num_pages=2)
+    keys = np.zeros((3, 132), np.uint8)
+    for r in range(3):
+        keys[r, :128] = 10 + r
+        keys[r, 128:] = np.frombuffer(np.float32(r + 0.5).tobytes(), np.uint8)
+    cache = np.zeros((2, 2 * 132), np.uint8)
+    out = oracle.store_keys(sh, case.spans, 2, keys, cache).reshape(2, 264)
+    # position 0 -> page 1 slot 0, position 1 -> page 1 slot 1, position 2 -> page 0 slot 0
+    assert (out[1, 0:128] == 10).all() and (out[1, 128:256] == 11).all() and (out[0, 0:128] == 12).all()
+    assert np.frombuffer(out[1, 256:260].tobytes(), np.float32)[0] == 0.5
+    assert np.frombuffer(out[1, 260:264].tobytes(), np.float32)[0] == 1.5
+    assert np.frombuffer(out[0, 256:260].tobytes(), np.float32)[0] == 2.5
+    assert (out[0, 128:256] == 0).all()
+
+
+# ----------------------------------------------------------------------------
+# indexer score: sum_h w[h] * relu(q[h] . k)   (mstar index_topk)
+# ----------------------------------------------------------------------------
+def _score_case(index_fmt=W.INDEX_BF16, page_start=2, pages=((5, 0, 3, 1),)):
+    """Row r (positions 6..9 of one request) has q[r,0] = (r+1, 0, 2), q[r,1] = (-1, 0, 0),
+    w[r] = (1, 5); key j = (j - 5, 7, 0).  Closed form:
+        score(r, j) = (r+1) * relu(j - 5) + 5 * relu(5 - j),  j = 0 .. pos(r)."""
+    Di = 3 if index_fmt == W.INDEX_BF16 else 128
+    sh = tiny_shape(index_dim=Di, page_size=4, index_fmt=index_fmt)
+    case = make_case(sh, [(6, 4)], pages=[list(pages[0])], page_start=page_start, num_pages=6)
+    keys_log = np.zeros((10, Di), np.float32)
+    keys_log[:, 0] = np.arange(10) - 5
+    keys_log[:, 1] = 7
+    rows = phys_rows(case, 0, np.arange(10))
+    if index_fmt == W.INDEX_BF16:
+        cache = np.zeros((6 * 4, Di), np.float32)
+        cache[rows] = keys_log
+        cache = bf16(cache).view(6, 4, Di)
+        step_keys = bf16(keys_log[6:10])
+    else:
+        # e4m3 codes of (j - 5) / 2 and 3.5 with scale 2: e4m3 holds k/2 exactly
+        codes = torch.from_numpy(keys_log / 2.0).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        scale = np.frombuffer(np.float32(2.0).tobytes(), np.uint8)
+        cache = np.zeros((6, 4 * (Di + 4)), np.uint8)
+        for j in range(6):  # history only; the step stores positions 6..9
+            pg, sl = divmod(int(rows[j]), 4)
+            cache[pg, sl * Di:(sl + 1) * Di] = codes[j]
+            cache[pg, 4 * Di + 4 * sl: 4 * Di + 4 * sl + 4] = scale
+        step_keys = np.concatenate([codes[6:10], np.tile(scale, (4, 1))], axis=1)
+    q = np.zeros((4, 2, Di), np.float32)
+    for r in range(4):
+        q[r, 0, 0], q[r, 0, 2], q[r, 1, 0] = r + 1, 2, -1
+    w = np.tile(np.array([1.0, 5.0], np.float32), (4, 1))
+    return sh, case, cache, step_keys, bf16(q), torch.from_numpy(w)
+
+
+@pytest.mark.parametrize("index_fmt", [W.INDEX_BF16, W.INDEX_FP8_132])
+def test_score_closed_form(index_fmt):
+    sh, case, cache, step_keys, q, w = _score_case(index_fmt)
+    cache = oracle.store_keys(sh, case.spans, case.num_pages, step_keys, cache)
+    scores, off = oracle.index_scores(sh, case.spans, case.num_pages, q, w, cache)
+    for r in range(4):
+        p = 6 + r
+        j = np.arange(p + 1)
+        expect = (r + 1) * np.maximum(j - 5, 0) + 5 * np.maximum(5 - j, 0)
+        assert np.array_equal(scores[off[r]:off[r + 1]], expect.astype(np.float32)), r
+
+
+def test_score_paging_invariance():
+    """The same logical keys under other page tables and page_start give the same scores."""
+    a = _score_case(page_start=0, pages=((0, 1, 2),))
+    b = _score_case(page_start=2, pages=((5, 0, 3, 1),))
+    outs = []
+    for sh, case, cache, step_keys, q, w in (a, b):
+        cache = oracle.store_keys(sh, case.spans, case.num_pages, step_keys, cache)
+        outs.append(oracle.index_scores(sh, case.spans, case.num_pages, q, w, cache)[0])
+    assert np.array_equal(outs[0], outs[1])
+
+
+def test_score_negative_weight_and_rounding_once():
+    """A negative head weight subtracts (it is not clipped), and the fp64 sum is
+    rounded to fp32 once: 1 + 2^-30 - 1 survives as 2^-30 only when summed in
+    double before rounding (fp32 partial sums would lose it)."""
+    sh = tiny_shape(index_heads=3, index_dim=1, page_size=4)
+    case = make_case(sh, [(0, 1)])
+    cache = bf16(np.ones((1, 4, 1))).view(1, 4, 1)
+    q = bf16(np.ones((1, 3, 1)))
+    w = torch.tensor([[1.0, 2.0 ** -30, -1.0]], dtype=torch.float32)
+    cache = oracle.store_keys(sh, case.spans, 1, bf16([[1.0]]), cache)
+    s, _ = oracle.index_scores(sh, case.spans, 1, q, w, cache)
+    assert s[0] == np.float32(2.0 ** -30)
+
+
+def test_score_integer_inputs_are_integers():
+    wl = W.build_workload("int", W.DSAShape(index_heads=8, index_dim=64, topk=16, heads=2, kv_lora_rank=4,
+                                            rope_dim=2, page_size=16, sm_scale=1.0),
+                          [(30, 5), (100, 1)], seed=7, dist=W.Distributions(integer=True))
+    ic = W.make_index_cache(wl)
+    st = W.make_step_inputs(wl)
+    cache = oracle.store_keys(wl.shape, wl.spans, wl.num_pages, st.keys, ic)
+    s, _ = oracle.index_scores(wl.shape, wl.spans, wl.num_pages, st.q, st.w, cache)
+    assert np.array_equal(s, np.round(s)) and (s >= 0).all()
+
+
+# ----------------------------------------------------------------------------
+# top-k: ties to the earlier position, -1 padding (mstar select_topk_causal)
+# ----------------------------------------------------------------------------
+def _topk_rows(score_rows, K):
+    sh = tiny_shape(topk=K)
+    case = make_case(sh, [(len(score_rows[0]) - 1, 1)] if len(score_rows) == 1 else
+                     [(len(r) - 1, 1) for r in score_rows])
+    off = np.zeros(len(score_rows) + 1, np.int64)
+    off[1:] = np.cumsum([len(r) for r in score_rows])
+    return oracle.topk(sh, case.spans, np.concatenate(score_rows).astype(np.float32), off)
+
+
+def _defining_property(s, S, K):
+    """S is the top-K set under (score desc, position asc) iff every member ranks
+    before every non-member and |S| = min(K, n)."""
+    n = len(s)
+    if len(S) != min(K, n) or len(set(S)) != len(S):
+        return False
+    rest = [j for j in range(n) if j not in S]
+    return all(s[i] > s[j] or (s[i] == s[j] and i < j) for i in S for j in rest)
+
+
+def test_topk_brute_force_enumeration():
+    rng = np.random.default_rng(3)
+    for n in range(1, 8):
+        for trial in range(6):
+            s = rng.integers(0, 3, size=n).astype(np.float32)   # many ties
+            for K in range(1, n + 2):
+                sel = _topk_rows([s], K)[0]
+                got = [int(x) for x in sel if x >= 0]
+                assert (sel[len(got):] == -1).all()
+                winners = [set(c) for c in itertools.combinations(range(n), min(K, n))
+                           if _defining_property(s, list(c), K)]
+                assert len(winners) == 1
+                assert set(got) == winners[0]
+
+
+def test_topk_tie_cases():
+    n, K = 20, 5
+    assert list(_topk_rows([np.zeros(n)], K)[0]) == [0, 1, 2, 3, 4]
+    assert list(_topk_rows([np.arange(n, dtype=np.float32)], K)[0]) == [19, 18, 17, 16, 15]
+    assert list(_topk_rows([-np.arange(n, dtype=np.float32)], K)[0]) == [0, 1, 2, 3, 4]
+    s = np.zeros(n, np.float32)
+    s[[3, 9, 12]] = 1.0
+    assert list(_topk_rows([s], K)[0]) == [3, 9, 12, 0, 1]
+    # -0.0 and +0.0 are equal scores: the earlier position wins
+    s = np.full(4, -1.0, np.float32)
+    s[1], s[2] = -0.0, 0.0
+    assert list(_topk_rows([s], 1)[0]) == [1]
+
+
+def test_topk_short_rows_pad():
+    sel = _topk_rows([np.array([2.0, 1.0, 3.0], np.float32)], 6)[0]
+    assert list(sel) == [2, 0, 1, -1, -1, -1]
+
+
+def test_topk_random_invariants():
+    rng = np.random.default_rng(11)
+    rows = [rng.standard_normal(n).astype(np.float32).round(1) for n in (1, 7, 64, 65, 300)]
+    K = 64
+    sel = _topk_rows(rows, K)
+    for s, srow in zip(rows, sel):
+        got = [int(x) for x in srow if x >= 0]
+        assert (srow[len(got):] == -1).all()
+        assert all(0 <= j < len(s) for j in got)
+        assert _defining_property(s, got, K)
+        # canonical order: score descending, position ascending
+        keys = [(-float(s[j]), j) for j in got]
+        assert keys == sorted(keys)
+
+
+def test_topk_packing_independence():
+    """A request's selection does not depend on the batch it is packed in nor on its pages."""
+    wl = W.build_workload("pack", W.DSAShape(index_heads=4, index_dim=32, topk=16, heads=2, kv_lora_rank=4,
+                                             rope_dim=2, page_size=8, sm_scale=1.0),
+                          [(40, 3), (0, 25), (70, 1)], seed=5, dist=W.Distributions(integer=True))
+    full = oracle.run_all(wl, W.make_index_cache(wl), W.make_latent_cache(wl), W.make_step_inputs(wl))
+    for order in ([2, 0], [1], [2, 1, 0]):
+        sub = wl.sub_workload(order)
+        got = oracle.run_all(sub, W.make_index_cache(sub), W.make_latent_cache(sub), W.make_step_inputs(sub))
+        r_sub = 0
+        for i in order:
+            s = wl.spans[i]
+            a = full["selection"][s.q_start:s.q_start + s.q_len]
+            b = got["selection"][r_sub:r_sub + s.q_len]
+            assert np.array_equal(a, b)
+            assert np.array_equal(full["out"][s.q_start:s.q_start + s.q_len], got["out"][r_sub:r_sub + s.q_len])
+            r_sub += s.q_len
+
+
+# ----------------------------------------------------------------------------
+# attend: absorbed MLA over the picked latents (mstar DSAManager.attend;
+# ttnn sparse_sdpa for V = the leading kv_lora_rank columns and for the sink)
+# ----------------------------------------------------------------------------
+def _latent_case(H=2, L=4, Rd=2, ctx=6, q_len=3, sm_scale=0.7, seed=0, P=4, pages=None, page_start=1):
+    sh = tiny_shape(heads=H, kv_lora_rank=L, rope_dim=Rd, page_size=P, sm_scale=sm_scale, topk=ctx + q_len)
+    case = make_case(sh, [(ctx, q_len)], pages=pages, page_start=page_start)
+    rng = np.random.default_rng(seed)
+    n = ctx + q_len
+    lat = rng.standard_normal((n, L + Rd)).astype(np.float32)
+    cache = np.zeros((case.num_pages * P, L + Rd), np.float32)
+    cache[phys_rows(case, 0, np.arange(n))] = lat
+    qn = rng.standard_normal((q_len, H, L)).astype(np.float32)
+    qp = rng.standard_normal((q_len, H, Rd)).astype(np.float32)
+    return sh, case, bf16(lat).double(), bf16(cache).view(case.num_pages, P, L + Rd), bf16(qn), bf16(qp)
+
+
+def test_attend_all_keys_equals_dense_causal_sdpa():
+    """With every visible key selected, sparse absorbed MLA is dense causal MQA:
+    q = [q_nope | q_pe], k = [c | k_pe], v = c, one KV head."""
+    H, L, Rd, ctx, q_len = 3, 8, 4, 5, 4
+    sh, case, lat, cache, qn, qp = _latent_case(H=H, L=L, Rd=Rd, ctx=ctx, q_len=q_len, pages=[[2, 0, 1]])
+    K = sh.topk
+    sel = np.full((q_len, K), -1, np.int32)
+    for r in range(q_len):
+        sel[r, :ctx + r + 1] = np.arange(ctx + r + 1)[::-1]   # any order
+    out = oracle.attend(sh, case.spans, case.num_pages, sel, qn, qp, cache)
+    q = torch.cat([qn.double(), qp.double()], dim=-1).transpose(0, 1)          # (H, q_len, L+R)
+    k = lat.unsqueeze(0).expand(H, -1, -1)                                        # (H, n, L+R)
+    v = lat[:, :L].unsqueeze(0).expand(H, -1, -1)
+    mask = torch.zeros(q_len, ctx + q_len, dtype=torch.bool)
+    for r in range(q_len):
+        mask[r, :ctx + r + 1] = True
+    ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=sh.sm_scale)
+    np.testing.assert_allclose(out, ref.transpose(0, 1).numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_attend_single_key_and_equal_latents():
+    sh, case, lat, cache, qn, qp = _latent_case()
+    sel = np.full((3, sh.topk), -1, np.int32)
+    sel[:, 0] = 4
+    out = oracle.attend(sh, case.spans, case.num_pages, sel, qn, qp, cache)
+    assert np.array_equal(out, np.broadcast_to(lat[4, :sh.kv_lora_rank].numpy(), out.shape))
+    # -1 entries in the middle are skipped
+    sel2 = np.full((3, sh.topk), -1, np.int32)
+    sel2[:, 2] = 4
+    assert np.array_equal(oracle.attend(sh, case.spans, case.num_pages, sel2, qn, qp, cache), out)
+
+
+def test_attend_uniform_logits_give_mean():
+    sh, case, lat, cache, qn, qp = _latent_case()
+    zero = torch.zeros_like(qn)
+    sel = np.full((3, sh.topk), -1, np.int32)
+    sel[:, :3] = [0, 2, 5]
+    out = oracle.attend(sh, case.spans, case.num_pages, sel, zero, torch.zeros_like(qp), cache)
+    mean = lat[[0, 2, 5], :sh.kv_lora_rank].numpy().mean(axis=0)
+    np.testing.assert_allclose(out, np.broadcast_to(mean, out.shape), rtol=0, atol=1e-15)
+
+
+def test_attend_sink_closed_forms():
+    """The sink is a logit in scaled units that joins only the denominator:
+    two keys with logit 0 and a sink 0 give (c_a + c_b) / 3; a sink at -1e30 is no sink."""
+    sh, case, lat, cache, qn, qp = _latent_case(sm_scale=3.0)
+    zero_n, zero_p = torch.zeros_like(qn), torch.zeros_like(qp)
+    sel = np.full((3, sh.topk), -1, np.int32)
+    sel[:, :2] = [1, 3]
+    sink0 = torch.zeros(sh.heads)
+    out = oracle.attend(sh, case.spans, case.num_pages, sel, zero_n, zero_p, cache, sink0)
+    expect = (lat[1, :sh.kv_lora_rank] + lat[3, :sh.kv_lora_rank]).numpy() / 3.0
+    np.testing.assert_allclose(out, np.broadcast_to(expect, out.shape), rtol=0, atol=1e-15)
+    far = torch.full((sh.heads,), -1e30)
+    a = oracle.attend(sh, case.spans, case.num_pages, sel, qn, qp, cache, far)
+    b = oracle.attend(sh, case.spans, case.num_pages, sel, qn, qp, cache, None)
+    np.testing.assert_allclose(a, b, rtol=0, atol=0)
+    # sink equal to the single key's logit: output is half the latent
+    sel1 = np.full((3, sh.topk), -1, np.int32)
+    sel1[:, 0] = 2
+    lg = (qn.double() @ lat[2, :sh.kv_lora_rank] + qp.double() @ lat[2, sh.kv_lora_rank:]) * sh.sm_scale
+    r0 = oracle.attend(sh, case.spans, case.num_pages, sel1[:1], qn[:1], qp[:1], cache, lg[0].float())
+    half = 0.5 * lat[2, :sh.kv_lora_rank].numpy()
+    np.testing.assert_allclose(r0[0], np.broadcast_to(half, r0[0].shape), rtol=1e-6, atol=1e-6)
+
+
+def test_attend_fp8_656_row_layout():
+    """A 656-byte row is [512 e4m3 | 4 fp32 scales, one per 128 | 64 bf16 rope]: with one
+    selected key the output is the dequantised c exactly."""
+    L, Rd, P = 512, 64, 2
+    sh = tiny_shape(heads=2, kv_lora_rank=L, rope_dim=Rd, page_size=P, topk=4, latent_fmt=W.LATENT_FP8_656)
+    assert sh.latent_row_bytes == 656
+    case = make_case(sh, [(1, 1)], pages=[[1]], num_pages=2)
+    rng = np.random.default_rng(2)
+    codes = rng.integers(0, 256, size=(L,), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x10   # no NaN codes
+    scales = np.array([0.5, 2.0, 3.0, 0.25], np.float32)
+    rope = bf16(rng.standard_normal(Rd)).view(torch.int16).numpy().view(np.uint8)
+    row = np.concatenate([codes, scales.view(np.uint8), rope])
+    cache = np.zeros((2, P, 656), np.uint8)
+    cache[1, 1] = row    # position 1 -> slot 1 of page 1
+    qn = bf16(rng.standard_normal((1, 2, L)))
+    qp = bf16(rng.standard_normal((1, 2, Rd)))
+    sel = np.array([[1, -1, -1, -1]], np.int32)
+    out = oracle.attend(sh, case.spans, 2, sel, qn, qp, cache)
+    deq = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy() * np.repeat(scales.astype(np.float64), 128)
+    assert np.array_equal(out[0, 0], deq) and np.array_equal(out[0, 1], deq)
+
+
+def test_attend_rejects_noncausal_selection():
+    sh, case, lat, cache, qn, qp = _latent_case()
+    sel = np.full((3, sh.topk), -1, np.int32)
+    sel[0, 0] = 7            # row 0 sits at position 6
+    with pytest.raises(oracle.OracleError):
+        oracle.attend(sh, case.spans, case.num_pages, sel, qn, qp, cache)
+
+
+def test_short_history_raises():
+    sh = tiny_shape(page_size=4)
+    case = make_case(sh, [(6, 2)], pages=[[0]], num_pages=1)     # 8 tokens need 2 pages
+    with pytest.raises(oracle.OracleError):
+        oracle.store_keys(sh, case.spans, 1, bf16(np.zeros((2, 3))), torch.zeros(1, 4, 3, dtype=torch.bfloat16))
+
+
+# ----------------------------------------------------------------------------
+# byte identities stated on the pages
+# ----------------------------------------------------------------------------
+def test_format_sizes_match_pages():
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "format_sizes.txt")
+    facts = {}
+    for line in open(path):
+        line = line.split("#")[0].strip()
+        if line:
+            k, v = line.split("=")
+            facts[k.strip()] = int(v)
+    bf = W.DSAShape(**W.DEEPSEEK)
+    f8 = W.DSAShape(**W.DEEPSEEK, latent_fmt=W.LATENT_FP8_656, index_fmt=W.INDEX_FP8_132)
+    assert bf.latent_row_bytes == facts["mla_latent_bf16"]
+    assert f8.latent_row_bytes == facts["mla_latent_fp8_packed"]
+    assert f8.index_row_bytes == facts["dsa_index_fp8"]
+    assert facts["selected_tokens"] == bf.topk
