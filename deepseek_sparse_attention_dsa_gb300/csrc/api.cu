@@ -1,0 +1,515 @@
+// api.cu -- the C ABI (include/dsa.h): contexts, plans, validation, scratch
+// management and the calls that launch the kernels.
+//
+// Planning follows mstar DSAManager.plan / DSAPlan / DSASpan
+// ("mstar.engine.resources.dsa.manager"): each span contributes q_len rows
+// starting at row q_start, the first at position ctx_start; a row's page list
+// is its span's, and its token 0 sits page_start slots into it.  The plan
+// flattens all of that into device arrays once, so no kernel of the step
+// needs the host again.
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "dsa_internal.h"
+
+using namespace dsa;
+
+namespace {
+
+bool valid_config(const dsa_config_t &c) {
+  if (c.index_heads <= 0 || c.index_dim <= 0 || c.topk <= 0 || c.heads <= 0 || c.kv_lora_rank <= 0 ||
+      c.rope_dim < 0 || c.page_size <= 0)
+    return false;
+  if (c.latent_fmt != DSA_LATENT_BF16 && c.latent_fmt != DSA_LATENT_FP8_656) return false;
+  if (c.index_fmt != DSA_INDEX_BF16 && c.index_fmt != DSA_INDEX_FP8_132) return false;
+  return true;
+}
+
+dsa_status supported_config(const dsa_config_t &c) {
+  // 16-byte vector copies of key rows and of latent rows
+  if ((c.index_dim * 2) % 16 != 0) return DSA_ERR_UNSUPPORTED;
+  if (c.index_fmt == DSA_INDEX_FP8_132 && c.index_dim != 128) return DSA_ERR_UNSUPPORTED;
+  if (c.latent_fmt == DSA_LATENT_FP8_656 && (c.kv_lora_rank % 128 != 0)) return DSA_ERR_UNSUPPORTED;
+  if (((c.kv_lora_rank + c.rope_dim) * 2) % 16 != 0) return DSA_ERR_UNSUPPORTED;
+  if (c.kv_lora_rank % 8 != 0 || c.rope_dim % 8 != 0) return DSA_ERR_UNSUPPORTED;
+  if (c.kv_lora_rank > 1024 || c.index_heads > 256 || c.heads > 1024) return DSA_ERR_UNSUPPORTED;
+  return DSA_OK;
+}
+
+template <typename T>
+size_t align_up(size_t x) {
+  return (x + alignof(T) - 1) / alignof(T) * alignof(T);
+}
+
+// Bump allocator over the staging vector: records offsets, fills pointers later.
+struct Layout {
+  size_t bytes = 0;
+  template <typename T>
+  size_t take(size_t n) {
+    bytes = (bytes + 255) / 256 * 256;
+    size_t off = bytes;
+    bytes += n * sizeof(T);
+    return off;
+  }
+};
+
+bool is_host_only(const dsa_ctx *ctx) { return ctx == nullptr || ctx->device < 0; }
+
+dsa_status ensure_scratch(dsa_ctx *ctx, size_t scores, size_t slots) {
+  if (scores > ctx->scores_cap) {
+    size_t cap = std::max(scores, ctx->scores_cap * 3 / 2);
+    if (ctx->scores) cudaFree(ctx->scores);
+    ctx->scores = nullptr;
+    ctx->scores_cap = 0;
+    if (cudaMalloc(&ctx->scores, cap * sizeof(float)) != cudaSuccess) return DSA_ERR_OOM;
+    ctx->scores_cap = cap;
+  }
+  if (slots > ctx->part_cap) {
+    size_t cap = std::max(slots, ctx->part_cap * 3 / 2);
+    if (ctx->opart) cudaFree(ctx->opart);
+    if (ctx->mlpart) cudaFree(ctx->mlpart);
+    ctx->opart = ctx->mlpart = nullptr;
+    ctx->part_cap = 0;
+    const size_t hl = static_cast<size_t>(ctx->cfg.heads) * ctx->cfg.kv_lora_rank;
+    if (cudaMalloc(&ctx->opart, cap * hl * sizeof(float)) != cudaSuccess) return DSA_ERR_OOM;
+    if (cudaMalloc(&ctx->mlpart, cap * ctx->cfg.heads * 2 * sizeof(float)) != cudaSuccess) return DSA_ERR_OOM;
+    ctx->part_cap = cap;
+  }
+  return DSA_OK;
+}
+
+}  // namespace
+
+// ----------------------------------------------------------------------------
+// tensor maps
+// ----------------------------------------------------------------------------
+namespace dsa {
+
+bool encode_tiled_2d(CUtensorMap *tm, CUtensorMapDataType dtype, void *base, uint64_t inner, uint64_t outer,
+                     uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(tm, dtype, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace dsa
+
+// ----------------------------------------------------------------------------
+// C ABI
+// ----------------------------------------------------------------------------
+extern "C" {
+
+const char *dsa_status_str(dsa_status s) {
+  switch (s) {
+    case DSA_OK: return "ok";
+    case DSA_ERR_INVALID_ARG: return "invalid argument";
+    case DSA_ERR_SHORT_HISTORY: return "span pages do not reach the positions the step needs";
+    case DSA_ERR_OOM: return "out of memory";
+    case DSA_ERR_CUDA: return "CUDA error";
+    case DSA_ERR_BOUNDS: return "device bounds check failed (selection or page id out of range)";
+    case DSA_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case DSA_ERR_UNSUPPORTED: return "unsupported shape or format";
+    default: return "unknown status";
+  }
+}
+
+dsa_status dsa_create(const dsa_config_t *cfg, int device, dsa_ctx_t **out) {
+  if (!cfg || !out) return DSA_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!valid_config(*cfg)) return DSA_ERR_INVALID_ARG;
+  dsa_status sup = supported_config(*cfg);
+  if (sup != DSA_OK) return sup;
+  dsa_ctx *ctx = new (std::nothrow) dsa_ctx();
+  if (!ctx) return DSA_ERR_OOM;
+  ctx->cfg = *cfg;
+  ctx->device = device;
+  if (device >= 0) {
+    if (cudaSetDevice(device) != cudaSuccess) { delete ctx; return DSA_ERR_CUDA; }
+    if (cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+      delete ctx;
+      return DSA_ERR_CUDA;
+    }
+    if (cudaMalloc(&ctx->err, sizeof(int)) != cudaSuccess) { delete ctx; return DSA_ERR_OOM; }
+    if (cudaMemset(ctx->err, 0, sizeof(int)) != cudaSuccess) { cudaFree(ctx->err); delete ctx; return DSA_ERR_CUDA; }
+  } else {
+    ctx->num_sms = 152;
+  }
+  *out = ctx;
+  return DSA_OK;
+}
+
+void dsa_destroy(dsa_ctx_t *ctx) {
+  if (!ctx) return;
+  if (ctx->device >= 0) {
+    cudaSetDevice(ctx->device);
+    cudaFree(ctx->err);
+    cudaFree(ctx->scores);
+    cudaFree(ctx->opart);
+    cudaFree(ctx->mlpart);
+  }
+  delete ctx;
+}
+
+dsa_status dsa_plan(dsa_ctx_t *ctx, const dsa_span_t *spans, int32_t num_spans, int32_t cache_pages,
+                    dsa_stream_t stream, dsa_plan_t **out) {
+  if (!ctx || !out || num_spans < 0 || (num_spans > 0 && !spans) || cache_pages < 0) return DSA_ERR_INVALID_ARG;
+  *out = nullptr;
+  const dsa_config_t &c = ctx->cfg;
+  const int64_t P = c.page_size;
+
+  // ---- validate spans (they must tile rows [0, T) in order)
+  int64_t T = 0, total_pages = 0, num_scores = 0;
+  int32_t max_pos = 0;
+  for (int32_t i = 0; i < num_spans; ++i) {
+    const dsa_span_t &s = spans[i];
+    if (s.q_start != T || s.q_len <= 0 || s.ctx_start < 0 || s.page_start < 0 || s.num_pages < 0)
+      return DSA_ERR_INVALID_ARG;
+    if (s.num_pages > 0 && !s.pages) return DSA_ERR_INVALID_ARG;
+    const int64_t end = static_cast<int64_t>(s.ctx_start) + s.q_len;     // tokens 0 .. end-1
+    if (end > INT32_MAX) return DSA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(s.num_pages) * P < s.page_start + end) return DSA_ERR_SHORT_HISTORY;
+    for (int32_t k = 0; k < s.num_pages; ++k)
+      if (s.pages[k] < 0 || s.pages[k] >= cache_pages) return DSA_ERR_INVALID_ARG;
+    T += s.q_len;
+    total_pages += s.num_pages;
+    // rows at positions ctx_start .. end-1 each score pos+1 keys
+    num_scores += (static_cast<int64_t>(s.ctx_start) + 1 + end) * s.q_len / 2;
+    max_pos = std::max<int32_t>(max_pos, static_cast<int32_t>(end - 1));
+    if (T > INT32_MAX / 2 || total_pages > INT32_MAX / 2) return DSA_ERR_INVALID_ARG;
+  }
+
+  dsa_plan_t *plan = new (std::nothrow) dsa_plan_t();
+  if (!plan) return DSA_ERR_OOM;
+  plan->ctx = ctx;
+  plan->stream = reinterpret_cast<cudaStream_t>(stream);
+  plan->T = static_cast<int32_t>(T);
+  plan->n_spans = num_spans;
+  plan->cache_pages = cache_pages;
+  plan->num_scores = num_scores;
+  plan->max_pos = max_pos;
+  {
+    // largest power of two <= 128 dividing the page size and every page_start,
+    // so a key box of that many rows never crosses a page boundary
+    int64_t g = P;
+    for (int32_t i = 0; i < num_spans; ++i) {
+      int64_t a = g, b = spans[i].page_start;
+      while (b) { int64_t t = a % b; a = b; b = t; }
+      g = a;
+    }
+    int bh = 1;
+    while (bh < 128 && g % (bh * 2) == 0) bh *= 2;
+    plan->box_rows = bh;
+  }
+
+  // ---- indexer groups: single rows (decode spans) and runs of G rows (chunks)
+  const int Gm = indexer_group_rows(c);
+  std::vector<IdxGroup> groups[2];
+  int32_t page_off = 0;
+  for (int32_t i = 0; i < num_spans; ++i) {
+    const dsa_span_t &s = spans[i];
+    const int set = (s.q_len > 1 && Gm > 1) ? 1 : 0;
+    const int G = set ? Gm : 1;
+    for (int32_t r = 0; r < s.q_len; r += G) {
+      IdxGroup g{};
+      g.row0 = s.q_start + r;
+      g.nrows = std::min<int32_t>(G, s.q_len - r);
+      g.pos0 = s.ctx_start + r;
+      g.page_off = page_off;
+      g.npages = s.num_pages;
+      g.page_start = s.page_start;
+      g.ntiles = (g.pos0 + g.nrows + kIndexTile - 1) / kIndexTile;
+      groups[set].push_back(g);
+    }
+    page_off += s.num_pages;
+  }
+  std::vector<IdxItem> items[2];
+  std::vector<int32_t> cta_begin[2];
+  int64_t n_index_items = 0;
+  for (int set = 0; set < 2; ++set) {
+    int64_t tiles = 0;
+    for (auto &g : groups[set]) tiles += g.ntiles;
+    if (tiles == 0) continue;
+    const int G = set ? Gm : 1;
+    const int cap = std::max(1, ctx->num_sms * indexer_ctas_per_sm(c, G));
+    // items of at most `tpi` tiles; CTAs take contiguous, tile-balanced item ranges
+    const int64_t tpi = std::max<int64_t>(2, std::min<int64_t>(32, tiles / (int64_t(cap) * 8)));
+    std::vector<int64_t> prefix{0};
+    for (int32_t gi = 0; gi < static_cast<int32_t>(groups[set].size()); ++gi) {
+      const IdxGroup &g = groups[set][gi];
+      for (int32_t t = 0; t < g.ntiles; t += static_cast<int32_t>(tpi)) {
+        IdxItem it{gi, t, std::min<int32_t>(g.ntiles, t + static_cast<int32_t>(tpi)), 0};
+        items[set].push_back(it);
+        prefix.push_back(prefix.back() + (it.tile1 - it.tile0));
+      }
+    }
+    const int n_items = static_cast<int>(items[set].size());
+    const int n_ctas = std::min(n_items, cap);
+    cta_begin[set].resize(n_ctas + 1);
+    size_t k = 0;
+    for (int b = 0; b <= n_ctas; ++b) {
+      const int64_t target = tiles * b / n_ctas;
+      while (k < prefix.size() - 1 && prefix[k] < target) ++k;
+      cta_begin[set][b] = static_cast<int32_t>(k);
+    }
+    cta_begin[set][n_ctas] = n_items;
+    plan->idx[set].G = G;
+    plan->idx[set].n_groups = static_cast<int>(groups[set].size());
+    plan->idx[set].n_items = n_items;
+    plan->idx[set].n_ctas = n_ctas;
+    n_index_items += n_items;
+  }
+  plan->n_index_items = static_cast<int32_t>(n_index_items);
+
+  // ---- attention units: rows split over key ranges when there are few rows
+  std::vector<AttUnit> units;
+  std::vector<AttCombine> combines;
+  {
+    const int64_t K = c.topk;
+    const int pairs = std::max(1, ctx->num_sms / 2);
+    int splits = 1;
+    if (T > 0 && T < 2 * pairs) splits = static_cast<int>(std::min<int64_t>(16, (2 * pairs + T - 1) / T));
+    int32_t slot = 0;
+    int32_t row = 0;
+    for (int32_t i = 0; i < num_spans; ++i) {
+      const dsa_span_t &s = spans[i];
+      for (int32_t r = 0; r < s.q_len; ++r, ++row) {
+        const int64_t pos = s.ctx_start + r;
+        const int64_t nsel = std::min<int64_t>(K, pos + 1);
+        const int64_t tiles = (nsel + kAttTile - 1) / kAttTile;
+        const int64_t sp = std::max<int64_t>(1, std::min<int64_t>(splits, tiles / 2));
+        if (sp == 1) {
+          units.push_back(AttUnit{row, 0, static_cast<int32_t>(nsel), -1});
+        } else {
+          combines.push_back(AttCombine{row, slot, static_cast<int32_t>(sp), 0});
+          for (int64_t k = 0; k < sp; ++k) {
+            const int64_t t0 = tiles * k / sp, t1 = tiles * (k + 1) / sp;
+            units.push_back(AttUnit{row, static_cast<int32_t>(t0 * kAttTile),
+                                    static_cast<int32_t>(std::min<int64_t>(nsel, t1 * kAttTile)), slot++});
+          }
+          plan->splits_max = std::max<int32_t>(plan->splits_max, static_cast<int32_t>(sp));
+        }
+      }
+    }
+    plan->n_units = static_cast<int32_t>(units.size());
+    plan->n_combine = static_cast<int32_t>(combines.size());
+    plan->n_slots = slot;
+  }
+
+  // needs_selection: some row sees more than topk keys (mstar DSAPlan)
+  plan->needs_selection = (max_pos + 1 > c.topk) ? 1 : 0;
+
+  // ---- device metadata in one buffer
+  Layout lay;
+  const size_t o_pos = lay.take<int32_t>(T), o_poff = lay.take<int32_t>(T), o_np = lay.take<int32_t>(T),
+               o_ps = lay.take<int32_t>(T), o_soff = lay.take<int64_t>(T), o_pages = lay.take<int32_t>(total_pages);
+  size_t o_g[2], o_i[2], o_c[2];
+  for (int set = 0; set < 2; ++set) {
+    o_g[set] = lay.take<IdxGroup>(groups[set].size());
+    o_i[set] = lay.take<IdxItem>(items[set].size());
+    o_c[set] = lay.take<int32_t>(cta_begin[set].size());
+  }
+  const size_t o_u = lay.take<AttUnit>(units.size()), o_cb = lay.take<AttCombine>(combines.size());
+  const size_t bytes = std::max<size_t>(lay.bytes, 256);
+  try {
+    plan->host.assign(bytes, 0);
+  } catch (...) {
+    delete plan;
+    return DSA_ERR_OOM;
+  }
+  char *h = plan->host.data();
+  {
+    auto *pos = reinterpret_cast<int32_t *>(h + o_pos);
+    auto *poff = reinterpret_cast<int32_t *>(h + o_poff);
+    auto *np = reinterpret_cast<int32_t *>(h + o_np);
+    auto *ps = reinterpret_cast<int32_t *>(h + o_ps);
+    auto *soff = reinterpret_cast<int64_t *>(h + o_soff);
+    auto *pg = reinterpret_cast<int32_t *>(h + o_pages);
+    int32_t row = 0, poff_acc = 0;
+    int64_t sacc = 0;
+    for (int32_t i = 0; i < num_spans; ++i) {
+      const dsa_span_t &s = spans[i];
+      if (s.num_pages) std::memcpy(pg + poff_acc, s.pages, sizeof(int32_t) * s.num_pages);
+      for (int32_t r = 0; r < s.q_len; ++r, ++row) {
+        pos[row] = s.ctx_start + r;
+        poff[row] = poff_acc;
+        np[row] = s.num_pages;
+        ps[row] = s.page_start;
+        soff[row] = sacc;
+        sacc += static_cast<int64_t>(pos[row]) + 1;
+      }
+      poff_acc += s.num_pages;
+    }
+    for (int set = 0; set < 2; ++set) {
+      if (!groups[set].empty()) std::memcpy(h + o_g[set], groups[set].data(), groups[set].size() * sizeof(IdxGroup));
+      if (!items[set].empty()) std::memcpy(h + o_i[set], items[set].data(), items[set].size() * sizeof(IdxItem));
+      if (!cta_begin[set].empty())
+        std::memcpy(h + o_c[set], cta_begin[set].data(), cta_begin[set].size() * sizeof(int32_t));
+    }
+    if (!units.empty()) std::memcpy(h + o_u, units.data(), units.size() * sizeof(AttUnit));
+    if (!combines.empty()) std::memcpy(h + o_cb, combines.data(), combines.size() * sizeof(AttCombine));
+  }
+
+  if (is_host_only(ctx)) {
+    *out = plan;
+    return DSA_OK;
+  }
+  if (cudaSetDevice(ctx->device) != cudaSuccess) { delete plan; return DSA_ERR_CUDA; }
+  dsa_status st = ensure_scratch(ctx, static_cast<size_t>(num_scores), static_cast<size_t>(plan->n_slots));
+  if (st != DSA_OK) { delete plan; return st; }
+  if (cudaMallocAsync(reinterpret_cast<void **>(&plan->dev), bytes, plan->stream) != cudaSuccess) {
+    delete plan;
+    return DSA_ERR_OOM;
+  }
+  if (cudaMemcpyAsync(plan->dev, h, bytes, cudaMemcpyHostToDevice, plan->stream) != cudaSuccess) {
+    cudaFreeAsync(plan->dev, plan->stream);
+    delete plan;
+    return DSA_ERR_CUDA;
+  }
+  char *d = plan->dev;
+  plan->row_pos = reinterpret_cast<int32_t *>(d + o_pos);
+  plan->row_page_off = reinterpret_cast<int32_t *>(d + o_poff);
+  plan->row_npages = reinterpret_cast<int32_t *>(d + o_np);
+  plan->row_page_start = reinterpret_cast<int32_t *>(d + o_ps);
+  plan->row_score_off = reinterpret_cast<int64_t *>(d + o_soff);
+  plan->pages = reinterpret_cast<int32_t *>(d + o_pages);
+  for (int set = 0; set < 2; ++set) {
+    plan->idx[set].groups = reinterpret_cast<IdxGroup *>(d + o_g[set]);
+    plan->idx[set].items = reinterpret_cast<IdxItem *>(d + o_i[set]);
+    plan->idx[set].cta_begin = reinterpret_cast<int32_t *>(d + o_c[set]);
+  }
+  plan->units = reinterpret_cast<AttUnit *>(d + o_u);
+  plan->combine = reinterpret_cast<AttCombine *>(d + o_cb);
+  *out = plan;
+  return DSA_OK;
+}
+
+void dsa_plan_destroy(dsa_plan_t *plan) {
+  if (!plan) return;
+  if (plan->dev && !is_host_only(plan->ctx)) {
+    cudaSetDevice(plan->ctx->device);
+    cudaFreeAsync(plan->dev, plan->stream);
+  }
+  delete plan;
+}
+
+dsa_status dsa_plan_get_info(const dsa_plan_t *plan, dsa_plan_info_t *info) {
+  if (!plan || !info) return DSA_ERR_INVALID_ARG;
+  info->num_rows = plan->T;
+  info->num_spans = plan->n_spans;
+  info->needs_selection = plan->needs_selection;
+  info->index_items = plan->n_index_items;
+  info->num_scores = plan->num_scores;
+  info->attend_units = plan->n_units;
+  info->attend_splits_max = plan->splits_max;
+  return DSA_OK;
+}
+
+static dsa_status check_call(dsa_ctx_t *ctx, const dsa_plan_t *plan) {
+  if (!ctx || !plan || plan->ctx != ctx || is_host_only(ctx)) return DSA_ERR_INVALID_ARG;
+  if (cudaSetDevice(ctx->device) != cudaSuccess) return DSA_ERR_CUDA;
+  return DSA_OK;
+}
+
+dsa_status dsa_store_keys(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *keys, void *index_cache,
+                          dsa_stream_t stream) {
+  dsa_status st = check_call(ctx, plan);
+  if (st != DSA_OK) return st;
+  ctx->last_launches = 0;
+  if (plan->T == 0) return DSA_OK;
+  if (!keys || !index_cache) return DSA_ERR_INVALID_ARG;
+  cudaError_t e = launch_store_keys(ctx, plan, keys, index_cache, reinterpret_cast<cudaStream_t>(stream),
+                                    &ctx->last_launches);
+  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+dsa_status dsa_index_scores(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *q, const float *w,
+                            const void *index_cache, float *scores, dsa_stream_t stream) {
+  dsa_status st = check_call(ctx, plan);
+  if (st != DSA_OK) return st;
+  ctx->last_launches = 0;
+  if (plan->T == 0) return DSA_OK;
+  if (!q || !w || !index_cache || !scores) return DSA_ERR_INVALID_ARG;
+  cudaError_t e = launch_index_scores(ctx, plan, q, w, index_cache, scores, reinterpret_cast<cudaStream_t>(stream),
+                                      &ctx->last_launches);
+  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+dsa_status dsa_topk_from_scores(dsa_ctx_t *ctx, const dsa_plan_t *plan, const float *scores, int32_t *selection,
+                                dsa_stream_t stream) {
+  dsa_status st = check_call(ctx, plan);
+  if (st != DSA_OK) return st;
+  ctx->last_launches = 0;
+  if (plan->T == 0) return DSA_OK;
+  if (!scores || !selection) return DSA_ERR_INVALID_ARG;
+  cudaError_t e = launch_topk(ctx, plan, scores, selection, reinterpret_cast<cudaStream_t>(stream),
+                              &ctx->last_launches);
+  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+dsa_status dsa_index_topk(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *q, const float *w,
+                          const void *index_cache, int32_t *selection, dsa_stream_t stream) {
+  dsa_status st = check_call(ctx, plan);
+  if (st != DSA_OK) return st;
+  ctx->last_launches = 0;
+  if (plan->T == 0) return DSA_OK;
+  if (!q || !w || !index_cache || !selection) return DSA_ERR_INVALID_ARG;
+  if (static_cast<size_t>(plan->num_scores) > ctx->scores_cap) return DSA_ERR_INVALID_ARG;  // plan of another size
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t n = 0;
+  cudaError_t e = launch_index_scores(ctx, plan, q, w, index_cache, ctx->scores, s, &n);
+  if (e == cudaSuccess) e = launch_topk(ctx, plan, ctx->scores, selection, s, &n);
+  ctx->last_launches = n;
+  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+dsa_status dsa_attend(dsa_ctx_t *ctx, const dsa_plan_t *plan, const int32_t *selection, const void *q_nope,
+                      const void *q_pe, const void *latent_cache, const float *sink, float sm_scale, void *out,
+                      dsa_stream_t stream) {
+  dsa_status st = check_call(ctx, plan);
+  if (st != DSA_OK) return st;
+  ctx->last_launches = 0;
+  if (plan->T == 0) return DSA_OK;
+  if (!selection || !q_nope || !latent_cache || !out || (!q_pe && ctx->cfg.rope_dim > 0)) return DSA_ERR_INVALID_ARG;
+  if (static_cast<size_t>(plan->n_slots) > ctx->part_cap) return DSA_ERR_INVALID_ARG;
+  cudaError_t e = launch_attend(ctx, plan, selection, q_nope, q_pe, latent_cache, sink, sm_scale, out,
+                                reinterpret_cast<cudaStream_t>(stream), &ctx->last_launches);
+  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+dsa_status dsa_get_error(dsa_ctx_t *ctx, dsa_stream_t stream) {
+  if (!ctx || is_host_only(ctx)) return DSA_ERR_INVALID_ARG;
+  if (cudaSetDevice(ctx->device) != cudaSuccess) return DSA_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DSA_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, ctx->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return DSA_ERR_CUDA;
+  if (word && cudaMemset(ctx->err, 0, sizeof(int)) != cudaSuccess) return DSA_ERR_CUDA;
+  if (word & kErrTimeout) return DSA_ERR_TIMEOUT;
+  if (word & kErrBounds) return DSA_ERR_BOUNDS;
+  return DSA_OK;
+}
+
+int32_t dsa_last_launch_count(const dsa_ctx_t *ctx) { return ctx ? ctx->last_launches : 0; }
+
+}  // extern "C"

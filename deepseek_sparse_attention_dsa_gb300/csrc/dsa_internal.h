@@ -1,0 +1,127 @@
+// dsa_internal.h -- host/device structures shared by the C-ABI layer and the
+// kernel launchers.  Not part of the public interface.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "dsa.h"
+#include "errors.h"
+
+namespace dsa {
+
+// A group of consecutive rows of one span that the indexer scores together
+// (1 row for decode rows, up to 4 for prefill chunks).
+struct IdxGroup {
+  int32_t row0;        // first row
+  int32_t nrows;       // rows in the group (positions pos0 .. pos0+nrows-1)
+  int32_t pos0;        // position of the first row
+  int32_t page_off;    // offset of the span's page list in the plan's pages[]
+  int32_t npages;      // length of that list
+  int32_t page_start;  // slot of token 0
+  int32_t ntiles;      // key tiles of 128 covering positions 0 .. pos0+nrows-1
+  int32_t pad;
+};
+
+// A contiguous run of key tiles of one group.
+struct IdxItem {
+  int32_t group;
+  int32_t tile0;
+  int32_t tile1;
+  int32_t pad;
+};
+
+// An attention work unit: selection entries [k0, k1) of one row; `slot` >= 0
+// when the row is split and the unit writes a partial result.
+struct AttUnit {
+  int32_t row;
+  int32_t k0;
+  int32_t k1;
+  int32_t slot;
+};
+
+// A row whose attention was split over `nsplit` units with partial slots
+// first_slot .. first_slot + nsplit - 1.
+struct AttCombine {
+  int32_t row;
+  int32_t first_slot;
+  int32_t nsplit;
+  int32_t pad;
+};
+
+constexpr int kIndexTile = 128;   // keys per indexer tile (UMMA M)
+constexpr int kAttTile = 64;      // keys per attention tile (UMMA N of QK)
+
+// Indexer launch set: groups with the same row-group size.
+struct IdxSet {
+  int G = 1;                      // rows per group
+  int n_groups = 0;
+  int n_items = 0;
+  int n_ctas = 0;                 // persistent grid
+  IdxGroup *groups = nullptr;     // device
+  IdxItem *items = nullptr;       // device
+  int32_t *cta_begin = nullptr;   // device [n_ctas + 1]: item range of each CTA
+};
+
+}  // namespace dsa
+
+struct dsa_ctx {
+  dsa_config_t cfg;
+  int device = -1;
+  int num_sms = 0;
+  int *err = nullptr;             // device error word
+  float *scores = nullptr;        // score scratch
+  size_t scores_cap = 0;          // floats
+  float *opart = nullptr;         // attention partial outputs [slots][H][L]
+  float *mlpart = nullptr;        // attention partial (m, l) [slots][H][2]
+  size_t part_cap = 0;            // slots
+  int32_t last_launches = 0;
+};
+
+struct dsa_plan {
+  dsa_ctx *ctx = nullptr;
+  cudaStream_t stream = nullptr;
+  int32_t T = 0, n_spans = 0, needs_selection = 0, cache_pages = 0, max_pos = 0;
+  int32_t box_rows = 1;           // TMA box height for key tiles: a power of two dividing page_size and every page_start
+  int64_t num_scores = 0;
+  std::vector<char> host;         // staging copy of the device metadata
+  char *dev = nullptr;
+  // device views
+  int32_t *row_pos = nullptr, *row_page_off = nullptr, *row_npages = nullptr, *row_page_start = nullptr;
+  int64_t *row_score_off = nullptr;
+  int32_t *pages = nullptr;
+  dsa::IdxSet idx[2];             // [0]: single-row groups, [1]: multi-row groups
+  dsa::AttUnit *units = nullptr;
+  int32_t n_units = 0, splits_max = 1;
+  dsa::AttCombine *combine = nullptr;
+  int32_t n_combine = 0, n_slots = 0;
+  int32_t n_index_items = 0;
+};
+
+namespace dsa {
+
+// Launchers (each returns cudaGetLastError() after its launches and adds the
+// number of kernels it launched to *launches).
+cudaError_t launch_store_keys(const dsa_ctx *ctx, const dsa_plan_t *plan, const void *keys, void *cache,
+                              cudaStream_t s, int32_t *launches);
+cudaError_t launch_index_scores(const dsa_ctx *ctx, const dsa_plan_t *plan, const void *q, const float *w,
+                                const void *cache, float *scores, cudaStream_t s, int32_t *launches);
+cudaError_t launch_topk(const dsa_ctx *ctx, const dsa_plan_t *plan, const float *scores, int32_t *sel,
+                        cudaStream_t s, int32_t *launches);
+cudaError_t launch_attend(const dsa_ctx *ctx, const dsa_plan_t *plan, const int32_t *sel, const void *q_nope,
+                          const void *q_pe, const void *latent, const float *sink, float sm_scale, void *out,
+                          cudaStream_t s, int32_t *launches);
+
+// Shapes the tensor-core kernels implement (others run the simple kernels).
+bool indexer_tc_supported(const dsa_config_t &c, int G);
+bool attend_tc_supported(const dsa_config_t &c);
+int indexer_group_rows(const dsa_config_t &c);   // rows per multi-row group (4 or 1)
+int indexer_ctas_per_sm(const dsa_config_t &c, int G);
+
+// Tensor-map encoding through the driver entry point (no libcuda link).
+bool encode_tiled_2d(CUtensorMap *tm, CUtensorMapDataType dtype, void *base, uint64_t inner, uint64_t outer,
+                     uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz);
+
+}  // namespace dsa

@@ -1,0 +1,6 @@
+// errors.h -- bits of the device error word (read back by dsa_get_error).
+#pragma once
+namespace dsa {
+constexpr int kErrBounds = 1;   // a selected position or page id out of range; access skipped
+constexpr int kErrTimeout = 2;  // a pipeline wait gave up after its time limit
+}  // namespace dsa

@@ -1,0 +1,453 @@
+// indexer.cu -- DSA indexer score on sm_103a tensor cores.
+//
+//   s[r, j] = sum_h w[r,h] * relu(q[r,h] . k[j])      (fp32; j = 0 .. pos(r))
+//
+// (mstar "mstar.engine.resources.dsa.manager", module summary and index_topk.)
+//
+// The head dots of a tile of 128 keys are one UMMA (tcgen05.mma, kind::f16,
+// bf16 inputs, fp32 accumulation in TMEM):
+//     D[key, n] = sum_d K[key, d] * Q[n, d],   M = 128 keys, N = G rows x Hi heads, K = Di
+// Keys come from the page-resident index cache through TMA (one box per
+// page-contiguous run, 128-byte swizzle); the query block of a group of G rows
+// of one request is the B operand and stays in shared memory while the group's
+// key tiles stream through a ring of stages.  Four epilogue warps read the
+// accumulator back (thread = key = TMEM lane) and reduce over the heads with
+// the relu and the head weights in registers, so the reduction needs no
+// cross-lane traffic.  The accumulator is double-buffered in TMEM so the
+// epilogue of tile t overlaps the MMAs of tile t+1.
+//
+// Warp roles (192 threads): warp 0 TMA producer, warp 1 MMA issuer (one
+// thread) and TMEM owner, warps 2-5 epilogue.  The grid is persistent: each
+// CTA walks a tile-balanced contiguous range of the plan's work items.
+//
+// Shapes outside the tensor-core instances (and the fp8 index format) run
+// index_simt_kernel, one CUDA-core thread per key.
+#include <cuda_runtime.h>
+
+#include <cuda_fp8.h>
+
+#include "dsa_internal.h"
+#include "ptx.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kEpiWarps = 4;
+constexpr int kIdxThreads = 64 + 32 * kEpiWarps;
+
+template <int HI, int DI, int G>
+struct IdxTraits {
+  static constexpr int CH = DI >= 64 ? 64 : DI;     // bf16 elements per swizzled row
+  static constexpr int NCH = DI / CH;               // chunks along the contraction
+  static constexpr int ROWB = CH * 2;               // bytes per swizzled row: 128 or 64
+  static constexpr uint32_t SWZ = ROWB == 128 ? kSwizzle128 : kSwizzle64;
+  static constexpr uint32_t SBO = 8 * ROWB;         // 8-row swizzle atom
+  static constexpr int N = ((G * HI + 15) / 16) * 16;
+  static constexpr int KSTEPS = CH / 16;            // UMMA K = 16 for bf16
+  static constexpr int KT_BYTES = 128 * DI * 2;
+  static constexpr int Q_BYTES = N * DI * 2;
+  static constexpr int QBUF = (G == 1) ? 2 : 1;
+  static constexpr int STAGES_MAX = (G == 1) ? 6 : 4;
+  static constexpr int STAGES = (STAGES_MAX * KT_BYTES + QBUF * Q_BYTES <= 200 * 1024) ? STAGES_MAX : 3;
+  static constexpr int TMEM_COLS = (2 * N <= 32) ? 32 : (2 * N <= 64) ? 64 : (2 * N <= 128) ? 128 : (2 * N <= 256) ? 256 : 512;
+  static constexpr uint32_t IDESC = mma_idesc(128, N, 1u, false, false);
+  // shared memory layout (bytes from a 1024-aligned base)
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_Q = OFF_K + STAGES * KT_BYTES;
+  static constexpr int OFF_W = OFF_Q + QBUF * Q_BYTES;
+  static constexpr int OFF_BAR = OFF_W + ((G * HI * 4 + 15) / 16) * 16;
+  static constexpr int NBAR = 2 * STAGES + 2 * QBUF + 4;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_MISC + 16 + 1024;  // + alignment slack
+  static_assert(N <= 256 && N >= 16, "UMMA N");
+  static_assert(DI % CH == 0 && CH % 16 == 0, "index dim");
+  static_assert(HI % 4 == 0, "heads");
+};
+
+struct IdxParams {
+  CUtensorMap tm_keys;      // index cache as [pages*P, Di] bf16, box {CH, BH}
+  CUtensorMap tm_q;         // q as [T*Hi, Di] bf16, box {CH, N}
+  const float *w;           // [T, Hi]
+  const IdxGroup *groups;
+  const IdxItem *items;
+  const int32_t *cta_begin;
+  const int32_t *pages;
+  const int64_t *row_score_off;
+  float *scores;
+  int *err;
+  int P, BH, num_pages;
+};
+
+template <int HI, int DI, int G>
+__global__ void __launch_bounds__(kIdxThreads, 1) index_tc_kernel(const __grid_constant__ IdxParams p) {
+  using C = IdxTraits<HI, DI, G>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  auto kfull = [&](int s) { return bar0 + 8u * s; };
+  auto kempty = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+  auto qfull = [&](int b) { return bar0 + 8u * (2 * C::STAGES + b); };
+  auto qempty = [&](int b) { return bar0 + 8u * (2 * C::STAGES + C::QBUF + b); };
+  auto afull = [&](int b) { return bar0 + 8u * (2 * C::STAGES + 2 * C::QBUF + b); };
+  auto aempty = [&](int b) { return bar0 + 8u * (2 * C::STAGES + 2 * C::QBUF + 2 + b); };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+  float *wsm = reinterpret_cast<float *>(smem + C::OFF_W);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = lane_id();
+  const int it0 = p.cta_begin[blockIdx.x], it1 = p.cta_begin[blockIdx.x + 1];
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(kfull(s), 1);
+      mbar_init(kempty(s), 1);
+    }
+    for (int b = 0; b < C::QBUF; ++b) {
+      mbar_init(qfull(b), 1);
+      mbar_init(qempty(b), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(afull(b), 1);
+      mbar_init(aempty(b), 32 * kEpiWarps);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&p.tm_keys);
+    tma_prefetch_desc(&p.tm_q);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    int stage = 0;
+    uint32_t kphase = 0;
+    int qb = -1, qcount = 0, cur_group = -1;
+    for (int it = it0; it < it1 && !*abort_flag; ++it) {
+      const IdxItem item = p.items[it];
+      const IdxGroup g = p.groups[item.group];
+      if (item.group != cur_group) {
+        cur_group = item.group;
+        qb = qcount % C::QBUF;
+        const uint32_t use = qcount / C::QBUF;
+        ++qcount;
+        bool qok = true;
+        if (lane == 0) {
+          qok = mbar_wait(qempty(qb), (use & 1) ^ 1, abort_flag, p.err);
+          if (qok) {
+            mbar_arrive_expect_tx(qfull(qb), C::Q_BYTES);
+            for (int c = 0; c < C::NCH; ++c)
+              tma_load_2d(sbase + C::OFF_Q + qb * C::Q_BYTES + c * C::N * C::ROWB, &p.tm_q, c * C::CH,
+                          g.row0 * HI, qfull(qb));
+          }
+        }
+        if (__shfl_sync(0xffffffffu, qok ? 1 : 0, 0) == 0) break;
+      }
+      const int nkeys_total = g.pos0 + g.nrows;  // keys 0 .. pos0+nrows-1
+      for (int t = item.tile0; t < item.tile1; ++t) {
+        const int nkeys = min(128, nkeys_total - t * 128);
+        const int nbox = (nkeys + p.BH - 1) / p.BH;
+        int myrow = -1;
+        if (lane < nbox) {
+          const int64_t slot = static_cast<int64_t>(g.page_start) + t * 128 + lane * p.BH;
+          const int64_t pi = slot / p.P;
+          if (pi < g.npages) {
+            const int page = p.pages[g.page_off + pi];
+            if (page >= 0 && page < p.num_pages) myrow = page * p.P + static_cast<int>(slot % p.P);
+          }
+          if (myrow < 0) atomicOr(p.err, kErrBounds);
+        }
+        const uint32_t valid = __ballot_sync(0xffffffffu, myrow >= 0);
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(kempty(stage), kphase ^ 1, abort_flag, p.err);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        const uint32_t bytes = __popc(valid) * p.BH * C::ROWB * C::NCH;
+        if (lane == 0) {
+          if (bytes) mbar_arrive_expect_tx(kfull(stage), bytes);
+          else mbar_arrive(kfull(stage));
+        }
+        for (int b = 0; b < nbox; ++b) {
+          const int row = __shfl_sync(0xffffffffu, myrow, b);
+          if (lane == 0 && row >= 0) {
+            for (int c = 0; c < C::NCH; ++c)
+              tma_load_2d(sbase + C::OFF_K + stage * C::KT_BYTES + c * 128 * C::ROWB + b * p.BH * C::ROWB,
+                          &p.tm_keys, c * C::CH, row, kfull(stage));
+          }
+        }
+        if (++stage == C::STAGES) {
+          stage = 0;
+          kphase ^= 1;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t kphase = 0;
+      int acc = 0;
+      uint32_t aphase = 0;
+      int qb = -1, qcount = 0, cur_group = -1;
+      bool ok = true;
+      for (int it = it0; it < it1 && ok; ++it) {
+        const IdxItem item = p.items[it];
+        if (item.group != cur_group) {
+          cur_group = item.group;
+          qb = qcount % C::QBUF;
+          const uint32_t use = qcount / C::QBUF;
+          ++qcount;
+          if (!mbar_wait(qfull(qb), use & 1, abort_flag, p.err)) break;
+        }
+        const uint32_t qaddr = sbase + C::OFF_Q + qb * C::Q_BYTES;
+        for (int t = item.tile0; t < item.tile1; ++t) {
+          if (!mbar_wait(kfull(stage), kphase, abort_flag, p.err)) { ok = false; break; }
+          if (!mbar_wait(aempty(acc), aphase ^ 1, abort_flag, p.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t kaddr = sbase + C::OFF_K + stage * C::KT_BYTES;
+          const uint32_t d = tmem_base + acc * C::N;
+#pragma unroll
+          for (int c = 0; c < C::NCH; ++c) {
+#pragma unroll
+            for (int k = 0; k < C::KSTEPS; ++k) {
+              const uint64_t ad = smem_desc(kaddr + c * 128 * C::ROWB + k * 32, 16, C::SBO, C::SWZ);
+              const uint64_t bd = smem_desc(qaddr + c * C::N * C::ROWB + k * 32, 16, C::SBO, C::SWZ);
+              mma_f16_ss(d, ad, bd, C::IDESC, (c | k) != 0 ? 1u : 0u);
+            }
+          }
+          mma_commit(kempty(stage));
+          mma_commit(afull(acc));
+          if (++stage == C::STAGES) {
+            stage = 0;
+            kphase ^= 1;
+          }
+          acc ^= 1;
+          if (acc == 0) aphase ^= 1;
+        }
+        // the query block is free once the group's last MMA completes
+        const bool last_of_group = (it + 1 >= it1) || (p.items[it + 1].group != cur_group);
+        if (last_of_group) mma_commit(qempty(qb));
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int et = threadIdx.x - 64;              // 0..127
+    const int quad = warp & 3;                    // TMEM lane quadrant of this warp
+    const int m = quad * 32 + lane;               // key within the tile
+    int acc = 0;
+    uint32_t aphase = 0;
+    int cur_group = -1;
+    int64_t soff[G];
+    int nrows = 0, pos0 = 0;
+    for (int it = it0; it < it1 && !*abort_flag; ++it) {
+      const IdxItem item = p.items[it];
+      if (item.group != cur_group) {
+        cur_group = item.group;
+        const IdxGroup g = p.groups[item.group];
+        nrows = g.nrows;
+        pos0 = g.pos0;
+        named_bar_sync(1, 32 * kEpiWarps);
+        for (int i = et; i < G * HI; i += 32 * kEpiWarps)
+          wsm[i] = (i < nrows * HI) ? p.w[static_cast<int64_t>(g.row0) * HI + i] : 0.f;
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) soff[gg] = gg < nrows ? p.row_score_off[g.row0 + gg] : 0;
+        named_bar_sync(1, 32 * kEpiWarps);
+      }
+      bool ok = true;
+      for (int t = item.tile0; t < item.tile1; ++t) {
+        if (!mbar_wait(afull(acc), aphase, abort_flag, p.err)) { ok = false; break; }
+        tc_fence_after();
+        const int key = t * 128 + m;
+        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * C::N;
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) {
+          if (gg < nrows) {
+            float s = 0.f;
+            if constexpr (HI >= 16) {
+              float v[HI];
+#pragma unroll
+              for (int h0 = 0; h0 < HI; h0 += 16) tmem_ld16(tbase + gg * HI + h0, *reinterpret_cast<float(*)[16]>(v + h0));
+              tmem_ld_wait();
+#pragma unroll
+              for (int h = 0; h < HI; ++h) s = fmaf(wsm[gg * HI + h], fmaxf(v[h], 0.f), s);
+            } else {
+              float v[4];
+#pragma unroll
+              for (int h0 = 0; h0 < HI; h0 += 4) {
+                tmem_ld4(tbase + gg * HI + h0, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int h = 0; h < 4; ++h) s = fmaf(wsm[gg * HI + h0 + h], fmaxf(v[h], 0.f), s);
+              }
+            }
+            if (key <= pos0 + gg) p.scores[soff[gg] + key] = s;
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(aempty(acc));
+        acc ^= 1;
+        if (acc == 0) aphase ^= 1;
+      }
+      if (!ok) break;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+}
+
+// ---------------------------------------------------------------------------
+// CUDA-core fallback: one block of 128 threads per work item, thread = key.
+// Handles any head count / dim and both index formats (fp8: code * scale).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(128) index_simt_kernel(const uint16_t *__restrict__ q, const float *__restrict__ w,
+                                                          const uint8_t *__restrict__ cache,
+                                                          const IdxGroup *__restrict__ groups,
+                                                          const IdxItem *__restrict__ items,
+                                                          const int32_t *__restrict__ pages,
+                                                          const int64_t *__restrict__ row_score_off,
+                                                          float *__restrict__ scores, int *err, int Hi, int Di,
+                                                          int P, int fp8, int num_pages) {
+  extern __shared__ float qs[];  // [Hi * Di] of one row, then [Hi] weights
+  const IdxItem item = items[blockIdx.x];
+  const IdxGroup g = groups[item.group];
+  for (int gg = 0; gg < g.nrows; ++gg) {
+    const int row = g.row0 + gg;
+    __syncthreads();
+    for (int i = threadIdx.x; i < Hi * Di; i += blockDim.x)
+      qs[i] = __uint_as_float(static_cast<uint32_t>(q[static_cast<int64_t>(row) * Hi * Di + i]) << 16);
+    for (int i = threadIdx.x; i < Hi; i += blockDim.x) qs[Hi * Di + i] = w[static_cast<int64_t>(row) * Hi + i];
+    __syncthreads();
+    const int pos = g.pos0 + gg;
+    for (int t = item.tile0; t < item.tile1; ++t) {
+      const int key = t * 128 + threadIdx.x;
+      if (key > pos) continue;
+      const int64_t slot = static_cast<int64_t>(g.page_start) + key;
+      const int64_t pi = slot / P;
+      int page = -1;
+      if (pi < g.npages) page = pages[g.page_off + pi];
+      if (page < 0 || page >= num_pages) {
+        atomicOr(err, kErrBounds);
+        continue;
+      }
+      const int64_t prow = static_cast<int64_t>(page) * P + slot % P;
+      float s = 0.f;
+      if (!fp8) {
+        const uint16_t *k = reinterpret_cast<const uint16_t *>(cache) + prow * Di;
+        for (int h = 0; h < Hi; ++h) {
+          float d = 0.f;
+          for (int i = 0; i < Di; ++i) d = fmaf(qs[h * Di + i], __uint_as_float(static_cast<uint32_t>(k[i]) << 16), d);
+          s = fmaf(qs[Hi * Di + h], fmaxf(d, 0.f), s);
+        }
+      } else {
+        const uint8_t *base = cache + static_cast<int64_t>(page) * P * (Di + 4);
+        const uint8_t *k = base + (slot % P) * Di;
+        const float scale = *reinterpret_cast<const float *>(base + static_cast<int64_t>(P) * Di + (slot % P) * 4);
+        for (int h = 0; h < Hi; ++h) {
+          float d = 0.f;
+          for (int i = 0; i < Di; ++i) {
+            __nv_fp8_e4m3 c;
+            c.__x = k[i];
+            d = fmaf(qs[h * Di + i], static_cast<float>(c), d);
+          }
+          s = fmaf(qs[Hi * Di + h], fmaxf(d * scale, 0.f), s);
+        }
+      }
+      scores[row_score_off[row] + key] = s;
+    }
+  }
+}
+
+template <int HI, int DI, int G>
+cudaError_t run_tc(const dsa_ctx *ctx, const dsa_plan_t *plan, const IdxSet &set, const void *q, const float *w,
+                   const void *cache, float *scores, cudaStream_t s, int BH) {
+  using C = IdxTraits<HI, DI, G>;
+  IdxParams prm{};
+  const dsa_config_t &c = ctx->cfg;
+  const CUtensorMapSwizzle swz = C::ROWB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  if (!encode_tiled_2d(&prm.tm_keys, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void *>(cache), DI,
+                       static_cast<uint64_t>(plan->cache_pages) * c.page_size, DI * 2, C::CH, BH, swz))
+    return cudaErrorInvalidValue;
+  if (!encode_tiled_2d(&prm.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void *>(q), DI,
+                       static_cast<uint64_t>(plan->T) * HI, DI * 2, C::CH, C::N, swz))
+    return cudaErrorInvalidValue;
+  prm.w = w;
+  prm.groups = set.groups;
+  prm.items = set.items;
+  prm.cta_begin = set.cta_begin;
+  prm.pages = plan->pages;
+  prm.row_score_off = plan->row_score_off;
+  prm.scores = scores;
+  prm.err = ctx->err;
+  prm.P = c.page_size;
+  prm.BH = BH;
+  prm.num_pages = plan->cache_pages;
+  auto kern = index_tc_kernel<HI, DI, G>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  kern<<<set.n_ctas, kIdxThreads, C::SMEM, s>>>(prm);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool indexer_tc_supported(const dsa_config_t &c, int G) {
+  if (c.index_fmt != DSA_INDEX_BF16) return false;
+  if (c.index_heads == 64 && c.index_dim == 128) return G == 1 || G == 4;
+  if (c.index_heads == 4 && c.index_dim == 32) return G == 1 || G == 4;
+  return false;
+}
+
+int indexer_group_rows(const dsa_config_t &c) { return indexer_tc_supported(c, 4) ? 4 : 1; }
+
+int indexer_ctas_per_sm(const dsa_config_t &, int) { return 1; }
+
+cudaError_t launch_index_scores(const dsa_ctx *ctx, const dsa_plan_t *plan, const void *q, const float *w,
+                                const void *cache, float *scores, cudaStream_t s, int32_t *launches) {
+  const dsa_config_t &c = ctx->cfg;
+  const int BH = plan->box_rows;
+  for (int si = 0; si < 2; ++si) {
+    const IdxSet &set = plan->idx[si];
+    if (set.n_items == 0) continue;
+    const bool tc = indexer_tc_supported(c, set.G) && BH >= 8;
+    cudaError_t e = cudaSuccess;
+    if (tc) {
+      if (c.index_heads == 64 && set.G == 1) e = run_tc<64, 128, 1>(ctx, plan, set, q, w, cache, scores, s, BH);
+      else if (c.index_heads == 64) e = run_tc<64, 128, 4>(ctx, plan, set, q, w, cache, scores, s, BH);
+      else if (set.G == 1) e = run_tc<4, 32, 1>(ctx, plan, set, q, w, cache, scores, s, BH);
+      else e = run_tc<4, 32, 4>(ctx, plan, set, q, w, cache, scores, s, BH);
+    } else {
+      const size_t sm = (static_cast<size_t>(c.index_heads) * c.index_dim + c.index_heads) * sizeof(float);
+      if (sm > 48 * 1024) {
+        e = cudaFuncSetAttribute(index_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sm));
+        if (e != cudaSuccess) return e;
+      }
+      index_simt_kernel<<<set.n_items, 128, sm, s>>>(static_cast<const uint16_t *>(q), w,
+                                                     static_cast<const uint8_t *>(cache), set.groups, set.items,
+                                                     plan->pages, plan->row_score_off, scores, ctx->err,
+                                                     c.index_heads, c.index_dim, c.page_size,
+                                                     c.index_fmt == DSA_INDEX_FP8_132, plan->cache_pages);
+      e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) return e;
+    *launches += 1;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace dsa

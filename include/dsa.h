@@ -1,0 +1,186 @@
+/*
+ * dsa.h -- C ABI of the GB300 (sm_103a) DeepSeek Sparse Attention library.
+ *
+ * The operation (mstar page "mstar.engine.resources.dsa.manager", module
+ * summary, index_topk, select_topk_causal and DSAManager.attend):
+ *
+ *   1. indexer score   s[r, j] = sum_h w[r,h] * relu(q[r,h] . k[j]), in fp32,
+ *                      for every key j = 0 .. pos(r) of row r's request
+ *                      (a row sees the keys up to its own position, itself included);
+ *   2. causal top-k    the topk highest-scoring positions of each row, int32,
+ *                      ties to the earlier position, -1 padded;
+ *   3. sparse MLA      absorbed MLA over the selected latents only:
+ *                      out[r,h] = softmax_j((q_nope[r,h] . c_j + q_pe[r,h] . kpe_j) * sm_scale) . c_j,
+ *                      shape (T, H, kv_lora_rank).
+ *
+ * Everything here is asynchronous on the caller's stream except dsa_create,
+ * dsa_plan (host work, then one host-to-device copy on the stream) and
+ * dsa_get_error (synchronises the stream).  All tensor arguments are DEVICE
+ * pointers owned by the caller, row-major and densely packed, unless stated
+ * otherwise.  Every call returns a dsa_status; no call aborts the process.
+ *
+ * Paged layout (DSASpan / DSAPlan on the mstar page): a request's token at
+ * position p lives at slot = page_start + p of its page list, i.e. in page
+ * pages[slot / page_size] at offset slot % page_size.  The latent cache and the
+ * index-key cache share page ids.
+ *
+ * Cache formats (per token, per layer):
+ *   latent  DSA_LATENT_BF16    : [kv_lora_rank | rope_dim] bf16 (1,152 B at 512+64)
+ *           DSA_LATENT_FP8_656 : [512 e4m3 | 4 fp32 scales, one per 128 | 64 bf16 rope]
+ *                                (656 B; ttnn.transformer.sparse_sdpa "kv" parameter;
+ *                                 LLMServingSim "What the KV cache actually holds")
+ *   index   DSA_INDEX_BF16     : index_dim bf16 per token, cache [pages][page_size][index_dim]
+ *           DSA_INDEX_FP8_132  : 128 e4m3 + one fp32 scale per token (132 B; LLMServingSim,
+ *                                same section), stored page-blocked: each page is
+ *                                [page_size x 128 codes][page_size x fp32 scale].
+ */
+#ifndef DSA_GB300_DSA_H_
+#define DSA_GB300_DSA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t).  NULL is the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st *dsa_stream_t;
+
+typedef int32_t dsa_status;
+enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1,    /* null pointer, bad size, spans that do not tile the rows */
+  DSA_ERR_SHORT_HISTORY = 2,  /* a span's pages cannot hold positions 0 .. ctx_start+q_len-1
+                                 (mstar IndexKeyStore.history raises in this case) */
+  DSA_ERR_OOM = 3,            /* device or host allocation failed */
+  DSA_ERR_CUDA = 4,           /* a CUDA runtime call failed */
+  DSA_ERR_BOUNDS = 5,         /* device side: a selected position outside 0..pos(r), or a
+                                 page id outside the cache; the access was skipped */
+  DSA_ERR_TIMEOUT = 6,        /* device side: a pipeline wait gave up after its time limit */
+  DSA_ERR_UNSUPPORTED = 7     /* shape or format the library does not implement */
+};
+
+enum { DSA_LATENT_BF16 = 0, DSA_LATENT_FP8_656 = 1 };
+enum { DSA_INDEX_BF16 = 0, DSA_INDEX_FP8_132 = 1 };
+
+/* Problem shape, fixed for a context. */
+typedef struct dsa_config {
+  int32_t index_heads;   /* indexer heads Hi (64 for DeepSeek-V3.2) */
+  int32_t index_dim;     /* indexer head dim Di (128) */
+  int32_t topk;          /* positions kept per row (2048) */
+  int32_t heads;         /* MLA query heads H (128) */
+  int32_t kv_lora_rank;  /* latent width L (512); also the output width */
+  int32_t rope_dim;      /* rope width R (64) */
+  int32_t page_size;     /* tokens per cache page */
+  int32_t latent_fmt;    /* DSA_LATENT_* */
+  int32_t index_fmt;     /* DSA_INDEX_* */
+} dsa_config_t;
+
+/* One request's rows of a step (mstar DSASpan): q_len rows from row q_start,
+ * the first at request-local position ctx_start; the request's token p sits
+ * at slot page_start + p of `pages` (num_pages HOST int32 page ids).  Spans
+ * must tile rows [0, T) in order. */
+typedef struct dsa_span {
+  int64_t request_id;    /* caller's id, carried for diagnostics only */
+  int32_t q_start;
+  int32_t q_len;         /* > 0 */
+  int32_t ctx_start;     /* >= 0 */
+  int32_t page_start;    /* >= 0 */
+  const int32_t *pages;  /* host memory, read during dsa_plan only */
+  int32_t num_pages;
+  int32_t reserved;      /* set to 0 */
+} dsa_span_t;
+
+typedef struct dsa_ctx dsa_ctx_t;
+typedef struct dsa_plan dsa_plan_t;
+
+/* Plan statistics (host-side copy). */
+typedef struct dsa_plan_info {
+  int32_t num_rows;          /* T */
+  int32_t num_spans;
+  int32_t needs_selection;   /* 1 when some row sees more than topk keys (mstar DSAPlan) */
+  int32_t index_items;       /* indexer work items (tiles of 128 keys, grouped) */
+  int64_t num_scores;        /* sum over rows of pos(r)+1: the score scratch length */
+  int32_t attend_units;      /* attention work units (row x key split) */
+  int32_t attend_splits_max; /* largest key split count of any row */
+} dsa_plan_info_t;
+
+/* Create a context on CUDA device `device` (>= 0).  device = -1 creates a
+ * host-only context: dsa_plan validates spans and fills dsa_plan_info but
+ * makes no CUDA call, and every compute entry point returns
+ * DSA_ERR_INVALID_ARG.  Returns DSA_ERR_UNSUPPORTED for shapes outside the
+ * library's kernels (see DSA_ERR_UNSUPPORTED below each entry point). */
+dsa_status dsa_create(const dsa_config_t *cfg, int device, dsa_ctx_t **out);
+void dsa_destroy(dsa_ctx_t *ctx);
+
+/* Build a plan from host spans (mstar DSAManager.plan / DSAPlan): validates
+ * the spans, computes every row's position and page list, the indexer work
+ * items and the attention units, and copies them to the device on `stream`
+ * (stream-ordered allocation).  cache_pages is the number of pages in the
+ * caches (page ids must be < cache_pages).  The plan may grow the context's
+ * scratch (cudaMalloc; synchronous when it grows).  Errors:
+ * DSA_ERR_INVALID_ARG (spans do not tile the rows in order, q_len <= 0,
+ * negative ctx_start/page_start, null pages, page id out of range),
+ * DSA_ERR_SHORT_HISTORY (too few pages for ctx_start + q_len tokens). */
+dsa_status dsa_plan(dsa_ctx_t *ctx, const dsa_span_t *spans, int32_t num_spans, int32_t cache_pages,
+                    dsa_stream_t stream, dsa_plan_t **out);
+/* Frees the plan's device metadata in order on the plan's stream. */
+void dsa_plan_destroy(dsa_plan_t *plan);
+dsa_status dsa_plan_get_info(const dsa_plan_t *plan, dsa_plan_info_t *info);
+
+/* Store the step's index keys (mstar DSAManager.store_keys): row r's key goes
+ * to the slot of its own position.  keys: (T, index_dim) bf16, or (T, 132)
+ * uint8 rows [128 e4m3 | fp32 scale] for DSA_INDEX_FP8_132.  index_cache: the
+ * page-resident index cache in the context's index format.  Must precede
+ * dsa_index_topk for the same step (the current chunk is stored before
+ * selection). */
+dsa_status dsa_store_keys(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *keys, void *index_cache,
+                          dsa_stream_t stream);
+
+/* Score and select (mstar index_topk + select_topk_causal): q (T, Hi, Di)
+ * bf16, w (T, Hi) fp32 (any scales folded in), index_cache as above;
+ * selection (T, topk) int32 out: each row's selected positions in ascending
+ * order, then -1 (rows that see fewer than topk keys keep them all).  Ties
+ * go to the earlier position.  Scores are fp32 and live in the context's
+ * scratch. */
+dsa_status dsa_index_topk(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *q, const float *w,
+                          const void *index_cache, int32_t *selection, dsa_stream_t stream);
+
+/* The indexer score alone (step 1): scores out, fp32, row r's pos(r)+1
+ * scores starting at offset sum_{i<r} (pos(i)+1) (dsa_plan_info.num_scores
+ * in total). */
+dsa_status dsa_index_scores(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *q, const float *w,
+                            const void *index_cache, float *scores, dsa_stream_t stream);
+
+/* The selection alone (step 2) over caller-provided scores in the layout
+ * dsa_index_scores writes. */
+dsa_status dsa_topk_from_scores(dsa_ctx_t *ctx, const dsa_plan_t *plan, const float *scores,
+                                int32_t *selection, dsa_stream_t stream);
+
+/* Sparse absorbed MLA (mstar DSAManager.attend; V = the first kv_lora_rank
+ * columns of each latent row as in ttnn sparse_sdpa): selection (T, topk)
+ * int32 request-local positions, -1 entries skipped (entries outside
+ * 0..pos(r) set DSA_ERR_BOUNDS and are skipped); q_nope (T, H, L) bf16;
+ * q_pe (T, H, R) bf16; latent_cache in the context's latent format with this
+ * step's latents already written; sink (H) fp32 logits already in scaled
+ * units that join only the softmax denominator, or NULL; out (T, H, L) bf16.
+ * A row with nothing selected and no sink gets zeros. */
+dsa_status dsa_attend(dsa_ctx_t *ctx, const dsa_plan_t *plan, const int32_t *selection, const void *q_nope,
+                      const void *q_pe, const void *latent_cache, const float *sink, float sm_scale, void *out,
+                      dsa_stream_t stream);
+
+/* Synchronise `stream`, read and clear the context's device error word.
+ * Returns DSA_OK, DSA_ERR_BOUNDS, DSA_ERR_TIMEOUT or DSA_ERR_CUDA. */
+dsa_status dsa_get_error(dsa_ctx_t *ctx, dsa_stream_t stream);
+
+/* Number of kernels the last compute call on this context launched (for
+ * accounting; host-side counter, no synchronisation). */
+int32_t dsa_last_launch_count(const dsa_ctx_t *ctx);
+
+const char *dsa_status_str(dsa_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSA_GB300_DSA_H_ */

@@ -1,0 +1,119 @@
+"""The C-ABI library on the host (no GPU): it builds, loads, exports every
+symbol include/dsa.h declares, and its planner validates spans as the header
+states (a host-only context, device -1, makes no CUDA call)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch  # noqa: F401  (loads the CUDA runtime the library links against)
+
+from deepseek_sparse_attention_dsa_gb300 import build as dsa_build
+from deepseek_sparse_attention_dsa_gb300 import dsa
+from deepseek_sparse_attention_dsa_gb300 import workloads as W
+from tests.dsa_cases import tiny_shape
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    dsa_build.build()
+    return dsa.load()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "dsa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = header_functions()
+    assert "dsa_plan" in names and "dsa_attend" in names and "dsa_index_topk" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) <= set(dsa.EXPORTED)
+
+
+def test_status_strings(lib):
+    for s in range(8):
+        assert lib.dsa_status_str(s)
+
+
+def _host_ctx(shape=None):
+    return dsa.Context(shape or W.DSAShape(**W.DEEPSEEK), device=-1)
+
+
+class S:
+    def __init__(self, q_start, q_len, ctx_start, pages, page_start=0):
+        self.q_start, self.q_len, self.ctx_start, self.pages, self.page_start = q_start, q_len, ctx_start, pages, page_start
+
+
+def _status(fn):
+    try:
+        fn()
+    except dsa.DSAError as e:
+        return e.status
+    return 0
+
+
+def test_create_rejects_bad_configs(lib):
+    bad = W.DSAShape(**dict(W.DEEPSEEK, page_size=0))
+    assert _status(lambda: dsa.Context(bad, device=-1)) == 1
+    odd = W.DSAShape(**dict(W.DEEPSEEK, index_dim=3))          # rows not a multiple of 16 bytes
+    assert _status(lambda: dsa.Context(odd, device=-1)) == 7
+    fp8 = W.DSAShape(**dict(W.DEEPSEEK, index_dim=64), index_fmt=W.INDEX_FP8_132)   # fp8 rows are 128 + 4
+    assert _status(lambda: dsa.Context(fp8, device=-1)) == 7
+
+
+def test_plan_validation(lib):
+    ctx = _host_ctx()
+    P = 64
+    pg = np.arange(4, dtype=np.int32)
+    ok = ctx.plan([S(0, 1, 100, pg[:2]), S(1, 3, 0, pg[2:3])], cache_pages=4)
+    assert ok.num_rows == 4 and not ok.needs_selection
+    assert ok.num_scores == 101 + (1 + 2 + 3)
+    # spans must tile rows in order
+    assert _status(lambda: ctx.plan([S(1, 1, 0, pg[:1])], 4)) == 1
+    assert _status(lambda: ctx.plan([S(0, 2, 0, pg[:1]), S(1, 1, 0, pg[1:2])], 4)) == 1
+    assert _status(lambda: ctx.plan([S(0, 0, 0, pg[:1])], 4)) == 1
+    assert _status(lambda: ctx.plan([S(0, 1, -1, pg[:1])], 4)) == 1
+    assert _status(lambda: ctx.plan([S(0, 1, 0, pg[:1], page_start=-8)], 4)) == 1
+    # too few pages for ctx_start + q_len tokens (mstar IndexKeyStore.history raises)
+    assert _status(lambda: ctx.plan([S(0, 1, P, pg[:1])], 4)) == 2
+    assert _status(lambda: ctx.plan([S(0, 1, P - 8, pg[:1], page_start=8)], 4)) == 2
+    # page ids must exist in the cache
+    assert _status(lambda: ctx.plan([S(0, 1, 0, np.array([4], np.int32))], 4)) == 1
+    assert _status(lambda: ctx.plan([S(0, 1, 0, np.array([-1], np.int32))], 4)) == 1
+    # empty step
+    empty = ctx.plan([], cache_pages=4)
+    assert empty.num_rows == 0 and empty.num_scores == 0
+
+
+def test_plan_needs_selection_and_units(lib):
+    ctx = _host_ctx()
+    K = W.DEEPSEEK["topk"]
+    pg = np.arange(64, dtype=np.int32)
+    short = ctx.plan([S(0, 1, K - 1, pg[:32])], cache_pages=64)      # sees exactly topk keys
+    assert not short.needs_selection
+    long = ctx.plan([S(0, 1, K, pg[:33])], cache_pages=64)           # sees topk + 1
+    assert long.needs_selection
+    # one decode row is split over several key ranges for occupancy; a full
+    # prefill batch is not
+    assert long.info.attend_splits_max > 1 and long.info.attend_units == long.info.attend_splits_max
+    wl = W.config(2)
+    big = ctx.plan(wl.spans, wl.num_pages)
+    assert big.info.attend_units == wl.num_rows and big.info.attend_splits_max == 1
+    assert big.num_scores == sum(range(8193, 16385))
+
+
+def test_compute_calls_refuse_host_only_context(lib):
+    ctx = _host_ctx()
+    plan = ctx.plan([S(0, 1, 0, np.array([0], np.int32))], cache_pages=1)
+    L = dsa.load()
+    st = L.dsa_index_topk(ctx.handle, plan.handle, None, None, None, None, None)
+    assert st == 1
+    assert L.dsa_attend(ctx.handle, plan.handle, None, None, None, None, None, ctypes.c_float(1.0), None, None) == 1
+    assert L.dsa_get_error(ctx.handle, None) == 1

@@ -1,0 +1,171 @@
+"""GPU parity: the CUDA library (through the C ABI) against the CPU oracle on
+the same seeded inputs, at sizes the oracle finishes in seconds that still
+span several tiles and a ragged tail."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from deepseek_sparse_attention_dsa_gb300 import dsa
+from deepseek_sparse_attention_dsa_gb300 import workloads as W
+from tests import harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from deepseek_sparse_attention_dsa_gb300 import build
+    build.build()
+
+
+def _run(wl, attend_with_oracle_selection=True, exact_selection=False):
+    ic, lc, st = H.host_inputs(wl)
+    ref = oracle.run_all(wl, ic, lc, st)
+    ctx = dsa.Context(wl.shape, 0)
+    dev = W.StepInputs(*(H.to_dev(x) for x in (st.q, st.w, st.keys, st.q_nope, st.q_pe, st.sink)))
+    got = H.gpu_pipeline(ctx, wl, ic.cuda(), lc.cuda(), dev)
+    # the stored cache is the oracle's, byte for byte
+    assert np.array_equal(got["index_cache"].view(torch.uint8).numpy().reshape(-1),
+                          ref["index_cache"].reshape(-1))
+    H.check_scores(got["scores"], ref["scores"], ref["offsets"])
+    H.check_selection(got["selection"], ref["selection"], ref["scores"], ref["offsets"], wl.shape.topk,
+                      exact=exact_selection)
+    fp8 = wl.shape.latent_fmt == W.LATENT_FP8_656
+    # end to end: the oracle attends over the GPU's selection (same rows, same set)
+    ref_e2e = oracle.attend(wl.shape, wl.spans, wl.num_pages, got["selection"], st.q_nope, st.q_pe, lc, st.sink)
+    H.check_attention(got["out"], ref_e2e, fp8)
+    if attend_with_oracle_selection:
+        # decoupled: the GPU attends over the oracle's selection
+        plan = ctx.plan(wl.spans, wl.num_pages)
+        out = ctx.attend(plan, torch.from_numpy(ref["selection"]).cuda(), dev.q_nope, dev.q_pe, lc.cuda(), dev.sink,
+                         wl.shape.sm_scale)
+        ctx.get_error()
+        H.check_attention(out.float().cpu().numpy(), ref["out"], fp8)
+    return ctx, ref, got
+
+
+def test_tiny_prefill_config():
+    _run(W.config(0))
+
+
+def test_tiny_prefill_integer_inputs_bit_exact():
+    wl = W.config(0)
+    wl.dist = W.Distributions(integer=True)
+    ic, lc, st = H.host_inputs(wl)
+    ref = oracle.run_all(wl, ic, lc, st)
+    ctx = dsa.Context(wl.shape, 0)
+    dev = W.StepInputs(*(H.to_dev(x) for x in (st.q, st.w, st.keys, st.q_nope, st.q_pe, st.sink)))
+    got = H.gpu_pipeline(ctx, wl, ic.cuda(), lc.cuda(), dev)
+    assert np.array_equal(got["scores"], ref["scores"])
+    H.check_selection(got["selection"], ref["selection"], ref["scores"], ref["offsets"], wl.shape.topk, exact=True)
+
+
+def test_deepseek_shapes_bf16():
+    _run(H.deepseek_small(seed=1))
+
+
+def test_deepseek_shapes_integer_bit_exact():
+    wl = H.deepseek_small(seed=2, integer=True, decode_ctx=(2300, 4100), chunk=(2040, 24))
+    ic, lc, st = H.host_inputs(wl)
+    cache = oracle.store_keys(wl.shape, wl.spans, wl.num_pages, st.keys, ic)
+    sc, off = oracle.index_scores(wl.shape, wl.spans, wl.num_pages, st.q, st.w, cache)
+    sel = oracle.topk(wl.shape, wl.spans, sc, off)
+    ctx = dsa.Context(wl.shape, 0)
+    plan = ctx.plan(wl.spans, wl.num_pages)
+    icd = ic.cuda()
+    ctx.store_keys(plan, st.keys.cuda(), icd)
+    g_sc = ctx.index_scores(plan, st.q.cuda(), st.w.cuda(), icd).cpu().numpy()[:plan.num_scores]
+    assert np.array_equal(g_sc, sc)
+    g_sel = ctx.index_topk(plan, st.q.cuda(), st.w.cuda(), icd).cpu().numpy()
+    ctx.get_error()
+    H.check_selection(g_sel, sel, sc, off, wl.shape.topk, exact=True)
+
+
+def test_deepseek_shapes_page_start_and_sink():
+    _run(H.deepseek_small(seed=3, sink=True, page_start=8, decode_ctx=(2049, 3333), chunk=(1990, 70)))
+
+
+def test_deepseek_shapes_fewer_heads():
+    _run(H.deepseek_small(seed=4, heads=64, decode_ctx=(2600,), chunk=(2040, 16)))
+
+
+def test_fp8_formats():
+    _run(H.deepseek_small(seed=5, fp8=True, sink=True, decode_ctx=(2200, 2900), chunk=(2030, 24)))
+
+
+def test_topk_from_oracle_scores_is_exact():
+    """Given the oracle's own fp32 scores, the GPU selection is the oracle's set exactly."""
+    for wl in (W.config(0), H.deepseek_small(seed=6, decode_ctx=(9000, 2049, 2048, 100), chunk=(2000, 100))):
+        ic, lc, st = H.host_inputs(wl)
+        cache = oracle.store_keys(wl.shape, wl.spans, wl.num_pages, st.keys, ic)
+        sc, off = oracle.index_scores(wl.shape, wl.spans, wl.num_pages, st.q, st.w, cache)
+        sel = oracle.topk(wl.shape, wl.spans, sc, off)
+        ctx = dsa.Context(wl.shape, 0)
+        plan = ctx.plan(wl.spans, wl.num_pages)
+        g = ctx.topk_from_scores(plan, torch.from_numpy(sc).cuda()).cpu().numpy()
+        H.check_selection(g, sel, sc, off, wl.shape.topk, exact=True)
+
+
+def test_topk_ties_and_signed_zero():
+    """Many equal scores (including -0.0 vs +0.0): the earliest positions win."""
+    sh = W.DSAShape(**W.DEEPSEEK)
+    n = 5000
+    wl = W.build_workload("ties", sh, [(n - 1, 1), (n - 1, 1)], seed=9)
+    off = np.array([0, n, 2 * n], np.int64)
+    rng = np.random.default_rng(0)
+    a = rng.integers(0, 3, size=n).astype(np.float32)          # three values, massive ties
+    b = np.zeros(n, np.float32)
+    b[rng.random(n) < 0.5] = -0.0
+    b[:100] = 1.0
+    sc = np.concatenate([a, b])
+    ref = oracle.topk(sh, wl.spans, sc, off)
+    ctx = dsa.Context(sh, 0)
+    plan = ctx.plan(wl.spans, wl.num_pages)
+    g = ctx.topk_from_scores(plan, torch.from_numpy(sc).cuda()).cpu().numpy()
+    H.check_selection(g, ref, sc, off, sh.topk, exact=True)
+
+
+def test_bounds_errors_are_reported_not_faulted():
+    """Selected positions past the row or below -1 set DSA_ERR_BOUNDS and are skipped."""
+    wl = H.deepseek_small(seed=7, decode_ctx=(3000,), chunk=None)
+    ic, lc, st = H.host_inputs(wl)
+    ctx = dsa.Context(wl.shape, 0)
+    plan = ctx.plan(wl.spans, wl.num_pages)
+    sel = torch.full((1, wl.shape.topk), -1, dtype=torch.int32)
+    sel[0, :10] = torch.arange(10)
+    sel[0, 10] = 3000           # row 0 sits at position 2999
+    sel[0, 11] = -5
+    out = ctx.attend(plan, sel.cuda(), st.q_nope.cuda(), st.q_pe.cuda(), lc.cuda(), None, wl.shape.sm_scale)
+    with pytest.raises(dsa.DSAError) as e:
+        ctx.get_error()
+    assert e.value.status == 5
+    ctx.get_error()  # the word was cleared
+    ref_sel = sel.numpy().copy()
+    ref_sel[0, 10:12] = -1
+    ref = oracle.attend(wl.shape, wl.spans, wl.num_pages, ref_sel, st.q_nope, st.q_pe, lc, None)
+    H.check_attention(out.float().cpu().numpy(), ref)
+
+
+def test_empty_step_and_launch_count():
+    sh = W.DSAShape(**W.DEEPSEEK)
+    ctx = dsa.Context(sh, 0)
+    plan = ctx.plan([], cache_pages=1)
+    assert plan.num_rows == 0
+    wl = H.deepseek_small(seed=8, decode_ctx=(2500,), chunk=None)
+    ic, lc, st = H.device_inputs(wl)
+    plan = ctx.plan(wl.spans, wl.num_pages)
+    ctx.index_topk(plan, st.q, st.w, ic)
+    assert ctx.last_launch_count() == 2
+    ctx.get_error()
+
+
+def test_generator_is_identical_on_gpu():
+    wl = H.deepseek_small(seed=10, fp8=True, sink=True, decode_ctx=(700,), chunk=(100, 5))
+    a = H.host_inputs(wl)
+    b = H.device_inputs(wl)
+    for x, y in zip(a[:2], b[:2]):
+        assert torch.equal(x.view(torch.uint8), y.cpu().view(torch.uint8))
+    for x, y in zip(a[2].__dict__.values(), b[2].__dict__.values()):
+        if x is not None:
+            assert torch.equal(x.contiguous().view(torch.uint8), y.cpu().contiguous().view(torch.uint8))
