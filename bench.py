@@ -1,0 +1,431 @@
+#!/usr/bin/env python3
+"""Benchmark of one DSA step (store keys -> indexer score -> causal top-k ->
+sparse absorbed MLA) on GB300, printed as one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Workloads (synthetic, seeded; DeepSeek-V3.2 shapes):
+  long_decode (default)  128 requests x 1 row, contexts ~U[65536, 131072]
+  decode                 32 requests x 1 row, contexts ~U[4096, 16384]
+  chunked_prefill        1 request, 8192 cached + 8192 new rows
+  mixed_fp8              16 decode rows + two 2048-row chunks, fp8 caches, sinks
+  tiny_prefill           2 requests, contexts 256 / 384 (small shapes)
+
+`value` is whole-job throughput (decode rows/s, or prefill tokens/s) with the
+caches and the step inputs resident in HBM; each step is timed with CUDA
+events on the launching stream and L2 is flushed (256 MB write) between steps
+outside the timed events.  `e2e` is the same metric through the public API
+with host buffers: per step dsa_plan from host spans, pinned host-to-device
+copies of the step's inputs, the step, and a device-to-host copy of its output.
+`--impl reference` times the CPU oracle (the only reference this method has)
+on a bounded sample of the same workload on the host cores.
+Multi-GPU (torchrun): independent replicas, one per rank (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from deepseek_sparse_attention_dsa_gb300 import workloads as W  # noqa: E402
+
+METRIC = "DSA decode rows/s + prefill tokens/s at 1 GB300; % HBM / tensor-core roofline"
+WORKLOADS = {"tiny_prefill": 0, "decode": 1, "chunked_prefill": 2, "long_decode": 3, "mixed_fp8": 4}
+
+
+def rank_info():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ----------------------------------------------------------------------------
+# algorithmic work (bytes / flops) of a workload
+# ----------------------------------------------------------------------------
+def algorithmic(wl):
+    sh = wl.shape
+    _, pos, _ = wl.row_table()
+    vis = pos + 1
+    nsel = np.minimum(vis, sh.topk)
+    T = len(pos)
+    idx_bytes = float(vis.sum()) * sh.index_row_bytes + T * (sh.index_heads * sh.index_dim * 2 + sh.index_heads * 4)
+    lat_bytes = float(nsel.sum()) * sh.latent_row_bytes
+    att_io = T * sh.heads * (sh.kv_lora_rank + sh.rope_dim) * 2 + T * sh.heads * sh.kv_lora_rank * 2 + T * sh.topk * 4
+    store = T * sh.index_row_bytes * 2
+    idx_flops = float(vis.sum()) * 2.0 * sh.index_heads * sh.index_dim
+    att_flops = float(nsel.sum()) * 2.0 * sh.heads * (sh.kv_lora_rank + sh.rope_dim + sh.kv_lora_rank)
+    return dict(index_bytes=idx_bytes, attend_bytes=lat_bytes + att_io, step_bytes=idx_bytes + lat_bytes + att_io + store,
+                index_flops=idx_flops, attend_flops=att_flops, rows=T, keys=int(vis.sum()), selected=int(nsel.sum()))
+
+
+def unit_of(wl):
+    decode = all(s.q_len == 1 for s in wl.spans)
+    return ("rows/s" if decode else "tokens/s"), decode
+
+
+def workload_config(name, wl):
+    sh = wl.shape
+    ctxs = [s.ctx_end for s in wl.spans]
+    return {"workload": name, "requests": len(wl.spans), "rows": wl.num_rows, "ctx_min": int(min(ctxs)),
+            "ctx_max": int(max(ctxs)), "ctx_mean": float(np.mean(ctxs)), "topk": sh.topk,
+            "indexer": "%dx%d %s" % (sh.index_heads, sh.index_dim, "fp8-132B" if sh.index_fmt else "bf16"),
+            "mla": "H=%d %d+%d %s" % (sh.heads, sh.kv_lora_rank, sh.rope_dim, "fp8-656B" if sh.latent_fmt else "bf16"),
+            "page_size": sh.page_size, "sink": bool(sh.has_sink), "seed": wl.seed,
+            "l2": "flushed between steps (256 MB write outside the timed events)"}
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------
+# our implementation
+# ----------------------------------------------------------------------------
+def run_ours(args, name, rank, world, local_rank):
+    from deepseek_sparse_attention_dsa_gb300 import build as lib_build
+    from deepseek_sparse_attention_dsa_gb300 import dsa
+
+    lib_build.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = W.config(WORKLOADS[name], seed=1000 + WORKLOADS[name] + 7919 * rank)
+    sh = wl.shape
+    unit, decode = unit_of(wl)
+    work = algorithmic(wl)
+
+    ic = W.make_index_cache(wl, device=dev)
+    lc = W.make_latent_cache(wl, device=dev)
+    st = W.make_step_inputs(wl, device=dev)
+    ctx = dsa.Context(sh, local_rank)
+    stream = torch.cuda.current_stream(dev)
+    t0 = time.perf_counter()
+    plan = ctx.plan(wl.spans, wl.num_pages)
+    torch.cuda.synchronize(dev)
+    plan_ms = (time.perf_counter() - t0) * 1e3
+    scores = torch.empty(max(1, plan.num_scores), dtype=torch.float32, device=dev)
+    sel = torch.empty(plan.num_rows, sh.topk, dtype=torch.int32, device=dev)
+    out = torch.empty(plan.num_rows, sh.heads, sh.kv_lora_rank, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    launches = [0]
+
+    def step(record):
+        if record:
+            ev[0].record(stream)
+        ctx.store_keys(plan, st.keys, ic)
+        n = ctx.last_launch_count()
+        if record:
+            ev[1].record(stream)
+        ctx.index_scores(plan, st.q, st.w, ic, scores)
+        n += ctx.last_launch_count()
+        if record:
+            ev[2].record(stream)
+        ctx.topk_from_scores(plan, scores, sel)
+        n += ctx.last_launch_count()
+        if record:
+            ev[3].record(stream)
+        ctx.attend(plan, sel, st.q_nope, st.q_pe, lc, st.sink, sh.sm_scale, out)
+        n += ctx.last_launch_count()
+        if record:
+            ev[4].record(stream)
+        launches[0] = n
+
+    for _ in range(args.warmup):
+        step(False)
+    ctx.get_error()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    stage = {"store": [], "index": [], "topk": [], "attend": [], "step": []}
+    n_launch = 0
+    with ClockSampler(local_rank) as clk:
+        for _ in range(args.steps):
+            flush.zero_()
+            step(True)
+            n_launch += launches[0]
+            ev[4].synchronize()
+            stage["store"].append(ev[0].elapsed_time(ev[1]))
+            stage["index"].append(ev[1].elapsed_time(ev[2]))
+            stage["topk"].append(ev[2].elapsed_time(ev[3]))
+            stage["attend"].append(ev[3].elapsed_time(ev[4]))
+            stage["step"].append(ev[0].elapsed_time(ev[4]))
+    torch.cuda.synchronize(dev)
+    ctx.get_error()
+    total_ms = float(sum(stage["step"]))
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    units_per_step = work["rows"]
+    value = units_per_step * world / (ms_per_step / 1e3)
+
+    # ---- end to end through the public API with host buffers
+    pinned = {k: getattr(st, k).cpu().pin_memory() for k in ("q", "w", "keys", "q_nope", "q_pe")}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+    d2h = out_h.numel() * out_h.element_size()
+    dbuf = {k: torch.empty_like(getattr(st, k)) for k in pinned}
+
+    def e2e_step():
+        p = ctx.plan(wl.spans, wl.num_pages)
+        for k, v in pinned.items():
+            dbuf[k].copy_(v, non_blocking=True)
+        ctx.store_keys(p, dbuf["keys"], ic)
+        s = ctx.index_topk(p, dbuf["q"], dbuf["w"], ic, sel)
+        ctx.attend(p, s, dbuf["q_nope"], dbuf["q_pe"], lc, st.sink, sh.sm_scale, out)
+        out_h.copy_(out, non_blocking=True)
+        torch.cuda.current_stream(dev).synchronize()
+        p.close()
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    e2e_steps = max(3, min(args.steps, 20))
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    ctx.get_error()
+
+    hbm, bf16, bf16_sus, peak_kind = measured_peaks()
+    idx_ms = statistics.mean(stage["index"])
+    att_ms = statistics.mean(stage["attend"])
+    if decode:
+        achieved = work["index_bytes"] / (idx_ms / 1e3) / 1e9
+        roof = {"kernel": "index_tc_kernel (indexer score)", "bound": "hbm", "achieved": round(achieved, 1),
+                "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                "traffic": profile_traffic("index_tc_kernel", name), "peak_kind": peak_kind + " (hbm_gbs)"}
+    else:
+        achieved = work["attend_flops"] / (att_ms / 1e3) / 1e12
+        roof = {"kernel": "attend_tc_kernel (sparse MLA)", "bound": "tensor", "achieved": round(achieved, 1),
+                "peak": bf16, "unit": "TFLOP/s", "frac": round(achieved / bf16, 4),
+                "traffic": profile_traffic("attend_tc_kernel", name), "peak_kind": peak_kind + " (bf16_tflops burst)"}
+    step_gbs = work["step_bytes"] / (ms_per_step / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if not sh.latent_fmt else "fp8+bf16",
+        "data": "synthetic (seeded counter-based generator; no dataset or weights)",
+        "config": workload_config(name, wl),
+        "roofline": roof,
+        "step_hbm": {"algorithmic_bytes": work["step_bytes"], "achieved_gbs": round(step_gbs, 1),
+                     "frac": round(step_gbs / hbm, 4)},
+        "stages_ms": {k: round(statistics.mean(v), 4) for k, v in stage.items()},
+        "index_tflops": round(work["index_flops"] / (idx_ms / 1e3) / 1e12, 2),
+        "attend_tflops": round(work["attend_flops"] / (att_ms / 1e3) / 1e12, 2),
+        "plan_ms": round(plan_ms, 3),
+        "e2e": {"value": round(units_per_step * world / e2e_s, 2), "unit": unit, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 3)},
+        "gpu_launches": n_launch,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_rows)
+    return line
+
+
+def profile_traffic(kernel, workload):
+    """dram bytes per launch from a committed ncu summary of this kernel and
+    workload, if its source fingerprint matches the current source."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "%s_%s.md" % (kernel.split("_kernel")[0], workload))
+    if not os.path.exists(path):
+        return None
+    src = {"index_tc": "indexer.cu", "attend_tc": "attend.cu"}.get(kernel.split("_kernel")[0])
+    fp = None
+    if src:
+        with open(os.path.join(ROOT, "deepseek_sparse_attention_dsa_gb300", "csrc", src), "rb") as f:
+            fp = hashlib.sha256(f.read()).hexdigest()[:16]
+    traffic, sha = None, None
+    for ln in open(path):
+        if ln.startswith("traffic_bytes_per_launch:"):
+            traffic = float(ln.split(":")[1])
+        if ln.startswith("source_sha256_16:"):
+            sha = ln.split(":")[1].strip()
+    if traffic is None or (fp is not None and sha != fp):
+        return None
+    return traffic
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle baseline
+# ----------------------------------------------------------------------------
+def oracle_sample(wl, nrows):
+    """A bounded sample of the workload for the oracle: its first spans
+    covering about `nrows` rows (or the first `nrows` rows of one long chunk),
+    with host copies of the inputs.  Inputs are generated on the GPU when one
+    is present (the generator is bit-identical on both) and only the latent
+    rows the sample's selection reads are filled."""
+    import oracle
+    take, rows = [], 0
+    for i, s in enumerate(wl.spans):
+        if rows >= nrows:
+            break
+        if rows + s.q_len > nrows and take:
+            break
+        take.append(i)
+        rows += s.q_len
+    sub = wl.sub_workload(take)
+    if rows > nrows:
+        sub.spans[0].q_len = nrows
+        rows = nrows
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    ic = W.make_index_cache(sub, device=dev).cpu()
+    st = W.make_step_inputs(sub, device=dev)
+    st = W.StepInputs(*(None if x is None else x.cpu() for x in (st.q, st.w, st.keys, st.q_nope, st.q_pe, st.sink)))
+    cache = oracle.store_keys(sub.shape, sub.spans, sub.num_pages, st.keys, ic)
+    sc, off = oracle.index_scores(sub.shape, sub.spans, sub.num_pages, st.q, st.w, cache)
+    sel = oracle.topk(sub.shape, sub.spans, sc, off)
+    _, pos, _ = sub.row_table()
+    toks = set()
+    for r, s in enumerate(sub.spans):
+        for i in range(s.q_len):
+            row = s.q_start + i
+            toks.update((s.token_base + sel[row][sel[row] >= 0]).tolist())
+    lc = W.make_latent_cache(sub, device=dev, tokens=toks).cpu()
+    return sub, ic, lc, st, rows, take
+
+
+def cpu_baseline(wl, nrows):
+    import oracle
+    sub, ic, lc, st, rows, take = oracle_sample(wl, nrows)
+    t0 = time.perf_counter()
+    oracle.run_all(sub, ic, lc, st)
+    dt = time.perf_counter() - t0
+    return {"value": round(rows / dt, 4), "unit": unit_of(wl)[0], "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": "%d rows of the same workload (spans %s%s), store+score+select+attend, %.1f s"
+                      % (rows, take[:4], "..." if len(take) > 4 else "", dt)}
+
+
+def run_reference(args, name, rank, world):
+    """The reference arm: the CPU oracle timed on the host cores, bounded samples."""
+    if rank != 0:
+        return None
+    import oracle
+    wl = W.config(WORKLOADS[name])
+    unit, _ = unit_of(wl)
+    sub, ic, lc, st, rows, take = oracle_sample(wl, args.cpu_rows)
+    for _ in range(min(args.warmup, 1)):
+        oracle.run_all(sub, ic, lc, st)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.run_all(sub, ic, lc, st)
+    dt = (time.perf_counter() - t0) / args.steps
+    v = rows / dt
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": workload_config(name, wl),
+            "cpu_baseline": {"value": round(v, 4), "unit": unit, "cores": oracle.max_threads(), "kind": "oracle",
+                             "sample": "%d rows per step (spans %s%s) of %s, store+score+select+attend"
+                                       % (rows, take[:4], "..." if len(take) > 4 else "", name)},
+            "e2e": {"value": round(v, 4), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="long_decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-rows", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
+    rank, world, local_rank = rank_info()
+    if args.impl == "reference":
+        line = run_reference(args, args.workload, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    line = run_ours(args, args.workload, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

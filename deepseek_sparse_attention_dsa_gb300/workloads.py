@@ -28,8 +28,8 @@ Formats (per token, per layer):
                                 each page is [page_size x 128 codes][page_size x fp32]
   * bf16 latent   (1,152 B)   : [kv_lora_rank | rope] bf16
   * fp8 latent    (656 B)     : [512 e4m3 | 4 fp32 scales (one per 128) | 64 bf16 rope]
-fp8 packing uses scale = amax / 448 per group (1 when amax == 0) and
-round-to-nearest-even e4m3 codes saturated at +-448 (torch's float8_e4m3fn cast).
+fp8 packing uses a power-of-two scale per group, 2^(floor(log2 amax) - 7) (1 when
+amax == 0), and round-to-nearest-even e4m3 codes (torch's float8_e4m3fn cast).
 """
 from __future__ import annotations
 
@@ -81,9 +81,11 @@ def _bits(ids: torch.Tensor, seed: int, stream: int, draw: int) -> torch.Tensor:
     key = _stream_key(seed, stream, draw)
     h = hash32((ids & _M32) ^ key)
     if ids.numel() and int(ids.max()) > _M32:
-        # ids above 2**32: fold the high word in with a second round
+        # ids at or above 2**32 fold their high word in with a second round;
+        # the choice is per element, so a value never depends on its neighbours
         key_hi = hash32(key ^ 0x5BD1E995)
-        h = hash32(h ^ _mul32(((ids >> 32) ^ key_hi) & _M32, 0x9E3779B1))
+        hi = ids >> 32
+        h = torch.where(hi != 0, hash32(h ^ _mul32((hi ^ key_hi) & _M32, 0x9E3779B1)), h)
     return h
 
 
@@ -234,6 +236,15 @@ class Workload:
             m[rows] = True
         return m
 
+    def row_workload(self, span_index: int, row_in_span: int) -> "Workload":
+        """One row of one span as its own single-row step (pages renumbered,
+        logical ids kept): the row sees the same keys and latents as in the
+        full workload."""
+        s = self.spans[span_index]
+        sp = replace(s, q_start=0, q_len=1, ctx_start=s.ctx_start + row_in_span,
+                     pages=np.arange(len(s.pages), dtype=np.int32))
+        return Workload(self.name + "/row", self.shape, [sp], len(s.pages), self.seed, self.dist)
+
     def sub_workload(self, span_indices) -> "Workload":
         """A workload holding only the given spans, re-packed from row 0 with
         pages renumbered 0..n-1.  Logical ids are kept, so every value is the same
@@ -272,11 +283,15 @@ def _latent_values(wl: Workload, tok: torch.Tensor) -> torch.Tensor:
 
 
 def _fp8_groups(x: torch.Tensor, group: int):
-    """Per-group e4m3 codes and fp32 scales (scale = amax / 448, 1 if amax == 0)."""
+    """Per-group e4m3 codes and fp32 scales.  The scale is a power of two,
+    2^(floor(log2 amax) - 7) (1 if amax == 0), so the largest |x| / scale lies in
+    [128, 256) within e4m3's range and every step is exact on any device."""
     n, d = x.shape
     g = x.view(n, d // group, group)
     amax = g.abs().amax(dim=2)
-    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    _, e = torch.frexp(amax)                      # amax = m * 2^e, m in [0.5, 1)
+    scale = torch.ldexp(torch.ones_like(amax), (e - 8).to(torch.int32))
+    scale = torch.where(amax > 0, scale, torch.ones_like(amax))
     codes = _to_e4m3_bytes(g / scale.unsqueeze(2)).view(n, d)
     return codes, scale.to(torch.float32)
 
@@ -337,13 +352,18 @@ def make_index_cache(wl: Workload, device="cpu", include_step: bool = False, chu
     return torch.cat([codes_all.view(wl.num_pages, -1), scales_all.view(wl.num_pages, -1)], dim=1).contiguous()
 
 
-def make_latent_cache(wl: Workload, device="cpu", chunk_rows: int = 1 << 19) -> torch.Tensor:
+def make_latent_cache(wl: Workload, device="cpu", chunk_rows: int = 1 << 19, tokens=None) -> torch.Tensor:
     """The paged MLA latent cache with every position < ctx_end written (the
     caller writes a step's latents before attention).  bf16:
-    [num_pages, page_size, L+R]; fp8: [num_pages, page_size, 656] uint8."""
+    [num_pages, page_size, L+R]; fp8: [num_pages, page_size, 656] uint8.
+    ``tokens``: optional collection of logical token ids; only those rows are
+    filled (the rest stay zero), to regenerate a few rows of a large cache."""
     sh = wl.shape
     P = sh.page_size
     m = wl.slot_token_map()
+    if tokens is not None:
+        keep = np.isin(m, np.asarray(sorted(tokens), dtype=np.int64))
+        m[~keep] = -1
     nrows = wl.num_pages * P
     if sh.latent_fmt == LATENT_BF16:
         out = torch.zeros(nrows, sh.latent_dim, dtype=torch.bfloat16, device=device)

@@ -1,0 +1,91 @@
+"""Parity at the evaluation workloads' full sizes (decode 32 x 4K-16K, chunked
+prefill 8192 + 8192, long decode 128 x 64K-128K, mixed fp8 step), run in the
+launch configuration bench.py times.  The GPU processes the whole step; the
+oracle recomputes sampled rows one by one from host-regenerated inputs (the
+generator is a pure function of logical ids, so a row's host inputs equal its
+device inputs)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from deepseek_sparse_attention_dsa_gb300 import dsa
+from deepseek_sparse_attention_dsa_gb300 import workloads as W
+from tests import harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from deepseek_sparse_attention_dsa_gb300 import build
+    build.build()
+
+
+def _sample_rows(wl, n_decode, n_prefill, seed):
+    rng = np.random.default_rng(seed)
+    dec = [i for i, s in enumerate(wl.spans) if s.q_len == 1]
+    pre = [i for i, s in enumerate(wl.spans) if s.q_len > 1]
+    rows = [(int(i), 0) for i in rng.choice(dec, size=min(n_decode, len(dec)), replace=False)] if dec else []
+    for k in range(n_prefill if pre else 0):
+        i = pre[k % len(pre)]
+        q_len = wl.spans[i].q_len
+        rows.append((i, int([0, q_len - 1, rng.integers(0, q_len)][k % 3])))
+    return rows
+
+
+def _check_workload(idx, n_decode, n_prefill):
+    wl = W.config(idx)
+    sh = wl.shape
+    dev = torch.device("cuda", 0)
+    ic = W.make_index_cache(wl, device=dev)
+    lc = W.make_latent_cache(wl, device=dev)
+    st = W.make_step_inputs(wl, device=dev)
+    ctx = dsa.Context(sh, 0)
+    plan = ctx.plan(wl.spans, wl.num_pages)
+    # the bench's step: store -> score -> select -> attend
+    ctx.store_keys(plan, st.keys, ic)
+    scores = ctx.index_scores(plan, st.q, st.w, ic)
+    sel = ctx.topk_from_scores(plan, scores)
+    out = ctx.attend(plan, sel, st.q_nope, st.q_pe, lc, st.sink, sh.sm_scale)
+    # dsa_index_topk (scratch scores) gives the same selection
+    sel2 = ctx.index_topk(plan, st.q, st.w, ic)
+    ctx.get_error()
+    assert torch.equal(sel, sel2)
+    _, pos_all, tok_all = wl.row_table()
+    off_all = np.zeros(wl.num_rows + 1, np.int64)
+    np.cumsum(pos_all + 1, out=off_all[1:])
+    fp8 = sh.latent_fmt == W.LATENT_FP8_656
+    for span_i, r_in in _sample_rows(wl, n_decode, n_prefill, seed=idx):
+        row = wl.spans[span_i].q_start + r_in
+        rw = wl.row_workload(span_i, r_in)
+        ric = W.make_index_cache(rw)
+        rst = W.make_step_inputs(rw)
+        cache = oracle.store_keys(sh, rw.spans, rw.num_pages, rst.keys, ric)
+        sc, off = oracle.index_scores(sh, rw.spans, rw.num_pages, rst.q, rst.w, cache)
+        osel = oracle.topk(sh, rw.spans, sc, off)
+        g_sc = scores[off_all[row]:off_all[row + 1]].cpu().numpy()
+        H.check_scores(g_sc, sc, off)
+        g_sel = sel[row:row + 1].cpu().numpy()
+        H.check_selection(g_sel, osel, sc, off, sh.topk)
+        # attention over the GPU's own selection, recomputed by the oracle
+        toks = rw.spans[0].token_base + g_sel[0][g_sel[0] >= 0]
+        rlc = W.make_latent_cache(rw, tokens=set(toks.tolist()))
+        ref = oracle.attend(sh, rw.spans, rw.num_pages, g_sel, rst.q_nope, rst.q_pe, rlc, rst.sink)
+        H.check_attention(out[row:row + 1].float().cpu().numpy(), ref, fp8)
+
+
+def test_decode_full_size():
+    _check_workload(1, n_decode=3, n_prefill=0)
+
+
+def test_chunked_prefill_full_size():
+    _check_workload(2, n_decode=0, n_prefill=3)
+
+
+def test_long_decode_full_size():
+    _check_workload(3, n_decode=2, n_prefill=0)
+
+
+def test_mixed_fp8_full_size():
+    _check_workload(4, n_decode=2, n_prefill=3)

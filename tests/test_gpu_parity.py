@@ -160,8 +160,9 @@ def test_empty_step_and_launch_count():
     ctx.get_error()
 
 
-def test_generator_is_identical_on_gpu():
-    wl = H.deepseek_small(seed=10, fp8=True, sink=True, decode_ctx=(700,), chunk=(100, 5))
+@pytest.mark.parametrize("fp8", [False, True])
+def test_generator_is_identical_on_gpu(fp8):
+    wl = H.deepseek_small(seed=10, fp8=fp8, sink=True, decode_ctx=(700,), chunk=(100, 5))
     a = H.host_inputs(wl)
     b = H.device_inputs(wl)
     for x, y in zip(a[:2], b[:2]):
