@@ -130,6 +130,7 @@ const char *dsa_status_str(dsa_status s) {
     case DSA_ERR_BOUNDS: return "device bounds check failed (selection or page id out of range)";
     case DSA_ERR_TIMEOUT: return "device pipeline wait timed out";
     case DSA_ERR_UNSUPPORTED: return "unsupported shape or format";
+    case DSA_ERR_SCRATCH_LIMIT: return "plan needs more scores than the static score array holds (DSA_STATIC_SCORES_MAX)";
     default: return "unknown status";
   }
 }

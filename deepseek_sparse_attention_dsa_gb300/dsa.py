@@ -27,11 +27,12 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "l
 
 DSA_OK = 0
 STATUS_NAMES = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_SHORT_HISTORY", 3: "DSA_ERR_OOM",
-                4: "DSA_ERR_CUDA", 5: "DSA_ERR_BOUNDS", 6: "DSA_ERR_TIMEOUT", 7: "DSA_ERR_UNSUPPORTED"}
+                4: "DSA_ERR_CUDA", 5: "DSA_ERR_BOUNDS", 6: "DSA_ERR_TIMEOUT", 7: "DSA_ERR_UNSUPPORTED",
+                8: "DSA_ERR_SCRATCH_LIMIT"}
 
 EXPORTED = ["dsa_create", "dsa_destroy", "dsa_plan", "dsa_plan_destroy", "dsa_plan_get_info", "dsa_store_keys",
             "dsa_index_topk", "dsa_index_scores", "dsa_topk_from_scores", "dsa_attend", "dsa_get_error",
-            "dsa_last_launch_count", "dsa_status_str"]
+            "dsa_last_launch_count", "dsa_status_str", "dsa_index_topk_static"]
 
 
 class DSAError(RuntimeError):
@@ -85,6 +86,7 @@ def load() -> ctypes.CDLL:
     L.dsa_store_keys.argtypes = [vp, vp, vp, vp, vp]
     L.dsa_index_topk.argtypes = [vp, vp, vp, vp, vp, vp, vp]
     L.dsa_index_scores.argtypes = [vp, vp, vp, vp, vp, vp, vp]
+    L.dsa_index_topk_static.argtypes = [vp, vp, vp, vp, vp, vp, vp]
     L.dsa_topk_from_scores.argtypes = [vp, vp, vp, vp, vp]
     L.dsa_attend.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp]
     L.dsa_get_error.argtypes = [vp, vp]
@@ -92,7 +94,7 @@ def load() -> ctypes.CDLL:
     L.dsa_last_launch_count.restype = i32
     L.dsa_status_str.argtypes = [i32]
     L.dsa_status_str.restype = ctypes.c_char_p
-    for name in ("dsa_create", "dsa_plan", "dsa_plan_get_info", "dsa_store_keys", "dsa_index_topk",
+    for name in ("dsa_create", "dsa_plan", "dsa_plan_get_info", "dsa_store_keys", "dsa_index_topk", "dsa_index_topk_static",
                  "dsa_index_scores", "dsa_topk_from_scores", "dsa_attend", "dsa_get_error"):
         getattr(L, name).restype = i32
     _lib = L
@@ -222,6 +224,19 @@ class Context:
                                      _ptr(index_cache, d, (torch.bfloat16, torch.uint8), "index_cache"),
                                      _ptr(selection, d, (torch.int32,), "selection"), _stream(stream)),
                "dsa_index_topk")
+        return selection
+
+    def index_topk_static(self, plan: Plan, q, w, index_cache, selection=None, stream=None) -> torch.Tensor:
+        """dsa_index_topk_static: the same selection, with the scores kept in
+        the library's fixed device array (no allocation in the call)."""
+        d = self.device
+        if selection is None:
+            selection = torch.empty(plan.num_rows, self.shape.topk, dtype=torch.int32, device=d)
+        _check(load().dsa_index_topk_static(self.handle, plan.handle, _ptr(q, d, (torch.bfloat16,), "q"),
+                                            _ptr(w, d, (torch.float32,), "w"),
+                                            _ptr(index_cache, d, (torch.bfloat16, torch.uint8), "index_cache"),
+                                            _ptr(selection, d, (torch.int32,), "selection"), _stream(stream)),
+               "dsa_index_topk_static")
         return selection
 
     def index_scores(self, plan: Plan, q, w, index_cache, scores=None, stream=None) -> torch.Tensor:

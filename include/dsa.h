@@ -170,6 +170,24 @@ dsa_status dsa_attend(dsa_ctx_t *ctx, const dsa_plan_t *plan, const int32_t *sel
                       const void *q_pe, const void *latent_cache, const float *sink, float sm_scale, void *out,
                       dsa_stream_t stream);
 
+/* dsa_index_topk for callers that cannot allocate device memory at step time
+ * (a process that reserves HBM up front in its own pool and permits no driver
+ * allocation while serving).  The pages have no counterpart to this call.
+ * Same arguments, results and errors as dsa_index_topk, but the fp32 scores
+ * live in a fixed array inside the library (DSA_STATIC_SCORES_MAX floats,
+ * 16 MiB, present on every GPU that loads the library until the process
+ * exits) instead of the context's scratch; the call itself allocates nothing.
+ * A plan with more than DSA_STATIC_SCORES_MAX scores (the sum over rows of
+ * pos+1) is rejected with DSA_ERR_SCRATCH_LIMIT before anything runs.  The
+ * first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * All calls share the array: calls whose kernels overlap on the GPU race and
+ * must be serialised by the caller. */
+#define DSA_STATIC_SCORES_MAX (4 * 1024 * 1024)
+enum { DSA_ERR_SCRATCH_LIMIT = 8 };
+dsa_status dsa_index_topk_static(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *q, const float *w,
+                                 const void *index_cache, int32_t *selection, dsa_stream_t stream);
+
 /* Synchronise `stream`, read and clear the context's device error word.
  * Returns DSA_OK, DSA_ERR_BOUNDS, DSA_ERR_TIMEOUT or DSA_ERR_CUDA. */
 dsa_status dsa_get_error(dsa_ctx_t *ctx, dsa_stream_t stream);
