@@ -11,6 +11,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -60,6 +61,13 @@ struct Layout {
 };
 
 bool is_host_only(const dsa_ctx *ctx) { return ctx == nullptr || ctx->device < 0; }
+
+// DSA_OK, or DSA_ERR_CUDA with the CUDA error recorded in the context.
+dsa_status cuda_status(dsa_ctx *ctx, cudaError_t e) {
+  if (e == cudaSuccess) return DSA_OK;
+  snprintf(ctx->last_cuda_error, sizeof(ctx->last_cuda_error), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+  return DSA_ERR_CUDA;
+}
 
 dsa_status ensure_scratch(dsa_ctx *ctx, size_t scores, size_t slots) {
   if (scores > ctx->scores_cap) {
@@ -441,7 +449,7 @@ dsa_status dsa_store_keys(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *ke
   if (!keys || !index_cache) return DSA_ERR_INVALID_ARG;
   cudaError_t e = launch_store_keys(ctx, plan, keys, index_cache, reinterpret_cast<cudaStream_t>(stream),
                                     &ctx->last_launches);
-  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  return cuda_status(ctx, e);
 }
 
 dsa_status dsa_index_scores(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *q, const float *w,
@@ -453,7 +461,7 @@ dsa_status dsa_index_scores(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *
   if (!q || !w || !index_cache || !scores) return DSA_ERR_INVALID_ARG;
   cudaError_t e = launch_index_scores(ctx, plan, q, w, index_cache, scores, reinterpret_cast<cudaStream_t>(stream),
                                       &ctx->last_launches);
-  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  return cuda_status(ctx, e);
 }
 
 dsa_status dsa_topk_from_scores(dsa_ctx_t *ctx, const dsa_plan_t *plan, const float *scores, int32_t *selection,
@@ -465,7 +473,7 @@ dsa_status dsa_topk_from_scores(dsa_ctx_t *ctx, const dsa_plan_t *plan, const fl
   if (!scores || !selection) return DSA_ERR_INVALID_ARG;
   cudaError_t e = launch_topk(ctx, plan, scores, selection, reinterpret_cast<cudaStream_t>(stream),
                               &ctx->last_launches);
-  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  return cuda_status(ctx, e);
 }
 
 dsa_status dsa_index_topk(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *q, const float *w,
@@ -481,7 +489,7 @@ dsa_status dsa_index_topk(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *q,
   cudaError_t e = launch_index_scores(ctx, plan, q, w, index_cache, ctx->scores, s, &n);
   if (e == cudaSuccess) e = launch_topk(ctx, plan, ctx->scores, selection, s, &n);
   ctx->last_launches = n;
-  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  return cuda_status(ctx, e);
 }
 
 dsa_status dsa_attend(dsa_ctx_t *ctx, const dsa_plan_t *plan, const int32_t *selection, const void *q_nope,
@@ -495,7 +503,7 @@ dsa_status dsa_attend(dsa_ctx_t *ctx, const dsa_plan_t *plan, const int32_t *sel
   if (static_cast<size_t>(plan->n_slots) > ctx->part_cap) return DSA_ERR_INVALID_ARG;
   cudaError_t e = launch_attend(ctx, plan, selection, q_nope, q_pe, latent_cache, sink, sm_scale, out,
                                 reinterpret_cast<cudaStream_t>(stream), &ctx->last_launches);
-  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  return cuda_status(ctx, e);
 }
 
 dsa_status dsa_get_error(dsa_ctx_t *ctx, dsa_stream_t stream) {
@@ -512,5 +520,7 @@ dsa_status dsa_get_error(dsa_ctx_t *ctx, dsa_stream_t stream) {
 }
 
 int32_t dsa_last_launch_count(const dsa_ctx_t *ctx) { return ctx ? ctx->last_launches : 0; }
+
+const char *dsa_last_cuda_error(const dsa_ctx_t *ctx) { return ctx ? ctx->last_cuda_error : ""; }
 
 }  // extern "C"

@@ -7,21 +7,26 @@
 // is the leading kv_lora_rank columns of the same latent row, and an optional
 // per-head sink joins only the softmax denominator).
 //
-// Tensor-core kernel (bf16 latents, H <= 128, kv_lora_rank % 128 == 0,
-// rope 64): a cluster of two CTAs handles one (row, key range).  CTA c owns
-// latent columns [c*L/2, (c+1)*L/2) and half of the rope columns.  For a tile
-// of 64 selected keys both CTAs
-//   * gather their columns of the 64 latent rows through the page table
-//     (cp.async, 128-byte swizzled, two producer groups keep two tiles in flight),
+// Tensor-core kernel (bf16 latents, H <= 128, kv_lora_rank in {128, 256,
+// 512}, rope 64): a cluster of two CTAs handles one (row, key range).  CTA c
+// owns latent columns [c*L/2, (c+1)*L/2) and rope columns [32c, 32c+32).  At
+// the start of a unit the producers resolve every selected position of the
+// unit to its physical cache row (one table in shared memory).  Then, per tile
+// of 64 selected keys, both CTAs
+//   * gather their 576 bytes of each of the 64 latent rows (cp.async, 128- and
+//     64-byte swizzled tiles; completion signalled to an mbarrier, three
+//     tiles in flight),
 //   * compute partial logits S_c = Q[:, cols_c] . C[:, cols_c]^T on the tensor
 //     core (M = 128 heads, N = 64 keys, fp32 in TMEM),
 //   * swap the partials through distributed shared memory so both hold the
-//     same full S, run the same online softmax (lazy rescaling: the running
-//     max moves only when it grows by more than 2^8),
-//   * and accumulate O_c += P . C[:, L/2 half] (M = 128, N = L/2 <= 256, fp32 in TMEM).
-// So the MMA work is split, not duplicated, and each latent byte is read once.
-// Rows split over several key ranges write fp32 partials (O, max, sum) that
-// attend_combine_kernel merges.
+//     same full S and run the same online softmax (base 2, the reference max
+//     moves only when it grows by more than 2^8, so O is rarely rescaled),
+//   * write P as bf16 into tensor memory over the S tile it came from, and
+//   * accumulate O_c += P . C[:, cols_c] (A from TMEM, B = the gathered tile
+//     read MN-major; M = 128, N = L/2, fp32 in TMEM).
+// The MMA work is split between the pair, not duplicated, and each latent byte
+// is read once.  Rows split over several key ranges write fp32 partials (O,
+// max, sum) that attend_combine_kernel merges.
 //
 // Other shapes and the fp8 latent format run attend_simt_kernel.
 #include <cuda_fp8.h>
@@ -38,44 +43,52 @@ constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr float kNegBig = -1.0e30f;
 
 // warp roles
+// (8 warps: registers are handed out per group of four warps, so a ninth
+// warp would cost as much register file as twelve)
 constexpr int kMmaWarp = 0;
-constexpr int kProdWarp0 = 1;               // warps 1-4: two producer groups of 64 threads
-constexpr int kSoftWarp0 = 5;               // warps 5-8: softmax, thread = head
-constexpr int kAttThreads = 9 * 32;
+constexpr int kProdWarp0 = 1;               // warps 1-3: producers (96 threads)
+constexpr int kSoftWarp0 = 4;               // warps 4-7: softmax, thread = head
+constexpr int kProdThreads = 96;
+constexpr int kAttThreads = 8 * 32;
 
 template <int L>
 struct AttTraits {
-  static constexpr int HALF = L / 2;                     // PV columns per CTA
-  static constexpr int NPV = HALF / 64;                  // 64-column chunks per CTA
-  static constexpr int NCH = NPV + 1;                    // + the rope chunk
+  static constexpr int HALF = L / 2;                     // latent columns per CTA
+  static constexpr int NPV = HALF / 64;                  // 64-column (128-byte) chunks per CTA
   static constexpr int TILE = kAttTile;                  // keys per tile
-  static constexpr int CHUNK = TILE * 128;               // [64 keys x 64 cols] bf16, swizzled
-  static constexpr int STAGE = NCH * CHUNK;
-  static constexpr int STAGES = 2;
+  static constexpr int CHUNK = TILE * 128;               // [64 keys x 64 cols] bf16, 128-byte swizzle
+  static constexpr int RCHUNK = TILE * 64;               // [64 keys x 32 rope cols], 64-byte swizzle
+  static constexpr int STAGE = NPV * CHUNK + RCHUNK;
+  static constexpr int STAGES = 3;
+  static constexpr int PIECES = NPV * 8 + 4;             // 16-byte pieces per key per CTA
   static constexpr int QCHUNK = 128 * 128;               // [128 heads x 64 cols]
-  static constexpr int QBYTES = NCH * QCHUNK;
-  static constexpr int PBYTES = 128 * TILE * 2;          // P tile, bf16
+  static constexpr int QRCHUNK = 128 * 64;               // [128 heads x 32 rope cols]
+  static constexpr int QBYTES = NPV * QCHUNK + QRCHUNK;
   static constexpr int XBYTES = 128 * TILE * 4;          // partial-logit exchange, fp32
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + QBYTES;
-  static constexpr int OFF_P = OFF_K + STAGES * STAGE;
-  static constexpr int OFF_X = OFF_P + PBYTES;
-  static constexpr int OFF_ROWS = OFF_X + XBYTES;        // int64 [STAGES][TILE]
-  static constexpr int OFF_BAR = OFF_ROWS + STAGES * TILE * 8;
+  static constexpr int OFF_X = OFF_K + STAGES * STAGE;
+  static constexpr int OFF_ROWS = OFF_X + XBYTES;        // int32 [topk]: physical row of each entry
   static constexpr int NBAR = 16;
-  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM = OFF_MISC + 16 + 1024;
+  // the row table holds topk entries rounded up to whole tiles
+  __host__ __device__ static constexpr int rows_bytes(int topk) { return (topk + TILE - 1) / TILE * TILE * 4; }
   static constexpr uint32_t IDESC_QK = mma_idesc(128, TILE, 1u, false, false);
   static constexpr uint32_t IDESC_PV = mma_idesc(128, HALF, 1u, false, true);
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t S_COL = 0;                   // two S buffers: cols 0..127
+  static constexpr uint32_t S_COL = 0;                   // two S tiles: cols 0..63, 64..127 (P over their first 32)
   static constexpr uint32_t O_COL = 256;                 // O half: cols 256 .. 256+HALF-1
   static_assert(HALF % 64 == 0 && HALF <= 256, "latent width");
 };
 
+// Shared-memory bytes of the tensor-core kernel for a given topk.
+template <int L>
+constexpr int att_smem_bytes(int topk) {
+  return AttTraits<L>::OFF_ROWS + AttTraits<L>::rows_bytes(topk) + AttTraits<L>::NBAR * 8 + 16 + 1024;
+}
+
 struct AttParams {
-  CUtensorMap tm_qn;       // q_nope as [T*H, L] bf16, box {64, 128}
-  CUtensorMap tm_qp;       // q_pe as [T*H, R] bf16, box {64, 128}
+  CUtensorMap tm_qn;       // q_nope as [T*H, L] bf16, box {64, 128}, 128-byte swizzle
+  CUtensorMap tm_qp;       // q_pe as [T*H, R] bf16, box {32, 128}, 64-byte swizzle
   const int32_t *sel;
   const uint8_t *latent;   // [pages*P][L+R] bf16
   const float *sink;
@@ -120,17 +133,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t bar0 = sbase + C::OFF_BAR;
+  const int off_bar = C::OFF_ROWS + C::rows_bytes(p.K);
+  const uint32_t bar0 = sbase + off_bar;
   const uint32_t b_qfull = bar0 + 0;
   auto kfull = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto kempty = [&](int s) { return bar0 + 8u * (3 + s); };
-  auto sfull = [&](int b) { return bar0 + 8u * (5 + b); };
-  auto sempty = [&](int b) { return bar0 + 8u * (7 + b); };
-  const uint32_t b_pfull = bar0 + 8u * 9, b_pvdone = bar0 + 8u * 10;
-  const uint32_t b_xfull = bar0 + 8u * 11, b_xfree = bar0 + 8u * 12;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
-  int64_t *rows_sm = reinterpret_cast<int64_t *>(smem + C::OFF_ROWS);
+  auto kempty = [&](int s) { return bar0 + 8u * (4 + s); };
+  auto sfull = [&](int b) { return bar0 + 8u * (7 + b); };
+  auto sempty = [&](int b) { return bar0 + 8u * (9 + b); };
+  const uint32_t b_pfull = bar0 + 8u * 11, b_pvdone = bar0 + 8u * 12;
+  const uint32_t b_xfull = bar0 + 8u * 13, b_xfree = bar0 + 8u * 14;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + off_bar + C::NBAR * 8);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + off_bar + C::NBAR * 8 + 4);
+  int32_t *rows_sm = reinterpret_cast<int32_t *>(smem + C::OFF_ROWS);
 
   const int warp = threadIdx.x / 32, lane = lane_id();
   const uint32_t crank = cluster_rank();
@@ -138,22 +152,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
   const AttUnit unit = p.units[blockIdx.x >> 1];
   const int row = unit.row;
   const int pos = p.row_pos[row];
-  const int ntiles = (unit.k1 - unit.k0 + C::TILE - 1) / C::TILE;
+  const int nent = unit.k1 - unit.k0;
+  const int ntiles = (nent + C::TILE - 1) / C::TILE;
 
   if (threadIdx.x == 0) {
     mbar_init(b_qfull, 1);
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(kfull(s), 64);
+      mbar_init(kfull(s), kProdThreads);
       mbar_init(kempty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(sfull(b), 1);
-      mbar_init(sempty(b), 128);
+      mbar_init(sempty(b), 1);
     }
     mbar_init(b_pfull, 128);
     mbar_init(b_pvdone, 1);
-    mbar_init(b_xfull, 128);
-    mbar_init(b_xfree, 128);
+    mbar_init(b_xfull, 1);   // armed locally with the exchange bytes; filled by the partner's st.async
+    mbar_init(b_xfree, 4);   // one arrival per partner softmax warp once it has read its copy
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -173,18 +188,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
       for (int ch = 0; ch < C::NPV; ++ch)
         tma_load_2d(sbase + C::OFF_Q + ch * C::QCHUNK, &p.tm_qn, static_cast<int>(crank) * C::HALF + ch * 64,
                     row * p.H, b_qfull);
-      tma_load_2d(sbase + C::OFF_Q + C::NPV * C::QCHUNK, &p.tm_qp, 0, row * p.H, b_qfull);
+      tma_load_2d(sbase + C::OFF_Q + C::NPV * C::QCHUNK, &p.tm_qp, static_cast<int>(crank) * 32, row * p.H,
+                  b_qfull);
       bool ok = mbar_wait(b_qfull, 0, abort_flag, p.err);
       const uint32_t o_tmem = tmem_base + C::O_COL;
+      const uint32_t qst = sbase + C::OFF_Q;
       for (int t = 0; ok && t <= ntiles; ++t) {
         if (t < ntiles) {
-          const int st = t & 1;
-          if (!mbar_wait(kfull(st), (t >> 1) & 1, abort_flag, p.err)) break;
-          if (!mbar_wait(sempty(st), ((t >> 1) & 1) ^ 1, abort_flag, p.err)) break;
+          const int st = t % C::STAGES, sb = t & 1;
+          if (!mbar_wait(kfull(st), (t / C::STAGES) & 1, abort_flag, p.err)) break;
+          fence_proxy_async_smem();   // the gathered tile (generic-proxy writes) feeds the tensor core
+          if (!mbar_wait(sempty(sb), ((t >> 1) & 1) ^ 1, abort_flag, p.err)) break;
           tc_fence_after();
-          const uint32_t s_tmem = tmem_base + C::S_COL + st * C::TILE;
+          const uint32_t s_tmem = tmem_base + C::S_COL + sb * C::TILE;
           const uint32_t kst = sbase + C::OFF_K + st * C::STAGE;
-          const uint32_t qst = sbase + C::OFF_Q;
 #pragma unroll
           for (int ch = 0; ch < C::NPV; ++ch) {
 #pragma unroll
@@ -194,71 +211,99 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
               mma_f16_ss(s_tmem, ad, bd, C::IDESC_QK, (ch | k) ? 1u : 0u);
             }
           }
-          // this CTA's half of the rope columns: 16-column steps 2c and 2c+1
 #pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            const int kk = 2 * static_cast<int>(crank) + k;
-            const uint64_t ad = smem_desc(qst + C::NPV * C::QCHUNK + kk * 32, 16, 1024, kSwizzle128);
-            const uint64_t bd = smem_desc(kst + C::NPV * C::CHUNK + kk * 32, 16, 1024, kSwizzle128);
+          for (int k = 0; k < 2; ++k) {   // this CTA's 32 rope columns
+            const uint64_t ad = smem_desc(qst + C::NPV * C::QCHUNK + k * 32, 16, 512, kSwizzle64);
+            const uint64_t bd = smem_desc(kst + C::NPV * C::CHUNK + k * 32, 16, 512, kSwizzle64);
             mma_f16_ss(s_tmem, ad, bd, C::IDESC_QK, 1u);
           }
-          mma_commit(sfull(st));
+          mma_commit(sfull(sb));
         }
         if (t >= 1) {
           const int u = t - 1;
           if (!mbar_wait(b_pfull, u & 1, abort_flag, p.err)) break;
           tc_fence_after();
-          const uint32_t pst = sbase + C::OFF_P;
-          const uint32_t kst = sbase + C::OFF_K + (u & 1) * C::STAGE;
+          const uint32_t p_tmem = tmem_base + C::S_COL + (u & 1) * C::TILE;
+          const uint32_t kst = sbase + C::OFF_K + (u % C::STAGES) * C::STAGE;
 #pragma unroll
           for (int k = 0; k < C::TILE / 16; ++k) {
-            const uint64_t ad = smem_desc(pst + k * 32, 16, 1024, kSwizzle128);
             const uint64_t bd = smem_desc(kst + k * 16 * 128, C::CHUNK, 1024, kSwizzle128);
-            mma_f16_ss(o_tmem, ad, bd, C::IDESC_PV, (u > 0 || k > 0) ? 1u : 0u);
+            mma_f16_ts(o_tmem, p_tmem + k * 8, bd, C::IDESC_PV, (u > 0 || k > 0) ? 1u : 0u);
           }
           mma_commit(b_pvdone);
-          mma_commit(kempty(u & 1));
+          mma_commit(kempty(u % C::STAGES));
+          mma_commit(sempty(u & 1));
         }
       }
     }
     __syncwarp();
   } else if (warp < kSoftWarp0) {
     // ------------------------------------------------------------ producers
-    const int grp = (warp - kProdWarp0) >> 1;           // 0: even tiles, 1: odd tiles
-    const int gt = (warp - kProdWarp0) * 32 % 64 + lane;  // 0..63 within the group
-    const int page_off = p.row_page_off[row], npages = p.row_npages[row], page_start = p.row_page_start[row];
-    const int32_t *selrow = p.sel + static_cast<int64_t>(row) * p.K;
-    const int col0 = static_cast<int>(crank) * C::HALF;
-    for (int t = grp; t < ntiles; t += 2) {
-      const int st = t & 1;  // == grp
-      if (!mbar_wait(kempty(st), ((t >> 1) & 1) ^ 1, abort_flag, p.err)) break;
-      {
-        const int e = unit.k0 + t * C::TILE + gt;
-        const int j = e < unit.k1 ? selrow[e] : -1;
-        rows_sm[st * C::TILE + gt] =
-            latent_row(j, pos, page_off, npages, page_start, p.pages, p.P, p.num_pages, p.err);
-      }
-      named_bar_sync(2 + grp, 64);
-      const uint32_t kst = sbase + C::OFF_K + st * C::STAGE;
-      for (int idx = gt; idx < C::TILE * C::NCH * 8; idx += 64) {
-        const int key = idx / (C::NCH * 8);
-        const int rem = idx - key * (C::NCH * 8);
-        const int ch = rem >> 3, piece = rem & 7;
-        const uint32_t dst = kst + ch * C::CHUNK + sw128_offset(key, piece);
-        const int64_t prow = rows_sm[st * C::TILE + key];
-        if (prow >= 0) {
-          const int col = (ch < C::NPV ? col0 + ch * 64 : L) + piece * 8;
-          cp_async_16(dst, p.latent + prow * ROWB + col * 2);
-        } else {
-          st_shared_zero16(dst);
+    const int pt = threadIdx.x - 32 * kProdWarp0;  // 0..95
+    {
+      const int page_off = p.row_page_off[row], npages = p.row_npages[row], page_start = p.row_page_start[row];
+      const int32_t *selrow = p.sel + static_cast<int64_t>(row) * p.K + unit.k0;
+      // eight entries per thread at a time: all selection loads, then all
+      // page-table loads, are in flight together
+      constexpr int kB = 8;
+      for (int base = 0; base < ntiles * C::TILE; base += kProdThreads * kB) {
+        int j[kB];
+#pragma unroll
+        for (int u = 0; u < kB; ++u) {
+          const int e = base + u * kProdThreads + pt;
+          j[u] = e < nent ? selrow[e] : -1;
+        }
+        int pg[kB];
+#pragma unroll
+        for (int u = 0; u < kB; ++u) {
+          pg[u] = -1;
+          if (j[u] >= 0 && j[u] <= pos) {
+            const int64_t pi = (static_cast<int64_t>(page_start) + j[u]) / p.P;
+            if (pi < npages) pg[u] = p.pages[page_off + pi];
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kB; ++u) {
+          const int e = base + u * kProdThreads + pt;
+          if (e >= ntiles * C::TILE) continue;
+          int32_t r = -1;
+          if (j[u] < -1 || j[u] > pos) {
+            atomicOr(p.err, kErrBounds);            // a position this row cannot see
+          } else if (j[u] >= 0) {
+            const int64_t slot = static_cast<int64_t>(page_start) + j[u];
+            if (pg[u] < 0 || pg[u] >= p.num_pages || slot / p.P >= npages) atomicOr(p.err, kErrBounds);
+            else r = static_cast<int32_t>(static_cast<int64_t>(pg[u]) * p.P + slot % p.P);
+          }
+          rows_sm[e] = r;
         }
       }
-      cp_async_commit();
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      mbar_arrive(kfull(st));
-      named_bar_sync(2 + grp, 64);  // the row table of this stage may be rewritten next round
     }
+    named_bar_sync(1, kProdThreads + 128);   // the row table is complete (producers + softmax)
+    const int col0 = static_cast<int>(crank) * C::HALF;
+    const int rcol0 = L + static_cast<int>(crank) * 32;
+    for (int t = 0; t < ntiles; ++t) {
+      const int st = t % C::STAGES;
+      if (!mbar_wait(kempty(st), ((t / C::STAGES) & 1) ^ 1, abort_flag, p.err)) break;
+      const uint32_t kst = sbase + C::OFF_K + st * C::STAGE;
+      for (int idx = pt; idx < C::TILE * C::PIECES; idx += kProdThreads) {
+        const int key = idx / C::PIECES;
+        const int piece = idx - key * C::PIECES;
+        const int32_t prow = rows_sm[t * C::TILE + key];
+        uint32_t dst;
+        int col;
+        if (piece < C::NPV * 8) {
+          dst = kst + (piece >> 3) * C::CHUNK + sw128_offset(key, piece & 7);
+          col = col0 + piece * 8;
+        } else {
+          dst = kst + C::NPV * C::CHUNK + sw64_offset(key, piece - C::NPV * 8);
+          col = rcol0 + (piece - C::NPV * 8) * 8;
+        }
+        const uint8_t *src = p.latent + (prow >= 0 ? static_cast<int64_t>(prow) * ROWB + col * 2 : 0);
+        cp_async_16_zfill(dst, src, prow >= 0 ? 16u : 0u);
+      }
+      cp_async_mbar_arrive(kfull(st));
+    }
+    cp_async_wait<0>();   // nothing in flight when the CTA leaves
   } else {
     // ------------------------------------------------------------ softmax
     const int quad = warp & 3;
@@ -267,41 +312,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
     const uint32_t x_own = sbase + C::OFF_X + h * 256;
     const uint32_t x_peer = map_to_cta(x_own, peer);
     const uint32_t peer_xfull = map_to_cta(b_xfull, peer), peer_xfree = map_to_cta(b_xfree, peer);
-    const uint32_t p_row = sbase + C::OFF_P + h * 128;   // P row h (swizzled within 1024-byte atoms)
-    const int32_t *selrow = p.sel + static_cast<int64_t>(row) * p.K;
     float m_ref = kNegBig, l = 0.f;
-    int jA = -1, jB = -1;
-    {
-      const int e = unit.k0 + lane;
-      jA = e < unit.k1 ? selrow[e] : -1;
-      jB = e + 32 < unit.k1 ? selrow[e + 32] : -1;
-    }
+    named_bar_sync(1, kProdThreads + 128);   // the row table is complete
     bool ok = true;
-    for (int t = 0; t < ntiles && ok; ++t) {
-      const uint32_t vlo = __ballot_sync(0xffffffffu, jA >= 0 && jA <= pos);
-      const uint32_t vhi = __ballot_sync(0xffffffffu, jB >= 0 && jB <= pos);
-      if (t + 1 < ntiles) {
-        const int e = unit.k0 + (t + 1) * C::TILE + lane;
-        jA = e < unit.k1 ? selrow[e] : -1;
-        jB = e + 32 < unit.k1 ? selrow[e + 32] : -1;
-      }
-      const int sb = t & 1;
-      if (!mbar_wait(sfull(sb), (t >> 1) & 1, abort_flag, p.err)) { ok = false; break; }
+    // The partial logits of tile t+1 are sent to the partner before the softmax
+    // of tile t runs, so the transfer overlaps the math.  The partner reads its
+    // copy of tile t before this CTA sends tile t+1 into the same buffer
+    // (xfree), which both CTAs reach without waiting on each other.
+    float s[C::TILE];
+    auto load_s = [&](int t, float (&dst)[C::TILE]) -> bool {
+      if (!mbar_wait(sfull(t & 1), (t >> 1) & 1, abort_flag, p.err)) return false;
       tc_fence_after();
-      float s[C::TILE];
 #pragma unroll
       for (int c0 = 0; c0 < C::TILE; c0 += 16)
-        tmem_ld16(tmem_base + lane_base + C::S_COL + sb * C::TILE + c0, *reinterpret_cast<float(*)[16]>(s + c0));
+        tmem_ld16(tmem_base + lane_base + C::S_COL + (t & 1) * C::TILE + c0,
+                  *reinterpret_cast<float(*)[16]>(dst + c0));
       tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(sempty(sb));
-
-      // swap partial logits with the other CTA of the pair
-      if (!mbar_wait<true>(b_xfree, (t & 1) ^ 1, abort_flag, p.err)) { ok = false; break; }
+      return true;
+    };
+    auto send_s = [&](const float (&src)[C::TILE]) {
 #pragma unroll
       for (int c = 0; c < 16; ++c)
-        st_cluster_v4(x_peer + ((c ^ (h & 15)) << 4), s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]);
-      mbar_arrive_remote(peer_xfull);
+        st_async_v4(x_peer + ((c ^ (h & 15)) << 4), src[4 * c], src[4 * c + 1], src[4 * c + 2], src[4 * c + 3],
+                    peer_xfull);
+    };
+    if (ntiles > 0) {
+      ok = load_s(0, s);
+      if (ok) send_s(s);
+    }
+    for (int t = 0; t < ntiles && ok; ++t) {
+      const uint32_t vlo = __ballot_sync(0xffffffffu, rows_sm[t * C::TILE + lane] >= 0);
+      const uint32_t vhi = __ballot_sync(0xffffffffu, rows_sm[t * C::TILE + 32 + lane] >= 0);
+      const int sb = t & 1;
+
+      // 1. the partner's partial logits of tile t (asynchronous remote stores
+      //    that land on this CTA's mbarrier as transaction bytes)
+      if (h == 0) mbar_arrive_expect_tx(b_xfull, C::XBYTES);
       if (!mbar_wait<true>(b_xfull, t & 1, abort_flag, p.err)) { ok = false; break; }
       const float4 *xr = reinterpret_cast<const float4 *>(smem + C::OFF_X + h * 256);
 #pragma unroll
@@ -312,7 +358,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
         s[4 * c + 2] += v.z;
         s[4 * c + 3] += v.w;
       }
-      mbar_arrive_remote(peer_xfree);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(peer_xfree);
+
+      // 2. this CTA's partial logits of tile t+1 go out now
+      float s_next[C::TILE];
+      if (t + 1 < ntiles) {
+        if (!load_s(t + 1, s_next)) { ok = false; break; }
+        if (!mbar_wait<true>(b_xfree, t & 1, abort_flag, p.err)) { ok = false; break; }
+        send_s(s_next);
+      }
 
       // online softmax in base 2 with a lazily moved reference max
       float tmax = -INFINITY;
@@ -339,33 +394,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
       }
       l = l * alpha + sum;
 
-      // O and the P buffer are free once the previous PV finished
-      if (t > 0) {
+      // O must hold every earlier tile before it is rescaled
+      if (rescale && t > 0) {
         if (!mbar_wait(b_pvdone, (t - 1) & 1, abort_flag, p.err)) { ok = false; break; }
         tc_fence_after();
-        if (rescale) {
 #pragma unroll 1
-          for (int c0 = 0; c0 < C::HALF; c0 += 16) {
-            float o[16];
-            tmem_ld16(tmem_base + lane_base + C::O_COL + c0, o);
-            tmem_ld_wait();
+        for (int c0 = 0; c0 < C::HALF; c0 += 16) {
+          float o[16];
+          tmem_ld16(tmem_base + lane_base + C::O_COL + c0, o);
+          tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) o[i] *= alpha;
-            tmem_st16(tmem_base + lane_base + C::O_COL + c0, o);
-          }
-          tmem_st_wait();
+          for (int i = 0; i < 16; ++i) o[i] *= alpha;
+          tmem_st16(tmem_base + lane_base + C::O_COL + c0, o);
         }
       }
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint32_t addr = p_row + ((static_cast<uint32_t>(c) ^ (h & 7u)) << 4);
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(packed[4 * c]),
-                     "r"(packed[4 * c + 1]), "r"(packed[4 * c + 2]), "r"(packed[4 * c + 3])
-                     : "memory");
-      }
-      fence_proxy_async_smem();
+      // P (bf16 pairs, lower key in the low half) over the first 32 columns of this S tile
+      tmem_st32(tmem_base + lane_base + C::S_COL + sb * C::TILE, packed);
+      tmem_st_wait();
       tc_fence_before();
       mbar_arrive(b_pfull);
+#pragma unroll
+      for (int i = 0; i < C::TILE; ++i) s[i] = s_next[i];
     }
     if (ok && ntiles > 0) ok = mbar_wait(b_pvdone, (ntiles - 1) & 1, abort_flag, p.err);
     tc_fence_after();
@@ -544,14 +593,13 @@ template <int L>
 cudaError_t run_tc(const dsa_ctx *ctx, const dsa_plan_t *plan, const int32_t *sel, const void *q_nope,
                    const void *q_pe, const void *latent, const float *sink, float sm_scale, void *out,
                    cudaStream_t s) {
-  using Cfg = AttTraits<L>;
   const dsa_config_t &c = ctx->cfg;
   AttParams prm{};
   if (!encode_tiled_2d(&prm.tm_qn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void *>(q_nope), L,
                        static_cast<uint64_t>(plan->T) * c.heads, L * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   if (!encode_tiled_2d(&prm.tm_qp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void *>(q_pe), 64,
-                       static_cast<uint64_t>(plan->T) * c.heads, 64 * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+                       static_cast<uint64_t>(plan->T) * c.heads, 64 * 2, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   prm.sel = sel;
   prm.latent = static_cast<const uint8_t *>(latent);
@@ -571,22 +619,21 @@ cudaError_t run_tc(const dsa_ctx *ctx, const dsa_plan_t *plan, const int32_t *se
   prm.P = c.page_size;
   prm.num_pages = plan->cache_pages;
   prm.scale_log2 = sm_scale * kLog2e;
+  const int smem = att_smem_bytes<L>(c.topk);
   auto kern = attend_tc_kernel<L>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  kern<<<2 * plan->n_units, kAttThreads, Cfg::SMEM, s>>>(prm);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<2 * plan->n_units, kAttThreads, smem, s>>>(prm);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 bool attend_tc_supported(const dsa_config_t &c) {
-  return c.latent_fmt == DSA_LATENT_BF16 && c.heads <= 128 && c.rope_dim == 64 &&
-         (c.kv_lora_rank == 512 || c.kv_lora_rank == 256 || c.kv_lora_rank == 128);
+  if (c.latent_fmt != DSA_LATENT_BF16 || c.heads > 128 || c.rope_dim != 64) return false;
+  if (c.kv_lora_rank != 512 && c.kv_lora_rank != 256 && c.kv_lora_rank != 128) return false;
+  // the per-unit row table (topk int32) must fit beside the tiles
+  return att_smem_bytes<512>(c.topk) <= 227 * 1024;
 }
 
 cudaError_t launch_attend(const dsa_ctx *ctx, const dsa_plan_t *plan, const int32_t *sel, const void *q_nope,

@@ -78,6 +78,7 @@ struct dsa_ctx {
   float *mlpart = nullptr;        // attention partial (m, l) [slots][H][2]
   size_t part_cap = 0;            // slots
   int32_t last_launches = 0;
+  char last_cuda_error[160] = {0};  // name and text of the last CUDA error a call returned DSA_ERR_CUDA for
 };
 
 struct dsa_plan {

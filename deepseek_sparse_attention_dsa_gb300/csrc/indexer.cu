@@ -152,19 +152,29 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_tc_kernel(const __grid_c
         if (__shfl_sync(0xffffffffu, qok ? 1 : 0, 0) == 0) break;
       }
       const int nkeys_total = g.pos0 + g.nrows;  // keys 0 .. pos0+nrows-1
-      for (int t = item.tile0; t < item.tile1; ++t) {
-        const int nkeys = min(128, nkeys_total - t * 128);
-        const int nbox = (nkeys + p.BH - 1) / p.BH;
-        int myrow = -1;
-        if (lane < nbox) {
+      // physical cache row of this lane's box of tile t (lane < boxes of t), or -1
+      auto box_row = [&](int t) -> int {
+        const int nb = (min(128, nkeys_total - t * 128) + p.BH - 1) / p.BH;
+        int r = -1;
+        if (lane < nb) {
           const int64_t slot = static_cast<int64_t>(g.page_start) + t * 128 + lane * p.BH;
           const int64_t pi = slot / p.P;
           if (pi < g.npages) {
             const int page = p.pages[g.page_off + pi];
-            if (page >= 0 && page < p.num_pages) myrow = page * p.P + static_cast<int>(slot % p.P);
+            if (page >= 0 && page < p.num_pages) r = page * p.P + static_cast<int>(slot % p.P);
           }
-          if (myrow < 0) atomicOr(p.err, kErrBounds);
+          if (r < 0) atomicOr(p.err, kErrBounds);
         }
+        return r;
+      };
+      // the page-table lookups of tile t+1 are issued before tile t waits for
+      // its stage, so their latency hides behind the pipeline
+      int next_row = box_row(item.tile0);
+      for (int t = item.tile0; t < item.tile1; ++t) {
+        const int nkeys = min(128, nkeys_total - t * 128);
+        const int nbox = (nkeys + p.BH - 1) / p.BH;
+        const int myrow = next_row;
+        if (t + 1 < item.tile1) next_row = box_row(t + 1);
         const uint32_t valid = __ballot_sync(0xffffffffu, myrow >= 0);
         bool ok = true;
         if (lane == 0) ok = mbar_wait(kempty(stage), kphase ^ 1, abort_flag, p.err);

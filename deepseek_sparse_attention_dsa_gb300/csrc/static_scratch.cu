@@ -19,6 +19,7 @@
 // the array and must be serialised by the caller.
 #include <cuda_runtime.h>
 
+#include <cstdio>
 #include <mutex>
 
 #include "dsa_internal.h"
@@ -64,5 +65,9 @@ extern "C" dsa_status dsa_index_topk_static(dsa_ctx_t *ctx, const dsa_plan_t *pl
   cudaError_t e = dsa::launch_index_scores(ctx, plan, q, w, index_cache, scores, s, &n);
   if (e == cudaSuccess) e = dsa::launch_topk(ctx, plan, scores, selection, s, &n);
   ctx->last_launches = n;
-  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  if (e != cudaSuccess) {
+    snprintf(ctx->last_cuda_error, sizeof(ctx->last_cuda_error), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+    return DSA_ERR_CUDA;
+  }
+  return DSA_OK;
 }

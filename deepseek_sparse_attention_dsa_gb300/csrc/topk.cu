@@ -22,6 +22,7 @@ namespace {
 
 constexpr int kTopkThreads = 1024;
 constexpr int kTopkWarps = kTopkThreads / 32;
+constexpr int kBatch = 8;   // independent loads in flight per thread
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t u = __float_as_uint(f);
@@ -96,7 +97,9 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const float *__re
   const float *s = scores + row_score_off[row];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
-  // ---- radix select of the k-th largest key
+  // ---- radix select of the k-th largest key.  Every loop below issues
+  // kBatch independent loads per thread before using any of them, so each
+  // pass is bound by L2 bandwidth rather than by one load's latency.
   uint32_t prefix = 0, pmask = 0;
   int need = K;
 #pragma unroll 1
@@ -105,18 +108,24 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const float *__re
     const int nbins = pass == 2 ? 1024 : 2048;
     for (int i = threadIdx.x; i < 2048; i += kTopkThreads) hist[i] = 0;
     __syncthreads();
-    if (pass == 0) {
-      for (int base = 0; base < n; base += kTopkThreads) {
-        const int i = base + threadIdx.x;
-        const bool in = i < n;
-        const int bin = in ? static_cast<int>(order_key(s[i]) >> 21) : -1;
-        const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-        if (in && (__ffs(peers) - 1) == lane) atomicAdd(&hist[bin], __popc(peers));
+    for (int base = 0; base < n; base += kTopkThreads * kBatch) {
+      uint32_t k[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int i = base + j * kTopkThreads + static_cast<int>(threadIdx.x);
+        k[j] = i < n ? order_key(__ldg(s + i)) : 0u;
       }
-    } else {
-      for (int i = threadIdx.x; i < n; i += kTopkThreads) {
-        const uint32_t k = order_key(s[i]);
-        if ((k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & (nbins - 1)], 1);
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const bool in = base + j * kTopkThreads + static_cast<int>(threadIdx.x) < n;
+        if (pass == 0) {
+          // equal bins of a warp are counted by one atomic
+          const int bin = in ? static_cast<int>(k[j] >> 21) : -1;
+          const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+          if (in && (__ffs(peers) - 1) == lane) atomicAdd(&hist[bin], __popc(peers));
+        } else if (in && (k[j] & pmask) == prefix) {
+          atomicAdd(&hist[(k[j] >> shift) & (nbins - 1)], 1);
+        }
       }
     }
     __syncthreads();
@@ -130,14 +139,22 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const float *__re
   // `need` = how many scores equal to tau are taken (the earliest ones)
 
   // ---- ordered compaction, one contiguous segment per warp
-  const int seg = ((n + kTopkWarps - 1) / kTopkWarps + 31) / 32 * 32;
+  const int seg = ((n + kTopkWarps - 1) / kTopkWarps + 32 * kBatch - 1) / (32 * kBatch) * (32 * kBatch);
   const int lo = warp * seg, hi = min(n, lo + seg);
   int cgt = 0, ceq = 0;
-  for (int base = lo; base < hi; base += 32) {
-    const int i = base + lane;
-    const uint32_t k = i < hi ? order_key(s[i]) : 0u;
-    cgt += __popc(__ballot_sync(0xffffffffu, i < hi && k > tau));
-    ceq += __popc(__ballot_sync(0xffffffffu, i < hi && k == tau));
+  for (int base = lo; base < hi; base += 32 * kBatch) {
+    uint32_t k[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int i = base + 32 * j + lane;
+      k[j] = i < hi ? order_key(__ldg(s + i)) : 0u;
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const bool in = base + 32 * j + lane < hi;
+      cgt += __popc(__ballot_sync(0xffffffffu, in && k[j] > tau));
+      ceq += __popc(__ballot_sync(0xffffffffu, in && k[j] == tau));
+    }
   }
   if (lane == 0) {
     wgt[warp] = cgt;
@@ -151,18 +168,26 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const float *__re
     eq_base += weq[w];
   }
   const uint32_t lt_mask = (1u << lane) - 1u;
-  for (int base = lo; base < hi; base += 32) {
-    const int i = base + lane;
-    const uint32_t k = i < hi ? order_key(s[i]) : 0u;
-    const bool gt = i < hi && k > tau;
-    const bool eq = i < hi && k == tau;
-    const uint32_t eqm = __ballot_sync(0xffffffffu, eq);
-    const bool take = gt || (eq && eq_base + __popc(eqm & lt_mask) < need);
-    const uint32_t tm = __ballot_sync(0xffffffffu, take);
-    const int slot = out_base + __popc(tm & lt_mask);
-    if (take && slot < K) out[slot] = i;
-    out_base += __popc(tm);
-    eq_base += __popc(eqm);
+  for (int base = lo; base < hi; base += 32 * kBatch) {
+    uint32_t k[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int i = base + 32 * j + lane;
+      k[j] = i < hi ? order_key(__ldg(s + i)) : 0u;
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int i = base + 32 * j + lane;
+      const bool gt = i < hi && k[j] > tau;
+      const bool eq = i < hi && k[j] == tau;
+      const uint32_t eqm = __ballot_sync(0xffffffffu, eq);
+      const bool take = gt || (eq && eq_base + __popc(eqm & lt_mask) < need);
+      const uint32_t tm = __ballot_sync(0xffffffffu, take);
+      const int slot = out_base + __popc(tm & lt_mask);
+      if (take && slot < K) out[slot] = i;
+      out_base += __popc(tm);
+      eq_base += __popc(eqm);
+    }
   }
 }
 

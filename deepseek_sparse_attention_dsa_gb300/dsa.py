@@ -32,13 +32,14 @@ STATUS_NAMES = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_SHORT_HISTORY
 
 EXPORTED = ["dsa_create", "dsa_destroy", "dsa_plan", "dsa_plan_destroy", "dsa_plan_get_info", "dsa_store_keys",
             "dsa_index_topk", "dsa_index_scores", "dsa_topk_from_scores", "dsa_attend", "dsa_get_error",
-            "dsa_last_launch_count", "dsa_status_str", "dsa_index_topk_static"]
+            "dsa_last_launch_count", "dsa_status_str", "dsa_index_topk_static", "dsa_last_cuda_error"]
 
 
 class DSAError(RuntimeError):
-    def __init__(self, status: int, what: str):
+    def __init__(self, status: int, what: str, detail: str = ""):
         self.status = status
-        super().__init__("%s: %s (%s)" % (what, STATUS_NAMES.get(status, str(status)), _status_str(status)))
+        super().__init__("%s: %s (%s)%s" % (what, STATUS_NAMES.get(status, str(status)), _status_str(status),
+                                           (" [" + detail + "]") if detail else ""))
 
 
 class _Config(ctypes.Structure):
@@ -92,6 +93,8 @@ def load() -> ctypes.CDLL:
     L.dsa_get_error.argtypes = [vp, vp]
     L.dsa_last_launch_count.argtypes = [vp]
     L.dsa_last_launch_count.restype = i32
+    L.dsa_last_cuda_error.argtypes = [vp]
+    L.dsa_last_cuda_error.restype = ctypes.c_char_p
     L.dsa_status_str.argtypes = [i32]
     L.dsa_status_str.restype = ctypes.c_char_p
     for name in ("dsa_create", "dsa_plan", "dsa_plan_get_info", "dsa_store_keys", "dsa_index_topk", "dsa_index_topk_static",
@@ -108,9 +111,15 @@ def _status_str(s: int) -> str:
         return "?"
 
 
-def _check(status: int, what: str):
+def _check(status: int, what: str, ctx_handle=None):
     if status != DSA_OK:
-        raise DSAError(status, what)
+        detail = ""
+        if ctx_handle is not None and status == 4:
+            try:
+                detail = load().dsa_last_cuda_error(ctx_handle).decode()
+            except Exception:
+                detail = ""
+        raise DSAError(status, what, detail)
 
 
 def _ptr(t: Optional[torch.Tensor], device: torch.device, dtypes, name: str):
@@ -213,7 +222,7 @@ class Context:
         d = self.device
         _check(load().dsa_store_keys(self.handle, plan.handle, _ptr(keys, d, (torch.bfloat16, torch.uint8), "keys"),
                                      _ptr(index_cache, d, (torch.bfloat16, torch.uint8), "index_cache"),
-                                     _stream(stream)), "dsa_store_keys")
+                                     _stream(stream)), "dsa_store_keys", self.handle)
 
     def index_topk(self, plan: Plan, q, w, index_cache, selection=None, stream=None) -> torch.Tensor:
         d = self.device
@@ -223,7 +232,7 @@ class Context:
                                      _ptr(w, d, (torch.float32,), "w"),
                                      _ptr(index_cache, d, (torch.bfloat16, torch.uint8), "index_cache"),
                                      _ptr(selection, d, (torch.int32,), "selection"), _stream(stream)),
-               "dsa_index_topk")
+               "dsa_index_topk", self.handle)
         return selection
 
     def index_topk_static(self, plan: Plan, q, w, index_cache, selection=None, stream=None) -> torch.Tensor:
@@ -236,7 +245,7 @@ class Context:
                                             _ptr(w, d, (torch.float32,), "w"),
                                             _ptr(index_cache, d, (torch.bfloat16, torch.uint8), "index_cache"),
                                             _ptr(selection, d, (torch.int32,), "selection"), _stream(stream)),
-               "dsa_index_topk_static")
+               "dsa_index_topk_static", self.handle)
         return selection
 
     def index_scores(self, plan: Plan, q, w, index_cache, scores=None, stream=None) -> torch.Tensor:
@@ -247,7 +256,7 @@ class Context:
                                        _ptr(w, d, (torch.float32,), "w"),
                                        _ptr(index_cache, d, (torch.bfloat16, torch.uint8), "index_cache"),
                                        _ptr(scores, d, (torch.float32,), "scores"), _stream(stream)),
-               "dsa_index_scores")
+               "dsa_index_scores", self.handle)
         return scores
 
     def topk_from_scores(self, plan: Plan, scores, selection=None, stream=None) -> torch.Tensor:
@@ -256,7 +265,7 @@ class Context:
             selection = torch.empty(plan.num_rows, self.shape.topk, dtype=torch.int32, device=d)
         _check(load().dsa_topk_from_scores(self.handle, plan.handle, _ptr(scores, d, (torch.float32,), "scores"),
                                            _ptr(selection, d, (torch.int32,), "selection"), _stream(stream)),
-               "dsa_topk_from_scores")
+               "dsa_topk_from_scores", self.handle)
         return selection
 
     def attend(self, plan: Plan, selection, q_nope, q_pe, latent_cache, sink=None, sm_scale=None, out=None,
@@ -271,11 +280,11 @@ class Context:
                                  _ptr(q_nope, d, (torch.bfloat16,), "q_nope"), _ptr(q_pe, d, (torch.bfloat16,), "q_pe"),
                                  _ptr(latent_cache, d, (torch.bfloat16, torch.uint8), "latent_cache"),
                                  _ptr(sink, d, (torch.float32,), "sink"), float(sm_scale),
-                                 _ptr(out, d, (torch.bfloat16,), "out"), _stream(stream)), "dsa_attend")
+                                 _ptr(out, d, (torch.bfloat16,), "out"), _stream(stream)), "dsa_attend", self.handle)
         return out
 
     def get_error(self, stream=None):
-        _check(load().dsa_get_error(self.handle, _stream(stream)), "dsa_get_error")
+        _check(load().dsa_get_error(self.handle, _stream(stream)), "dsa_get_error", self.handle)
 
     def last_launch_count(self) -> int:
         return int(load().dsa_last_launch_count(self.handle))

@@ -198,6 +198,10 @@ int32_t dsa_last_launch_count(const dsa_ctx_t *ctx);
 
 const char *dsa_status_str(dsa_status s);
 
+/* Name and text of the CUDA error behind the context's last DSA_ERR_CUDA
+ * ("" when there was none); owned by the context. */
+const char *dsa_last_cuda_error(const dsa_ctx_t *ctx);
+
 #ifdef __cplusplus
 }
 #endif
