@@ -8,25 +8,25 @@
 // per-head sink joins only the softmax denominator).
 //
 // Tensor-core kernel (bf16 latents, H <= 128, kv_lora_rank in {128, 256,
-// 512}, rope 64): a cluster of two CTAs handles one (row, key range).  CTA c
-// owns latent columns [c*L/2, (c+1)*L/2) and rope columns [32c, 32c+32).  At
-// the start of a unit the producers resolve every selected position of the
-// unit to its physical cache row (one table in shared memory).  Then, per tile
-// of 64 selected keys, both CTAs
-//   * gather their 576 bytes of each of the 64 latent rows (cp.async, 128- and
-//     64-byte swizzled tiles; completion signalled to an mbarrier, three
-//     tiles in flight),
-//   * compute partial logits S_c = Q[:, cols_c] . C[:, cols_c]^T on the tensor
-//     core (M = 128 heads, N = 64 keys, fp32 in TMEM),
-//   * swap the partials through distributed shared memory so both hold the
-//     same full S and run the same online softmax (base 2, the reference max
-//     moves only when it grows by more than 2^8, so O is rarely rescaled),
-//   * write P as bf16 into tensor memory over the S tile it came from, and
-//   * accumulate O_c += P . C[:, cols_c] (A from TMEM, B = the gathered tile
-//     read MN-major; M = 128, N = L/2, fp32 in TMEM).
-// The MMA work is split between the pair, not duplicated, and each latent byte
-// is read once.  Rows split over several key ranges write fp32 partials (O,
-// max, sum) that attend_combine_kernel merges.
+// 512}, rope 64).  One CTA per (row, key range, output half c): it computes
+// the full logits of all 128 heads and accumulates O for latent columns
+// [c*L/2, (c+1)*L/2), so the two halves of a row share nothing but their
+// inputs (the QK contraction is done by both; in exchange no CTA ever waits on
+// another).  Per tile of 64 selected keys:
+//   * 3 producer warps gather the 64 latent rows through the page table
+//     (cp.async into 128-byte swizzled tiles; completion lands on an mbarrier;
+//     the page-table lookups of the next tiles are already in flight);
+//   * one thread issues S = Q . C^T (M = 128 heads, N = 64 keys, K = L + R,
+//     fp32 in TMEM); the first columns of Q live in TMEM (the MMA's A operand
+//     from tensor memory), the rest in shared memory;
+//   * 4 softmax warps (thread = head) run a base-2 online softmax whose
+//     reference max moves only when it grows by more than 2^8 (so O is rarely
+//     rescaled) and write P as bf16 over the S tile in TMEM;
+//   * one thread issues O += P . C[:, half] (A = P from TMEM, B = the gathered
+//     tile read MN-major; M = 128, N = L/2, fp32 in TMEM).
+// S is double-buffered in TMEM so QK of tile t+1 overlaps the softmax of tile t.
+// Rows split over several key ranges write fp32 partials (O, max, sum) that
+// attend_combine_kernel merges.
 //
 // Other shapes and the fp8 latent format run attend_simt_kernel.
 #include <cuda_fp8.h>
@@ -42,9 +42,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr float kNegBig = -1.0e30f;
 
-// warp roles
-// (8 warps: registers are handed out per group of four warps, so a ninth
-// warp would cost as much register file as twelve)
+// warp roles (8 warps: registers are handed out per group of four warps)
 constexpr int kMmaWarp = 0;
 constexpr int kProdWarp0 = 1;               // warps 1-3: producers (96 threads)
 constexpr int kSoftWarp0 = 4;               // warps 4-7: softmax, thread = head
@@ -53,44 +51,43 @@ constexpr int kAttThreads = 8 * 32;
 
 template <int L>
 struct AttTraits {
-  static constexpr int HALF = L / 2;                     // latent columns per CTA
-  static constexpr int NPV = HALF / 64;                  // 64-column (128-byte) chunks per CTA
+  static constexpr int R = 64;
+  static constexpr int HALF = L / 2;                     // output columns per CTA
+  static constexpr int NPV = HALF / 64;                  // 64-column chunks of the output half
+  static constexpr int NCH = (L + R) / 64;               // 64-column chunks of a latent row
   static constexpr int TILE = kAttTile;                  // keys per tile
   static constexpr int CHUNK = TILE * 128;               // [64 keys x 64 cols] bf16, 128-byte swizzle
-  static constexpr int RCHUNK = TILE * 64;               // [64 keys x 32 rope cols], 64-byte swizzle
-  static constexpr int STAGE = NPV * CHUNK + RCHUNK;
-  static constexpr int STAGES = 3;
-  static constexpr int PIECES = NPV * 8 + 4;             // 16-byte pieces per key per CTA
+  static constexpr int STAGE = NCH * CHUNK;
+  static constexpr int STAGES = 2;
+  // tensor memory: [Q columns held in TMEM | S tile 0 | S tile 1 | O half]
+  static constexpr int S_COLS = 2 * TILE;
+  static constexpr int QT_CH_MAX = (512 - HALF - S_COLS) / 32;  // 64-column Q chunks that fit
+  static constexpr int QT_CH = QT_CH_MAX < L / 64 ? QT_CH_MAX : L / 64;  // q_nope chunks only
+  static constexpr uint32_t S_COL = QT_CH * 32;
+  static constexpr uint32_t O_COL = S_COL + S_COLS;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr int QS_CH = NCH - QT_CH;              // Q chunks in shared memory
   static constexpr int QCHUNK = 128 * 128;               // [128 heads x 64 cols]
-  static constexpr int QRCHUNK = 128 * 64;               // [128 heads x 32 rope cols]
-  static constexpr int QBYTES = NPV * QCHUNK + QRCHUNK;
-  static constexpr int XBYTES = 128 * TILE * 4;          // partial-logit exchange, fp32
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + QBYTES;
-  static constexpr int OFF_X = OFF_K + STAGES * STAGE;
-  static constexpr int OFF_ROWS = OFF_X + XBYTES;        // int32 [topk]: physical row of each entry
-  static constexpr int NBAR = 16;
-  // the row table holds topk entries rounded up to whole tiles
-  __host__ __device__ static constexpr int rows_bytes(int topk) { return (topk + TILE - 1) / TILE * TILE * 4; }
+  static constexpr int OFF_K = OFF_Q + QS_CH * QCHUNK;
+  static constexpr int OFF_ROWS = OFF_K + STAGES * STAGE;  // int32 [STAGES][TILE]
+  static constexpr int OFF_BAR = OFF_ROWS + STAGES * TILE * 4;
+  static constexpr int NBAR = 14;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_MISC + 16 + 1024;
   static constexpr uint32_t IDESC_QK = mma_idesc(128, TILE, 1u, false, false);
   static constexpr uint32_t IDESC_PV = mma_idesc(128, HALF, 1u, false, true);
-  static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t S_COL = 0;                   // two S tiles: cols 0..63, 64..127 (P over their first 32)
-  static constexpr uint32_t O_COL = 256;                 // O half: cols 256 .. 256+HALF-1
   static_assert(HALF % 64 == 0 && HALF <= 256, "latent width");
+  static_assert(O_COL + HALF <= TMEM_COLS, "tensor memory");
+  static_assert(SMEM <= 227 * 1024, "shared memory");
 };
-
-// Shared-memory bytes of the tensor-core kernel for a given topk.
-template <int L>
-constexpr int att_smem_bytes(int topk) {
-  return AttTraits<L>::OFF_ROWS + AttTraits<L>::rows_bytes(topk) + AttTraits<L>::NBAR * 8 + 16 + 1024;
-}
 
 struct AttParams {
   CUtensorMap tm_qn;       // q_nope as [T*H, L] bf16, box {64, 128}, 128-byte swizzle
-  CUtensorMap tm_qp;       // q_pe as [T*H, R] bf16, box {32, 128}, 64-byte swizzle
+  CUtensorMap tm_qp;       // q_pe as [T*H, R] bf16, box {64, 128}, 128-byte swizzle
   const int32_t *sel;
   const uint8_t *latent;   // [pages*P][L+R] bf16
+  const __nv_bfloat16 *q_nope;
   const float *sink;
   const AttUnit *units;
   const int32_t *row_pos, *row_page_off, *row_npages, *row_page_start, *pages;
@@ -125,38 +122,37 @@ __device__ __forceinline__ int64_t latent_row(int j, int pos, int page_off, int 
 }
 
 template <int L>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
-    attend_tc_kernel(const __grid_constant__ AttParams p) {
+__global__ void __launch_bounds__(kAttThreads, 1) attend_tc_kernel(const __grid_constant__ AttParams p) {
   using C = AttTraits<L>;
-  constexpr int R = 64;
+  constexpr int R = C::R;
   constexpr int ROWB = (L + R) * 2;        // bytes per latent row
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  const int off_bar = C::OFF_ROWS + C::rows_bytes(p.K);
-  const uint32_t bar0 = sbase + off_bar;
-  const uint32_t b_qfull = bar0 + 0;
-  auto kfull = [&](int s) { return bar0 + 8u * (1 + s); };
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  const uint32_t b_qsfull = bar0 + 0, b_qtfull = bar0 + 8;
+  auto kfull = [&](int s) { return bar0 + 8u * (2 + s); };
   auto kempty = [&](int s) { return bar0 + 8u * (4 + s); };
-  auto sfull = [&](int b) { return bar0 + 8u * (7 + b); };
-  auto sempty = [&](int b) { return bar0 + 8u * (9 + b); };
-  const uint32_t b_pfull = bar0 + 8u * 11, b_pvdone = bar0 + 8u * 12;
-  const uint32_t b_xfull = bar0 + 8u * 13, b_xfree = bar0 + 8u * 14;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + off_bar + C::NBAR * 8);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + off_bar + C::NBAR * 8 + 4);
+  auto sfull = [&](int b) { return bar0 + 8u * (6 + b); };
+  auto sempty = [&](int b) { return bar0 + 8u * (8 + b); };
+  auto pfull = [&](int b) { return bar0 + 8u * (10 + b); };
+  const uint32_t b_pvdone = bar0 + 8u * 12;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
   int32_t *rows_sm = reinterpret_cast<int32_t *>(smem + C::OFF_ROWS);
 
   const int warp = threadIdx.x / 32, lane = lane_id();
-  const uint32_t crank = cluster_rank();
-  const uint32_t peer = crank ^ 1u;
+  const int half = blockIdx.x & 1;
   const AttUnit unit = p.units[blockIdx.x >> 1];
   const int row = unit.row;
   const int pos = p.row_pos[row];
   const int nent = unit.k1 - unit.k0;
   const int ntiles = (nent + C::TILE - 1) / C::TILE;
+  const int32_t *selrow = p.sel + static_cast<int64_t>(row) * p.K + unit.k0;
 
   if (threadIdx.x == 0) {
-    mbar_init(b_qfull, 1);
+    mbar_init(b_qsfull, 1);
+    mbar_init(b_qtfull, 128);
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(kfull(s), kProdThreads);
       mbar_init(kempty(s), 1);
@@ -165,10 +161,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
       mbar_init(sfull(b), 1);
       mbar_init(sempty(b), 1);
     }
-    mbar_init(b_pfull, 128);
+    mbar_init(pfull(0), 128);
+    mbar_init(pfull(1), 128);
     mbar_init(b_pvdone, 1);
-    mbar_init(b_xfull, 1);   // armed locally with the exchange bytes; filled by the partner's st.async
-    mbar_init(b_xfree, 4);   // one arrival per partner softmax warp once it has read its copy
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -177,131 +172,141 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  cluster_sync();  // both CTAs' barriers exist before any remote arrive
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      mbar_arrive_expect_tx(b_qfull, C::QBYTES);
-      for (int ch = 0; ch < C::NPV; ++ch)
-        tma_load_2d(sbase + C::OFF_Q + ch * C::QCHUNK, &p.tm_qn, static_cast<int>(crank) * C::HALF + ch * 64,
-                    row * p.H, b_qfull);
-      tma_load_2d(sbase + C::OFF_Q + C::NPV * C::QCHUNK, &p.tm_qp, static_cast<int>(crank) * 32, row * p.H,
-                  b_qfull);
-      bool ok = mbar_wait(b_qfull, 0, abort_flag, p.err);
+      mbar_arrive_expect_tx(b_qsfull, C::QS_CH * C::QCHUNK);
+      for (int ch = C::QT_CH; ch < C::NCH; ++ch) {
+        const uint32_t dst = sbase + C::OFF_Q + (ch - C::QT_CH) * C::QCHUNK;
+        if (ch * 64 < L) tma_load_2d(dst, &p.tm_qn, ch * 64, row * p.H, b_qsfull);
+        else tma_load_2d(dst, &p.tm_qp, ch * 64 - L, row * p.H, b_qsfull);
+      }
+      bool ok = mbar_wait(b_qsfull, 0, abort_flag, p.err) && mbar_wait(b_qtfull, 0, abort_flag, p.err);
       const uint32_t o_tmem = tmem_base + C::O_COL;
-      const uint32_t qst = sbase + C::OFF_Q;
-      for (int t = 0; ok && t <= ntiles; ++t) {
-        if (t < ntiles) {
-          const int st = t % C::STAGES, sb = t & 1;
-          if (!mbar_wait(kfull(st), (t / C::STAGES) & 1, abort_flag, p.err)) break;
-          fence_proxy_async_smem();   // the gathered tile (generic-proxy writes) feeds the tensor core
-          if (!mbar_wait(sempty(sb), ((t >> 1) & 1) ^ 1, abort_flag, p.err)) break;
-          tc_fence_after();
-          const uint32_t s_tmem = tmem_base + C::S_COL + sb * C::TILE;
-          const uint32_t kst = sbase + C::OFF_K + st * C::STAGE;
+      // descriptors are built once; a K step of 16 columns (32 bytes) adds 2 to
+      // the encoded start address, a chunk adds chunk_bytes / 16
+      const uint64_t qdesc = smem_desc(sbase + C::OFF_Q, 16, 1024, kSwizzle128);
+      const uint64_t kdesc0 = smem_desc(sbase + C::OFF_K, 16, 1024, kSwizzle128);
+      const uint64_t vdesc0 = smem_desc(sbase + C::OFF_K + half * C::NPV * C::CHUNK, C::CHUNK, 1024, kSwizzle128);
+      constexpr uint64_t kStageStep = C::STAGE >> 4;
+      // issue QK of the next tile or PV of the oldest softmaxed tile, whichever is ready
+      int nq = 0, np = 0;
+      uint64_t idle_since = 0;
+      uint32_t idle = 0;
+      while (ok && np < ntiles) {
+        bool progressed = false;
+        if (nq < ntiles && nq < np + 2) {
+          const int st = nq & 1;
+          if (mbar_test(kfull(st), (nq >> 1) & 1) && mbar_test(sempty(st), ((nq >> 1) & 1) ^ 1)) {
+            fence_proxy_async_smem();   // the gathered tile (cp.async writes) feeds the tensor core
+            tc_fence_after();
+            const uint32_t s_tmem = tmem_base + C::S_COL + st * C::TILE;
 #pragma unroll
-          for (int ch = 0; ch < C::NPV; ++ch) {
+            for (int ch = 0; ch < C::QT_CH; ++ch)       // Q columns in tensor memory
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint64_t ad = smem_desc(qst + ch * C::QCHUNK + k * 32, 16, 1024, kSwizzle128);
-              const uint64_t bd = smem_desc(kst + ch * C::CHUNK + k * 32, 16, 1024, kSwizzle128);
-              mma_f16_ss(s_tmem, ad, bd, C::IDESC_QK, (ch | k) ? 1u : 0u);
-            }
+              for (int k = 0; k < 4; ++k)
+                mma_f16_ts(s_tmem, tmem_base + ch * 32 + k * 8, kdesc0 + st * kStageStep + (ch * C::CHUNK >> 4) + 2 * k,
+                           C::IDESC_QK, (ch | k) ? 1u : 0u);
+#pragma unroll
+            for (int ch = C::QT_CH; ch < C::NCH; ++ch)   // Q columns in shared memory
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                mma_f16_ss(s_tmem, qdesc + ((ch - C::QT_CH) * C::QCHUNK >> 4) + 2 * k,
+                           kdesc0 + st * kStageStep + (ch * C::CHUNK >> 4) + 2 * k, C::IDESC_QK, (ch | k) ? 1u : 0u);
+            mma_commit(sfull(st));
+            ++nq;
+            progressed = true;
           }
-#pragma unroll
-          for (int k = 0; k < 2; ++k) {   // this CTA's 32 rope columns
-            const uint64_t ad = smem_desc(qst + C::NPV * C::QCHUNK + k * 32, 16, 512, kSwizzle64);
-            const uint64_t bd = smem_desc(kst + C::NPV * C::CHUNK + k * 32, 16, 512, kSwizzle64);
-            mma_f16_ss(s_tmem, ad, bd, C::IDESC_QK, 1u);
-          }
-          mma_commit(sfull(sb));
         }
-        if (t >= 1) {
-          const int u = t - 1;
-          if (!mbar_wait(b_pfull, u & 1, abort_flag, p.err)) break;
+        if (np < nq && mbar_test(pfull(np & 1), (np >> 1) & 1)) {
           tc_fence_after();
-          const uint32_t p_tmem = tmem_base + C::S_COL + (u & 1) * C::TILE;
-          const uint32_t kst = sbase + C::OFF_K + (u % C::STAGES) * C::STAGE;
+          const int st = np & 1;
+          const uint32_t p_tmem = tmem_base + C::S_COL + st * C::TILE;
 #pragma unroll
-          for (int k = 0; k < C::TILE / 16; ++k) {
-            const uint64_t bd = smem_desc(kst + k * 16 * 128, C::CHUNK, 1024, kSwizzle128);
-            mma_f16_ts(o_tmem, p_tmem + k * 8, bd, C::IDESC_PV, (u > 0 || k > 0) ? 1u : 0u);
-          }
+          for (int k = 0; k < C::TILE / 16; ++k)
+            mma_f16_ts(o_tmem, p_tmem + k * 8, vdesc0 + st * kStageStep + (k * 16 * 128 >> 4), C::IDESC_PV,
+                       (np > 0 || k > 0) ? 1u : 0u);
           mma_commit(b_pvdone);
-          mma_commit(kempty(u % C::STAGES));
-          mma_commit(sempty(u & 1));
+          mma_commit(kempty(st));
+          mma_commit(sempty(st));
+          ++np;
+          progressed = true;
         }
+        if (progressed) {
+          idle = 0;
+        } else if ((++idle & 255) == 0) {
+          if (*abort_flag) break;
+          if (idle_since == 0) idle_since = globaltimer();
+          else if (globaltimer() - idle_since > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicOr(p.err, kErrTimeout);
+            break;
+          }
+        }
+        if (progressed) idle_since = 0;
       }
     }
     __syncwarp();
   } else if (warp < kSoftWarp0) {
     // ------------------------------------------------------------ producers
+    // Three warps copy each tile with cp.async: eight lanes per 128-byte chunk
+    // of a latent row, 128-byte swizzled into the tile; the arrival on the
+    // stage's mbarrier fires when this thread's copies have landed.  Warp 1
+    // resolves the tile's rows (lane l: keys l and l+32); the selection
+    // entries of tile t+2 and the page ids of tile t+1 are loaded while tile t
+    // is issued.
     const int pt = threadIdx.x - 32 * kProdWarp0;  // 0..95
-    {
-      const int page_off = p.row_page_off[row], npages = p.row_npages[row], page_start = p.row_page_start[row];
-      const int32_t *selrow = p.sel + static_cast<int64_t>(row) * p.K + unit.k0;
-      // eight entries per thread at a time: all selection loads, then all
-      // page-table loads, are in flight together
-      constexpr int kB = 8;
-      for (int base = 0; base < ntiles * C::TILE; base += kProdThreads * kB) {
-        int j[kB];
-#pragma unroll
-        for (int u = 0; u < kB; ++u) {
-          const int e = base + u * kProdThreads + pt;
-          j[u] = e < nent ? selrow[e] : -1;
-        }
-        int pg[kB];
-#pragma unroll
-        for (int u = 0; u < kB; ++u) {
-          pg[u] = -1;
-          if (j[u] >= 0 && j[u] <= pos) {
-            const int64_t pi = (static_cast<int64_t>(page_start) + j[u]) / p.P;
-            if (pi < npages) pg[u] = p.pages[page_off + pi];
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < kB; ++u) {
-          const int e = base + u * kProdThreads + pt;
-          if (e >= ntiles * C::TILE) continue;
-          int32_t r = -1;
-          if (j[u] < -1 || j[u] > pos) {
-            atomicOr(p.err, kErrBounds);            // a position this row cannot see
-          } else if (j[u] >= 0) {
-            const int64_t slot = static_cast<int64_t>(page_start) + j[u];
-            if (pg[u] < 0 || pg[u] >= p.num_pages || slot / p.P >= npages) atomicOr(p.err, kErrBounds);
-            else r = static_cast<int32_t>(static_cast<int64_t>(pg[u]) * p.P + slot % p.P);
-          }
-          rows_sm[e] = r;
-        }
+    const int page_off = p.row_page_off[row], npages = p.row_npages[row], page_start = p.row_page_start[row];
+    const bool resolver = warp == kProdWarp0;
+    auto sel_at = [&](int t, int k) -> int {
+      const int e = t * C::TILE + k;
+      return (resolver && t < ntiles && e < nent) ? selrow[e] : -1;
+    };
+    auto page_of = [&](int j) -> int {
+      if (j < 0 || j > pos) return -1;
+      const int64_t pi = (static_cast<int64_t>(page_start) + j) / p.P;
+      return pi < npages ? p.pages[page_off + pi] : -1;
+    };
+    auto phys = [&](int j, int pg) -> int32_t {   // -1: masked (zero-filled, its P is 0)
+      if (j == -1) return -1;
+      if (j < -1 || j > pos || pg < 0 || pg >= p.num_pages) {
+        atomicOr(p.err, kErrBounds);
+        return -1;
       }
-    }
-    named_bar_sync(1, kProdThreads + 128);   // the row table is complete (producers + softmax)
-    const int col0 = static_cast<int>(crank) * C::HALF;
-    const int rcol0 = L + static_cast<int>(crank) * 32;
+      const int64_t slot = static_cast<int64_t>(page_start) + j;
+      return static_cast<int32_t>(static_cast<int64_t>(pg) * p.P + slot % p.P);
+    };
+    int ja0 = sel_at(0, lane), jb0 = sel_at(0, lane + 32);
+    int ja1 = sel_at(1, lane), jb1 = sel_at(1, lane + 32);
+    int pa0 = page_of(ja0), pb0 = page_of(jb0);
+    const int piece = lane & 7, sub = pt >> 3;        // sub: 0..11, one 128-byte chunk per 8 lanes
     for (int t = 0; t < ntiles; ++t) {
-      const int st = t % C::STAGES;
-      if (!mbar_wait(kempty(st), ((t / C::STAGES) & 1) ^ 1, abort_flag, p.err)) break;
+      const int st = t & 1;
+      const int pa1 = page_of(ja1), pb1 = page_of(jb1);
+      const int ja2 = sel_at(t + 2, lane), jb2 = sel_at(t + 2, lane + 32);
+      if (!mbar_wait(kempty(st), ((t >> 1) & 1) ^ 1, abort_flag, p.err)) break;
+      int32_t *rows = rows_sm + st * C::TILE;
+      if (resolver) {
+        rows[lane] = phys(ja0, pa0);
+        rows[lane + 32] = phys(jb0, pb0);
+      }
+      named_bar_sync(2, kProdThreads);
       const uint32_t kst = sbase + C::OFF_K + st * C::STAGE;
-      for (int idx = pt; idx < C::TILE * C::PIECES; idx += kProdThreads) {
-        const int key = idx / C::PIECES;
-        const int piece = idx - key * C::PIECES;
-        const int32_t prow = rows_sm[t * C::TILE + key];
-        uint32_t dst;
-        int col;
-        if (piece < C::NPV * 8) {
-          dst = kst + (piece >> 3) * C::CHUNK + sw128_offset(key, piece & 7);
-          col = col0 + piece * 8;
-        } else {
-          dst = kst + C::NPV * C::CHUNK + sw64_offset(key, piece - C::NPV * 8);
-          col = rcol0 + (piece - C::NPV * 8) * 8;
-        }
-        const uint8_t *src = p.latent + (prow >= 0 ? static_cast<int64_t>(prow) * ROWB + col * 2 : 0);
+      // chunk q = key * NCH + ch: consecutive q are consecutive chunks of one row
+#pragma unroll 4
+      for (int q = sub; q < C::TILE * C::NCH; q += kProdThreads / 8) {
+        const int key = q / C::NCH, ch = q - key * C::NCH;
+        const int32_t prow = rows[key];
+        const uint32_t dst = kst + ch * C::CHUNK + sw128_offset(key, piece);
+        const uint8_t *src = p.latent + (prow >= 0 ? static_cast<int64_t>(prow) * ROWB + ch * 128 + piece * 16 : 0);
         cp_async_16_zfill(dst, src, prow >= 0 ? 16u : 0u);
       }
       cp_async_mbar_arrive(kfull(st));
+      ja0 = ja1; jb0 = jb1; ja1 = ja2; jb1 = jb2; pa0 = pa1; pb0 = pb1;
     }
     cp_async_wait<0>();   // nothing in flight when the CTA leaves
   } else {
@@ -309,90 +314,76 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
     const int quad = warp & 3;
     const int h = quad * 32 + lane;                      // head = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t x_own = sbase + C::OFF_X + h * 256;
-    const uint32_t x_peer = map_to_cta(x_own, peer);
-    const uint32_t peer_xfull = map_to_cta(b_xfull, peer), peer_xfree = map_to_cta(b_xfree, peer);
+    // the first QT_CH x 64 columns of this head's q_nope go to tensor memory
+    // (bf16 pairs, the lower column in the low half of each 32-bit word)
+    {
+      const uint4 *qrow = reinterpret_cast<const uint4 *>(p.q_nope + (static_cast<int64_t>(row) * p.H + h) * L);
+#pragma unroll 1
+      for (int ch = 0; ch < C::QT_CH; ++ch) {
+        uint32_t v[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 x = h < p.H ? __ldg(qrow + ch * 8 + i) : make_uint4(0, 0, 0, 0);
+          v[4 * i] = x.x;
+          v[4 * i + 1] = x.y;
+          v[4 * i + 2] = x.z;
+          v[4 * i + 3] = x.w;
+        }
+        tmem_st32(tmem_base + lane_base + ch * 32, v);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(b_qtfull);
+    }
     float m_ref = kNegBig, l = 0.f;
-    named_bar_sync(1, kProdThreads + 128);   // the row table is complete
+    int jA = -1, jB = -1;
+    {
+      jA = lane < nent ? selrow[lane] : -1;
+      jB = lane + 32 < nent ? selrow[lane + 32] : -1;
+    }
     bool ok = true;
-    // The partial logits of tile t+1 are sent to the partner before the softmax
-    // of tile t runs, so the transfer overlaps the math.  The partner reads its
-    // copy of tile t before this CTA sends tile t+1 into the same buffer
-    // (xfree), which both CTAs reach without waiting on each other.
-    float s[C::TILE];
-    auto load_s = [&](int t, float (&dst)[C::TILE]) -> bool {
-      if (!mbar_wait(sfull(t & 1), (t >> 1) & 1, abort_flag, p.err)) return false;
+    for (int t = 0; t < ntiles && ok; ++t) {
+      const uint32_t vlo = __ballot_sync(0xffffffffu, jA >= 0 && jA <= pos);
+      const uint32_t vhi = __ballot_sync(0xffffffffu, jB >= 0 && jB <= pos);
+      if (t + 1 < ntiles) {
+        const int e = (t + 1) * C::TILE + lane;
+        jA = e < nent ? selrow[e] : -1;
+        jB = e + 32 < nent ? selrow[e + 32] : -1;
+      }
+      const int sb = t & 1;
+      if (!mbar_wait(sfull(sb), (t >> 1) & 1, abort_flag, p.err)) { ok = false; break; }
       tc_fence_after();
+      float s[C::TILE];
 #pragma unroll
       for (int c0 = 0; c0 < C::TILE; c0 += 16)
-        tmem_ld16(tmem_base + lane_base + C::S_COL + (t & 1) * C::TILE + c0,
-                  *reinterpret_cast<float(*)[16]>(dst + c0));
+        tmem_ld16(tmem_base + lane_base + C::S_COL + sb * C::TILE + c0, *reinterpret_cast<float(*)[16]>(s + c0));
       tmem_ld_wait();
-      return true;
-    };
-    auto send_s = [&](const float (&src)[C::TILE]) {
-#pragma unroll
-      for (int c = 0; c < 16; ++c)
-        st_async_v4(x_peer + ((c ^ (h & 15)) << 4), src[4 * c], src[4 * c + 1], src[4 * c + 2], src[4 * c + 3],
-                    peer_xfull);
-    };
-    if (ntiles > 0) {
-      ok = load_s(0, s);
-      if (ok) send_s(s);
-    }
-    for (int t = 0; t < ntiles && ok; ++t) {
-      const uint32_t vlo = __ballot_sync(0xffffffffu, rows_sm[t * C::TILE + lane] >= 0);
-      const uint32_t vhi = __ballot_sync(0xffffffffu, rows_sm[t * C::TILE + 32 + lane] >= 0);
-      const int sb = t & 1;
-
-      // 1. the partner's partial logits of tile t (asynchronous remote stores
-      //    that land on this CTA's mbarrier as transaction bytes)
-      if (h == 0) mbar_arrive_expect_tx(b_xfull, C::XBYTES);
-      if (!mbar_wait<true>(b_xfull, t & 1, abort_flag, p.err)) { ok = false; break; }
-      const float4 *xr = reinterpret_cast<const float4 *>(smem + C::OFF_X + h * 256);
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const float4 v = xr[c ^ (h & 15)];
-        s[4 * c] += v.x;
-        s[4 * c + 1] += v.y;
-        s[4 * c + 2] += v.z;
-        s[4 * c + 3] += v.w;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive_remote(peer_xfree);
-
-      // 2. this CTA's partial logits of tile t+1 go out now
-      float s_next[C::TILE];
-      if (t + 1 < ntiles) {
-        if (!load_s(t + 1, s_next)) { ok = false; break; }
-        if (!mbar_wait<true>(b_xfree, t & 1, abort_flag, p.err)) { ok = false; break; }
-        send_s(s_next);
-      }
 
       // online softmax in base 2 with a lazily moved reference max
-      float tmax = -INFINITY;
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int i = 0; i < C::TILE; ++i) {
         const bool v = ((i < 32 ? vlo >> i : vhi >> (i - 32)) & 1u) != 0;
         s[i] = v ? s[i] * p.scale_log2 : -INFINITY;
-        tmax = fmaxf(tmax, s[i]);
+        mx[i & 3] = fmaxf(mx[i & 3], s[i]);
       }
+      const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       float alpha = 1.f;
       const bool rescale = tmax > m_ref + kRescaleThreshold;
       if (rescale) {
         alpha = exp2f(m_ref - tmax);
         m_ref = tmax;
       }
-      float sum = 0.f;
+      float sm[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t packed[C::TILE / 2];
 #pragma unroll
       for (int i = 0; i < C::TILE; i += 2) {
         const __nv_bfloat162 pb = __floats2bfloat162_rn(exp2f(s[i] - m_ref), exp2f(s[i + 1] - m_ref));
         const float2 pf = __bfloat1622float2(pb);
-        sum += pf.x + pf.y;
+        sm[(i >> 1) & 3] += pf.x + pf.y;
         packed[i / 2] = *reinterpret_cast<const uint32_t *>(&pb);
       }
-      l = l * alpha + sum;
+      l = l * alpha + ((sm[0] + sm[1]) + (sm[2] + sm[3]));
 
       // O must hold every earlier tile before it is rescaled
       if (rescale && t > 0) {
@@ -412,14 +403,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
       tmem_st32(tmem_base + lane_base + C::S_COL + sb * C::TILE, packed);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(b_pfull);
-#pragma unroll
-      for (int i = 0; i < C::TILE; ++i) s[i] = s_next[i];
+      mbar_arrive(pfull(sb));
     }
     if (ok && ntiles > 0) ok = mbar_wait(b_pvdone, (ntiles - 1) & 1, abort_flag, p.err);
     tc_fence_after();
     if (ok && h < p.H) {
-      const int col0 = static_cast<int>(crank) * C::HALF;
+      const int col0 = half * C::HALF;
       if (unit.slot < 0) {
         float f = 0.f;
         if (p.sink) {
@@ -468,7 +457,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
 #pragma unroll
           for (int i = 0; i < 4; ++i) d4[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
         }
-        if (crank == 0) {
+        if (half == 0) {
           float *ml = p.mlpart + (static_cast<int64_t>(unit.slot) * p.H + h) * 2;
           ml[0] = m_ref;
           ml[1] = l;
@@ -479,7 +468,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // no CTA leaves while its partner may still touch its shared memory
+  tc_fence_after();
   if (warp == kMmaWarp) tmem_dealloc(tmem_base, C::TMEM_COLS);
 }
 
@@ -593,16 +582,18 @@ template <int L>
 cudaError_t run_tc(const dsa_ctx *ctx, const dsa_plan_t *plan, const int32_t *sel, const void *q_nope,
                    const void *q_pe, const void *latent, const float *sink, float sm_scale, void *out,
                    cudaStream_t s) {
+  using Cfg = AttTraits<L>;
   const dsa_config_t &c = ctx->cfg;
   AttParams prm{};
   if (!encode_tiled_2d(&prm.tm_qn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void *>(q_nope), L,
                        static_cast<uint64_t>(plan->T) * c.heads, L * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   if (!encode_tiled_2d(&prm.tm_qp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void *>(q_pe), 64,
-                       static_cast<uint64_t>(plan->T) * c.heads, 64 * 2, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
+                       static_cast<uint64_t>(plan->T) * c.heads, 64 * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   prm.sel = sel;
   prm.latent = static_cast<const uint8_t *>(latent);
+  prm.q_nope = static_cast<const __nv_bfloat16 *>(q_nope);
   prm.sink = sink;
   prm.units = plan->units;
   prm.row_pos = plan->row_pos;
@@ -619,21 +610,22 @@ cudaError_t run_tc(const dsa_ctx *ctx, const dsa_plan_t *plan, const int32_t *se
   prm.P = c.page_size;
   prm.num_pages = plan->cache_pages;
   prm.scale_log2 = sm_scale * kLog2e;
-  const int smem = att_smem_bytes<L>(c.topk);
   auto kern = attend_tc_kernel<L>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  kern<<<2 * plan->n_units, kAttThreads, smem, s>>>(prm);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  kern<<<2 * plan->n_units, kAttThreads, Cfg::SMEM, s>>>(prm);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 bool attend_tc_supported(const dsa_config_t &c) {
-  if (c.latent_fmt != DSA_LATENT_BF16 || c.heads > 128 || c.rope_dim != 64) return false;
-  if (c.kv_lora_rank != 512 && c.kv_lora_rank != 256 && c.kv_lora_rank != 128) return false;
-  // the per-unit row table (topk int32) must fit beside the tiles
-  return att_smem_bytes<512>(c.topk) <= 227 * 1024;
+  return c.latent_fmt == DSA_LATENT_BF16 && c.heads <= 128 && c.rope_dim == 64 &&
+         (c.kv_lora_rank == 512 || c.kv_lora_rank == 256 || c.kv_lora_rank == 128);
 }
 
 cudaError_t launch_attend(const dsa_ctx *ctx, const dsa_plan_t *plan, const int32_t *sel, const void *q_nope,
