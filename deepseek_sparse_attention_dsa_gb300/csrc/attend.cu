@@ -12,11 +12,11 @@
 // the full logits of all 128 heads and accumulates O for latent columns
 // [c*L/2, (c+1)*L/2), so the two halves of a row share nothing but their
 // inputs (the QK contraction is done by both; in exchange no CTA ever waits on
-// another).  Per tile of 64 selected keys:
-//   * 3 producer warps gather the 64 latent rows through the page table
+// another).  Per tile of 32 selected keys (four tiles in flight):
+//   * 7 producer warps gather the tile's latent rows through the page table
 //     (cp.async into 128-byte swizzled tiles; completion lands on an mbarrier;
 //     the page-table lookups of the next tiles are already in flight);
-//   * one thread issues S = Q . C^T (M = 128 heads, N = 64 keys, K = L + R,
+//   * one thread issues S = Q . C^T (M = 128 heads, N = 32 keys, K = L + R,
 //     fp32 in TMEM); the first columns of Q live in TMEM (the MMA's A operand
 //     from tensor memory), the rest in shared memory;
 //   * 4 softmax warps (thread = head) run a base-2 online softmax whose
@@ -42,12 +42,12 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr float kNegBig = -1.0e30f;
 
-// warp roles (8 warps: registers are handed out per group of four warps)
+// warp roles (12 warps; registers are handed out per group of four warps)
 constexpr int kMmaWarp = 0;
-constexpr int kProdWarp0 = 1;               // warps 1-3: producers (96 threads)
-constexpr int kSoftWarp0 = 4;               // warps 4-7: softmax, thread = head
-constexpr int kProdThreads = 96;
-constexpr int kAttThreads = 8 * 32;
+constexpr int kProdWarp0 = 1;               // warps 1-7: producers (224 threads)
+constexpr int kSoftWarp0 = 8;               // warps 8-11: softmax, thread = head
+constexpr int kProdThreads = 224;
+constexpr int kAttThreads = 12 * 32;
 
 template <int L>
 struct AttTraits {
@@ -55,10 +55,10 @@ struct AttTraits {
   static constexpr int HALF = L / 2;                     // output columns per CTA
   static constexpr int NPV = HALF / 64;                  // 64-column chunks of the output half
   static constexpr int NCH = (L + R) / 64;               // 64-column chunks of a latent row
-  static constexpr int TILE = kAttTile;                  // keys per tile
-  static constexpr int CHUNK = TILE * 128;               // [64 keys x 64 cols] bf16, 128-byte swizzle
+  static constexpr int TILE = 32;                        // keys per tile (UMMA N of QK)
+  static constexpr int CHUNK = TILE * 128;               // [32 keys x 64 cols] bf16, 128-byte swizzle
   static constexpr int STAGE = NCH * CHUNK;
-  static constexpr int STAGES = 2;
+  static constexpr int STAGES = 4;
   // tensor memory: [Q columns held in TMEM | S tile 0 | S tile 1 | O half]
   static constexpr int S_COLS = 2 * TILE;
   static constexpr int QT_CH_MAX = (512 - HALF - S_COLS) / 32;  // 64-column Q chunks that fit
@@ -72,13 +72,14 @@ struct AttTraits {
   static constexpr int OFF_K = OFF_Q + QS_CH * QCHUNK;
   static constexpr int OFF_ROWS = OFF_K + STAGES * STAGE;  // int32 [STAGES][TILE]
   static constexpr int OFF_BAR = OFF_ROWS + STAGES * TILE * 4;
-  static constexpr int NBAR = 14;
+  static constexpr int NBAR = 20;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;
   static constexpr uint32_t IDESC_QK = mma_idesc(128, TILE, 1u, false, false);
   static constexpr uint32_t IDESC_PV = mma_idesc(128, HALF, 1u, false, true);
   static_assert(HALF % 64 == 0 && HALF <= 256, "latent width");
   static_assert(O_COL + HALF <= TMEM_COLS, "tensor memory");
+  static_assert(QT_CH * QCHUNK <= STAGES * STAGE, "Q staging");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
@@ -126,17 +127,19 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_tc_kernel(const __grid_
   using C = AttTraits<L>;
   constexpr int R = C::R;
   constexpr int ROWB = (L + R) * 2;        // bytes per latent row
+  constexpr int T = C::TILE;
+  constexpr int NS = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + C::OFF_BAR;
-  const uint32_t b_qsfull = bar0 + 0, b_qtfull = bar0 + 8;
-  auto kfull = [&](int s) { return bar0 + 8u * (2 + s); };
-  auto kempty = [&](int s) { return bar0 + 8u * (4 + s); };
-  auto sfull = [&](int b) { return bar0 + 8u * (6 + b); };
-  auto sempty = [&](int b) { return bar0 + 8u * (8 + b); };
-  auto pfull = [&](int b) { return bar0 + 8u * (10 + b); };
-  const uint32_t b_pvdone = bar0 + 8u * 12;
+  const uint32_t b_qsfull = bar0 + 0, b_qtfull = bar0 + 8, b_qtdone = bar0 + 16;
+  auto kfull = [&](int s) { return bar0 + 8u * (3 + s); };
+  auto kempty = [&](int s) { return bar0 + 8u * (3 + NS + s); };
+  auto sfull = [&](int b) { return bar0 + 8u * (3 + 2 * NS + b); };
+  auto sempty = [&](int b) { return bar0 + 8u * (5 + 2 * NS + b); };
+  auto pfull = [&](int b) { return bar0 + 8u * (7 + 2 * NS + b); };
+  const uint32_t b_pvdone = bar0 + 8u * (9 + 2 * NS);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
   int32_t *rows_sm = reinterpret_cast<int32_t *>(smem + C::OFF_ROWS);
@@ -147,22 +150,22 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_tc_kernel(const __grid_
   const int row = unit.row;
   const int pos = p.row_pos[row];
   const int nent = unit.k1 - unit.k0;
-  const int ntiles = (nent + C::TILE - 1) / C::TILE;
+  const int ntiles = (nent + T - 1) / T;
   const int32_t *selrow = p.sel + static_cast<int64_t>(row) * p.K + unit.k0;
 
   if (threadIdx.x == 0) {
     mbar_init(b_qsfull, 1);
-    mbar_init(b_qtfull, 128);
-    for (int s = 0; s < C::STAGES; ++s) {
+    mbar_init(b_qtfull, 1);
+    mbar_init(b_qtdone, 128);
+    for (int s = 0; s < NS; ++s) {
       mbar_init(kfull(s), kProdThreads);
       mbar_init(kempty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(sfull(b), 1);
       mbar_init(sempty(b), 1);
+      mbar_init(pfull(b), 128);
     }
-    mbar_init(pfull(0), 128);
-    mbar_init(pfull(1), 128);
     mbar_init(b_pvdone, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -179,13 +182,18 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_tc_kernel(const __grid_
   if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      // Q columns kept in shared memory, and (through the still idle stage
+      // buffers) the columns the softmax warps move into tensor memory
       mbar_arrive_expect_tx(b_qsfull, C::QS_CH * C::QCHUNK);
       for (int ch = C::QT_CH; ch < C::NCH; ++ch) {
         const uint32_t dst = sbase + C::OFF_Q + (ch - C::QT_CH) * C::QCHUNK;
         if (ch * 64 < L) tma_load_2d(dst, &p.tm_qn, ch * 64, row * p.H, b_qsfull);
         else tma_load_2d(dst, &p.tm_qp, ch * 64 - L, row * p.H, b_qsfull);
       }
-      bool ok = mbar_wait(b_qsfull, 0, abort_flag, p.err) && mbar_wait(b_qtfull, 0, abort_flag, p.err);
+      mbar_arrive_expect_tx(b_qtfull, C::QT_CH * C::QCHUNK);
+      for (int ch = 0; ch < C::QT_CH; ++ch)
+        tma_load_2d(sbase + C::OFF_K + ch * C::QCHUNK, &p.tm_qn, ch * 64, row * p.H, b_qtfull);
+      bool ok = mbar_wait(b_qsfull, 0, abort_flag, p.err) && mbar_wait(b_qtdone, 0, abort_flag, p.err);
       const uint32_t o_tmem = tmem_base + C::O_COL;
       // descriptors are built once; a K step of 16 columns (32 bytes) adds 2 to
       // the encoded start address, a chunk adds chunk_bytes / 16
@@ -200,44 +208,46 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_tc_kernel(const __grid_
       while (ok && np < ntiles) {
         bool progressed = false;
         if (nq < ntiles && nq < np + 2) {
-          const int st = nq & 1;
-          if (mbar_test(kfull(st), (nq >> 1) & 1) && mbar_test(sempty(st), ((nq >> 1) & 1) ^ 1)) {
+          const int st = nq % NS, sb = nq & 1;
+          if (mbar_test(kfull(st), (nq / NS) & 1) && mbar_test(sempty(sb), ((nq >> 1) & 1) ^ 1)) {
             fence_proxy_async_smem();   // the gathered tile (cp.async writes) feeds the tensor core
             tc_fence_after();
-            const uint32_t s_tmem = tmem_base + C::S_COL + st * C::TILE;
+            const uint32_t s_tmem = tmem_base + C::S_COL + sb * T;
+            const uint64_t kd = kdesc0 + st * kStageStep;
 #pragma unroll
             for (int ch = 0; ch < C::QT_CH; ++ch)       // Q columns in tensor memory
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                mma_f16_ts(s_tmem, tmem_base + ch * 32 + k * 8, kdesc0 + st * kStageStep + (ch * C::CHUNK >> 4) + 2 * k,
-                           C::IDESC_QK, (ch | k) ? 1u : 0u);
+                mma_f16_ts(s_tmem, tmem_base + ch * 32 + k * 8, kd + (ch * C::CHUNK >> 4) + 2 * k, C::IDESC_QK,
+                           (ch | k) ? 1u : 0u);
 #pragma unroll
             for (int ch = C::QT_CH; ch < C::NCH; ++ch)   // Q columns in shared memory
 #pragma unroll
               for (int k = 0; k < 4; ++k)
                 mma_f16_ss(s_tmem, qdesc + ((ch - C::QT_CH) * C::QCHUNK >> 4) + 2 * k,
-                           kdesc0 + st * kStageStep + (ch * C::CHUNK >> 4) + 2 * k, C::IDESC_QK, (ch | k) ? 1u : 0u);
-            mma_commit(sfull(st));
+                           kd + (ch * C::CHUNK >> 4) + 2 * k, C::IDESC_QK, (ch | k) ? 1u : 0u);
+            mma_commit(sfull(sb));
             ++nq;
             progressed = true;
           }
         }
         if (np < nq && mbar_test(pfull(np & 1), (np >> 1) & 1)) {
           tc_fence_after();
-          const int st = np & 1;
-          const uint32_t p_tmem = tmem_base + C::S_COL + st * C::TILE;
+          const int st = np % NS, sb = np & 1;
+          const uint32_t p_tmem = tmem_base + C::S_COL + sb * T;
 #pragma unroll
-          for (int k = 0; k < C::TILE / 16; ++k)
+          for (int k = 0; k < T / 16; ++k)
             mma_f16_ts(o_tmem, p_tmem + k * 8, vdesc0 + st * kStageStep + (k * 16 * 128 >> 4), C::IDESC_PV,
                        (np > 0 || k > 0) ? 1u : 0u);
           mma_commit(b_pvdone);
           mma_commit(kempty(st));
-          mma_commit(sempty(st));
+          mma_commit(sempty(sb));
           ++np;
           progressed = true;
         }
         if (progressed) {
           idle = 0;
+          idle_since = 0;
         } else if ((++idle & 255) == 0) {
           if (*abort_flag) break;
           if (idle_since == 0) idle_since = globaltimer();
@@ -247,7 +257,6 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_tc_kernel(const __grid_
             break;
           }
         }
-        if (progressed) idle_since = 0;
       }
     }
     __syncwarp();
@@ -256,14 +265,13 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_tc_kernel(const __grid_
     // Three warps copy each tile with cp.async: eight lanes per 128-byte chunk
     // of a latent row, 128-byte swizzled into the tile; the arrival on the
     // stage's mbarrier fires when this thread's copies have landed.  Warp 1
-    // resolves the tile's rows (lane l: keys l and l+32); the selection
-    // entries of tile t+2 and the page ids of tile t+1 are loaded while tile t
-    // is issued.
-    const int pt = threadIdx.x - 32 * kProdWarp0;  // 0..95
+    // resolves the tile's rows (lane l: key l); the selection entries of tile
+    // t+2 and the page ids of tile t+1 are loaded while tile t is issued.
+    const int pt = threadIdx.x - 32 * kProdWarp0;  // 0..223
     const int page_off = p.row_page_off[row], npages = p.row_npages[row], page_start = p.row_page_start[row];
     const bool resolver = warp == kProdWarp0;
-    auto sel_at = [&](int t, int k) -> int {
-      const int e = t * C::TILE + k;
+    auto sel_at = [&](int t) -> int {
+      const int e = t * T + lane;
       return (resolver && t < ntiles && e < nent) ? selrow[e] : -1;
     };
     auto page_of = [&](int j) -> int {
@@ -280,25 +288,23 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_tc_kernel(const __grid_
       const int64_t slot = static_cast<int64_t>(page_start) + j;
       return static_cast<int32_t>(static_cast<int64_t>(pg) * p.P + slot % p.P);
     };
-    int ja0 = sel_at(0, lane), jb0 = sel_at(0, lane + 32);
-    int ja1 = sel_at(1, lane), jb1 = sel_at(1, lane + 32);
-    int pa0 = page_of(ja0), pb0 = page_of(jb0);
-    const int piece = lane & 7, sub = pt >> 3;        // sub: 0..11, one 128-byte chunk per 8 lanes
-    for (int t = 0; t < ntiles; ++t) {
-      const int st = t & 1;
-      const int pa1 = page_of(ja1), pb1 = page_of(jb1);
-      const int ja2 = sel_at(t + 2, lane), jb2 = sel_at(t + 2, lane + 32);
-      if (!mbar_wait(kempty(st), ((t >> 1) & 1) ^ 1, abort_flag, p.err)) break;
-      int32_t *rows = rows_sm + st * C::TILE;
-      if (resolver) {
-        rows[lane] = phys(ja0, pa0);
-        rows[lane + 32] = phys(jb0, pb0);
-      }
+    int j0 = sel_at(0), j1 = sel_at(1);
+    int pg0 = page_of(j0);
+    const int piece = lane & 7, sub = pt >> 3;        // sub: one 128-byte chunk per 8 lanes
+    // the stage buffers hold the tensor-memory part of Q until it has been moved
+    bool ok = mbar_wait(b_qtdone, 0, abort_flag, p.err);
+    for (int t = 0; ok && t < ntiles; ++t) {
+      const int st = t % NS;
+      const int pg1 = page_of(j1);
+      const int j2 = sel_at(t + 2);
+      if (!mbar_wait(kempty(st), ((t / NS) & 1) ^ 1, abort_flag, p.err)) break;
+      int32_t *rows = rows_sm + st * T;
+      if (resolver) rows[lane] = phys(j0, pg0);
       named_bar_sync(2, kProdThreads);
       const uint32_t kst = sbase + C::OFF_K + st * C::STAGE;
       // chunk q = key * NCH + ch: consecutive q are consecutive chunks of one row
 #pragma unroll 4
-      for (int q = sub; q < C::TILE * C::NCH; q += kProdThreads / 8) {
+      for (int q = sub; q < T * C::NCH; q += kProdThreads / 8) {
         const int key = q / C::NCH, ch = q - key * C::NCH;
         const int32_t prow = rows[key];
         const uint32_t dst = kst + ch * C::CHUNK + sw128_offset(key, piece);
@@ -306,7 +312,9 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_tc_kernel(const __grid_
         cp_async_16_zfill(dst, src, prow >= 0 ? 16u : 0u);
       }
       cp_async_mbar_arrive(kfull(st));
-      ja0 = ja1; jb0 = jb1; ja1 = ja2; jb1 = jb2; pa0 = pa1; pb0 = pb1;
+      j0 = j1;
+      j1 = j2;
+      pg0 = pg1;
     }
     cp_async_wait<0>();   // nothing in flight when the CTA leaves
   } else {
@@ -314,16 +322,17 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_tc_kernel(const __grid_
     const int quad = warp & 3;
     const int h = quad * 32 + lane;                      // head = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    // the first QT_CH x 64 columns of this head's q_nope go to tensor memory
-    // (bf16 pairs, the lower column in the low half of each 32-bit word)
-    {
-      const uint4 *qrow = reinterpret_cast<const uint4 *>(p.q_nope + (static_cast<int64_t>(row) * p.H + h) * L);
+    bool ok = mbar_wait(b_qtfull, 0, abort_flag, p.err);
+    if (ok) {
+      // this head's row of the tensor-memory part of Q: from the staged
+      // swizzled chunks into TMEM (bf16 pairs, lower column in the low half)
 #pragma unroll 1
       for (int ch = 0; ch < C::QT_CH; ++ch) {
+        const uint8_t *src = smem + C::OFF_K + ch * C::QCHUNK + h * 128;
         uint32_t v[32];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const uint4 x = h < p.H ? __ldg(qrow + ch * 8 + i) : make_uint4(0, 0, 0, 0);
+          const uint4 x = *reinterpret_cast<const uint4 *>(src + ((i ^ (h & 7)) << 4));
           v[4 * i] = x.x;
           v[4 * i + 1] = x.y;
           v[4 * i + 2] = x.z;
@@ -332,39 +341,31 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_tc_kernel(const __grid_
         tmem_st32(tmem_base + lane_base + ch * 32, v);
       }
       tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(b_qtfull);
     }
+    tc_fence_before();
+    mbar_arrive(b_qtdone);
     float m_ref = kNegBig, l = 0.f;
-    int jA = -1, jB = -1;
-    {
-      jA = lane < nent ? selrow[lane] : -1;
-      jB = lane + 32 < nent ? selrow[lane + 32] : -1;
-    }
-    bool ok = true;
+    int jn = lane < nent ? selrow[lane] : -1;
     for (int t = 0; t < ntiles && ok; ++t) {
-      const uint32_t vlo = __ballot_sync(0xffffffffu, jA >= 0 && jA <= pos);
-      const uint32_t vhi = __ballot_sync(0xffffffffu, jB >= 0 && jB <= pos);
+      const uint32_t valid = __ballot_sync(0xffffffffu, jn >= 0 && jn <= pos);
       if (t + 1 < ntiles) {
-        const int e = (t + 1) * C::TILE + lane;
-        jA = e < nent ? selrow[e] : -1;
-        jB = e + 32 < nent ? selrow[e + 32] : -1;
+        const int e = (t + 1) * T + lane;
+        jn = e < nent ? selrow[e] : -1;
       }
       const int sb = t & 1;
       if (!mbar_wait(sfull(sb), (t >> 1) & 1, abort_flag, p.err)) { ok = false; break; }
       tc_fence_after();
-      float s[C::TILE];
+      float s[T];
 #pragma unroll
-      for (int c0 = 0; c0 < C::TILE; c0 += 16)
-        tmem_ld16(tmem_base + lane_base + C::S_COL + sb * C::TILE + c0, *reinterpret_cast<float(*)[16]>(s + c0));
+      for (int c0 = 0; c0 < T; c0 += 16)
+        tmem_ld16(tmem_base + lane_base + C::S_COL + sb * T + c0, *reinterpret_cast<float(*)[16]>(s + c0));
       tmem_ld_wait();
 
       // online softmax in base 2 with a lazily moved reference max
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int i = 0; i < C::TILE; ++i) {
-        const bool v = ((i < 32 ? vlo >> i : vhi >> (i - 32)) & 1u) != 0;
-        s[i] = v ? s[i] * p.scale_log2 : -INFINITY;
+      for (int i = 0; i < T; ++i) {
+        s[i] = ((valid >> i) & 1u) ? s[i] * p.scale_log2 : -INFINITY;
         mx[i & 3] = fmaxf(mx[i & 3], s[i]);
       }
       const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
@@ -375,9 +376,9 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_tc_kernel(const __grid_
         m_ref = tmax;
       }
       float sm[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t packed[C::TILE / 2];
+      uint32_t packed[T / 2];
 #pragma unroll
-      for (int i = 0; i < C::TILE; i += 2) {
+      for (int i = 0; i < T; i += 2) {
         const __nv_bfloat162 pb = __floats2bfloat162_rn(exp2f(s[i] - m_ref), exp2f(s[i + 1] - m_ref));
         const float2 pf = __bfloat1622float2(pb);
         sm[(i >> 1) & 3] += pf.x + pf.y;
@@ -399,8 +400,8 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_tc_kernel(const __grid_
           tmem_st16(tmem_base + lane_base + C::O_COL + c0, o);
         }
       }
-      // P (bf16 pairs, lower key in the low half) over the first 32 columns of this S tile
-      tmem_st32(tmem_base + lane_base + C::S_COL + sb * C::TILE, packed);
+      // P (bf16 pairs, lower key in the low half) over the first T/2 columns of this S tile
+      tmem_st16(tmem_base + lane_base + C::S_COL + sb * T, *reinterpret_cast<const float(*)[16]>(packed));
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(pfull(sb));
