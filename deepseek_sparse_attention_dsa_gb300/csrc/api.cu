@@ -99,8 +99,8 @@ dsa_status ensure_scratch(dsa_ctx *ctx, size_t scores, size_t slots) {
 // ----------------------------------------------------------------------------
 namespace dsa {
 
-bool encode_tiled_2d(CUtensorMap *tm, CUtensorMapDataType dtype, void *base, uint64_t inner, uint64_t outer,
-                     uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -111,12 +111,32 @@ bool encode_tiled_2d(CUtensorMap *tm, CUtensorMapDataType dtype, void *base, uin
         q == cudaDriverEntryPointSuccess)
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
   });
+  return fn;
+}
+}  // namespace
+
+bool encode_tiled_2d(CUtensorMap *tm, CUtensorMapDataType dtype, void *base, uint64_t inner, uint64_t outer,
+                     uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {row_stride_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(tm, dtype, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool encode_tiled_3d(CUtensorMap *tm, CUtensorMapDataType dtype, void *base, const uint64_t dims[3],
+                     const uint64_t strides_bytes[2], const uint32_t box[3], CUtensorMapSwizzle swz) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
+  if (!fn) return false;
+  cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+  cuuint64_t st[2] = {strides_bytes[0], strides_bytes[1]};
+  cuuint32_t bx[3] = {box[0], box[1], box[2]};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(tm, dtype, 3, base, d, st, bx, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }

@@ -28,7 +28,11 @@
 // Rows split over several key ranges write fp32 partials (O, max, sum) that
 // attend_combine_kernel merges.
 //
-// Other shapes and the fp8 latent format run attend_simt_kernel.
+// fp8 latents (656-byte rows) take the same kernel: the producers load the
+// codes, scales and rope into registers, dequantise (code x the scale of its
+// 128-column group, rounded to bf16) and store the bf16 tile the MMAs read.
+// Other shapes run attend_simt_kernel.
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
@@ -100,6 +104,26 @@ struct AttParams {
   float scale_log2;        // sm_scale * log2(e)
 };
 
+// 16 e4m3 codes (one 16-byte piece, lowest address first) times `scale`,
+// rounded to 16 bf16 (two 16-byte pieces).
+__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 raw, float scale, uint4 &lo, uint4 &hi) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int hlf = 0; hlf < 2; ++hlf) {
+      const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * hlf)) & 0xFFFFu),
+                                                       __NV_E4M3);
+      const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
+      const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
+      o[2 * i + hlf] = *reinterpret_cast<const uint32_t *>(&b);
+    }
+  }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
 // Physical latent row of selection entry j for a row, or -1 (masked).  -1 is
 // the padding value; any other value outside 0..pos is a bounds error.
 __device__ __forceinline__ int64_t latent_row(int j, int pos, int page_off, int npages, int page_start,
@@ -122,7 +146,7 @@ __device__ __forceinline__ int64_t latent_row(int j, int pos, int page_off, int 
   return static_cast<int64_t>(page) * P + slot % P;
 }
 
-template <int L>
+template <int L, bool FP8>
 __global__ void __launch_bounds__(kAttThreads, 1) attend_tc_kernel(const __grid_constant__ AttParams p) {
   using C = AttTraits<L>;
   constexpr int R = C::R;
@@ -297,21 +321,70 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_tc_kernel(const __grid_
       const int st = t % NS;
       const int pg1 = page_of(j1);
       const int j2 = sel_at(t + 2);
-      if (!mbar_wait(kempty(st), ((t / NS) & 1) ^ 1, abort_flag, p.err)) break;
+      if (!FP8 && !mbar_wait(kempty(st), ((t / NS) & 1) ^ 1, abort_flag, p.err)) break;
       int32_t *rows = rows_sm + st * T;
       if (resolver) rows[lane] = phys(j0, pg0);
       named_bar_sync(2, kProdThreads);
       const uint32_t kst = sbase + C::OFF_K + st * C::STAGE;
-      // chunk q = key * NCH + ch: consecutive q are consecutive chunks of one row
+      if constexpr (!FP8) {
+        // chunk q = key * NCH + ch: consecutive q are consecutive chunks of one row
 #pragma unroll 4
-      for (int q = sub; q < T * C::NCH; q += kProdThreads / 8) {
-        const int key = q / C::NCH, ch = q - key * C::NCH;
-        const int32_t prow = rows[key];
-        const uint32_t dst = kst + ch * C::CHUNK + sw128_offset(key, piece);
-        const uint8_t *src = p.latent + (prow >= 0 ? static_cast<int64_t>(prow) * ROWB + ch * 128 + piece * 16 : 0);
-        cp_async_16_zfill(dst, src, prow >= 0 ? 16u : 0u);
+        for (int q = sub; q < T * C::NCH; q += kProdThreads / 8) {
+          const int key = q / C::NCH, ch = q - key * C::NCH;
+          const int32_t prow = rows[key];
+          const uint32_t dst = kst + ch * C::CHUNK + sw128_offset(key, piece);
+          const uint8_t *src =
+              p.latent + (prow >= 0 ? static_cast<int64_t>(prow) * ROWB + ch * 128 + piece * 16 : 0);
+          cp_async_16_zfill(dst, src, prow >= 0 ? 16u : 0u);
+        }
+        cp_async_mbar_arrive(kfull(st));
+      } else {
+        // 656-byte rows [L e4m3 | L/128 fp32 scales | R bf16]: 16-byte pieces are
+        // loaded into registers, dequantised (code x scale, rounded to bf16) and
+        // stored into the same swizzled bf16 tile the bf16 path gathers.  The
+        // loads are issued before the stage is known to be free.
+        constexpr int CP = L / 16, RP = R * 2 / 16, PPK = CP + RP;
+        constexpr int RB8 = L + 4 * (L / 128) + 2 * R;
+        constexpr int PER = (T * PPK + kProdThreads - 1) / kProdThreads;
+        uint4 raw[PER];
+        float scl[PER];
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+          const int i = pt + u * kProdThreads;
+          raw[u] = make_uint4(0, 0, 0, 0);
+          scl[u] = 0.f;
+          if (i < T * PPK) {
+            const int key = i / PPK, k = i - key * PPK;
+            const int32_t prow = rows[key];
+            if (prow >= 0) {
+              const uint8_t *base = p.latent + static_cast<int64_t>(prow) * RB8;
+              if (k < CP) {
+                raw[u] = __ldg(reinterpret_cast<const uint4 *>(base + 16 * k));
+                scl[u] = __ldg(reinterpret_cast<const float *>(base + L) + k / 8);
+              } else {
+                raw[u] = __ldg(reinterpret_cast<const uint4 *>(base + L + 4 * (L / 128) + 16 * (k - CP)));
+              }
+            }
+          }
+        }
+        if (!mbar_wait(kempty(st), ((t / NS) & 1) ^ 1, abort_flag, p.err)) break;
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+          const int i = pt + u * kProdThreads;
+          if (i >= T * PPK) continue;
+          const int key = i / PPK, k = i - key * PPK;
+          if (k < CP) {
+            uint4 lo, hi;
+            e4m3x16_to_bf16(raw[u], scl[u], lo, hi);
+            const uint32_t chunk = kst + (k / 4) * C::CHUNK;
+            st_shared_v4(chunk + sw128_offset(key, (k % 4) * 2), lo);
+            st_shared_v4(chunk + sw128_offset(key, (k % 4) * 2 + 1), hi);
+          } else {
+            st_shared_v4(kst + (C::NCH - 1) * C::CHUNK + sw128_offset(key, k - CP), raw[u]);
+          }
+        }
+        mbar_arrive(kfull(st));
       }
-      cp_async_mbar_arrive(kfull(st));
       j0 = j1;
       j1 = j2;
       pg0 = pg1;
@@ -579,7 +652,7 @@ __global__ void __launch_bounds__(128) attend_simt_kernel(
   }
 }
 
-template <int L>
+template <int L, bool FP8>
 cudaError_t run_tc(const dsa_ctx *ctx, const dsa_plan_t *plan, const int32_t *sel, const void *q_nope,
                    const void *q_pe, const void *latent, const float *sink, float sm_scale, void *out,
                    cudaStream_t s) {
@@ -611,7 +684,7 @@ cudaError_t run_tc(const dsa_ctx *ctx, const dsa_plan_t *plan, const int32_t *se
   prm.P = c.page_size;
   prm.num_pages = plan->cache_pages;
   prm.scale_log2 = sm_scale * kLog2e;
-  auto kern = attend_tc_kernel<L>;
+  auto kern = attend_tc_kernel<L, FP8>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
@@ -625,8 +698,9 @@ cudaError_t run_tc(const dsa_ctx *ctx, const dsa_plan_t *plan, const int32_t *se
 }  // namespace
 
 bool attend_tc_supported(const dsa_config_t &c) {
-  return c.latent_fmt == DSA_LATENT_BF16 && c.heads <= 128 && c.rope_dim == 64 &&
-         (c.kv_lora_rank == 512 || c.kv_lora_rank == 256 || c.kv_lora_rank == 128);
+  if (c.heads > 128 || c.rope_dim != 64) return false;
+  if (c.latent_fmt == DSA_LATENT_FP8_656) return c.kv_lora_rank == 512;
+  return c.kv_lora_rank == 512 || c.kv_lora_rank == 256 || c.kv_lora_rank == 128;
 }
 
 cudaError_t launch_attend(const dsa_ctx *ctx, const dsa_plan_t *plan, const int32_t *sel, const void *q_nope,
@@ -635,9 +709,14 @@ cudaError_t launch_attend(const dsa_ctx *ctx, const dsa_plan_t *plan, const int3
   const dsa_config_t &c = ctx->cfg;
   cudaError_t e;
   if (attend_tc_supported(c)) {
-    if (c.kv_lora_rank == 512) e = run_tc<512>(ctx, plan, sel, q_nope, q_pe, latent, sink, sm_scale, out, s);
-    else if (c.kv_lora_rank == 256) e = run_tc<256>(ctx, plan, sel, q_nope, q_pe, latent, sink, sm_scale, out, s);
-    else e = run_tc<128>(ctx, plan, sel, q_nope, q_pe, latent, sink, sm_scale, out, s);
+    if (c.latent_fmt == DSA_LATENT_FP8_656)
+      e = run_tc<512, true>(ctx, plan, sel, q_nope, q_pe, latent, sink, sm_scale, out, s);
+    else if (c.kv_lora_rank == 512)
+      e = run_tc<512, false>(ctx, plan, sel, q_nope, q_pe, latent, sink, sm_scale, out, s);
+    else if (c.kv_lora_rank == 256)
+      e = run_tc<256, false>(ctx, plan, sel, q_nope, q_pe, latent, sink, sm_scale, out, s);
+    else
+      e = run_tc<128, false>(ctx, plan, sel, q_nope, q_pe, latent, sink, sm_scale, out, s);
     if (e != cudaSuccess) return e;
     *launches += 1;
     if (plan->n_combine > 0) {

@@ -125,4 +125,7 @@ int indexer_ctas_per_sm(const dsa_config_t &c, int G);
 bool encode_tiled_2d(CUtensorMap *tm, CUtensorMapDataType dtype, void *base, uint64_t inner, uint64_t outer,
                      uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz);
 
+bool encode_tiled_3d(CUtensorMap *tm, CUtensorMapDataType dtype, void *base, const uint64_t dims[3],
+                     const uint64_t strides_bytes[2], const uint32_t box[3], CUtensorMapSwizzle swz);
+
 }  // namespace dsa

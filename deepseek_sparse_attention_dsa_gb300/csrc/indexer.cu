@@ -20,10 +20,12 @@
 // thread) and TMEM owner, warps 2-5 epilogue.  The grid is persistent: each
 // CTA walks a tile-balanced contiguous range of the plan's work items.
 //
-// Shapes outside the tensor-core instances (and the fp8 index format) run
-// index_simt_kernel, one CUDA-core thread per key.
+// The fp8 index format (132-byte keys) runs index_fp8_tc_kernel, the same
+// contraction behind a code -> bf16 conversion stage.  Shapes outside the
+// tensor-core instances run index_simt_kernel, one CUDA-core thread per key.
 #include <cuda_runtime.h>
 
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
 #include "dsa_internal.h"
@@ -414,10 +416,441 @@ cudaError_t run_tc(const dsa_ctx *ctx, const dsa_plan_t *plan, const IdxSet &set
   return cudaGetLastError();
 }
 
+
+// ---------------------------------------------------------------------------
+// fp8 index keys on the tensor cores.  A 132-byte key is 128 e4m3 codes and
+// one fp32 scale (LLMServingSim, "What the KV cache actually holds"), stored
+// page-blocked: [P x 128 codes][P x fp32 scale] per page.  TMA brings each
+// tile's code rows (3-D map: byte, slot, page) and scales (2-D map over the
+// scale blocks) into a staging ring; four converter warps turn the codes into
+// bf16 tiles (every e4m3 value is exactly a bf16 value), so the UMMA chain is
+// the bf16 one.  The epilogue applies the key's scale:
+//     relu(scale * d) = |scale| * relu(sign(scale) * d)
+// so s = |scale| * sum_h w_h relu(+-d_h), one multiply per key instead of one
+// per head (exact for the power-of-two scales the quantiser writes; otherwise
+// a rounding-level reassociation).
+//
+// Warp roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer, warps 2-5
+// epilogue, warps 6-9 converters (thread = key of the tile).
+// ---------------------------------------------------------------------------
+constexpr int kCvtWarps = 4;
+constexpr int kFp8Threads = 64 + 32 * kEpiWarps + 32 * kCvtWarps;
+
+template <int G>
+struct IdxF8Traits {
+  static constexpr int HI = 64, DI = 128;
+  static constexpr int N = G * HI;
+  static constexpr int CODE_BYTES = 128 * 128;           // staged codes of one tile (128-byte swizzle)
+  static constexpr int SC_BYTES = 128 * 4;               // scales of one tile
+  // Staged scales: a TMA destination in shared memory must be 128-byte
+  // aligned, so box b of a tile lands at b * max(128, 4 * BH) bytes (up to 16
+  // boxes of 8 keys: 2 KB per stage).
+  static constexpr int SC8_BYTES = 2048;
+  static constexpr int S8 = 4;                           // staging stages
+  static constexpr int KT_BYTES = 128 * DI * 2;          // converted bf16 tile: 2 swizzled 64-column chunks
+  static constexpr int QBUF = (G == 1) ? 2 : 1;
+  static constexpr int S16 = (G == 1) ? 3 : 2;           // converted stages
+  // Scale ring read by the epilogue.  The converter writes the scale of tile
+  // n only after the MMA of tile n - S16 has finished, which waited for the
+  // epilogue to release the accumulator of tile n - S16 - 2; S16 + 2 slots
+  // keep a slot alive until the epilogue of its tile has read it.
+  static constexpr int SCR = S16 + 2;
+  static constexpr int Q_BYTES = N * DI * 2;
+  static constexpr int TMEM_COLS = (2 * N <= 128) ? 128 : (2 * N <= 256) ? 256 : 512;
+  static constexpr uint32_t IDESC = mma_idesc(128, N, 1u, false, false);
+  static constexpr int OFF_C8 = 0;
+  static constexpr int OFF_K = OFF_C8 + S8 * CODE_BYTES;
+  static constexpr int OFF_Q = OFF_K + S16 * KT_BYTES;
+  static constexpr int OFF_SC8 = OFF_Q + QBUF * Q_BYTES;
+  static constexpr int OFF_SC = OFF_SC8 + S8 * SC8_BYTES;
+  static constexpr int OFF_W = OFF_SC + SCR * SC_BYTES;
+  static constexpr int OFF_BAR = OFF_W + G * HI * 4;
+  static constexpr int NBAR = 2 * S8 + 2 * S16 + 2 * QBUF + 4;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_MISC + 16 + 1024;
+  static_assert(SMEM <= 227 * 1024, "shared memory");
+  static_assert(N <= 256, "UMMA N");
+};
+
+struct IdxF8Params {
+  CUtensorMap tm_codes;     // codes as [pages][P][128] uint8, box {128, BH, 1}, 128-byte swizzle
+  CUtensorMap tm_scales;    // scales as [pages][P] fp32 (page stride P*132 bytes), box {BH, 1}
+  CUtensorMap tm_q;         // q as [T*Hi, Di] bf16, box {64, N}
+  const float *w;
+  const IdxGroup *groups;
+  const IdxItem *items;
+  const int32_t *cta_begin;
+  const int32_t *pages;
+  const int64_t *row_score_off;
+  float *scores;
+  int *err;
+  int P, BH, num_pages;
+};
+
+// e4m3 -> bf16 of the four codes of a 32-bit word (lowest byte first), two
+// bf16 per output word
+__device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t w) {
+  uint32_t o[2];
+#pragma unroll
+  for (int hlf = 0; hlf < 2; ++hlf) {
+    const __half2_raw hr =
+        __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>((w >> (16 * hlf)) & 0xFFFFu), __NV_E4M3);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
+    const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+    o[hlf] = *reinterpret_cast<const uint32_t *>(&b);
+  }
+  return make_uint2(o[0], o[1]);
+}
+
+template <int G>
+__global__ void __launch_bounds__(kFp8Threads, 1) index_fp8_tc_kernel(const __grid_constant__ IdxF8Params p) {
+  using C = IdxF8Traits<G>;
+  constexpr int HI = C::HI;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  auto c8full = [&](int s) { return bar0 + 8u * s; };
+  auto c8empty = [&](int s) { return bar0 + 8u * (C::S8 + s); };
+  auto kfull = [&](int s) { return bar0 + 8u * (2 * C::S8 + s); };
+  auto kempty = [&](int s) { return bar0 + 8u * (2 * C::S8 + C::S16 + s); };
+  auto qfull = [&](int b) { return bar0 + 8u * (2 * C::S8 + 2 * C::S16 + b); };
+  auto qempty = [&](int b) { return bar0 + 8u * (2 * C::S8 + 2 * C::S16 + C::QBUF + b); };
+  auto afull = [&](int b) { return bar0 + 8u * (2 * C::S8 + 2 * C::S16 + 2 * C::QBUF + b); };
+  auto aempty = [&](int b) { return bar0 + 8u * (2 * C::S8 + 2 * C::S16 + 2 * C::QBUF + 2 + b); };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+  float *wsm = reinterpret_cast<float *>(smem + C::OFF_W);
+  float *scr = reinterpret_cast<float *>(smem + C::OFF_SC);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = lane_id();
+  const int it0 = p.cta_begin[blockIdx.x], it1 = p.cta_begin[blockIdx.x + 1];
+  const int sc_stride = max(32, p.BH);   // floats between the staged scale boxes of a tile
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::S8; ++s) {
+      mbar_init(c8full(s), 1);
+      mbar_init(c8empty(s), 32 * kCvtWarps);
+    }
+    for (int s = 0; s < C::S16; ++s) {
+      mbar_init(kfull(s), 32 * kCvtWarps);
+      mbar_init(kempty(s), 1);
+    }
+    for (int b = 0; b < C::QBUF; ++b) {
+      mbar_init(qfull(b), 1);
+      mbar_init(qempty(b), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(afull(b), 1);
+      mbar_init(aempty(b), 32 * kEpiWarps);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&p.tm_codes);
+    tma_prefetch_desc(&p.tm_scales);
+    tma_prefetch_desc(&p.tm_q);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    int s8 = 0;
+    uint32_t ph8 = 0;
+    int qcount = 0, cur_group = -1;
+    for (int it = it0; it < it1 && !*abort_flag; ++it) {
+      const IdxItem item = p.items[it];
+      const IdxGroup g = p.groups[item.group];
+      if (item.group != cur_group) {
+        cur_group = item.group;
+        const int qb = qcount % C::QBUF;
+        const uint32_t use = qcount / C::QBUF;
+        ++qcount;
+        bool qok = true;
+        if (lane == 0) {
+          qok = mbar_wait(qempty(qb), (use & 1) ^ 1, abort_flag, p.err);
+          if (qok) {
+            mbar_arrive_expect_tx(qfull(qb), C::Q_BYTES);
+            for (int c = 0; c < C::DI / 64; ++c)
+              tma_load_2d(sbase + C::OFF_Q + qb * C::Q_BYTES + c * C::N * 128, &p.tm_q, c * 64, g.row0 * HI,
+                          qfull(qb));
+          }
+        }
+        if (__shfl_sync(0xffffffffu, qok ? 1 : 0, 0) == 0) break;
+      }
+      const int nkeys_total = g.pos0 + g.nrows;
+      // (page, slot) of this lane's box of tile t, page -1 past the tile
+      auto box_at = [&](int t, int &slot_out) -> int {
+        const int nb = (min(128, nkeys_total - t * 128) + p.BH - 1) / p.BH;
+        int page = -1;
+        slot_out = 0;
+        if (lane < nb) {
+          const int64_t slot = static_cast<int64_t>(g.page_start) + t * 128 + lane * p.BH;
+          const int64_t pi = slot / p.P;
+          if (pi < g.npages) {
+            const int pg = p.pages[g.page_off + pi];
+            if (pg >= 0 && pg < p.num_pages) {
+              page = pg;
+              slot_out = static_cast<int>(slot % p.P);
+            }
+          }
+          if (page < 0) atomicOr(p.err, kErrBounds);
+        }
+        return page;
+      };
+      int next_slot = 0;
+      int next_page = box_at(item.tile0, next_slot);
+      for (int t = item.tile0; t < item.tile1; ++t) {
+        const int nkeys = min(128, nkeys_total - t * 128);
+        const int nbox = (nkeys + p.BH - 1) / p.BH;
+        const int mypage = next_page, myslot = next_slot;
+        if (t + 1 < item.tile1) next_page = box_at(t + 1, next_slot);
+        const uint32_t valid = __ballot_sync(0xffffffffu, mypage >= 0);
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(c8empty(s8), ph8 ^ 1, abort_flag, p.err);
+        if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) break;
+        const uint32_t bytes = __popc(valid) * p.BH * (128 + 4);
+        if (lane == 0) {
+          if (bytes) mbar_arrive_expect_tx(c8full(s8), bytes);
+          else mbar_arrive(c8full(s8));
+        }
+        for (int b = 0; b < nbox; ++b) {
+          const int page = __shfl_sync(0xffffffffu, mypage, b);
+          const int slot = __shfl_sync(0xffffffffu, myslot, b);
+          if (lane == 0 && page >= 0) {
+            tma_load_3d(sbase + C::OFF_C8 + s8 * C::CODE_BYTES + b * p.BH * 128, &p.tm_codes, 0, slot, page,
+                        c8full(s8));
+            tma_load_2d(sbase + C::OFF_SC8 + s8 * C::SC8_BYTES + b * sc_stride * 4, &p.tm_scales, slot, page,
+                        c8full(s8));
+          }
+        }
+        if (++s8 == C::S8) {
+          s8 = 0;
+          ph8 ^= 1;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int st = 0;
+      uint32_t ph = 0;
+      int acc = 0;
+      uint32_t aphase = 0;
+      int qb = 0, qcount = 0, cur_group = -1;
+      bool ok = true;
+      for (int it = it0; it < it1 && ok; ++it) {
+        const IdxItem item = p.items[it];
+        if (item.group != cur_group) {
+          cur_group = item.group;
+          qb = qcount % C::QBUF;
+          const uint32_t use = qcount / C::QBUF;
+          ++qcount;
+          if (!mbar_wait(qfull(qb), use & 1, abort_flag, p.err)) break;
+        }
+        const uint32_t qaddr = sbase + C::OFF_Q + qb * C::Q_BYTES;
+        for (int t = item.tile0; t < item.tile1; ++t) {
+          if (!mbar_wait(kfull(st), ph, abort_flag, p.err)) { ok = false; break; }
+          if (!mbar_wait(aempty(acc), aphase ^ 1, abort_flag, p.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t kaddr = sbase + C::OFF_K + st * C::KT_BYTES;
+          const uint32_t d = tmem_base + acc * C::N;
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t ad = smem_desc(kaddr + c * 128 * 128 + k * 32, 16, 1024, kSwizzle128);
+              const uint64_t bd = smem_desc(qaddr + c * C::N * 128 + k * 32, 16, 1024, kSwizzle128);
+              mma_f16_ss(d, ad, bd, C::IDESC, (c | k) != 0 ? 1u : 0u);
+            }
+          }
+          mma_commit(kempty(st));
+          mma_commit(afull(acc));
+          if (++st == C::S16) {
+            st = 0;
+            ph ^= 1;
+          }
+          acc ^= 1;
+          if (acc == 0) aphase ^= 1;
+        }
+        const bool last_of_group = (it + 1 >= it1) || (p.items[it + 1].group != cur_group);
+        if (last_of_group) mma_commit(qempty(qb));
+      }
+    }
+    __syncwarp();
+  } else if (warp < 2 + kEpiWarps) {
+    // ------------------------------------------------------------ epilogue
+    const int et = threadIdx.x - 64;
+    const int quad = warp & 3;
+    const int m = quad * 32 + lane;
+    int acc = 0;
+    uint32_t aphase = 0;
+    int sc = 0;
+    int cur_group = -1;
+    int64_t soff[G];
+    int nrows = 0, pos0 = 0;
+    for (int it = it0; it < it1 && !*abort_flag; ++it) {
+      const IdxItem item = p.items[it];
+      if (item.group != cur_group) {
+        cur_group = item.group;
+        const IdxGroup g = p.groups[item.group];
+        nrows = g.nrows;
+        pos0 = g.pos0;
+        named_bar_sync(1, 32 * kEpiWarps);
+        for (int i = et; i < G * HI; i += 32 * kEpiWarps)
+          wsm[i] = (i < nrows * HI) ? p.w[static_cast<int64_t>(g.row0) * HI + i] : 0.f;
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) soff[gg] = gg < nrows ? p.row_score_off[g.row0 + gg] : 0;
+        named_bar_sync(1, 32 * kEpiWarps);
+      }
+      bool ok = true;
+      for (int t = item.tile0; t < item.tile1; ++t) {
+        if (!mbar_wait(afull(acc), aphase, abort_flag, p.err)) { ok = false; break; }
+        tc_fence_after();
+        const float scale = scr[sc * 128 + m];
+        const float mag = fabsf(scale);
+        const bool neg = scale < 0.f;
+        const int key = t * 128 + m;
+        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * C::N;
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) {
+          if (gg < nrows) {
+            float v[HI];
+#pragma unroll
+            for (int h0 = 0; h0 < HI; h0 += 16)
+              tmem_ld16(tbase + gg * HI + h0, *reinterpret_cast<float(*)[16]>(v + h0));
+            tmem_ld_wait();
+            float s = 0.f;
+            if (!neg) {
+#pragma unroll
+              for (int h = 0; h < HI; ++h) s = fmaf(wsm[gg * HI + h], fmaxf(v[h], 0.f), s);
+            } else {
+#pragma unroll
+              for (int h = 0; h < HI; ++h) s = fmaf(wsm[gg * HI + h], fmaxf(-v[h], 0.f), s);
+            }
+            if (key <= pos0 + gg) p.scores[soff[gg] + key] = s * mag;
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(aempty(acc));
+        acc ^= 1;
+        if (acc == 0) aphase ^= 1;
+        if (++sc == C::SCR) sc = 0;
+      }
+      if (!ok) break;
+    }
+  } else {
+    // ------------------------------------------------------------ converters
+    // thread c converts key c of each tile: its 128 codes (staged with the
+    // 128-byte swizzle) become 256 bytes of bf16 in two swizzled 64-column
+    // chunks, the layout TMA gives a bf16 tile
+    const int c = threadIdx.x - (64 + 32 * kEpiWarps);
+    int s8 = 0, st = 0, sc = 0;
+    uint32_t ph8 = 0, ph = 0;
+    for (int it = it0; it < it1 && !*abort_flag; ++it) {
+      const IdxItem item = p.items[it];
+      bool ok = true;
+      for (int t = item.tile0; t < item.tile1; ++t) {
+        if (!mbar_wait(c8full(s8), ph8, abort_flag, p.err)) { ok = false; break; }
+        const uint8_t *src = smem + C::OFF_C8 + s8 * C::CODE_BYTES + c * 128;
+        uint4 in[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) in[i] = *reinterpret_cast<const uint4 *>(src + ((i ^ (c & 7)) << 4));
+        const float scale = reinterpret_cast<const float *>(smem + C::OFF_SC8 + s8 * C::SC8_BYTES)
+            [(c / p.BH) * sc_stride + c % p.BH];
+        mbar_arrive(c8empty(s8));
+        if (++s8 == C::S8) {
+          s8 = 0;
+          ph8 ^= 1;
+        }
+        if (!mbar_wait(kempty(st), ph ^ 1, abort_flag, p.err)) { ok = false; break; }
+        const uint32_t row = sbase + C::OFF_K + st * C::KT_BYTES + c * 128;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          // codes 16i .. 16i+15 -> bf16 columns 16i .. 16i+15: chunk (16i)/64,
+          // 16-byte pieces 2(i%4) and 2(i%4)+1 of the row
+          const uint2 a = e4m3x4_to_bf16x4(in[i].x), b = e4m3x4_to_bf16x4(in[i].y);
+          const uint2 e = e4m3x4_to_bf16x4(in[i].z), f = e4m3x4_to_bf16x4(in[i].w);
+          const uint32_t chunk = row + (i / 4) * (128 * 128);
+          const int piece = 2 * (i % 4);
+          st_shared_v4(chunk + ((piece ^ (c & 7)) << 4), make_uint4(a.x, a.y, b.x, b.y));
+          st_shared_v4(chunk + (((piece + 1) ^ (c & 7)) << 4), make_uint4(e.x, e.y, f.x, f.y));
+        }
+        scr[sc * 128 + c] = scale;
+        fence_proxy_async_smem();
+        mbar_arrive(kfull(st));
+        if (++st == C::S16) {
+          st = 0;
+          ph ^= 1;
+        }
+        if (++sc == C::SCR) sc = 0;
+      }
+      if (!ok) break;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+}
+
+template <int G>
+cudaError_t run_fp8(const dsa_ctx *ctx, const dsa_plan_t *plan, const IdxSet &set, const void *q, const float *w,
+                    const void *cache, float *scores, cudaStream_t s, int BH) {
+  using C = IdxF8Traits<G>;
+  const dsa_config_t &c = ctx->cfg;
+  IdxF8Params prm{};
+  const uint64_t P = static_cast<uint64_t>(c.page_size);
+  {
+    const uint64_t dims[3] = {128, P, static_cast<uint64_t>(plan->cache_pages)};
+    const uint64_t strides[2] = {128, P * 132};
+    const uint32_t box[3] = {128, static_cast<uint32_t>(BH), 1};
+    if (!encode_tiled_3d(&prm.tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<void *>(cache), dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  if (!encode_tiled_2d(&prm.tm_scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                       static_cast<uint8_t *>(const_cast<void *>(cache)) + P * 128, P, plan->cache_pages, P * 132,
+                       BH, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  if (!encode_tiled_2d(&prm.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void *>(q), C::DI,
+                       static_cast<uint64_t>(plan->T) * C::HI, C::DI * 2, 64, C::N, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  prm.w = w;
+  prm.groups = set.groups;
+  prm.items = set.items;
+  prm.cta_begin = set.cta_begin;
+  prm.pages = plan->pages;
+  prm.row_score_off = plan->row_score_off;
+  prm.scores = scores;
+  prm.err = ctx->err;
+  prm.P = c.page_size;
+  prm.BH = BH;
+  prm.num_pages = plan->cache_pages;
+  auto kern = index_fp8_tc_kernel<G>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  kern<<<set.n_ctas, kFp8Threads, C::SMEM, s>>>(prm);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 bool indexer_tc_supported(const dsa_config_t &c, int G) {
-  if (c.index_fmt != DSA_INDEX_BF16) return false;
+  if (c.index_fmt == DSA_INDEX_FP8_132)
+    return c.index_heads == 64 && c.index_dim == 128 && c.page_size % 8 == 0 && (G == 1 || G == 4);
   if (c.index_heads == 64 && c.index_dim == 128) return G == 1 || G == 4;
   if (c.index_heads == 4 && c.index_dim == 32) return G == 1 || G == 4;
   return false;
@@ -436,7 +869,10 @@ cudaError_t launch_index_scores(const dsa_ctx *ctx, const dsa_plan_t *plan, cons
     if (set.n_items == 0) continue;
     const bool tc = indexer_tc_supported(c, set.G) && BH >= 8;
     cudaError_t e = cudaSuccess;
-    if (tc) {
+    if (tc && c.index_fmt == DSA_INDEX_FP8_132) {
+      e = set.G == 1 ? run_fp8<1>(ctx, plan, set, q, w, cache, scores, s, BH)
+                     : run_fp8<4>(ctx, plan, set, q, w, cache, scores, s, BH);
+    } else if (tc) {
       if (c.index_heads == 64 && set.G == 1) e = run_tc<64, 128, 1>(ctx, plan, set, q, w, cache, scores, s, BH);
       else if (c.index_heads == 64) e = run_tc<64, 128, 4>(ctx, plan, set, q, w, cache, scores, s, BH);
       else if (set.G == 1) e = run_tc<4, 32, 1>(ctx, plan, set, q, w, cache, scores, s, BH);

@@ -94,6 +94,12 @@ def test_fp8_formats():
     _run(H.deepseek_small(seed=5, fp8=True, sink=True, decode_ctx=(2200, 2900), chunk=(2030, 24)))
 
 
+def test_fp8_page_start_ragged():
+    """fp8 keys and latents with spans starting mid-page, a context shorter than
+    one key tile and chunks whose tails leave partial tiles and groups."""
+    _run(H.deepseek_small(seed=7, fp8=True, page_start=8, decode_ctx=(2049, 130, 4097), chunk=(1990, 70)))
+
+
 def test_topk_from_oracle_scores_is_exact():
     """Given the oracle's own fp32 scores, the GPU selection is the oracle's set exactly."""
     for wl in (W.config(0), H.deepseek_small(seed=6, decode_ctx=(9000, 2049, 2048, 100), chunk=(2000, 100))):
