@@ -7,30 +7,35 @@
 // is the leading kv_lora_rank columns of the same latent row, and an optional
 // per-head sink joins only the softmax denominator).
 //
-// Tensor-core kernel (bf16 latents, H <= 128, kv_lora_rank in {128, 256,
-// 512}, rope 64).  One CTA per (row, key range, output half c): it computes
-// the full logits of all 128 heads and accumulates O for latent columns
-// [c*L/2, (c+1)*L/2), so the two halves of a row share nothing but their
-// inputs (the QK contraction is done by both; in exchange no CTA ever waits on
-// another).  Per tile of 32 selected keys (four tiles in flight):
-//   * 7 producer warps gather the tile's latent rows through the page table
-//     (cp.async into 128-byte swizzled tiles; completion lands on an mbarrier;
-//     the page-table lookups of the next tiles are already in flight);
-//   * one thread issues S = Q . C^T (M = 128 heads, N = 32 keys, K = L + R,
-//     fp32 in TMEM); the first columns of Q live in TMEM (the MMA's A operand
-//     from tensor memory), the rest in shared memory;
-//   * 4 softmax warps (thread = head) run a base-2 online softmax whose
-//     reference max moves only when it grows by more than 2^8 (so O is rarely
-//     rescaled) and write P as bf16 over the S tile in TMEM;
-//   * one thread issues O += P . C[:, half] (A = P from TMEM, B = the gathered
-//     tile read MN-major; M = 128, N = L/2, fp32 in TMEM).
-// S is double-buffered in TMEM so QK of tile t+1 overlaps the softmax of tile t.
-// Rows split over several key ranges write fp32 partials (O, max, sum) that
-// attend_combine_kernel merges.
+// Tensor-core kernel (H <= 128, kv_lora_rank in {128, 256, 512}, rope 64): a
+// cluster of two CTAs handles one (row, key range).  CTA c owns latent
+// columns [c*L/2, (c+1)*L/2) and rope columns [32c, 32c+32), so every latent
+// byte is gathered once and every MMA is issued once.  Per tile of 64 selected
+// keys, four tiles in flight:
+//   * 7 producer warps gather the CTA's 576 bytes of each latent row through
+//     the page table (cp.async into 128- and 64-byte swizzled tiles;
+//     completion lands on an mbarrier; the selection entries and page ids of
+//     the next tiles are already in flight).  fp8 latents (656-byte rows) are
+//     loaded into registers, dequantised (code x the scale of its 128-column
+//     group, rounded to bf16) and stored as the same bf16 tiles;
+//   * one thread issues the partial logits S_c = Q[:, cols_c] . C[:, cols_c]^T
+//     (M = 128 heads, N = 64 keys, fp32 in TMEM; the q_nope columns of this
+//     CTA live in tensor memory as the A operand, the rope columns in shared
+//     memory).  A K = 16 tcgen05.mma costs about the same for N = 32 as for
+//     N = 64 on sm_103a, so splitting the contraction between the pair halves
+//     the instruction count per key where duplicating it would double it;
+//   * 4 softmax warps (thread = head) swap the partial logits with the partner
+//     through distributed shared memory (st.async landing on the partner's
+//     mbarrier, double-buffered), so both CTAs hold the identical full S and
+//     run the same base-2 online softmax (the reference max moves only when
+//     it grows by more than 2^8, so O is rarely rescaled); P goes to TMEM as
+//     bf16 over the S tile it came from;
+//   * one thread issues O_c += P . C[:, cols_c] (A = P from TMEM, B = the
+//     gathered tile read MN-major; M = 128, N = L/2, fp32 in TMEM).
+// S is double-buffered in TMEM so QK of tile t+1 overlaps the softmax of tile
+// t.  Rows split over several key ranges write fp32 partials (O, max, sum)
+// that attend_combine_kernel merges.
 //
-// fp8 latents (656-byte rows) take the same kernel: the producers load the
-// codes, scales and rope into registers, dequantise (code x the scale of its
-// 128-column group, rounded to bf16) and store the bf16 tile the MMAs read.
 // Other shapes run attend_simt_kernel.
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -56,43 +61,46 @@ constexpr int kAttThreads = 12 * 32;
 template <int L>
 struct AttTraits {
   static constexpr int R = 64;
-  static constexpr int HALF = L / 2;                     // output columns per CTA
-  static constexpr int NPV = HALF / 64;                  // 64-column chunks of the output half
-  static constexpr int NCH = (L + R) / 64;               // 64-column chunks of a latent row
-  static constexpr int TILE = 32;                        // keys per tile (UMMA N of QK)
-  static constexpr int CHUNK = TILE * 128;               // [32 keys x 64 cols] bf16, 128-byte swizzle
-  static constexpr int STAGE = NCH * CHUNK;
+  static constexpr int HALF = L / 2;                     // latent (and output) columns per CTA
+  static constexpr int NPV = HALF / 64;                  // 64-column chunks of those
+  static constexpr int RH = R / 2;                       // rope columns per CTA
+  static constexpr int TILE = kAttTile;                  // keys per tile (UMMA N of QK)
+  static constexpr int CHUNK = TILE * 128;               // [64 keys x 64 cols] bf16, 128-byte swizzle
+  static constexpr int RCHUNK = TILE * 64;               // [64 keys x 32 rope cols], 64-byte swizzle
+  static constexpr int STAGE = NPV * CHUNK + RCHUNK;
   static constexpr int STAGES = 4;
-  // tensor memory: [Q columns held in TMEM | S tile 0 | S tile 1 | O half]
-  static constexpr int S_COLS = 2 * TILE;
-  static constexpr int QT_CH_MAX = (512 - HALF - S_COLS) / 32;  // 64-column Q chunks that fit
-  static constexpr int QT_CH = QT_CH_MAX < L / 64 ? QT_CH_MAX : L / 64;  // q_nope chunks only
-  static constexpr uint32_t S_COL = QT_CH * 32;
-  static constexpr uint32_t O_COL = S_COL + S_COLS;
-  static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr int QS_CH = NCH - QT_CH;              // Q chunks in shared memory
+  static constexpr int PIECES = NPV * 8 + 4;             // 16-byte pieces of a key's part
   static constexpr int QCHUNK = 128 * 128;               // [128 heads x 64 cols]
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + QS_CH * QCHUNK;
-  static constexpr int OFF_ROWS = OFF_K + STAGES * STAGE;  // int32 [STAGES][TILE]
+  static constexpr int QRBYTES = 128 * 64;               // [128 heads x 32 rope cols]
+  static constexpr int XBYTES = 128 * TILE * 4;          // partial logits of a tile, fp32
+  // tensor memory: [q_nope columns of this CTA | S tile 0 | S tile 1 | O]
+  static constexpr uint32_t S_COL = 128;
+  static constexpr uint32_t O_COL = 256;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr int OFF_QR = 0;
+  static constexpr int OFF_K = 8192;
+  static constexpr int OFF_X = OFF_K + STAGES * STAGE;   // x_in, x_out: [128 heads][64 keys] fp32 each
+  static constexpr int OFF_ROWS = OFF_X + 2 * XBYTES;    // int32 [STAGES][TILE]
   static constexpr int OFF_BAR = OFF_ROWS + STAGES * TILE * 4;
-  static constexpr int NBAR = 20;
+  static constexpr int NBAR = 24;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;
   static constexpr uint32_t IDESC_QK = mma_idesc(128, TILE, 1u, false, false);
   static constexpr uint32_t IDESC_PV = mma_idesc(128, HALF, 1u, false, true);
   static_assert(HALF % 64 == 0 && HALF <= 256, "latent width");
-  static_assert(O_COL + HALF <= TMEM_COLS, "tensor memory");
-  static_assert(QT_CH * QCHUNK <= STAGES * STAGE, "Q staging");
+  static_assert(NPV * 32 <= static_cast<int>(S_COL), "tensor memory: q_nope columns");
+  static_assert(O_COL + HALF <= TMEM_COLS, "tensor memory: O");
+  static_assert(QRBYTES <= OFF_K && STAGE % 1024 == 0, "alignment");
+  static_assert(NPV * QCHUNK <= STAGES * STAGE, "Q staging");
+  static_assert(NBAR >= 14 + 2 * STAGES, "barriers");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
 struct AttParams {
   CUtensorMap tm_qn;       // q_nope as [T*H, L] bf16, box {64, 128}, 128-byte swizzle
-  CUtensorMap tm_qp;       // q_pe as [T*H, R] bf16, box {64, 128}, 128-byte swizzle
+  CUtensorMap tm_qp;       // q_pe as [T*H, R] bf16, box {32, 128}, 64-byte swizzle
   const int32_t *sel;
-  const uint8_t *latent;   // [pages*P][L+R] bf16
-  const __nv_bfloat16 *q_nope;
+  const uint8_t *latent;   // bf16 rows [L+R] or fp8 656-byte rows, [pages*P]
   const float *sink;
   const AttUnit *units;
   const int32_t *row_pos, *row_page_off, *row_npages, *row_page_start, *pages;
@@ -124,6 +132,14 @@ __device__ __forceinline__ void e4m3x16_to_bf16(const uint4 raw, float scale, ui
   hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
+// 2^x with the MUFU approximation (relative error ~2^-22; tiny results flush
+// to zero, which the bf16 probabilities would round to anyway).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Physical latent row of selection entry j for a row, or -1 (masked).  -1 is
 // the padding value; any other value outside 0..pos is a bounds error.
 __device__ __forceinline__ int64_t latent_row(int j, int pos, int page_off, int npages, int page_start,
@@ -147,29 +163,31 @@ __device__ __forceinline__ int64_t latent_row(int j, int pos, int page_off, int 
 }
 
 template <int L, bool FP8>
-__global__ void __launch_bounds__(kAttThreads, 1) attend_tc_kernel(const __grid_constant__ AttParams p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
+    attend_tc_kernel(const __grid_constant__ AttParams p) {
   using C = AttTraits<L>;
   constexpr int R = C::R;
-  constexpr int ROWB = (L + R) * 2;        // bytes per latent row
   constexpr int T = C::TILE;
   constexpr int NS = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + C::OFF_BAR;
-  const uint32_t b_qsfull = bar0 + 0, b_qtfull = bar0 + 8, b_qtdone = bar0 + 16;
-  auto kfull = [&](int s) { return bar0 + 8u * (3 + s); };
-  auto kempty = [&](int s) { return bar0 + 8u * (3 + NS + s); };
-  auto sfull = [&](int b) { return bar0 + 8u * (3 + 2 * NS + b); };
-  auto sempty = [&](int b) { return bar0 + 8u * (5 + 2 * NS + b); };
-  auto pfull = [&](int b) { return bar0 + 8u * (7 + 2 * NS + b); };
-  const uint32_t b_pvdone = bar0 + 8u * (9 + 2 * NS);
+  const uint32_t b_qsfull = bar0, b_qtfull = bar0 + 8, b_qtdone = bar0 + 16, b_pvdone = bar0 + 24;
+  auto kfull = [&](int s) { return bar0 + 8u * (4 + s); };
+  auto kempty = [&](int s) { return bar0 + 8u * (4 + NS + s); };
+  auto sfull = [&](int b) { return bar0 + 8u * (4 + 2 * NS + b); };
+  auto sempty = [&](int b) { return bar0 + 8u * (6 + 2 * NS + b); };
+  auto pfull = [&](int b) { return bar0 + 8u * (8 + 2 * NS + b); };
+  const uint32_t b_xfull = bar0 + 8u * (10 + 2 * NS);   // the partner's partial landed in x_in
+  const uint32_t b_xfree = bar0 + 8u * (11 + 2 * NS);   // the partner has read what we sent
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
   int32_t *rows_sm = reinterpret_cast<int32_t *>(smem + C::OFF_ROWS);
 
   const int warp = threadIdx.x / 32, lane = lane_id();
-  const int half = blockIdx.x & 1;
+  const uint32_t crank = cluster_rank();
+  const uint32_t peer = crank ^ 1u;
   const AttUnit unit = p.units[blockIdx.x >> 1];
   const int row = unit.row;
   const int pos = p.row_pos[row];
@@ -181,6 +199,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_tc_kernel(const __grid_
     mbar_init(b_qsfull, 1);
     mbar_init(b_qtfull, 1);
     mbar_init(b_qtdone, 128);
+    mbar_init(b_pvdone, 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(kfull(s), kProdThreads);
       mbar_init(kempty(s), 1);
@@ -190,7 +209,8 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_tc_kernel(const __grid_
       mbar_init(sempty(b), 1);
       mbar_init(pfull(b), 128);
     }
-    mbar_init(b_pvdone, 1);
+    mbar_init(b_xfull, 1);   // armed locally with the tile's bytes, filled by the partner's bulk copy
+    mbar_init(b_xfree, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -199,31 +219,29 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_tc_kernel(const __grid_
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();   // both CTAs' barriers exist before any remote arrival
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      // Q columns kept in shared memory, and (through the still idle stage
-      // buffers) the columns the softmax warps move into tensor memory
-      mbar_arrive_expect_tx(b_qsfull, C::QS_CH * C::QCHUNK);
-      for (int ch = C::QT_CH; ch < C::NCH; ++ch) {
-        const uint32_t dst = sbase + C::OFF_Q + (ch - C::QT_CH) * C::QCHUNK;
-        if (ch * 64 < L) tma_load_2d(dst, &p.tm_qn, ch * 64, row * p.H, b_qsfull);
-        else tma_load_2d(dst, &p.tm_qp, ch * 64 - L, row * p.H, b_qsfull);
-      }
-      mbar_arrive_expect_tx(b_qtfull, C::QT_CH * C::QCHUNK);
-      for (int ch = 0; ch < C::QT_CH; ++ch)
-        tma_load_2d(sbase + C::OFF_K + ch * C::QCHUNK, &p.tm_qn, ch * 64, row * p.H, b_qtfull);
+      // rope columns of Q into shared memory; the q_nope columns (through the
+      // still idle stage buffers) for the softmax warps to move into TMEM
+      mbar_arrive_expect_tx(b_qsfull, C::QRBYTES);
+      tma_load_2d(sbase + C::OFF_QR, &p.tm_qp, static_cast<int>(crank) * C::RH, row * p.H, b_qsfull);
+      mbar_arrive_expect_tx(b_qtfull, C::NPV * C::QCHUNK);
+      for (int ch = 0; ch < C::NPV; ++ch)
+        tma_load_2d(sbase + C::OFF_K + ch * C::QCHUNK, &p.tm_qn, static_cast<int>(crank) * C::HALF + ch * 64,
+                    row * p.H, b_qtfull);
       bool ok = mbar_wait(b_qsfull, 0, abort_flag, p.err) && mbar_wait(b_qtdone, 0, abort_flag, p.err);
       const uint32_t o_tmem = tmem_base + C::O_COL;
-      // descriptors are built once; a K step of 16 columns (32 bytes) adds 2 to
-      // the encoded start address, a chunk adds chunk_bytes / 16
-      const uint64_t qdesc = smem_desc(sbase + C::OFF_Q, 16, 1024, kSwizzle128);
+      // descriptors are built once; a K step of 16 columns adds 32 bytes (2
+      // encoded), a stage adds STAGE / 16
+      const uint64_t qrdesc = smem_desc(sbase + C::OFF_QR, 16, 512, kSwizzle64);
       const uint64_t kdesc0 = smem_desc(sbase + C::OFF_K, 16, 1024, kSwizzle128);
-      const uint64_t vdesc0 = smem_desc(sbase + C::OFF_K + half * C::NPV * C::CHUNK, C::CHUNK, 1024, kSwizzle128);
+      const uint64_t krdesc0 = smem_desc(sbase + C::OFF_K + C::NPV * C::CHUNK, 16, 512, kSwizzle64);
+      const uint64_t vdesc0 = smem_desc(sbase + C::OFF_K, C::CHUNK, 1024, kSwizzle128);
       constexpr uint64_t kStageStep = C::STAGE >> 4;
       // issue QK of the next tile or PV of the oldest softmaxed tile, whichever is ready
       int nq = 0, np = 0;
@@ -234,22 +252,19 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_tc_kernel(const __grid_
         if (nq < ntiles && nq < np + 2) {
           const int st = nq % NS, sb = nq & 1;
           if (mbar_test(kfull(st), (nq / NS) & 1) && mbar_test(sempty(sb), ((nq >> 1) & 1) ^ 1)) {
-            fence_proxy_async_smem();   // the gathered tile (cp.async writes) feeds the tensor core
+            fence_proxy_async_smem();   // the gathered tile feeds the tensor core
             tc_fence_after();
             const uint32_t s_tmem = tmem_base + C::S_COL + sb * T;
-            const uint64_t kd = kdesc0 + st * kStageStep;
+            const uint64_t kd = kdesc0 + st * kStageStep, krd = krdesc0 + st * kStageStep;
 #pragma unroll
-            for (int ch = 0; ch < C::QT_CH; ++ch)       // Q columns in tensor memory
+            for (int ch = 0; ch < C::NPV; ++ch)          // q_nope columns in tensor memory
 #pragma unroll
               for (int k = 0; k < 4; ++k)
                 mma_f16_ts(s_tmem, tmem_base + ch * 32 + k * 8, kd + (ch * C::CHUNK >> 4) + 2 * k, C::IDESC_QK,
                            (ch | k) ? 1u : 0u);
 #pragma unroll
-            for (int ch = C::QT_CH; ch < C::NCH; ++ch)   // Q columns in shared memory
-#pragma unroll
-              for (int k = 0; k < 4; ++k)
-                mma_f16_ss(s_tmem, qdesc + ((ch - C::QT_CH) * C::QCHUNK >> 4) + 2 * k,
-                           kd + (ch * C::CHUNK >> 4) + 2 * k, C::IDESC_QK, (ch | k) ? 1u : 0u);
+            for (int k = 0; k < 2; ++k)                  // rope columns in shared memory
+              mma_f16_ss(s_tmem, qrdesc + 2 * k, krd + 2 * k, C::IDESC_QK, 1u);
             mma_commit(sfull(sb));
             ++nq;
             progressed = true;
@@ -272,7 +287,11 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_tc_kernel(const __grid_
         if (progressed) {
           idle = 0;
           idle_since = 0;
-        } else if ((++idle & 255) == 0) {
+        } else {
+          ++idle;
+          __nanosleep(32);   // leave the issue slots to the softmax warp on this sub-partition
+        }
+        if (!progressed && (idle & 255) == 0) {
           if (*abort_flag) break;
           if (idle_since == 0) idle_since = globaltimer();
           else if (globaltimer() - idle_since > kWaitLimitNs) {
@@ -286,16 +305,15 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_tc_kernel(const __grid_
     __syncwarp();
   } else if (warp < kSoftWarp0) {
     // ------------------------------------------------------------ producers
-    // Three warps copy each tile with cp.async: eight lanes per 128-byte chunk
-    // of a latent row, 128-byte swizzled into the tile; the arrival on the
-    // stage's mbarrier fires when this thread's copies have landed.  Warp 1
-    // resolves the tile's rows (lane l: key l); the selection entries of tile
-    // t+2 and the page ids of tile t+1 are loaded while tile t is issued.
+    // Warps 1-2 resolve the tile's rows (key = 32 * (warp - 1) + lane); the
+    // selection entries of tile t+2 and the page ids of tile t+1 are loaded
+    // while tile t is issued.
     const int pt = threadIdx.x - 32 * kProdWarp0;  // 0..223
     const int page_off = p.row_page_off[row], npages = p.row_npages[row], page_start = p.row_page_start[row];
-    const bool resolver = warp == kProdWarp0;
+    const bool resolver = warp < kProdWarp0 + 2;
+    const int rkey = (warp - kProdWarp0) * 32 + lane;
     auto sel_at = [&](int t) -> int {
-      const int e = t * T + lane;
+      const int e = t * T + rkey;
       return (resolver && t < ntiles && e < nent) ? selrow[e] : -1;
     };
     auto page_of = [&](int j) -> int {
@@ -314,36 +332,44 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_tc_kernel(const __grid_
     };
     int j0 = sel_at(0), j1 = sel_at(1);
     int pg0 = page_of(j0);
-    const int piece = lane & 7, sub = pt >> 3;        // sub: one 128-byte chunk per 8 lanes
-    // the stage buffers hold the tensor-memory part of Q until it has been moved
+    // the stage buffers hold the q_nope columns of Q until they have been moved
+    // Every exit from the tile loop is decided at the named barrier (an OR
+    // over the producers), so no producer is left waiting there alone.
     bool ok = mbar_wait(b_qtdone, 0, abort_flag, p.err);
-    for (int t = 0; ok && t < ntiles; ++t) {
+    for (int t = 0; t < ntiles; ++t) {
       const int st = t % NS;
       const int pg1 = page_of(j1);
       const int j2 = sel_at(t + 2);
-      if (!FP8 && !mbar_wait(kempty(st), ((t / NS) & 1) ^ 1, abort_flag, p.err)) break;
+      if (!FP8 && ok) ok = mbar_wait(kempty(st), ((t / NS) & 1) ^ 1, abort_flag, p.err);
       int32_t *rows = rows_sm + st * T;
-      if (resolver) rows[lane] = phys(j0, pg0);
-      named_bar_sync(2, kProdThreads);
+      if (resolver && ok) rows[rkey] = phys(j0, pg0);
+      if (named_bar_any(2, kProdThreads, !ok)) break;
       const uint32_t kst = sbase + C::OFF_K + st * C::STAGE;
       if constexpr (!FP8) {
-        // chunk q = key * NCH + ch: consecutive q are consecutive chunks of one row
-#pragma unroll 4
-        for (int q = sub; q < T * C::NCH; q += kProdThreads / 8) {
-          const int key = q / C::NCH, ch = q - key * C::NCH;
+        constexpr int ROWB = (L + R) * 2;
+        // piece q of a key: this CTA's q_nope columns, then its rope columns
+        for (int idx = pt; idx < T * C::PIECES; idx += kProdThreads) {
+          const int key = idx / C::PIECES, piece = idx - key * C::PIECES;
           const int32_t prow = rows[key];
-          const uint32_t dst = kst + ch * C::CHUNK + sw128_offset(key, piece);
-          const uint8_t *src =
-              p.latent + (prow >= 0 ? static_cast<int64_t>(prow) * ROWB + ch * 128 + piece * 16 : 0);
+          uint32_t dst;
+          int off;
+          if (piece < C::NPV * 8) {
+            dst = kst + (piece >> 3) * C::CHUNK + sw128_offset(key, piece & 7);
+            off = static_cast<int>(crank) * C::HALF * 2 + piece * 16;
+          } else {
+            dst = kst + C::NPV * C::CHUNK + sw64_offset(key, piece - C::NPV * 8);
+            off = L * 2 + static_cast<int>(crank) * C::RH * 2 + (piece - C::NPV * 8) * 16;
+          }
+          const uint8_t *src = p.latent + (prow >= 0 ? static_cast<int64_t>(prow) * ROWB + off : 0);
           cp_async_16_zfill(dst, src, prow >= 0 ? 16u : 0u);
         }
         cp_async_mbar_arrive(kfull(st));
       } else {
-        // 656-byte rows [L e4m3 | L/128 fp32 scales | R bf16]: 16-byte pieces are
-        // loaded into registers, dequantised (code x scale, rounded to bf16) and
-        // stored into the same swizzled bf16 tile the bf16 path gathers.  The
-        // loads are issued before the stage is known to be free.
-        constexpr int CP = L / 16, RP = R * 2 / 16, PPK = CP + RP;
+        // 656-byte rows [L e4m3 | L/128 fp32 scales | R bf16]: this CTA's
+        // codes (HALF/16 pieces) and rope half (4 pieces) are loaded into
+        // registers before the stage is known to be free, dequantised (code x
+        // scale, rounded to bf16) and stored as the bf16 tile.
+        constexpr int CPH = C::HALF / 16, RP = 4, PPK = CPH + RP;
         constexpr int RB8 = L + 4 * (L / 128) + 2 * R;
         constexpr int PER = (T * PPK + kProdThreads - 1) / kProdThreads;
         uint4 raw[PER];
@@ -358,32 +384,35 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_tc_kernel(const __grid_
             const int32_t prow = rows[key];
             if (prow >= 0) {
               const uint8_t *base = p.latent + static_cast<int64_t>(prow) * RB8;
-              if (k < CP) {
-                raw[u] = __ldg(reinterpret_cast<const uint4 *>(base + 16 * k));
-                scl[u] = __ldg(reinterpret_cast<const float *>(base + L) + k / 8);
+              if (k < CPH) {
+                raw[u] = __ldg(reinterpret_cast<const uint4 *>(base + static_cast<int>(crank) * C::HALF + 16 * k));
+                scl[u] = __ldg(reinterpret_cast<const float *>(base + L) + (static_cast<int>(crank) * C::HALF) / 128 +
+                               k / 8);
               } else {
-                raw[u] = __ldg(reinterpret_cast<const uint4 *>(base + L + 4 * (L / 128) + 16 * (k - CP)));
+                raw[u] = __ldg(reinterpret_cast<const uint4 *>(base + L + 4 * (L / 128) +
+                                                               static_cast<int>(crank) * C::RH * 2 + 16 * (k - CPH)));
               }
             }
           }
         }
-        if (!mbar_wait(kempty(st), ((t / NS) & 1) ^ 1, abort_flag, p.err)) break;
+        ok = mbar_wait(kempty(st), ((t / NS) & 1) ^ 1, abort_flag, p.err);
 #pragma unroll
         for (int u = 0; u < PER; ++u) {
           const int i = pt + u * kProdThreads;
-          if (i >= T * PPK) continue;
+          if (!ok || i >= T * PPK) continue;
           const int key = i / PPK, k = i - key * PPK;
-          if (k < CP) {
+          if (k < CPH) {
             uint4 lo, hi;
             e4m3x16_to_bf16(raw[u], scl[u], lo, hi);
             const uint32_t chunk = kst + (k / 4) * C::CHUNK;
             st_shared_v4(chunk + sw128_offset(key, (k % 4) * 2), lo);
             st_shared_v4(chunk + sw128_offset(key, (k % 4) * 2 + 1), hi);
           } else {
-            st_shared_v4(kst + (C::NCH - 1) * C::CHUNK + sw128_offset(key, k - CP), raw[u]);
+            st_shared_v4(kst + C::NPV * C::CHUNK + sw64_offset(key, k - CPH), raw[u]);
           }
         }
-        mbar_arrive(kfull(st));
+        fence_proxy_async_smem();
+        if (ok) mbar_arrive(kfull(st));
       }
       j0 = j1;
       j1 = j2;
@@ -395,12 +424,16 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_tc_kernel(const __grid_
     const int quad = warp & 3;
     const int h = quad * 32 + lane;                      // head = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t x_in = sbase + C::OFF_X, x_out = sbase + C::OFF_X + C::XBYTES;
+    const uint32_t peer_x_in = map_to_cta(x_in, peer);
+    const uint32_t peer_xfull = map_to_cta(b_xfull, peer), peer_xfree = map_to_cta(b_xfree, peer);
+    volatile int *early_flag = abort_flag + 1;
     bool ok = mbar_wait(b_qtfull, 0, abort_flag, p.err);
     if (ok) {
-      // this head's row of the tensor-memory part of Q: from the staged
-      // swizzled chunks into TMEM (bf16 pairs, lower column in the low half)
+      // this head's row of the q_nope columns: from the staged swizzled
+      // chunks into TMEM (bf16 pairs, lower column in the low half)
 #pragma unroll 1
-      for (int ch = 0; ch < C::QT_CH; ++ch) {
+      for (int ch = 0; ch < C::NPV; ++ch) {
         const uint8_t *src = smem + C::OFF_K + ch * C::QCHUNK + h * 128;
         uint32_t v[32];
 #pragma unroll
@@ -418,50 +451,141 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_tc_kernel(const __grid_
     tc_fence_before();
     mbar_arrive(b_qtdone);
     float m_ref = kNegBig, l = 0.f;
-    int jn = lane < nent ? selrow[lane] : -1;
-    for (int t = 0; t < ntiles && ok; ++t) {
-      const uint32_t valid = __ballot_sync(0xffffffffu, jn >= 0 && jn <= pos);
+    int jn0 = lane < nent ? selrow[lane] : -1;
+    int jn1 = 32 + lane < nent ? selrow[32 + lane] : -1;
+    // This CTA's partial logits of tile u are staged in x_out (row h, 16-byte
+    // chunks swizzled by h) and copied by the bulk-copy engine into the
+    // partner's x_in once the partner has read tile u-1 from it.  Tile t+1 is
+    // sent before the softmax of tile t when its QK is already done, so the
+    // transfer overlaps the math; otherwise right after it.
+    // Exits are decided at the named barriers of the 128 softmax threads (an
+    // OR of their failures), so no thread is left waiting there alone.
+    auto send_partial = [&](int u) {
+      const int b = u & 1;
+      bool good = ok && mbar_wait(sfull(b), (u >> 1) & 1, abort_flag, p.err);
+      if (good) tc_fence_after();
+      if (h == 0 && good) bulk_wait_read_all();   // the copy of tile u-1 has read x_out
+      if (named_bar_any(3, 128, !good)) {
+        ok = false;
+        return;
+      }
+      float v[T];
+#pragma unroll
+      for (int c0 = 0; c0 < T; c0 += 16)
+        tmem_ld16(tmem_base + lane_base + C::S_COL + b * T + c0, *reinterpret_cast<float(*)[16]>(v + c0));
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < T / 4; ++c)
+        st_shared_v4(x_out + h * 256 + ((c ^ (h & 15)) << 4),
+                     make_uint4(__float_as_uint(v[4 * c]), __float_as_uint(v[4 * c + 1]), __float_as_uint(v[4 * c + 2]),
+                                __float_as_uint(v[4 * c + 3])));
+      fence_proxy_async_smem();
+      named_bar_sync(3, 128);
+      if (h == 0) {
+        if (mbar_wait<true>(b_xfree, (u & 1) ^ 1, abort_flag, p.err)) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            bulk_copy_to_cta(peer_x_in + q * (C::XBYTES / 4), x_out + q * (C::XBYTES / 4), C::XBYTES / 4, peer_xfull);
+          bulk_commit();
+        } else {
+          ok = false;   // seen by the others at the next barrier
+        }
+      }
+    };
+    int sent = 0;   // tiles whose partial has been sent
+    if (ntiles > 0) {
+      send_partial(0);
+      sent = 1;
+    }
+    for (int t = 0; t < ntiles; ++t) {
+      const uint32_t vlo = __ballot_sync(0xffffffffu, jn0 >= 0 && jn0 <= pos);
+      const uint32_t vhi = __ballot_sync(0xffffffffu, jn1 >= 0 && jn1 <= pos);
       if (t + 1 < ntiles) {
         const int e = (t + 1) * T + lane;
-        jn = e < nent ? selrow[e] : -1;
+        jn0 = e < nent ? selrow[e] : -1;
+        jn1 = e + 32 < nent ? selrow[e + 32] : -1;
       }
       const int sb = t & 1;
-      if (!mbar_wait(sfull(sb), (t >> 1) & 1, abort_flag, p.err)) { ok = false; break; }
-      tc_fence_after();
+      if (h == 0 && ok) mbar_arrive_expect_tx(b_xfull, C::XBYTES);
+      const bool good = ok && mbar_wait<true>(b_xfull, t & 1, abort_flag, p.err);
+      if (named_bar_any(4, 128, !good)) {   // the partner's partial of tile t is here
+        ok = false;
+        break;
+      }
+      // full logits of tile t = our partial (TMEM) + the partner's (x_in),
+      // written back over our partial so that x_in can be released before
+      // tile t+1 is sent (the partner may be waiting for that to send its own)
       float s[T];
+#pragma unroll
+      for (int c0 = 0; c0 < T; c0 += 16)
+        tmem_ld16(tmem_base + lane_base + C::S_COL + sb * T + c0, *reinterpret_cast<float(*)[16]>(s + c0));
+      tmem_ld_wait();
+      {
+        const float4 *xr = reinterpret_cast<const float4 *>(smem + C::OFF_X + h * 256);
+#pragma unroll
+        for (int c = 0; c < T / 4; ++c) {
+          const float4 v = xr[c ^ (h & 15)];
+          // a + b == b + a in IEEE arithmetic: both CTAs get the same S
+          s[4 * c] += v.x;
+          s[4 * c + 1] += v.y;
+          s[4 * c + 2] += v.z;
+          s[4 * c + 3] += v.w;
+        }
+      }
+#pragma unroll
+      for (int c0 = 0; c0 < T; c0 += 16)
+        tmem_st16(tmem_base + lane_base + C::S_COL + sb * T + c0, *reinterpret_cast<const float(*)[16]>(s + c0));
+      tmem_st_wait();
+      // one decision for all 128 threads: send tile t+1 now if its QK is done
+      if (h == 0)
+        *early_flag = (sent == t + 1 && t + 1 < ntiles && mbar_test(sfull((t + 1) & 1), ((t + 1) >> 1) & 1)) ? 1 : 0;
+      named_bar_sync(4, 128);   // x_in has been read by every head; early_flag is set
+      if (h == 0) mbar_arrive_remote_relaxed(peer_xfree);   // the reads of x_in fed the TMEM store above
+      if (*early_flag) {
+        send_partial(t + 1);
+        sent = t + 2;
+      }
+      if (named_bar_any(4, 128, !ok)) {     // early_flag has been read; a failed send is seen by all
+        ok = false;
+        break;
+      }
 #pragma unroll
       for (int c0 = 0; c0 < T; c0 += 16)
         tmem_ld16(tmem_base + lane_base + C::S_COL + sb * T + c0, *reinterpret_cast<float(*)[16]>(s + c0));
       tmem_ld_wait();
 
       // online softmax in base 2 with a lazily moved reference max
+      // (scale_log2 > 0, so the max of the raw logits picks the same key)
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int i = 0; i < T; ++i) {
-        s[i] = ((valid >> i) & 1u) ? s[i] * p.scale_log2 : -INFINITY;
+        const bool v = (((i < 32) ? (vlo >> i) : (vhi >> (i - 32))) & 1u) != 0;
+        s[i] = v ? s[i] : -INFINITY;
         mx[i & 3] = fmaxf(mx[i & 3], s[i]);
       }
-      const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.scale_log2;
       float alpha = 1.f;
       const bool rescale = tmax > m_ref + kRescaleThreshold;
       if (rescale) {
-        alpha = exp2f(m_ref - tmax);
+        alpha = fast_exp2(m_ref - tmax);
         m_ref = tmax;
       }
       float sm[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t packed[T / 2];
 #pragma unroll
       for (int i = 0; i < T; i += 2) {
-        const __nv_bfloat162 pb = __floats2bfloat162_rn(exp2f(s[i] - m_ref), exp2f(s[i + 1] - m_ref));
+        const __nv_bfloat162 pb = __floats2bfloat162_rn(fast_exp2(fmaf(s[i], p.scale_log2, -m_ref)),
+                                                        fast_exp2(fmaf(s[i + 1], p.scale_log2, -m_ref)));
         const float2 pf = __bfloat1622float2(pb);
         sm[(i >> 1) & 3] += pf.x + pf.y;
         packed[i / 2] = *reinterpret_cast<const uint32_t *>(&pb);
       }
       l = l * alpha + ((sm[0] + sm[1]) + (sm[2] + sm[3]));
 
-      // O must hold every earlier tile before it is rescaled
+      // O must hold every earlier tile before it is rescaled (QK of this tile
+      // waited for PV of tile t-2, so only PV of t-1 can still be running)
       if (rescale && t > 0) {
-        if (!mbar_wait(b_pvdone, (t - 1) & 1, abort_flag, p.err)) { ok = false; break; }
+        ok = mbar_wait(b_pvdone, (t - 1) & 1, abort_flag, p.err);   // a failure is seen at the next barrier
         tc_fence_after();
 #pragma unroll 1
         for (int c0 = 0; c0 < C::HALF; c0 += 16) {
@@ -474,15 +598,20 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_tc_kernel(const __grid_
         }
       }
       // P (bf16 pairs, lower key in the low half) over the first T/2 columns of this S tile
-      tmem_st16(tmem_base + lane_base + C::S_COL + sb * T, *reinterpret_cast<const float(*)[16]>(packed));
+      tmem_st32(tmem_base + lane_base + C::S_COL + sb * T, packed);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(pfull(sb));
+      if (sent == t + 1 && t + 1 < ntiles) {
+        send_partial(t + 1);   // a failure is seen at the next barrier
+        sent = t + 2;
+      }
     }
+    if (h == 0) bulk_wait_read_all();
     if (ok && ntiles > 0) ok = mbar_wait(b_pvdone, (ntiles - 1) & 1, abort_flag, p.err);
     tc_fence_after();
     if (ok && h < p.H) {
-      const int col0 = half * C::HALF;
+      const int col0 = static_cast<int>(crank) * C::HALF;
       if (unit.slot < 0) {
         float f = 0.f;
         if (p.sink) {
@@ -531,7 +660,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_tc_kernel(const __grid_
 #pragma unroll
           for (int i = 0; i < 4; ++i) d4[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
         }
-        if (half == 0) {
+        if (crank == 0) {
           float *ml = p.mlpart + (static_cast<int64_t>(unit.slot) * p.H + h) * 2;
           ml[0] = m_ref;
           ml[1] = l;
@@ -542,6 +671,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_tc_kernel(const __grid_
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync();   // the partner sends nothing more into this CTA's shared memory
   tc_fence_after();
   if (warp == kMmaWarp) tmem_dealloc(tmem_base, C::TMEM_COLS);
 }
@@ -663,11 +793,10 @@ cudaError_t run_tc(const dsa_ctx *ctx, const dsa_plan_t *plan, const int32_t *se
                        static_cast<uint64_t>(plan->T) * c.heads, L * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   if (!encode_tiled_2d(&prm.tm_qp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void *>(q_pe), 64,
-                       static_cast<uint64_t>(plan->T) * c.heads, 64 * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+                       static_cast<uint64_t>(plan->T) * c.heads, 64 * 2, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   prm.sel = sel;
   prm.latent = static_cast<const uint8_t *>(latent);
-  prm.q_nope = static_cast<const __nv_bfloat16 *>(q_nope);
   prm.sink = sink;
   prm.units = plan->units;
   prm.row_pos = plan->row_pos;

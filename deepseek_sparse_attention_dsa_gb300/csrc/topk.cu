@@ -4,14 +4,27 @@
 // scores are broken toward the lower position).
 //
 // One CTA per row.  Scores are mapped to order-preserving 32-bit keys (-0.0
-// ranks as +0.0).  Three histogram passes (11 + 11 + 10 bits, shared-memory
-// atomics; the first pass aggregates equal bins within a warp) pin down the
-// exact key tau of the k-th largest score and how many scores equal to tau
-// must be taken.  Then each warp owns a contiguous segment of the row: a
-// counting pass gives every warp its output offset and its rank among the
-// tau-ties, and a writing pass emits, in ascending position order, every
-// position above tau plus the earliest tau-ties.  A row that sees at most
-// topk keys takes them all and pads with -1.
+// ranks as +0.0).  The selection is exact; only the amount of work depends on
+// the data:
+//   1. candidates: a row with at most kCandCap keys takes all of them.  A
+//      longer row takes an evenly strided sample (4096..8191 keys) into shared
+//      memory, finds the sample key whose rank, scaled by the stride, lies a
+//      safe margin above topk, and keeps every key of the row at or above it
+//      (one pass over the row).  When that leaves fewer than topk keys or more
+//      than kCandCap, the threshold is found by radix passes over the row in
+//      global memory instead.
+//   2. the k-th largest key tau and the number of tau ties to take (the
+//      earliest ones) come from radix passes (11 + 11 + 10 bits, shared-memory
+//      histograms) over the candidates;
+//   3. output in ascending position order: the chosen positions are set in a
+//      bitmap of the row (shared memory, up to kBitmapBits positions), whose
+//      word counts are prefix-summed; every set bit is written at its rank.
+//      Rows longer than the bitmap, or with more than kTieCap tau ties among
+//      which some are dropped, use an ordered compaction over the row instead:
+//      each warp owns a contiguous segment, a counting pass gives every warp
+//      its output offset and its rank among the tau ties, and a writing pass
+//      emits every position above tau plus the earliest ties.
+// A row that sees at most topk keys takes them all and pads with -1.
 #include <cuda_runtime.h>
 
 #include "dsa_internal.h"
@@ -22,7 +35,25 @@ namespace {
 
 constexpr int kTopkThreads = 1024;
 constexpr int kTopkWarps = kTopkThreads / 32;
-constexpr int kBatch = 8;   // independent loads in flight per thread
+constexpr int kBatch = 8;             // independent loads in flight per thread
+constexpr int kCandCap = 8192;        // candidate keys held in shared memory
+constexpr int kSampleMin = 4096;      // a strided sample holds kSampleMin .. 2*kSampleMin-1 keys
+constexpr int kBitmapWords = 8192;    // 262,144 positions
+constexpr int kTieCap = 2048;         // tau ties ranked by position in shared memory
+
+struct TopkSmem {
+  union {
+    uint32_t sample[2 * kSampleMin];
+    uint32_t bits[kBitmapWords];
+  };
+  uint32_t ckey[kCandCap];
+  int32_t cpos[kCandCap];
+  int hist[2048];                     // radix histograms; tie positions during output
+  int ws[kTopkWarps];
+  int res[2];
+  int n_cand, n_tie;
+  int wgt[kTopkWarps], weq[kTopkWarps];
+};
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t u = __float_as_uint(f);
@@ -57,19 +88,28 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *ws, int *total) 
   return before + x - v;
 }
 
-// Bin (counted from the top) that holds the need-th largest key; *above gets
-// the number of keys in higher bins.
-__device__ __forceinline__ int find_bin(const int *hist, int nbins, int need, int *ws, int *res, int *above) {
-  const int b0 = nbins - 1 - 2 * static_cast<int>(threadIdx.x), b1 = b0 - 1;
-  const int c0 = b0 >= 0 ? hist[b0] : 0, c1 = b1 >= 0 ? hist[b1] : 0;
+// Bin (counted from the top) that holds the need-th largest key of a
+// histogram of NB <= 2048 bins; *above gets the number of keys in higher bins.
+template <int NB>
+__device__ __forceinline__ int find_bin(const int *hist, int need, int *ws, int *res, int *above) {
+  constexpr int PER = NB >= kTopkThreads ? NB / kTopkThreads : 1;
+  int c[PER];
+  int sum = 0;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int idx = static_cast<int>(threadIdx.x) * PER + j;   // rank of the bin from the top
+    c[j] = idx < NB ? hist[NB - 1 - idx] : 0;
+    sum += c[j];
+  }
   int total;
-  const int ex = block_exclusive_scan(c0 + c1, ws, &total);
-  if (ex < need && need <= ex + c0) {
-    res[0] = b0;
-    res[1] = ex;
-  } else if (ex + c0 < need && need <= ex + c0 + c1) {
-    res[0] = b1;
-    res[1] = ex + c0;
+  int run = block_exclusive_scan(sum, ws, &total);
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    if (run < need && need <= run + c[j]) {
+      res[0] = NB - 1 - (static_cast<int>(threadIdx.x) * PER + j);
+      res[1] = run;
+    }
+    run += c[j];
   }
   __syncthreads();
   *above = res[1];
@@ -78,14 +118,53 @@ __device__ __forceinline__ int find_bin(const int *hist, int nbins, int need, in
   return b;
 }
 
+// The rank-th largest key (rank >= 1) of the keys produced by `for_each`
+// (called as for_each(visit) with visit(key) for every key, by every thread
+// over its share), by three radix passes of 11, 11 and 10 bits.  *ties gets
+// how many keys equal to the result lie within the top `rank`.
+template <typename ForEach>
+__device__ __forceinline__ uint32_t radix_select(ForEach for_each, int rank, TopkSmem &sm, int *ties) {
+  uint32_t prefix = 0, pmask = 0;
+  int need = rank;
+#pragma unroll 1
+  for (int pass = 0; pass < 3; ++pass) {
+    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+    const int nbins = pass == 2 ? 1024 : 2048;
+    for (int i = threadIdx.x; i < 2048; i += kTopkThreads) sm.hist[i] = 0;
+    __syncthreads();
+    for_each([&](uint32_t key) {
+      if ((key & pmask) == prefix) atomicAdd(&sm.hist[(key >> shift) & (nbins - 1)], 1);
+    });
+    __syncthreads();
+    int above;
+    const int b = pass == 2 ? find_bin<1024>(sm.hist, need, sm.ws, sm.res, &above)
+                            : find_bin<2048>(sm.hist, need, sm.ws, sm.res, &above);
+    prefix |= static_cast<uint32_t>(b) << shift;
+    pmask |= static_cast<uint32_t>(nbins - 1) << shift;
+    need -= above;
+  }
+  *ties = need;
+  return prefix;
+}
+
+// Warp-aggregated append: lanes with `take` get consecutive slots after *counter.
+__device__ __forceinline__ int warp_append(bool take, int *counter) {
+  const uint32_t m = __ballot_sync(0xffffffffu, take);
+  if (m == 0) return -1;
+  const int lane = threadIdx.x & 31;
+  const int leader = __ffs(m) - 1;
+  int base = 0;
+  if (lane == leader) base = atomicAdd(counter, __popc(m));
+  base = __shfl_sync(0xffffffffu, base, leader);
+  return take ? base + __popc(m & ((1u << lane) - 1u)) : -1;
+}
+
 __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const float *__restrict__ scores,
                                                                const int64_t *__restrict__ row_score_off,
                                                                const int32_t *__restrict__ row_pos, int K,
                                                                int32_t *__restrict__ sel) {
-  __shared__ int hist[2048];
-  __shared__ int ws[kTopkWarps];
-  __shared__ int res[2];
-  __shared__ int wgt[kTopkWarps], weq[kTopkWarps];
+  extern __shared__ uint8_t topk_smem_raw[];
+  TopkSmem &sm = *reinterpret_cast<TopkSmem *>(topk_smem_raw);
 
   const int row = blockIdx.x;
   const int n = row_pos[row] + 1;
@@ -96,49 +175,140 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const float *__re
   }
   const float *s = scores + row_score_off[row];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int tid = static_cast<int>(threadIdx.x);
 
-  // ---- radix select of the k-th largest key.  Every loop below issues
-  // kBatch independent loads per thread before using any of them, so each
-  // pass is bound by L2 bandwidth rather than by one load's latency.
-  uint32_t prefix = 0, pmask = 0;
-  int need = K;
-#pragma unroll 1
-  for (int pass = 0; pass < 3; ++pass) {
-    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-    const int nbins = pass == 2 ? 1024 : 2048;
-    for (int i = threadIdx.x; i < 2048; i += kTopkThreads) hist[i] = 0;
+  // ---- 1. candidates
+  if (tid == 0) sm.n_cand = 0;
+  __syncthreads();
+  bool cand_ok;
+  if (n <= kCandCap) {
+    for (int i = tid; i < n; i += kTopkThreads) {
+      sm.ckey[i] = order_key(__ldg(s + i));
+      sm.cpos[i] = i;
+    }
+    if (tid == 0) sm.n_cand = n;
+    cand_ok = true;
+  } else {
+    const int stride = n / kSampleMin;                 // >= 2
+    const int m = (n + stride - 1) / stride;           // kSampleMin .. 2*kSampleMin-1
+    for (int j = tid; j < m; j += kTopkThreads) sm.sample[j] = order_key(__ldg(s + static_cast<int64_t>(j) * stride));
     __syncthreads();
+    // sample rank whose scaled count is about 1.15 topk plus three standard deviations
+    const float ks = static_cast<float>(K) / static_cast<float>(stride);
+    int rank = static_cast<int>(1.15f * ks + 3.f * sqrtf(ks)) + 8;
+    rank = min(rank, m);
+    int unused;
+    const uint32_t l0 = radix_select(
+        [&](auto visit) {
+          for (int j = tid; j < m; j += kTopkThreads) visit(sm.sample[j]);
+        },
+        rank, sm, &unused);
+    // every key of the row at or above l0
     for (int base = 0; base < n; base += kTopkThreads * kBatch) {
       uint32_t k[kBatch];
 #pragma unroll
       for (int j = 0; j < kBatch; ++j) {
-        const int i = base + j * kTopkThreads + static_cast<int>(threadIdx.x);
+        const int i = base + j * kTopkThreads + tid;
         k[j] = i < n ? order_key(__ldg(s + i)) : 0u;
       }
 #pragma unroll
       for (int j = 0; j < kBatch; ++j) {
-        const bool in = base + j * kTopkThreads + static_cast<int>(threadIdx.x) < n;
-        if (pass == 0) {
-          // equal bins of a warp are counted by one atomic
-          const int bin = in ? static_cast<int>(k[j] >> 21) : -1;
-          const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-          if (in && (__ffs(peers) - 1) == lane) atomicAdd(&hist[bin], __popc(peers));
-        } else if (in && (k[j] & pmask) == prefix) {
-          atomicAdd(&hist[(k[j] >> shift) & (nbins - 1)], 1);
+        const int i = base + j * kTopkThreads + tid;
+        const int c = warp_append(i < n && k[j] >= l0, &sm.n_cand);
+        if (c >= 0 && c < kCandCap) {
+          sm.ckey[c] = k[j];
+          sm.cpos[c] = i;
         }
       }
     }
     __syncthreads();
-    int above;
-    const int b = find_bin(hist, nbins, need, ws, res, &above);
-    prefix |= static_cast<uint32_t>(b) << shift;
-    pmask |= static_cast<uint32_t>(nbins - 1) << shift;
-    need -= above;
+    cand_ok = sm.n_cand >= K && sm.n_cand <= kCandCap;
   }
-  const uint32_t tau = prefix;  // exact key of the k-th largest score
-  // `need` = how many scores equal to tau are taken (the earliest ones)
+  __syncthreads();
+  const int n_cand = sm.n_cand;
 
-  // ---- ordered compaction, one contiguous segment per warp
+  // ---- 2. tau and the number of tau ties taken
+  int need;
+  uint32_t tau;
+  if (cand_ok) {
+    tau = radix_select(
+        [&](auto visit) {
+          for (int i = tid; i < n_cand; i += kTopkThreads) visit(sm.ckey[i]);
+        },
+        K, sm, &need);
+  } else {
+    tau = radix_select(
+        [&](auto visit) {
+          for (int base = 0; base < n; base += kTopkThreads * kBatch) {
+            uint32_t k[kBatch];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+              const int i = base + j * kTopkThreads + tid;
+              k[j] = i < n ? order_key(__ldg(s + i)) : 0u;
+            }
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j)
+              if (base + j * kTopkThreads + tid < n) visit(k[j]);
+          }
+        },
+        K, sm, &need);
+  }
+
+  // ---- 3. output through a bitmap of the row
+  if (cand_ok && n <= 32 * kBitmapWords) {
+    const int nw = (n + 31) >> 5;
+    for (int w = tid; w < nw; w += kTopkThreads) sm.bits[w] = 0u;
+    if (tid == 0) sm.n_tie = 0;
+    __syncthreads();
+    for (int i = tid; i < n_cand; i += kTopkThreads) {
+      const uint32_t key = sm.ckey[i];
+      if (key > tau) {
+        const int pos = sm.cpos[i];
+        atomicOr(&sm.bits[pos >> 5], 1u << (pos & 31));
+      } else if (key == tau) {
+        const int t = atomicAdd(&sm.n_tie, 1);
+        if (t < kTieCap) sm.hist[t] = sm.cpos[i];
+      }
+    }
+    __syncthreads();
+    const int n_tie = sm.n_tie;
+    if (n_tie == need || n_tie <= kTieCap) {
+      // the earliest `need` ties: a tie's rank is the number of ties before it
+      for (int t = tid; t < min(n_tie, kTieCap); t += kTopkThreads) {
+        const int pos = sm.hist[t];
+        int r = 0;
+        if (n_tie != need)
+          for (int u = 0; u < n_tie; ++u) r += sm.hist[u] < pos ? 1 : 0;
+        if (r < need) atomicOr(&sm.bits[pos >> 5], 1u << (pos & 31));
+      }
+      if (n_tie == need && n_tie > kTieCap) {
+        for (int i = tid; i < n_cand; i += kTopkThreads)
+          if (sm.ckey[i] == tau) atomicOr(&sm.bits[sm.cpos[i] >> 5], 1u << (sm.cpos[i] & 31));
+      }
+      __syncthreads();
+      // each thread owns a contiguous run of words
+      const int per = (nw + kTopkThreads - 1) / kTopkThreads;
+      const int w0 = tid * per;
+      int cnt = 0;
+      for (int q = 0; q < per; ++q)
+        if (w0 + q < nw) cnt += __popc(sm.bits[w0 + q]);
+      int tot;
+      int slot = block_exclusive_scan(cnt, sm.ws, &tot);
+      for (int q = 0; q < per; ++q) {
+        if (w0 + q >= nw) break;
+        uint32_t b = sm.bits[w0 + q];
+        while (b) {
+          const int bit = __ffs(b) - 1;
+          b &= b - 1u;
+          if (slot < K) out[slot] = ((w0 + q) << 5) + bit;
+          ++slot;
+        }
+      }
+      return;
+    }
+  }
+
+  // ---- ordered compaction over the row, one contiguous segment per warp
   const int seg = ((n + kTopkWarps - 1) / kTopkWarps + 32 * kBatch - 1) / (32 * kBatch) * (32 * kBatch);
   const int lo = warp * seg, hi = min(n, lo + seg);
   int cgt = 0, ceq = 0;
@@ -157,15 +327,15 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const float *__re
     }
   }
   if (lane == 0) {
-    wgt[warp] = cgt;
-    weq[warp] = ceq;
+    sm.wgt[warp] = cgt;
+    sm.weq[warp] = ceq;
   }
   __syncthreads();
   int out_base = 0, eq_base = 0;
   for (int w = 0; w < warp; ++w) {
-    const int take_eq = max(0, min(weq[w], need - eq_base));
-    out_base += wgt[w] + take_eq;
-    eq_base += weq[w];
+    const int take_eq = max(0, min(sm.weq[w], need - eq_base));
+    out_base += sm.wgt[w] + take_eq;
+    eq_base += sm.weq[w];
   }
   const uint32_t lt_mask = (1u << lane) - 1u;
   for (int base = lo; base < hi; base += 32 * kBatch) {
@@ -195,7 +365,15 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const float *__re
 
 cudaError_t launch_topk(const dsa_ctx *ctx, const dsa_plan_t *plan, const float *scores, int32_t *sel,
                         cudaStream_t s, int32_t *launches) {
-  topk_kernel<<<plan->T, kTopkThreads, 0, s>>>(scores, plan->row_score_off, plan->row_pos, ctx->cfg.topk, sel);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(sizeof(TopkSmem)));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  topk_kernel<<<plan->T, kTopkThreads, sizeof(TopkSmem), s>>>(scores, plan->row_score_off, plan->row_pos,
+                                                               ctx->cfg.topk, sel);
   *launches += 1;
   return cudaGetLastError();
 }

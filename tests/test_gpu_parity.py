@@ -132,6 +132,41 @@ def test_topk_ties_and_signed_zero():
     H.check_selection(g, ref, sc, off, sh.topk, exact=True)
 
 
+def test_topk_paths():
+    """Rows that take each path of the selection kernel: every key a candidate,
+    a strided sample, a sample the data fools (fallback to exact passes over
+    the row), a row longer than the position bitmap, and threshold ties below,
+    equal to and above what the tie ranking holds."""
+    sh = W.DSAShape(**W.DEEPSEEK)
+    K = sh.topk
+    rng = np.random.default_rng(11)
+    rows = []
+    rows.append(rng.standard_normal(8000).astype(np.float32))                     # all candidates
+    rows.append(rng.standard_normal(100000).astype(np.float32))                   # sampled
+    rows.append(rng.standard_normal(300000).astype(np.float32))                   # past the bitmap
+    fool = (rng.random(50000) * 10 + 1).astype(np.float32)
+    fool[:: 50000 // 4096] = 0.0                                                  # the sample sees only zeros
+    rows.append(fool)
+    for n_tie, n_top in ((3000, 1000), (1500, 1000), (1048, 1000)):               # ties > cap, <= cap, == need
+        r = (rng.random(20000) * 0.5).astype(np.float32)
+        idx = rng.permutation(20000)
+        r[idx[:n_top]] = (2.0 + rng.random(n_top)).astype(np.float32)
+        r[idx[n_top:n_top + n_tie]] = 1.0
+        rows.append(r)
+    reqs = [(len(r) - 1, 1) for r in rows]
+    wl = W.build_workload("topk_paths", sh, reqs, seed=12)
+    off = np.zeros(len(rows) + 1, np.int64)
+    off[1:] = np.cumsum([len(r) for r in rows])
+    sc = np.concatenate(rows)
+    ref = oracle.topk(sh, wl.spans, sc, off)
+    ctx = dsa.Context(sh, 0)
+    plan = ctx.plan(wl.spans, wl.num_pages)
+    assert plan.num_scores == len(sc)
+    g = ctx.topk_from_scores(plan, torch.from_numpy(sc).cuda()).cpu().numpy()
+    ctx.get_error()
+    H.check_selection(g, ref, sc, off, K, exact=True)
+
+
 def test_bounds_errors_are_reported_not_faulted():
     """Selected positions past the row or below -1 set DSA_ERR_BOUNDS and are skipped."""
     wl = H.deepseek_small(seed=7, decode_ctx=(3000,), chunk=None)
