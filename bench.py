@@ -161,6 +161,9 @@ def run_ours(args, name, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     wl = W.config(WORKLOADS[name], seed=1000 + WORKLOADS[name] + 7919 * rank)
+    if args.requests:
+        # the first N requests only: a smaller case of the same workload for profiler captures
+        wl = wl.sub_workload(range(min(args.requests, len(wl.spans))))
     sh = wl.shape
     unit, decode = unit_of(wl)
     work = algorithmic(wl)
@@ -410,6 +413,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-rows", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--requests", type=int, default=0,
+                    help="keep only the first N requests of the workload (profiler captures; not a bench line)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
     rank, world, local_rank = rank_info()

@@ -68,7 +68,7 @@ struct AttTraits {
   static constexpr int CHUNK = TILE * 128;               // [64 keys x 64 cols] bf16, 128-byte swizzle
   static constexpr int RCHUNK = TILE * 64;               // [64 keys x 32 rope cols], 64-byte swizzle
   static constexpr int STAGE = NPV * CHUNK + RCHUNK;
-  static constexpr int STAGES = 4;
+  static constexpr int STAGES = 3;
   static constexpr int PIECES = NPV * 8 + 4;             // 16-byte pieces of a key's part
   static constexpr int QCHUNK = 128 * 128;               // [128 heads x 64 cols]
   static constexpr int QRBYTES = 128 * 64;               // [128 heads x 32 rope cols]
@@ -79,8 +79,8 @@ struct AttTraits {
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr int OFF_QR = 0;
   static constexpr int OFF_K = 8192;
-  static constexpr int OFF_X = OFF_K + STAGES * STAGE;   // x_in, x_out: [128 heads][64 keys] fp32 each
-  static constexpr int OFF_ROWS = OFF_X + 2 * XBYTES;    // int32 [STAGES][TILE]
+  static constexpr int OFF_X = OFF_K + STAGES * STAGE;   // x_in[2], x_out: [128 heads][64 keys] fp32 each
+  static constexpr int OFF_ROWS = OFF_X + 3 * XBYTES;    // int32 [STAGES][TILE]
   static constexpr int OFF_BAR = OFF_ROWS + STAGES * TILE * 4;
   static constexpr int NBAR = 24;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -179,8 +179,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
   auto sfull = [&](int b) { return bar0 + 8u * (4 + 2 * NS + b); };
   auto sempty = [&](int b) { return bar0 + 8u * (6 + 2 * NS + b); };
   auto pfull = [&](int b) { return bar0 + 8u * (8 + 2 * NS + b); };
-  const uint32_t b_xfull = bar0 + 8u * (10 + 2 * NS);   // the partner's partial landed in x_in
-  const uint32_t b_xfree = bar0 + 8u * (11 + 2 * NS);   // the partner has read what we sent
+  auto xfull = [&](int b) { return bar0 + 8u * (10 + 2 * NS + b); };   // the partner's partial landed in x_in[b]
+  auto xfree = [&](int b) { return bar0 + 8u * (12 + 2 * NS + b); };   // the partner has read our x_in[b] copy
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
   int32_t *rows_sm = reinterpret_cast<int32_t *>(smem + C::OFF_ROWS);
@@ -209,8 +209,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
       mbar_init(sempty(b), 1);
       mbar_init(pfull(b), 128);
     }
-    mbar_init(b_xfull, 1);   // armed locally with the tile's bytes, filled by the partner's bulk copy
-    mbar_init(b_xfree, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(xfull(b), 1);   // armed locally with the tile's bytes, filled by the partner's bulk copy
+      mbar_init(xfree(b), 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -424,9 +426,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
     const int quad = warp & 3;
     const int h = quad * 32 + lane;                      // head = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t x_in = sbase + C::OFF_X, x_out = sbase + C::OFF_X + C::XBYTES;
-    const uint32_t peer_x_in = map_to_cta(x_in, peer);
-    const uint32_t peer_xfull = map_to_cta(b_xfull, peer), peer_xfree = map_to_cta(b_xfree, peer);
+    const uint32_t x_in0 = sbase + C::OFF_X, x_out = sbase + C::OFF_X + 2 * C::XBYTES;
+    const uint32_t peer_x_in0 = map_to_cta(x_in0, peer);
     volatile int *early_flag = abort_flag + 1;
     bool ok = mbar_wait(b_qtfull, 0, abort_flag, p.err);
     if (ok) {
@@ -455,14 +456,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
     int jn1 = 32 + lane < nent ? selrow[32 + lane] : -1;
     // This CTA's partial logits of tile u are staged in x_out (row h, 16-byte
     // chunks swizzled by h) and copied by the bulk-copy engine into the
-    // partner's x_in once the partner has read tile u-1 from it.  Tile t+1 is
-    // sent before the softmax of tile t when its QK is already done, so the
-    // transfer overlaps the math; otherwise right after it.
+    // partner's x_in[u & 1] once the partner has read tile u-2 from it.  Tile
+    // t+1 is sent before tile t is received when its QK is already done, so
+    // the transfer overlaps the softmax; otherwise right after the softmax.
     // Exits are decided at the named barriers of the 128 softmax threads (an
     // OR of their failures), so no thread is left waiting there alone.
     auto send_partial = [&](int u) {
       const int b = u & 1;
-      bool good = ok && mbar_wait(sfull(b), (u >> 1) & 1, abort_flag, p.err);
+      const uint32_t use = static_cast<uint32_t>(u >> 1);
+      bool good = ok && mbar_wait(sfull(b), use & 1, abort_flag, p.err);
       if (good) tc_fence_after();
       if (h == 0 && good) bulk_wait_read_all();   // the copy of tile u-1 has read x_out
       if (named_bar_any(3, 128, !good)) {
@@ -482,10 +484,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
       fence_proxy_async_smem();
       named_bar_sync(3, 128);
       if (h == 0) {
-        if (mbar_wait<true>(b_xfree, (u & 1) ^ 1, abort_flag, p.err)) {
+        if (mbar_wait<true>(xfree(b), (use & 1) ^ 1, abort_flag, p.err)) {
+          const uint32_t dst = peer_x_in0 + b * C::XBYTES, bar = map_to_cta(xfull(b), peer);
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            bulk_copy_to_cta(peer_x_in + q * (C::XBYTES / 4), x_out + q * (C::XBYTES / 4), C::XBYTES / 4, peer_xfull);
+            bulk_copy_to_cta(dst + q * (C::XBYTES / 4), x_out + q * (C::XBYTES / 4), C::XBYTES / 4, bar);
           bulk_commit();
         } else {
           ok = false;   // seen by the others at the next barrier
@@ -506,22 +509,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
         jn1 = e + 32 < nent ? selrow[e + 32] : -1;
       }
       const int sb = t & 1;
-      if (h == 0 && ok) mbar_arrive_expect_tx(b_xfull, C::XBYTES);
-      const bool good = ok && mbar_wait<true>(b_xfull, t & 1, abort_flag, p.err);
-      if (named_bar_any(4, 128, !good)) {   // the partner's partial of tile t is here
+      // one decision for all 128 threads: send tile t+1 now if its QK is done
+      if (h == 0)
+        *early_flag = (ok && sent == t + 1 && t + 1 < ntiles && mbar_test(sfull((t + 1) & 1), ((t + 1) >> 1) & 1))
+                          ? 1 : 0;
+      named_bar_sync(4, 128);
+      if (*early_flag) {
+        send_partial(t + 1);
+        sent = t + 2;
+      }
+      if (h == 0 && ok) mbar_arrive_expect_tx(xfull(sb), C::XBYTES);
+      const bool good = ok && mbar_wait<true>(xfull(sb), (t >> 1) & 1, abort_flag, p.err);
+      if (named_bar_any(4, 128, !good)) {   // the partner's partial of tile t is here; early_flag has been read
         ok = false;
         break;
       }
-      // full logits of tile t = our partial (TMEM) + the partner's (x_in),
-      // written back over our partial so that x_in can be released before
-      // tile t+1 is sent (the partner may be waiting for that to send its own)
+      // full logits of tile t: our partial (TMEM) + the partner's (x_in)
       float s[T];
 #pragma unroll
       for (int c0 = 0; c0 < T; c0 += 16)
         tmem_ld16(tmem_base + lane_base + C::S_COL + sb * T + c0, *reinterpret_cast<float(*)[16]>(s + c0));
       tmem_ld_wait();
       {
-        const float4 *xr = reinterpret_cast<const float4 *>(smem + C::OFF_X + h * 256);
+        const float4 *xr = reinterpret_cast<const float4 *>(smem + C::OFF_X + sb * C::XBYTES + h * 256);
 #pragma unroll
         for (int c = 0; c < T / 4; ++c) {
           const float4 v = xr[c ^ (h & 15)];
@@ -532,27 +542,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
           s[4 * c + 3] += v.w;
         }
       }
-#pragma unroll
-      for (int c0 = 0; c0 < T; c0 += 16)
-        tmem_st16(tmem_base + lane_base + C::S_COL + sb * T + c0, *reinterpret_cast<const float(*)[16]>(s + c0));
-      tmem_st_wait();
-      // one decision for all 128 threads: send tile t+1 now if its QK is done
-      if (h == 0)
-        *early_flag = (sent == t + 1 && t + 1 < ntiles && mbar_test(sfull((t + 1) & 1), ((t + 1) >> 1) & 1)) ? 1 : 0;
-      named_bar_sync(4, 128);   // x_in has been read by every head; early_flag is set
-      if (h == 0) mbar_arrive_remote_relaxed(peer_xfree);   // the reads of x_in fed the TMEM store above
-      if (*early_flag) {
-        send_partial(t + 1);
-        sent = t + 2;
-      }
-      if (named_bar_any(4, 128, !ok)) {     // early_flag has been read; a failed send is seen by all
-        ok = false;
-        break;
-      }
-#pragma unroll
-      for (int c0 = 0; c0 < T; c0 += 16)
-        tmem_ld16(tmem_base + lane_base + C::S_COL + sb * T + c0, *reinterpret_cast<float(*)[16]>(s + c0));
-      tmem_ld_wait();
+      named_bar_sync(4, 128);   // every head has read x_in[sb]
+      if (h == 0) mbar_arrive_remote_relaxed(map_to_cta(xfree(sb), peer));
 
       // online softmax in base 2 with a lazily moved reference max
       // (scale_log2 > 0, so the max of the raw logits picks the same key)
