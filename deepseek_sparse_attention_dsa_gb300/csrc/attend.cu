@@ -51,12 +51,13 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr float kNegBig = -1.0e30f;
 
-// warp roles (12 warps; registers are handed out per group of four warps)
+// warp roles (16 warps; registers are handed out per group of four warps)
 constexpr int kMmaWarp = 0;
 constexpr int kProdWarp0 = 1;               // warps 1-7: producers (224 threads)
 constexpr int kSoftWarp0 = 8;               // warps 8-11: softmax, thread = head
+constexpr int kSendWarp0 = 12;              // warps 12-15: partial-logit senders, thread = head
 constexpr int kProdThreads = 224;
-constexpr int kAttThreads = 12 * 32;
+constexpr int kAttThreads = 16 * 32;
 
 template <int L>
 struct AttTraits {
@@ -92,7 +93,7 @@ struct AttTraits {
   static_assert(O_COL + HALF <= TMEM_COLS, "tensor memory: O");
   static_assert(QRBYTES <= OFF_K && STAGE % 1024 == 0, "alignment");
   static_assert(NPV * QCHUNK <= STAGES * STAGE, "Q staging");
-  static_assert(NBAR >= 14 + 2 * STAGES, "barriers");
+  static_assert(NBAR >= 16 + 2 * STAGES, "barriers");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
@@ -181,6 +182,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
   auto pfull = [&](int b) { return bar0 + 8u * (8 + 2 * NS + b); };
   auto xfull = [&](int b) { return bar0 + 8u * (10 + 2 * NS + b); };   // the partner's partial landed in x_in[b]
   auto xfree = [&](int b) { return bar0 + 8u * (12 + 2 * NS + b); };   // the partner has read our x_in[b] copy
+  auto sread = [&](int b) { return bar0 + 8u * (14 + 2 * NS + b); };   // the senders have read S tile b
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
   int32_t *rows_sm = reinterpret_cast<int32_t *>(smem + C::OFF_ROWS);
@@ -208,10 +210,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
       mbar_init(sfull(b), 1);
       mbar_init(sempty(b), 1);
       mbar_init(pfull(b), 128);
+      mbar_init(sread(b), 128);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(xfull(b), 1);   // armed locally with the tile's bytes, filled by the partner's bulk copy
-      mbar_init(xfree(b), 1);
+      mbar_init(xfree(b), 4);   // one arrival per partner softmax warp
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -421,14 +424,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
       pg0 = pg1;
     }
     cp_async_wait<0>();   // nothing in flight when the CTA leaves
+  } else if (warp >= kSendWarp0) {
+    // ------------------------------------------------------------ senders
+    // Warp q (heads 32q..32q+31) copies its rows of this CTA's partial logits
+    // of every tile, as soon as its QK is done, into x_out (row h, 16-byte
+    // chunks swizzled by h) and bulk-copies those 8 KB into the partner's
+    // x_in[u & 1] once all four partner softmax warps have read tile u-2 from
+    // it (a bulk copy lands ~1 us sooner than the same bytes sent by st.async
+    // from registers).  The S tile may be overwritten by P once every sender
+    // has read it (sread).
+    const int quad = warp & 3;
+    const int h = quad * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t row_off = static_cast<uint32_t>(quad) * (C::XBYTES / 4);
+    const uint32_t x_out = sbase + C::OFF_X + 2 * C::XBYTES;
+    const uint32_t peer_x_in0 = map_to_cta(sbase + C::OFF_X, peer);
+    for (int u = 0; u < ntiles; ++u) {
+      const int b = u & 1;
+      const uint32_t use = static_cast<uint32_t>(u >> 1);
+      if (!mbar_wait(sfull(b), use & 1, abort_flag, p.err)) break;
+      tc_fence_after();
+      if (lane == 0) bulk_wait_read_all();   // this warp's copy of tile u-1 has read its x_out rows
+      __syncwarp();
+      float v[T];
+#pragma unroll
+      for (int c0 = 0; c0 < T; c0 += 16)
+        tmem_ld16(tmem_base + lane_base + C::S_COL + b * T + c0, *reinterpret_cast<float(*)[16]>(v + c0));
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(sread(b));
+#pragma unroll
+      for (int c = 0; c < T / 4; ++c)
+        st_shared_v4(x_out + h * 256 + ((c ^ (h & 15)) << 4),
+                     make_uint4(__float_as_uint(v[4 * c]), __float_as_uint(v[4 * c + 1]), __float_as_uint(v[4 * c + 2]),
+                                __float_as_uint(v[4 * c + 3])));
+      fence_proxy_async_smem();
+      __syncwarp();
+      int sent_ok = 1;
+      if (lane == 0) {
+        if (mbar_wait<true>(xfree(b), (use & 1) ^ 1, abort_flag, p.err)) {
+          bulk_copy_to_cta(peer_x_in0 + b * C::XBYTES + row_off, x_out + row_off, C::XBYTES / 4,
+                           map_to_cta(xfull(b), peer));
+          bulk_commit();
+        } else {
+          sent_ok = 0;
+        }
+      }
+      if (__shfl_sync(0xffffffffu, sent_ok, 0) == 0) break;
+    }
+    if (lane == 0) bulk_wait_read_all();   // x_out stays valid until every copy has read it
   } else {
     // ------------------------------------------------------------ softmax
     const int quad = warp & 3;
     const int h = quad * 32 + lane;                      // head = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t x_in0 = sbase + C::OFF_X, x_out = sbase + C::OFF_X + 2 * C::XBYTES;
-    const uint32_t peer_x_in0 = map_to_cta(x_in0, peer);
-    volatile int *early_flag = abort_flag + 1;
     bool ok = mbar_wait(b_qtfull, 0, abort_flag, p.err);
     if (ok) {
       // this head's row of the q_nope columns: from the staged swizzled
@@ -454,53 +503,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
     float m_ref = kNegBig, l = 0.f;
     int jn0 = lane < nent ? selrow[lane] : -1;
     int jn1 = 32 + lane < nent ? selrow[32 + lane] : -1;
-    // This CTA's partial logits of tile u are staged in x_out (row h, 16-byte
-    // chunks swizzled by h) and copied by the bulk-copy engine into the
-    // partner's x_in[u & 1] once the partner has read tile u-2 from it.  Tile
-    // t+1 is sent before tile t is received when its QK is already done, so
-    // the transfer overlaps the softmax; otherwise right after the softmax.
-    // Exits are decided at the named barriers of the 128 softmax threads (an
-    // OR of their failures), so no thread is left waiting there alone.
-    auto send_partial = [&](int u) {
-      const int b = u & 1;
-      const uint32_t use = static_cast<uint32_t>(u >> 1);
-      bool good = ok && mbar_wait(sfull(b), use & 1, abort_flag, p.err);
-      if (good) tc_fence_after();
-      if (h == 0 && good) bulk_wait_read_all();   // the copy of tile u-1 has read x_out
-      if (named_bar_any(3, 128, !good)) {
-        ok = false;
-        return;
-      }
-      float v[T];
-#pragma unroll
-      for (int c0 = 0; c0 < T; c0 += 16)
-        tmem_ld16(tmem_base + lane_base + C::S_COL + b * T + c0, *reinterpret_cast<float(*)[16]>(v + c0));
-      tmem_ld_wait();
-#pragma unroll
-      for (int c = 0; c < T / 4; ++c)
-        st_shared_v4(x_out + h * 256 + ((c ^ (h & 15)) << 4),
-                     make_uint4(__float_as_uint(v[4 * c]), __float_as_uint(v[4 * c + 1]), __float_as_uint(v[4 * c + 2]),
-                                __float_as_uint(v[4 * c + 3])));
-      fence_proxy_async_smem();
-      named_bar_sync(3, 128);
-      if (h == 0) {
-        if (mbar_wait<true>(xfree(b), (use & 1) ^ 1, abort_flag, p.err)) {
-          const uint32_t dst = peer_x_in0 + b * C::XBYTES, bar = map_to_cta(xfull(b), peer);
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            bulk_copy_to_cta(dst + q * (C::XBYTES / 4), x_out + q * (C::XBYTES / 4), C::XBYTES / 4, bar);
-          bulk_commit();
-        } else {
-          ok = false;   // seen by the others at the next barrier
-        }
-      }
-    };
-    int sent = 0;   // tiles whose partial has been sent
-    if (ntiles > 0) {
-      send_partial(0);
-      sent = 1;
-    }
-    for (int t = 0; t < ntiles; ++t) {
+    for (int t = 0; t < ntiles && ok; ++t) {
       const uint32_t vlo = __ballot_sync(0xffffffffu, jn0 >= 0 && jn0 <= pos);
       const uint32_t vhi = __ballot_sync(0xffffffffu, jn1 >= 0 && jn1 <= pos);
       if (t + 1 < ntiles) {
@@ -509,27 +512,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
         jn1 = e + 32 < nent ? selrow[e + 32] : -1;
       }
       const int sb = t & 1;
-      // one decision for all 128 threads: send tile t+1 now if its QK is done
-      if (h == 0)
-        *early_flag = (ok && sent == t + 1 && t + 1 < ntiles && mbar_test(sfull((t + 1) & 1), ((t + 1) >> 1) & 1))
-                          ? 1 : 0;
-      named_bar_sync(4, 128);
-      if (*early_flag) {
-        send_partial(t + 1);
-        sent = t + 2;
-      }
-      if (h == 0 && ok) mbar_arrive_expect_tx(xfull(sb), C::XBYTES);
-      const bool good = ok && mbar_wait<true>(xfull(sb), (t >> 1) & 1, abort_flag, p.err);
-      if (named_bar_any(4, 128, !good)) {   // the partner's partial of tile t is here; early_flag has been read
-        ok = false;
-        break;
-      }
-      // full logits of tile t: our partial (TMEM) + the partner's (x_in)
+      const uint32_t use = static_cast<uint32_t>(t >> 1);
+      if (h == 0) mbar_arrive_expect_tx(xfull(sb), C::XBYTES);
+      if (!mbar_wait(sfull(sb), use & 1, abort_flag, p.err)) { ok = false; break; }
+      tc_fence_after();
       float s[T];
 #pragma unroll
       for (int c0 = 0; c0 < T; c0 += 16)
         tmem_ld16(tmem_base + lane_base + C::S_COL + sb * T + c0, *reinterpret_cast<float(*)[16]>(s + c0));
       tmem_ld_wait();
+      // full logits of tile t: our partial + the partner's (x_in[sb])
+      if (!mbar_wait<true>(xfull(sb), use & 1, abort_flag, p.err)) { ok = false; break; }
       {
         const float4 *xr = reinterpret_cast<const float4 *>(smem + C::OFF_X + sb * C::XBYTES + h * 256);
 #pragma unroll
@@ -542,8 +535,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
           s[4 * c + 3] += v.w;
         }
       }
-      named_bar_sync(4, 128);   // every head has read x_in[sb]
-      if (h == 0) mbar_arrive_remote_relaxed(map_to_cta(xfree(sb), peer));
+      __syncwarp();   // this warp's rows of x_in[sb] have been read
+      if (lane == 0) mbar_arrive_remote_relaxed(map_to_cta(xfree(sb), peer));
 
       // online softmax in base 2 with a lazily moved reference max
       // (scale_log2 > 0, so the max of the raw logits picks the same key)
@@ -561,22 +554,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
         alpha = fast_exp2(m_ref - tmax);
         m_ref = tmax;
       }
-      float sm[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t packed[T / 2];
-#pragma unroll
-      for (int i = 0; i < T; i += 2) {
-        const __nv_bfloat162 pb = __floats2bfloat162_rn(fast_exp2(fmaf(s[i], p.scale_log2, -m_ref)),
-                                                        fast_exp2(fmaf(s[i + 1], p.scale_log2, -m_ref)));
-        const float2 pf = __bfloat1622float2(pb);
-        sm[(i >> 1) & 3] += pf.x + pf.y;
-        packed[i / 2] = *reinterpret_cast<const uint32_t *>(&pb);
-      }
-      l = l * alpha + ((sm[0] + sm[1]) + (sm[2] + sm[3]));
-
       // O must hold every earlier tile before it is rescaled (QK of this tile
       // waited for PV of tile t-2, so only PV of t-1 can still be running)
       if (rescale && t > 0) {
-        ok = mbar_wait(b_pvdone, (t - 1) & 1, abort_flag, p.err);   // a failure is seen at the next barrier
+        if (!mbar_wait(b_pvdone, (t - 1) & 1, abort_flag, p.err)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll 1
         for (int c0 = 0; c0 < C::HALF; c0 += 16) {
@@ -588,17 +569,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
           tmem_st16(tmem_base + lane_base + C::O_COL + c0, o);
         }
       }
-      // P (bf16 pairs, lower key in the low half) over the first T/2 columns of this S tile
-      tmem_st32(tmem_base + lane_base + C::S_COL + sb * T, packed);
+      // P (bf16 pairs, lower key in the low half) over the first T/2 columns
+      // of this S tile, once the senders have read it; written in two halves
+      if (!mbar_wait(sread(sb), use & 1, abort_flag, p.err)) { ok = false; break; }
+      float sm[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int half2 = 0; half2 < 2; ++half2) {
+        uint32_t packed[T / 4];
+#pragma unroll
+        for (int i = 0; i < T / 2; i += 2) {
+          const int k = half2 * (T / 2) + i;
+          const __nv_bfloat162 pb = __floats2bfloat162_rn(fast_exp2(fmaf(s[k], p.scale_log2, -m_ref)),
+                                                          fast_exp2(fmaf(s[k + 1], p.scale_log2, -m_ref)));
+          const float2 pf = __bfloat1622float2(pb);
+          sm[(i >> 1) & 3] += pf.x + pf.y;
+          packed[i / 2] = *reinterpret_cast<const uint32_t *>(&pb);
+        }
+        tmem_st16(tmem_base + lane_base + C::S_COL + sb * T + half2 * (T / 4),
+                  *reinterpret_cast<const float(*)[16]>(packed));
+      }
+      l = l * alpha + ((sm[0] + sm[1]) + (sm[2] + sm[3]));
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(pfull(sb));
-      if (sent == t + 1 && t + 1 < ntiles) {
-        send_partial(t + 1);   // a failure is seen at the next barrier
-        sent = t + 2;
-      }
     }
-    if (h == 0) bulk_wait_read_all();
     if (ok && ntiles > 0) ok = mbar_wait(b_pvdone, (ntiles - 1) & 1, abort_flag, p.err);
     tc_fence_after();
     if (ok && h < p.H) {
