@@ -69,19 +69,30 @@ struct AttTraits {
   static constexpr int CHUNK = TILE * 128;               // [64 keys x 64 cols] bf16, 128-byte swizzle
   static constexpr int RCHUNK = TILE * 64;               // [64 keys x 32 rope cols], 64-byte swizzle
   static constexpr int STAGE = NPV * CHUNK + RCHUNK;
-  static constexpr int STAGES = 3;
+  static constexpr int STAGES = 4;
   static constexpr int PIECES = NPV * 8 + 4;             // 16-byte pieces of a key's part
   static constexpr int QCHUNK = 128 * 128;               // [128 heads x 64 cols]
   static constexpr int QRBYTES = 128 * 64;               // [128 heads x 32 rope cols]
   static constexpr int XBYTES = 128 * TILE * 4;          // partial logits of a tile, fp32
-  // tensor memory: [q_nope columns of this CTA | S tile 0 | S tile 1 | O]
+  static constexpr int XBUF = 1;                         // receive buffers for the partner's partial logits
+  static constexpr int XOUT = XBYTES / 2;                // send staging: 16 rows (4 KB) per sender warp at a time
+  static_assert(XOUT / 4 == 16 * 256, "send staging slot");
+  // q_nope chunks of this CTA: the first QT_CH in tensor memory (A operand),
+  // the rest in shared memory
+  static constexpr int QT_CH = NPV < 3 ? NPV : 3;
+  static constexpr int QS_CH = NPV - QT_CH;
+  // tensor memory: [q_nope chunks | P | S tile 0 | S tile 1 | O].  P has its
+  // own columns, so an S tile is free for the next QK as soon as it has been
+  // read, not only after PV.
+  static constexpr uint32_t P_COL = 96;
   static constexpr uint32_t S_COL = 128;
   static constexpr uint32_t O_COL = 256;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr int OFF_QR = 0;
-  static constexpr int OFF_K = 8192;
-  static constexpr int OFF_X = OFF_K + STAGES * STAGE;   // x_in[2], x_out: [128 heads][64 keys] fp32 each
-  static constexpr int OFF_ROWS = OFF_X + 3 * XBYTES;    // int32 [STAGES][TILE]
+  static constexpr int OFF_QS = 8192;                    // q_nope chunks in shared memory
+  static constexpr int OFF_K = OFF_QS + QS_CH * QCHUNK;
+  static constexpr int OFF_X = OFF_K + STAGES * STAGE;   // x_in[XBUF] then x_out (XOUT bytes)
+  static constexpr int OFF_ROWS = OFF_X + XBUF * XBYTES + XOUT;   // int32 [STAGES][TILE]
   static constexpr int OFF_BAR = OFF_ROWS + STAGES * TILE * 4;
   static constexpr int NBAR = 24;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -89,10 +100,10 @@ struct AttTraits {
   static constexpr uint32_t IDESC_QK = mma_idesc(128, TILE, 1u, false, false);
   static constexpr uint32_t IDESC_PV = mma_idesc(128, HALF, 1u, false, true);
   static_assert(HALF % 64 == 0 && HALF <= 256, "latent width");
-  static_assert(NPV * 32 <= static_cast<int>(S_COL), "tensor memory: q_nope columns");
+  static_assert(QT_CH * 32 <= static_cast<int>(P_COL) && P_COL + TILE / 2 <= S_COL, "tensor memory: Q, P");
   static_assert(O_COL + HALF <= TMEM_COLS, "tensor memory: O");
   static_assert(QRBYTES <= OFF_K && STAGE % 1024 == 0, "alignment");
-  static_assert(NPV * QCHUNK <= STAGES * STAGE, "Q staging");
+  static_assert(QT_CH * QCHUNK <= STAGES * STAGE, "Q staging");
   static_assert(NBAR >= 16 + 2 * STAGES, "barriers");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
@@ -182,7 +193,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
   auto pfull = [&](int b) { return bar0 + 8u * (8 + 2 * NS + b); };
   auto xfull = [&](int b) { return bar0 + 8u * (10 + 2 * NS + b); };   // the partner's partial landed in x_in[b]
   auto xfree = [&](int b) { return bar0 + 8u * (12 + 2 * NS + b); };   // the partner has read our x_in[b] copy
-  auto sread = [&](int b) { return bar0 + 8u * (14 + 2 * NS + b); };   // the senders have read S tile b
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
   int32_t *rows_sm = reinterpret_cast<int32_t *>(smem + C::OFF_ROWS);
@@ -208,9 +218,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(sfull(b), 1);
-      mbar_init(sempty(b), 1);
+      mbar_init(sempty(b), 256);   // S tile b read by the 128 softmax and the 128 sender threads
       mbar_init(pfull(b), 128);
-      mbar_init(sread(b), 128);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(xfull(b), 1);   // armed locally with the tile's bytes, filled by the partner's bulk copy
@@ -233,10 +242,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
     if (lane == 0) {
       // rope columns of Q into shared memory; the q_nope columns (through the
       // still idle stage buffers) for the softmax warps to move into TMEM
-      mbar_arrive_expect_tx(b_qsfull, C::QRBYTES);
+      mbar_arrive_expect_tx(b_qsfull, C::QRBYTES + C::QS_CH * C::QCHUNK);
       tma_load_2d(sbase + C::OFF_QR, &p.tm_qp, static_cast<int>(crank) * C::RH, row * p.H, b_qsfull);
-      mbar_arrive_expect_tx(b_qtfull, C::NPV * C::QCHUNK);
-      for (int ch = 0; ch < C::NPV; ++ch)
+      for (int ch = C::QT_CH; ch < C::NPV; ++ch)
+        tma_load_2d(sbase + C::OFF_QS + (ch - C::QT_CH) * C::QCHUNK, &p.tm_qn,
+                    static_cast<int>(crank) * C::HALF + ch * 64, row * p.H, b_qsfull);
+      mbar_arrive_expect_tx(b_qtfull, C::QT_CH * C::QCHUNK);
+      for (int ch = 0; ch < C::QT_CH; ++ch)
         tma_load_2d(sbase + C::OFF_K + ch * C::QCHUNK, &p.tm_qn, static_cast<int>(crank) * C::HALF + ch * 64,
                     row * p.H, b_qtfull);
       bool ok = mbar_wait(b_qsfull, 0, abort_flag, p.err) && mbar_wait(b_qtdone, 0, abort_flag, p.err);
@@ -244,6 +256,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
       // descriptors are built once; a K step of 16 columns adds 32 bytes (2
       // encoded), a stage adds STAGE / 16
       const uint64_t qrdesc = smem_desc(sbase + C::OFF_QR, 16, 512, kSwizzle64);
+      const uint64_t qsdesc = smem_desc(sbase + C::OFF_QS, 16, 1024, kSwizzle128);
       const uint64_t kdesc0 = smem_desc(sbase + C::OFF_K, 16, 1024, kSwizzle128);
       const uint64_t krdesc0 = smem_desc(sbase + C::OFF_K + C::NPV * C::CHUNK, 16, 512, kSwizzle64);
       const uint64_t vdesc0 = smem_desc(sbase + C::OFF_K, C::CHUNK, 1024, kSwizzle128);
@@ -254,7 +267,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
       uint32_t idle = 0;
       while (ok && np < ntiles) {
         bool progressed = false;
-        if (nq < ntiles && nq < np + 2) {
+        if (nq < ntiles) {
           const int st = nq % NS, sb = nq & 1;
           if (mbar_test(kfull(st), (nq / NS) & 1) && mbar_test(sempty(sb), ((nq >> 1) & 1) ^ 1)) {
             fence_proxy_async_smem();   // the gathered tile feeds the tensor core
@@ -262,11 +275,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
             const uint32_t s_tmem = tmem_base + C::S_COL + sb * T;
             const uint64_t kd = kdesc0 + st * kStageStep, krd = krdesc0 + st * kStageStep;
 #pragma unroll
-            for (int ch = 0; ch < C::NPV; ++ch)          // q_nope columns in tensor memory
+            for (int ch = 0; ch < C::QT_CH; ++ch)        // q_nope chunks in tensor memory
 #pragma unroll
               for (int k = 0; k < 4; ++k)
                 mma_f16_ts(s_tmem, tmem_base + ch * 32 + k * 8, kd + (ch * C::CHUNK >> 4) + 2 * k, C::IDESC_QK,
                            (ch | k) ? 1u : 0u);
+#pragma unroll
+            for (int ch = C::QT_CH; ch < C::NPV; ++ch)   // q_nope chunks in shared memory
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                mma_f16_ss(s_tmem, qsdesc + ((ch - C::QT_CH) * C::QCHUNK >> 4) + 2 * k,
+                           kd + (ch * C::CHUNK >> 4) + 2 * k, C::IDESC_QK, 1u);
 #pragma unroll
             for (int k = 0; k < 2; ++k)                  // rope columns in shared memory
               mma_f16_ss(s_tmem, qrdesc + 2 * k, krd + 2 * k, C::IDESC_QK, 1u);
@@ -277,15 +296,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
         }
         if (np < nq && mbar_test(pfull(np & 1), (np >> 1) & 1)) {
           tc_fence_after();
-          const int st = np % NS, sb = np & 1;
-          const uint32_t p_tmem = tmem_base + C::S_COL + sb * T;
+          const int st = np % NS;
+          const uint32_t p_tmem = tmem_base + C::P_COL;
 #pragma unroll
           for (int k = 0; k < T / 16; ++k)
             mma_f16_ts(o_tmem, p_tmem + k * 8, vdesc0 + st * kStageStep + (k * 16 * 128 >> 4), C::IDESC_PV,
                        (np > 0 || k > 0) ? 1u : 0u);
           mma_commit(b_pvdone);
           mma_commit(kempty(st));
-          mma_commit(sempty(sb));
           ++np;
           progressed = true;
         }
@@ -427,50 +445,55 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
   } else if (warp >= kSendWarp0) {
     // ------------------------------------------------------------ senders
     // Warp q (heads 32q..32q+31) copies its rows of this CTA's partial logits
-    // of every tile, as soon as its QK is done, into x_out (row h, 16-byte
-    // chunks swizzled by h) and bulk-copies those 8 KB into the partner's
-    // x_in[u & 1] once all four partner softmax warps have read tile u-2 from
-    // it (a bulk copy lands ~1 us sooner than the same bytes sent by st.async
-    // from registers).  The S tile may be overwritten by P once every sender
-    // has read it (sread).
+    // of every tile, as soon as its QK is done, into its x_out slot (16 rows
+    // at a time, row h's 16-byte chunks swizzled by h) and bulk-copies them
+    // into the partner's x_in[u % XBUF] once all four partner softmax warps have
+    // read tile u-2 from it (a bulk copy lands ~1 us sooner than the same
+    // bytes sent by st.async from registers).  The S tile is released (sempty)
+    // once its values are in registers.
     const int quad = warp & 3;
     const int h = quad * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t row_off = static_cast<uint32_t>(quad) * (C::XBYTES / 4);
-    const uint32_t x_out = sbase + C::OFF_X + 2 * C::XBYTES;
+    const uint32_t slot = sbase + C::OFF_X + C::XBUF * C::XBYTES + quad * (C::XOUT / 4);
     const uint32_t peer_x_in0 = map_to_cta(sbase + C::OFF_X, peer);
     for (int u = 0; u < ntiles; ++u) {
       const int b = u & 1;
       const uint32_t use = static_cast<uint32_t>(u >> 1);
       if (!mbar_wait(sfull(b), use & 1, abort_flag, p.err)) break;
       tc_fence_after();
-      if (lane == 0) bulk_wait_read_all();   // this warp's copy of tile u-1 has read its x_out rows
-      __syncwarp();
       float v[T];
 #pragma unroll
       for (int c0 = 0; c0 < T; c0 += 16)
         tmem_ld16(tmem_base + lane_base + C::S_COL + b * T + c0, *reinterpret_cast<float(*)[16]>(v + c0));
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(sread(b));
-#pragma unroll
-      for (int c = 0; c < T / 4; ++c)
-        st_shared_v4(x_out + h * 256 + ((c ^ (h & 15)) << 4),
-                     make_uint4(__float_as_uint(v[4 * c]), __float_as_uint(v[4 * c + 1]), __float_as_uint(v[4 * c + 2]),
-                                __float_as_uint(v[4 * c + 3])));
-      fence_proxy_async_smem();
-      __syncwarp();
+      mbar_arrive(sempty(b));
       int sent_ok = 1;
-      if (lane == 0) {
-        if (mbar_wait<true>(xfree(b), (use & 1) ^ 1, abort_flag, p.err)) {
-          bulk_copy_to_cta(peer_x_in0 + b * C::XBYTES + row_off, x_out + row_off, C::XBYTES / 4,
-                           map_to_cta(xfull(b), peer));
+      const int xb = u % C::XBUF;
+      const uint32_t xuse = static_cast<uint32_t>(u / C::XBUF);
+      if (lane == 0) sent_ok = mbar_wait<true>(xfree(xb), (xuse & 1) ^ 1, abort_flag, p.err) ? 1 : 0;
+      if (__shfl_sync(0xffffffffu, sent_ok, 0) == 0) break;
+      const uint32_t dst = peer_x_in0 + xb * C::XBYTES + static_cast<uint32_t>(quad * 32) * 256;
+      const uint32_t bar = map_to_cta(xfull(xb), peer);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        if (lane == 0) bulk_wait_read_all();   // the slot's previous copy has been read
+        __syncwarp();
+        if ((lane >> 4) == hh) {
+          const uint32_t r = slot + (lane & 15) * 256;
+#pragma unroll
+          for (int c = 0; c < T / 4; ++c)
+            st_shared_v4(r + ((c ^ (h & 15)) << 4),
+                         make_uint4(__float_as_uint(v[4 * c]), __float_as_uint(v[4 * c + 1]),
+                                    __float_as_uint(v[4 * c + 2]), __float_as_uint(v[4 * c + 3])));
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) {
+          bulk_copy_to_cta(dst + hh * (C::XOUT / 4), slot, C::XOUT / 4, bar);   // 16 rows of 256 bytes
           bulk_commit();
-        } else {
-          sent_ok = 0;
         }
       }
-      if (__shfl_sync(0xffffffffu, sent_ok, 0) == 0) break;
     }
     if (lane == 0) bulk_wait_read_all();   // x_out stays valid until every copy has read it
   } else {
@@ -483,7 +506,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
       // this head's row of the q_nope columns: from the staged swizzled
       // chunks into TMEM (bf16 pairs, lower column in the low half)
 #pragma unroll 1
-      for (int ch = 0; ch < C::NPV; ++ch) {
+      for (int ch = 0; ch < C::QT_CH; ++ch) {
         const uint8_t *src = smem + C::OFF_K + ch * C::QCHUNK + h * 128;
         uint32_t v[32];
 #pragma unroll
@@ -513,7 +536,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
       }
       const int sb = t & 1;
       const uint32_t use = static_cast<uint32_t>(t >> 1);
-      if (h == 0) mbar_arrive_expect_tx(xfull(sb), C::XBYTES);
+      const int xb = t % C::XBUF;
+      if (h == 0) mbar_arrive_expect_tx(xfull(xb), C::XBYTES);
       if (!mbar_wait(sfull(sb), use & 1, abort_flag, p.err)) { ok = false; break; }
       tc_fence_after();
       float s[T];
@@ -521,10 +545,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
       for (int c0 = 0; c0 < T; c0 += 16)
         tmem_ld16(tmem_base + lane_base + C::S_COL + sb * T + c0, *reinterpret_cast<float(*)[16]>(s + c0));
       tmem_ld_wait();
-      // full logits of tile t: our partial + the partner's (x_in[sb])
-      if (!mbar_wait<true>(xfull(sb), use & 1, abort_flag, p.err)) { ok = false; break; }
+      // full logits of tile t: our partial + the partner's (x_in[xb])
+      if (!mbar_wait<true>(xfull(xb), (t / C::XBUF) & 1, abort_flag, p.err)) { ok = false; break; }
       {
-        const float4 *xr = reinterpret_cast<const float4 *>(smem + C::OFF_X + sb * C::XBYTES + h * 256);
+        const float4 *xr = reinterpret_cast<const float4 *>(smem + C::OFF_X + xb * C::XBYTES + h * 256);
 #pragma unroll
         for (int c = 0; c < T / 4; ++c) {
           const float4 v = xr[c ^ (h & 15)];
@@ -535,8 +559,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
           s[4 * c + 3] += v.w;
         }
       }
-      __syncwarp();   // this warp's rows of x_in[sb] have been read
-      if (lane == 0) mbar_arrive_remote_relaxed(map_to_cta(xfree(sb), peer));
+      __syncwarp();   // this warp's rows of x_in[xb] have been read
+      if (lane == 0) mbar_arrive_remote_relaxed(map_to_cta(xfree(xb), peer));
+      tc_fence_before();
+      mbar_arrive(sempty(sb));   // our partial is in registers: the S tile can take QK of tile t+2
 
       // online softmax in base 2 with a lazily moved reference max
       // (scale_log2 > 0, so the max of the raw logits picks the same key)
@@ -554,11 +580,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
         alpha = fast_exp2(m_ref - tmax);
         m_ref = tmax;
       }
-      // O must hold every earlier tile before it is rescaled (QK of this tile
-      // waited for PV of tile t-2, so only PV of t-1 can still be running)
-      if (rescale && t > 0) {
+      // PV of tile t-1 must be done before P is overwritten and before O is
+      // rescaled (PV of t-2 finished before PV of t-1 was issued)
+      if (t > 0) {
         if (!mbar_wait(b_pvdone, (t - 1) & 1, abort_flag, p.err)) { ok = false; break; }
         tc_fence_after();
+      }
+      if (rescale && t > 0) {
 #pragma unroll 1
         for (int c0 = 0; c0 < C::HALF; c0 += 16) {
           float o[16];
@@ -569,9 +597,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
           tmem_st16(tmem_base + lane_base + C::O_COL + c0, o);
         }
       }
-      // P (bf16 pairs, lower key in the low half) over the first T/2 columns
-      // of this S tile, once the senders have read it; written in two halves
-      if (!mbar_wait(sread(sb), use & 1, abort_flag, p.err)) { ok = false; break; }
+      // P (bf16 pairs, lower key in the low half) into its columns, in two halves
       float sm[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int half2 = 0; half2 < 2; ++half2) {
@@ -585,7 +611,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
           sm[(i >> 1) & 3] += pf.x + pf.y;
           packed[i / 2] = *reinterpret_cast<const uint32_t *>(&pb);
         }
-        tmem_st16(tmem_base + lane_base + C::S_COL + sb * T + half2 * (T / 4),
+        tmem_st16(tmem_base + lane_base + C::P_COL + half2 * (T / 4),
                   *reinterpret_cast<const float(*)[16]>(packed));
       }
       l = l * alpha + ((sm[0] + sm[1]) + (sm[2] + sm[3]));

@@ -18,7 +18,8 @@
 //
 // Warp roles (192 threads): warp 0 TMA producer, warp 1 MMA issuer (one
 // thread) and TMEM owner, warps 2-5 epilogue.  The grid is persistent: each
-// CTA walks a tile-balanced contiguous range of the plan's work items.
+// CTA walks a tile-balanced contiguous range of the plan's work items; single-
+// row groups (decode) run two CTAs per SM.
 //
 // The fp8 index format (132-byte keys) runs index_fp8_tc_kernel, the same
 // contraction behind a code -> bf16 conversion stage.  Shapes outside the
@@ -49,7 +50,9 @@ struct IdxTraits {
   static constexpr int KT_BYTES = 128 * DI * 2;
   static constexpr int Q_BYTES = N * DI * 2;
   static constexpr int QBUF = (G == 1) ? 2 : 1;
-  static constexpr int STAGES_MAX = (G == 1) ? 6 : 4;
+  // single-row groups run two CTAs per SM with two stages each: two
+  // independent pipelines keep more of HBM busy than one CTA with six stages
+  static constexpr int STAGES_MAX = (G == 1) ? 2 : 4;
   static constexpr int STAGES = (STAGES_MAX * KT_BYTES + QBUF * Q_BYTES <= 200 * 1024) ? STAGES_MAX : 3;
   static constexpr int TMEM_COLS = (2 * N <= 32) ? 32 : (2 * N <= 64) ? 64 : (2 * N <= 128) ? 128 : (2 * N <= 256) ? 256 : 512;
   static constexpr uint32_t IDESC = mma_idesc(128, N, 1u, false, false);
@@ -81,7 +84,7 @@ struct IdxParams {
 };
 
 template <int HI, int DI, int G>
-__global__ void __launch_bounds__(kIdxThreads, 1) index_tc_kernel(const __grid_constant__ IdxParams p) {
+__global__ void __launch_bounds__(kIdxThreads, 2) index_tc_kernel(const __grid_constant__ IdxParams p) {
   using C = IdxTraits<HI, DI, G>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -858,7 +861,7 @@ bool indexer_tc_supported(const dsa_config_t &c, int G) {
 
 int indexer_group_rows(const dsa_config_t &c) { return indexer_tc_supported(c, 4) ? 4 : 1; }
 
-int indexer_ctas_per_sm(const dsa_config_t &, int) { return 1; }
+int indexer_ctas_per_sm(const dsa_config_t &c, int G) { return (c.index_fmt == DSA_INDEX_BF16 && G == 1) ? 2 : 1; }
 
 cudaError_t launch_index_scores(const dsa_ctx *ctx, const dsa_plan_t *plan, const void *q, const float *w,
                                 const void *cache, float *scores, cudaStream_t s, int32_t *launches) {
