@@ -315,9 +315,25 @@ dsa_status dsa_plan(dsa_ctx_t *ctx, const dsa_span_t *spans, int32_t num_spans, 
   std::vector<AttCombine> combines;
   {
     const int64_t K = c.topk;
+    // A row is one two-CTA cluster; `pairs` clusters run at a time.  Rows are
+    // split over key ranges only when that shortens the estimated time:
+    // waves x (a unit's fixed start-up, about ten tile periods, + its tiles),
+    // plus the merge of the partials (about 0.15 tile periods per row).
     const int pairs = std::max(1, ctx->num_sms / 2);
+    const int64_t full_tiles = (K + kAttTile - 1) / kAttTile;
     int splits = 1;
-    if (T > 0 && T < 2 * pairs) splits = static_cast<int>(std::min<int64_t>(16, (2 * pairs + T - 1) / T));
+    if (T > 0) {
+      double best = 0.0;
+      for (int sp = 1; sp <= 16 && sp <= std::max<int64_t>(1, full_tiles / 2); ++sp) {
+        const int64_t waves = (static_cast<int64_t>(T) * sp + pairs - 1) / pairs;
+        const double est = static_cast<double>(waves) * (10.0 + static_cast<double>((full_tiles + sp - 1) / sp)) +
+                           (sp > 1 ? 0.15 * static_cast<double>(T) : 0.0);
+        if (sp == 1 || est < best) {
+          best = est;
+          splits = sp;
+        }
+      }
+    }
     int32_t slot = 0;
     int32_t row = 0;
     for (int32_t i = 0; i < num_spans; ++i) {
