@@ -261,12 +261,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
       const uint64_t krdesc0 = smem_desc(sbase + C::OFF_K + C::NPV * C::CHUNK, 16, 512, kSwizzle64);
       const uint64_t vdesc0 = smem_desc(sbase + C::OFF_K, C::CHUNK, 1024, kSwizzle128);
       constexpr uint64_t kStageStep = C::STAGE >> 4;
-      // issue QK of the next tile or PV of the oldest softmaxed tile, whichever is ready
+      // issue PV of the oldest softmaxed tile or QK of the next tile, whichever
+      // is ready, PV first: it releases the stage and the P columns, while QK
+      // only runs ahead
       int nq = 0, np = 0;
       uint64_t idle_since = 0;
       uint32_t idle = 0;
       while (ok && np < ntiles) {
         bool progressed = false;
+        if (np < nq && mbar_test(pfull(np & 1), (np >> 1) & 1)) {
+          tc_fence_after();
+          const int st = np % NS;
+          const uint32_t p_tmem = tmem_base + C::P_COL;
+#pragma unroll
+          for (int k = 0; k < T / 16; ++k)
+            mma_f16_ts(o_tmem, p_tmem + k * 8, vdesc0 + st * kStageStep + (k * 16 * 128 >> 4), C::IDESC_PV,
+                       (np > 0 || k > 0) ? 1u : 0u);
+          mma_commit(b_pvdone);
+          mma_commit(kempty(st));
+          ++np;
+          progressed = true;
+        }
         if (nq < ntiles) {
           const int st = nq % NS, sb = nq & 1;
           if (mbar_test(kfull(st), (nq / NS) & 1) && mbar_test(sempty(sb), ((nq >> 1) & 1) ^ 1)) {
@@ -293,19 +308,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
             ++nq;
             progressed = true;
           }
-        }
-        if (np < nq && mbar_test(pfull(np & 1), (np >> 1) & 1)) {
-          tc_fence_after();
-          const int st = np % NS;
-          const uint32_t p_tmem = tmem_base + C::P_COL;
-#pragma unroll
-          for (int k = 0; k < T / 16; ++k)
-            mma_f16_ts(o_tmem, p_tmem + k * 8, vdesc0 + st * kStageStep + (k * 16 * 128 >> 4), C::IDESC_PV,
-                       (np > 0 || k > 0) ? 1u : 0u);
-          mma_commit(b_pvdone);
-          mma_commit(kempty(st));
-          ++np;
-          progressed = true;
         }
         if (progressed) {
           idle = 0;
