@@ -3,7 +3,9 @@
 // selection must not depend on the batch packing or the device, so equal
 // scores are broken toward the lower position).
 //
-// One CTA per row.  Scores are mapped to order-preserving 32-bit keys (-0.0
+// CTAs select one row at a time: 1024 threads with a row each when a step
+// has at most one row per SM, else 512-thread CTAs, two per SM, taking rows
+// in turn.  Scores are mapped to order-preserving 32-bit keys (-0.0
 // ranks as +0.0).  The selection is exact; only the amount of work depends on
 // the data:
 //   1. candidates: a row with at most kCandCap keys takes all of them.  A
@@ -27,21 +29,26 @@
 // A row that sees at most topk keys takes them all and pads with -1.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "dsa_internal.h"
 #include "ptx.cuh"
 
 namespace dsa {
 namespace {
 
-constexpr int kTopkThreads = 1024;
-constexpr int kTopkWarps = kTopkThreads / 32;
+// CTA sizes: 1024 threads, one CTA per SM, when every row has its own CTA;
+// 512 threads, two per SM, when persistent CTAs take several rows each
+constexpr int kMaxWarps = 32;
 constexpr int kBatch = 8;             // independent loads in flight per thread
 constexpr int kCandCap = 8192;        // candidate keys held in shared memory
 constexpr int kSampleMin = 4096;      // a strided sample holds kSampleMin .. 2*kSampleMin-1 keys
 constexpr int kBitmapWords = 8192;    // 262,144 positions
 constexpr int kTieCap = 2048;         // tau ties ranked by position in shared memory
 
+template <int NT>
 struct TopkSmem {
+  static constexpr int kWarps = NT / 32;
   union {
     uint32_t sample[2 * kSampleMin];
     uint32_t bits[kBitmapWords];
@@ -49,10 +56,10 @@ struct TopkSmem {
   uint32_t ckey[kCandCap];
   int32_t cpos[kCandCap];
   int hist[2048];                     // radix histograms; tie positions during output
-  int ws[kTopkWarps];
+  int ws[kWarps];
   int res[2];
   int n_cand, n_tie;
-  int wgt[kTopkWarps], weq[kTopkWarps];
+  int wgt[kWarps], weq[kWarps];
 };
 
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -62,7 +69,10 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 }
 
 // Exclusive prefix sum over the block of one int per thread; *total gets the sum.
+template <int NT>
 __device__ __forceinline__ int block_exclusive_scan(int v, int *ws, int *total) {
+  constexpr int kTopkWarps = NT / 32;
+  static_assert(kTopkWarps <= kMaxWarps, "one warp scans the per-warp sums");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
 #pragma unroll
@@ -73,13 +83,13 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *ws, int *total) 
   if (lane == 31) ws[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int s = ws[lane];
+    int s = lane < kTopkWarps ? ws[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, s, o);
       if (lane >= o) s += y;
     }
-    ws[lane] = s;
+    if (lane < kTopkWarps) ws[lane] = s;
   }
   __syncthreads();
   const int before = warp ? ws[warp - 1] : 0;
@@ -90,9 +100,9 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *ws, int *total) 
 
 // Bin (counted from the top) that holds the need-th largest key of a
 // histogram of NB <= 2048 bins; *above gets the number of keys in higher bins.
-template <int NB>
+template <int NB, int NT>
 __device__ __forceinline__ int find_bin(const int *hist, int need, int *ws, int *res, int *above) {
-  constexpr int PER = NB >= kTopkThreads ? NB / kTopkThreads : 1;
+  constexpr int PER = NB >= NT ? NB / NT : 1;
   int c[PER];
   int sum = 0;
 #pragma unroll
@@ -102,7 +112,7 @@ __device__ __forceinline__ int find_bin(const int *hist, int need, int *ws, int 
     sum += c[j];
   }
   int total;
-  int run = block_exclusive_scan(sum, ws, &total);
+  int run = block_exclusive_scan<NT>(sum, ws, &total);
 #pragma unroll
   for (int j = 0; j < PER; ++j) {
     if (run < need && need <= run + c[j]) {
@@ -122,23 +132,23 @@ __device__ __forceinline__ int find_bin(const int *hist, int need, int *ws, int 
 // (called as for_each(visit) with visit(key) for every key, by every thread
 // over its share), by three radix passes of 11, 11 and 10 bits.  *ties gets
 // how many keys equal to the result lie within the top `rank`.
-template <typename ForEach>
-__device__ __forceinline__ uint32_t radix_select(ForEach for_each, int rank, TopkSmem &sm, int *ties) {
+template <int NT, typename ForEach>
+__device__ __forceinline__ uint32_t radix_select(ForEach for_each, int rank, TopkSmem<NT> &sm, int *ties) {
   uint32_t prefix = 0, pmask = 0;
   int need = rank;
 #pragma unroll 1
   for (int pass = 0; pass < 3; ++pass) {
     const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
     const int nbins = pass == 2 ? 1024 : 2048;
-    for (int i = threadIdx.x; i < 2048; i += kTopkThreads) sm.hist[i] = 0;
+    for (int i = threadIdx.x; i < 2048; i += NT) sm.hist[i] = 0;
     __syncthreads();
     for_each([&](uint32_t key) {
       if ((key & pmask) == prefix) atomicAdd(&sm.hist[(key >> shift) & (nbins - 1)], 1);
     });
     __syncthreads();
     int above;
-    const int b = pass == 2 ? find_bin<1024>(sm.hist, need, sm.ws, sm.res, &above)
-                            : find_bin<2048>(sm.hist, need, sm.ws, sm.res, &above);
+    const int b = pass == 2 ? find_bin<1024, NT>(sm.hist, need, sm.ws, sm.res, &above)
+                            : find_bin<2048, NT>(sm.hist, need, sm.ws, sm.res, &above);
     prefix |= static_cast<uint32_t>(b) << shift;
     pmask |= static_cast<uint32_t>(nbins - 1) << shift;
     need -= above;
@@ -159,14 +169,12 @@ __device__ __forceinline__ int warp_append(bool take, int *counter) {
   return take ? base + __popc(m & ((1u << lane) - 1u)) : -1;
 }
 
-__global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const float *__restrict__ scores,
-                                                               const int64_t *__restrict__ row_score_off,
-                                                               const int32_t *__restrict__ row_pos, int K,
-                                                               int32_t *__restrict__ sel) {
-  extern __shared__ uint8_t topk_smem_raw[];
-  TopkSmem &sm = *reinterpret_cast<TopkSmem *>(topk_smem_raw);
-
-  const int row = blockIdx.x;
+template <int NT>
+__device__ __forceinline__ void select_row(const float *__restrict__ scores, const int64_t *__restrict__ row_score_off,
+                                           const int32_t *__restrict__ row_pos, int K, int32_t *__restrict__ sel,
+                                           int row, TopkSmem<NT> &sm) {
+  constexpr int kTopkThreads = NT;
+  constexpr int kTopkWarps = NT / 32;
   const int n = row_pos[row] + 1;
   int32_t *out = sel + static_cast<int64_t>(row) * K;
   if (n <= K) {
@@ -198,7 +206,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const float *__re
     int rank = static_cast<int>(1.15f * ks + 3.f * sqrtf(ks)) + 8;
     rank = min(rank, m);
     int unused;
-    const uint32_t l0 = radix_select(
+    const uint32_t l0 = radix_select<NT>(
         [&](auto visit) {
           for (int j = tid; j < m; j += kTopkThreads) visit(sm.sample[j]);
         },
@@ -231,13 +239,13 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const float *__re
   int need;
   uint32_t tau;
   if (cand_ok) {
-    tau = radix_select(
+    tau = radix_select<NT>(
         [&](auto visit) {
           for (int i = tid; i < n_cand; i += kTopkThreads) visit(sm.ckey[i]);
         },
         K, sm, &need);
   } else {
-    tau = radix_select(
+    tau = radix_select<NT>(
         [&](auto visit) {
           for (int base = 0; base < n; base += kTopkThreads * kBatch) {
             uint32_t k[kBatch];
@@ -293,7 +301,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const float *__re
       for (int q = 0; q < per; ++q)
         if (w0 + q < nw) cnt += __popc(sm.bits[w0 + q]);
       int tot;
-      int slot = block_exclusive_scan(cnt, sm.ws, &tot);
+      int slot = block_exclusive_scan<NT>(cnt, sm.ws, &tot);
       for (int q = 0; q < per; ++q) {
         if (w0 + q >= nw) break;
         uint32_t b = sm.bits[w0 + q];
@@ -361,21 +369,49 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const float *__re
   }
 }
 
+
+template <int NT>
+__global__ void __launch_bounds__(NT, 1024 / NT) topk_kernel(const float *__restrict__ scores,
+                                                           const int64_t *__restrict__ row_score_off,
+                                                           const int32_t *__restrict__ row_pos, int T, int K,
+                                                           int32_t *__restrict__ sel) {
+  extern __shared__ uint8_t topk_smem_raw[];
+  TopkSmem<NT> &sm = *reinterpret_cast<TopkSmem<NT> *>(topk_smem_raw);
+  // CTA b takes rows b, b + gridDim.x, ...
+  for (int row = blockIdx.x; row < T; row += gridDim.x) {
+    __syncthreads();   // shared memory of the previous row is no longer read
+    select_row<NT>(scores, row_score_off, row_pos, K, sel, row, sm);
+  }
+}
+
+template <int NT>
+cudaError_t run_topk(const float *scores, const int64_t *row_score_off, const int32_t *row_pos, int T, int K,
+                     int32_t *sel, int grid, cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(topk_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(sizeof(TopkSmem<NT>)));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  topk_kernel<NT><<<grid, NT, sizeof(TopkSmem<NT>), s>>>(scores, row_score_off, row_pos, T, K, sel);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const dsa_ctx *ctx, const dsa_plan_t *plan, const float *scores, int32_t *sel,
                         cudaStream_t s, int32_t *launches) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(sizeof(TopkSmem)));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  topk_kernel<<<plan->T, kTopkThreads, sizeof(TopkSmem), s>>>(scores, plan->row_score_off, plan->row_pos,
-                                                               ctx->cfg.topk, sel);
+  // up to one row per SM: 1024-thread CTAs, one row each; more rows: 512-thread
+  // CTAs, two per SM, each taking rows in turn
+  cudaError_t e;
+  if (plan->T <= ctx->num_sms)
+    e = run_topk<1024>(scores, plan->row_score_off, plan->row_pos, plan->T, ctx->cfg.topk, sel, std::max(1, plan->T), s);
+  else
+    e = run_topk<512>(scores, plan->row_score_off, plan->row_pos, plan->T, ctx->cfg.topk, sel,
+                      std::min(plan->T, 2 * ctx->num_sms), s);
   *launches += 1;
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace dsa

@@ -167,6 +167,25 @@ def test_topk_paths():
     H.check_selection(g, ref, sc, off, K, exact=True)
 
 
+def test_topk_many_rows_per_cta():
+    """More rows than the persistent selection grid holds CTAs, so each CTA
+    selects several rows in turn (its shared memory reused between rows)."""
+    sh = W.DSAShape(**W.DEEPSEEK)
+    rng = np.random.default_rng(13)
+    lens = rng.integers(2049, 12000, size=700)
+    rows = [rng.standard_normal(int(n)).astype(np.float32) for n in lens]
+    wl = W.build_workload("topk_many", sh, [(len(r) - 1, 1) for r in rows], seed=14)
+    off = np.zeros(len(rows) + 1, np.int64)
+    off[1:] = np.cumsum([len(r) for r in rows])
+    sc = np.concatenate(rows)
+    ref = oracle.topk(sh, wl.spans, sc, off)
+    ctx = dsa.Context(sh, 0)
+    plan = ctx.plan(wl.spans, wl.num_pages)
+    g = ctx.topk_from_scores(plan, torch.from_numpy(sc).cuda()).cpu().numpy()
+    ctx.get_error()
+    H.check_selection(g, ref, sc, off, sh.topk, exact=True)
+
+
 def test_bounds_errors_are_reported_not_faulted():
     """Selected positions past the row or below -1 set DSA_ERR_BOUNDS and are skipped."""
     wl = H.deepseek_small(seed=7, decode_ctx=(3000,), chunk=None)
