@@ -488,6 +488,33 @@ dsa_status dsa_store_keys(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *ke
   return cuda_status(ctx, e);
 }
 
+dsa_status dsa_quantize_store_keys(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *keys_bf16,
+                                   void *index_cache, dsa_stream_t stream) {
+  dsa_status st = check_call(ctx, plan);
+  if (st != DSA_OK) return st;
+  ctx->last_launches = 0;
+  if (ctx->cfg.index_fmt != DSA_INDEX_FP8_132 || ctx->cfg.index_dim != 128) return DSA_ERR_UNSUPPORTED;
+  if (plan->T == 0) return DSA_OK;
+  if (!keys_bf16 || !index_cache) return DSA_ERR_INVALID_ARG;
+  cudaError_t e = launch_quantize_keys(ctx, plan, keys_bf16, index_cache, reinterpret_cast<cudaStream_t>(stream),
+                                       &ctx->last_launches);
+  return cuda_status(ctx, e);
+}
+
+dsa_status dsa_quantize_store_latents(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *latents_bf16,
+                                      void *latent_cache, dsa_stream_t stream) {
+  dsa_status st = check_call(ctx, plan);
+  if (st != DSA_OK) return st;
+  ctx->last_launches = 0;
+  if (ctx->cfg.latent_fmt != DSA_LATENT_FP8_656 || ctx->cfg.kv_lora_rank != 512 || ctx->cfg.rope_dim != 64)
+    return DSA_ERR_UNSUPPORTED;
+  if (plan->T == 0) return DSA_OK;
+  if (!latents_bf16 || !latent_cache) return DSA_ERR_INVALID_ARG;
+  cudaError_t e = launch_quantize_latents(ctx, plan, latents_bf16, latent_cache,
+                                          reinterpret_cast<cudaStream_t>(stream), &ctx->last_launches);
+  return cuda_status(ctx, e);
+}
+
 dsa_status dsa_index_scores(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *q, const float *w,
                             const void *index_cache, float *scores, dsa_stream_t stream) {
   dsa_status st = check_call(ctx, plan);

@@ -105,6 +105,10 @@ namespace dsa {
 
 // Launchers (each returns cudaGetLastError() after its launches and adds the
 // number of kernels it launched to *launches).
+cudaError_t launch_quantize_keys(const dsa_ctx *ctx, const dsa_plan_t *plan, const void *keys, void *cache,
+                                 cudaStream_t s, int32_t *launches);
+cudaError_t launch_quantize_latents(const dsa_ctx *ctx, const dsa_plan_t *plan, const void *latents, void *cache,
+                                    cudaStream_t s, int32_t *launches);
 cudaError_t launch_store_keys(const dsa_ctx *ctx, const dsa_plan_t *plan, const void *keys, void *cache,
                               cudaStream_t s, int32_t *launches);
 cudaError_t launch_index_scores(const dsa_ctx *ctx, const dsa_plan_t *plan, const void *q, const float *w,

@@ -32,7 +32,8 @@ STATUS_NAMES = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_SHORT_HISTORY
 
 EXPORTED = ["dsa_create", "dsa_destroy", "dsa_plan", "dsa_plan_destroy", "dsa_plan_get_info", "dsa_store_keys",
             "dsa_index_topk", "dsa_index_scores", "dsa_topk_from_scores", "dsa_attend", "dsa_get_error",
-            "dsa_last_launch_count", "dsa_status_str", "dsa_index_topk_static", "dsa_last_cuda_error"]
+            "dsa_last_launch_count", "dsa_status_str", "dsa_index_topk_static", "dsa_last_cuda_error",
+            "dsa_quantize_store_keys", "dsa_quantize_store_latents"]
 
 
 class DSAError(RuntimeError):
@@ -85,6 +86,8 @@ def load() -> ctypes.CDLL:
     L.dsa_plan_destroy.restype = None
     L.dsa_plan_get_info.argtypes = [vp, ctypes.POINTER(PlanInfo)]
     L.dsa_store_keys.argtypes = [vp, vp, vp, vp, vp]
+    L.dsa_quantize_store_keys.argtypes = [vp, vp, vp, vp, vp]
+    L.dsa_quantize_store_latents.argtypes = [vp, vp, vp, vp, vp]
     L.dsa_index_topk.argtypes = [vp, vp, vp, vp, vp, vp, vp]
     L.dsa_index_scores.argtypes = [vp, vp, vp, vp, vp, vp, vp]
     L.dsa_index_topk_static.argtypes = [vp, vp, vp, vp, vp, vp, vp]
@@ -98,7 +101,8 @@ def load() -> ctypes.CDLL:
     L.dsa_status_str.argtypes = [i32]
     L.dsa_status_str.restype = ctypes.c_char_p
     for name in ("dsa_create", "dsa_plan", "dsa_plan_get_info", "dsa_store_keys", "dsa_index_topk", "dsa_index_topk_static",
-                 "dsa_index_scores", "dsa_topk_from_scores", "dsa_attend", "dsa_get_error"):
+                 "dsa_index_scores", "dsa_topk_from_scores", "dsa_attend", "dsa_get_error", "dsa_quantize_store_keys",
+                 "dsa_quantize_store_latents"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -223,6 +227,21 @@ class Context:
         _check(load().dsa_store_keys(self.handle, plan.handle, _ptr(keys, d, (torch.bfloat16, torch.uint8), "keys"),
                                      _ptr(index_cache, d, (torch.bfloat16, torch.uint8), "index_cache"),
                                      _stream(stream)), "dsa_store_keys", self.handle)
+
+    def quantize_store_keys(self, plan: Plan, keys_bf16: torch.Tensor, index_cache: torch.Tensor, stream=None):
+        """bf16 index keys (T, 128) -> 132-byte fp8 rows at each row's slot (fp8 index format only)."""
+        d = self.device
+        _check(load().dsa_quantize_store_keys(self.handle, plan.handle, _ptr(keys_bf16, d, (torch.bfloat16,), "keys"),
+                                              _ptr(index_cache, d, (torch.uint8,), "index_cache"), _stream(stream)),
+               "dsa_quantize_store_keys", self.handle)
+
+    def quantize_store_latents(self, plan: Plan, latents_bf16: torch.Tensor, latent_cache: torch.Tensor, stream=None):
+        """bf16 latent rows (T, 512 + 64) -> 656-byte fp8 rows at each row's slot (fp8 latent format only)."""
+        d = self.device
+        _check(load().dsa_quantize_store_latents(self.handle, plan.handle,
+                                                 _ptr(latents_bf16, d, (torch.bfloat16,), "latents"),
+                                                 _ptr(latent_cache, d, (torch.uint8,), "latent_cache"), _stream(stream)),
+               "dsa_quantize_store_latents", self.handle)
 
     def index_topk(self, plan: Plan, q, w, index_cache, selection=None, stream=None) -> torch.Tensor:
         d = self.device

@@ -138,6 +138,28 @@ dsa_status dsa_plan_get_info(const dsa_plan_t *plan, dsa_plan_info_t *info);
 dsa_status dsa_store_keys(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *keys, void *index_cache,
                           dsa_stream_t stream);
 
+/* Quantize-on-store (an extension: the pages store rows already in cache
+ * format, mstar DSAManager.store_keys; the fp8 row layouts are LLMServingSim's
+ * "What the KV cache actually holds").  Each row is quantised into the slot
+ * of its own position, like dsa_store_keys:
+ *   per group: scale = amax / 448 in fp32 (1 for an all-zero group);
+ *   code = E4M3(x / scale), the fp32 quotient rounded to nearest with ties to
+ *   even, saturating at 448 (the largest finite E4M3 value).
+ * dsa_quantize_store_keys: keys_bf16 (T, 128) bf16 -> 132-byte rows (one group
+ *   per row) in the page-blocked index cache; needs DSA_INDEX_FP8_132 and
+ *   index_dim 128.
+ * dsa_quantize_store_latents: latents_bf16 (T, 512 + 64) bf16 -> 656-byte rows
+ *   (four groups of 128 columns; the 64 rope values copied as bf16); needs
+ *   DSA_LATENT_FP8_656, kv_lora_rank 512, rope_dim 64.
+ * Device pointers, caller-owned; the caches are written in place.  Errors:
+ * DSA_ERR_UNSUPPORTED for other formats or shapes, DSA_ERR_INVALID_ARG for
+ * null pointers; a page id outside the cache sets the device error word
+ * (DSA_ERR_BOUNDS at the next dsa_get_error) and the row is skipped. */
+dsa_status dsa_quantize_store_keys(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *keys_bf16,
+                                   void *index_cache, dsa_stream_t stream);
+dsa_status dsa_quantize_store_latents(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *latents_bf16,
+                                      void *latent_cache, dsa_stream_t stream);
+
 /* Score and select (mstar index_topk + select_topk_causal): q (T, Hi, Di)
  * bf16, w (T, Hi) fp32 (any scales folded in), index_cache as above;
  * selection (T, topk) int32 out: each row's selected positions in ascending

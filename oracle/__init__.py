@@ -19,6 +19,8 @@ Functions (all return numpy arrays):
   topk(shape, spans, scores, offsets)                   -> (T, topk) int32, -1 padded
   attend(shape, spans, num_pages, sel, q_nope, q_pe, latent_cache, sink) -> (T, H, L) float64
   e4m3_values(codes)                                    -> float64 values of e4m3 bytes
+  e4m3_encode(values)                                   -> e4m3 codes of fp32 values
+  quantize_store_keys / quantize_store_latents          -> caches with this step's bf16 rows quantised
 
 Parity status of each function is recorded in the docstring of each test in
 tests/test_oracle_pins.py.
@@ -58,6 +60,11 @@ def lib():
         L.oracle_e4m3_value.restype = ctypes.c_double
         L.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
         L.oracle_store_keys.argtypes = [ctypes.POINTER(_Rows), ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+        L.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        L.oracle_e4m3_encode.restype = ctypes.c_uint8
+        L.oracle_quantize_store_keys.argtypes = [ctypes.POINTER(_Rows), ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+        L.oracle_quantize_store_latents.argtypes = [ctypes.POINTER(_Rows), ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                                    ctypes.c_void_p]
         L.oracle_index_scores.argtypes = [ctypes.POINTER(_Rows), ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
         L.oracle_topk.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
@@ -147,6 +154,33 @@ def store_keys(shape, spans, num_pages, keys, cache) -> np.ndarray:
     out = _np(cache).view(np.uint8).copy()
     _check(lib().oracle_store_keys(ctypes.byref(rt.struct), int(shape.index_fmt), int(shape.index_dim),
                                    k.ctypes.data, out.ctypes.data))
+    return out
+
+
+def e4m3_encode(values) -> np.ndarray:
+    """fp32 values -> E4M3 codes (round to nearest even, saturating at 448)."""
+    v = np.asarray(values, dtype=np.float32).reshape(-1)
+    L = lib()
+    return np.array([L.oracle_e4m3_encode(float(x)) for x in v], dtype=np.uint8)
+
+
+def quantize_store_keys(shape, spans, num_pages, keys_bf16, cache) -> np.ndarray:
+    """bf16 index keys (T, index_dim) -> the 132-byte fp8 rows stored at each row's slot."""
+    rt = RowTable(spans, shape.page_size, num_pages)
+    k = _np(keys_bf16).view(np.uint16)
+    out = _np(cache).view(np.uint8).copy()
+    _check(lib().oracle_quantize_store_keys(ctypes.byref(rt.struct), int(shape.index_dim), k.ctypes.data,
+                                            out.ctypes.data))
+    return out
+
+
+def quantize_store_latents(shape, spans, num_pages, latents_bf16, cache) -> np.ndarray:
+    """bf16 latent rows (T, L + R) -> the 656-byte fp8 rows stored at each row's slot."""
+    rt = RowTable(spans, shape.page_size, num_pages)
+    a = _np(latents_bf16).view(np.uint16)
+    out = _np(cache).view(np.uint8).copy()
+    _check(lib().oracle_quantize_store_latents(ctypes.byref(rt.struct), int(shape.kv_lora_rank), int(shape.rope_dim),
+                                               a.ctypes.data, out.ctypes.data))
     return out
 
 

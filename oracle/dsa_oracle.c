@@ -126,6 +126,91 @@ int oracle_store_keys(const oracle_rows *R, int index_fmt, int index_dim, const 
   return OR_OK;
 }
 
+/* ------------------------------------------------------------------------ */
+/* quantize-on-store (an extension past the pages: they store rows that are  */
+/* already in cache format)                                                  */
+/* ------------------------------------------------------------------------ */
+
+/* fp32 -> E4M3 code, round to nearest with ties to even.  The representable
+ * magnitudes of a binade [2^E, 2^(E+1)) are multiples of 2^(E-3); below 2^-6
+ * (the subnormal range) they are multiples of 2^-9.  Magnitudes at or above
+ * the largest finite value, 448, encode as 448 (the quantiser scales groups so
+ * that nothing exceeds it).  The sign is the sign bit of the input (-0 gives
+ * code 0x80). */
+uint8_t oracle_e4m3_encode(float xf) {
+  const double x = (double)xf;
+  const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+  const double a = fabs(x);
+  if (isnan(a)) return 0x7F;
+  if (a >= 448.0) return sign | 0x7E;
+  int E = (a < ldexp(1.0, -6)) ? -6 : ilogb(a);
+  const double steps = nearbyint(a / ldexp(1.0, E - 3)); /* exact quotient, rounded to even */
+  int k = (int)steps;
+  if (E == -6 && k < 8) return sign | (uint8_t)k;        /* subnormal (or zero) */
+  if (k == 16) {                                          /* rounded up into the next binade */
+    E += 1;
+    k = 8;
+  }
+  return sign | (uint8_t)(((E + 7) << 3) | (k - 8));
+}
+
+/* One group: scale = amax / 448 in fp32 (1 when the group is all zeros),
+ * codes = E4M3(x / scale) with the quotient rounded to fp32 first. */
+static float quantize_group(const uint16_t *src, int n, uint8_t *codes) {
+  float amax = 0.0f;
+  for (int i = 0; i < n; i++) {
+    float v = (float)bf16_value(src[i]);
+    if (fabsf(v) > amax) amax = fabsf(v);
+  }
+  const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+  for (int i = 0; i < n; i++) {
+    const float q = (float)bf16_value(src[i]) / scale;
+    codes[i] = oracle_e4m3_encode(q);
+  }
+  return scale;
+}
+
+/* keys: T rows of index_dim bf16 -> the page-blocked 132-byte layout at the
+ * slot of each row's own position (one scale per row). */
+int oracle_quantize_store_keys(const oracle_rows *R, int index_dim, const uint16_t *keys, uint8_t *cache) {
+  int err = OR_OK;
+  uint8_t *codes = (uint8_t *)malloc((size_t)index_dim);
+  if (!codes) return OR_NOMEM;
+  for (int64_t r = 0; r < R->T; r++) {
+    int64_t row = phys_row(R, r, R->pos[r], &err);
+    if (row < 0) {
+      free(codes);
+      return err;
+    }
+    int64_t page = row / R->page_size, s = row % R->page_size;
+    uint8_t *base = cache + page * (size_t)R->page_size * (index_dim + 4);
+    const float scale = quantize_group(keys + r * index_dim, index_dim, codes);
+    memcpy(base + s * index_dim, codes, (size_t)index_dim);
+    memcpy(base + (size_t)R->page_size * index_dim + s * 4, &scale, 4);
+  }
+  free(codes);
+  return OR_OK;
+}
+
+/* latents: T rows of (L + Rd) bf16 -> 656-byte rows [L codes | L/128 fp32
+ * scales, one per group of 128 | Rd bf16 rope, copied] at each row's slot. */
+int oracle_quantize_store_latents(const oracle_rows *R, int L, int Rd, const uint16_t *lat, uint8_t *cache) {
+  int err = OR_OK;
+  const size_t row_bytes = (size_t)L + 4 * (size_t)(L / 128) + 2 * (size_t)Rd;
+  for (int64_t r = 0; r < R->T; r++) {
+    int64_t row = phys_row(R, r, R->pos[r], &err);
+    if (row < 0) return err;
+    uint8_t *dst = cache + row * row_bytes;
+    const uint16_t *src = lat + r * (L + Rd);
+    for (int g = 0; g < L / 128; g++) {
+      const float scale = quantize_group(src + 128 * g, 128, dst + 128 * g);
+      memcpy(dst + L + 4 * g, &scale, 4);
+    }
+    memcpy(dst + L + 4 * (L / 128), src + L, 2 * (size_t)Rd);
+  }
+  return OR_OK;
+}
+
 /* The index key of token j of row r, as doubles. */
 static int load_index_key(const oracle_rows *R, int64_t r, int64_t j, int index_fmt, int index_dim,
                           const uint8_t *cache, double *k) {

@@ -186,6 +186,55 @@ def test_topk_many_rows_per_cta():
     H.check_selection(g, ref, sc, off, sh.topk, exact=True)
 
 
+def test_quantize_on_store_bit_exact():
+    """bf16 rows quantised into the 132-byte index rows and 656-byte latent rows
+    give the oracle's bytes exactly (scales, codes, ties to even, saturation,
+    zero groups, copied rope), and the pipeline over the quantised caches
+    matches the oracle."""
+    wl = H.deepseek_small(seed=15, fp8=True, sink=True, page_start=8, decode_ctx=(2049, 700), chunk=(1990, 40))
+    sh = wl.shape
+    ic, lc, st = H.host_inputs(wl)
+    T = wl.num_rows
+    rng = np.random.default_rng(16)
+    keys = rng.standard_normal((T, 128)).astype(np.float32) * 3
+    keys[0] = 0.0                                        # an all-zero group
+    keys[1, 5] = 1e4                                     # one large value
+    keys[2, :] = -0.0
+    lat = rng.standard_normal((T, 576)).astype(np.float32)
+    lat[3, 128:256] = 0.0
+    kb, lb = torch.from_numpy(keys).to(torch.bfloat16), torch.from_numpy(lat).to(torch.bfloat16)
+    ref_ic = oracle.quantize_store_keys(sh, wl.spans, wl.num_pages, kb, ic)
+    ref_lc = oracle.quantize_store_latents(sh, wl.spans, wl.num_pages, lb, lc)
+    ctx = dsa.Context(sh, 0)
+    plan = ctx.plan(wl.spans, wl.num_pages)
+    g_ic, g_lc = ic.cuda(), lc.cuda()
+    ctx.quantize_store_keys(plan, kb.cuda(), g_ic)
+    ctx.quantize_store_latents(plan, lb.cuda(), g_lc)
+    ctx.get_error()
+    assert np.array_equal(g_ic.cpu().numpy().reshape(-1), ref_ic.reshape(-1))
+    assert np.array_equal(g_lc.cpu().numpy().reshape(-1), ref_lc.reshape(-1))
+    # selection and attention over the quantised caches
+    sc, off = oracle.index_scores(sh, wl.spans, wl.num_pages, st.q, st.w, ref_ic)
+    sel = oracle.topk(sh, wl.spans, sc, off)
+    g_sel = ctx.index_topk(plan, st.q.cuda(), st.w.cuda(), g_ic).cpu().numpy()
+    H.check_selection(g_sel, sel, sc, off, sh.topk)
+    ref_out = oracle.attend(sh, wl.spans, wl.num_pages, sel, st.q_nope, st.q_pe, ref_lc, st.sink)
+    out = ctx.attend(plan, torch.from_numpy(sel).cuda(), st.q_nope.cuda(), st.q_pe.cuda(), g_lc,
+                     None if st.sink is None else st.sink.cuda(), sh.sm_scale)
+    ctx.get_error()
+    H.check_attention(out.float().cpu().numpy(), ref_out, True)
+
+
+def test_quantize_on_store_rejects_bf16_formats():
+    wl = H.deepseek_small(seed=17, decode_ctx=(300,), chunk=None)
+    ctx = dsa.Context(wl.shape, 0)
+    plan = ctx.plan(wl.spans, wl.num_pages)
+    keys = torch.zeros(wl.num_rows, 128, dtype=torch.bfloat16, device="cuda")
+    cache = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(dsa.DSAError):
+        ctx.quantize_store_keys(plan, keys, cache)
+
+
 def test_bounds_errors_are_reported_not_faulted():
     """Selected positions past the row or below -1 set DSA_ERR_BOUNDS and are skipped."""
     wl = H.deepseek_small(seed=7, decode_ctx=(3000,), chunk=None)

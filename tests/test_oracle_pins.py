@@ -41,6 +41,70 @@ def test_e4m3_spec_points():
     assert v[6] == 7.0 / 8.0 * 2.0 ** -6  # largest subnormal
 
 
+def test_e4m3_encode_inverts_every_code():
+    """Encoding the value of every finite code gives the code back (-0 -> 0x80)."""
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    vals = oracle.e4m3_values(codes).astype(np.float32)
+    assert np.array_equal(oracle.e4m3_encode(vals), codes)
+
+
+def test_e4m3_encode_matches_torch_cast():
+    """Round to nearest even, as torch's float32 -> float8_e4m3fn cast, over the finite range."""
+    rng = np.random.default_rng(3)
+    x = np.concatenate([rng.standard_normal(3000) * 40, rng.standard_normal(2000) * 1e-2,
+                        (rng.random(1000) - 0.5) * 890]).astype(np.float32)
+    x = x[np.abs(x) < 448]
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e4m3_encode(x), ref)
+
+
+def test_e4m3_encode_ties_and_saturation():
+    v = oracle.e4m3_values(np.arange(0x7F, dtype=np.uint8))       # 0 .. 448, increasing
+    mids = ((v[:-1] + v[1:]) / 2).astype(np.float32)               # exact midpoints
+    want = np.array([c if c % 2 == 0 else c + 1 for c in range(0x7E)], dtype=np.uint8)
+    assert np.array_equal(oracle.e4m3_encode(mids), want)          # ties go to the even code
+    assert np.array_equal(oracle.e4m3_encode(-mids), want | 0x80)
+    assert list(oracle.e4m3_encode([448.0, 449.0, 1e6, -500.0])) == [0x7E, 0x7E, 0x7E, 0xFE]
+
+
+def test_quantize_keys_and_latents_bounds():
+    """Each group's largest magnitude maps to +-448 * scale; every value is within
+    half an E4M3 step (times the scale) of its dequantised code; an all-zero
+    group gets scale 1; rope values are copied bit for bit."""
+    sh = tiny_shape(index_dim=128, page_size=4, kv_lora_rank=512, rope_dim=64, index_fmt=W.INDEX_FP8_132,
+                    latent_fmt=W.LATENT_FP8_656)
+    case = make_case(sh, [(0, 3)], num_pages=1)
+    rng = np.random.default_rng(5)
+    keys = rng.standard_normal((3, 128)).astype(np.float32) * np.array([[1.0], [1e-3], [0.0]], np.float32)
+    kb = bf16(keys)
+    kc = oracle.quantize_store_keys(sh, case.spans, 1, kb, np.zeros(4 * 132, np.uint8))
+    codes = kc[:4 * 128].reshape(4, 128)[:3]
+    scales = kc[4 * 128:].view(np.float32)[:3]
+    kf = kb.float().numpy()
+    for r in range(3):
+        amax = np.abs(kf[r]).max()
+        assert scales[r] == (np.float32(amax) / np.float32(448) if amax > 0 else 1.0)
+        deq = oracle.e4m3_values(codes[r]) * scales[r]
+        if amax > 0:
+            i = np.argmax(np.abs(kf[r]))
+            assert codes[r][i] & 0x7F == 0x7E
+        q = kf[r] / scales[r]
+        step = np.where(np.abs(q) < 2.0 ** -6, 2.0 ** -9, 2.0 ** (np.floor(np.log2(np.maximum(np.abs(q), 1e-30))) - 3))
+        assert np.all(np.abs(deq - kf[r]) <= 0.5 * step * scales[r] * (1 + 1e-6) + 1e-30)
+    lat = rng.standard_normal((3, 576)).astype(np.float32)
+    lat[1, :128] = 0.0
+    lb = bf16(lat)
+    lc = oracle.quantize_store_latents(sh, case.spans, 1, lb, np.zeros(4 * 656, np.uint8)).reshape(4, 656)
+    lf = lb.float().numpy()
+    for r in range(3):
+        sc = lc[r, 512:528].view(np.float32)
+        for g in range(4):
+            amax = np.abs(lf[r, 128 * g:128 * (g + 1)]).max()
+            assert sc[g] == (np.float32(amax) / np.float32(448) if amax > 0 else 1.0)
+        assert np.array_equal(lc[r, 528:656].view(np.uint16), lb.view(torch.int16).numpy()[r, 512:].view(np.uint16))
+    assert lc[1, :128].max() == 0 and lc[1, 512:516].view(np.float32)[0] == 1.0
+
+
 # ----------------------------------------------------------------------------
 # slot mapping (DSASpan: page_start is the first token's offset in the pages)
 # ----------------------------------------------------------------------------
