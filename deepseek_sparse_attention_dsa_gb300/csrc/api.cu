@@ -536,6 +536,7 @@ dsa_status dsa_topk_from_scores(dsa_ctx_t *ctx, const dsa_plan_t *plan, const fl
   if (!scores || !selection) return DSA_ERR_INVALID_ARG;
   cudaError_t e = launch_topk(ctx, plan, scores, selection, reinterpret_cast<cudaStream_t>(stream),
                               &ctx->last_launches);
+  if (e == cudaSuccess) plan->last_selection = selection;
   return cuda_status(ctx, e);
 }
 
@@ -551,6 +552,7 @@ dsa_status dsa_index_topk(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *q,
   int32_t n = 0;
   cudaError_t e = launch_index_scores(ctx, plan, q, w, index_cache, ctx->scores, s, &n);
   if (e == cudaSuccess) e = launch_topk(ctx, plan, ctx->scores, selection, s, &n);
+  if (e == cudaSuccess) plan->last_selection = selection;
   ctx->last_launches = n;
   return cuda_status(ctx, e);
 }
@@ -567,6 +569,14 @@ dsa_status dsa_attend(dsa_ctx_t *ctx, const dsa_plan_t *plan, const int32_t *sel
   cudaError_t e = launch_attend(ctx, plan, selection, q_nope, q_pe, latent_cache, sink, sm_scale, out,
                                 reinterpret_cast<cudaStream_t>(stream), &ctx->last_launches);
   return cuda_status(ctx, e);
+}
+
+dsa_status dsa_attend_shared(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *q_nope, const void *q_pe,
+                             const void *latent_cache, const float *sink, float sm_scale, void *out,
+                             dsa_stream_t stream) {
+  if (plan && plan->T > 0 && !plan->last_selection) return DSA_ERR_INVALID_ARG;   // no FULL layer yet
+  return dsa_attend(ctx, plan, plan ? plan->last_selection : nullptr, q_nope, q_pe, latent_cache, sink, sm_scale,
+                    out, stream);
 }
 
 dsa_status dsa_get_error(dsa_ctx_t *ctx, dsa_stream_t stream) {

@@ -99,6 +99,9 @@ struct dsa_plan {
   dsa::AttCombine *combine = nullptr;
   int32_t n_combine = 0, n_slots = 0;
   int32_t n_index_items = 0;
+  // the selection the last FULL layer's dsa_index_topk / dsa_topk_from_scores
+  // wrote for this plan (mstar DSAPlan.last_selection), for SHARED layers
+  mutable const int32_t *last_selection = nullptr;
 };
 
 namespace dsa {

@@ -33,7 +33,7 @@ STATUS_NAMES = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_SHORT_HISTORY
 EXPORTED = ["dsa_create", "dsa_destroy", "dsa_plan", "dsa_plan_destroy", "dsa_plan_get_info", "dsa_store_keys",
             "dsa_index_topk", "dsa_index_scores", "dsa_topk_from_scores", "dsa_attend", "dsa_get_error",
             "dsa_last_launch_count", "dsa_status_str", "dsa_index_topk_static", "dsa_last_cuda_error",
-            "dsa_quantize_store_keys", "dsa_quantize_store_latents"]
+            "dsa_quantize_store_keys", "dsa_quantize_store_latents", "dsa_attend_shared"]
 
 
 class DSAError(RuntimeError):
@@ -93,6 +93,7 @@ def load() -> ctypes.CDLL:
     L.dsa_index_topk_static.argtypes = [vp, vp, vp, vp, vp, vp, vp]
     L.dsa_topk_from_scores.argtypes = [vp, vp, vp, vp, vp]
     L.dsa_attend.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp]
+    L.dsa_attend_shared.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp]
     L.dsa_get_error.argtypes = [vp, vp]
     L.dsa_last_launch_count.argtypes = [vp]
     L.dsa_last_launch_count.restype = i32
@@ -102,7 +103,7 @@ def load() -> ctypes.CDLL:
     L.dsa_status_str.restype = ctypes.c_char_p
     for name in ("dsa_create", "dsa_plan", "dsa_plan_get_info", "dsa_store_keys", "dsa_index_topk", "dsa_index_topk_static",
                  "dsa_index_scores", "dsa_topk_from_scores", "dsa_attend", "dsa_get_error", "dsa_quantize_store_keys",
-                 "dsa_quantize_store_latents"):
+                 "dsa_quantize_store_latents", "dsa_attend_shared"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -300,6 +301,23 @@ class Context:
                                  _ptr(latent_cache, d, (torch.bfloat16, torch.uint8), "latent_cache"),
                                  _ptr(sink, d, (torch.float32,), "sink"), float(sm_scale),
                                  _ptr(out, d, (torch.bfloat16,), "out"), _stream(stream)), "dsa_attend", self.handle)
+        return out
+
+    def attend_shared(self, plan: Plan, q_nope, q_pe, latent_cache, sink=None, sm_scale=None, out=None,
+                      stream=None) -> torch.Tensor:
+        """A SHARED layer: attend over the selection the last FULL layer wrote for this plan."""
+        d = self.device
+        sh = self.shape
+        if sm_scale is None:
+            sm_scale = sh.sm_scale
+        if out is None:
+            out = torch.empty(plan.num_rows, sh.heads, sh.kv_lora_rank, dtype=torch.bfloat16, device=d)
+        _check(load().dsa_attend_shared(self.handle, plan.handle, _ptr(q_nope, d, (torch.bfloat16,), "q_nope"),
+                                        _ptr(q_pe, d, (torch.bfloat16,), "q_pe"),
+                                        _ptr(latent_cache, d, (torch.bfloat16, torch.uint8), "latent_cache"),
+                                        _ptr(sink, d, (torch.float32,), "sink"), float(sm_scale),
+                                        _ptr(out, d, (torch.bfloat16,), "out"), _stream(stream)),
+               "dsa_attend_shared", self.handle)
         return out
 
     def get_error(self, stream=None):

@@ -192,6 +192,19 @@ dsa_status dsa_attend(dsa_ctx_t *ctx, const dsa_plan_t *plan, const int32_t *sel
                       const void *q_pe, const void *latent_cache, const float *sink, float sm_scale, void *out,
                       dsa_stream_t stream);
 
+/* A SHARED layer (mstar DSAManager.shared_selection, DSAPlan.last_selection:
+ * "SHARED layers reuse the last FULL layer's pick this forward", IndexShare):
+ * dsa_attend over the selection buffer that the last dsa_index_topk or
+ * dsa_topk_from_scores call with this plan wrote.  The plan keeps only the
+ * pointer: the caller keeps that buffer alive and unchanged for the SHARED
+ * layers of the step.  dsa_index_topk_static does not record its output here
+ * (pass its selection to dsa_attend).  Same arguments and errors as
+ * dsa_attend, plus DSA_ERR_INVALID_ARG when no selection has been recorded for
+ * this plan. */
+dsa_status dsa_attend_shared(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *q_nope, const void *q_pe,
+                             const void *latent_cache, const float *sink, float sm_scale, void *out,
+                             dsa_stream_t stream);
+
 /* dsa_index_topk for callers that cannot allocate device memory at step time
  * (a process that reserves HBM up front in its own pool and permits no driver
  * allocation while serving).  The pages have no counterpart to this call.

@@ -235,6 +235,40 @@ def test_quantize_on_store_rejects_bf16_formats():
         ctx.quantize_store_keys(plan, keys, cache)
 
 
+def test_full_and_shared_layers():
+    """A forward of four layers over one plan: FULL, SHARED, FULL, SHARED.  Each
+    SHARED layer attends with its own queries and latents over the selection
+    the last FULL layer wrote (IndexShare); a FULL layer's selection replaces it."""
+    base = H.deepseek_small(seed=18, sink=True, decode_ctx=(2300, 900), chunk=(2040, 24))
+    layers = [W.Workload(base.name, base.shape, base.spans, base.num_pages, 18 + 97 * i, base.dist) for i in range(4)]
+    full = [True, False, True, False]
+    ctx = dsa.Context(base.shape, 0)
+    plan = ctx.plan(base.spans, base.num_pages)
+    with pytest.raises(dsa.DSAError):              # no FULL layer yet
+        ctx.attend_shared(plan, torch.zeros(1, device="cuda", dtype=torch.bfloat16),
+                          torch.zeros(1, device="cuda", dtype=torch.bfloat16),
+                          torch.zeros(1, device="cuda", dtype=torch.bfloat16))
+    last_sel = None
+    for wl, is_full in zip(layers, full):
+        ic, lc, st = H.host_inputs(wl)
+        dev = W.StepInputs(*(H.to_dev(x) for x in (st.q, st.w, st.keys, st.q_nope, st.q_pe, st.sink)))
+        lcd = lc.cuda()
+        if is_full:
+            icd = ic.cuda()
+            ctx.store_keys(plan, dev.keys, icd)
+            sel = ctx.index_topk(plan, dev.q, dev.w, icd)
+            cache = oracle.store_keys(wl.shape, wl.spans, wl.num_pages, st.keys, ic)
+            sc, off = oracle.index_scores(wl.shape, wl.spans, wl.num_pages, st.q, st.w, cache)
+            H.check_selection(sel.cpu().numpy(), oracle.topk(wl.shape, wl.spans, sc, off), sc, off, wl.shape.topk)
+            out = ctx.attend(plan, sel, dev.q_nope, dev.q_pe, lcd, dev.sink)
+            last_sel = sel
+        else:
+            out = ctx.attend_shared(plan, dev.q_nope, dev.q_pe, lcd, dev.sink)
+        ctx.get_error()
+        ref = oracle.attend(wl.shape, wl.spans, wl.num_pages, last_sel.cpu().numpy(), st.q_nope, st.q_pe, lc, st.sink)
+        H.check_attention(out.float().cpu().numpy(), ref, False)
+
+
 def test_bounds_errors_are_reported_not_faulted():
     """Selected positions past the row or below -1 set DSA_ERR_BOUNDS and are skipped."""
     wl = H.deepseek_small(seed=7, decode_ctx=(3000,), chunk=None)
