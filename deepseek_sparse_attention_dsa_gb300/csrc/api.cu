@@ -159,6 +159,7 @@ const char *dsa_status_str(dsa_status s) {
     case DSA_ERR_TIMEOUT: return "device pipeline wait timed out";
     case DSA_ERR_UNSUPPORTED: return "unsupported shape or format";
     case DSA_ERR_SCRATCH_LIMIT: return "plan needs more scores than the static score array holds (DSA_STATIC_SCORES_MAX)";
+    case DSA_ERR_BAD_SPANS: return "a capturable plan's update found invalid spans or exceeded its capacities; the plan was emptied";
     default: return "unknown status";
   }
 }
@@ -282,7 +283,7 @@ dsa_status dsa_plan(dsa_ctx_t *ctx, const dsa_span_t *spans, int32_t num_spans, 
     const int G = set ? Gm : 1;
     const int cap = std::max(1, ctx->num_sms * indexer_ctas_per_sm(c, G));
     // items of at most `tpi` tiles; CTAs take contiguous, tile-balanced item ranges
-    const int64_t tpi = std::max<int64_t>(2, std::min<int64_t>(32, tiles / (int64_t(cap) * 8)));
+    const int64_t tpi = index_tiles_per_item(tiles, cap);
     std::vector<int64_t> prefix{0};
     for (int32_t gi = 0; gi < static_cast<int32_t>(groups[set].size()); ++gi) {
       const IdxGroup &g = groups[set][gi];
@@ -315,25 +316,7 @@ dsa_status dsa_plan(dsa_ctx_t *ctx, const dsa_span_t *spans, int32_t num_spans, 
   std::vector<AttCombine> combines;
   {
     const int64_t K = c.topk;
-    // A row is one two-CTA cluster; `pairs` clusters run at a time.  Rows are
-    // split over key ranges only when that shortens the estimated time:
-    // waves x (a unit's fixed start-up, about ten tile periods, + its tiles),
-    // plus the merge of the partials (about 0.15 tile periods per row).
-    const int pairs = std::max(1, ctx->num_sms / 2);
-    const int64_t full_tiles = (K + kAttTile - 1) / kAttTile;
-    int splits = 1;
-    if (T > 0) {
-      double best = 0.0;
-      for (int sp = 1; sp <= 16 && sp <= std::max<int64_t>(1, full_tiles / 2); ++sp) {
-        const int64_t waves = (static_cast<int64_t>(T) * sp + pairs - 1) / pairs;
-        const double est = static_cast<double>(waves) * (10.0 + static_cast<double>((full_tiles + sp - 1) / sp)) +
-                           (sp > 1 ? 0.15 * static_cast<double>(T) : 0.0);
-        if (sp == 1 || est < best) {
-          best = est;
-          splits = sp;
-        }
-      }
-    }
+    const int splits = attention_splits(T, K, ctx->num_sms);
     int32_t slot = 0;
     int32_t row = 0;
     for (int32_t i = 0; i < num_spans; ++i) {
@@ -342,7 +325,7 @@ dsa_status dsa_plan(dsa_ctx_t *ctx, const dsa_span_t *spans, int32_t num_spans, 
         const int64_t pos = s.ctx_start + r;
         const int64_t nsel = std::min<int64_t>(K, pos + 1);
         const int64_t tiles = (nsel + kAttTile - 1) / kAttTile;
-        const int64_t sp = std::max<int64_t>(1, std::min<int64_t>(splits, tiles / 2));
+        const int64_t sp = attention_row_units(pos, K, splits);
         if (sp == 1) {
           units.push_back(AttUnit{row, 0, static_cast<int32_t>(nsel), -1});
         } else {
@@ -451,11 +434,138 @@ dsa_status dsa_plan(dsa_ctx_t *ctx, const dsa_span_t *spans, int32_t num_spans, 
 
 void dsa_plan_destroy(dsa_plan_t *plan) {
   if (!plan) return;
-  if (plan->dev && !is_host_only(plan->ctx)) {
+  if (plan->capturable) {
+    cudaSetDevice(plan->ctx->device);
+    cudaFree(plan->dev);
+    cudaFree(plan->own_scores);
+    cudaFree(plan->own_opart);
+    cudaFree(plan->own_mlpart);
+  } else if (plan->dev && !is_host_only(plan->ctx)) {
     cudaSetDevice(plan->ctx->device);
     cudaFreeAsync(plan->dev, plan->stream);
   }
   delete plan;
+}
+
+dsa_status dsa_plan_capturable(dsa_ctx_t *ctx, int32_t max_rows, int32_t max_spans, int64_t max_scores,
+                               int32_t page_start_align, int32_t cache_pages, dsa_stream_t stream,
+                               dsa_plan_t **out) {
+  if (!out) return DSA_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!ctx || is_host_only(ctx) || max_rows <= 0 || max_spans <= 0 || max_rows > INT32_MAX / 2 ||
+      max_spans > INT32_MAX / 2 || max_scores < max_rows || max_scores > (int64_t(1) << 40) || page_start_align <= 0 ||
+      cache_pages < 0)
+    return DSA_ERR_INVALID_ARG;
+  const dsa_config_t &c = ctx->cfg;
+  // worst-case work for any update within the capacities
+  const int64_t items_cap = max_scores / kIndexTile + 2 * static_cast<int64_t>(max_rows) + 1;
+  int64_t units_cap = 1;
+  for (int64_t t = 1; t <= max_rows; ++t)
+    units_cap = std::max<int64_t>(units_cap, t * attention_splits(t, c.topk, ctx->num_sms));
+  if (items_cap > INT32_MAX / 2 || units_cap > INT32_MAX / 2) return DSA_ERR_INVALID_ARG;
+  const int idx_cap = std::max(1, ctx->num_sms * indexer_ctas_per_sm(c, 1));
+
+  dsa_plan_t *plan = new (std::nothrow) dsa_plan_t();
+  if (!plan) return DSA_ERR_OOM;
+  plan->ctx = ctx;
+  plan->stream = reinterpret_cast<cudaStream_t>(stream);
+  plan->capturable = true;
+  plan->T = max_rows;
+  plan->n_spans = max_spans;
+  plan->max_spans = max_spans;
+  plan->needs_selection = 1;
+  plan->cache_pages = cache_pages;
+  plan->num_scores = max_scores;
+  plan->max_pos = INT32_MAX;
+  plan->page_start_align = page_start_align;
+  {
+    // largest power of two <= 128 dividing the page size and the alignment
+    int64_t a = c.page_size, b = page_start_align;
+    while (b) { int64_t t = a % b; a = b; b = t; }
+    int bh = 1;
+    while (bh < 128 && a % (bh * 2) == 0) bh *= 2;
+    plan->box_rows = bh;
+  }
+  plan->items_cap = static_cast<int32_t>(items_cap);
+  plan->combine_cap = max_rows;
+  plan->n_units = static_cast<int32_t>(units_cap);
+  plan->n_combine = max_rows;
+  plan->n_slots = static_cast<int32_t>(units_cap);
+  plan->n_index_items = plan->items_cap;
+  plan->splits_max = 16;
+  IdxSet &set = plan->idx[0];
+  set.G = 1;
+  set.n_groups = max_rows;
+  set.n_items = plan->items_cap;
+  set.n_ctas = idx_cap;
+
+  Layout lay;
+  const size_t o_pos = lay.take<int32_t>(max_rows), o_poff = lay.take<int32_t>(max_rows),
+               o_np = lay.take<int32_t>(max_rows), o_ps = lay.take<int32_t>(max_rows),
+               o_soff = lay.take<int64_t>(max_rows), o_g = lay.take<IdxGroup>(max_rows),
+               o_i = lay.take<IdxItem>(items_cap), o_t0 = lay.take<int64_t>(items_cap + 1),
+               o_c = lay.take<int32_t>(idx_cap + 1), o_u = lay.take<AttUnit>(units_cap),
+               o_cb = lay.take<AttCombine>(max_rows), o_q0 = lay.take<int32_t>(max_spans + 1),
+               o_n = lay.take<int32_t>(8);
+  auto fail = [&](dsa_status st) {
+    dsa_plan_destroy(plan);
+    return st;
+  };
+  if (cudaSetDevice(ctx->device) != cudaSuccess) return fail(DSA_ERR_CUDA);
+  const size_t hl = static_cast<size_t>(c.heads) * c.kv_lora_rank;
+  if (cudaMalloc(reinterpret_cast<void **>(&plan->dev), lay.bytes) != cudaSuccess ||
+      cudaMalloc(reinterpret_cast<void **>(&plan->own_scores), static_cast<size_t>(max_scores) * sizeof(float)) !=
+          cudaSuccess ||
+      cudaMalloc(reinterpret_cast<void **>(&plan->own_opart), static_cast<size_t>(units_cap) * hl * sizeof(float)) !=
+          cudaSuccess ||
+      cudaMalloc(reinterpret_cast<void **>(&plan->own_mlpart),
+                 static_cast<size_t>(units_cap) * c.heads * 2 * sizeof(float)) != cudaSuccess)
+    return fail(DSA_ERR_OOM);
+  char *d = plan->dev;
+  plan->row_pos = reinterpret_cast<int32_t *>(d + o_pos);
+  plan->row_page_off = reinterpret_cast<int32_t *>(d + o_poff);
+  plan->row_npages = reinterpret_cast<int32_t *>(d + o_np);
+  plan->row_page_start = reinterpret_cast<int32_t *>(d + o_ps);
+  plan->row_score_off = reinterpret_cast<int64_t *>(d + o_soff);
+  set.groups = reinterpret_cast<IdxGroup *>(d + o_g);
+  set.items = reinterpret_cast<IdxItem *>(d + o_i);
+  plan->item_tile0 = reinterpret_cast<int64_t *>(d + o_t0);
+  set.cta_begin = reinterpret_cast<int32_t *>(d + o_c);
+  plan->units = reinterpret_cast<AttUnit *>(d + o_u);
+  plan->combine = reinterpret_cast<AttCombine *>(d + o_cb);
+  plan->span_q0 = reinterpret_cast<int32_t *>(d + o_q0);
+  plan->counts = reinterpret_cast<int32_t *>(d + o_n);
+  // an empty plan until the first update: every row is padding, no work
+  std::vector<char> h(lay.bytes, 0);
+  std::fill_n(reinterpret_cast<int32_t *>(h.data() + o_pos), max_rows, -1);
+  for (int64_t i = 0; i < items_cap; ++i) reinterpret_cast<IdxItem *>(h.data() + o_i)[i] = IdxItem{-1, 0, 0, 0};
+  for (int64_t i = 0; i < units_cap; ++i) reinterpret_cast<AttUnit *>(h.data() + o_u)[i] = AttUnit{-1, 0, 0, -1};
+  for (int32_t i = 0; i < max_rows; ++i) reinterpret_cast<AttCombine *>(h.data() + o_cb)[i] = AttCombine{-1, 0, 0, 0};
+  if (cudaMemcpy(plan->dev, h.data(), lay.bytes, cudaMemcpyHostToDevice) != cudaSuccess) return fail(DSA_ERR_CUDA);
+  *out = plan;
+  return DSA_OK;
+}
+
+dsa_status dsa_plan_update(dsa_ctx_t *ctx, dsa_plan_t *plan, const int32_t *num_spans,
+                           const dsa_device_span_t *spans, const int32_t *pages, int64_t num_page_ids,
+                           dsa_stream_t stream) {
+  if (!ctx || !plan || plan->ctx != ctx || !plan->capturable || is_host_only(ctx)) return DSA_ERR_INVALID_ARG;
+  if (!num_spans || !spans || !pages || num_page_ids < 0) return DSA_ERR_INVALID_ARG;
+  if (cudaSetDevice(ctx->device) != cudaSuccess) return DSA_ERR_CUDA;
+  plan->pages = const_cast<int32_t *>(pages);
+  plan->page_ids = num_page_ids;
+  ctx->last_launches = 1;
+  return cuda_status(ctx, launch_plan_update(ctx, plan, num_spans, spans, num_page_ids,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dsa_status dsa_plan_read_counts(const dsa_plan_t *plan, int32_t counts[8]) {
+  if (!plan || !counts || !plan->capturable) return DSA_ERR_INVALID_ARG;
+  if (cudaSetDevice(plan->ctx->device) != cudaSuccess) return DSA_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return DSA_ERR_CUDA;
+  if (cudaMemcpy(counts, plan->counts, 8 * sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  return DSA_OK;
 }
 
 dsa_status dsa_plan_get_info(const dsa_plan_t *plan, dsa_plan_info_t *info) {
@@ -547,11 +657,13 @@ dsa_status dsa_index_topk(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *q,
   ctx->last_launches = 0;
   if (plan->T == 0) return DSA_OK;
   if (!q || !w || !index_cache || !selection) return DSA_ERR_INVALID_ARG;
-  if (static_cast<size_t>(plan->num_scores) > ctx->scores_cap) return DSA_ERR_INVALID_ARG;  // plan of another size
+  if (!plan->own_scores && static_cast<size_t>(plan->num_scores) > ctx->scores_cap)
+    return DSA_ERR_INVALID_ARG;  // plan of another size
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int32_t n = 0;
-  cudaError_t e = launch_index_scores(ctx, plan, q, w, index_cache, ctx->scores, s, &n);
-  if (e == cudaSuccess) e = launch_topk(ctx, plan, ctx->scores, selection, s, &n);
+  float *scores = plan_scores(ctx, plan);
+  cudaError_t e = launch_index_scores(ctx, plan, q, w, index_cache, scores, s, &n);
+  if (e == cudaSuccess) e = launch_topk(ctx, plan, scores, selection, s, &n);
   if (e == cudaSuccess) plan->last_selection = selection;
   ctx->last_launches = n;
   return cuda_status(ctx, e);
@@ -565,7 +677,7 @@ dsa_status dsa_attend(dsa_ctx_t *ctx, const dsa_plan_t *plan, const int32_t *sel
   ctx->last_launches = 0;
   if (plan->T == 0) return DSA_OK;
   if (!selection || !q_nope || !latent_cache || !out || (!q_pe && ctx->cfg.rope_dim > 0)) return DSA_ERR_INVALID_ARG;
-  if (static_cast<size_t>(plan->n_slots) > ctx->part_cap) return DSA_ERR_INVALID_ARG;
+  if (!plan->own_opart && static_cast<size_t>(plan->n_slots) > ctx->part_cap) return DSA_ERR_INVALID_ARG;
   cudaError_t e = launch_attend(ctx, plan, selection, q_nope, q_pe, latent_cache, sink, sm_scale, out,
                                 reinterpret_cast<cudaStream_t>(stream), &ctx->last_launches);
   return cuda_status(ctx, e);
@@ -588,6 +700,7 @@ dsa_status dsa_get_error(dsa_ctx_t *ctx, dsa_stream_t stream) {
   if (cudaMemcpy(&word, ctx->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return DSA_ERR_CUDA;
   if (word && cudaMemset(ctx->err, 0, sizeof(int)) != cudaSuccess) return DSA_ERR_CUDA;
   if (word & kErrTimeout) return DSA_ERR_TIMEOUT;
+  if (word & kErrSpans) return DSA_ERR_BAD_SPANS;
   if (word & kErrBounds) return DSA_ERR_BOUNDS;
   return DSA_OK;
 }

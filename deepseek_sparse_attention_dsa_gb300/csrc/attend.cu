@@ -202,6 +202,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
   const uint32_t peer = crank ^ 1u;
   const AttUnit unit = p.units[blockIdx.x >> 1];
   const int row = unit.row;
+  if (row < 0) return;   // padding of a capturable plan: both CTAs of the pair leave before any cluster step
   const int pos = p.row_pos[row];
   const int nent = unit.k1 - unit.k0;
   const int ntiles = (nent + T - 1) / T;
@@ -699,6 +700,7 @@ __global__ void __launch_bounds__(128) attend_combine_kernel(const AttCombine *_
                                                              const float *__restrict__ sink, __nv_bfloat16 *out,
                                                              int H, int L) {
   const AttCombine cb = combine[blockIdx.x / H];
+  if (cb.row < 0) return;   // padding of a capturable plan
   const int h = blockIdx.x % H;
   float m = sink ? sink[h] * kLog2e : -INFINITY;
   for (int s = 0; s < cb.nsplit; ++s) m = fmaxf(m, mlpart[((cb.first_slot + s) * static_cast<int64_t>(H) + h) * 2]);
@@ -744,6 +746,7 @@ __global__ void __launch_bounds__(128) attend_simt_kernel(
   float *red = lg + K;
   const int row = blockIdx.x / H, h = blockIdx.x % H;
   const int pos = row_pos[row];
+  if (pos < 0) return;   // padding row of a capturable plan
   for (int i = threadIdx.x; i < L + R; i += blockDim.x)
     qs[i] = i < L ? __bfloat162float(q_nope[(static_cast<int64_t>(row) * H + h) * L + i])
                   : __bfloat162float(q_pe[(static_cast<int64_t>(row) * H + h) * R + (i - L)]);
@@ -818,8 +821,8 @@ cudaError_t run_tc(const dsa_ctx *ctx, const dsa_plan_t *plan, const int32_t *se
   prm.row_page_start = plan->row_page_start;
   prm.pages = plan->pages;
   prm.out = static_cast<__nv_bfloat16 *>(out);
-  prm.opart = ctx->opart;
-  prm.mlpart = ctx->mlpart;
+  prm.opart = plan_opart(ctx, plan);
+  prm.mlpart = plan_mlpart(ctx, plan);
   prm.err = ctx->err;
   prm.H = c.heads;
   prm.K = c.topk;
@@ -862,7 +865,8 @@ cudaError_t launch_attend(const dsa_ctx *ctx, const dsa_plan_t *plan, const int3
     if (e != cudaSuccess) return e;
     *launches += 1;
     if (plan->n_combine > 0) {
-      attend_combine_kernel<<<plan->n_combine * c.heads, 128, 0, s>>>(plan->combine, ctx->opart, ctx->mlpart, sink,
+      attend_combine_kernel<<<plan->n_combine * c.heads, 128, 0, s>>>(plan->combine, plan_opart(ctx, plan),
+                                                                      plan_mlpart(ctx, plan), sink,
                                                                       static_cast<__nv_bfloat16 *>(out), c.heads,
                                                                       c.kv_lora_rank);
       e = cudaGetLastError();

@@ -54,6 +54,45 @@ struct AttCombine {
 constexpr int kIndexTile = 128;   // keys per indexer tile (UMMA M)
 constexpr int kAttTile = 64;      // keys per attention tile (UMMA N of QK)
 
+// Tiles per indexer work item for `tiles` tiles over `cap` persistent CTAs.
+__host__ __device__ inline int64_t index_tiles_per_item(int64_t tiles, int cap) {
+  const int64_t t = tiles / (static_cast<int64_t>(cap) * 8);
+  return t < 2 ? 2 : (t > 32 ? 32 : t);
+}
+
+// Key ranges per attention row for a step of T rows.  A row is one two-CTA
+// cluster and num_sms / 2 clusters run at a time; a row is split only when
+// that shortens waves x (a unit's fixed start-up, about ten tile periods, +
+// its tiles) plus the merge of the partials (about 0.15 tile periods per
+// row).  The host planner and the device planner share this function, so
+// both make the same units.
+__host__ __device__ inline int attention_splits(int64_t T, int64_t topk, int num_sms) {
+  const int64_t pairs = num_sms / 2 > 1 ? num_sms / 2 : 1;
+  const int64_t full_tiles = (topk + kAttTile - 1) / kAttTile;
+  const int64_t sp_max = full_tiles / 2 > 1 ? full_tiles / 2 : 1;
+  int splits = 1;
+  if (T <= 0) return 1;
+  double best = 0.0;
+  for (int sp = 1; sp <= 16 && sp <= sp_max; ++sp) {
+    const int64_t waves = (T * sp + pairs - 1) / pairs;
+    const double est = static_cast<double>(waves) * (10.0 + static_cast<double>((full_tiles + sp - 1) / sp)) +
+                       (sp > 1 ? 0.15 * static_cast<double>(T) : 0.0);
+    if (sp == 1 || est < best) {
+      best = est;
+      splits = sp;
+    }
+  }
+  return splits;
+}
+
+// Attention units of one row at position pos when rows split `splits` ways.
+__host__ __device__ inline int attention_row_units(int64_t pos, int64_t topk, int splits) {
+  const int64_t nsel = pos + 1 < topk ? pos + 1 : topk;
+  const int64_t tiles = (nsel + kAttTile - 1) / kAttTile;
+  const int64_t sp = splits < tiles / 2 ? splits : tiles / 2;
+  return sp > 1 ? static_cast<int>(sp) : 1;
+}
+
 // Indexer launch set: groups with the same row-group size.
 struct IdxSet {
   int G = 1;                      // rows per group
@@ -102,7 +141,23 @@ struct dsa_plan {
   // the selection the last FULL layer's dsa_index_topk / dsa_topk_from_scores
   // wrote for this plan (mstar DSAPlan.last_selection), for SHARED layers
   mutable const int32_t *last_selection = nullptr;
+  // capturable plans (dsa_plan_capturable): the host fields above hold the
+  // capacities, the device metadata is rewritten by dsa_plan_update, and the
+  // plan owns its scratch
+  bool capturable = false;
+  int32_t max_spans = 0, items_cap = 0, combine_cap = 0, page_start_align = 1;
+  int64_t page_ids = 0;                 // length of the page array of the last update
+  float *own_scores = nullptr, *own_opart = nullptr, *own_mlpart = nullptr;
+  int32_t *span_q0 = nullptr;           // device scratch [max_spans + 1]
+  int64_t *item_tile0 = nullptr;        // device scratch [items_cap + 1]
+  int32_t *counts = nullptr;            // device [8], see dsa_plan_read_counts
 };
+
+namespace dsa {
+inline float *plan_scores(const dsa_ctx *c, const dsa_plan_t *p) { return p->own_scores ? p->own_scores : c->scores; }
+inline float *plan_opart(const dsa_ctx *c, const dsa_plan_t *p) { return p->own_opart ? p->own_opart : c->opart; }
+inline float *plan_mlpart(const dsa_ctx *c, const dsa_plan_t *p) { return p->own_mlpart ? p->own_mlpart : c->mlpart; }
+}  // namespace dsa
 
 namespace dsa {
 
@@ -118,6 +173,8 @@ cudaError_t launch_index_scores(const dsa_ctx *ctx, const dsa_plan_t *plan, cons
                                 const void *cache, float *scores, cudaStream_t s, int32_t *launches);
 cudaError_t launch_topk(const dsa_ctx *ctx, const dsa_plan_t *plan, const float *scores, int32_t *sel,
                         cudaStream_t s, int32_t *launches);
+cudaError_t launch_plan_update(const dsa_ctx *ctx, dsa_plan_t *plan, const int32_t *num_spans,
+                               const dsa_device_span_t *spans, int64_t num_page_ids, cudaStream_t s);
 cudaError_t launch_attend(const dsa_ctx *ctx, const dsa_plan_t *plan, const int32_t *sel, const void *q_nope,
                           const void *q_pe, const void *latent, const float *sink, float sm_scale, void *out,
                           cudaStream_t s, int32_t *launches);

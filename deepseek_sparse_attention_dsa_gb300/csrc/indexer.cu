@@ -354,6 +354,7 @@ __global__ void __launch_bounds__(128) index_simt_kernel(const uint16_t *__restr
                                                           int P, int fp8, int num_pages) {
   extern __shared__ float qs[];  // [Hi * Di] of one row, then [Hi] weights
   const IdxItem item = items[blockIdx.x];
+  if (item.group < 0) return;   // padding of a capturable plan
   const IdxGroup g = groups[item.group];
   for (int gg = 0; gg < g.nrows; ++gg) {
     const int row = g.row0 + gg;

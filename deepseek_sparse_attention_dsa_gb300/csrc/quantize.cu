@@ -69,7 +69,7 @@ __global__ void __launch_bounds__(256) quantize_keys_kernel(const uint2 *__restr
                                                             const int32_t *__restrict__ pages, int T, int P,
                                                             int num_pages, int *err) {
   const int r = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-  if (r >= T) return;
+  if (r >= T || row_pos[r] < 0) return;   // past the rows, or a padding row of a capturable plan
   const int lane = lane_id();
   const int64_t prow = own_row(r, row_pos, row_page_off, row_npages, row_page_start, pages, P, num_pages, err);
   if (prow < 0) return;
@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(256) quantize_latents_kernel(const uint8_t *__
                                                                int num_pages, int *err) {
   constexpr int L = 512, R = 64, SRC = (L + R) * 2, ROW = L + 4 * (L / 128) + 2 * R;
   const int r = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-  if (r >= T) return;
+  if (r >= T || row_pos[r] < 0) return;   // past the rows, or a padding row of a capturable plan
   const int lane = lane_id();
   const int64_t prow = own_row(r, row_pos, row_page_off, row_npages, row_page_start, pages, P, num_pages, err);
   if (prow < 0) return;

@@ -22,7 +22,7 @@ __global__ void __launch_bounds__(256) store_keys_bf16_kernel(const uint4 *__res
                                                               const int32_t *__restrict__ pages, int T, int P,
                                                               int vec_per_row, int num_pages, int *err) {
   const int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-  if (row >= T) return;
+  if (row >= T || row_pos[row] < 0) return;   // past the rows, or a padding row of a capturable plan
   const int64_t slot = static_cast<int64_t>(row_page_start[row]) + row_pos[row];
   const int64_t pi = slot / P;
   if (pi >= row_npages[row]) {
@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(256) store_keys_fp8_kernel(const uint8_t *__re
                                                              const int32_t *__restrict__ pages, int T, int P, int D,
                                                              int num_pages, int *err) {
   const int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-  if (row >= T) return;
+  if (row >= T || row_pos[row] < 0) return;   // past the rows, or a padding row of a capturable plan
   const int64_t slot = static_cast<int64_t>(row_page_start[row]) + row_pos[row];
   const int64_t pi = slot / P;
   if (pi >= row_npages[row]) {

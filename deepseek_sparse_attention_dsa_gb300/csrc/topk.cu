@@ -379,6 +379,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) topk_kernel(const float *__rest
   TopkSmem<NT> &sm = *reinterpret_cast<TopkSmem<NT> *>(topk_smem_raw);
   // CTA b takes rows b, b + gridDim.x, ...
   for (int row = blockIdx.x; row < T; row += gridDim.x) {
+    if (row_pos[row] < 0) continue;   // padding row of a capturable plan (uniform over the CTA)
     __syncthreads();   // shared memory of the previous row is no longer read
     select_row<NT>(scores, row_score_off, row_pos, K, sel, row, sm);
   }

@@ -28,12 +28,16 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "l
 DSA_OK = 0
 STATUS_NAMES = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_SHORT_HISTORY", 3: "DSA_ERR_OOM",
                 4: "DSA_ERR_CUDA", 5: "DSA_ERR_BOUNDS", 6: "DSA_ERR_TIMEOUT", 7: "DSA_ERR_UNSUPPORTED",
-                8: "DSA_ERR_SCRATCH_LIMIT"}
+                8: "DSA_ERR_SCRATCH_LIMIT", 9: "DSA_ERR_BAD_SPANS"}
 
 EXPORTED = ["dsa_create", "dsa_destroy", "dsa_plan", "dsa_plan_destroy", "dsa_plan_get_info", "dsa_store_keys",
             "dsa_index_topk", "dsa_index_scores", "dsa_topk_from_scores", "dsa_attend", "dsa_get_error",
             "dsa_last_launch_count", "dsa_status_str", "dsa_index_topk_static", "dsa_last_cuda_error",
-            "dsa_quantize_store_keys", "dsa_quantize_store_latents", "dsa_attend_shared"]
+            "dsa_quantize_store_keys", "dsa_quantize_store_latents", "dsa_attend_shared", "dsa_plan_capturable",
+            "dsa_plan_update", "dsa_plan_read_counts"]
+
+# dsa_device_span_t: q_len, ctx_start, page_start, page_off, num_pages, reserved (int32 each)
+DEVICE_SPAN_FIELDS = 6
 
 
 class DSAError(RuntimeError):
@@ -94,6 +98,9 @@ def load() -> ctypes.CDLL:
     L.dsa_topk_from_scores.argtypes = [vp, vp, vp, vp, vp]
     L.dsa_attend.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp]
     L.dsa_attend_shared.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp]
+    L.dsa_plan_capturable.argtypes = [vp, i32, i32, i64, i32, i32, vp, ctypes.POINTER(vp)]
+    L.dsa_plan_update.argtypes = [vp, vp, vp, vp, vp, i64, vp]
+    L.dsa_plan_read_counts.argtypes = [vp, ctypes.POINTER(i32 * 8)]
     L.dsa_get_error.argtypes = [vp, vp]
     L.dsa_last_launch_count.argtypes = [vp]
     L.dsa_last_launch_count.restype = i32
@@ -103,7 +110,8 @@ def load() -> ctypes.CDLL:
     L.dsa_status_str.restype = ctypes.c_char_p
     for name in ("dsa_create", "dsa_plan", "dsa_plan_get_info", "dsa_store_keys", "dsa_index_topk", "dsa_index_topk_static",
                  "dsa_index_scores", "dsa_topk_from_scores", "dsa_attend", "dsa_get_error", "dsa_quantize_store_keys",
-                 "dsa_quantize_store_latents", "dsa_attend_shared"):
+                 "dsa_quantize_store_latents", "dsa_attend_shared", "dsa_plan_capturable", "dsa_plan_update",
+                 "dsa_plan_read_counts"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -150,10 +158,11 @@ def _stream(stream) -> ctypes.c_void_p:
 class Plan:
     """A step's rows (dsa_plan_t).  Keeps the spans' page arrays alive."""
 
-    def __init__(self, ctx: "Context", handle: ctypes.c_void_p, keepalive):
+    def __init__(self, ctx: "Context", handle: ctypes.c_void_p, keepalive, capturable: bool = False):
         self.ctx = ctx
         self.handle = handle
         self._keep = keepalive
+        self.capturable = capturable
         info = PlanInfo()
         _check(load().dsa_plan_get_info(handle, ctypes.byref(info)), "dsa_plan_get_info")
         self.info = info
@@ -169,6 +178,13 @@ class Plan:
     @property
     def num_scores(self) -> int:
         return int(self.info.num_scores)
+
+    def read_counts(self) -> dict:
+        """dsa_plan_read_counts (capturable plans; synchronises the device)."""
+        c = (ctypes.c_int32 * 8)()
+        _check(load().dsa_plan_read_counts(self.handle, ctypes.byref(c)), "dsa_plan_read_counts")
+        return {"rows": c[0], "index_items": c[1], "attend_units": c[2], "split_rows": c[3], "slots": c[4],
+                "valid": bool(c[5]), "splits": c[6], "num_scores": c[7]}
 
     def close(self):
         if self.handle:
@@ -221,6 +237,29 @@ class Context:
         st = None if self.device_index < 0 else _stream(stream)
         _check(load().dsa_plan(self.handle, arr, len(spans), int(cache_pages), st, ctypes.byref(h)), "dsa_plan")
         return Plan(self, h, (arr, keep))
+
+    def plan_capturable(self, max_rows: int, max_spans: int, max_scores: int, cache_pages: int,
+                        page_start_align: int = 1, stream=None) -> Plan:
+        """dsa_plan_capturable: a fixed-capacity plan that dsa_plan_update
+        rewrites on the device (capturable in a CUDA graph)."""
+        h = ctypes.c_void_p()
+        st = None if self.device_index < 0 else _stream(stream)
+        _check(load().dsa_plan_capturable(self.handle, int(max_rows), int(max_spans), int(max_scores),
+                                          int(page_start_align), int(cache_pages), st, ctypes.byref(h)),
+               "dsa_plan_capturable", self.handle)
+        return Plan(self, h, None, capturable=True)
+
+    def plan_update(self, plan: Plan, num_spans: torch.Tensor, spans: torch.Tensor, pages: torch.Tensor, stream=None):
+        """dsa_plan_update: num_spans (1,) int32, spans (max_spans, 6) int32
+        [q_len, ctx_start, page_start, page_off, num_pages, 0], pages int32;
+        all on the device.  Enqueued on the stream; nothing synchronises."""
+        d = self.device
+        if spans.dim() != 2 or spans.shape[1] != DEVICE_SPAN_FIELDS:
+            raise ValueError("spans must be (max_spans, %d) int32" % DEVICE_SPAN_FIELDS)
+        plan._keep = (num_spans, spans, pages)   # the plan keeps pointing at the page array
+        _check(load().dsa_plan_update(self.handle, plan.handle, _ptr(num_spans, d, (torch.int32,), "num_spans"),
+                                      _ptr(spans, d, (torch.int32,), "spans"), _ptr(pages, d, (torch.int32,), "pages"),
+                                      int(pages.numel()), _stream(stream)), "dsa_plan_update", self.handle)
 
     # -------------------------------------------------------------- compute
     def store_keys(self, plan: Plan, keys: torch.Tensor, index_cache: torch.Tensor, stream=None):

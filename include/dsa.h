@@ -223,8 +223,79 @@ enum { DSA_ERR_SCRATCH_LIMIT = 8 };
 dsa_status dsa_index_topk_static(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *q, const float *w,
                                  const void *index_cache, int32_t *selection, dsa_stream_t stream);
 
+/* ---- Capturable plans --------------------------------------------------
+ * The pages' follow-up gives selection and attention fixed-shape buffers "so
+ * a decode can capture" (mstar.engine.resources.dsa.manager, module
+ * overview), and graph mode pads a layout to its bucket's ceiling with
+ * zero-length entries and sizes index buffers for the worst prefix sum the
+ * bucket allows (mstar.engine.resources.attn.ragged.block_causal:
+ * RaggedBlockCausalWrapper, max_blocks, max_prefix_tokens).
+ *
+ * dsa_plan_capturable allocates a plan for at most max_rows rows in at most
+ * max_spans spans whose rows score at most max_scores keys in total (the sum
+ * over rows of pos+1), with every span's page_start a multiple of
+ * page_start_align (>= 1).  The plan owns its metadata and score/partial
+ * scratch (plain cudaMalloc, so a captured graph may keep pointing at them)
+ * and starts empty.  dsa_plan_update recomputes it ON THE DEVICE, enqueued
+ * on `stream`, from spans in device memory:
+ *   num_spans  device int32 scalar, 0 .. max_spans;
+ *   spans      device dsa_device_span_t[max_spans] (the first num_spans read);
+ *   pages      device int32 page ids; span s uses pages[page_off ..
+ *              page_off + num_pages); num_page_ids is the array's length.
+ * The rows are the spans' rows in order (row 0 = span 0's first row).  The
+ * update makes no allocation, copy or synchronisation, so it and every call
+ * that follows with this plan can be captured in a CUDA graph and replayed
+ * after the caller rewrites num_spans / spans / pages in place (the plan
+ * keeps the `pages` pointer: pass the same array to every update of a
+ * captured sequence).
+ *
+ * With a capturable plan every entry point above takes max_rows rows of
+ * per-row input and output (q, w, keys, q_nope, q_pe, selection, out) and
+ * treats rows at or after the update's row count as padding: nothing of a
+ * padding row is read or written.  Work is launched for the plan's
+ * capacity; padded work items exit at once.  The indexer scores every row
+ * with the single-row kernel (a host plan groups the rows of a prefill chunk
+ * four at a time), so scores can differ from a host plan's in the last bit
+ * for chunk rows; decode rows get identical results.  dsa_plan_get_info
+ * returns the capacities (num_rows = max_rows, num_scores = max_scores,
+ * attend_units = the most units any update can make, needs_selection = 1).
+ *
+ * A span is invalid when q_len < 1, ctx_start < 0, page_start < 0 or not a
+ * multiple of page_start_align, num_pages < 0, page_off < 0, page_off +
+ * num_pages > num_page_ids, or num_pages * page_size < page_start +
+ * ctx_start + q_len; the update is invalid when num_spans is outside 0 ..
+ * max_spans, the rows exceed max_rows or the scores exceed max_scores.
+ * Then the plan is left empty (every later call does nothing) and the
+ * device error word records it: DSA_ERR_BAD_SPANS at the next dsa_get_error.
+ * Page ids themselves are checked where they are used (DSA_ERR_BOUNDS).
+ * Host-side errors: DSA_ERR_INVALID_ARG (host-only context, non-positive
+ * capacities or alignment, max_scores < max_rows, null pointers, a plan that
+ * is not capturable), DSA_ERR_OOM. */
+typedef struct dsa_device_span {
+  int32_t q_len;
+  int32_t ctx_start;
+  int32_t page_start;
+  int32_t page_off;
+  int32_t num_pages;
+  int32_t reserved;      /* set to 0 */
+} dsa_device_span_t;
+enum { DSA_ERR_BAD_SPANS = 9 };
+dsa_status dsa_plan_capturable(dsa_ctx_t *ctx, int32_t max_rows, int32_t max_spans, int64_t max_scores,
+                               int32_t page_start_align, int32_t cache_pages, dsa_stream_t stream,
+                               dsa_plan_t **out);
+dsa_status dsa_plan_update(dsa_ctx_t *ctx, dsa_plan_t *plan, const int32_t *num_spans,
+                           const dsa_device_span_t *spans, const int32_t *pages, int64_t num_page_ids,
+                           dsa_stream_t stream);
+/* The counts the last update of a capturable plan computed, copied to the
+ * host after synchronising the device: counts[0] rows, [1] indexer items,
+ * [2] attention units, [3] split rows, [4] partial slots, [5] 1 when the
+ * spans were valid, [6] the key split of the rows, [7] the scored keys
+ * (clamped to INT32_MAX).  DSA_ERR_INVALID_ARG for a host plan. */
+dsa_status dsa_plan_read_counts(const dsa_plan_t *plan, int32_t counts[8]);
+
 /* Synchronise `stream`, read and clear the context's device error word.
- * Returns DSA_OK, DSA_ERR_BOUNDS, DSA_ERR_TIMEOUT or DSA_ERR_CUDA. */
+ * Returns DSA_OK, DSA_ERR_BOUNDS, DSA_ERR_TIMEOUT, DSA_ERR_BAD_SPANS or
+ * DSA_ERR_CUDA. */
 dsa_status dsa_get_error(dsa_ctx_t *ctx, dsa_stream_t stream);
 
 /* Number of kernels the last compute call on this context launched (for

@@ -38,8 +38,9 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for s in range(8):
-        assert lib.dsa_status_str(s)
+    for s in range(10):
+        assert lib.dsa_status_str(s) and lib.dsa_status_str(s) != b"unknown status"
+    assert lib.dsa_status_str(10) == b"unknown status"
 
 
 def _host_ctx(shape=None):
@@ -117,3 +118,16 @@ def test_compute_calls_refuse_host_only_context(lib):
     assert st == 1
     assert L.dsa_attend(ctx.handle, plan.handle, None, None, None, None, None, ctypes.c_float(1.0), None, None) == 1
     assert L.dsa_get_error(ctx.handle, None) == 1
+
+
+def test_capturable_plan_calls_refuse_host_only_context_and_host_plans(lib):
+    ctx = _host_ctx()
+    assert _status(lambda: ctx.plan_capturable(8, 8, 1000, 10)) == 1
+    L = dsa.load()
+    h = ctypes.c_void_p()
+    assert L.dsa_plan_capturable(None, 8, 8, 1000, 1, 10, None, ctypes.byref(h)) == 1
+    assert L.dsa_plan_capturable(ctx.handle, 8, 8, 1000, 1, 10, None, None) == 1
+    plan = ctx.plan([S(0, 1, 0, np.array([0], np.int32))], cache_pages=1)
+    assert L.dsa_plan_update(ctx.handle, plan.handle, None, None, None, 0, None) == 1
+    counts = (ctypes.c_int32 * 8)()
+    assert L.dsa_plan_read_counts(plan.handle, ctypes.byref(counts)) == 1   # a host plan has no device counts
