@@ -234,6 +234,41 @@ def run_ours(args, name, rank, world, local_rank):
         total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
     units_per_step = work["rows"]
+    eager_ms = ms_per_step
+
+    # ---- decode: the step as one CUDA graph over a capturable plan, which
+    # re-plans on the device every step (spans, pages and counts in device
+    # memory), so no host work sits between the kernels
+    graph = None
+    if decode and not args.eager:
+        graph = capture_decode_step(ctx, wl, ic, lc, st, sel, out, dev)
+        for _ in range(args.warmup):
+            graph["replay"]()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+        g_ms = []
+        with ClockSampler(local_rank) as gclk:
+            for _ in range(args.steps):
+                flush.zero_()
+                ev[0].record(stream)
+                graph["replay"]()
+                ev[1].record(stream)
+                ev[1].synchronize()
+                g_ms.append(ev[0].elapsed_time(ev[1]))
+        torch.cuda.synchronize(dev)
+        ctx.get_error()
+        counts = graph["plan"].read_counts()
+        assert counts["valid"] and counts["rows"] == work["rows"], counts
+        total_ms = float(sum(g_ms))
+        if world > 1:
+            t = torch.tensor([total_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            total_ms = float(t.item())
+        ms_per_step = total_ms / args.steps
+        n_launch = graph["launches"] * args.steps
+        clk = gclk
     value = units_per_step * world / (ms_per_step / 1e3)
 
     # ---- end to end through the public API with host buffers
@@ -243,7 +278,24 @@ def run_ours(args, name, rank, world, local_rank):
     d2h = out_h.numel() * out_h.element_size()
     dbuf = {k: torch.empty_like(getattr(st, k)) for k in pinned}
 
-    def e2e_step():
+    if graph is not None:
+        # per step: this step's inputs and its spans and page table to the
+        # device, the captured step, the output back
+        pin_sp = {k: v.cpu().pin_memory() for k, v in graph["spans"].items()}
+        h2d += sum(t.numel() * t.element_size() for t in pin_sp.values())
+
+        def e2e_step():
+            for k, v in pinned.items():
+                graph["inputs"][k].copy_(v, non_blocking=True)
+            for k, v in pin_sp.items():
+                graph["spans"][k].copy_(v, non_blocking=True)
+            graph["replay"]()
+            out_h.copy_(out, non_blocking=True)
+            torch.cuda.current_stream(dev).synchronize()
+    else:
+        e2e_step = None
+
+    def e2e_eager_step():
         p = ctx.plan(wl.spans, wl.num_pages)
         for k, v in pinned.items():
             dbuf[k].copy_(v, non_blocking=True)
@@ -254,6 +306,8 @@ def run_ours(args, name, rank, world, local_rank):
         torch.cuda.current_stream(dev).synchronize()
         p.close()
 
+    if e2e_step is None:
+        e2e_step = e2e_eager_step
     for _ in range(max(1, args.warmup)):
         e2e_step()
     e2e_steps = max(3, min(args.steps, 20))
@@ -296,6 +350,9 @@ def run_ours(args, name, rank, world, local_rank):
         "index_tflops": round(work["index_flops"] / (idx_ms / 1e3) / 1e12, 2),
         "attend_tflops": round(work["attend_flops"] / (att_ms / 1e3) / 1e12, 2),
         "plan_ms": round(plan_ms, 3),
+        "step_path": ("CUDA graph: device re-plan + store + index/top-k + attend" if graph else
+                      "eager calls over a host plan built once"),
+        "eager_ms_per_step": round(eager_ms, 4),
         "e2e": {"value": round(units_per_step * world / e2e_s, 2), "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 3)},
         "gpu_launches": n_launch,
@@ -304,6 +361,52 @@ def run_ours(args, name, rank, world, local_rank):
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_rows)
     return line
+
+
+def capture_decode_step(ctx, wl, ic, lc, st, sel, out, dev):
+    """The decode step as one CUDA graph over a capturable plan: the plan is
+    rewritten on the device from the spans and page table in device memory
+    (dsa_plan_update), then store_keys, index_topk and attend run over it.
+    Replaying the graph after rewriting those tensors serves the next step."""
+    import math
+    sh = wl.shape
+    rows, pages, off = [], [], 0
+    for s in wl.spans:
+        rows.append([s.q_len, s.ctx_start, s.page_start, off, len(s.pages), 0])
+        pages.append(np.asarray(s.pages, np.int32))
+        off += len(s.pages)
+    spans = {"num_spans": torch.tensor([len(rows)], dtype=torch.int32, device=dev),
+             "spans": torch.tensor(rows, dtype=torch.int32, device=dev),
+             "pages": torch.from_numpy(np.concatenate(pages)).to(dev)}
+    max_scores = sum((s.ctx_start + 1 + s.ctx_end) * s.q_len // 2 for s in wl.spans)
+    align = math.gcd(sh.page_size, *[int(s.page_start) for s in wl.spans])
+    plan = ctx.plan_capturable(wl.num_rows, len(rows), max_scores, wl.num_pages, page_start_align=align)
+    inputs = {k: getattr(st, k).clone() for k in ("q", "w", "keys", "q_nope", "q_pe")}
+    launches = [0]
+
+    def step():
+        n = 0
+        ctx.plan_update(plan, spans["num_spans"], spans["spans"], spans["pages"])
+        n += ctx.last_launch_count()
+        ctx.store_keys(plan, inputs["keys"], ic)
+        n += ctx.last_launch_count()
+        ctx.index_topk(plan, inputs["q"], inputs["w"], ic, sel)
+        n += ctx.last_launch_count()
+        ctx.attend(plan, sel, inputs["q_nope"], inputs["q_pe"], lc, st.sink, sh.sm_scale, out)
+        n += ctx.last_launch_count()
+        launches[0] = n
+
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        step()   # outside the capture: one-time kernel attributes
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize(dev)
+    ctx.get_error()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    return {"plan": plan, "graph": g, "replay": g.replay, "inputs": inputs, "spans": spans, "launches": launches[0]}
 
 
 def profile_traffic(kernel, workload):
@@ -413,6 +516,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-rows", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="decode workloads: time the eager calls over a host plan instead of the captured step")
     ap.add_argument("--requests", type=int, default=0,
                     help="keep only the first N requests of the workload (profiler captures; not a bench line)")
     args = ap.parse_args()

@@ -452,8 +452,8 @@ dsa_status dsa_plan_capturable(dsa_ctx_t *ctx, int32_t max_rows, int32_t max_spa
                                dsa_plan_t **out) {
   if (!out) return DSA_ERR_INVALID_ARG;
   *out = nullptr;
-  if (!ctx || is_host_only(ctx) || max_rows <= 0 || max_spans <= 0 || max_rows > INT32_MAX / 2 ||
-      max_spans > INT32_MAX / 2 || max_scores < max_rows || max_scores > (int64_t(1) << 40) || page_start_align <= 0 ||
+  if (!ctx || is_host_only(ctx) || max_rows <= 0 || max_spans <= 0 || max_rows > kPlanMaxRows ||
+      max_spans > kPlanMaxSpans || max_scores < max_rows || max_scores > (int64_t(1) << 40) || page_start_align <= 0 ||
       cache_pages < 0)
     return DSA_ERR_INVALID_ARG;
   const dsa_config_t &c = ctx->cfg;
@@ -503,15 +503,15 @@ dsa_status dsa_plan_capturable(dsa_ctx_t *ctx, int32_t max_rows, int32_t max_spa
   const size_t o_pos = lay.take<int32_t>(max_rows), o_poff = lay.take<int32_t>(max_rows),
                o_np = lay.take<int32_t>(max_rows), o_ps = lay.take<int32_t>(max_rows),
                o_soff = lay.take<int64_t>(max_rows), o_g = lay.take<IdxGroup>(max_rows),
-               o_i = lay.take<IdxItem>(items_cap), o_t0 = lay.take<int64_t>(items_cap + 1),
-               o_c = lay.take<int32_t>(idx_cap + 1), o_u = lay.take<AttUnit>(units_cap),
-               o_cb = lay.take<AttCombine>(max_rows), o_q0 = lay.take<int32_t>(max_spans + 1),
-               o_n = lay.take<int32_t>(8);
+               o_i = lay.take<IdxItem>(items_cap), o_c = lay.take<int32_t>(idx_cap + 1),
+               o_u = lay.take<AttUnit>(units_cap), o_cb = lay.take<AttCombine>(max_rows), o_n = lay.take<int32_t>(8),
+               o_sp = lay.take<int8_t>(max_rows + 1);
   auto fail = [&](dsa_status st) {
     dsa_plan_destroy(plan);
     return st;
   };
   if (cudaSetDevice(ctx->device) != cudaSuccess) return fail(DSA_ERR_CUDA);
+  if (prepare_plan_update(max_rows, max_spans) != cudaSuccess) return fail(DSA_ERR_CUDA);
   const size_t hl = static_cast<size_t>(c.heads) * c.kv_lora_rank;
   if (cudaMalloc(reinterpret_cast<void **>(&plan->dev), lay.bytes) != cudaSuccess ||
       cudaMalloc(reinterpret_cast<void **>(&plan->own_scores), static_cast<size_t>(max_scores) * sizeof(float)) !=
@@ -529,18 +529,19 @@ dsa_status dsa_plan_capturable(dsa_ctx_t *ctx, int32_t max_rows, int32_t max_spa
   plan->row_score_off = reinterpret_cast<int64_t *>(d + o_soff);
   set.groups = reinterpret_cast<IdxGroup *>(d + o_g);
   set.items = reinterpret_cast<IdxItem *>(d + o_i);
-  plan->item_tile0 = reinterpret_cast<int64_t *>(d + o_t0);
   set.cta_begin = reinterpret_cast<int32_t *>(d + o_c);
   plan->units = reinterpret_cast<AttUnit *>(d + o_u);
   plan->combine = reinterpret_cast<AttCombine *>(d + o_cb);
-  plan->span_q0 = reinterpret_cast<int32_t *>(d + o_q0);
   plan->counts = reinterpret_cast<int32_t *>(d + o_n);
+  plan->splits_by_rows = reinterpret_cast<int8_t *>(d + o_sp);
   // an empty plan until the first update: every row is padding, no work
   std::vector<char> h(lay.bytes, 0);
   std::fill_n(reinterpret_cast<int32_t *>(h.data() + o_pos), max_rows, -1);
   for (int64_t i = 0; i < items_cap; ++i) reinterpret_cast<IdxItem *>(h.data() + o_i)[i] = IdxItem{-1, 0, 0, 0};
   for (int64_t i = 0; i < units_cap; ++i) reinterpret_cast<AttUnit *>(h.data() + o_u)[i] = AttUnit{-1, 0, 0, -1};
   for (int32_t i = 0; i < max_rows; ++i) reinterpret_cast<AttCombine *>(h.data() + o_cb)[i] = AttCombine{-1, 0, 0, 0};
+  for (int32_t t = 0; t <= max_rows; ++t)
+    reinterpret_cast<int8_t *>(h.data() + o_sp)[t] = static_cast<int8_t>(attention_splits(t, c.topk, ctx->num_sms));
   if (cudaMemcpy(plan->dev, h.data(), lay.bytes, cudaMemcpyHostToDevice) != cudaSuccess) return fail(DSA_ERR_CUDA);
   *out = plan;
   return DSA_OK;

@@ -694,14 +694,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
 // Merge of split rows: o = sum_s 2^(m_s - m) O_s / (sum_s 2^(m_s - m) l_s [+ 2^(sink - m)]).
 // One block per (row, head); threads over the latent columns.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) attend_combine_kernel(const AttCombine *__restrict__ combine,
-                                                             const float *__restrict__ opart,
-                                                             const float *__restrict__ mlpart,
-                                                             const float *__restrict__ sink, __nv_bfloat16 *out,
-                                                             int H, int L) {
-  const AttCombine cb = combine[blockIdx.x / H];
+__device__ void combine_one(const AttCombine cb, int h, const float *__restrict__ opart,
+                            const float *__restrict__ mlpart, const float *__restrict__ sink, __nv_bfloat16 *out,
+                            int H, int L) {
   if (cb.row < 0) return;   // padding of a capturable plan
-  const int h = blockIdx.x % H;
   float m = sink ? sink[h] * kLog2e : -INFINITY;
   for (int s = 0; s < cb.nsplit; ++s) m = fmaxf(m, mlpart[((cb.first_slot + s) * static_cast<int64_t>(H) + h) * 2]);
   float lsum = sink ? exp2f(sink[h] * kLog2e - m) : 0.f;
@@ -718,6 +714,18 @@ __global__ void __launch_bounds__(128) attend_combine_kernel(const AttCombine *_
     }
     out[(static_cast<int64_t>(cb.row) * H + h) * L + d] = __float2bfloat16_rn(acc * inv);
   }
+}
+
+
+__global__ void __launch_bounds__(128) attend_combine_kernel(const AttCombine *__restrict__ combine,
+                                                             const float *__restrict__ opart,
+                                                             const float *__restrict__ mlpart,
+                                                             const float *__restrict__ sink, __nv_bfloat16 *out,
+                                                             int H, int L, int n_merge,
+                                                             const int32_t *__restrict__ n_merge_dev) {
+  // (merge, head) pairs; a capturable plan's merge count is on the device
+  const int n_work = (n_merge_dev ? *n_merge_dev : n_merge) * H;
+  for (int w = blockIdx.x; w < n_work; w += gridDim.x) combine_one(combine[w / H], w % H, opart, mlpart, sink, out, H, L);
 }
 
 // ---------------------------------------------------------------------------
@@ -865,10 +873,13 @@ cudaError_t launch_attend(const dsa_ctx *ctx, const dsa_plan_t *plan, const int3
     if (e != cudaSuccess) return e;
     *launches += 1;
     if (plan->n_combine > 0) {
-      attend_combine_kernel<<<plan->n_combine * c.heads, 128, 0, s>>>(plan->combine, plan_opart(ctx, plan),
-                                                                      plan_mlpart(ctx, plan), sink,
-                                                                      static_cast<__nv_bfloat16 *>(out), c.heads,
-                                                                      c.kv_lora_rank);
+      // a capturable plan's merge count is known only on the device: a grid
+      // that strides over its (merge, head) pairs
+      const int grid = plan->capturable ? std::min(plan->n_combine * c.heads, ctx->num_sms * 16)
+                                        : plan->n_combine * c.heads;
+      attend_combine_kernel<<<grid, 128, 0, s>>>(plan->combine, plan_opart(ctx, plan), plan_mlpart(ctx, plan), sink,
+                                                 static_cast<__nv_bfloat16 *>(out), c.heads, c.kv_lora_rank,
+                                                 plan->n_combine, plan->capturable ? plan->counts + 3 : nullptr);
       e = cudaGetLastError();
       if (e != cudaSuccess) return e;
       *launches += 1;

@@ -53,6 +53,8 @@ struct AttCombine {
 
 constexpr int kIndexTile = 128;   // keys per indexer tile (UMMA M)
 constexpr int kAttTile = 64;      // keys per attention tile (UMMA N of QK)
+constexpr int kPlanMaxRows = 8192;   // capturable plans: rows and spans the device planner holds in shared memory
+constexpr int kPlanMaxSpans = 4096;
 
 // Tiles per indexer work item for `tiles` tiles over `cap` persistent CTAs.
 __host__ __device__ inline int64_t index_tiles_per_item(int64_t tiles, int cap) {
@@ -148,9 +150,8 @@ struct dsa_plan {
   int32_t max_spans = 0, items_cap = 0, combine_cap = 0, page_start_align = 1;
   int64_t page_ids = 0;                 // length of the page array of the last update
   float *own_scores = nullptr, *own_opart = nullptr, *own_mlpart = nullptr;
-  int32_t *span_q0 = nullptr;           // device scratch [max_spans + 1]
-  int64_t *item_tile0 = nullptr;        // device scratch [items_cap + 1]
   int32_t *counts = nullptr;            // device [8], see dsa_plan_read_counts
+  int8_t *splits_by_rows = nullptr;     // device [T + 1]: the attention key split of a step of that many rows
 };
 
 namespace dsa {
@@ -175,6 +176,9 @@ cudaError_t launch_topk(const dsa_ctx *ctx, const dsa_plan_t *plan, const float 
                         cudaStream_t s, int32_t *launches);
 cudaError_t launch_plan_update(const dsa_ctx *ctx, dsa_plan_t *plan, const int32_t *num_spans,
                                const dsa_device_span_t *spans, int64_t num_page_ids, cudaStream_t s);
+// Shared memory the device planner needs for these capacities; sets the
+// kernel's limit (call when the plan is made, outside any stream capture).
+cudaError_t prepare_plan_update(int32_t max_rows, int32_t max_spans);
 cudaError_t launch_attend(const dsa_ctx *ctx, const dsa_plan_t *plan, const int32_t *sel, const void *q_nope,
                           const void *q_pe, const void *latent, const float *sink, float sm_scale, void *out,
                           cudaStream_t s, int32_t *launches);

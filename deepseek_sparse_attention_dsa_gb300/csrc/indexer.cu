@@ -351,8 +351,10 @@ __global__ void __launch_bounds__(128) index_simt_kernel(const uint16_t *__restr
                                                           const int32_t *__restrict__ pages,
                                                           const int64_t *__restrict__ row_score_off,
                                                           float *__restrict__ scores, int *err, int Hi, int Di,
-                                                          int P, int fp8, int num_pages) {
+                                                          int P, int fp8, int num_pages,
+                                                          const int32_t *__restrict__ n_items_dev) {
   extern __shared__ float qs[];  // [Hi * Di] of one row, then [Hi] weights
+  if (n_items_dev && static_cast<int>(blockIdx.x) >= *n_items_dev) return;   // capturable plan: past its items
   const IdxItem item = items[blockIdx.x];
   if (item.group < 0) return;   // padding of a capturable plan
   const IdxGroup g = groups[item.group];
@@ -902,7 +904,8 @@ cudaError_t launch_index_scores(const dsa_ctx *ctx, const dsa_plan_t *plan, cons
                                                      static_cast<const uint8_t *>(cache), set.groups, set.items,
                                                      plan->pages, plan->row_score_off, scores, ctx->err,
                                                      c.index_heads, c.index_dim, c.page_size,
-                                                     c.index_fmt == DSA_INDEX_FP8_132, plan->cache_pages);
+                                                     c.index_fmt == DSA_INDEX_FP8_132, plan->cache_pages,
+                                                     plan->capturable ? plan->counts + 1 : nullptr);
       e = cudaGetLastError();
     }
     if (e != cudaSuccess) return e;

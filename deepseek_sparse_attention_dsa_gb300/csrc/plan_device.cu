@@ -8,13 +8,17 @@
 // max_blocks, max_prefix_tokens).  plan_update_kernel recomputes, from spans
 // in device memory, what dsa_plan computes on the host: each row's position
 // and page list, the score offsets, the indexer groups (one row each), items
-// and per-CTA item ranges, and the attention units and merges.  Padding is
-// marked so that its work exits at once: rows past the step get position -1,
-// items and units past the step's counts group / row -1.
+// and per-CTA item ranges, and the attention units and merges.  Rows past the
+// step get position -1 and attention units / merges past its counts row -1,
+// so their work exits at once; the counts themselves stay on the device.
 //
-// One CTA of 1024 threads; each thread takes a contiguous run of spans or
-// rows, and block-wide exclusive scans give the offsets.
+// One CTA of 1024 threads.  The spans and the per-row offsets live in shared
+// memory; each thread takes a contiguous run of spans or rows (at most
+// kMaxRowsPerThread), and block-wide exclusive scans give the offsets, so the
+// planner is a handful of passes with no chain of global-memory round trips.
 #include <cuda_runtime.h>
+
+#include <mutex>
 
 #include "dsa_internal.h"
 #include "ptx.cuh"
@@ -23,23 +27,24 @@ namespace dsa {
 namespace {
 
 constexpr int kPlanThreads = 1024;
+constexpr int kMaxRowsPerThread = kPlanMaxRows / kPlanThreads;
+static_assert(kPlanMaxRows % kPlanThreads == 0, "rows per thread");
 
 struct PlanUpdateParams {
   const int32_t *num_spans;
   const dsa_device_span_t *spans;
   int64_t num_page_ids;
   int64_t max_scores;
-  int32_t max_rows, max_spans, items_cap, units_cap, combine_cap, idx_cap;
+  int32_t max_rows, max_spans, units_cap, combine_cap, idx_cap;
   int32_t P, align, topk, num_sms;
-  int32_t *span_q0;
   int32_t *row_pos, *row_page_off, *row_npages, *row_page_start;
   int64_t *row_score_off;
   IdxGroup *groups;
   IdxItem *items;
-  int64_t *item_tile0;
   int32_t *cta_begin;
   AttUnit *units;
   AttCombine *combine;
+  const int8_t *splits_by_rows;   // [max_rows + 1]: attention_splits(T, topk, num_sms)
   int32_t *counts;
   int *err;
 };
@@ -77,17 +82,25 @@ __device__ __forceinline__ int64_t ceil_div(int64_t a, int64_t b) { return (a + 
 __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_update_kernel(const PlanUpdateParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  // shared memory: per row [max_rows + 1] int64 tile offsets and int32 item
+  // offsets, then per span [max_spans + 1] first rows and [max_spans] ctx_start,
+  // page_off, num_pages, page_start
+  int64_t *r_tile0 = reinterpret_cast<int64_t *>(smem_raw);
+  int32_t *r_item0 = reinterpret_cast<int32_t *>(r_tile0 + p.max_rows + 1);
+  int32_t *s_q0 = r_item0 + p.max_rows + 1;
+  int32_t *s_ctx = s_q0 + p.max_spans + 1;
+  int32_t *s_poff = s_ctx + p.max_spans;
+  int32_t *s_np = s_poff + p.max_spans;
+  int32_t *s_ps = s_np + p.max_spans;
   __shared__ int64_t sh[32];
   const int tid = threadIdx.x;
 
-  // ---- spans: validity, rows and scores
+  // ---- spans into shared memory, validity, rows and scores
   int n = *p.num_spans;
   bool ok = n >= 0 && n <= p.max_spans;
   if (!ok) n = 0;
-  const int spt = (p.max_spans + kPlanThreads - 1) / kPlanThreads;
-  const int sa = min(tid * spt, n), sb = min(sa + spt, n);
-  int64_t my_rows = 0, my_scores = 0;
-  for (int i = sa; i < sb; ++i) {
+  for (int i = tid; i < n; i += kPlanThreads) {
     const dsa_device_span_t s = p.spans[i];
     const int64_t end = static_cast<int64_t>(s.ctx_start) + s.q_len;   // tokens 0 .. end-1
     const bool v = s.q_len >= 1 && s.ctx_start >= 0 && s.page_start >= 0 && s.page_start % p.align == 0 &&
@@ -95,55 +108,66 @@ __global__ void __launch_bounds__(kPlanThreads) plan_update_kernel(const PlanUpd
                    static_cast<int64_t>(s.page_off) + s.num_pages <= p.num_page_ids && end <= INT32_MAX &&
                    static_cast<int64_t>(s.num_pages) * p.P >= s.page_start + end;
     ok = ok && v;
-    if (v) {
-      my_rows += s.q_len;
-      // rows at positions ctx_start .. end-1 score pos+1 keys each
-      my_scores += (static_cast<int64_t>(s.ctx_start) + 1 + end) * s.q_len / 2;
-    }
+    s_q0[i] = v ? s.q_len : 0;
+    s_ctx[i] = s.ctx_start;
+    s_poff[i] = s.page_off;
+    s_np[i] = s.num_pages;
+    s_ps[i] = s.page_start;
   }
   ok = __syncthreads_and(ok) != 0;
+  const int spt = (p.max_spans + kPlanThreads - 1) / kPlanThreads;
+  const int sa = min(tid * spt, n), sb = min(sa + spt, n);
+  int64_t my_rows = 0, my_scores = 0;
+  for (int i = sa; i < sb; ++i) {
+    const int64_t q = s_q0[i], c = s_ctx[i];
+    my_rows += q;
+    my_scores += (2 * c + 1 + q) * q / 2;   // rows at positions c .. c+q-1 score pos+1 keys each
+  }
   int64_t T = 0, total_scores = 0;
   const int64_t row0 = block_exclusive_scan(my_rows, &T, sh);
-  const int64_t score0 = block_exclusive_scan(my_scores, &total_scores, sh);
-  (void)score0;
+  block_exclusive_scan(my_scores, &total_scores, sh);
   if (T > p.max_rows || total_scores > p.max_scores) ok = false;   // uniform: totals are block-wide
   if (!ok) {
     n = 0;
     T = 0;
-    total_scores = 0;
     if (tid == 0) atomicOr(p.err, kErrSpans);
   } else {
     int64_t r = row0;
     for (int i = sa; i < sb; ++i) {
-      p.span_q0[i] = static_cast<int32_t>(r);
-      r += p.spans[i].q_len;
+      const int32_t q = s_q0[i];
+      s_q0[i] = static_cast<int32_t>(r);
+      r += q;
     }
-    if (tid == 0) p.span_q0[n] = static_cast<int32_t>(T);
+    if (tid == 0) s_q0[n] = static_cast<int32_t>(T);
   }
-  __syncthreads();   // span_q0 is visible to the block
+  __syncthreads();
 
-  // ---- rows: position and page list; score and indexer-tile offsets
+  // ---- rows: position and page list (kept in registers for the later passes)
   const int rpt = (p.max_rows + kPlanThreads - 1) / kPlanThreads;
-  const int ra = min(tid * rpt, p.max_rows), rb = min(ra + rpt, p.max_rows);
+  const int ra = min(tid * rpt, p.max_rows), rn = min(rpt, p.max_rows - ra);
+  int32_t pos[kMaxRowsPerThread];
   int64_t my_sc = 0, my_tiles = 0;
-  for (int r = ra; r < rb; ++r) {
-    int32_t pos = -1, poff = 0, np = 0, ps = 0;
+#pragma unroll
+  for (int k = 0; k < kMaxRowsPerThread; ++k) {
+    pos[k] = -1;
+    if (k >= rn) continue;
+    const int r = ra + k;
+    int32_t poff = 0, np = 0, ps = 0;
     if (r < T) {
       int lo = 0, hi = n - 1;   // the last span whose first row is <= r
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (p.span_q0[mid] <= r) lo = mid;
+        if (s_q0[mid] <= r) lo = mid;
         else hi = mid - 1;
       }
-      const dsa_device_span_t s = p.spans[lo];
-      pos = s.ctx_start + (r - p.span_q0[lo]);
-      poff = s.page_off;
-      np = s.num_pages;
-      ps = s.page_start;
-      my_sc += static_cast<int64_t>(pos) + 1;
-      my_tiles += ceil_div(static_cast<int64_t>(pos) + 1, kIndexTile);
+      pos[k] = s_ctx[lo] + (r - s_q0[lo]);
+      poff = s_poff[lo];
+      np = s_np[lo];
+      ps = s_ps[lo];
+      my_sc += static_cast<int64_t>(pos[k]) + 1;
+      my_tiles += ceil_div(static_cast<int64_t>(pos[k]) + 1, kIndexTile);
     }
-    p.row_pos[r] = pos;
+    p.row_pos[r] = pos[k];
     p.row_page_off[r] = poff;
     p.row_npages[r] = np;
     p.row_page_start[r] = ps;
@@ -152,45 +176,43 @@ __global__ void __launch_bounds__(kPlanThreads) plan_update_kernel(const PlanUpd
   int64_t sc = block_exclusive_scan(my_sc, &sc_total, sh);
   int64_t tile = block_exclusive_scan(my_tiles, &tiles_total, sh);
 
-  // ---- indexer items and attention units per row
-  const int64_t tpi = index_tiles_per_item(tiles_total, p.idx_cap);
-  const int splits = attention_splits(T, p.topk, p.num_sms);
+  // ---- indexer items and attention units per row (the key split of a
+  // T-row step comes from the plan's table, made on the host with the host
+  // planner's own function)
+  const int32_t tpi = static_cast<int32_t>(index_tiles_per_item(tiles_total, p.idx_cap));   // 2 .. 32
+  const int splits = p.splits_by_rows[T];
   // counts packed two per scan: (items << 32 | units), (slots << 32 | merges)
   int64_t my_iu = 0, my_sm = 0;
-  for (int r = ra; r < rb; ++r) {
-    const int32_t pos = p.row_pos[r];
-    if (pos < 0) continue;
-    const int64_t tiles = ceil_div(static_cast<int64_t>(pos) + 1, kIndexTile);
-    const int u = attention_row_units(pos, p.topk, splits);
-    my_iu += (ceil_div(tiles, tpi) << 32) + u;
+#pragma unroll
+  for (int k = 0; k < kMaxRowsPerThread; ++k) {
+    if (pos[k] < 0) continue;
+    const int32_t tiles = pos[k] / kIndexTile + 1;   // ceil((pos + 1) / 128)
+    const int u = attention_row_units(pos[k], p.topk, splits);
+    my_iu += (static_cast<int64_t>((tiles + tpi - 1) / tpi) << 32) + u;
     my_sm += u > 1 ? ((static_cast<int64_t>(u) << 32) + 1) : 0;
   }
   int64_t iu_total = 0, sm_total = 0;
   int64_t iu = block_exclusive_scan(my_iu, &iu_total, sh);
   int64_t smc = block_exclusive_scan(my_sm, &sm_total, sh);
-  int32_t n_items = static_cast<int32_t>(iu_total >> 32), n_units = static_cast<int32_t>(iu_total & 0xffffffff);
-  int32_t n_slots = static_cast<int32_t>(sm_total >> 32), n_merge = static_cast<int32_t>(sm_total & 0xffffffff);
-  // the capacities bound these counts for every update the span checks admit;
-  // should one not fit, the plan is emptied rather than overrun
-  if (n_items > p.items_cap || n_units > p.units_cap || n_merge > p.combine_cap || n_slots > p.units_cap) {
-    if (tid == 0) atomicOr(p.err, kErrSpans);
-    ok = false;
-    T = 0;
-    n_items = n_units = n_merge = n_slots = 0;
-    tiles_total = 0;
-    for (int r = ra; r < rb; ++r) p.row_pos[r] = -1;
-  }
-  for (int r = ra; r < rb; ++r) {
-    const int32_t pos = p.row_pos[r];
+  const int32_t n_items = static_cast<int32_t>(iu_total >> 32), n_units = static_cast<int32_t>(iu_total & 0xffffffff);
+  const int32_t n_slots = static_cast<int32_t>(sm_total >> 32), n_merge = static_cast<int32_t>(sm_total & 0xffffffff);
+  // the plan's capacities bound these counts for every update the span checks
+  // admit (see dsa_plan_capturable), so the writes below stay in bounds
+#pragma unroll
+  for (int k = 0; k < kMaxRowsPerThread; ++k) {
+    if (k >= rn) continue;
+    const int r = ra + k;
     p.row_score_off[r] = sc;
-    if (pos < 0) continue;
-    sc += static_cast<int64_t>(pos) + 1;
-    const int64_t tiles = ceil_div(static_cast<int64_t>(pos) + 1, kIndexTile);
+    r_tile0[r] = tile;
+    r_item0[r] = static_cast<int32_t>(iu >> 32);
+    if (pos[k] < 0) continue;
+    sc += static_cast<int64_t>(pos[k]) + 1;
+    const int32_t tiles = pos[k] / kIndexTile + 1;
     // the row is indexer group r (one row per group)
     IdxGroup g;
     g.row0 = r;
     g.nrows = 1;
-    g.pos0 = pos;
+    g.pos0 = pos[k];
     g.page_off = p.row_page_off[r];
     g.npages = p.row_npages[r];
     g.page_start = p.row_page_start[r];
@@ -198,50 +220,55 @@ __global__ void __launch_bounds__(kPlanThreads) plan_update_kernel(const PlanUpd
     g.pad = 0;
     p.groups[r] = g;
     int32_t item = static_cast<int32_t>(iu >> 32);
-    for (int64_t t0 = 0; t0 < tiles; t0 += tpi, ++item) {
-      p.items[item] = IdxItem{r, static_cast<int32_t>(t0), static_cast<int32_t>(min64(tiles, t0 + tpi)), 0};
-      p.item_tile0[item] = tile + t0;
-    }
+    for (int32_t t0 = 0; t0 < tiles; t0 += tpi, ++item) p.items[item] = IdxItem{r, t0, min(tiles, t0 + tpi), 0};
     tile += tiles;
-    // attention: whole row, or `u` key ranges with partial slots and a merge
-    const int64_t nsel = min64(p.topk, static_cast<int64_t>(pos) + 1);
+    // attention: the whole row, or `u` key ranges with partial slots and a merge
+    const int64_t nsel = min64(p.topk, static_cast<int64_t>(pos[k]) + 1);
     const int64_t atiles = ceil_div(nsel, kAttTile);
-    const int u = attention_row_units(pos, p.topk, splits);
+    const int u = attention_row_units(pos[k], p.topk, splits);
     const int32_t unit = static_cast<int32_t>(iu & 0xffffffff);
     if (u == 1) {
       p.units[unit] = AttUnit{r, 0, static_cast<int32_t>(nsel), -1};
     } else {
       const int32_t slot = static_cast<int32_t>(smc >> 32);
       p.combine[static_cast<int32_t>(smc & 0xffffffff)] = AttCombine{r, slot, u, 0};
-      for (int k = 0; k < u; ++k) {
-        const int64_t t0 = atiles * k / u, t1 = atiles * (k + 1) / u;
-        p.units[unit + k] = AttUnit{r, static_cast<int32_t>(t0 * kAttTile),
-                                    static_cast<int32_t>(min64(nsel, t1 * kAttTile)), slot + k};
+      for (int j = 0; j < u; ++j) {
+        const int64_t t0 = atiles * j / u, t1 = atiles * (j + 1) / u;
+        p.units[unit + j] = AttUnit{r, static_cast<int32_t>(t0 * kAttTile),
+                                    static_cast<int32_t>(min64(nsel, t1 * kAttTile)), slot + j};
       }
       smc += (static_cast<int64_t>(u) << 32) + 1;
     }
-    iu += (ceil_div(tiles, tpi) << 32) + u;
+    iu += (static_cast<int64_t>((tiles + tpi - 1) / tpi) << 32) + u;
   }
-  // padding: work past the step's counts exits at once
-  for (int i = n_items + tid; i < p.items_cap; i += kPlanThreads) p.items[i] = IdxItem{-1, 0, 0, 0};
+  if (tid == 0) {
+    r_tile0[p.max_rows] = tiles_total;
+    r_item0[p.max_rows] = n_items;
+  }
+  // padding: units and merges past the step's counts exit at once
   for (int i = n_units + tid; i < p.units_cap; i += kPlanThreads) p.units[i] = AttUnit{-1, 0, 0, -1};
   for (int i = n_merge + tid; i < p.combine_cap; i += kPlanThreads) p.combine[i] = AttCombine{-1, 0, 0, 0};
-  if (tid == 0) p.item_tile0[n_items] = tiles_total;
-  __syncthreads();   // item_tile0 is visible to the block
+  __syncthreads();
 
   // ---- per-CTA item ranges of the persistent indexer: CTA b starts at the
-  // first item that begins at or after tile tiles_total * b / idx_cap
+  // first item that begins at or after tile tiles_total * b / idx_cap.  Item
+  // starts grow along the rows, so the search runs over rows: the first row
+  // whose last item starts at or after the target, then the item inside it.
   for (int b = tid; b <= p.idx_cap; b += kPlanThreads) {
     int32_t k = n_items;
     if (b < p.idx_cap) {
       const int64_t target = tiles_total * b / p.idx_cap;
-      int lo = 0, hi = n_items;   // first k in [0, n_items] with item_tile0[k] >= target
+      int lo = 0, hi = static_cast<int>(T);   // first row in [0, T) whose last item starts at or after target
       while (lo < hi) {
         const int mid = (lo + hi) >> 1;
-        if (p.item_tile0[mid] < target) lo = mid + 1;
+        const int64_t last = r_tile0[mid] + static_cast<int64_t>(r_item0[mid + 1] - r_item0[mid] - 1) * tpi;
+        if (last < target) lo = mid + 1;
         else hi = mid;
       }
-      k = lo;
+      if (lo < T) {
+        const int32_t d = static_cast<int32_t>(target > r_tile0[lo] ? target - r_tile0[lo] : 0);   // < the row's tiles
+        k = r_item0[lo] + (d + tpi - 1) / tpi;
+      }
     }
     p.cta_begin[b] = k;
   }
@@ -259,6 +286,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_update_kernel(const PlanUpd
 
 }  // namespace
 
+static size_t plan_update_smem(int32_t max_rows, int32_t max_spans) {
+  return static_cast<size_t>(max_rows + 1) * (sizeof(int64_t) + sizeof(int32_t)) +
+         static_cast<size_t>(max_spans + 1) * sizeof(int32_t) + static_cast<size_t>(max_spans) * 4 * sizeof(int32_t);
+}
+
 cudaError_t launch_plan_update(const dsa_ctx *ctx, dsa_plan_t *plan, const int32_t *num_spans,
                                const dsa_device_span_t *spans, int64_t num_page_ids, cudaStream_t s) {
   PlanUpdateParams p;
@@ -268,7 +300,6 @@ cudaError_t launch_plan_update(const dsa_ctx *ctx, dsa_plan_t *plan, const int32
   p.max_scores = plan->num_scores;
   p.max_rows = plan->T;
   p.max_spans = plan->max_spans;
-  p.items_cap = plan->items_cap;
   p.units_cap = plan->n_units;
   p.combine_cap = plan->combine_cap;
   p.idx_cap = plan->idx[0].n_ctas;
@@ -276,7 +307,6 @@ cudaError_t launch_plan_update(const dsa_ctx *ctx, dsa_plan_t *plan, const int32
   p.align = plan->page_start_align;
   p.topk = ctx->cfg.topk;
   p.num_sms = ctx->num_sms;
-  p.span_q0 = plan->span_q0;
   p.row_pos = plan->row_pos;
   p.row_page_off = plan->row_page_off;
   p.row_npages = plan->row_npages;
@@ -284,14 +314,26 @@ cudaError_t launch_plan_update(const dsa_ctx *ctx, dsa_plan_t *plan, const int32
   p.row_score_off = plan->row_score_off;
   p.groups = plan->idx[0].groups;
   p.items = plan->idx[0].items;
-  p.item_tile0 = plan->item_tile0;
   p.cta_begin = plan->idx[0].cta_begin;
   p.units = plan->units;
   p.combine = plan->combine;
+  p.splits_by_rows = plan->splits_by_rows;
   p.counts = plan->counts;
   p.err = ctx->err;
-  plan_update_kernel<<<1, kPlanThreads, 0, s>>>(p);
+  plan_update_kernel<<<1, kPlanThreads, plan_update_smem(plan->T, plan->max_spans), s>>>(p);
   return cudaGetLastError();
+}
+
+cudaError_t prepare_plan_update(int32_t max_rows, int32_t max_spans) {
+  static std::mutex mu;
+  static size_t limit = 48 * 1024;
+  const size_t smem = plan_update_smem(max_rows, max_spans);
+  std::lock_guard<std::mutex> lock(mu);
+  if (smem <= limit) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(plan_update_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e == cudaSuccess) limit = smem;
+  return e;
 }
 
 }  // namespace dsa

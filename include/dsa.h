@@ -231,10 +231,11 @@ dsa_status dsa_index_topk_static(dsa_ctx_t *ctx, const dsa_plan_t *plan, const v
  * bucket allows (mstar.engine.resources.attn.ragged.block_causal:
  * RaggedBlockCausalWrapper, max_blocks, max_prefix_tokens).
  *
- * dsa_plan_capturable allocates a plan for at most max_rows rows in at most
- * max_spans spans whose rows score at most max_scores keys in total (the sum
- * over rows of pos+1), with every span's page_start a multiple of
- * page_start_align (>= 1).  The plan owns its metadata and score/partial
+ * dsa_plan_capturable allocates a plan for at most max_rows (<= 8192) rows in
+ * at most max_spans (<= 4096) spans whose rows score at most max_scores keys
+ * in total (the sum over rows of pos+1), with every span's page_start a
+ * multiple of page_start_align (>= 1); the device planner is one CTA that
+ * holds the spans and rows in shared memory.  The plan owns its metadata and score/partial
  * scratch (plain cudaMalloc, so a captured graph may keep pointing at them)
  * and starts empty.  dsa_plan_update recomputes it ON THE DEVICE, enqueued
  * on `stream`, from spans in device memory:
@@ -268,9 +269,9 @@ dsa_status dsa_index_topk_static(dsa_ctx_t *ctx, const dsa_plan_t *plan, const v
  * Then the plan is left empty (every later call does nothing) and the
  * device error word records it: DSA_ERR_BAD_SPANS at the next dsa_get_error.
  * Page ids themselves are checked where they are used (DSA_ERR_BOUNDS).
- * Host-side errors: DSA_ERR_INVALID_ARG (host-only context, non-positive
- * capacities or alignment, max_scores < max_rows, null pointers, a plan that
- * is not capturable), DSA_ERR_OOM. */
+ * Host-side errors: DSA_ERR_INVALID_ARG (host-only context, capacities out
+ * of range, non-positive alignment, max_scores < max_rows, null pointers, a
+ * plan that is not capturable), DSA_ERR_OOM. */
 typedef struct dsa_device_span {
   int32_t q_len;
   int32_t ctx_start;
