@@ -276,6 +276,28 @@ def run_ours(args, name, rank, world, local_rank):
                     "path": "CUDA graph: device re-plan + store + index/top-k + attend", "clocks": gclk.summary()}
     value = units_per_step * world / (ms_per_step / 1e3)
 
+    # ---- fp8 index cache: the indexer with an e4m3 query as well (the step
+    # above scores with the bf16 query)
+    fp8q = None
+    if sh.index_fmt == W.INDEX_FP8_132:
+        codes, qscale = ctx.quantize_q(plan, st.q)
+        qt, it = [], []
+        for i in range(args.warmup + args.steps):
+            flush.zero_()
+            ev[0].record(stream)
+            ctx.quantize_q(plan, st.q, codes, qscale)
+            ev[1].record(stream)
+            ctx.index_scores_fp8q(plan, codes, qscale, st.w, ic, scores)
+            ev[2].record(stream)
+            ev[2].synchronize()
+            if i >= args.warmup:
+                qt.append(ev[0].elapsed_time(ev[1]))
+                it.append(ev[1].elapsed_time(ev[2]))
+        ctx.get_error()
+        fp8q = {"quantize_ms": round(statistics.mean(qt), 4), "index_ms": round(statistics.mean(it), 4),
+                "index_tflops": round(work["index_flops"] / (statistics.mean(it) / 1e3) / 1e12, 2),
+                "path": "dsa_quantize_q + dsa_index_scores_fp8q (e4m3 x e4m3 tensor cores)"}
+
     # ---- end to end through the public API with host buffers
     pinned = {k: getattr(st, k).cpu().pin_memory() for k in ("q", "w", "keys", "q_nope", "q_pe")}
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -357,6 +379,7 @@ def run_ours(args, name, rank, world, local_rank):
         "plan_ms": round(plan_ms, 3),
         "step_path": "calls over a host plan built once (store, index/top-k, attend)",
         "captured_step": captured,
+        "fp8_query": fp8q,
         "e2e": {"value": round(units_per_step * world / e2e_s, 2), "unit": unit, "h2d_bytes_per_step": h2d,
                 "path": ("per step: inputs + spans + page table to the device, the captured step (device re-plan), "
                          "output back" if graph is not None else

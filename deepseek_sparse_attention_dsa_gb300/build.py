@@ -19,8 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libdsa_gb300.so")
-SOURCES = ["api.cu", "plan_device.cu", "store_keys.cu", "quantize.cu", "indexer.cu", "topk.cu", "attend.cu",
-           "static_scratch.cu"]
+SOURCES = ["api.cu", "plan_device.cu", "store_keys.cu", "quantize.cu", "indexer.cu", "indexer_f8q.cu", "topk.cu",
+           "attend.cu", "static_scratch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

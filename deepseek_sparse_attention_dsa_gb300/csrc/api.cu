@@ -670,6 +670,56 @@ dsa_status dsa_index_topk(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *q,
   return cuda_status(ctx, e);
 }
 
+static bool f8q_ok(const dsa_ctx_t *ctx, const dsa_plan_t *plan) {
+  return ctx->cfg.index_fmt == DSA_INDEX_FP8_132 && ctx->cfg.index_heads == 64 && ctx->cfg.index_dim == 128 &&
+         indexer_f8q_supported(ctx->cfg, plan);
+}
+
+dsa_status dsa_quantize_q(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *q_bf16, void *q_codes, float *q_scale,
+                          dsa_stream_t stream) {
+  dsa_status st = check_call(ctx, plan);
+  if (st != DSA_OK) return st;
+  ctx->last_launches = 0;
+  if (ctx->cfg.index_heads != 64 || ctx->cfg.index_dim != 128) return DSA_ERR_UNSUPPORTED;
+  if (plan->T == 0) return DSA_OK;
+  if (!q_bf16 || !q_codes || !q_scale) return DSA_ERR_INVALID_ARG;
+  cudaError_t e = launch_quantize_q(ctx, plan, q_bf16, q_codes, q_scale, reinterpret_cast<cudaStream_t>(stream),
+                                    &ctx->last_launches);
+  return cuda_status(ctx, e);
+}
+
+dsa_status dsa_index_scores_fp8q(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *q_codes, const float *q_scale,
+                                 const float *w, const void *index_cache, float *scores, dsa_stream_t stream) {
+  dsa_status st = check_call(ctx, plan);
+  if (st != DSA_OK) return st;
+  ctx->last_launches = 0;
+  if (!f8q_ok(ctx, plan)) return DSA_ERR_UNSUPPORTED;
+  if (plan->T == 0) return DSA_OK;
+  if (!q_codes || !q_scale || !w || !index_cache || !scores) return DSA_ERR_INVALID_ARG;
+  cudaError_t e = launch_index_scores_f8q(ctx, plan, q_codes, q_scale, w, index_cache, scores,
+                                          reinterpret_cast<cudaStream_t>(stream), &ctx->last_launches);
+  return cuda_status(ctx, e);
+}
+
+dsa_status dsa_index_topk_fp8q(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *q_codes, const float *q_scale,
+                               const float *w, const void *index_cache, int32_t *selection, dsa_stream_t stream) {
+  dsa_status st = check_call(ctx, plan);
+  if (st != DSA_OK) return st;
+  ctx->last_launches = 0;
+  if (!f8q_ok(ctx, plan)) return DSA_ERR_UNSUPPORTED;
+  if (plan->T == 0) return DSA_OK;
+  if (!q_codes || !q_scale || !w || !index_cache || !selection) return DSA_ERR_INVALID_ARG;
+  if (!plan->own_scores && static_cast<size_t>(plan->num_scores) > ctx->scores_cap) return DSA_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t n = 0;
+  float *scores = plan_scores(ctx, plan);
+  cudaError_t e = launch_index_scores_f8q(ctx, plan, q_codes, q_scale, w, index_cache, scores, s, &n);
+  if (e == cudaSuccess) e = launch_topk(ctx, plan, scores, selection, s, &n);
+  if (e == cudaSuccess) plan->last_selection = selection;
+  ctx->last_launches = n;
+  return cuda_status(ctx, e);
+}
+
 dsa_status dsa_attend(dsa_ctx_t *ctx, const dsa_plan_t *plan, const int32_t *selection, const void *q_nope,
                       const void *q_pe, const void *latent_cache, const float *sink, float sm_scale, void *out,
                       dsa_stream_t stream) {

@@ -168,6 +168,12 @@ cudaError_t launch_quantize_keys(const dsa_ctx *ctx, const dsa_plan_t *plan, con
                                  cudaStream_t s, int32_t *launches);
 cudaError_t launch_quantize_latents(const dsa_ctx *ctx, const dsa_plan_t *plan, const void *latents, void *cache,
                                     cudaStream_t s, int32_t *launches);
+cudaError_t launch_quantize_q(const dsa_ctx *ctx, const dsa_plan_t *plan, const void *q, void *codes, float *scales,
+                              cudaStream_t s, int32_t *launches);
+cudaError_t launch_index_scores_f8q(const dsa_ctx *ctx, const dsa_plan_t *plan, const void *q_codes,
+                                    const float *q_scale, const float *w, const void *cache, float *scores,
+                                    cudaStream_t s, int32_t *launches);
+bool indexer_f8q_supported(const dsa_config_t &c, const dsa_plan_t *plan);
 cudaError_t launch_store_keys(const dsa_ctx *ctx, const dsa_plan_t *plan, const void *keys, void *cache,
                               cudaStream_t s, int32_t *launches);
 cudaError_t launch_index_scores(const dsa_ctx *ctx, const dsa_plan_t *plan, const void *q, const float *w,

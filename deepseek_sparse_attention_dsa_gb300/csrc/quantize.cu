@@ -130,7 +130,40 @@ __global__ void __launch_bounds__(256) quantize_latents_kernel(const uint8_t *__
   if (lane < 8) reinterpret_cast<uint4 *>(dst + L + 4 * (L / 128))[lane] = reinterpret_cast<const uint4 *>(src + 2 * L)[lane];
 }
 
+// 128 bf16 values of one (row, head) of the indexer query -> 128 codes and one
+// scale (dsa_quantize_q); lane l handles values 4l .. 4l+3.  Rows at position
+// -1 (padding of a capturable plan) are skipped.
+__global__ void __launch_bounds__(256) quantize_q_kernel(const uint2 *__restrict__ q, uint32_t *__restrict__ codes,
+                                                         float *__restrict__ scales,
+                                                         const int32_t *__restrict__ row_pos, int T, int Hi) {
+  const int64_t g = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
+  if (g >= static_cast<int64_t>(T) * Hi || row_pos[g / Hi] < 0) return;
+  const int lane = lane_id();
+  const uint2 raw = q[g * 32 + lane];
+  const float v[4] = {bf16_bits_to_float(raw.x & 0xFFFFu), bf16_bits_to_float(raw.x >> 16),
+                      bf16_bits_to_float(raw.y & 0xFFFFu), bf16_bits_to_float(raw.y >> 16)};
+  float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+  for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float scale = amax > 0.f ? amax / 448.f : 1.f;
+  uint32_t word = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) word |= e4m3_code(v[i] / scale) << (8 * i);
+  codes[g * 32 + lane] = word;
+  if (lane == 0) scales[g] = scale;
+}
+
 }  // namespace
+
+cudaError_t launch_quantize_q(const dsa_ctx *ctx, const dsa_plan_t *plan, const void *q, void *codes, float *scales,
+                              cudaStream_t s, int32_t *launches) {
+  const int64_t groups = static_cast<int64_t>(plan->T) * ctx->cfg.index_heads;
+  quantize_q_kernel<<<static_cast<unsigned>((groups + 7) / 8), 256, 0, s>>>(
+      static_cast<const uint2 *>(q), static_cast<uint32_t *>(codes), scales, plan->row_pos, plan->T,
+      ctx->cfg.index_heads);
+  *launches += 1;
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quantize_keys(const dsa_ctx *ctx, const dsa_plan_t *plan, const void *keys, void *cache,
                                  cudaStream_t s, int32_t *launches) {

@@ -34,7 +34,8 @@ EXPORTED = ["dsa_create", "dsa_destroy", "dsa_plan", "dsa_plan_destroy", "dsa_pl
             "dsa_index_topk", "dsa_index_scores", "dsa_topk_from_scores", "dsa_attend", "dsa_get_error",
             "dsa_last_launch_count", "dsa_status_str", "dsa_index_topk_static", "dsa_last_cuda_error",
             "dsa_quantize_store_keys", "dsa_quantize_store_latents", "dsa_attend_shared", "dsa_plan_capturable",
-            "dsa_plan_update", "dsa_plan_read_counts"]
+            "dsa_plan_update", "dsa_plan_read_counts", "dsa_quantize_q", "dsa_index_scores_fp8q",
+            "dsa_index_topk_fp8q"]
 
 # dsa_device_span_t: q_len, ctx_start, page_start, page_off, num_pages, reserved (int32 each)
 DEVICE_SPAN_FIELDS = 6
@@ -101,6 +102,9 @@ def load() -> ctypes.CDLL:
     L.dsa_plan_capturable.argtypes = [vp, i32, i32, i64, i32, i32, vp, ctypes.POINTER(vp)]
     L.dsa_plan_update.argtypes = [vp, vp, vp, vp, vp, i64, vp]
     L.dsa_plan_read_counts.argtypes = [vp, ctypes.POINTER(i32 * 8)]
+    L.dsa_quantize_q.argtypes = [vp, vp, vp, vp, vp, vp]
+    L.dsa_index_scores_fp8q.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
+    L.dsa_index_topk_fp8q.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
     L.dsa_get_error.argtypes = [vp, vp]
     L.dsa_last_launch_count.argtypes = [vp]
     L.dsa_last_launch_count.restype = i32
@@ -111,7 +115,7 @@ def load() -> ctypes.CDLL:
     for name in ("dsa_create", "dsa_plan", "dsa_plan_get_info", "dsa_store_keys", "dsa_index_topk", "dsa_index_topk_static",
                  "dsa_index_scores", "dsa_topk_from_scores", "dsa_attend", "dsa_get_error", "dsa_quantize_store_keys",
                  "dsa_quantize_store_latents", "dsa_attend_shared", "dsa_plan_capturable", "dsa_plan_update",
-                 "dsa_plan_read_counts"):
+                 "dsa_plan_read_counts", "dsa_quantize_q", "dsa_index_scores_fp8q", "dsa_index_topk_fp8q"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -305,6 +309,46 @@ class Context:
                                             _ptr(index_cache, d, (torch.bfloat16, torch.uint8), "index_cache"),
                                             _ptr(selection, d, (torch.int32,), "selection"), _stream(stream)),
                "dsa_index_topk_static", self.handle)
+        return selection
+
+    def quantize_q(self, plan: Plan, q_bf16, codes=None, scales=None, stream=None):
+        """dsa_quantize_q: the indexer query (T, 64, 128) bf16 -> (codes uint8 of the
+        same shape, scales (T, 64) fp32), one scale per (row, head)."""
+        d = self.device
+        if codes is None:
+            codes = torch.empty(q_bf16.shape, dtype=torch.uint8, device=d)
+        if scales is None:
+            scales = torch.empty(q_bf16.shape[:-1], dtype=torch.float32, device=d)
+        _check(load().dsa_quantize_q(self.handle, plan.handle, _ptr(q_bf16, d, (torch.bfloat16,), "q"),
+                                     _ptr(codes, d, (torch.uint8,), "q_codes"),
+                                     _ptr(scales, d, (torch.float32,), "q_scale"), _stream(stream)),
+               "dsa_quantize_q", self.handle)
+        return codes, scales
+
+    def index_scores_fp8q(self, plan: Plan, q_codes, q_scale, w, index_cache, scores=None, stream=None):
+        """dsa_index_scores_fp8q: scores with an e4m3 query (fp8 index cache)."""
+        d = self.device
+        if scores is None:
+            scores = torch.empty(max(1, plan.num_scores), dtype=torch.float32, device=d)
+        _check(load().dsa_index_scores_fp8q(self.handle, plan.handle, _ptr(q_codes, d, (torch.uint8,), "q_codes"),
+                                            _ptr(q_scale, d, (torch.float32,), "q_scale"),
+                                            _ptr(w, d, (torch.float32,), "w"),
+                                            _ptr(index_cache, d, (torch.uint8,), "index_cache"),
+                                            _ptr(scores, d, (torch.float32,), "scores"), _stream(stream)),
+               "dsa_index_scores_fp8q", self.handle)
+        return scores
+
+    def index_topk_fp8q(self, plan: Plan, q_codes, q_scale, w, index_cache, selection=None, stream=None):
+        """dsa_index_topk_fp8q: score with an e4m3 query, then the causal top-k."""
+        d = self.device
+        if selection is None:
+            selection = torch.empty(plan.num_rows, self.shape.topk, dtype=torch.int32, device=d)
+        _check(load().dsa_index_topk_fp8q(self.handle, plan.handle, _ptr(q_codes, d, (torch.uint8,), "q_codes"),
+                                          _ptr(q_scale, d, (torch.float32,), "q_scale"),
+                                          _ptr(w, d, (torch.float32,), "w"),
+                                          _ptr(index_cache, d, (torch.uint8,), "index_cache"),
+                                          _ptr(selection, d, (torch.int32,), "selection"), _stream(stream)),
+               "dsa_index_topk_fp8q", self.handle)
         return selection
 
     def index_scores(self, plan: Plan, q, w, index_cache, scores=None, stream=None) -> torch.Tensor:

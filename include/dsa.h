@@ -223,6 +223,35 @@ enum { DSA_ERR_SCRATCH_LIMIT = 8 };
 dsa_status dsa_index_topk_static(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *q, const float *w,
                                  const void *index_cache, int32_t *selection, dsa_stream_t stream);
 
+/* ---- fp8 query for the indexer -----------------------------------------
+ * The indexer score with an e4m3 query over the fp8 index cache
+ * (DSA_INDEX_FP8_132, index_heads 64, index_dim 128): ttnn
+ * .transformer.sparse_sdpa takes its q as "bf16 or fp8_e4m3"; the index row
+ * is LLMServingSim's 132-byte [128 e4m3 | fp32 scale] ("What the KV cache
+ * actually holds").  Here the query of (row r, head h) is
+ *   q[r,h,d] = e4m3(q_codes[r,h,d]) * q_scale[r,h],
+ * and the score is the same definition as dsa_index_scores:
+ *   s[r,j] = sum_h w[r,h] * relu(q[r,h] . k[j]),  k[j,d] = e4m3(code) * scale,
+ * computed with e4m3 x e4m3 tensor-core products accumulated in fp32.
+ *
+ * dsa_quantize_q: q_bf16 (T, 64, 128) bf16 -> q_codes (T, 64, 128) uint8 e4m3
+ *   and q_scale (T, 64) fp32 with the quantize-on-store rule per (row, head):
+ *   scale = amax / 448 in fp32 (1 for an all-zero head), code = E4M3(x /
+ *   scale), round to nearest even, saturating at 448.
+ * dsa_index_scores_fp8q / dsa_index_topk_fp8q: as dsa_index_scores /
+ *   dsa_index_topk with (q_codes, q_scale) in place of q (q_scale may have
+ *   any sign; the quantiser writes scales >= 0).
+ * Device pointers, caller-owned.  DSA_ERR_UNSUPPORTED for other index formats
+ * or shapes, a page size that is not a multiple of 8, or spans whose
+ * page_start leaves fewer than 8 rows of a page contiguous (the host planner's
+ * key-box height); DSA_ERR_INVALID_ARG for null pointers. */
+dsa_status dsa_quantize_q(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *q_bf16, void *q_codes, float *q_scale,
+                          dsa_stream_t stream);
+dsa_status dsa_index_scores_fp8q(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *q_codes, const float *q_scale,
+                                 const float *w, const void *index_cache, float *scores, dsa_stream_t stream);
+dsa_status dsa_index_topk_fp8q(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *q_codes, const float *q_scale,
+                               const float *w, const void *index_cache, int32_t *selection, dsa_stream_t stream);
+
 /* ---- Capturable plans --------------------------------------------------
  * The pages' follow-up gives selection and attention fixed-shape buffers "so
  * a decode can capture" (mstar.engine.resources.dsa.manager, module

@@ -67,6 +67,10 @@ def lib():
                                                     ctypes.c_void_p]
         L.oracle_index_scores.argtypes = [ctypes.POINTER(_Rows), ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+        L.oracle_index_scores_fp8q.argtypes = [ctypes.POINTER(_Rows), ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                               ctypes.c_void_p, ctypes.c_void_p]
+        L.oracle_quantize_rows.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
         L.oracle_topk.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
         L.oracle_attend.argtypes = [ctypes.POINTER(_Rows), ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
@@ -194,6 +198,32 @@ def index_scores(shape, spans, num_pages, q, w, cache):
     _check(lib().oracle_index_scores(ctypes.byref(rt.struct), int(shape.index_heads), int(shape.index_dim),
                                      int(shape.index_fmt), qa.ctypes.data, wa.ctypes.data, ca.ctypes.data,
                                      off.ctypes.data, scores.ctypes.data))
+    return scores, off
+
+
+def quantize_rows(x_bf16, width: int):
+    """bf16 values, rows of `width` -> (e4m3 codes uint8, one fp32 scale per row)
+    by the quantize-on-store rule (fp8 query)."""
+    a = _np(x_bf16).view(np.uint16).reshape(-1)
+    n = a.size // width
+    codes = np.empty(n * width, np.uint8)
+    scales = np.empty(n, np.float32)
+    _check(lib().oracle_quantize_rows(n, int(width), a.ctypes.data, codes.ctypes.data, scales.ctypes.data))
+    return codes, scales
+
+
+def index_scores_fp8q(shape, spans, num_pages, q_codes, q_scale, w, cache):
+    """Indexer scores with an fp8 query: q = e4m3(q_codes) * q_scale per (row, head)."""
+    rt = RowTable(spans, shape.page_size, num_pages)
+    qc = _np(q_codes).view(np.uint8)
+    qs = _np(q_scale, np.float32)
+    wa = _np(w, np.float32)
+    ca = _np(cache).view(np.uint8)
+    off = rt.score_offsets()
+    scores = np.zeros(int(off[-1]), np.float32)
+    _check(lib().oracle_index_scores_fp8q(ctypes.byref(rt.struct), int(shape.index_heads), int(shape.index_dim),
+                                          int(shape.index_fmt), qc.ctypes.data, qs.ctypes.data, wa.ctypes.data,
+                                          ca.ctypes.data, off.ctypes.data, scores.ctypes.data))
     return scores, off
 
 

@@ -233,11 +233,13 @@ static int load_index_key(const oracle_rows *R, int64_t r, int64_t j, int index_
 /* indexer score                                                             */
 /* ------------------------------------------------------------------------ */
 
-/* q: [T][index_heads][index_dim] bf16, w: [T][index_heads] fp32.
+/* q: [T][index_heads][index_dim] bf16 (q_codes == NULL), or e4m3 codes
+ * q_codes [T][index_heads][index_dim] with one fp32 scale per (row, head)
+ * q_scale [T][index_heads]: q = e4m3(code) * scale.  w: [T][index_heads] fp32.
  * scores: row r's pos(r)+1 scores start at score_off[r]. */
-int oracle_index_scores(const oracle_rows *R, int index_heads, int index_dim, int index_fmt,
-                        const uint16_t *q, const float *w, const uint8_t *cache,
-                        const int64_t *score_off, float *scores) {
+static int index_scores(const oracle_rows *R, int index_heads, int index_dim, int index_fmt,
+                        const uint16_t *q, const uint8_t *q_codes, const float *q_scale, const float *w,
+                        const uint8_t *cache, const int64_t *score_off, float *scores) {
   int status = OR_OK;
 #pragma omp parallel
   {
@@ -246,8 +248,11 @@ int oracle_index_scores(const oracle_rows *R, int index_heads, int index_dim, in
 #pragma omp for schedule(dynamic, 1)
     for (int64_t r = 0; r < R->T; r++) {
       if (!k || !qd) { status = OR_NOMEM; continue; }
-      for (int64_t i = 0; i < (int64_t)index_heads * index_dim; i++)
-        qd[i] = bf16_value(q[r * index_heads * index_dim + i]);
+      for (int64_t i = 0; i < (int64_t)index_heads * index_dim; i++) {
+        const int64_t at = r * index_heads * index_dim + i;
+        qd[i] = q_codes ? oracle_e4m3_value(q_codes[at]) * (double)q_scale[r * index_heads + i / index_dim]
+                        : bf16_value(q[at]);
+      }
       for (int64_t j = 0; j <= R->pos[r]; j++) {
         int e = load_index_key(R, r, j, index_fmt, index_dim, cache, k);
         if (e != OR_OK) { status = e; break; }
@@ -265,6 +270,26 @@ int oracle_index_scores(const oracle_rows *R, int index_heads, int index_dim, in
     free(qd);
   }
   return status;
+}
+
+int oracle_index_scores(const oracle_rows *R, int index_heads, int index_dim, int index_fmt,
+                        const uint16_t *q, const float *w, const uint8_t *cache,
+                        const int64_t *score_off, float *scores) {
+  return index_scores(R, index_heads, index_dim, index_fmt, q, NULL, NULL, w, cache, score_off, scores);
+}
+
+/* The same score with an fp8 query (e4m3 codes x one fp32 scale per head). */
+int oracle_index_scores_fp8q(const oracle_rows *R, int index_heads, int index_dim, int index_fmt,
+                             const uint8_t *q_codes, const float *q_scale, const float *w, const uint8_t *cache,
+                             const int64_t *score_off, float *scores) {
+  return index_scores(R, index_heads, index_dim, index_fmt, NULL, q_codes, q_scale, w, cache, score_off, scores);
+}
+
+/* n_rows rows of `width` bf16 -> e4m3 codes and one scale per row, by the
+ * quantize-on-store rule (fp8 query). */
+int oracle_quantize_rows(int64_t n_rows, int width, const uint16_t *src, uint8_t *codes, float *scales) {
+  for (int64_t r = 0; r < n_rows; r++) scales[r] = quantize_group(src + r * width, width, codes + r * width);
+  return OR_OK;
 }
 
 /* ------------------------------------------------------------------------ */

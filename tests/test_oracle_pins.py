@@ -455,3 +455,71 @@ def test_format_sizes_match_pages():
     assert f8.latent_row_bytes == facts["mla_latent_fp8_packed"]
     assert f8.index_row_bytes == facts["dsa_index_fp8"]
     assert facts["selected_tokens"] == bf.topk
+
+
+# ---------------------------------------------------------------- fp8 query
+def _fp8_index_case(seed, index_heads=2, index_dim=8):
+    """A tiny fp8-index case: two requests, random non-NaN key codes, signed scales."""
+    sh = tiny_shape(index_heads=index_heads, index_dim=index_dim, page_size=4, index_fmt=W.INDEX_FP8_132)
+    case = make_case(sh, [(0, 6), (3, 2)])
+    rng = np.random.default_rng(seed)
+    P, D = sh.page_size, index_dim
+    npg = case.num_pages
+    cache = np.zeros(npg * P * (D + 4), np.uint8)
+    for pg in range(npg):
+        base = pg * P * (D + 4)
+        codes = rng.integers(0, 0x7F, size=P * D).astype(np.uint8) | (rng.integers(0, 2, size=P * D) << 7).astype(np.uint8)
+        cache[base:base + P * D] = codes
+        cache[base + P * D:base + P * (D + 4)] = (rng.choice([0.25, 0.5, -1.0, 2.0], size=P).astype(np.float32)).view(np.uint8)
+    T = sum(s.q_len for s in case.spans)
+    w = rng.uniform(0, 1, size=(T, index_heads)).astype(np.float32)
+    return sh, case, cache, w, rng
+
+
+def test_fp8_query_equals_the_bf16_query_it_decodes_to():
+    """q = e4m3(code) * 2^k is exact in bf16, so the fp8-query score must equal the
+    bf16-query score of the decoded values bit for bit (same fp64 products)."""
+    sh, case, cache, w, rng = _fp8_index_case(31)
+    T, Hi, D = w.shape[0], sh.index_heads, sh.index_dim
+    codes = (rng.integers(0, 0x77, size=(T, Hi, D)).astype(np.uint8) | (rng.integers(0, 2, size=(T, Hi, D)) << 7)).astype(np.uint8)
+    scales = rng.choice([0.125, 0.5, 1.0, 4.0], size=(T, Hi)).astype(np.float32)
+    qv = oracle.e4m3_values(codes.reshape(-1)).reshape(T, Hi, D) * scales[:, :, None]
+    q_bf16 = bf16(qv.astype(np.float32))
+    assert np.array_equal(q_bf16.float().numpy(), qv.astype(np.float32))   # exact in bf16
+    s_ref, off = oracle.index_scores(sh, case.spans, case.num_pages, q_bf16, w, cache)
+    s_f8, off2 = oracle.index_scores_fp8q(sh, case.spans, case.num_pages, codes, scales, w, cache)
+    assert np.array_equal(off, off2)
+    assert np.array_equal(s_f8, s_ref)
+    assert np.any(s_ref > 0) and np.any(s_ref == 0)   # both sides of the relu are exercised
+
+
+def test_fp8_query_scale_sign_and_size():
+    """A negative query scale is the sign-flipped code (relu sees -q); a power-of-two
+    scale multiplies every score by itself (relu is positively homogeneous)."""
+    sh, case, cache, w, rng = _fp8_index_case(32)
+    T, Hi, D = w.shape[0], sh.index_heads, sh.index_dim
+    codes = rng.integers(0, 0x77, size=(T, Hi, D)).astype(np.uint8)
+    ones = np.ones((T, Hi), np.float32)
+    s1, _ = oracle.index_scores_fp8q(sh, case.spans, case.num_pages, codes, ones, w, cache)
+    s4, _ = oracle.index_scores_fp8q(sh, case.spans, case.num_pages, codes, 4 * ones, w, cache)
+    assert np.array_equal(s4, 4 * s1)
+    sneg, _ = oracle.index_scores_fp8q(sh, case.spans, case.num_pages, codes, -ones, w, cache)
+    sflip, _ = oracle.index_scores_fp8q(sh, case.spans, case.num_pages, codes ^ 0x80, ones, w, cache)
+    assert np.array_equal(sneg, sflip)
+    assert not np.array_equal(sneg, s1)
+
+
+def test_quantize_rows_recovers_representable_rows():
+    """Rows made of E4M3 values times 2^k whose largest magnitude is 448 * 2^k come
+    back as the same codes with scale 2^k; an all-zero row gets scale 1."""
+    rng = np.random.default_rng(33)
+    codes = rng.integers(0, 0x7E, size=(5, 128)).astype(np.uint8) | (rng.integers(0, 2, size=(5, 128)) << 7).astype(np.uint8)
+    codes[:, 17] = 0x7E                                   # +448 in every row
+    k = np.array([-3, 0, 2, 5, -1])
+    vals = oracle.e4m3_values(codes.reshape(-1)).reshape(5, 128) * np.ldexp(1.0, k)[:, None]
+    vals[4] = 0.0
+    got_codes, got_scales = oracle.quantize_rows(bf16(vals.astype(np.float32)), 128)
+    got_codes = got_codes.reshape(5, 128)
+    assert np.array_equal(got_scales[:4], np.ldexp(1.0, k[:4]).astype(np.float32))
+    assert np.array_equal(got_codes[:4], codes[:4])
+    assert got_scales[4] == 1.0 and not np.any(got_codes[4] & 0x7F)
