@@ -736,11 +736,12 @@ __global__ void __launch_bounds__(kFp8Threads, 1) index_fp8_tc_kernel(const __gr
       }
       bool ok = true;
       for (int t = item.tile0; t < item.tile1; ++t) {
-        if (!mbar_wait(afull(acc), aphase, abort_flag, p.err)) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, mbar_wait(afull(acc), aphase, abort_flag, p.err))) { ok = false; break; }
         tc_fence_after();
         const float scale = scr[sc * 128 + m];
         const float mag = fabsf(scale);
         const bool neg = scale < 0.f;
+        const bool all_pos = __all_sync(0xffffffffu, !neg);
         const int key = t * 128 + m;
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * C::N;
 #pragma unroll
@@ -751,7 +752,10 @@ __global__ void __launch_bounds__(kFp8Threads, 1) index_fp8_tc_kernel(const __gr
             for (int h0 = 0; h0 < HI; h0 += 16)
               tmem_ld16(tbase + gg * HI + h0, *reinterpret_cast<float(*)[16]>(v + h0));
             tmem_ld_wait();
-            const float s = weighted_relu_sum<HI>(wsm + gg * HI, v, neg ? -1.f : 1.f);
+            // (the quantiser's scales are >= 0: a warp with no negative scale
+            // takes the relu without the sign multiply)
+            const float s = all_pos ? weighted_relu_sum<HI>(wsm + gg * HI, v, 1.f)
+                                    : weighted_relu_sum<HI>(wsm + gg * HI, v, neg ? -1.f : 1.f);
             if (key <= pos0 + gg) p.scores[soff[gg] + key] = s * mag;
           }
         }

@@ -27,8 +27,6 @@
 namespace dsa {
 namespace {
 
-constexpr int kF8qEpiWarps = 4;
-constexpr int kF8qThreads = 64 + 32 * kF8qEpiWarps;
 
 __device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                           uint32_t accumulate) {
@@ -44,6 +42,12 @@ template <int G>
 struct F8qTraits {
   static constexpr int HI = 64, DI = 128;
   static constexpr int N = G * HI;
+  // epilogue warps: two per TMEM lane quadrant for row groups, each taking
+  // half of the group's rows (the MMAs of a group tile are half the
+  // epilogue's work); one per quadrant for single rows
+  static constexpr int EPI = (G == 4) ? 8 : 4;
+  static constexpr int THREADS = 64 + 32 * EPI;
+  static constexpr int RPH = G / (EPI / 4);              // rows per epilogue warp
   static constexpr int CODE_BYTES = 128 * 128;           // one tile of key codes, 128-byte swizzle
   // staged scales: a TMA destination must be 128-byte aligned, so box b of a
   // tile lands at b * max(128, 4 * BH) bytes (up to 16 boxes of 8 keys)
@@ -83,7 +87,7 @@ struct F8qParams {
 };
 
 template <int G>
-__global__ void __launch_bounds__(kF8qThreads, 1) index_f8q_kernel(const __grid_constant__ F8qParams p) {
+__global__ void __launch_bounds__(F8qTraits<G>::THREADS, 1) index_f8q_kernel(const __grid_constant__ F8qParams p) {
   using C = F8qTraits<G>;
   constexpr int HI = C::HI;
   extern __shared__ uint8_t smem_raw[];
@@ -109,7 +113,7 @@ __global__ void __launch_bounds__(kF8qThreads, 1) index_f8q_kernel(const __grid_
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(sfull(s), 1);
-      mbar_init(sempty(s), 1 + 32 * kF8qEpiWarps);   // the MMA commit and every epilogue thread
+      mbar_init(sempty(s), 1 + C::EPI);   // the MMA commit and one lane of each epilogue warp
     }
     for (int b = 0; b < C::QBUF; ++b) {
       mbar_init(qfull(b), 1);
@@ -117,7 +121,7 @@ __global__ void __launch_bounds__(kF8qThreads, 1) index_f8q_kernel(const __grid_
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(afull(b), 1);
-      mbar_init(aempty(b), 32 * kF8qEpiWarps);
+      mbar_init(aempty(b), C::EPI);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -255,12 +259,14 @@ __global__ void __launch_bounds__(kF8qThreads, 1) index_f8q_kernel(const __grid_
     // ------------------------------------------------------------ epilogue
     const int et = threadIdx.x - 64;
     const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;            // which of the group's rows this warp takes
     const int m = quad * 32 + lane;
     int acc = 0, st = 0;
     uint32_t aphase = 0, ph = 0;
     int cur_group = -1;
     int64_t soff[G];
     int nrows = 0, pos0 = 0;
+    bool signed_q = false;   // some head of the group has a negative query scale
     for (int it = it0; it < it1 && !*abort_flag; ++it) {
       const IdxItem item = p.items[it];
       if (item.group != cur_group) {
@@ -268,8 +274,9 @@ __global__ void __launch_bounds__(kF8qThreads, 1) index_f8q_kernel(const __grid_
         const IdxGroup g = p.groups[item.group];
         nrows = g.nrows;
         pos0 = g.pos0;
-        named_bar_sync(1, 32 * kF8qEpiWarps);
-        for (int i = et; i < G * HI; i += 32 * kF8qEpiWarps) {
+        named_bar_sync(1, 32 * C::EPI);
+        bool neg = false;
+        for (int i = et; i < G * HI; i += 32 * C::EPI) {
           float wv = 0.f, qs = 0.f;
           if (i < nrows * HI) {
             wv = p.w[static_cast<int64_t>(g.row0) * HI + i];
@@ -277,31 +284,37 @@ __global__ void __launch_bounds__(kF8qThreads, 1) index_f8q_kernel(const __grid_
           }
           wsm[i] = wv * fabsf(qs);
           ssm[i] = qs < 0.f ? -1.f : 1.f;
+          neg = neg || qs < 0.f;
         }
 #pragma unroll
         for (int gg = 0; gg < G; ++gg) soff[gg] = gg < nrows ? p.row_score_off[g.row0 + gg] : 0;
-        named_bar_sync(1, 32 * kF8qEpiWarps);
+        signed_q = named_bar_any(1, 32 * C::EPI, neg);   // also the barrier after the writes
       }
       bool ok = true;
       for (int t = item.tile0; t < item.tile1; ++t) {
-        if (!mbar_wait(afull(acc), aphase, abort_flag, p.err)) { ok = false; break; }
+        // waits are made warp-uniform: each warp arrives once, by lane 0
+        if (!__all_sync(0xffffffffu, mbar_wait(afull(acc), aphase, abort_flag, p.err))) { ok = false; break; }
         tc_fence_after();
         // the key scales of this tile's stage (the stage filled phase `ph`;
-        // it is not refilled before this thread's release below)
-        if (!mbar_wait(sfull(st), ph, abort_flag, p.err)) { ok = false; break; }
+        // it is not refilled before this warp releases it below)
+        if (!__all_sync(0xffffffffu, mbar_wait(sfull(st), ph, abort_flag, p.err))) { ok = false; break; }
         const float ks = reinterpret_cast<const float *>(smem + C::OFF_ST + st * C::STAGE + C::CODE_BYTES)
             [(m / p.BH) * sc_stride + m % p.BH];
-        mbar_arrive(sempty(st));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sempty(st));
         if (++st == C::STAGES) {
           st = 0;
           ph ^= 1;
         }
         const float mag = fabsf(ks);
         const float ksign = ks < 0.f ? -1.f : 1.f;
+        // the quantiser's scales are >= 0: then relu needs no sign at all
+        const bool unsigned_tile = __all_sync(0xffffffffu, ks >= 0.f) && !signed_q;
         const int key = t * 128 + m;
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * C::N;
 #pragma unroll
-        for (int gg = 0; gg < G; ++gg) {
+        for (int j = 0; j < C::RPH; ++j) {
+          const int gg = half * C::RPH + j;
           if (gg < nrows) {
             float v[HI];
 #pragma unroll
@@ -309,21 +322,42 @@ __global__ void __launch_bounds__(kF8qThreads, 1) index_f8q_kernel(const __grid_
               tmem_ld16(tbase + gg * HI + h0, *reinterpret_cast<float(*)[16]>(v + h0));
             tmem_ld_wait();
             const float4 *w4 = reinterpret_cast<const float4 *>(wsm + gg * HI);
-            const float4 *s4 = reinterpret_cast<const float4 *>(ssm + gg * HI);
             float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+            if (unsigned_tile) {
 #pragma unroll
-            for (int h = 0; h < HI; h += 4) {
-              const float4 ww = w4[h / 4], sg = s4[h / 4];
-              a0 = fmaf(ww.x, fmaxf(ksign * sg.x * v[h], 0.f), a0);
-              a1 = fmaf(ww.y, fmaxf(ksign * sg.y * v[h + 1], 0.f), a1);
-              a2 = fmaf(ww.z, fmaxf(ksign * sg.z * v[h + 2], 0.f), a2);
-              a3 = fmaf(ww.w, fmaxf(ksign * sg.w * v[h + 3], 0.f), a3);
+              for (int h = 0; h < HI; h += 4) {
+                const float4 ww = w4[h / 4];
+                a0 = fmaf(ww.x, fmaxf(v[h], 0.f), a0);
+                a1 = fmaf(ww.y, fmaxf(v[h + 1], 0.f), a1);
+                a2 = fmaf(ww.z, fmaxf(v[h + 2], 0.f), a2);
+                a3 = fmaf(ww.w, fmaxf(v[h + 3], 0.f), a3);
+              }
+            } else if (!signed_q) {   // one sign per key
+#pragma unroll
+              for (int h = 0; h < HI; h += 4) {
+                const float4 ww = w4[h / 4];
+                a0 = fmaf(ww.x, fmaxf(ksign * v[h], 0.f), a0);
+                a1 = fmaf(ww.y, fmaxf(ksign * v[h + 1], 0.f), a1);
+                a2 = fmaf(ww.z, fmaxf(ksign * v[h + 2], 0.f), a2);
+                a3 = fmaf(ww.w, fmaxf(ksign * v[h + 3], 0.f), a3);
+              }
+            } else {
+              const float4 *s4 = reinterpret_cast<const float4 *>(ssm + gg * HI);
+#pragma unroll
+              for (int h = 0; h < HI; h += 4) {
+                const float4 ww = w4[h / 4], sg = s4[h / 4];
+                a0 = fmaf(ww.x, fmaxf(ksign * sg.x * v[h], 0.f), a0);
+                a1 = fmaf(ww.y, fmaxf(ksign * sg.y * v[h + 1], 0.f), a1);
+                a2 = fmaf(ww.z, fmaxf(ksign * sg.z * v[h + 2], 0.f), a2);
+                a3 = fmaf(ww.w, fmaxf(ksign * sg.w * v[h + 3], 0.f), a3);
+              }
             }
             if (key <= pos0 + gg) p.scores[soff[gg] + key] = ((a0 + a1) + (a2 + a3)) * mag;
           }
         }
         tc_fence_before();
-        mbar_arrive(aempty(acc));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(aempty(acc));
         acc ^= 1;
         if (acc == 0) aphase ^= 1;
       }
@@ -378,7 +412,7 @@ cudaError_t run_f8q(const dsa_ctx *ctx, const dsa_plan_t *plan, const IdxSet &se
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kern<<<set.n_ctas, kF8qThreads, C::SMEM, s>>>(prm);
+  kern<<<set.n_ctas, C::THREADS, C::SMEM, s>>>(prm);
   return cudaGetLastError();
 }
 
