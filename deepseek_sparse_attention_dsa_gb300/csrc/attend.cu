@@ -24,16 +24,18 @@
 //     memory).  A K = 16 tcgen05.mma costs about the same for N = 32 as for
 //     N = 64 on sm_103a, so splitting the contraction between the pair halves
 //     the instruction count per key where duplicating it would double it;
-//   * 4 softmax warps (thread = head) swap the partial logits with the partner
-//     through distributed shared memory (st.async landing on the partner's
-//     mbarrier, double-buffered), so both CTAs hold the identical full S and
-//     run the same base-2 online softmax (the reference max moves only when
-//     it grows by more than 2^8, so O is rarely rescaled); P goes to TMEM as
-//     bf16 over the S tile it came from;
+//   * 4 sender warps (thread = head) take each S tile out of TMEM as soon as
+//     its QK is done, stage it in shared memory and bulk-copy it into the
+//     partner's receive buffer (the copy lands on the partner's mbarrier);
+//   * 4 softmax warps (thread = head) add the partner's partial to their own
+//     (a + b == b + a, so both CTAs hold the identical full S) and run the
+//     same base-2 online softmax (the reference max moves only when it grows
+//     by more than 2^8, so O is rarely rescaled); P goes to TMEM as bf16 in
+//     its own columns;
 //   * one thread issues O_c += P . C[:, cols_c] (A = P from TMEM, B = the
 //     gathered tile read MN-major; M = 128, N = L/2, fp32 in TMEM).
 // S is double-buffered in TMEM so QK of tile t+1 overlaps the softmax of tile
-// t.  Rows split over several key ranges write fp32 partials (O, max, sum)
+// t; an S tile is free once the softmax and sender warps have read it.  Rows split over several key ranges write fp32 partials (O, max, sum)
 // that attend_combine_kernel merges.
 //
 // Other shapes run attend_simt_kernel.
