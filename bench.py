@@ -439,6 +439,19 @@ def capture_decode_step(ctx, wl, ic, lc, st, sel, out, dev):
     return {"plan": plan, "graph": g, "replay": g.replay, "inputs": inputs, "spans": spans, "launches": launches[0]}
 
 
+def source_fingerprint(path):
+    """sha256 (16 hex digits) of a CUDA source with its // comments and blank
+    lines dropped: the code a profile was taken of, not its commentary."""
+    import hashlib
+    import re
+    lines = []
+    for ln in open(path, encoding="utf-8"):
+        code = re.sub(r"//.*$", "", ln.rstrip("\n")).rstrip()
+        if code:
+            lines.append(code)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
+
+
 def profile_traffic(kernel, workload):
     """dram bytes per launch from a committed ncu summary of this kernel and
     workload, if its source fingerprint matches the current source."""
@@ -449,8 +462,7 @@ def profile_traffic(kernel, workload):
     src = {"index_tc": "indexer.cu", "attend_tc": "attend.cu"}.get(kernel.split("_kernel")[0])
     fp = None
     if src:
-        with open(os.path.join(ROOT, "deepseek_sparse_attention_dsa_gb300", "csrc", src), "rb") as f:
-            fp = hashlib.sha256(f.read()).hexdigest()[:16]
+        fp = source_fingerprint(os.path.join(ROOT, "deepseek_sparse_attention_dsa_gb300", "csrc", src))
     traffic, sha = None, None
     for ln in open(path):
         if ln.startswith("traffic_bytes_per_launch:"):
