@@ -105,7 +105,11 @@ struct AttTraits {
   static_assert(QT_CH * 32 <= static_cast<int>(P_COL) && P_COL + TILE / 2 <= S_COL, "tensor memory: Q, P");
   static_assert(O_COL + HALF <= TMEM_COLS, "tensor memory: O");
   static_assert(QRBYTES <= OFF_K && STAGE % 1024 == 0, "alignment");
-  static_assert(QT_CH * QCHUNK <= STAGES * STAGE, "Q staging");
+  // the q_nope chunks bound for TMEM are staged in the stage buffers from
+  // QT_STAGE on, so the first tiles' gathers need not wait for the move
+  static constexpr int QT_STAGE = 2;
+  static constexpr int OFF_QT = OFF_K + QT_STAGE * STAGE;
+  static_assert(STAGES > QT_STAGE && QT_CH * QCHUNK <= (STAGES - QT_STAGE) * STAGE, "Q staging");
   static_assert(NBAR >= 16 + 2 * STAGES, "barriers");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
@@ -252,7 +256,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
                     static_cast<int>(crank) * C::HALF + ch * 64, row * p.H, b_qsfull);
       mbar_arrive_expect_tx(b_qtfull, C::QT_CH * C::QCHUNK);
       for (int ch = 0; ch < C::QT_CH; ++ch)
-        tma_load_2d(sbase + C::OFF_K + ch * C::QCHUNK, &p.tm_qn, static_cast<int>(crank) * C::HALF + ch * 64,
+        tma_load_2d(sbase + C::OFF_QT + ch * C::QCHUNK, &p.tm_qn, static_cast<int>(crank) * C::HALF + ch * 64,
                     row * p.H, b_qtfull);
       bool ok = mbar_wait(b_qsfull, 0, abort_flag, p.err) && mbar_wait(b_qtdone, 0, abort_flag, p.err);
       const uint32_t o_tmem = tmem_base + C::O_COL;
@@ -360,14 +364,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
     };
     int j0 = sel_at(0), j1 = sel_at(1);
     int pg0 = page_of(j0);
-    // the stage buffers hold the q_nope columns of Q until they have been moved
+    // Stage buffers QT_STAGE.. hold the q_nope columns of Q until the softmax
+    // warps have moved them into TMEM; the tiles before gather at once.
     // Every exit from the tile loop is decided at the named barrier (an OR
     // over the producers), so no producer is left waiting there alone.
-    bool ok = mbar_wait(b_qtdone, 0, abort_flag, p.err);
+    bool ok = true;
     for (int t = 0; t < ntiles; ++t) {
       const int st = t % NS;
       const int pg1 = page_of(j1);
       const int j2 = sel_at(t + 2);
+      if (t == C::QT_STAGE && ok) ok = mbar_wait(b_qtdone, 0, abort_flag, p.err);
       if (!FP8 && ok) ok = mbar_wait(kempty(st), ((t / NS) & 1) ^ 1, abort_flag, p.err);
       int32_t *rows = rows_sm + st * T;
       if (resolver && ok) rows[rkey] = phys(j0, pg0);
@@ -512,7 +518,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
       // chunks into TMEM (bf16 pairs, lower column in the low half)
 #pragma unroll 1
       for (int ch = 0; ch < C::QT_CH; ++ch) {
-        const uint8_t *src = smem + C::OFF_K + ch * C::QCHUNK + h * 128;
+        const uint8_t *src = smem + C::OFF_QT + ch * C::QCHUNK + h * 128;
         uint32_t v[32];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
