@@ -10,6 +10,16 @@ loudly when the library has not been built: there is no CPU path.
     out = ctx.attend(plan, sel, q_nope, q_pe, latent_cache, sink, sm_scale)   # dsa_attend
     ctx.get_error()                                # dsa_get_error (synchronises)
 
+A decode step that re-plans on the device (capturable in a CUDA graph):
+
+    plan = ctx.plan_capturable(max_rows, max_spans, max_scores, cache_pages)
+    ctx.plan_update(plan, num_spans, spans, pages)  # device tensors, no sync
+    ... then store_keys / index_topk / attend with max_rows-row buffers
+
+fp8 query for the indexer (fp8 index cache): quantize_q, index_scores_fp8q,
+index_topk_fp8q.  Quantize-on-store: quantize_store_keys / _latents.  SHARED
+layers: attend_shared.
+
 Tensors are torch tensors on the context's device, contiguous, in the dtypes
 the header states; the calls run on torch's current CUDA stream unless a
 stream is given.
