@@ -20,6 +20,8 @@ copies of the step's inputs, the step, and a device-to-host copy of its output;
 for decode workloads the step is instead one CUDA graph over a capturable plan
 (dsa_plan_update re-plans on the device from spans and a page table copied up
 with the inputs), which is also timed device-resident as `captured_step`.
+The end-to-end loop keeps two buffer sets with the copies on their own
+streams, so each step's transfers overlap the neighbouring steps' kernels.
 `--impl reference` times the CPU oracle (the only reference this method has)
 on a bounded sample of the same workload on the host cores.
 Multi-GPU (torchrun): independent replicas, one per rank (weak scaling).
