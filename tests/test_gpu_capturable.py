@@ -222,3 +222,28 @@ def test_invalid_spans_empty_the_plan_and_are_reported(bad):
     ctx.get_error()
     assert bool((sel == SENTINEL).all()) and bool((out == 3.0).all())
     assert torch.equal(icd.cpu(), ic)   # an emptied plan stores nothing
+
+
+def test_fp8_caches_sink_and_shared_layer_match_the_host_plan():
+    """fp8 index / latent caches, an attention sink, split rows, and a SHARED
+    layer attending over the selection the capturable plan's FULL layer wrote."""
+    wl = H.deepseek_small(seed=26, fp8=True, sink=True, decode_ctx=(2500, 5000, 700), chunk=None)
+    ic, lc, st = H.host_inputs(wl)
+    ctx = dsa.Context(wl.shape, 0)
+    sel_h, out_h, ic_h = _host_path(ctx, wl, ic, lc, st)
+    R, T = 4, wl.num_rows
+    plan = ctx.plan_capturable(R, 4, R * 6000, wl.num_pages)
+    ns, spans, pages = _device_spans(wl, 4)
+    ctx.plan_update(plan, ns, spans, pages)
+    icd, lcd = ic.clone().cuda(), lc.cuda()
+    ctx.store_keys(plan, _padded(st.keys, R), icd)
+    sel = ctx.index_topk(plan, _padded(st.q, R), _padded(st.w, R), icd)
+    out = ctx.attend(plan, sel, _padded(st.q_nope, R), _padded(st.q_pe, R), lcd, st.sink.cuda(), wl.shape.sm_scale)
+    shared = ctx.attend_shared(plan, _padded(st.q_nope, R), _padded(st.q_pe, R), lcd, st.sink.cuda(),
+                               wl.shape.sm_scale)
+    ctx.get_error()
+    assert torch.equal(icd.cpu(), ic_h)
+    assert torch.equal(sel[:T].cpu(), sel_h)
+    assert torch.equal(out[:T].cpu(), out_h)
+    assert torch.equal(shared[:T].cpu(), out_h)   # same queries, same recorded selection
+    assert plan.read_counts()["split_rows"] > 0
