@@ -34,6 +34,25 @@ def _sample_rows(wl, n_decode, n_prefill, seed):
     return rows
 
 
+def _captured(ctx, wl, ic, lc, st):
+    """The bench's captured decode step: a capturable plan updated on the
+    device from the spans, then store / index_topk / attend over it."""
+    rows, pages, o = [], [], 0
+    for s in wl.spans:
+        rows.append([s.q_len, s.ctx_start, s.page_start, o, len(s.pages), 0])
+        pages.append(np.asarray(s.pages, np.int32))
+        o += len(s.pages)
+    max_scores = sum((s.ctx_start + 1 + s.ctx_end) * s.q_len // 2 for s in wl.spans)
+    plan = ctx.plan_capturable(wl.num_rows, len(rows), max_scores, wl.num_pages, page_start_align=wl.shape.page_size)
+    ctx.plan_update(plan, torch.tensor([len(rows)], dtype=torch.int32, device="cuda"),
+                    torch.tensor(rows, dtype=torch.int32, device="cuda"),
+                    torch.from_numpy(np.concatenate(pages)).cuda())
+    ctx.store_keys(plan, st.keys, ic)
+    sel = ctx.index_topk(plan, st.q, st.w, ic)
+    out = ctx.attend(plan, sel, st.q_nope, st.q_pe, lc, st.sink, wl.shape.sm_scale)
+    return sel, out
+
+
 def _check_workload(idx, n_decode, n_prefill):
     wl = W.config(idx)
     sh = wl.shape
@@ -52,6 +71,16 @@ def _check_workload(idx, n_decode, n_prefill):
     sel2 = ctx.index_topk(plan, st.q, st.w, ic)
     ctx.get_error()
     assert torch.equal(sel, sel2)
+    if all(s.q_len == 1 for s in wl.spans):
+        # decode steps: the captured path (device re-plan) gives the same bits
+        csel, cout = _captured(ctx, wl, ic, lc, st)
+        ctx.get_error()
+        assert torch.equal(csel, sel) and torch.equal(cout, out)
+    f8q = None
+    if sh.index_fmt == W.INDEX_FP8_132:
+        codes, qscale = ctx.quantize_q(plan, st.q)
+        f8q = (codes, qscale, ctx.index_topk_fp8q(plan, codes, qscale, st.w, ic))
+        ctx.get_error()
     _, pos_all, tok_all = wl.row_table()
     off_all = np.zeros(wl.num_rows + 1, np.int64)
     np.cumsum(pos_all + 1, out=off_all[1:])
@@ -73,6 +102,15 @@ def _check_workload(idx, n_decode, n_prefill):
         rlc = W.make_latent_cache(rw, tokens=set(toks.tolist()))
         ref = oracle.attend(sh, rw.spans, rw.num_pages, g_sel, rst.q_nope, rst.q_pe, rlc, rst.sink)
         H.check_attention(out[row:row + 1].float().cpu().numpy(), ref, fp8)
+        if f8q is not None:
+            # the fp8-query indexer on the same row: the GPU's codes are the
+            # oracle's quantisation of the row's query; scores and selection
+            rc, rs = oracle.quantize_rows(rst.q, 128)
+            assert np.array_equal(f8q[0][row].cpu().numpy().reshape(-1), rc)
+            assert np.array_equal(f8q[1][row].cpu().numpy().reshape(-1), rs)
+            fsc, foff = oracle.index_scores_fp8q(sh, rw.spans, rw.num_pages, rc, rs, rst.w, cache)
+            H.check_selection(f8q[2][row:row + 1].cpu().numpy(), oracle.topk(sh, rw.spans, fsc, foff), fsc, foff,
+                              sh.topk)
 
 
 def test_decode_full_size():
