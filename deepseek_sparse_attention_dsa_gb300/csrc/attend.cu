@@ -26,17 +26,22 @@
 //     the instruction count per key where duplicating it would double it;
 //   * 4 sender warps (thread = head) take each S tile out of TMEM as soon as
 //     its QK is done, stage it in shared memory and bulk-copy it into the
-//     partner's receive buffer (the copy lands on the partner's mbarrier);
-//   * 4 softmax warps (thread = head) add the partner's partial to their own
-//     (a + b == b + a, so both CTAs hold the identical full S) and run the
-//     same base-2 online softmax (the reference max moves only when it grows
-//     by more than 2^8, so O is rarely rescaled); P goes to TMEM as bf16 in
-//     its own columns;
+//     partner's receive buffer (the copy lands on the partner's mbarrier).
+//     The receive buffer is two halves of 32 keys with their own barriers,
+//     so the first half of tile t+1 travels while tile t's second half is
+//     being merged;
+//   * 8 softmax warps, two per TMEM lane quadrant (thread = head, 32 keys of
+//     the tile each), add the partner's partial to their own (a + b == b + a,
+//     so both CTAs hold the identical full S) and run the same base-2 online
+//     softmax (the pair shares each tile's max through shared memory; the
+//     reference max moves only when it grows by more than 2^8, so O is rarely
+//     rescaled); P goes to TMEM as bf16 in its own columns;
 //   * one thread issues O_c += P . C[:, cols_c] (A = P from TMEM, B = the
 //     gathered tile read MN-major; M = 128, N = L/2, fp32 in TMEM).
 // S is double-buffered in TMEM so QK of tile t+1 overlaps the softmax of tile
-// t; an S tile is free once the softmax and sender warps have read it.  Rows split over several key ranges write fp32 partials (O, max, sum)
-// that attend_combine_kernel merges.
+// t; an S tile is free once the softmax and sender warps have read it.  Rows
+// split over several key ranges write fp32 partials (O, max, sum) that
+// attend_combine_kernel merges.
 //
 // Other shapes run attend_simt_kernel.
 #include <cuda_fp16.h>
@@ -56,10 +61,10 @@ constexpr float kNegBig = -1.0e30f;
 // warp roles (16 warps; registers are handed out per group of four warps)
 constexpr int kMmaWarp = 0;
 constexpr int kProdWarp0 = 1;               // warps 1-7: producers (224 threads)
-constexpr int kSoftWarp0 = 8;               // warps 8-11: softmax, thread = head
-constexpr int kSendWarp0 = 12;              // warps 12-15: partial-logit senders, thread = head
+constexpr int kSoftWarp0 = 8;               // warps 8-15: softmax, thread = head; warps 8-11 keys 0-31, 12-15 keys 32-63
+constexpr int kSendWarp0 = 16;              // warps 16-19: partial-logit senders, thread = head
 constexpr int kProdThreads = 224;
-constexpr int kAttThreads = 16 * 32;
+constexpr int kAttThreads = 20 * 32;
 
 template <int L>
 struct AttTraits {
@@ -76,9 +81,12 @@ struct AttTraits {
   static constexpr int QCHUNK = 128 * 128;               // [128 heads x 64 cols]
   static constexpr int QRBYTES = 128 * 64;               // [128 heads x 32 rope cols]
   static constexpr int XBYTES = 128 * TILE * 4;          // partial logits of a tile, fp32
-  static constexpr int XBUF = 1;                         // receive buffers for the partner's partial logits
-  static constexpr int XOUT = XBYTES / 2;                // send staging: 16 rows (4 KB) per sender warp at a time
-  static_assert(XOUT / 4 == 16 * 256, "send staging slot");
+  // The receive buffer x_in is two halves, one per 32 keys of the tile, each
+  // with its own full/free barriers: the partner sends the first half of tile
+  // t+1 as soon as the first half of tile t has been merged.
+  static constexpr int XHALF = XBYTES / 2;               // [128 heads x 32 keys] fp32, 128-byte rows
+  static constexpr int XOUT = XHALF;                     // send staging: one half-row block (4 KB) per sender warp
+  static_assert(XOUT / 4 == 32 * 128 && TILE == 64, "send staging slot");
   // q_nope chunks of this CTA: the first QT_CH in tensor memory (A operand),
   // the rest in shared memory
   static constexpr int QT_CH = NPV < 3 ? NPV : 3;
@@ -93,9 +101,10 @@ struct AttTraits {
   static constexpr int OFF_QR = 0;
   static constexpr int OFF_QS = 8192;                    // q_nope chunks in shared memory
   static constexpr int OFF_K = OFF_QS + QS_CH * QCHUNK;
-  static constexpr int OFF_X = OFF_K + STAGES * STAGE;   // x_in[XBUF] then x_out (XOUT bytes)
-  static constexpr int OFF_ROWS = OFF_X + XBUF * XBYTES + XOUT;   // int32 [STAGES][TILE]
-  static constexpr int OFF_BAR = OFF_ROWS + STAGES * TILE * 4;
+  static constexpr int OFF_X = OFF_K + STAGES * STAGE;   // x_in (two halves) then x_out (XOUT bytes)
+  static constexpr int OFF_ROWS = OFF_X + XBYTES + XOUT;   // int32 [STAGES][TILE]
+  static constexpr int OFF_RED = OFF_ROWS + STAGES * TILE * 4;   // fp32 [2 tiles][2 halves][128] maxima, [2][128] sums
+  static constexpr int OFF_BAR = OFF_RED + (4 + 2) * 128 * 4;
   static constexpr int NBAR = 24;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;
@@ -217,7 +226,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(b_qsfull, 1);
     mbar_init(b_qtfull, 1);
-    mbar_init(b_qtdone, 128);
+    mbar_init(b_qtdone, 8);   // softmax arrivals are one elected lane per warp (after __syncwarp)
     mbar_init(b_pvdone, 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(kfull(s), kProdThreads);
@@ -225,12 +234,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(sfull(b), 1);
-      mbar_init(sempty(b), 256);   // S tile b read by the 128 softmax and the 128 sender threads
-      mbar_init(pfull(b), 128);
+      mbar_init(sempty(b), 12);   // S tile b read by the 8 softmax and the 4 sender warps
+      mbar_init(pfull(b), 8);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(xfull(b), 1);   // armed locally with the tile's bytes, filled by the partner's bulk copy
-      mbar_init(xfree(b), 4);   // one arrival per partner softmax warp
+      mbar_init(xfree(b), 4);   // one arrival per partner softmax warp of half b
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -455,19 +464,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
     cp_async_wait<0>();   // nothing in flight when the CTA leaves
   } else if (warp >= kSendWarp0) {
     // ------------------------------------------------------------ senders
-    // Warp q (heads 32q..32q+31) copies its rows of this CTA's partial logits
-    // of every tile, as soon as its QK is done, into its x_out slot (16 rows
-    // at a time, row h's 16-byte chunks swizzled by h) and bulk-copies them
-    // into the partner's x_in[u % XBUF] once all four partner softmax warps have
-    // read tile u-2 from it (a bulk copy lands ~1 us sooner than the same
-    // bytes sent by st.async from registers).  The S tile is released (sempty)
-    // once its values are in registers.
+    // Warp q (heads 32q..32q+31) sends its rows of this CTA's partial logits
+    // of every tile, as soon as its QK is done, in two halves of 32 keys: a
+    // half is staged in the warp's 4 KB x_out slot (row h's 16-byte chunks
+    // swizzled by h) and bulk-copied into the same half of the partner's x_in
+    // once all four partner softmax warps have merged that half of tile u-1
+    // (a bulk copy lands ~1 us sooner than the same bytes sent by st.async
+    // from registers).  The S tile is released (sempty) once its values are
+    // in registers.
     const int quad = warp & 3;
     const int h = quad * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t slot = sbase + C::OFF_X + C::XBUF * C::XBYTES + quad * (C::XOUT / 4);
-    const uint32_t peer_x_in0 = map_to_cta(sbase + C::OFF_X, peer);
-    for (int u = 0; u < ntiles; ++u) {
+    const uint32_t slot = sbase + C::OFF_X + C::XBYTES + quad * (C::XOUT / 4);
+    const uint32_t dst0 = map_to_cta(sbase + C::OFF_X, peer) + static_cast<uint32_t>(quad * 32) * 128;
+    bool ok = true;
+    for (int u = 0; u < ntiles && ok; ++u) {
       const int b = u & 1;
       const uint32_t use = static_cast<uint32_t>(u >> 1);
       if (!mbar_wait(sfull(b), use & 1, abort_flag, p.err)) break;
@@ -478,46 +489,57 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
         tmem_ld16(tmem_base + lane_base + C::S_COL + b * T + c0, *reinterpret_cast<float(*)[16]>(v + c0));
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(sempty(b));
-      int sent_ok = 1;
-      const int xb = u % C::XBUF;
-      const uint32_t xuse = static_cast<uint32_t>(u / C::XBUF);
-      if (lane == 0) sent_ok = mbar_wait<true>(xfree(xb), (xuse & 1) ^ 1, abort_flag, p.err) ? 1 : 0;
-      if (__shfl_sync(0xffffffffu, sent_ok, 0) == 0) break;
-      const uint32_t dst = peer_x_in0 + xb * C::XBYTES + static_cast<uint32_t>(quad * 32) * 256;
-      const uint32_t bar = map_to_cta(xfull(xb), peer);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sempty(b));
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         if (lane == 0) bulk_wait_read_all();   // the slot's previous copy has been read
         __syncwarp();
-        if ((lane >> 4) == hh) {
-          const uint32_t r = slot + (lane & 15) * 256;
+        const uint32_t r = slot + lane * 128;
 #pragma unroll
-          for (int c = 0; c < T / 4; ++c)
-            st_shared_v4(r + ((c ^ (h & 15)) << 4),
-                         make_uint4(__float_as_uint(v[4 * c]), __float_as_uint(v[4 * c + 1]),
-                                    __float_as_uint(v[4 * c + 2]), __float_as_uint(v[4 * c + 3])));
-          fence_proxy_async_smem();
+        for (int c = 0; c < T / 8; ++c) {
+          const int k = hh * (T / 2) + 4 * c;
+          st_shared_v4(r + ((c ^ (h & 7)) << 4), make_uint4(__float_as_uint(v[k]), __float_as_uint(v[k + 1]),
+                                                           __float_as_uint(v[k + 2]), __float_as_uint(v[k + 3])));
         }
+        fence_proxy_async_smem();
         __syncwarp();
+        int sent_ok = 1;
         if (lane == 0) {
-          bulk_copy_to_cta(dst + hh * (C::XOUT / 4), slot, C::XOUT / 4, bar);   // 16 rows of 256 bytes
-          bulk_commit();
+          sent_ok = mbar_wait<true>(xfree(hh), (static_cast<uint32_t>(u) & 1) ^ 1, abort_flag, p.err) ? 1 : 0;
+          if (sent_ok) {
+            bulk_copy_to_cta(dst0 + hh * C::XHALF, slot, C::XOUT / 4, map_to_cta(xfull(hh), peer));   // 32 rows of 128 bytes
+            bulk_commit();
+          }
+        }
+        if (__shfl_sync(0xffffffffu, sent_ok, 0) == 0) {
+          ok = false;
+          break;
         }
       }
     }
     if (lane == 0) bulk_wait_read_all();   // x_out stays valid until every copy has read it
   } else {
     // ------------------------------------------------------------ softmax
+    // Two warps per TMEM lane quadrant: warp half hf takes keys 32hf..32hf+31
+    // of every tile (the half of x_in the partner sends for them) and output
+    // columns [hf, hf+1) * HALF/2.  The pair shares each tile's maximum
+    // through shared memory, so both take the same reference max, and adds
+    // its row sums at the end; every exit from the tile loop is decided at
+    // the pair's barrier (an OR of their failures).
     const int quad = warp & 3;
+    const int hf = (warp - kSoftWarp0) >> 2;
     const int h = quad * 32 + lane;                      // head = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    bool ok = mbar_wait(b_qtfull, 0, abort_flag, p.err);
+    const uint32_t pair_bar = 3 + quad;
+    float *red = reinterpret_cast<float *>(smem + C::OFF_RED);   // [t&1][hf][h] maxima, then [hf][h] sums
+    bool ok = __all_sync(0xffffffffu, mbar_wait(b_qtfull, 0, abort_flag, p.err));
     if (ok) {
       // this head's row of the q_nope columns: from the staged swizzled
-      // chunks into TMEM (bf16 pairs, lower column in the low half)
+      // chunks into TMEM (bf16 pairs, lower column in the low half); the
+      // pair's warps take alternate chunks
 #pragma unroll 1
-      for (int ch = 0; ch < C::QT_CH; ++ch) {
+      for (int ch = hf; ch < C::QT_CH; ch += 2) {
         const uint8_t *src = smem + C::OFF_QT + ch * C::QCHUNK + h * 128;
         uint32_t v[32];
 #pragma unroll
@@ -533,107 +555,122 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
       tmem_st_wait();
     }
     tc_fence_before();
-    mbar_arrive(b_qtdone);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(b_qtdone);
+    constexpr int TH = T / 2;                            // keys of a tile per warp
     float m_ref = kNegBig, l = 0.f;
-    int jn0 = lane < nent ? selrow[lane] : -1;
-    int jn1 = 32 + lane < nent ? selrow[32 + lane] : -1;
-    for (int t = 0; t < ntiles && ok; ++t) {
-      const uint32_t vlo = __ballot_sync(0xffffffffu, jn0 >= 0 && jn0 <= pos);
-      const uint32_t vhi = __ballot_sync(0xffffffffu, jn1 >= 0 && jn1 <= pos);
+    int jn = hf * TH + lane < nent ? selrow[hf * TH + lane] : -1;
+    for (int t = 0; t < ntiles; ++t) {
+      const uint32_t vmask = __ballot_sync(0xffffffffu, jn >= 0 && jn <= pos);
       if (t + 1 < ntiles) {
-        const int e = (t + 1) * T + lane;
-        jn0 = e < nent ? selrow[e] : -1;
-        jn1 = e + 32 < nent ? selrow[e + 32] : -1;
+        const int e = (t + 1) * T + hf * TH + lane;
+        jn = e < nent ? selrow[e] : -1;
       }
       const int sb = t & 1;
       const uint32_t use = static_cast<uint32_t>(t >> 1);
-      const int xb = t % C::XBUF;
-      if (h == 0) mbar_arrive_expect_tx(xfull(xb), C::XBYTES);
-      if (!mbar_wait(sfull(sb), use & 1, abort_flag, p.err)) { ok = false; break; }
+      if (h == 0) mbar_arrive_expect_tx(xfull(hf), C::XHALF);
+      bool good = ok && __all_sync(0xffffffffu, mbar_wait(sfull(sb), use & 1, abort_flag, p.err));
       tc_fence_after();
-      float s[T];
+      float s[TH];
+      if (good) {
 #pragma unroll
-      for (int c0 = 0; c0 < T; c0 += 16)
-        tmem_ld16(tmem_base + lane_base + C::S_COL + sb * T + c0, *reinterpret_cast<float(*)[16]>(s + c0));
-      tmem_ld_wait();
-      // full logits of tile t: our partial + the partner's (x_in[xb])
-      if (!mbar_wait<true>(xfull(xb), (t / C::XBUF) & 1, abort_flag, p.err)) { ok = false; break; }
-      {
-        const float4 *xr = reinterpret_cast<const float4 *>(smem + C::OFF_X + xb * C::XBYTES + h * 256);
+        for (int c0 = 0; c0 < TH; c0 += 16)
+          tmem_ld16(tmem_base + lane_base + C::S_COL + sb * T + hf * TH + c0,
+                    *reinterpret_cast<float(*)[16]>(s + c0));
+        tmem_ld_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (good && lane == 0) mbar_arrive(sempty(sb));   // our partial is in registers: the S tile can take QK of tile t+2
+      // full logits of this warp's keys: our partial + the partner's (x_in half hf)
+      good = good && __all_sync(0xffffffffu,
+                                mbar_wait<true>(xfull(hf), static_cast<uint32_t>(t) & 1, abort_flag, p.err));
+      float lmax = -INFINITY;
+      if (good) {
+        const float4 *xr = reinterpret_cast<const float4 *>(smem + C::OFF_X + hf * C::XHALF + h * 128);
 #pragma unroll
-        for (int c = 0; c < T / 4; ++c) {
-          const float4 v = xr[c ^ (h & 15)];
+        for (int c = 0; c < TH / 4; ++c) {
+          const float4 v = xr[c ^ (h & 7)];
           // a + b == b + a in IEEE arithmetic: both CTAs get the same S
           s[4 * c] += v.x;
           s[4 * c + 1] += v.y;
           s[4 * c + 2] += v.z;
           s[4 * c + 3] += v.w;
         }
-      }
-      __syncwarp();   // this warp's rows of x_in[xb] have been read
-      if (lane == 0) mbar_arrive_remote_relaxed(map_to_cta(xfree(xb), peer));
-      tc_fence_before();
-      mbar_arrive(sempty(sb));   // our partial is in registers: the S tile can take QK of tile t+2
-
-      // online softmax in base 2 with a lazily moved reference max
-      // (scale_log2 > 0, so the max of the raw logits picks the same key)
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        // (scale_log2 > 0, so the max of the raw logits picks the same key)
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int i = 0; i < T; ++i) {
-        const bool v = (((i < 32) ? (vlo >> i) : (vhi >> (i - 32))) & 1u) != 0;
-        s[i] = v ? s[i] : -INFINITY;
-        mx[i & 3] = fmaxf(mx[i & 3], s[i]);
+        for (int i = 0; i < TH; ++i) {
+          s[i] = ((vmask >> i) & 1u) ? s[i] : -INFINITY;
+          mx[i & 3] = fmaxf(mx[i & 3], s[i]);
+        }
+        lmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       }
-      const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.scale_log2;
+      // this warp's rows of its x_in half have been read (a release arrive
+      // here costs more than it saves)
+      __syncwarp();
+      if (good && lane == 0) mbar_arrive_remote_relaxed(map_to_cta(xfree(hf), peer));
+      red[(sb * 2 + hf) * 128 + h] = lmax;
+      if (named_bar_any(pair_bar, 64, !good)) {   // both halves' maxima are in place
+        ok = false;
+        break;
+      }
+      // online softmax in base 2 with a lazily moved reference max
+      const float tmax = fmaxf(red[(sb * 2) * 128 + h], red[(sb * 2 + 1) * 128 + h]) * p.scale_log2;
       float alpha = 1.f;
       const bool rescale = tmax > m_ref + kRescaleThreshold;
       if (rescale) {
         alpha = fast_exp2(m_ref - tmax);
         m_ref = tmax;
       }
+      // P (bf16 pairs, lower key in the low half) for this warp's keys
+      float sm[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t packed[TH / 2];
+#pragma unroll
+      for (int i = 0; i < TH; i += 2) {
+        const __nv_bfloat162 pb = __floats2bfloat162_rn(fast_exp2(fmaf(s[i], p.scale_log2, -m_ref)),
+                                                        fast_exp2(fmaf(s[i + 1], p.scale_log2, -m_ref)));
+        const float2 pf = __bfloat1622float2(pb);
+        sm[(i >> 1) & 3] += pf.x + pf.y;
+        packed[i / 2] = *reinterpret_cast<const uint32_t *>(&pb);
+      }
+      l = l * alpha + ((sm[0] + sm[1]) + (sm[2] + sm[3]));
       // PV of tile t-1 must be done before P is overwritten and before O is
-      // rescaled (PV of t-2 finished before PV of t-1 was issued)
+      // rescaled (PV of t-2 finished before PV of t-1 was issued); a failure
+      // here is seen at the next pair barrier
       if (t > 0) {
-        if (!mbar_wait(b_pvdone, (t - 1) & 1, abort_flag, p.err)) { ok = false; break; }
+        good = __all_sync(0xffffffffu, mbar_wait(b_pvdone, (t - 1) & 1, abort_flag, p.err));
         tc_fence_after();
       }
-      if (rescale && t > 0) {
+      if (good && rescale && t > 0) {
 #pragma unroll 1
-        for (int c0 = 0; c0 < C::HALF; c0 += 16) {
+        for (int c0 = 0; c0 < C::HALF / 2; c0 += 16) {
           float o[16];
-          tmem_ld16(tmem_base + lane_base + C::O_COL + c0, o);
+          tmem_ld16(tmem_base + lane_base + C::O_COL + hf * (C::HALF / 2) + c0, o);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 16; ++i) o[i] *= alpha;
-          tmem_st16(tmem_base + lane_base + C::O_COL + c0, o);
+          tmem_st16(tmem_base + lane_base + C::O_COL + hf * (C::HALF / 2) + c0, o);
         }
       }
-      // P (bf16 pairs, lower key in the low half) into its columns, in two halves
-      float sm[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int half2 = 0; half2 < 2; ++half2) {
-        uint32_t packed[T / 4];
-#pragma unroll
-        for (int i = 0; i < T / 2; i += 2) {
-          const int k = half2 * (T / 2) + i;
-          const __nv_bfloat162 pb = __floats2bfloat162_rn(fast_exp2(fmaf(s[k], p.scale_log2, -m_ref)),
-                                                          fast_exp2(fmaf(s[k + 1], p.scale_log2, -m_ref)));
-          const float2 pf = __bfloat1622float2(pb);
-          sm[(i >> 1) & 3] += pf.x + pf.y;
-          packed[i / 2] = *reinterpret_cast<const uint32_t *>(&pb);
-        }
-        tmem_st16(tmem_base + lane_base + C::P_COL + half2 * (T / 4),
-                  *reinterpret_cast<const float(*)[16]>(packed));
+      if (good) {
+        tmem_st16(tmem_base + lane_base + C::P_COL + hf * (TH / 2), *reinterpret_cast<const float(*)[16]>(packed));
+        tmem_st_wait();
       }
-      l = l * alpha + ((sm[0] + sm[1]) + (sm[2] + sm[3]));
-      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(pfull(sb));
+      __syncwarp();
+      if (good && lane == 0) mbar_arrive(pfull(sb));
+      ok = good;
     }
-    if (ok && ntiles > 0) ok = mbar_wait(b_pvdone, (ntiles - 1) & 1, abort_flag, p.err);
+    if (ok && ntiles > 0) ok = __all_sync(0xffffffffu, mbar_wait(b_pvdone, (ntiles - 1) & 1, abort_flag, p.err));
     tc_fence_after();
+    // the row sum is the two halves' sums (in a fixed order, the same in both CTAs)
+    red[(4 + hf) * 128 + h] = l;
+    named_bar_sync(pair_bar, 64);
+    l = red[4 * 128 + h] + red[5 * 128 + h];
     if (ok && h < p.H) {
-      const int col0 = static_cast<int>(crank) * C::HALF;
+      const int col0 = static_cast<int>(crank) * C::HALF + hf * (C::HALF / 2);
+      const uint32_t ocol = C::O_COL + hf * (C::HALF / 2);
       if (unit.slot < 0) {
         float f = 0.f;
         if (p.sink) {
@@ -647,10 +684,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
         }
         __nv_bfloat16 *dst = p.out + (static_cast<int64_t>(row) * p.H + h) * L + col0;
 #pragma unroll 1
-        for (int c0 = 0; c0 < C::HALF; c0 += 16) {
+        for (int c0 = 0; c0 < C::HALF / 2; c0 += 16) {
           float o[16];
           if (ntiles > 0) {
-            tmem_ld16(tmem_base + lane_base + C::O_COL + c0, o);
+            tmem_ld16(tmem_base + lane_base + ocol + c0, o);
             tmem_ld_wait();
           } else {
 #pragma unroll
@@ -669,10 +706,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
       } else {
         float *dst = p.opart + (static_cast<int64_t>(unit.slot) * p.H + h) * L + col0;
 #pragma unroll 1
-        for (int c0 = 0; c0 < C::HALF; c0 += 16) {
+        for (int c0 = 0; c0 < C::HALF / 2; c0 += 16) {
           float o[16];
           if (ntiles > 0) {
-            tmem_ld16(tmem_base + lane_base + C::O_COL + c0, o);
+            tmem_ld16(tmem_base + lane_base + ocol + c0, o);
             tmem_ld_wait();
           } else {
 #pragma unroll
@@ -682,7 +719,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
 #pragma unroll
           for (int i = 0; i < 4; ++i) d4[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
         }
-        if (crank == 0) {
+        if (crank == 0 && hf == 0) {
           float *ml = p.mlpart + (static_cast<int64_t>(unit.slot) * p.H + h) * 2;
           ml[0] = m_ref;
           ml[1] = l;
