@@ -481,7 +481,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
     for (int u = 0; u < ntiles && ok; ++u) {
       const int b = u & 1;
       const uint32_t use = static_cast<uint32_t>(u >> 1);
-      if (!mbar_wait(sfull(b), use & 1, abort_flag, p.err)) break;
+      // warp-uniform, as the TMEM loads below are warp-collective
+      if (!__all_sync(0xffffffffu, mbar_wait(sfull(b), use & 1, abort_flag, p.err))) break;
       tc_fence_after();
       float v[T];
 #pragma unroll
@@ -642,7 +643,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
         good = __all_sync(0xffffffffu, mbar_wait(b_pvdone, (t - 1) & 1, abort_flag, p.err));
         tc_fence_after();
       }
-      if (good && rescale && t > 0) {
+      // the O loads and stores are warp-collective: the warp rescales when any
+      // of its heads needs it (alpha is exactly 1 for the others)
+      if (good && t > 0 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
         for (int c0 = 0; c0 < C::HALF / 2; c0 += 16) {
           float o[16];
@@ -668,12 +671,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
     red[(4 + hf) * 128 + h] = l;
     named_bar_sync(pair_bar, 64);
     l = red[4 * 128 + h] + red[5 * 128 + h];
-    if (ok && h < p.H) {
+    // (ok is warp-uniform and every lane takes its row out of TMEM, since the
+    // loads are warp-collective; only heads below H are stored)
+    const bool store = h < p.H;
+    if (ok) {
       const int col0 = static_cast<int>(crank) * C::HALF + hf * (C::HALF / 2);
       const uint32_t ocol = C::O_COL + hf * (C::HALF / 2);
       if (unit.slot < 0) {
         float f = 0.f;
-        if (p.sink) {
+        if (p.sink && store) {
           const float xs = p.sink[h] * kLog2e;
           const float mf = fmaxf(m_ref, xs);
           const float a = exp2f(m_ref - mf);
@@ -686,6 +692,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
 #pragma unroll 1
         for (int c0 = 0; c0 < C::HALF / 2; c0 += 16) {
           float o[16];
+          __syncwarp();   // converged for the warp-collective load
           if (ntiles > 0) {
             tmem_ld16(tmem_base + lane_base + ocol + c0, o);
             tmem_ld_wait();
@@ -693,6 +700,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) o[i] = 0.f;
           }
+          if (!store) continue;
           uint32_t w[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
@@ -708,6 +716,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
 #pragma unroll 1
         for (int c0 = 0; c0 < C::HALF / 2; c0 += 16) {
           float o[16];
+          __syncwarp();   // converged for the warp-collective load
           if (ntiles > 0) {
             tmem_ld16(tmem_base + lane_base + ocol + c0, o);
             tmem_ld_wait();
@@ -715,11 +724,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) o[i] = 0.f;
           }
+          if (!store) continue;
           float4 *d4 = reinterpret_cast<float4 *>(dst + c0);
 #pragma unroll
           for (int i = 0; i < 4; ++i) d4[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
         }
-        if (crank == 0 && hf == 0) {
+        if (crank == 0 && hf == 0 && store) {
           float *ml = p.mlpart + (static_cast<int64_t>(unit.slot) * p.H + h) * 2;
           ml[0] = m_ref;
           ml[1] = l;

@@ -298,7 +298,8 @@ __global__ void __launch_bounds__(kIdxThreads, 2) index_tc_kernel(const __grid_c
       }
       bool ok = true;
       for (int t = item.tile0; t < item.tile1; ++t) {
-        if (!mbar_wait(afull(acc), aphase, abort_flag, p.err)) { ok = false; break; }
+        // warp-uniform, as the TMEM loads below are warp-collective
+        if (!__all_sync(0xffffffffu, mbar_wait(afull(acc), aphase, abort_flag, p.err))) { ok = false; break; }
         tc_fence_after();
         const int key = t * 128 + m;
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * C::N;

@@ -85,11 +85,11 @@ def check_attention(gpu_out, ref_out, fp8=False):
 
 
 def deepseek_small(seed=0, fp8=False, sink=False, page_start=0, integer=False, heads=128, decode_ctx=(2500, 5000, 3001, 700),
-                   chunk=(2090, 40)):
+                   chunk=(2090, 40), kv_lora_rank=512):
     """DeepSeek-V3.2 shapes (indexer 64x128, topk 2048, MLA 128 x 512+64,
     page 64) at contexts the oracle finishes in seconds: a few decode rows
     and one prefill chunk that crosses topk."""
-    sh = W.DSAShape(**dict(W.DEEPSEEK, heads=heads),
+    sh = W.DSAShape(**dict(W.DEEPSEEK, heads=heads, kv_lora_rank=kv_lora_rank),
                     latent_fmt=W.LATENT_FP8_656 if fp8 else W.LATENT_BF16,
                     index_fmt=W.INDEX_FP8_132 if fp8 else W.INDEX_BF16, has_sink=sink)
     reqs = [(c - 1, 1) for c in decode_ctx] + ([chunk] if chunk else [])
