@@ -91,12 +91,12 @@ def test_deepseek_shapes_fewer_heads():
 
 
 @pytest.mark.parametrize("kv_lora_rank,heads,fp8", [(256, 128, False), (128, 128, False), (256, 40, False),
-                                                  (256, 128, True)])
+                                                  (512, 72, True), (256, 128, True)])
 def test_attention_other_latent_widths(kv_lora_rank, heads, fp8):
     """The tensor-core attention at its other latent widths (each CTA of the
     pair owns 128 or 64 latent columns instead of 256) and with fewer heads
-    than the 128 TMEM lanes; fp8 latents of width 256 take the CUDA-core
-    kernel."""
+    than the 128 TMEM lanes (40 and 72 split a warp of heads); fp8 latents of
+    width 256 take the CUDA-core kernel."""
     _run(H.deepseek_small(seed=20 + kv_lora_rank // 64 + heads + fp8, kv_lora_rank=kv_lora_rank, heads=heads,
                           fp8=fp8, sink=fp8, decode_ctx=(2300, 700), chunk=(2040, 12)))
 
