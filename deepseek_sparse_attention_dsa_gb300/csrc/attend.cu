@@ -58,7 +58,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr float kNegBig = -1.0e30f;
 
-// warp roles (16 warps; registers are handed out per group of four warps)
+// warp roles (20 warps; every warp of a TMEM lane quadrant q sits on sub-partition q = warp % 4)
 constexpr int kMmaWarp = 0;
 constexpr int kProdWarp0 = 1;               // warps 1-7: producers (224 threads)
 constexpr int kSoftWarp0 = 8;               // warps 8-15: softmax, thread = head; warps 8-11 keys 0-31, 12-15 keys 32-63
@@ -330,7 +330,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
           idle_since = 0;
         } else {
           ++idle;
-          __nanosleep(32);   // leave the issue slots to the softmax warp on this sub-partition
+          __nanosleep(32);   // leave the issue slots to the other warps on this sub-partition
         }
         if (!progressed && (idle & 255) == 0) {
           if (*abort_flag) break;
