@@ -53,6 +53,7 @@ struct AttCombine {
 
 constexpr int kIndexTile = 128;   // keys per indexer tile (UMMA M)
 constexpr int kAttTile = 64;      // keys per attention tile (UMMA N of QK)
+constexpr int kNoBox = -0x7fffffff - 1;   // index producers: a lane with no key box in the tile
 constexpr int kPlanMaxRows = 8192;   // capturable plans: rows and spans the device planner holds in shared memory
 constexpr int kPlanMaxSpans = 4096;
 

@@ -65,6 +65,7 @@ struct IdxTraits {
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;  // + alignment slack
   static_assert(N <= 256 && N >= 16, "UMMA N");
+  static_assert((kIndexTile / 8) * NCH <= 32, "one producer lane per (box, chunk) of a tile");
   static_assert(DI % CH == 0 && CH % 16 == 0, "index dim");
   static_assert(HI % 4 == 0, "heads");
 };
@@ -176,29 +177,36 @@ __global__ void __launch_bounds__(kIdxThreads, 2) index_tc_kernel(const __grid_c
         if (__shfl_sync(0xffffffffu, qok ? 1 : 0, 0) == 0) break;
       }
       const int nkeys_total = g.pos0 + g.nrows;  // keys 0 .. pos0+nrows-1
-      // physical cache row of this lane's box of tile t (lane < boxes of t), or -1
-      auto box_row = [&](int t) -> int {
-        const int nb = (min(128, nkeys_total - t * 128) + p.BH - 1) / p.BH;
-        int r = -1;
-        if (lane < nb) {
-          const int64_t slot = static_cast<int64_t>(g.page_start) + t * 128 + lane * p.BH;
-          const int64_t pi = slot / p.P;
-          if (pi < g.npages) {
-            const int page = p.pages[g.page_off + pi];
-            if (page >= 0 && page < p.num_pages) r = page * p.P + static_cast<int>(slot % p.P);
-          }
-          if (r < 0) atomicOr(p.err, kErrBounds);
-        }
-        return r;
+      // raw page id of this lane's box of tile t (kNoBox: the tile has no box
+      // for this lane; -1: past the request's pages), looked up four tiles
+      // ahead of its issue (a shift queue in registers); the check and the
+      // cache row come when the tile is issued
+      auto box_page = [&](int t) -> int {
+        const int nb = t < item.tile1 ? (min(128, nkeys_total - t * 128) + p.BH - 1) / p.BH : 0;
+        if (lane >= nb) return kNoBox;
+        const int64_t pi = (static_cast<int64_t>(g.page_start) + t * 128 + lane * p.BH) / p.P;
+        return pi < g.npages ? __ldg(p.pages + g.page_off + pi) : -1;
       };
-      // the page-table lookups of tile t+1 are issued before tile t waits for
-      // its stage, so their latency hides behind the pipeline
-      int next_row = box_row(item.tile0);
+      // physical cache row of this lane's box of tile t, or -1
+      auto box_row = [&](int t, int page) -> int {
+        if (page == kNoBox) return -1;
+        if (page < 0 || page >= p.num_pages) {
+          atomicOr(p.err, kErrBounds);
+          return -1;
+        }
+        const int64_t slot = static_cast<int64_t>(g.page_start) + t * 128 + lane * p.BH;
+        return page * p.P + static_cast<int>(slot % p.P);
+      };
+      int la0 = box_page(item.tile0), la1 = box_page(item.tile0 + 1), la2 = box_page(item.tile0 + 2),
+          la3 = box_page(item.tile0 + 3);
       for (int t = item.tile0; t < item.tile1; ++t) {
         const int nkeys = min(128, nkeys_total - t * 128);
         const int nbox = (nkeys + p.BH - 1) / p.BH;
-        const int myrow = next_row;
-        if (t + 1 < item.tile1) next_row = box_row(t + 1);
+        const int myrow = box_row(t, la0);
+        la0 = la1;
+        la1 = la2;
+        la2 = la3;
+        la3 = box_page(t + 4);
         const uint32_t valid = __ballot_sync(0xffffffffu, myrow >= 0);
         bool ok = true;
         if (lane == 0) ok = mbar_wait(kempty(stage), kphase ^ 1, abort_flag, p.err);
@@ -209,13 +217,15 @@ __global__ void __launch_bounds__(kIdxThreads, 2) index_tc_kernel(const __grid_c
           if (bytes) mbar_arrive_expect_tx(kfull(stage), bytes);
           else mbar_arrive(kfull(stage));
         }
-        for (int b = 0; b < nbox; ++b) {
-          const int row = __shfl_sync(0xffffffffu, myrow, b);
-          if (lane == 0 && row >= 0) {
-            for (int c = 0; c < C::NCH; ++c)
-              tma_load_2d(sbase + C::OFF_K + stage * C::KT_BYTES + c * 128 * C::ROWB + b * p.BH * C::ROWB,
-                          &p.tm_keys, c * C::CH, row, kfull(stage));
-          }
+        {
+          // every (box, chunk) of the tile from its own lane: the tile's loads
+          // go out as one warp instruction, not one by one from lane 0 (a
+          // box has >= 8 rows, so nbox * NCH <= 32)
+          const int b = lane / C::NCH, c = lane % C::NCH;
+          const int row = __shfl_sync(0xffffffffu, myrow, b & 31);
+          if (b < nbox && row >= 0)
+            tma_load_2d(sbase + C::OFF_K + stage * C::KT_BYTES + c * 128 * C::ROWB + b * p.BH * C::ROWB,
+                        &p.tm_keys, c * C::CH, row, kfull(stage));
         }
         if (++stage == C::STAGES) {
           stage = 0;
@@ -611,32 +621,37 @@ __global__ void __launch_bounds__(kFp8Threads, 1) index_fp8_tc_kernel(const __gr
         if (__shfl_sync(0xffffffffu, qok ? 1 : 0, 0) == 0) break;
       }
       const int nkeys_total = g.pos0 + g.nrows;
-      // (page, slot) of this lane's box of tile t, page -1 past the tile
-      auto box_at = [&](int t, int &slot_out) -> int {
-        const int nb = (min(128, nkeys_total - t * 128) + p.BH - 1) / p.BH;
-        int page = -1;
+      // raw page id of this lane's box of tile t (kNoBox: no box for this lane;
+      // -1: past the request's pages), looked up four tiles ahead of its issue
+      // (a shift queue in registers) and checked when the tile is issued
+      auto box_page = [&](int t) -> int {
+        const int nb = t < item.tile1 ? (min(128, nkeys_total - t * 128) + p.BH - 1) / p.BH : 0;
+        if (lane >= nb) return kNoBox;
+        const int64_t pi = (static_cast<int64_t>(g.page_start) + t * 128 + lane * p.BH) / p.P;
+        return pi < g.npages ? __ldg(p.pages + g.page_off + pi) : -1;
+      };
+      // (page, slot) of this lane's box of tile t, page -1 if there is none
+      auto box_at = [&](int t, int page, int &slot_out) -> int {
         slot_out = 0;
-        if (lane < nb) {
-          const int64_t slot = static_cast<int64_t>(g.page_start) + t * 128 + lane * p.BH;
-          const int64_t pi = slot / p.P;
-          if (pi < g.npages) {
-            const int pg = p.pages[g.page_off + pi];
-            if (pg >= 0 && pg < p.num_pages) {
-              page = pg;
-              slot_out = static_cast<int>(slot % p.P);
-            }
-          }
-          if (page < 0) atomicOr(p.err, kErrBounds);
+        if (page == kNoBox) return -1;
+        if (page < 0 || page >= p.num_pages) {
+          atomicOr(p.err, kErrBounds);
+          return -1;
         }
+        slot_out = static_cast<int>((static_cast<int64_t>(g.page_start) + t * 128 + lane * p.BH) % p.P);
         return page;
       };
-      int next_slot = 0;
-      int next_page = box_at(item.tile0, next_slot);
+      int lp0 = box_page(item.tile0), lp1 = box_page(item.tile0 + 1), lp2 = box_page(item.tile0 + 2),
+          lp3 = box_page(item.tile0 + 3);
       for (int t = item.tile0; t < item.tile1; ++t) {
         const int nkeys = min(128, nkeys_total - t * 128);
         const int nbox = (nkeys + p.BH - 1) / p.BH;
-        const int mypage = next_page, myslot = next_slot;
-        if (t + 1 < item.tile1) next_page = box_at(t + 1, next_slot);
+        int myslot;
+        const int mypage = box_at(t, lp0, myslot);
+        lp0 = lp1;
+        lp1 = lp2;
+        lp2 = lp3;
+        lp3 = box_page(t + 4);
         const uint32_t valid = __ballot_sync(0xffffffffu, mypage >= 0);
         bool ok = true;
         if (lane == 0) ok = mbar_wait(c8empty(s8), ph8 ^ 1, abort_flag, p.err);

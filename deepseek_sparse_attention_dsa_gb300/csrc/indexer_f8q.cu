@@ -162,53 +162,63 @@ __global__ void __launch_bounds__(F8qTraits<G>::THREADS, 1) index_f8q_kernel(con
         if (__shfl_sync(0xffffffffu, qok ? 1 : 0, 0) == 0) break;
       }
       const int nkeys_total = g.pos0 + g.nrows;
-      // (page, slot) of this lane's box of tile t, page -1 past the tile
-      auto box_at = [&](int t, int &slot_out) -> int {
-        const int nb = (min(128, nkeys_total - t * 128) + p.BH - 1) / p.BH;
-        int page = -1;
+      // raw page id of this lane's box of tile t (kNoBox: no box for this lane;
+      // -1: past the request's pages), looked up four tiles ahead of its issue
+      // and checked when the tile is issued
+      auto box_page = [&](int t) -> int {
+        const int nb = t < item.tile1 ? (min(128, nkeys_total - t * 128) + p.BH - 1) / p.BH : 0;
+        if (lane >= nb) return kNoBox;
+        const int64_t pi = (static_cast<int64_t>(g.page_start) + t * 128 + lane * p.BH) / p.P;
+        return pi < g.npages ? __ldg(p.pages + g.page_off + pi) : -1;
+      };
+      // (page, slot) of this lane's box of tile t, page -1 if there is none
+      auto box_at = [&](int t, int page, int &slot_out) -> int {
         slot_out = 0;
-        if (lane < nb) {
-          const int64_t slot = static_cast<int64_t>(g.page_start) + t * 128 + lane * p.BH;
-          const int64_t pi = slot / p.P;
-          if (pi < g.npages) {
-            const int pg = p.pages[g.page_off + pi];
-            if (pg >= 0 && pg < p.num_pages) {
-              page = pg;
-              slot_out = static_cast<int>(slot % p.P);
-            }
-          }
-          if (page < 0) atomicOr(p.err, kErrBounds);
+        if (page == kNoBox) return -1;
+        if (page < 0 || page >= p.num_pages) {
+          atomicOr(p.err, kErrBounds);
+          return -1;
         }
+        slot_out = static_cast<int>((static_cast<int64_t>(g.page_start) + t * 128 + lane * p.BH) % p.P);
         return page;
       };
-      int next_slot = 0;
-      int next_page = box_at(item.tile0, next_slot);
-      for (int t = item.tile0; t < item.tile1; ++t) {
-        const int nkeys = min(128, nkeys_total - t * 128);
-        const int nbox = (nkeys + p.BH - 1) / p.BH;
-        const int mypage = next_page, myslot = next_slot;
-        if (t + 1 < item.tile1) next_page = box_at(t + 1, next_slot);
-        const uint32_t valid = __ballot_sync(0xffffffffu, mypage >= 0);
-        bool ok = true;
-        if (lane == 0) ok = mbar_wait(sempty(st), ph ^ 1, abort_flag, p.err);
-        if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) break;
-        const uint32_t bytes = __popc(valid) * p.BH * (128 + 4);
-        if (lane == 0) {
-          if (bytes) mbar_arrive_expect_tx(sfull(st), bytes);
-          else mbar_arrive(sfull(st));
-        }
-        const uint32_t stage = sbase + C::OFF_ST + st * C::STAGE;
-        for (int b = 0; b < nbox; ++b) {
-          const int page = __shfl_sync(0xffffffffu, mypage, b);
-          const int slot = __shfl_sync(0xffffffffu, myslot, b);
-          if (lane == 0 && page >= 0) {
-            tma_load_3d(stage + b * p.BH * 128, &p.tm_codes, 0, slot, page, sfull(st));
-            tma_load_2d(stage + C::CODE_BYTES + b * sc_stride * 4, &p.tm_scales, slot, page, sfull(st));
+      // four lookups in flight: the loop is unrolled by four so that every
+      // looked-up page id stays in its own register until its tile is issued
+      int lp[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) lp[u] = box_page(item.tile0 + u);
+      bool stop = false;
+      for (int t0 = item.tile0; t0 < item.tile1 && !stop; t0 += 4) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int t = t0 + u;
+          if (t >= item.tile1) break;
+          int myslot;
+          const int mypage = box_at(t, lp[u], myslot);
+          lp[u] = box_page(t + 4);
+          const uint32_t valid = __ballot_sync(0xffffffffu, mypage >= 0);
+          bool ok = true;
+          if (lane == 0) ok = mbar_wait(sempty(st), ph ^ 1, abort_flag, p.err);
+          if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) {
+            stop = true;
+            break;
           }
-        }
-        if (++st == C::STAGES) {
-          st = 0;
-          ph ^= 1;
+          const uint32_t bytes = __popc(valid) * p.BH * (128 + 4);
+          if (lane == 0) {
+            if (bytes) mbar_arrive_expect_tx(sfull(st), bytes);
+            else mbar_arrive(sfull(st));
+          }
+          // every box from the lane that looked it up (lane b holds box b):
+          // the tile's loads go out as one warp instruction
+          const uint32_t stage = sbase + C::OFF_ST + st * C::STAGE;
+          if (mypage >= 0) {
+            tma_load_3d(stage + lane * p.BH * 128, &p.tm_codes, 0, myslot, mypage, sfull(st));
+            tma_load_2d(stage + C::CODE_BYTES + lane * sc_stride * 4, &p.tm_scales, myslot, mypage, sfull(st));
+          }
+          if (++st == C::STAGES) {
+            st = 0;
+            ph ^= 1;
+          }
         }
       }
     }
