@@ -184,8 +184,10 @@ __global__ void __launch_bounds__(kIdxThreads, 2) index_tc_kernel(const __grid_c
       auto box_page = [&](int t) -> int {
         const int nb = t < item.tile1 ? (min(128, nkeys_total - t * 128) + p.BH - 1) / p.BH : 0;
         if (lane >= nb) return kNoBox;
-        const int64_t pi = (static_cast<int64_t>(g.page_start) + t * 128 + lane * p.BH) / p.P;
-        return pi < g.npages ? __ldg(p.pages + g.page_off + pi) : -1;
+        // (32-bit: a slot is page_start + a position, both non-negative int32)
+        const uint32_t pi = (static_cast<uint32_t>(g.page_start) + static_cast<uint32_t>(t * 128 + lane * p.BH)) /
+                            static_cast<uint32_t>(p.P);
+        return pi < static_cast<uint32_t>(g.npages) ? __ldg(p.pages + g.page_off + pi) : -1;
       };
       // physical cache row of this lane's box of tile t, or -1
       auto box_row = [&](int t, int page) -> int {
@@ -194,8 +196,8 @@ __global__ void __launch_bounds__(kIdxThreads, 2) index_tc_kernel(const __grid_c
           atomicOr(p.err, kErrBounds);
           return -1;
         }
-        const int64_t slot = static_cast<int64_t>(g.page_start) + t * 128 + lane * p.BH;
-        return page * p.P + static_cast<int>(slot % p.P);
+        const uint32_t slot = static_cast<uint32_t>(g.page_start) + static_cast<uint32_t>(t * 128 + lane * p.BH);
+        return page * p.P + static_cast<int>(slot % static_cast<uint32_t>(p.P));
       };
       int la0 = box_page(item.tile0), la1 = box_page(item.tile0 + 1), la2 = box_page(item.tile0 + 2),
           la3 = box_page(item.tile0 + 3);
@@ -627,8 +629,10 @@ __global__ void __launch_bounds__(kFp8Threads, 1) index_fp8_tc_kernel(const __gr
       auto box_page = [&](int t) -> int {
         const int nb = t < item.tile1 ? (min(128, nkeys_total - t * 128) + p.BH - 1) / p.BH : 0;
         if (lane >= nb) return kNoBox;
-        const int64_t pi = (static_cast<int64_t>(g.page_start) + t * 128 + lane * p.BH) / p.P;
-        return pi < g.npages ? __ldg(p.pages + g.page_off + pi) : -1;
+        // (32-bit: a slot is page_start + a position, both non-negative int32)
+        const uint32_t pi = (static_cast<uint32_t>(g.page_start) + static_cast<uint32_t>(t * 128 + lane * p.BH)) /
+                            static_cast<uint32_t>(p.P);
+        return pi < static_cast<uint32_t>(g.npages) ? __ldg(p.pages + g.page_off + pi) : -1;
       };
       // (page, slot) of this lane's box of tile t, page -1 if there is none
       auto box_at = [&](int t, int page, int &slot_out) -> int {
@@ -638,7 +642,8 @@ __global__ void __launch_bounds__(kFp8Threads, 1) index_fp8_tc_kernel(const __gr
           atomicOr(p.err, kErrBounds);
           return -1;
         }
-        slot_out = static_cast<int>((static_cast<int64_t>(g.page_start) + t * 128 + lane * p.BH) % p.P);
+        slot_out = static_cast<int>((static_cast<uint32_t>(g.page_start) + static_cast<uint32_t>(t * 128 + lane * p.BH)) %
+                                    static_cast<uint32_t>(p.P));
         return page;
       };
       int lp0 = box_page(item.tile0), lp1 = box_page(item.tile0 + 1), lp2 = box_page(item.tile0 + 2),

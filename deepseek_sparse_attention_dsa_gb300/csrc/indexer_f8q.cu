@@ -168,8 +168,10 @@ __global__ void __launch_bounds__(F8qTraits<G>::THREADS, 1) index_f8q_kernel(con
       auto box_page = [&](int t) -> int {
         const int nb = t < item.tile1 ? (min(128, nkeys_total - t * 128) + p.BH - 1) / p.BH : 0;
         if (lane >= nb) return kNoBox;
-        const int64_t pi = (static_cast<int64_t>(g.page_start) + t * 128 + lane * p.BH) / p.P;
-        return pi < g.npages ? __ldg(p.pages + g.page_off + pi) : -1;
+        // (32-bit: a slot is page_start + a position, both non-negative int32)
+        const uint32_t pi = (static_cast<uint32_t>(g.page_start) + static_cast<uint32_t>(t * 128 + lane * p.BH)) /
+                            static_cast<uint32_t>(p.P);
+        return pi < static_cast<uint32_t>(g.npages) ? __ldg(p.pages + g.page_off + pi) : -1;
       };
       // (page, slot) of this lane's box of tile t, page -1 if there is none
       auto box_at = [&](int t, int page, int &slot_out) -> int {
@@ -179,7 +181,8 @@ __global__ void __launch_bounds__(F8qTraits<G>::THREADS, 1) index_f8q_kernel(con
           atomicOr(p.err, kErrBounds);
           return -1;
         }
-        slot_out = static_cast<int>((static_cast<int64_t>(g.page_start) + t * 128 + lane * p.BH) % p.P);
+        slot_out = static_cast<int>((static_cast<uint32_t>(g.page_start) + static_cast<uint32_t>(t * 128 + lane * p.BH)) %
+                                    static_cast<uint32_t>(p.P));
         return page;
       };
       // four lookups in flight: the loop is unrolled by four so that every
