@@ -40,7 +40,7 @@ namespace {
 // CTA sizes: 1024 threads, one CTA per SM, when every row has its own CTA;
 // 512 threads, two per SM, when persistent CTAs take several rows each
 constexpr int kMaxWarps = 32;
-constexpr int kBatch = 8;             // independent loads in flight per thread
+constexpr int kBatch = 16;            // independent loads in flight per thread
 constexpr int kCandCap = 8192;        // candidate keys held in shared memory
 constexpr int kSampleMin = 4096;      // a strided sample holds kSampleMin .. 2*kSampleMin-1 keys
 constexpr int kBitmapWords = 8192;    // 262,144 positions
