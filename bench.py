@@ -22,6 +22,11 @@ for decode workloads the step is instead one CUDA graph over a capturable plan
 with the inputs), which is also timed device-resident as `captured_step`.
 The end-to-end loop keeps two buffer sets with the copies on their own
 streams, so each step's transfers overlap the neighbouring steps' kernels.
+Decode workloads also time the prefill workloads (`--prefill`, default
+chunked_prefill and mixed_fp8) in the same process at the same steps and
+warm-up, reported under `prefill`: tokens/s, the stage split, and the
+indexer's and the attention's TFLOP/s as fractions of the measured dense bf16
+peak, with the clocks of that leg.
 `--impl reference` times the CPU oracle (the only reference this method has)
 on a bounded sample of the same workload on the host cores.
 Multi-GPU (torchrun): independent replicas, one per rank (weak scaling).
@@ -158,34 +163,13 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 # our implementation
 # ----------------------------------------------------------------------------
-def run_ours(args, name, rank, world, local_rank):
-    from deepseek_sparse_attention_dsa_gb300 import build as lib_build
-    from deepseek_sparse_attention_dsa_gb300 import dsa
-
-    lib_build.build()
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    wl = W.config(WORKLOADS[name], seed=1000 + WORKLOADS[name] + 7919 * rank)
-    if args.requests:
-        # the first N requests only: a smaller case of the same workload for profiler captures
-        wl = wl.sub_workload(range(min(args.requests, len(wl.spans))))
+def timed_steps(ctx, plan, wl, ic, lc, st, scores, sel, out, flush, args, world, dev):
+    """W untimed steps, then K steps each timed per stage with CUDA events on
+    the launching stream (L2 flushed before each step, outside the events),
+    with the clocks sampled meanwhile.  A step = store keys, index score,
+    top-k, attend over a host plan built once."""
     sh = wl.shape
-    unit, decode = unit_of(wl)
-    work = algorithmic(wl)
-
-    ic = W.make_index_cache(wl, device=dev)
-    lc = W.make_latent_cache(wl, device=dev)
-    st = W.make_step_inputs(wl, device=dev)
-    ctx = dsa.Context(sh, local_rank)
     stream = torch.cuda.current_stream(dev)
-    t0 = time.perf_counter()
-    plan = ctx.plan(wl.spans, wl.num_pages)
-    torch.cuda.synchronize(dev)
-    plan_ms = (time.perf_counter() - t0) * 1e3
-    scores = torch.empty(max(1, plan.num_scores), dtype=torch.float32, device=dev)
-    sel = torch.empty(plan.num_rows, sh.topk, dtype=torch.int32, device=dev)
-    out = torch.empty(plan.num_rows, sh.heads, sh.kv_lora_rank, dtype=torch.bfloat16, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
     launches = [0]
 
@@ -219,7 +203,7 @@ def run_ours(args, name, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     stage = {"store": [], "index": [], "topk": [], "attend": [], "step": []}
     n_launch = 0
-    with ClockSampler(local_rank) as clk:
+    with ClockSampler(dev.index) as clk:
         for _ in range(args.steps):
             flush.zero_()
             step(True)
@@ -232,6 +216,80 @@ def run_ours(args, name, rank, world, local_rank):
             stage["step"].append(ev[0].elapsed_time(ev[4]))
     torch.cuda.synchronize(dev)
     ctx.get_error()
+    return stage, n_launch, clk.summary()
+
+
+def prefill_leg(args, name, rank, world, dev, flush):
+    """A prefill workload timed like the headline step, in the same process
+    and at the same steps and warm-up: tokens/s, the stage split, and the
+    indexer's and the attention's TFLOP/s against the measured bf16 peak."""
+    from deepseek_sparse_attention_dsa_gb300 import dsa
+    wl = W.config(WORKLOADS[name], seed=1000 + WORKLOADS[name] + 7919 * rank)
+    sh = wl.shape
+    work = algorithmic(wl)
+    ic = W.make_index_cache(wl, device=dev)
+    lc = W.make_latent_cache(wl, device=dev)
+    st = W.make_step_inputs(wl, device=dev)
+    ctx = dsa.Context(sh, dev.index)
+    plan = ctx.plan(wl.spans, wl.num_pages)
+    scores = torch.empty(max(1, plan.num_scores), dtype=torch.float32, device=dev)
+    sel = torch.empty(plan.num_rows, sh.topk, dtype=torch.int32, device=dev)
+    out = torch.empty(plan.num_rows, sh.heads, sh.kv_lora_rank, dtype=torch.bfloat16, device=dev)
+    stage, n_launch, clk = timed_steps(ctx, plan, wl, ic, lc, st, scores, sel, out, flush, args, world, dev)
+    total_ms = float(sum(stage["step"]))
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms = total_ms / args.steps
+    _, bf16, _, peak_kind = measured_peaks()
+    idx_ms = statistics.mean(stage["index"])
+    att_ms = statistics.mean(stage["attend"])
+    idx_tf = work["index_flops"] / (idx_ms / 1e3) / 1e12
+    att_tf = work["attend_flops"] / (att_ms / 1e3) / 1e12
+    leg = {"workload": name, "value": round(work["rows"] * world / (ms / 1e3), 2), "unit": unit_of(wl)[0],
+           "ms_per_step": round(ms, 4), "stages_ms": {k: round(statistics.mean(v), 4) for k, v in stage.items()},
+           "index_tflops": round(idx_tf, 2), "index_frac": round(idx_tf / bf16, 4),
+           "attend_tflops": round(att_tf, 2), "attend_frac": round(att_tf / bf16, 4),
+           "peak_tflops": bf16, "peak_kind": peak_kind + " (bf16_tflops burst)",
+           "index_flops_per_step": work["index_flops"], "attend_flops_per_step": work["attend_flops"],
+           "gpu_launches": n_launch, "clocks": clk, "config": workload_config(name, wl)}
+    plan.close()
+    del ic, lc, st, scores, sel, out
+    torch.cuda.empty_cache()
+    return leg
+
+
+def run_ours(args, name, rank, world, local_rank):
+    from deepseek_sparse_attention_dsa_gb300 import build as lib_build
+    from deepseek_sparse_attention_dsa_gb300 import dsa
+
+    lib_build.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = W.config(WORKLOADS[name], seed=1000 + WORKLOADS[name] + 7919 * rank, page_start=args.page_start)
+    if args.requests:
+        # the first N requests only: a smaller case of the same workload for profiler captures
+        wl = wl.sub_workload(range(min(args.requests, len(wl.spans))))
+    sh = wl.shape
+    unit, decode = unit_of(wl)
+    work = algorithmic(wl)
+
+    ic = W.make_index_cache(wl, device=dev)
+    lc = W.make_latent_cache(wl, device=dev)
+    st = W.make_step_inputs(wl, device=dev)
+    ctx = dsa.Context(sh, local_rank)
+    stream = torch.cuda.current_stream(dev)
+    t0 = time.perf_counter()
+    plan = ctx.plan(wl.spans, wl.num_pages)
+    torch.cuda.synchronize(dev)
+    plan_ms = (time.perf_counter() - t0) * 1e3
+    scores = torch.empty(max(1, plan.num_scores), dtype=torch.float32, device=dev)
+    sel = torch.empty(plan.num_rows, sh.topk, dtype=torch.int32, device=dev)
+    out = torch.empty(plan.num_rows, sh.heads, sh.kv_lora_rank, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    stage, n_launch, clk_summary = timed_steps(ctx, plan, wl, ic, lc, st, scores, sel, out, flush, args, world, dev)
     total_ms = float(sum(stage["step"]))
     if world > 1:
         t = torch.tensor([total_ms], device=dev)
@@ -438,8 +496,10 @@ def run_ours(args, name, rank, world, local_rank):
                          "copies on their own streams overlapping the neighbouring steps"),
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 3)},
         "gpu_launches": n_launch,
-        "clocks": clk.summary(),
+        "clocks": clk_summary,
     }
+    if args.prefill and decode and not args.requests and not args.page_start:
+        line["prefill"] = [prefill_leg(args, p, rank, world, dev, flush) for p in args.prefill.split(",") if p]
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_rows)
     return line
@@ -612,6 +672,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true",
                     help="decode workloads: time the eager calls over a host plan instead of the captured step")
+    ap.add_argument("--prefill", default="chunked_prefill,mixed_fp8",
+                    help="decode workloads: prefill workloads timed in the same run (comma list; '' for none)")
+    ap.add_argument("--page-start", type=int, default=0,
+                    help="every request's token 0 at this slot of its first page (0 in the evaluation workloads)")
     ap.add_argument("--requests", type=int, default=0,
                     help="keep only the first N requests of the workload (profiler captures; not a bench line)")
     args = ap.parse_args()

@@ -182,6 +182,14 @@ dsa_status dsa_create(const dsa_config_t *cfg, int device, dsa_ctx_t **out) {
     }
     if (cudaMalloc(&ctx->err, sizeof(int)) != cudaSuccess) { delete ctx; return DSA_ERR_OOM; }
     if (cudaMemset(ctx->err, 0, sizeof(int)) != cudaSuccess) { cudaFree(ctx->err); delete ctx; return DSA_ERR_CUDA; }
+    // the fixed score array of dsa_index_topk_static: looking up its address
+    // loads the module that holds it, so the array is on the device from here
+    // on and the static entry point never makes the driver allocate
+    if (static_scores_address(device, &ctx->static_scores) != cudaSuccess) {
+      cudaFree(ctx->err);
+      delete ctx;
+      return DSA_ERR_CUDA;
+    }
   } else {
     ctx->num_sms = 152;
   }
@@ -238,19 +246,7 @@ dsa_status dsa_plan(dsa_ctx_t *ctx, const dsa_span_t *spans, int32_t num_spans, 
   plan->cache_pages = cache_pages;
   plan->num_scores = num_scores;
   plan->max_pos = max_pos;
-  {
-    // largest power of two <= 128 dividing the page size and every page_start,
-    // so a key box of that many rows never crosses a page boundary
-    int64_t g = P;
-    for (int32_t i = 0; i < num_spans; ++i) {
-      int64_t a = g, b = spans[i].page_start;
-      while (b) { int64_t t = a % b; a = b; b = t; }
-      g = a;
-    }
-    int bh = 1;
-    while (bh < 128 && g % (bh * 2) == 0) bh *= 2;
-    plan->box_rows = bh;
-  }
+  plan->box_rows = index_box_rows(c.page_size);
 
   // ---- indexer groups: single rows (decode spans) and runs of G rows (chunks)
   const int Gm = indexer_group_rows(c);
@@ -268,7 +264,8 @@ dsa_status dsa_plan(dsa_ctx_t *ctx, const dsa_span_t *spans, int32_t num_spans, 
       g.page_off = page_off;
       g.npages = s.num_pages;
       g.page_start = s.page_start;
-      g.ntiles = (g.pos0 + g.nrows + kIndexTile - 1) / kIndexTile;
+      g.lead = index_tile_lead(s.page_start, plan->box_rows);
+      g.ntiles = index_group_tiles(static_cast<int64_t>(g.pos0) + g.nrows, g.lead);
       groups[set].push_back(g);
     }
     page_off += s.num_pages;
@@ -478,14 +475,7 @@ dsa_status dsa_plan_capturable(dsa_ctx_t *ctx, int32_t max_rows, int32_t max_spa
   plan->num_scores = max_scores;
   plan->max_pos = INT32_MAX;
   plan->page_start_align = page_start_align;
-  {
-    // largest power of two <= 128 dividing the page size and the alignment
-    int64_t a = c.page_size, b = page_start_align;
-    while (b) { int64_t t = a % b; a = b; b = t; }
-    int bh = 1;
-    while (bh < 128 && a % (bh * 2) == 0) bh *= 2;
-    plan->box_rows = bh;
-  }
+  plan->box_rows = index_box_rows(c.page_size);
   plan->items_cap = static_cast<int32_t>(items_cap);
   plan->combine_cap = max_rows;
   plan->n_units = static_cast<int32_t>(units_cap);
@@ -578,6 +568,11 @@ dsa_status dsa_plan_get_info(const dsa_plan_t *plan, dsa_plan_info_t *info) {
   info->num_scores = plan->num_scores;
   info->attend_units = plan->n_units;
   info->attend_splits_max = plan->splits_max;
+  bool tc = plan->box_rows >= 8;
+  for (int set = 0; set < 2; ++set)
+    if (plan->idx[set].n_items > 0 && !indexer_tc_supported(plan->ctx->cfg, plan->idx[set].G)) tc = false;
+  info->index_tensor_cores = tc ? 1 : 0;
+  info->index_box_rows = plan->box_rows;
   return DSA_OK;
 }
 

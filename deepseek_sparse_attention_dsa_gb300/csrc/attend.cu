@@ -893,12 +893,8 @@ cudaError_t run_tc(const dsa_ctx *ctx, const dsa_plan_t *plan, const int32_t *se
   prm.num_pages = plan->cache_pages;
   prm.scale_log2 = sm_scale * kLog2e;
   auto kern = attend_tc_kernel<L, FP8>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> smem_limit_set{0};
+  if (cudaError_t e = ensure_smem_limit(kern, Cfg::SMEM, ctx->device, smem_limit_set); e != cudaSuccess) return e;
   kern<<<2 * plan->n_units, kAttThreads, Cfg::SMEM, s>>>(prm);
   return cudaGetLastError();
 }

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <vector>
 
 #include "dsa.h"
@@ -21,8 +22,8 @@ struct IdxGroup {
   int32_t page_off;    // offset of the span's page list in the plan's pages[]
   int32_t npages;      // length of that list
   int32_t page_start;  // slot of token 0
-  int32_t ntiles;      // key tiles of 128 covering positions 0 .. pos0+nrows-1
-  int32_t pad;
+  int32_t ntiles;      // key tiles of 128 covering positions 0 .. pos0+nrows-1 (index_group_tiles)
+  int32_t lead;        // tile rows before token 0: tile t holds positions t*128 - lead .. t*128 - lead + 127
 };
 
 // A contiguous run of key tiles of one group.
@@ -56,6 +57,38 @@ constexpr int kAttTile = 64;      // keys per attention tile (UMMA N of QK)
 constexpr int kNoBox = -0x7fffffff - 1;   // index producers: a lane with no key box in the tile
 constexpr int kPlanMaxRows = 8192;   // capturable plans: rows and spans the device planner holds in shared memory
 constexpr int kPlanMaxSpans = 4096;
+
+// Height of the indexer's TMA key boxes: the largest power of two <= 128 that
+// divides the page size.  Key tiles start on a multiple of it in slot space
+// (a span's page_start rounded down), so every box of a tile lies inside one
+// page whatever the span's page_start.
+__host__ __device__ inline int index_box_rows(int page_size) {
+  int bh = 1;
+  while (bh < kIndexTile && page_size % (bh * 2) == 0) bh *= 2;
+  return bh;
+}
+// Tile rows ahead of a span's token 0: page_start's distance above the box
+// boundary below it.
+__host__ __device__ inline int32_t index_tile_lead(int32_t page_start, int box_rows) {
+  return page_start % box_rows;
+}
+// Key tiles of a group whose rows see positions 0 .. nkeys-1.
+__host__ __device__ inline int32_t index_group_tiles(int64_t nkeys, int32_t lead) {
+  return static_cast<int32_t>((lead + nkeys + kIndexTile - 1) / kIndexTile);
+}
+
+// Raises a kernel's dynamic shared-memory limit on the current device once.
+// The limit belongs to the device, so each GPU the process uses gets its own
+// bit in `done` (devices past 63 set it on every launch); two host threads
+// racing here both set the same value, which is harmless.
+template <typename Kernel>
+cudaError_t ensure_smem_limit(Kernel kern, int bytes, int device, std::atomic<uint64_t> &done) {
+  const uint64_t bit = (device >= 0 && device < 64) ? (uint64_t(1) << device) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 // Tiles per indexer work item for `tiles` tiles over `cap` persistent CTAs.
 __host__ __device__ inline int64_t index_tiles_per_item(int64_t tiles, int cap) {
@@ -121,13 +154,14 @@ struct dsa_ctx {
   size_t part_cap = 0;            // slots
   int32_t last_launches = 0;
   char last_cuda_error[160] = {0};  // name and text of the last CUDA error a call returned DSA_ERR_CUDA for
+  float *static_scores = nullptr; // device address of the library's fixed score array (dsa_index_topk_static)
 };
 
 struct dsa_plan {
   dsa_ctx *ctx = nullptr;
   cudaStream_t stream = nullptr;
   int32_t T = 0, n_spans = 0, needs_selection = 0, cache_pages = 0, max_pos = 0;
-  int32_t box_rows = 1;           // TMA box height for key tiles: a power of two dividing page_size and every page_start
+  int32_t box_rows = 1;           // TMA box height of the indexer's key tiles (index_box_rows of the page size)
   int64_t num_scores = 0;
   std::vector<char> host;         // staging copy of the device metadata
   char *dev = nullptr;
@@ -189,6 +223,11 @@ cudaError_t prepare_plan_update(int32_t max_rows, int32_t max_spans);
 cudaError_t launch_attend(const dsa_ctx *ctx, const dsa_plan_t *plan, const int32_t *sel, const void *q_nope,
                           const void *q_pe, const void *latent, const float *sink, float sm_scale, void *out,
                           cudaStream_t s, int32_t *launches);
+
+// Device address of the fixed score array behind dsa_index_topk_static on the
+// current device (loads the module that holds it, so the array is taken when
+// the context is created rather than at the first call).
+cudaError_t static_scores_address(int device, float **out);
 
 // Shapes the tensor-core kernels implement (others run the simple kernels).
 bool indexer_tc_supported(const dsa_config_t &c, int G);

@@ -176,16 +176,16 @@ __global__ void __launch_bounds__(kIdxThreads, 2) index_tc_kernel(const __grid_c
         }
         if (__shfl_sync(0xffffffffu, qok ? 1 : 0, 0) == 0) break;
       }
-      const int nkeys_total = g.pos0 + g.nrows;  // keys 0 .. pos0+nrows-1
+      const int nrows_total = g.lead + g.pos0 + g.nrows;  // tile rows: lead rows, then keys 0 .. pos0+nrows-1
       // raw page id of this lane's box of tile t (kNoBox: the tile has no box
       // for this lane; -1: past the request's pages), looked up four tiles
       // ahead of its issue (a shift queue in registers); the check and the
       // cache row come when the tile is issued
       auto box_page = [&](int t) -> int {
-        const int nb = t < item.tile1 ? (min(128, nkeys_total - t * 128) + p.BH - 1) / p.BH : 0;
+        const int nb = t < item.tile1 ? (min(128, nrows_total - t * 128) + p.BH - 1) / p.BH : 0;
         if (lane >= nb) return kNoBox;
-        // (32-bit: a slot is page_start + a position, both non-negative int32)
-        const uint32_t pi = (static_cast<uint32_t>(g.page_start) + static_cast<uint32_t>(t * 128 + lane * p.BH)) /
+        // (32-bit: a slot is the tile's first slot, page_start - lead >= 0, plus a row)
+        const uint32_t pi = (static_cast<uint32_t>(g.page_start - g.lead) + static_cast<uint32_t>(t * 128 + lane * p.BH)) /
                             static_cast<uint32_t>(p.P);
         return pi < static_cast<uint32_t>(g.npages) ? __ldg(p.pages + g.page_off + pi) : -1;
       };
@@ -196,13 +196,13 @@ __global__ void __launch_bounds__(kIdxThreads, 2) index_tc_kernel(const __grid_c
           atomicOr(p.err, kErrBounds);
           return -1;
         }
-        const uint32_t slot = static_cast<uint32_t>(g.page_start) + static_cast<uint32_t>(t * 128 + lane * p.BH);
+        const uint32_t slot = static_cast<uint32_t>(g.page_start - g.lead) + static_cast<uint32_t>(t * 128 + lane * p.BH);
         return page * p.P + static_cast<int>(slot % static_cast<uint32_t>(p.P));
       };
       int la0 = box_page(item.tile0), la1 = box_page(item.tile0 + 1), la2 = box_page(item.tile0 + 2),
           la3 = box_page(item.tile0 + 3);
       for (int t = item.tile0; t < item.tile1; ++t) {
-        const int nkeys = min(128, nkeys_total - t * 128);
+        const int nkeys = min(128, nrows_total - t * 128);
         const int nbox = (nkeys + p.BH - 1) / p.BH;
         const int myrow = box_row(t, la0);
         la0 = la1;
@@ -293,7 +293,7 @@ __global__ void __launch_bounds__(kIdxThreads, 2) index_tc_kernel(const __grid_c
     uint32_t aphase = 0;
     int cur_group = -1;
     int64_t soff[G];
-    int nrows = 0, pos0 = 0;
+    int nrows = 0, pos0 = 0, lead = 0;
     for (int it = it0; it < it1 && !*abort_flag; ++it) {
       const IdxItem item = p.items[it];
       if (item.group != cur_group) {
@@ -301,6 +301,7 @@ __global__ void __launch_bounds__(kIdxThreads, 2) index_tc_kernel(const __grid_c
         const IdxGroup g = p.groups[item.group];
         nrows = g.nrows;
         pos0 = g.pos0;
+        lead = g.lead;
         named_bar_sync(1, 32 * kEpiWarps);
         for (int i = et; i < G * HI; i += 32 * kEpiWarps)
           wsm[i] = (i < nrows * HI) ? p.w[static_cast<int64_t>(g.row0) * HI + i] : 0.f;
@@ -313,7 +314,7 @@ __global__ void __launch_bounds__(kIdxThreads, 2) index_tc_kernel(const __grid_c
         // warp-uniform, as the TMEM loads below are warp-collective
         if (!__all_sync(0xffffffffu, mbar_wait(afull(acc), aphase, abort_flag, p.err))) { ok = false; break; }
         tc_fence_after();
-        const int key = t * 128 + m;
+        const int key = t * 128 + m - lead;   // < 0: a slot before the span's token 0
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * C::N;
 #pragma unroll
         for (int gg = 0; gg < G; ++gg) {
@@ -335,7 +336,7 @@ __global__ void __launch_bounds__(kIdxThreads, 2) index_tc_kernel(const __grid_c
                 for (int h = 0; h < 4; ++h) s = fmaf(wsm[gg * HI + h0 + h], fmaxf(v[h], 0.f), s);
               }
             }
-            if (key <= pos0 + gg) p.scores[soff[gg] + key] = s;
+            if (key >= 0 && key <= pos0 + gg) p.scores[soff[gg] + key] = s;
           }
         }
         tc_fence_before();
@@ -380,8 +381,8 @@ __global__ void __launch_bounds__(128) index_simt_kernel(const uint16_t *__restr
     __syncthreads();
     const int pos = g.pos0 + gg;
     for (int t = item.tile0; t < item.tile1; ++t) {
-      const int key = t * 128 + threadIdx.x;
-      if (key > pos) continue;
+      const int key = t * 128 + threadIdx.x - g.lead;
+      if (key < 0 || key > pos) continue;
       const int64_t slot = static_cast<int64_t>(g.page_start) + key;
       const int64_t pi = slot / P;
       int page = -1;
@@ -443,12 +444,8 @@ cudaError_t run_tc(const dsa_ctx *ctx, const dsa_plan_t *plan, const IdxSet &set
   prm.BH = BH;
   prm.num_pages = plan->cache_pages;
   auto kern = index_tc_kernel<HI, DI, G>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> smem_limit_set{0};
+  if (cudaError_t e = ensure_smem_limit(kern, C::SMEM, ctx->device, smem_limit_set); e != cudaSuccess) return e;
   kern<<<set.n_ctas, kIdxThreads, C::SMEM, s>>>(prm);
   return cudaGetLastError();
 }
@@ -464,8 +461,9 @@ cudaError_t run_tc(const dsa_ctx *ctx, const dsa_plan_t *plan, const IdxSet &set
 // the bf16 one.  The epilogue applies the key's scale:
 //     relu(scale * d) = |scale| * relu(sign(scale) * d)
 // so s = |scale| * sum_h w_h relu(+-d_h), one multiply per key instead of one
-// per head (exact for the power-of-two scales the quantiser writes; otherwise
-// a rounding-level reassociation).
+// per head.  For a power-of-two scale the two forms are equal; for any other
+// scale (the quantiser writes amax / 448) they differ by where one fp32
+// rounding falls, a relative difference of order 2^-24 in the score.
 //
 // Warp roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer, warps 2-5
 // epilogue, warps 6-9 converters (thread = key of the tile).
@@ -622,15 +620,15 @@ __global__ void __launch_bounds__(kFp8Threads, 1) index_fp8_tc_kernel(const __gr
         }
         if (__shfl_sync(0xffffffffu, qok ? 1 : 0, 0) == 0) break;
       }
-      const int nkeys_total = g.pos0 + g.nrows;
+      const int nrows_total = g.lead + g.pos0 + g.nrows;  // tile rows: lead rows, then keys 0 .. pos0+nrows-1
       // raw page id of this lane's box of tile t (kNoBox: no box for this lane;
       // -1: past the request's pages), looked up four tiles ahead of its issue
       // (a shift queue in registers) and checked when the tile is issued
       auto box_page = [&](int t) -> int {
-        const int nb = t < item.tile1 ? (min(128, nkeys_total - t * 128) + p.BH - 1) / p.BH : 0;
+        const int nb = t < item.tile1 ? (min(128, nrows_total - t * 128) + p.BH - 1) / p.BH : 0;
         if (lane >= nb) return kNoBox;
-        // (32-bit: a slot is page_start + a position, both non-negative int32)
-        const uint32_t pi = (static_cast<uint32_t>(g.page_start) + static_cast<uint32_t>(t * 128 + lane * p.BH)) /
+        // (32-bit: a slot is the tile's first slot, page_start - lead >= 0, plus a row)
+        const uint32_t pi = (static_cast<uint32_t>(g.page_start - g.lead) + static_cast<uint32_t>(t * 128 + lane * p.BH)) /
                             static_cast<uint32_t>(p.P);
         return pi < static_cast<uint32_t>(g.npages) ? __ldg(p.pages + g.page_off + pi) : -1;
       };
@@ -642,14 +640,14 @@ __global__ void __launch_bounds__(kFp8Threads, 1) index_fp8_tc_kernel(const __gr
           atomicOr(p.err, kErrBounds);
           return -1;
         }
-        slot_out = static_cast<int>((static_cast<uint32_t>(g.page_start) + static_cast<uint32_t>(t * 128 + lane * p.BH)) %
+        slot_out = static_cast<int>((static_cast<uint32_t>(g.page_start - g.lead) + static_cast<uint32_t>(t * 128 + lane * p.BH)) %
                                     static_cast<uint32_t>(p.P));
         return page;
       };
       int lp0 = box_page(item.tile0), lp1 = box_page(item.tile0 + 1), lp2 = box_page(item.tile0 + 2),
           lp3 = box_page(item.tile0 + 3);
       for (int t = item.tile0; t < item.tile1; ++t) {
-        const int nkeys = min(128, nkeys_total - t * 128);
+        const int nkeys = min(128, nrows_total - t * 128);
         const int nbox = (nkeys + p.BH - 1) / p.BH;
         int myslot;
         const int mypage = box_at(t, lp0, myslot);
@@ -740,7 +738,7 @@ __global__ void __launch_bounds__(kFp8Threads, 1) index_fp8_tc_kernel(const __gr
     int sc = 0;
     int cur_group = -1;
     int64_t soff[G];
-    int nrows = 0, pos0 = 0;
+    int nrows = 0, pos0 = 0, lead = 0;
     for (int it = it0; it < it1 && !*abort_flag; ++it) {
       const IdxItem item = p.items[it];
       if (item.group != cur_group) {
@@ -748,6 +746,7 @@ __global__ void __launch_bounds__(kFp8Threads, 1) index_fp8_tc_kernel(const __gr
         const IdxGroup g = p.groups[item.group];
         nrows = g.nrows;
         pos0 = g.pos0;
+        lead = g.lead;
         named_bar_sync(1, 32 * kEpiWarps);
         for (int i = et; i < G * HI; i += 32 * kEpiWarps)
           wsm[i] = (i < nrows * HI) ? p.w[static_cast<int64_t>(g.row0) * HI + i] : 0.f;
@@ -763,7 +762,7 @@ __global__ void __launch_bounds__(kFp8Threads, 1) index_fp8_tc_kernel(const __gr
         const float mag = fabsf(scale);
         const bool neg = scale < 0.f;
         const bool all_pos = __all_sync(0xffffffffu, !neg);
-        const int key = t * 128 + m;
+        const int key = t * 128 + m - lead;   // < 0: a slot before the span's token 0
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * C::N;
 #pragma unroll
         for (int gg = 0; gg < G; ++gg) {
@@ -777,7 +776,7 @@ __global__ void __launch_bounds__(kFp8Threads, 1) index_fp8_tc_kernel(const __gr
             // takes the relu without the sign multiply)
             const float s = all_pos ? weighted_relu_sum<HI>(wsm + gg * HI, v, 1.f)
                                     : weighted_relu_sum<HI>(wsm + gg * HI, v, neg ? -1.f : 1.f);
-            if (key <= pos0 + gg) p.scores[soff[gg] + key] = s * mag;
+            if (key >= 0 && key <= pos0 + gg) p.scores[soff[gg] + key] = s * mag;
           }
         }
         tc_fence_before();
@@ -878,12 +877,8 @@ cudaError_t run_fp8(const dsa_ctx *ctx, const dsa_plan_t *plan, const IdxSet &se
   prm.BH = BH;
   prm.num_pages = plan->cache_pages;
   auto kern = index_fp8_tc_kernel<G>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> smem_limit_set{0};
+  if (cudaError_t e = ensure_smem_limit(kern, C::SMEM, ctx->device, smem_limit_set); e != cudaSuccess) return e;
   kern<<<set.n_ctas, kFp8Threads, C::SMEM, s>>>(prm);
   return cudaGetLastError();
 }

@@ -161,15 +161,15 @@ __global__ void __launch_bounds__(F8qTraits<G>::THREADS, 1) index_f8q_kernel(con
         }
         if (__shfl_sync(0xffffffffu, qok ? 1 : 0, 0) == 0) break;
       }
-      const int nkeys_total = g.pos0 + g.nrows;
+      const int nrows_total = g.lead + g.pos0 + g.nrows;  // tile rows: lead rows, then keys 0 .. pos0+nrows-1
       // raw page id of this lane's box of tile t (kNoBox: no box for this lane;
       // -1: past the request's pages), looked up four tiles ahead of its issue
       // and checked when the tile is issued
       auto box_page = [&](int t) -> int {
-        const int nb = t < item.tile1 ? (min(128, nkeys_total - t * 128) + p.BH - 1) / p.BH : 0;
+        const int nb = t < item.tile1 ? (min(128, nrows_total - t * 128) + p.BH - 1) / p.BH : 0;
         if (lane >= nb) return kNoBox;
-        // (32-bit: a slot is page_start + a position, both non-negative int32)
-        const uint32_t pi = (static_cast<uint32_t>(g.page_start) + static_cast<uint32_t>(t * 128 + lane * p.BH)) /
+        // (32-bit: a slot is the tile's first slot, page_start - lead >= 0, plus a row)
+        const uint32_t pi = (static_cast<uint32_t>(g.page_start - g.lead) + static_cast<uint32_t>(t * 128 + lane * p.BH)) /
                             static_cast<uint32_t>(p.P);
         return pi < static_cast<uint32_t>(g.npages) ? __ldg(p.pages + g.page_off + pi) : -1;
       };
@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(F8qTraits<G>::THREADS, 1) index_f8q_kernel(con
           atomicOr(p.err, kErrBounds);
           return -1;
         }
-        slot_out = static_cast<int>((static_cast<uint32_t>(g.page_start) + static_cast<uint32_t>(t * 128 + lane * p.BH)) %
+        slot_out = static_cast<int>((static_cast<uint32_t>(g.page_start - g.lead) + static_cast<uint32_t>(t * 128 + lane * p.BH)) %
                                     static_cast<uint32_t>(p.P));
         return page;
       };
@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(F8qTraits<G>::THREADS, 1) index_f8q_kernel(con
     uint32_t aphase = 0, ph = 0;
     int cur_group = -1;
     int64_t soff[G];
-    int nrows = 0, pos0 = 0;
+    int nrows = 0, pos0 = 0, lead = 0;
     bool signed_q = false;   // some head of the group has a negative query scale
     for (int it = it0; it < it1 && !*abort_flag; ++it) {
       const IdxItem item = p.items[it];
@@ -287,6 +287,7 @@ __global__ void __launch_bounds__(F8qTraits<G>::THREADS, 1) index_f8q_kernel(con
         const IdxGroup g = p.groups[item.group];
         nrows = g.nrows;
         pos0 = g.pos0;
+        lead = g.lead;
         named_bar_sync(1, 32 * C::EPI);
         bool neg = false;
         for (int i = et; i < G * HI; i += 32 * C::EPI) {
@@ -323,7 +324,7 @@ __global__ void __launch_bounds__(F8qTraits<G>::THREADS, 1) index_f8q_kernel(con
         const float ksign = ks < 0.f ? -1.f : 1.f;
         // the quantiser's scales are >= 0: then relu needs no sign at all
         const bool unsigned_tile = __all_sync(0xffffffffu, ks >= 0.f) && !signed_q;
-        const int key = t * 128 + m;
+        const int key = t * 128 + m - lead;   // < 0: a slot before the span's token 0
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * C::N;
 #pragma unroll
         for (int j = 0; j < C::RPH; ++j) {
@@ -365,7 +366,7 @@ __global__ void __launch_bounds__(F8qTraits<G>::THREADS, 1) index_f8q_kernel(con
                 a3 = fmaf(ww.w, fmaxf(ksign * sg.w * v[h + 3], 0.f), a3);
               }
             }
-            if (key <= pos0 + gg) p.scores[soff[gg] + key] = ((a0 + a1) + (a2 + a3)) * mag;
+            if (key >= 0 && key <= pos0 + gg) p.scores[soff[gg] + key] = ((a0 + a1) + (a2 + a3)) * mag;
           }
         }
         tc_fence_before();
@@ -419,12 +420,8 @@ cudaError_t run_f8q(const dsa_ctx *ctx, const dsa_plan_t *plan, const IdxSet &se
   prm.BH = BH;
   prm.num_pages = plan->cache_pages;
   auto kern = index_f8q_kernel<G>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> smem_limit_set{0};
+  if (cudaError_t e = ensure_smem_limit(kern, C::SMEM, ctx->device, smem_limit_set); e != cudaSuccess) return e;
   kern<<<set.n_ctas, C::THREADS, C::SMEM, s>>>(prm);
   return cudaGetLastError();
 }

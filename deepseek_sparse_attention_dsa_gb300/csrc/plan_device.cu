@@ -36,7 +36,7 @@ struct PlanUpdateParams {
   int64_t num_page_ids;
   int64_t max_scores;
   int32_t max_rows, max_spans, units_cap, combine_cap, idx_cap;
-  int32_t P, align, topk, num_sms;
+  int32_t P, align, topk, num_sms, box_rows;
   int32_t *row_pos, *row_page_off, *row_npages, *row_page_start;
   int64_t *row_score_off;
   IdxGroup *groups;
@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_update_kernel(const PlanUpd
       np = s_np[lo];
       ps = s_ps[lo];
       my_sc += static_cast<int64_t>(pos[k]) + 1;
-      my_tiles += ceil_div(static_cast<int64_t>(pos[k]) + 1, kIndexTile);
+      my_tiles += index_group_tiles(static_cast<int64_t>(pos[k]) + 1, index_tile_lead(ps, p.box_rows));
     }
     p.row_pos[r] = pos[k];
     p.row_page_off[r] = poff;
@@ -186,7 +186,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_update_kernel(const PlanUpd
 #pragma unroll
   for (int k = 0; k < kMaxRowsPerThread; ++k) {
     if (pos[k] < 0) continue;
-    const int32_t tiles = pos[k] / kIndexTile + 1;   // ceil((pos + 1) / 128)
+    const int32_t tiles = index_group_tiles(static_cast<int64_t>(pos[k]) + 1,
+                                            index_tile_lead(p.row_page_start[ra + k], p.box_rows));
     const int u = attention_row_units(pos[k], p.topk, splits);
     my_iu += (static_cast<int64_t>((tiles + tpi - 1) / tpi) << 32) + u;
     my_sm += u > 1 ? ((static_cast<int64_t>(u) << 32) + 1) : 0;
@@ -207,7 +208,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_update_kernel(const PlanUpd
     r_item0[r] = static_cast<int32_t>(iu >> 32);
     if (pos[k] < 0) continue;
     sc += static_cast<int64_t>(pos[k]) + 1;
-    const int32_t tiles = pos[k] / kIndexTile + 1;
+    const int32_t lead = index_tile_lead(p.row_page_start[r], p.box_rows);
+    const int32_t tiles = index_group_tiles(static_cast<int64_t>(pos[k]) + 1, lead);
     // the row is indexer group r (one row per group)
     IdxGroup g;
     g.row0 = r;
@@ -216,8 +218,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_update_kernel(const PlanUpd
     g.page_off = p.row_page_off[r];
     g.npages = p.row_npages[r];
     g.page_start = p.row_page_start[r];
-    g.ntiles = static_cast<int32_t>(tiles);
-    g.pad = 0;
+    g.ntiles = tiles;
+    g.lead = lead;
     p.groups[r] = g;
     int32_t item = static_cast<int32_t>(iu >> 32);
     for (int32_t t0 = 0; t0 < tiles; t0 += tpi, ++item) p.items[item] = IdxItem{r, t0, min(tiles, t0 + tpi), 0};
@@ -305,6 +307,7 @@ cudaError_t launch_plan_update(const dsa_ctx *ctx, dsa_plan_t *plan, const int32
   p.idx_cap = plan->idx[0].n_ctas;
   p.P = ctx->cfg.page_size;
   p.align = plan->page_start_align;
+  p.box_rows = plan->box_rows;
   p.topk = ctx->cfg.topk;
   p.num_sms = ctx->num_sms;
   p.row_pos = plan->row_pos;

@@ -38,10 +38,6 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
-// Arrive on a barrier in another CTA of the cluster (address from mapa).
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
-}
 // Same without release semantics: for a signal that orders nothing but
 // reads the caller has already completed.
 __device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_bar) {
@@ -72,15 +68,18 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 
 // Bounded wait.  `abort_flag` (shared memory) short-circuits every later wait
 // once any role of the CTA has given up; on timeout the error word is set.
+// The kernels use the default limit; dsa_selftest_wait_timeout passes a
+// shorter one to make a wait run out under test.
 template <bool kCluster = false>
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, int *err) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, int *err,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if ((i & 255) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (globaltimer() - t0 > limit_ns) {
         *abort_flag = 1;
         atomicOr(err, kErrTimeout);
         return false;
@@ -144,16 +143,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm,
       "l"(tm), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
 }
-// Gather of four rows (y0..y3) of a 2-D tensor, columns x .. x+box-1, into
-// four consecutive box rows in shared memory (tensor map box height 1).
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *tm, int32_t x, int32_t y0, int32_t y1,
-                                            int32_t y2, int32_t y3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
-      "%3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(tm), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
-      : "memory");
-}
 // Non-blocking test of an mbarrier phase.
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -166,17 +155,7 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Plain bulk copy global -> shared (16-byte aligned addresses, size multiple of 16).
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
-
 // ----------------------------------------------------------------- cp.async
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
 // 16-byte copy that reads `src_bytes` (0 or 16) bytes and zero-fills the rest.
 __device__ __forceinline__ void cp_async_16_zfill(uint32_t dst, const void *src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
@@ -187,15 +166,10 @@ __device__ __forceinline__ void cp_async_16_zfill(uint32_t dst, const void *src,
 __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
-__device__ __forceinline__ void st_shared_zero16(uint32_t dst) {
-  asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0) : "memory");
-}
-
 // ----------------------------------------------------------------- cluster
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -206,17 +180,6 @@ __device__ __forceinline__ uint32_t map_to_cta(uint32_t smem_addr, uint32_t cta)
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(cta));
   return r;
-}
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
-// Asynchronous 16-byte store into another CTA's shared memory whose arrival
-// decrements the tx-count of that CTA's mbarrier (both addresses from mapa).
-__device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, float c, float d, uint32_t remote_bar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
-               "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
-               : "memory");
 }
 // Bulk copy from this CTA's shared memory into another CTA's (dst and bar
 // from mapa); the bytes land on that CTA's mbarrier as transaction bytes.

@@ -386,15 +386,12 @@ __global__ void __launch_bounds__(NT, 1024 / NT) topk_kernel(const float *__rest
 }
 
 template <int NT>
-cudaError_t run_topk(const float *scores, const int64_t *row_score_off, const int32_t *row_pos, int T, int K,
-                     int32_t *sel, int grid, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(topk_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(sizeof(TopkSmem<NT>)));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+cudaError_t run_topk(int device, const float *scores, const int64_t *row_score_off, const int32_t *row_pos, int T,
+                     int K, int32_t *sel, int grid, cudaStream_t s) {
+  static std::atomic<uint64_t> smem_limit_set{0};
+  if (cudaError_t e = ensure_smem_limit(topk_kernel<NT>, static_cast<int>(sizeof(TopkSmem<NT>)), device, smem_limit_set);
+      e != cudaSuccess)
+    return e;
   topk_kernel<NT><<<grid, NT, sizeof(TopkSmem<NT>), s>>>(scores, row_score_off, row_pos, T, K, sel);
   return cudaGetLastError();
 }
@@ -407,9 +404,9 @@ cudaError_t launch_topk(const dsa_ctx *ctx, const dsa_plan_t *plan, const float 
   // CTAs, two per SM, each taking rows in turn
   cudaError_t e;
   if (plan->T <= ctx->num_sms)
-    e = run_topk<1024>(scores, plan->row_score_off, plan->row_pos, plan->T, ctx->cfg.topk, sel, std::max(1, plan->T), s);
+    e = run_topk<1024>(ctx->device, scores, plan->row_score_off, plan->row_pos, plan->T, ctx->cfg.topk, sel, std::max(1, plan->T), s);
   else
-    e = run_topk<512>(scores, plan->row_score_off, plan->row_pos, plan->T, ctx->cfg.topk, sel,
+    e = run_topk<512>(ctx->device, scores, plan->row_score_off, plan->row_pos, plan->T, ctx->cfg.topk, sel,
                       std::min(plan->T, 2 * ctx->num_sms), s);
   *launches += 1;
   return e;

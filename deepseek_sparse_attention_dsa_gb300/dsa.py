@@ -45,7 +45,7 @@ EXPORTED = ["dsa_create", "dsa_destroy", "dsa_plan", "dsa_plan_destroy", "dsa_pl
             "dsa_last_launch_count", "dsa_status_str", "dsa_index_topk_static", "dsa_last_cuda_error",
             "dsa_quantize_store_keys", "dsa_quantize_store_latents", "dsa_attend_shared", "dsa_plan_capturable",
             "dsa_plan_update", "dsa_plan_read_counts", "dsa_quantize_q", "dsa_index_scores_fp8q",
-            "dsa_index_topk_fp8q"]
+            "dsa_index_topk_fp8q", "dsa_selftest_wait_timeout"]
 
 # dsa_device_span_t: q_len, ctx_start, page_start, page_off, num_pages, reserved (int32 each)
 DEVICE_SPAN_FIELDS = 6
@@ -73,7 +73,8 @@ class _Span(ctypes.Structure):
 class PlanInfo(ctypes.Structure):
     _fields_ = [("num_rows", ctypes.c_int32), ("num_spans", ctypes.c_int32), ("needs_selection", ctypes.c_int32),
                 ("index_items", ctypes.c_int32), ("num_scores", ctypes.c_int64), ("attend_units", ctypes.c_int32),
-                ("attend_splits_max", ctypes.c_int32)]
+                ("attend_splits_max", ctypes.c_int32), ("index_tensor_cores", ctypes.c_int32),
+                ("index_box_rows", ctypes.c_int32)]
 
 
 _lib = None
@@ -116,6 +117,7 @@ def load() -> ctypes.CDLL:
     L.dsa_index_scores_fp8q.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
     L.dsa_index_topk_fp8q.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
     L.dsa_get_error.argtypes = [vp, vp]
+    L.dsa_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint64, vp, vp]
     L.dsa_last_launch_count.argtypes = [vp]
     L.dsa_last_launch_count.restype = i32
     L.dsa_last_cuda_error.argtypes = [vp]
@@ -125,7 +127,8 @@ def load() -> ctypes.CDLL:
     for name in ("dsa_create", "dsa_plan", "dsa_plan_get_info", "dsa_store_keys", "dsa_index_topk", "dsa_index_topk_static",
                  "dsa_index_scores", "dsa_topk_from_scores", "dsa_attend", "dsa_get_error", "dsa_quantize_store_keys",
                  "dsa_quantize_store_latents", "dsa_attend_shared", "dsa_plan_capturable", "dsa_plan_update",
-                 "dsa_plan_read_counts", "dsa_quantize_q", "dsa_index_scores_fp8q", "dsa_index_topk_fp8q"):
+                 "dsa_plan_read_counts", "dsa_quantize_q", "dsa_index_scores_fp8q", "dsa_index_topk_fp8q",
+                 "dsa_selftest_wait_timeout"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -192,6 +195,11 @@ class Plan:
     @property
     def num_scores(self) -> int:
         return int(self.info.num_scores)
+
+    @property
+    def index_tensor_cores(self) -> bool:
+        """True when the plan's index scores run on the tensor-core kernels."""
+        return bool(self.info.index_tensor_cores)
 
     def read_counts(self) -> dict:
         """dsa_plan_read_counts (capturable plans; synchronises the device)."""

@@ -28,8 +28,11 @@ Formats (per token, per layer):
                                 each page is [page_size x 128 codes][page_size x fp32]
   * bf16 latent   (1,152 B)   : [kv_lora_rank | rope] bf16
   * fp8 latent    (656 B)     : [512 e4m3 | 4 fp32 scales (one per 128) | 64 bf16 rope]
-fp8 packing uses a power-of-two scale per group, 2^(floor(log2 amax) - 7) (1 when
-amax == 0), and round-to-nearest-even e4m3 codes (torch's float8_e4m3fn cast).
+fp8 packing uses, per group of values, scale = amax / 448 in fp32 (1 when
+amax == 0) and round-to-nearest-even e4m3 codes of x / scale, saturating at
++-448 (torch's float8_e4m3fn cast) -- the rule of the library's quantise-on-
+store.  ``Distributions.fp8_scale = "pow2"`` packs with power-of-two scales
+instead, 2^(floor(log2 amax) - 7), under which code x scale is exact in bf16.
 """
 from __future__ import annotations
 
@@ -182,6 +185,7 @@ class Distributions:
     lat_std: float = 0.5          # MLA latents
     sink_std: float = 1.0
     integer: bool = False         # q, k in {-3..3}, w in {0..3}: exact fp32 scores
+    fp8_scale: str = "amax"       # fp8 rows: "amax" (scale = amax/448) or "pow2" (power-of-two scales)
 
 
 @dataclass
@@ -282,15 +286,25 @@ def _latent_values(wl: Workload, tok: torch.Tensor) -> torch.Tensor:
     return _normal(ids, wl.seed, S_LATENT, wl.dist.lat_std)
 
 
-def _fp8_groups(x: torch.Tensor, group: int):
-    """Per-group e4m3 codes and fp32 scales.  The scale is a power of two,
-    2^(floor(log2 amax) - 7) (1 if amax == 0), so the largest |x| / scale lies in
-    [128, 256) within e4m3's range and every step is exact on any device."""
+def _fp8_groups(x: torch.Tensor, group: int, scale_rule: str = "amax"):
+    """Per-group e4m3 codes and fp32 scales.
+
+    "amax" (the default): scale = amax / 448 in fp32 (1 if amax == 0), codes
+    = e4m3 of the fp32 quotient x / scale, saturating at +-448 -- the same rule
+    as the library's quantise-on-store.  IEEE fp32 division and torch's e4m3
+    cast give the same bytes on the CPU and the GPU.
+    "pow2": scale = 2^(floor(log2 amax) - 7), so the largest |x| / scale lies in
+    [128, 256) and code x scale is exact in bf16 -- an extra exactness case."""
     n, d = x.shape
-    g = x.view(n, d // group, group)
+    g = x.to(torch.float32).view(n, d // group, group)
     amax = g.abs().amax(dim=2)
-    _, e = torch.frexp(amax)                      # amax = m * 2^e, m in [0.5, 1)
-    scale = torch.ldexp(torch.ones_like(amax), (e - 8).to(torch.int32))
+    if scale_rule == "pow2":
+        _, e = torch.frexp(amax)                      # amax = m * 2^e, m in [0.5, 1)
+        scale = torch.ldexp(torch.ones_like(amax), (e - 8).to(torch.int32))
+    elif scale_rule == "amax":
+        scale = amax / torch.tensor(448.0, dtype=torch.float32, device=amax.device)
+    else:
+        raise ValueError("fp8 scale rule %r" % (scale_rule,))
     scale = torch.where(amax > 0, scale, torch.ones_like(amax))
     codes = _to_e4m3_bytes(g / scale.unsqueeze(2)).view(n, d)
     return codes, scale.to(torch.float32)
@@ -302,7 +316,7 @@ def index_rows_bytes(wl: Workload, tok: torch.Tensor) -> torch.Tensor:
     x = _index_key_values(wl, tok)
     if wl.shape.index_fmt == INDEX_BF16:
         return _to_bf16(x)
-    codes, scale = _fp8_groups(x, wl.shape.index_dim)
+    codes, scale = _fp8_groups(x, wl.shape.index_dim, wl.dist.fp8_scale)
     return torch.cat([codes, scale.contiguous().view(torch.uint8).view(-1, 4)], dim=1)
 
 
@@ -313,7 +327,7 @@ def latent_rows_bytes(wl: Workload, tok: torch.Tensor) -> torch.Tensor:
     if sh.latent_fmt == LATENT_BF16:
         return _to_bf16(x)
     L = sh.kv_lora_rank
-    codes, scale = _fp8_groups(x[:, :L].contiguous(), 128)
+    codes, scale = _fp8_groups(x[:, :L].contiguous(), 128, wl.dist.fp8_scale)
     rope = _to_bf16(x[:, L:].contiguous()).view(torch.uint8).view(-1, 2 * sh.rope_dim)
     return torch.cat([codes, scale.contiguous().view(torch.uint8).view(-1, 4 * (L // 128)), rope], dim=1)
 
@@ -437,19 +451,22 @@ def _page_permutation(seed: int, n: int) -> np.ndarray:
 
 
 def build_workload(name: str, shape: DSAShape, requests, seed: int,
-                   dist: Optional[Distributions] = None, page_start: int = 0,
+                   dist: Optional[Distributions] = None, page_start=0,
                    spare_pages: int = 0, permute_pages: bool = True) -> Workload:
-    """requests: list of (ctx_start, q_len).  Each request gets
+    """requests: list of (ctx_start, q_len); page_start: one value for every
+    request or one per request.  Each request gets
     ceil((page_start + ctx_start + q_len) / page_size) pages from a seeded
     permutation of one pool; rows are packed in request order."""
     P = shape.page_size
-    need = [-(-(page_start + c + q) // P) for c, q in requests]
+    starts = [int(page_start)] * len(requests) if np.isscalar(page_start) else [int(x) for x in page_start]
+    assert len(starts) == len(requests)
+    need = [-(-(ps + c + q) // P) for (c, q), ps in zip(requests, starts)]
     total = sum(need) + spare_pages
     perm = _page_permutation(seed, total) if permute_pages else np.arange(total, dtype=np.int32)
     spans, q0, p0, tb = [], 0, 0, 0
-    for i, ((c, q), n) in enumerate(zip(requests, need)):
+    for i, ((c, q), n, ps) in enumerate(zip(requests, need, starts)):
         spans.append(Span(request_id=i, q_start=q0, q_len=q, ctx_start=c,
-                          pages=perm[p0:p0 + n].copy(), page_start=page_start, token_base=tb))
+                          pages=perm[p0:p0 + n].copy(), page_start=ps, token_base=tb))
         q0 += q
         p0 += n
         tb += c + q + 1
@@ -462,7 +479,7 @@ DEEPSEEK = dict(index_heads=64, index_dim=128, topk=2048, heads=128, kv_lora_ran
 CONFIG_NAMES = ["tiny_prefill", "decode", "chunked_prefill", "long_decode", "mixed_fp8"]
 
 
-def config(i: int, seed: Optional[int] = None) -> Workload:
+def config(i: int, seed: Optional[int] = None, page_start=0) -> Workload:
     """The five evaluation workloads (seed defaults to 1000 + i).
 
     0 tiny_prefill    2 requests, contexts 256 / 384, every row queried; indexer 4x32,
@@ -472,6 +489,9 @@ def config(i: int, seed: Optional[int] = None) -> Workload:
     3 long_decode     128 requests x 1 row, contexts ~U[65536, 131072].
     4 mixed_fp8       16 decode rows (contexts ~U[8192, 32768]) + two 2048-row chunks
                       ending at 4096 and 12288; fp8 656-B latents, 132-B index rows, sinks.
+
+    page_start (0 in the evaluation workloads) moves every request's token 0 to
+    that slot of its first page.
     """
     seed = 1000 + i if seed is None else seed
     name = CONFIG_NAMES[i]
@@ -479,21 +499,21 @@ def config(i: int, seed: Optional[int] = None) -> Workload:
         sh = DSAShape(index_heads=4, index_dim=32, topk=64, heads=8, kv_lora_rank=64, rope_dim=16,
                       page_size=16, sm_scale=1.0 / math.sqrt(80.0))
         return build_workload(name, sh, [(0, 256), (0, 384)], seed,
-                              Distributions(w=("uniform", 0.0, 1.0)))
+                              Distributions(w=("uniform", 0.0, 1.0)), page_start=page_start)
     if i == 1:
         ctx = _uniform_ints(seed, S_CTX, 32, 4096, 16384)
         return build_workload(name, DSAShape(**DEEPSEEK), [(int(c) - 1, 1) for c in ctx], seed,
-                              Distributions(w=("uniform", 0.0, 1.0 / 8)))
+                              Distributions(w=("uniform", 0.0, 1.0 / 8)), page_start=page_start)
     if i == 2:
         return build_workload(name, DSAShape(**DEEPSEEK), [(8192, 8192)], seed,
-                              Distributions(w=("normal", 1.0)))
+                              Distributions(w=("normal", 1.0)), page_start=page_start)
     if i == 3:
         ctx = _uniform_ints(seed, S_CTX, 128, 65536, 131072)
         return build_workload(name, DSAShape(**DEEPSEEK), [(int(c) - 1, 1) for c in ctx], seed,
-                              Distributions(w=("uniform", 0.0, 1.0 / 8)))
+                              Distributions(w=("uniform", 0.0, 1.0 / 8)), page_start=page_start)
     if i == 4:
         sh = DSAShape(**DEEPSEEK, latent_fmt=LATENT_FP8_656, index_fmt=INDEX_FP8_132, has_sink=True)
         ctx = _uniform_ints(seed, S_CTX, 16, 8192, 32768)
         reqs = [(int(c) - 1, 1) for c in ctx] + [(2048, 2048), (10240, 2048)]
-        return build_workload(name, sh, reqs, seed, Distributions(w=("uniform", 0.0, 1.0 / 8)))
+        return build_workload(name, sh, reqs, seed, Distributions(w=("uniform", 0.0, 1.0 / 8)), page_start=page_start)
     raise ValueError(i)

@@ -104,6 +104,9 @@ typedef struct dsa_plan_info {
   int64_t num_scores;        /* sum over rows of pos(r)+1: the score scratch length */
   int32_t attend_units;      /* attention work units (row x key split) */
   int32_t attend_splits_max; /* largest key split count of any row */
+  int32_t index_tensor_cores;/* 1 when the plan's index scores run on the tensor-core kernels (any
+                                page_start, page_size a multiple of 8), 0 for the CUDA-core kernel */
+  int32_t index_box_rows;    /* height of the indexer's TMA key boxes (a power of two dividing page_size) */
 } dsa_plan_info_t;
 
 /* Create a context on CUDA device `device` (>= 0).  device = -1 creates a
@@ -210,14 +213,15 @@ dsa_status dsa_attend_shared(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void 
  * allocation while serving).  The pages have no counterpart to this call.
  * Same arguments, results and errors as dsa_index_topk, but the fp32 scores
  * live in a fixed array inside the library (DSA_STATIC_SCORES_MAX floats,
- * 16 MiB, present on every GPU that loads the library until the process
- * exits) instead of the context's scratch; the call itself allocates nothing.
- * A plan with more than DSA_STATIC_SCORES_MAX scores (the sum over rows of
- * pos+1) is rejected with DSA_ERR_SCRATCH_LIMIT before anything runs.  The
- * first call on a device looks up the array's device address
- * (cudaGetSymbolAddress); make that first call before any stream capture.
- * All calls share the array: calls whose kernels overlap on the GPU race and
- * must be serialised by the caller. */
+ * 16 MiB) instead of the context's scratch; the call itself allocates
+ * nothing.  The array is taken on a GPU when the first context on it is
+ * created: dsa_create looks up its device address (cudaGetSymbolAddress),
+ * which loads the module holding it even under lazy module loading, and it
+ * stays until the process exits.  A plan with more than
+ * DSA_STATIC_SCORES_MAX scores (the sum over rows of pos+1) is rejected with
+ * DSA_ERR_SCRATCH_LIMIT before anything runs.  All calls share the array:
+ * calls whose kernels overlap on the GPU race and must be serialised by the
+ * caller. */
 #define DSA_STATIC_SCORES_MAX (4 * 1024 * 1024)
 enum { DSA_ERR_SCRATCH_LIMIT = 8 };
 dsa_status dsa_index_topk_static(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *q, const float *w,
@@ -242,9 +246,8 @@ dsa_status dsa_index_topk_static(dsa_ctx_t *ctx, const dsa_plan_t *plan, const v
  *   dsa_index_topk with (q_codes, q_scale) in place of q (q_scale may have
  *   any sign; the quantiser writes scales >= 0).
  * Device pointers, caller-owned.  DSA_ERR_UNSUPPORTED for other index formats
- * or shapes, a page size that is not a multiple of 8, or spans whose
- * page_start leaves fewer than 8 rows of a page contiguous (the host planner's
- * key-box height); DSA_ERR_INVALID_ARG for null pointers. */
+ * or shapes, or a page size that is not a multiple of 8 (any page_start is
+ * accepted); DSA_ERR_INVALID_ARG for null pointers. */
 dsa_status dsa_quantize_q(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *q_bf16, void *q_codes, float *q_scale,
                           dsa_stream_t stream);
 dsa_status dsa_index_scores_fp8q(dsa_ctx_t *ctx, const dsa_plan_t *plan, const void *q_codes, const float *q_scale,
@@ -263,8 +266,9 @@ dsa_status dsa_index_topk_fp8q(dsa_ctx_t *ctx, const dsa_plan_t *plan, const voi
  * dsa_plan_capturable allocates a plan for at most max_rows (<= 8192) rows in
  * at most max_spans (<= 4096) spans whose rows score at most max_scores keys
  * in total (the sum over rows of pos+1), with every span's page_start a
- * multiple of page_start_align (>= 1); the device planner is one CTA that
- * holds the spans and rows in shared memory.  The plan owns its metadata and score/partial
+ * multiple of page_start_align (>= 1; a validation constraint only, the
+ * kernels take any page_start); the device planner is one CTA that holds
+ * the spans and rows in shared memory.  The plan owns its metadata and score/partial
  * scratch (plain cudaMalloc, so a captured graph may keep pointing at them)
  * and starts empty.  dsa_plan_update recomputes it ON THE DEVICE, enqueued
  * on `stream`, from spans in device memory:
@@ -327,6 +331,20 @@ dsa_status dsa_plan_read_counts(const dsa_plan_t *plan, int32_t counts[8]);
  * Returns DSA_OK, DSA_ERR_BOUNDS, DSA_ERR_TIMEOUT, DSA_ERR_BAD_SPANS or
  * DSA_ERR_CUDA. */
 dsa_status dsa_get_error(dsa_ctx_t *ctx, dsa_stream_t stream);
+
+/* Drive the pipeline's bounded wait to its limit, for testing the failure
+ * path (mstar IndexKeyStore.history: a failure is reported to the caller, not
+ * fatal).  One CTA takes tensor memory, waits on an mbarrier that nothing
+ * arrives on with a limit of limit_ns nanoseconds (the kernels' own limit is
+ * one second), then waits on it again, frees the tensor memory and exits.
+ * result: DEVICE int64[5], caller-owned: [0] 1 if the first wait succeeded,
+ * [1] its duration in ns, [2] 1 if the second wait succeeded, [3] its
+ * duration in ns, [4] the CTA's abort flag at the end.  Expected: the first
+ * wait gives up after about limit_ns and sets DSA_ERR_TIMEOUT in the error
+ * word (read by dsa_get_error), the abort flag it raises ends the second wait
+ * at once, and the context stays usable.  DSA_ERR_INVALID_ARG for a
+ * host-only context, a null result or limit_ns outside 1 .. 1e9. */
+dsa_status dsa_selftest_wait_timeout(dsa_ctx_t *ctx, uint64_t limit_ns, int64_t *result, dsa_stream_t stream);
 
 /* Number of kernels the last compute call on this context launched (for
  * accounting; host-side counter, no synchronisation). */

@@ -131,3 +131,21 @@ def test_capturable_plan_calls_refuse_host_only_context_and_host_plans(lib):
     assert L.dsa_plan_update(ctx.handle, plan.handle, None, None, None, 0, None) == 1
     counts = (ctypes.c_int32 * 8)()
     assert L.dsa_plan_read_counts(plan.handle, ctypes.byref(counts)) == 1   # a host plan has no device counts
+
+
+def test_indexer_stays_on_tensor_cores_for_any_page_start(lib):
+    """Key tiles start on the box boundary below a span's page_start, so the
+    box height depends on the page size only and any page_start keeps the
+    tensor-core indexer; a page size that is not a multiple of 8 cannot."""
+    ctx = _host_ctx()
+    pg = np.arange(8, dtype=np.int32)
+    for ps in (0, 1, 3, 37, 63, 64, 70):
+        plan = ctx.plan([S(0, 1, 200, pg[:6], page_start=ps), S(1, 5, 9, pg[6:8], page_start=(ps * 7) % 64)],
+                        cache_pages=8)
+        assert plan.info.index_box_rows == 64 and plan.index_tensor_cores, ps
+    tiny = W.config(0)
+    plan = _host_ctx(tiny.shape).plan([S(0, 2, 0, np.arange(2, dtype=np.int32), page_start=5)], cache_pages=2)
+    assert plan.info.index_box_rows == 16 and plan.index_tensor_cores
+    small_pages = W.DSAShape(**dict(W.DEEPSEEK, page_size=4))
+    plan = _host_ctx(small_pages).plan([S(0, 1, 10, np.arange(3, dtype=np.int32), page_start=1)], cache_pages=3)
+    assert plan.info.index_box_rows == 4 and not plan.index_tensor_cores

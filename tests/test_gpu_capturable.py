@@ -116,6 +116,44 @@ def test_chunk_rows_match_the_oracle():
     assert plan.read_counts()["split_rows"] >= 0
 
 
+@pytest.mark.parametrize("fp8", [False, True])
+def test_odd_page_starts_match_the_oracle(fp8):
+    """A capturable plan with alignment 1 and spans starting at slots 3, 37 and
+    61 (bf16 and fp8 keys): the device planner gives the same tile leads as the
+    host planner, the indexer stays on the tensor cores, and scores,
+    selection and attention match the oracle."""
+    wl = H.deepseek_small(seed=27 + fp8, fp8=fp8, sink=fp8, page_start=[3, 37, 61],
+                          decode_ctx=(2500, 5000, 700), chunk=None)
+    ic, lc, st = H.host_inputs(wl)
+    ref = oracle.run_all(wl, ic, lc, st)
+    ctx = dsa.Context(wl.shape, 0)
+    R = wl.num_rows + 2
+    max_scores = int(ref["offsets"][-1]) + 3000
+    plan = ctx.plan_capturable(R, 4, max_scores, wl.num_pages)   # page_start_align 1
+    assert plan.index_tensor_cores
+    ns, spans, pages = _device_spans(wl, 4)
+    ctx.plan_update(plan, ns, spans, pages)
+    icd, lcd = ic.clone().cuda(), lc.cuda()
+    ctx.store_keys(plan, _padded(st.keys, R), icd)
+    scores = torch.zeros(max_scores, dtype=torch.float32, device="cuda")
+    ctx.index_scores(plan, _padded(st.q, R), _padded(st.w, R), icd, scores=scores)
+    sel = ctx.index_topk(plan, _padded(st.q, R), _padded(st.w, R), icd)
+    sink = st.sink.cuda() if st.sink is not None else None
+    out = ctx.attend(plan, sel, _padded(st.q_nope, R), _padded(st.q_pe, R), lcd, sink, wl.shape.sm_scale)
+    ctx.get_error()
+    T = wl.num_rows
+    n = int(ref["offsets"][-1])
+    H.check_scores(scores[:n].cpu().numpy(), ref["scores"], ref["offsets"])
+    H.check_selection(sel[:T].cpu().numpy(), ref["selection"], ref["scores"], ref["offsets"], wl.shape.topk)
+    ref_e2e = oracle.attend(wl.shape, wl.spans, wl.num_pages, sel[:T].cpu().numpy(), st.q_nope, st.q_pe, lc, st.sink)
+    H.check_attention(out[:T].float().cpu().numpy(), ref_e2e, fp8)
+    # the host plan of the same step gives bit-identical decode scores
+    hplan = ctx.plan(wl.spans, wl.num_pages)
+    hs = ctx.index_scores(hplan, st.q.cuda(), st.w.cuda(), icd)
+    ctx.get_error()
+    assert torch.equal(hs[:n].cpu(), scores[:n].cpu())
+
+
 def test_graph_replay_follows_the_spans_in_device_memory():
     """Capture update + store + index/top-k + attend once; replay it for two
     different decode steps (other contexts, fewer requests) whose spans, pages,

@@ -22,15 +22,24 @@ def built():
     build.build()
 
 
-def _sample_rows(wl, n_decode, n_prefill, seed):
+def _sample_rows(wl, n_decode, n_random_per_residue, seed):
+    """Decode rows drawn at random; for every prefill chunk its first four and
+    last four rows and `n_random_per_residue` random rows of each residue mod 4
+    (the indexer scores chunk rows in groups of four, one TMEM column block per
+    row of the group, so every slot of a group is checked)."""
     rng = np.random.default_rng(seed)
     dec = [i for i, s in enumerate(wl.spans) if s.q_len == 1]
     pre = [i for i, s in enumerate(wl.spans) if s.q_len > 1]
     rows = [(int(i), 0) for i in rng.choice(dec, size=min(n_decode, len(dec)), replace=False)] if dec else []
-    for k in range(n_prefill if pre else 0):
-        i = pre[k % len(pre)]
+    for i in pre:
         q_len = wl.spans[i].q_len
-        rows.append((i, int([0, q_len - 1, rng.integers(0, q_len)][k % 3])))
+        picked = set(range(min(4, q_len))) | set(range(max(0, q_len - 4), q_len))
+        for res in range(4):
+            cand = np.arange(res, q_len, 4)
+            if len(cand):
+                picked |= set(int(x) for x in rng.choice(cand, size=min(n_random_per_residue, len(cand)),
+                                                         replace=False))
+        rows += [(i, r) for r in sorted(picked)]
     return rows
 
 
@@ -53,7 +62,7 @@ def _captured(ctx, wl, ic, lc, st):
     return sel, out
 
 
-def _check_workload(idx, n_decode, n_prefill):
+def _check_workload(idx, n_decode, n_random_per_residue):
     wl = W.config(idx)
     sh = wl.shape
     dev = torch.device("cuda", 0)
@@ -85,7 +94,7 @@ def _check_workload(idx, n_decode, n_prefill):
     off_all = np.zeros(wl.num_rows + 1, np.int64)
     np.cumsum(pos_all + 1, out=off_all[1:])
     fp8 = sh.latent_fmt == W.LATENT_FP8_656
-    for span_i, r_in in _sample_rows(wl, n_decode, n_prefill, seed=idx):
+    for span_i, r_in in _sample_rows(wl, n_decode, n_random_per_residue, seed=idx):
         row = wl.spans[span_i].q_start + r_in
         rw = wl.row_workload(span_i, r_in)
         ric = W.make_index_cache(rw)
@@ -114,16 +123,18 @@ def _check_workload(idx, n_decode, n_prefill):
 
 
 def test_decode_full_size():
-    _check_workload(1, n_decode=3, n_prefill=0)
+    _check_workload(1, n_decode=16, n_random_per_residue=0)
 
 
 def test_chunked_prefill_full_size():
-    _check_workload(2, n_decode=0, n_prefill=3)
+    _check_workload(2, n_decode=0, n_random_per_residue=2)
 
 
 def test_long_decode_full_size():
-    _check_workload(3, n_decode=2, n_prefill=0)
+    _check_workload(3, n_decode=16, n_random_per_residue=0)
 
 
 def test_mixed_fp8_full_size():
-    _check_workload(4, n_decode=2, n_prefill=3)
+    """The mixed step over fp8 caches whose scales follow the quantise-on-store
+    rule (amax / 448): 16 decode rows and 12 rows of each chunk."""
+    _check_workload(4, n_decode=16, n_random_per_residue=1)

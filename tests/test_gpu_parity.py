@@ -105,6 +105,29 @@ def test_fp8_formats():
     _run(H.deepseek_small(seed=5, fp8=True, sink=True, decode_ctx=(2200, 2900), chunk=(2030, 24)))
 
 
+@pytest.mark.parametrize("fp8", [False, True])
+def test_any_page_start_stays_on_tensor_cores(fp8):
+    """Spans whose token 0 sits at any slot of a page (page_start 3, 37, 0, 61
+    and 70, which also skips the first page's start): key tiles start on the
+    box boundary below page_start, the epilogue drops the rows before token 0,
+    and the plan keeps the tensor-core indexer (bf16 and fp8 keys)."""
+    wl = H.deepseek_small(seed=50 + fp8, fp8=fp8, sink=fp8, page_start=[3, 37, 0, 61, 70],
+                          decode_ctx=(2049, 130, 4097, 700), chunk=(1990, 70))
+    ctx, ref, got = _run(wl)
+    plan = ctx.plan(wl.spans, wl.num_pages)
+    assert plan.index_tensor_cores and plan.info.index_box_rows == 64
+    plan.close()
+
+
+def test_fp8_power_of_two_scales():
+    """An extra exactness case: fp8 rows packed with power-of-two scales, under
+    which the attention producers' code x scale is exact in bf16 and the fp8-key
+    epilogue's factored scale is exact; the tolerances are the same."""
+    wl = H.deepseek_small(seed=6, fp8=True, sink=True, decode_ctx=(2200, 2900), chunk=(2030, 24))
+    wl.dist = W.Distributions(w=("uniform", 0.0, 0.125), fp8_scale="pow2")
+    _run(wl)
+
+
 def test_fp8_page_start_ragged():
     """fp8 keys and latents with spans starting mid-page, a context shorter than
     one key tile and chunks whose tails leave partial tiles and groups."""

@@ -3,7 +3,9 @@ memory while serving (their process reserves HBM up front in its own pool).
 Its scores live in the library's fixed device array instead of the context's
 scratch.  Checked through the C ABI against dsa_index_topk on two calls in a
 row (a larger step, then a smaller one that reuses the array's stale
-contents), and the size limit is checked.  Collected last on purpose."""
+contents) and on a third, larger step, with the device's free memory
+unchanged around the calls; the size limit is checked too.  Collected last on
+purpose."""
 import ctypes
 
 import numpy as np
@@ -31,19 +33,31 @@ def _call_static(ctx, plan, q, w, cache, sel):
 
 
 def test_static_entry_matches_index_topk_twice():
+    """Two calls in a row (the second over the first's stale scores), then a
+    third on a larger plan; each must equal dsa_index_topk.  Around the calls
+    after the first, the device's free memory must not move: the entry point
+    makes the driver allocate nothing (its array was taken by dsa_create)."""
     sh = W.DSAShape(**W.DEEPSEEK)
     ctx = dsa.Context(sh, 0)
     first = H.deepseek_small(seed=31, decode_ctx=(9000, 4100, 2500), chunk=(2100, 36))
     second = H.deepseek_small(seed=32, decode_ctx=(3000,), chunk=(1500, 8))
-    for wl in (first, second):
+    third = H.deepseek_small(seed=33, decode_ctx=(12000, 7000, 5000, 300), chunk=(3000, 40))
+    for i, wl in enumerate((first, second, third)):
         ic, _, st = H.device_inputs(wl)
         plan = ctx.plan(wl.spans, wl.num_pages)
         ctx.store_keys(plan, st.keys, ic)
+        # the regular call first: it loads every kernel the static call uses
         ref = ctx.index_topk(plan, st.q, st.w, ic)
         got = torch.full_like(ref, -7)
+        torch.cuda.synchronize()
+        free_before = torch.cuda.mem_get_info()[0]
         assert _call_static(ctx, plan, st.q, st.w, ic, got) == dsa.DSA_OK
+        torch.cuda.synchronize()
+        free_after = torch.cuda.mem_get_info()[0]
         ctx.get_error()
         assert torch.equal(got, ref)
+        if i > 0:
+            assert free_after == free_before, "the static entry point changed the device's free memory"
         plan.close()
 
 
