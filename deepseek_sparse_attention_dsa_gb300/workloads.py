@@ -51,7 +51,7 @@ INDEX_FP8_132 = 1
 _M32 = 0xFFFFFFFF
 
 # stream ids: one independent random stream per kind of tensor
-S_INDEX_KEY, S_LATENT, S_Q, S_W, S_QNOPE, S_QPE, S_SINK, S_CTX, S_PAGES = range(1, 10)
+S_INDEX_KEY, S_LATENT, S_Q, S_W, S_QNOPE, S_QPE, S_SINK, S_CTX, S_PAGES, S_KV, S_MSA_Q = range(1, 12)
 
 
 # ----------------------------------------------------------------------------
@@ -159,6 +159,42 @@ class DSAShape:
 
 
 @dataclass
+class MSAShape:
+    """Block-sparse MSA (LLMServingSim, "Sparse attention (DSA and block-sparse
+    MSA)", MiniMax-M3 column): the top ``topk_blocks`` blocks of
+    ``block_size`` tokens per row, over plain GQA (``q_heads`` query heads
+    sharing ``kv_heads`` key/value heads of ``head_dim``), with one bf16 index
+    vector of ``index_dim`` per token.  The pages fix 16 blocks of 128 tokens,
+    a bf16 index vector, and 2 x kv_heads x head_dim x 2 = 2,048 bytes of K and
+    V per token (kv_heads x head_dim = 512); the 4 x 128 split, 64 query heads
+    and the 64-head indexer query are readings."""
+    index_heads: int = 64
+    index_dim: int = 128
+    page_size: int = 64
+    block_size: int = 128
+    topk_blocks: int = 16
+    q_heads: int = 64
+    kv_heads: int = 4
+    head_dim: int = 128
+    sm_scale: float = 1.0 / math.sqrt(128.0)
+
+    @property
+    def kv_row_elems(self) -> int:
+        return 2 * self.kv_heads * self.head_dim
+
+    @property
+    def kv_row_bytes(self) -> int:
+        return 2 * self.kv_row_elems
+
+    def index_shape(self) -> "DSAShape":
+        """The token-level indexer as a DSAShape (index fields and page size;
+        the MLA fields stand in and are not read by the MSA calls)."""
+        return DSAShape(index_heads=self.index_heads, index_dim=self.index_dim,
+                        topk=self.block_size * self.topk_blocks, heads=self.q_heads, kv_lora_rank=self.head_dim,
+                        rope_dim=0, page_size=self.page_size, sm_scale=self.sm_scale)
+
+
+@dataclass
 class Span:
     """One request's rows of a step: q_len rows from row q_start, the first at
     position ctx_start; ``pages`` are its cache pages and ``page_start`` the slot
@@ -196,6 +232,7 @@ class Workload:
     num_pages: int
     seed: int
     dist: Distributions = field(default_factory=Distributions)
+    msa: Optional[MSAShape] = None   # set for block-sparse MSA workloads
 
     @property
     def num_rows(self) -> int:
@@ -247,7 +284,7 @@ class Workload:
         s = self.spans[span_index]
         sp = replace(s, q_start=0, q_len=1, ctx_start=s.ctx_start + row_in_span,
                      pages=np.arange(len(s.pages), dtype=np.int32))
-        return Workload(self.name + "/row", self.shape, [sp], len(s.pages), self.seed, self.dist)
+        return Workload(self.name + "/row", self.shape, [sp], len(s.pages), self.seed, self.dist, self.msa)
 
     def sub_workload(self, span_indices) -> "Workload":
         """A workload holding only the given spans, re-packed from row 0 with
@@ -260,7 +297,7 @@ class Workload:
             spans.append(replace(s, q_start=q0, pages=np.arange(pbase, pbase + npg, dtype=np.int32)))
             q0 += s.q_len
             pbase += npg
-        return Workload(self.name + "/sub", self.shape, spans, pbase, self.seed, self.dist)
+        return Workload(self.name + "/sub", self.shape, spans, pbase, self.seed, self.dist, self.msa)
 
 
 # ----------------------------------------------------------------------------
@@ -437,6 +474,45 @@ def make_step_inputs(wl: Workload, device="cpu") -> StepInputs:
     )
 
 
+def kv_rows(wl: Workload, tok: torch.Tensor) -> torch.Tensor:
+    """GQA key/value rows of the given tokens: (n, 2 * kv_heads * head_dim)
+    bf16, [K of kv heads 0..kv_heads-1 | V of the same heads], ~N(0, lat_std)."""
+    width = wl.msa.kv_row_elems
+    ids = tok.view(-1, 1) * width + torch.arange(width, device=tok.device).view(1, -1)
+    return _to_bf16(_normal(ids, wl.seed, S_KV, wl.dist.lat_std))
+
+
+def make_kv_cache(wl: Workload, device="cpu", chunk_rows: int = 1 << 18, tokens=None) -> torch.Tensor:
+    """The paged GQA cache of an MSA workload, [num_pages, page_size,
+    2 * kv_heads * head_dim] bf16, with every position < ctx_end written.
+    ``tokens``: optional logical ids; only those rows are filled."""
+    P = wl.shape.page_size
+    m = wl.slot_token_map()
+    if tokens is not None:
+        keep = np.isin(m, np.asarray(sorted(tokens), dtype=np.int64))
+        m[~keep] = -1
+    nrows = wl.num_pages * P
+    out = torch.zeros(nrows, wl.msa.kv_row_elems, dtype=torch.bfloat16, device=device)
+    for a, b in _chunks(nrows, chunk_rows):
+        sel = np.nonzero(m[a:b] >= 0)[0]
+        if len(sel) == 0:
+            continue
+        rows = torch.from_numpy(sel + a).to(device)
+        tok = torch.from_numpy(m[a:b][sel]).to(device)
+        out[rows] = kv_rows(wl, tok)
+    return out.view(wl.num_pages, P, -1)
+
+
+def make_msa_q(wl: Workload, device="cpu") -> torch.Tensor:
+    """GQA queries of an MSA workload, (T, q_heads, head_dim) bf16 ~N(0, qn_std)."""
+    ms = wl.msa
+    _, _, tok_np = wl.row_table()
+    tok = torch.from_numpy(tok_np).to(device)
+    width = ms.q_heads * ms.head_dim
+    ids = tok.view(-1, 1) * width + torch.arange(width, device=device).view(1, -1)
+    return _to_bf16(_normal(ids, wl.seed, S_MSA_Q, wl.dist.qn_std)).view(len(tok_np), ms.q_heads, ms.head_dim)
+
+
 # ----------------------------------------------------------------------------
 # workloads
 # ----------------------------------------------------------------------------
@@ -517,3 +593,37 @@ def config(i: int, seed: Optional[int] = None, page_start=0) -> Workload:
         reqs = [(int(c) - 1, 1) for c in ctx] + [(2048, 2048), (10240, 2048)]
         return build_workload(name, sh, reqs, seed, Distributions(w=("uniform", 0.0, 1.0 / 8)), page_start=page_start)
     raise ValueError(i)
+
+
+MSA_CONFIG_NAMES = ["msa_small", "msa_decode", "msa_prefill"]
+
+
+def msa_config(name: str, seed: Optional[int] = None, page_start=0) -> Workload:
+    """Block-sparse MSA workloads (the pages give no MSA workload; these mirror
+    the DSA ones at the MiniMax-M3 selection shape, top 16 blocks of 128):
+
+    msa_small    3 requests: decode rows at contexts 1500 and 700 and a 96-row
+                 chunk at positions 1024..1119; top 4 blocks of 128, 8 query
+                 heads over 2 kv heads (selection spans several blocks, the
+                 oracle runs in seconds).
+    msa_decode   128 requests x 1 row, contexts ~U[65536, 131072]; top 16
+                 blocks of 128, 64 query heads over 4 kv heads of 128.
+    msa_prefill  1 request, 8192 cached + 8192 new rows; shapes as msa_decode.
+    Index keys and queries as the DSA workloads (indexer 64 x 128 bf16); K, V
+    ~N(0, 0.5), GQA queries ~N(0, 1)."""
+    i = MSA_CONFIG_NAMES.index(name)
+    seed = 2000 + i if seed is None else seed
+    if name == "msa_small":
+        ms = MSAShape(topk_blocks=4, q_heads=8, kv_heads=2)
+        reqs = [(1499, 1), (699, 1), (1024, 96)]
+    elif name == "msa_decode":
+        ms = MSAShape()
+        ctx = _uniform_ints(seed, S_CTX, 128, 65536, 131072)
+        reqs = [(int(c) - 1, 1) for c in ctx]
+    else:
+        ms = MSAShape()
+        reqs = [(8192, 8192)]
+    wl = build_workload(name, ms.index_shape(), reqs, seed, Distributions(w=("uniform", 0.0, 1.0 / 8)),
+                        page_start=page_start)
+    wl.msa = ms
+    return wl

@@ -21,6 +21,9 @@ Functions (all return numpy arrays):
   e4m3_values(codes)                                    -> float64 values of e4m3 bytes
   e4m3_encode(values)                                   -> e4m3 codes of fp32 values
   quantize_store_keys / quantize_store_latents          -> caches with this step's bf16 rows quantised
+  msa_block_scores(msa, spans, scores, offsets)         -> (block scores fp32, block offsets)
+  msa_select(msa, spans, block_scores, block_offsets)   -> (T, topk_blocks) int32 block ids, -1 padded
+  msa_attend(msa, spans, num_pages, sel, q, kv_cache)   -> (T, q_heads, head_dim) float64
 
 Parity status of each function is recorded in the docstring of each test in
 tests/test_oracle_pins.py.
@@ -75,6 +78,11 @@ def lib():
         L.oracle_attend.argtypes = [ctypes.POINTER(_Rows), ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                     ctypes.c_double, ctypes.c_void_p]
+        L.oracle_msa_block_scores.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                              ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+        L.oracle_msa_attend.argtypes = [ctypes.POINTER(_Rows), ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                        ctypes.c_double, ctypes.c_void_p]
         L.oracle_set_num_threads.argtypes = [ctypes.c_int]
         L.oracle_max_threads.restype = ctypes.c_int
         _lib = L
@@ -260,3 +268,64 @@ def run_all(wl, index_cache, latent_cache, step):
     sel = topk(sh, wl.spans, scores, off)
     out = attend(sh, wl.spans, wl.num_pages, sel, step.q_nope, step.q_pe, latent_cache, step.sink)
     return dict(index_cache=cache, scores=scores, offsets=off, selection=sel, out=out)
+
+
+# ----------------------------------------------------------------------------
+# block-sparse MSA (LLMServingSim, "Sparse attention (DSA and block-sparse
+# MSA)", MiniMax-M3 column)
+# ----------------------------------------------------------------------------
+def msa_block_offsets(spans, block_size: int) -> np.ndarray:
+    rt = RowTable(spans, 1, 1)
+    off = np.zeros(rt.T + 1, np.int64)
+    np.cumsum(rt.pos // int(block_size) + 1, out=off[1:])
+    return off
+
+
+def msa_block_scores(msa, spans, scores, offsets):
+    """Largest token score of each block of block_size positions the row sees."""
+    rt = RowTable(spans, 1, 1)
+    sc = np.ascontiguousarray(scores, dtype=np.float32)
+    off = np.ascontiguousarray(offsets, dtype=np.int64)
+    boff = msa_block_offsets(spans, msa.block_size)
+    bs = np.zeros(int(boff[-1]), np.float32)
+    _check(lib().oracle_msa_block_scores(rt.T, int(msa.block_size), rt.pos.ctypes.data, sc.ctypes.data,
+                                         off.ctypes.data, boff.ctypes.data, bs.ctypes.data))
+    return bs, boff
+
+
+def msa_select(msa, spans, block_scores, block_offsets) -> np.ndarray:
+    """The causal top-k of the DSA selection, over a row's blocks: the
+    topk_blocks highest block scores, ties to the lower block, -1 padded."""
+    rt = RowTable(spans, 1, 1)
+    last = np.ascontiguousarray(rt.pos // int(msa.block_size), dtype=np.int64)   # the row's last block
+    bs = np.ascontiguousarray(block_scores, dtype=np.float32)
+    boff = np.ascontiguousarray(block_offsets, dtype=np.int64)
+    sel = np.empty((rt.T, int(msa.topk_blocks)), np.int32)
+    _check(lib().oracle_topk(rt.T, int(msa.topk_blocks), last.ctypes.data, bs.ctypes.data, boff.ctypes.data,
+                             sel.ctypes.data))
+    return sel
+
+
+def msa_attend(msa, spans, num_pages, sel, q, kv_cache) -> np.ndarray:
+    """GQA attention over the visible positions of the selected blocks."""
+    rt = RowTable(spans, msa.page_size, num_pages)
+    s = _np(sel, np.int32)
+    qa = _np(q).view(np.uint16)
+    ca = _np(kv_cache).view(np.uint8)
+    out = np.zeros((rt.T, int(msa.q_heads), int(msa.head_dim)), np.float64)
+    _check(lib().oracle_msa_attend(ctypes.byref(rt.struct), int(msa.q_heads), int(msa.kv_heads), int(msa.head_dim),
+                                   int(msa.block_size), int(s.shape[1]), s.ctypes.data, qa.ctypes.data,
+                                   ca.ctypes.data, float(msa.sm_scale), out.ctypes.data))
+    return out
+
+
+def msa_run_all(wl, index_cache, kv_cache, step, q):
+    """store -> token scores -> block scores -> block selection -> GQA attention."""
+    sh, ms = wl.shape, wl.msa
+    cache = store_keys(sh, wl.spans, wl.num_pages, step.keys, index_cache)
+    scores, off = index_scores(sh, wl.spans, wl.num_pages, step.q, step.w, cache)
+    bscores, boff = msa_block_scores(ms, wl.spans, scores, off)
+    sel = msa_select(ms, wl.spans, bscores, boff)
+    out = msa_attend(ms, wl.spans, wl.num_pages, sel, q, kv_cache)
+    return dict(index_cache=cache, scores=scores, offsets=off, block_scores=bscores, block_offsets=boff,
+                selection=sel, out=out)

@@ -22,6 +22,12 @@
  *          with l_j = (q_nope[r,h] . c_j + q_pe[r,h] . kpe_j) * sm_scale over the
  *          selected j, m the maximum of the l_j (and of the sink)
  *
+ * Block-sparse MSA (LLMServingSim, the MiniMax-M3 column of "Two shapes,
+ * three checkpoints"): block scores are the largest token score of each block
+ * of block_size positions the row sees, the top topk_blocks blocks are kept
+ * (the same causal top-k, over blocks), and GQA attention runs over the
+ * visible positions of the kept blocks.
+ *
  * Paged layout (DSASpan / DSAPlan): a row at request-local position p finds
  * token j at slot = page_start + j of its span's page list,
  * physical row = pages[slot / page_size] * page_size + slot % page_size.
@@ -423,6 +429,103 @@ int oracle_attend(const oracle_rows *Rw, int H, int L, int Rd, int topk, int lat
     free(logit);
     free(qn);
     free(qp);
+  }
+  return status;
+}
+
+/* ------------------------------------------------------------------------ */
+/* block-sparse MSA (LLMServingSim, "Sparse attention (DSA and block-sparse  */
+/* MSA)", table "Two shapes, three checkpoints", MiniMax-M3 column: the top  */
+/* 16 blocks of 128 tokens, over plain GQA, one bf16 index vector per token) */
+/* ------------------------------------------------------------------------ */
+
+/* Block scores.  Block b of row r holds positions b*block_size ..
+ * (b+1)*block_size - 1; its score is the largest token score (the DSA indexer
+ * score above) among the positions the row sees, 0 .. pos(r).  Row r has
+ * pos(r)/block_size + 1 blocks, its scores starting at block_off[r].  The
+ * selection is then the causal top-k above over these block scores (ties to
+ * the lower block). */
+int oracle_msa_block_scores(int64_t T, int block_size, const int64_t *pos, const float *scores,
+                            const int64_t *score_off, const int64_t *block_off, float *block_scores) {
+  if (block_size <= 0) return OR_BAD_ARG;
+  for (int64_t r = 0; r < T; r++) {
+    int64_t nblk = pos[r] / block_size + 1;
+    for (int64_t b = 0; b < nblk; b++) {
+      int64_t j0 = b * block_size, j1 = j0 + block_size - 1;
+      if (j1 > pos[r]) j1 = pos[r];
+      float m = scores[score_off[r] + j0];
+      for (int64_t j = j0 + 1; j <= j1; j++)
+        if (scores[score_off[r] + j] > m) m = scores[score_off[r] + j];
+      block_scores[block_off[r] + b] = m;
+    }
+  }
+  return OR_OK;
+}
+
+/* GQA attention over the tokens of the selected blocks.
+ * kv cache: one row per token, [K of kv heads 0..kv_heads-1 | V of the same
+ * heads], head_dim bf16 each (2 * kv_heads * head_dim * 2 bytes), in the
+ * paged layout of oracle_rows.  sel: [T][topk_blocks] block ids, -1 skipped;
+ * any other id must lie in 0 .. pos(r)/block_size.  q: [T][q_heads][head_dim]
+ * bf16; query head h reads kv head h / (q_heads / kv_heads).
+ * out[r][h] = sum_j e^{l_j - m} v_j / sum_j e^{l_j - m}, l_j = (q . k_j) * sm_scale,
+ * over the positions j <= pos(r) of the selected blocks, in double. */
+int oracle_msa_attend(const oracle_rows *R, int q_heads, int kv_heads, int head_dim, int block_size,
+                      int topk_blocks, const int32_t *sel, const uint16_t *q, const uint8_t *kv, double sm_scale,
+                      double *out) {
+  if (kv_heads <= 0 || q_heads % kv_heads != 0 || block_size <= 0 || topk_blocks <= 0) return OR_BAD_ARG;
+  const int group = q_heads / kv_heads;
+  const size_t row_elems = 2 * (size_t)kv_heads * head_dim;
+  const int64_t max_tokens = (int64_t)topk_blocks * block_size;
+  int status = OR_OK;
+#pragma omp parallel
+  {
+    int64_t *rows = (int64_t *)malloc(sizeof(int64_t) * max_tokens);
+    double *logit = (double *)malloc(sizeof(double) * max_tokens);
+    double *qd = (double *)malloc(sizeof(double) * head_dim);
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t r = 0; r < R->T; r++) {
+      if (!rows || !logit || !qd) { status = OR_NOMEM; continue; }
+      int64_t n = 0;
+      int bad = OR_OK;
+      for (int i = 0; i < topk_blocks && bad == OR_OK; i++) {
+        int64_t b = sel[r * topk_blocks + i];
+        if (b == -1) continue;
+        if (b < 0 || b > R->pos[r] / block_size) { bad = OR_BAD_SELECTION; break; }
+        for (int64_t j = b * block_size; j < (b + 1) * block_size && j <= R->pos[r]; j++) {
+          int e = OR_OK;
+          int64_t row = phys_row(R, r, j, &e);
+          if (row < 0) { bad = e; break; }
+          rows[n++] = row;
+        }
+      }
+      if (bad != OR_OK) { status = bad; continue; }
+      for (int h = 0; h < q_heads; h++) {
+        const int g = h / group;
+        const uint16_t *qr = q + ((size_t)r * q_heads + h) * head_dim;
+        for (int d = 0; d < head_dim; d++) qd[d] = bf16_value(qr[d]);
+        double m = -INFINITY;
+        for (int64_t t = 0; t < n; t++) {
+          const uint16_t *k = (const uint16_t *)kv + rows[t] * row_elems + (size_t)g * head_dim;
+          double a = 0.0;
+          for (int d = 0; d < head_dim; d++) a += qd[d] * bf16_value(k[d]);
+          logit[t] = a * sm_scale;
+          if (logit[t] > m) m = logit[t];
+        }
+        double den = 0.0;
+        for (int64_t t = 0; t < n; t++) den += exp(logit[t] - m);
+        double *o = out + ((size_t)r * q_heads + h) * head_dim;
+        for (int d = 0; d < head_dim; d++) o[d] = 0.0;
+        for (int64_t t = 0; t < n; t++) {
+          const uint16_t *v = (const uint16_t *)kv + rows[t] * row_elems + ((size_t)kv_heads + g) * head_dim;
+          double p = exp(logit[t] - m) / den;
+          for (int d = 0; d < head_dim; d++) o[d] += p * bf16_value(v[d]);
+        }
+      }
+    }
+    free(rows);
+    free(logit);
+    free(qd);
   }
   return status;
 }

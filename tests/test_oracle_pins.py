@@ -523,3 +523,145 @@ def test_quantize_rows_recovers_representable_rows():
     assert np.array_equal(got_scales[:4], np.ldexp(1.0, k[:4]).astype(np.float32))
     assert np.array_equal(got_codes[:4], codes[:4])
     assert got_scales[4] == 1.0 and not np.any(got_codes[4] & 0x7F)
+
+
+# ----------------------------------------------------------------------------
+# block-sparse MSA (LLMServingSim, "Sparse attention (DSA and block-sparse
+# MSA)", MiniMax-M3 column): block scores, block selection, GQA attention
+# ----------------------------------------------------------------------------
+def _msa_rows(positions):
+    """Single-row spans at the given positions (pages are not read here)."""
+    sh = tiny_shape()
+    return make_case(sh, [(int(p), 1) for p in positions]).spans
+
+
+def test_msa_block_scores_closed_form_and_causal_tail():
+    """Token scores s_j = j: a block's score is its last visible position,
+    min(b*bs + bs - 1, pos); blocks past pos do not exist and positions past
+    pos inside the last block are not read (a spike there is ignored)."""
+    ms = W.MSAShape(block_size=4)
+    pos = [10, 3, 0, 17]
+    spans = _msa_rows(pos)
+    rows = []
+    for p in pos:
+        s = np.arange(p + 1, dtype=np.float32)
+        rows.append(s)
+    off = np.zeros(len(rows) + 1, np.int64)
+    off[1:] = np.cumsum([len(r) for r in rows])
+    bs, boff = oracle.msa_block_scores(ms, spans, np.concatenate(rows), off)
+    for r, p in enumerate(pos):
+        got = bs[boff[r]:boff[r + 1]]
+        assert len(got) == p // 4 + 1
+        assert list(got) == [float(min(4 * b + 3, p)) for b in range(p // 4 + 1)]
+    # a spike at position 9 of a row at pos 10 lifts block 2 only; the next
+    # row's first score (a larger spike) lies where position 11 would be and
+    # must not reach it
+    s = np.zeros(11 + 3, np.float32)
+    s[9] = 5.0
+    s[11] = 50.0
+    bs, boff = oracle.msa_block_scores(ms, _msa_rows([10, 2]), s, np.array([0, 11, 14]))
+    assert list(bs[:3]) == [0.0, 0.0, 5.0] and list(bs[3:]) == [50.0]
+
+
+def test_msa_selection_with_unit_blocks_is_the_token_selection():
+    """block_size 1: every block is one position, so the block selection is the
+    DSA token selection (itself pinned by brute force above)."""
+    rng = np.random.default_rng(5)
+    pos = [0, 6, 40, 41]
+    rows = [rng.integers(0, 4, size=p + 1).astype(np.float32) for p in pos]   # ties
+    off = np.zeros(len(rows) + 1, np.int64)
+    off[1:] = np.cumsum([len(r) for r in rows])
+    spans = _msa_rows(pos)
+    for k in (1, 5, 16):
+        ms = W.MSAShape(block_size=1, topk_blocks=k)
+        bs, boff = oracle.msa_block_scores(ms, spans, np.concatenate(rows), off)
+        assert np.array_equal(bs, np.concatenate(rows))
+        sel = oracle.msa_select(ms, spans, bs, boff)
+        ref = oracle.topk(tiny_shape(topk=k), spans, np.concatenate(rows), off)
+        assert np.array_equal(sel, ref)
+
+
+def test_msa_selection_ties_padding_and_order():
+    ms = W.MSAShape(block_size=4, topk_blocks=3)
+    # equal block scores: the lowest blocks win
+    spans = _msa_rows([23])
+    sel = oracle.msa_select(ms, spans, np.zeros(6, np.float32), np.array([0, 6]))
+    assert list(sel[0]) == [0, 1, 2]
+    # fewer blocks than topk_blocks: all of them, then -1
+    spans = _msa_rows([5])
+    sel = oracle.msa_select(ms, spans, np.array([1.0, 2.0], np.float32), np.array([0, 2]))
+    assert list(sel[0]) == [1, 0, -1]
+    # rank order: score descending, block ascending
+    spans = _msa_rows([27])
+    sel = oracle.msa_select(ms, spans, np.array([3, 1, 3, 9, 0, 3, 2], np.float32), np.array([0, 7]))
+    assert list(sel[0]) == [3, 0, 2]
+
+
+def _gqa_case(q_heads=4, kv_heads=2, D=8, bs=4, P=4, page_start=1, ctx=13, q_len=3, seed=0, pages=None):
+    ms = W.MSAShape(index_heads=2, index_dim=8, page_size=P, block_size=bs, topk_blocks=16, q_heads=q_heads,
+                    kv_heads=kv_heads, head_dim=D, sm_scale=0.3)
+    case = make_case(tiny_shape(page_size=P), [(ctx, q_len)], pages=pages, page_start=page_start)
+    rng = np.random.default_rng(seed)
+    n = ctx + q_len
+    kvv = rng.standard_normal((n, 2 * kv_heads * D)).astype(np.float32)
+    cache = np.zeros((case.num_pages * P, 2 * kv_heads * D), np.float32)
+    cache[phys_rows(case, 0, np.arange(n))] = kvv
+    q = rng.standard_normal((q_len, q_heads, D)).astype(np.float32)
+    return ms, case, bf16(kvv).double(), bf16(cache).view(case.num_pages, P, -1), bf16(q)
+
+
+def test_msa_attend_every_block_equals_dense_causal_gqa():
+    """With every block selected, MSA attention is dense causal GQA: computed
+    here by torch's scaled_dot_product_attention in fp64, K and V taken from
+    the row layout [K heads | V heads], query head h on kv head h // group."""
+    qh, kh, D, ctx, q_len = 6, 2, 8, 13, 3
+    ms, case, kvv, cache, q = _gqa_case(q_heads=qh, kv_heads=kh, D=D, ctx=ctx, q_len=q_len, pages=[[3, 0, 4, 1, 2]])
+    nblk = (ctx + q_len - 1) // ms.block_size + 1
+    sel = np.full((q_len, ms.topk_blocks), -1, np.int32)
+    for r in range(q_len):
+        nb = (ctx + r) // ms.block_size + 1
+        sel[r, :nb] = np.arange(nb)[::-1]   # any order
+    assert nblk <= ms.topk_blocks
+    out = oracle.msa_attend(ms, case.spans, case.num_pages, sel, q, cache)
+    n = ctx + q_len
+    k = kvv[:, :kh * D].view(n, kh, D).transpose(0, 1).repeat_interleave(qh // kh, dim=0)   # (qh, n, D)
+    v = kvv[:, kh * D:].view(n, kh, D).transpose(0, 1).repeat_interleave(qh // kh, dim=0)
+    mask = torch.zeros(q_len, n, dtype=torch.bool)
+    for r in range(q_len):
+        mask[r, :ctx + r + 1] = True
+    ref = torch.nn.functional.scaled_dot_product_attention(q.double().transpose(0, 1), k, v, attn_mask=mask,
+                                                           scale=ms.sm_scale)
+    assert np.allclose(out, ref.transpose(0, 1).numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_msa_attend_head_groups_read_their_kv_head():
+    """V of kv head g constant g + 1: every query head of group g outputs g + 1."""
+    qh, kh, D = 8, 4, 4
+    ms, case, kvv, cache, q = _gqa_case(q_heads=qh, kv_heads=kh, D=D, ctx=9, q_len=2)
+    c = cache.clone().float().view(-1, 2 * kh * D)
+    for g in range(kh):
+        c[:, (kh + g) * D:(kh + g + 1) * D] = g + 1
+    sel = np.array([[0, 2, -1, -1] + [-1] * 12, [1, -1, -1, -1] + [-1] * 12], np.int32)
+    out = oracle.msa_attend(ms, case.spans, case.num_pages, sel, q, bf16(c.numpy()).view(cache.shape))
+    for h in range(qh):
+        assert np.allclose(out[:, h, :], h // (qh // kh) + 1, rtol=0, atol=1e-14)   # softmax weights sum to 1
+
+
+def test_msa_attend_uniform_logits_give_the_mean_of_visible_values():
+    """q = 0: equal logits, so each head outputs the mean V over the visible
+    positions of its selected blocks (the row at position 13 with blocks 1 and
+    3 of size 4 sees positions 4..7 and 12..13)."""
+    ms, case, kvv, cache, q = _gqa_case(ctx=13, q_len=1, kv_heads=1, q_heads=2)
+    sel = np.array([[3, 1] + [-1] * 14], np.int32)
+    out = oracle.msa_attend(ms, case.spans, case.num_pages, sel, torch.zeros_like(q), cache)
+    D = ms.head_dim
+    vis = [4, 5, 6, 7, 12, 13]
+    mean = kvv[vis][:, D:2 * D].mean(dim=0).numpy()
+    assert np.allclose(out[0, 0], mean, rtol=0, atol=1e-14) and np.allclose(out[0, 1], mean, rtol=0, atol=1e-14)
+
+
+def test_msa_attend_rejects_blocks_past_the_row():
+    ms, case, kvv, cache, q = _gqa_case(ctx=13, q_len=1)
+    sel = np.array([[4] + [-1] * 15], np.int32)   # the row at position 13 has blocks 0..3
+    with pytest.raises(oracle.OracleError):
+        oracle.msa_attend(ms, case.spans, case.num_pages, sel, q, cache)
