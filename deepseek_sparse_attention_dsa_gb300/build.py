@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libdsa_gb300.so")
 SOURCES = ["api.cu", "plan_device.cu", "store_keys.cu", "quantize.cu", "indexer.cu", "indexer_f8q.cu", "topk.cu",
-           "attend.cu", "static_scratch.cu", "selftest.cu"]
+           "attend.cu", "msa.cu", "static_scratch.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

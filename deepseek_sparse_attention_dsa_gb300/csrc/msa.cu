@@ -1,0 +1,844 @@
+// msa.cu -- block-sparse MSA on sm_103a: block selection and GQA attention
+// over the selected blocks.
+//
+// LLMServingSim, "Sparse attention (DSA and block-sparse MSA)", table "Two
+// shapes, three checkpoints", MiniMax-M3 column: every row keeps the top 16
+// blocks of 128 tokens and attends over them with plain GQA; the index cache
+// holds one bf16 vector per token.  The pages give no block-scoring formula;
+// the reading built here: a token's score is the DSA indexer score over its
+// index vector (index_tc_kernel, unchanged), a block's score is the largest
+// score among the positions the row sees, the selection is the causal top-k
+// over blocks with ties to the lower block, and attention covers the
+// positions <= the row's own in the kept blocks.
+//
+// msa_select_kernel: one CTA per row; warps take blocks and reduce their
+// scores to order-preserving 32-bit keys (redux.sync max), then topk_blocks
+// rounds of a block-wide argmax (ties to the lower block) pick the blocks,
+// written in ascending order with a -1 tail.
+//
+// msa_attend_tc_kernel (block_size 128, head_dim 128): one CTA per row walks
+// (tile, kv head) steps.  A tile is 128 positions, one UMMA M:
+//     S^T[token, head] = K[token, :] . Q_g[head, :]      (M = 128 tokens, N = group heads padded to 16)
+//     O^T_g[dim, head] += V[:, dim]^T . P^T[:, head]     (M = 128 dims, A = V read MN-major, B = P^T)
+// Warp 0 issues the TMA loads of a step's K and V boxes (the paged cache as
+// a 2-D tensor, 128-byte swizzle) into a ring of stages, warp 1 issues the
+// MMAs (QK of step t+1 before PV of step t), and four softmax warps
+// (thread = TMEM lane = token of S, dim of O) reduce each head's maximum with
+// redux.sync over order keys and its sum with shuffles, keep a per-head
+// reference max that moves only when it grows by more than 2^8 (O is then
+// rescaled in TMEM), write P^T as bf16 in the 128-byte-swizzled K-major
+// layout, and normalise at the end.  Tiles start on the box boundary below
+// the span's page_start (as the indexer's key tiles do): with page_start a
+// multiple of the box height a tile is exactly one block, otherwise a block
+// spans two tiles and rows outside the kept blocks are masked (their V rows
+// are zeroed before PV so no stale value meets a zero probability).
+//
+// msa_attend_simt_kernel covers other shapes: one CTA per (row, query head),
+// fp32 on CUDA cores.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+
+#include "dsa_internal.h"
+#include "ptx.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr float kMsaLog2e = 1.4426950408889634f;
+constexpr float kMsaRescale = 8.0f;         // log2 units the reference max may lag the true max
+constexpr float kMsaNegBig = -1.0e30f;
+
+constexpr int kSelThreads = 512;
+constexpr int kSelMaxBlocks = 16384;          // blocks per row held in shared memory
+constexpr int kMsaMaxK = 64;                  // topk_blocks
+constexpr int kMsaTile = 128;                 // positions per tile (UMMA M)
+constexpr int kMsaMaxTiles = 2 * kMsaMaxK;
+constexpr int kMsaThreads = 192;              // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+constexpr int kMsaMaxKvHeads = 8;
+
+__device__ __forceinline__ uint32_t score_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;   // -0.0 ranks as +0.0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_score(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// ---------------------------------------------------------------------------
+// block selection
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kSelThreads) msa_select_kernel(const float *__restrict__ scores,
+                                                                 const int64_t *__restrict__ row_score_off,
+                                                                 const int32_t *__restrict__ row_pos, int T, int bs,
+                                                                 int K, int32_t *__restrict__ sel) {
+  extern __shared__ uint32_t bkey[];   // [kSelMaxBlocks] block keys; 0 = taken (below every finite score)
+  __shared__ unsigned long long wbest[kSelThreads / 32];
+  __shared__ int chosen[kMsaMaxK];
+  constexpr int kWarps = kSelThreads / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int row = blockIdx.x; row < T; row += gridDim.x) {
+    const int pos = row_pos[row];
+    if (pos < 0) continue;   // padding row (uniform over the CTA)
+    const int nblk = pos / bs + 1;
+    const float *s = scores + row_score_off[row];
+    // block maxima: warp w takes blocks w, w + kWarps, ...; four blocks per
+    // pass keep their loads in flight together
+    for (int b0 = warp; b0 < nblk; b0 += 4 * kWarps) {
+      uint32_t m[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int b = b0 + u * kWarps;
+        m[u] = 0u;
+        if (b < nblk) {
+          const int j0 = b * bs, j1 = min(j0 + bs - 1, pos);
+          for (int j = j0 + lane; j <= j1; j += 32) m[u] = max(m[u], score_key(__ldg(s + j)));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int b = b0 + u * kWarps;
+        const uint32_t mu = __reduce_max_sync(0xffffffffu, m[u]);
+        if (lane == 0 && b < nblk) bkey[b] = mu;
+      }
+    }
+    __syncthreads();
+    int32_t *out = sel + static_cast<int64_t>(row) * K;
+    if (nblk <= K) {
+      for (int i = threadIdx.x; i < K; i += kSelThreads) out[i] = i < nblk ? i : -1;
+    } else {
+      // K rounds of argmax over (key, lower block first)
+      for (int k = 0; k < K; ++k) {
+        unsigned long long best = 0ull;
+        for (int i = threadIdx.x; i < nblk; i += kSelThreads) {
+          const unsigned long long v =
+              (static_cast<unsigned long long>(bkey[i]) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(i));
+          best = v > best ? v : best;
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+          const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, o);
+          best = y > best ? y : best;
+        }
+        if (lane == 0) wbest[warp] = best;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+          unsigned long long b = 0ull;
+          for (int w = 0; w < kWarps; ++w) b = wbest[w] > b ? wbest[w] : b;
+          const int idx = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(b & 0xFFFFFFFFull));
+          chosen[k] = idx;
+          bkey[idx] = 0u;
+        }
+        __syncthreads();
+      }
+      if (threadIdx.x == 0) {   // ascending block order
+        for (int a = 1; a < K; ++a) {
+          const int v = chosen[a];
+          int c = a - 1;
+          while (c >= 0 && chosen[c] > v) {
+            chosen[c + 1] = chosen[c];
+            --c;
+          }
+          chosen[c + 1] = v;
+        }
+      }
+      __syncthreads();
+      for (int i = threadIdx.x; i < K; i += kSelThreads) out[i] = chosen[i];
+    }
+    __syncthreads();   // bkey and chosen are reused by the next row
+  }
+}
+
+// ---------------------------------------------------------------------------
+// GQA attention over the selected blocks, tensor cores
+// ---------------------------------------------------------------------------
+struct MsaParams {
+  CUtensorMap tm_kv;   // kv cache as [pages*P, 2*Hkv*128] bf16, box {64, BH}, 128-byte swizzle
+  CUtensorMap tm_q;    // q as [T*Hq, 128] bf16, box {64, NG}, 128-byte swizzle
+  const int32_t *sel;  // [T][K] block ids, -1 padded
+  const int32_t *row_pos, *row_page_off, *row_npages, *row_page_start, *pages;
+  __nv_bfloat16 *out;  // [T][Hq][128]
+  int *err;
+  int Hq, Hkv, group, K, P, BH, num_pages, stages;
+  float scale_log2;    // sm_scale * log2(e)
+};
+
+// Shared-memory layout of one CTA (bytes from a 1024-aligned base).
+struct MsaLayout {
+  uint32_t off_q, off_p, off_red, off_ml, off_tiles, off_bar, off_misc, bytes;
+  __host__ __device__ MsaLayout(int NG, int stages, int Hkv) {
+    const uint32_t ch = kMsaTile * 128, stage = 4 * ch;   // K and V, two 64-column chunks each
+    off_q = stages * stage;
+    off_p = off_q + Hkv * 2 * NG * 128;
+    off_red = off_p + 2 * 2 * NG * 128;
+    off_ml = off_red + 2 * 4 * NG * 4;
+    off_tiles = off_ml + 2 * Hkv * NG * 4;
+    off_bar = (off_tiles + 2 * kMsaMaxTiles * 4 + 7) / 8 * 8;
+    off_misc = off_bar + 24 * 8;
+    bytes = off_misc + 16 + 1024;   // + alignment slack
+  }
+};
+
+template <int NG>
+__global__ void __launch_bounds__(kMsaThreads, 1) msa_attend_tc_kernel(const __grid_constant__ MsaParams p) {
+  constexpr int CH = kMsaTile * 128;        // [128 rows][64 columns] bf16
+  constexpr int KVB = 2 * CH;               // K (or V) of one kv head
+  constexpr int STAGE = 2 * KVB;
+  constexpr int QG = 2 * NG * 128;          // Q of one kv head: 2 chunks [NG heads][64 dims]
+  constexpr int PB = 2 * NG * 128;          // P^T: 2 chunks [NG heads][64 tokens]
+  constexpr uint32_t IDESC_QK = mma_idesc(128, NG, 1u, false, false);
+  constexpr uint32_t IDESC_PV = mma_idesc(128, NG, 1u, true, false);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int S = p.stages, Hkv = p.Hkv;
+  const MsaLayout lay(NG, S, Hkv);
+  const uint32_t bar0 = sbase + lay.off_bar;
+  auto kfull = [&](int s) { return bar0 + 8u * s; };
+  auto vfull = [&](int s) { return bar0 + 8u * (3 + s); };
+  auto kempty = [&](int s) { return bar0 + 8u * (6 + s); };
+  auto sfull = [&](int b) { return bar0 + 8u * (9 + b); };
+  auto sempty = [&](int b) { return bar0 + 8u * (11 + b); };
+  auto pfull = [&](int b) { return bar0 + 8u * (13 + b); };
+  auto pempty = [&](int b) { return bar0 + 8u * (15 + b); };
+  const uint32_t b_pvdone = bar0 + 8u * 17, b_qfull = bar0 + 8u * 18;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + lay.off_misc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + lay.off_misc + 4);
+  int *ntiles_sm = reinterpret_cast<int *>(smem + lay.off_misc + 8);
+  int32_t *tile_u = reinterpret_cast<int32_t *>(smem + lay.off_tiles);
+  int32_t *tile_fl = tile_u + kMsaMaxTiles;
+  float *m_sm = reinterpret_cast<float *>(smem + lay.off_ml);
+  float *l_sm = m_sm + Hkv * NG;
+  uint32_t *redmax = reinterpret_cast<uint32_t *>(smem + lay.off_red);   // [4 quads][NG]
+  float *redsum = reinterpret_cast<float *>(smem + lay.off_red) + 4 * NG;  // [4 quads][NG]
+
+  const int warp = threadIdx.x / 32, lane = lane_id();
+  const int row = blockIdx.x;
+  const int pos = p.row_pos[row];
+  if (pos < 0) return;   // padding row of a capturable plan: the whole CTA leaves before any barrier
+  const int page_start = p.row_page_start[row], page_off = p.row_page_off[row], npages = p.row_npages[row];
+  const int lead = page_start % p.BH;
+
+  if (warp == 0) {
+    // ---- the row's tiles: kept blocks in ascending order (rank placement,
+    // the selection may come in any order), each block's tile and, when
+    // page_start is off the box boundary, the tile holding its tail
+    const int32_t *sr = p.sel + static_cast<int64_t>(row) * p.K;
+    const int last = pos / kMsaTile;
+    int b[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int e = lane + 32 * h;
+      int v = e < p.K ? sr[e] : -1;
+      if (v < -1 || v > last) {
+        atomicOr(p.err, kErrBounds);
+        v = -1;
+      }
+      b[h] = v;
+    }
+    int rank[2] = {0, 0};
+    for (int e = 0; e < 64; ++e) {
+      const int v = __shfl_sync(0xffffffffu, b[e >> 5], e & 31);
+      if (v < 0) continue;
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        if (b[h] >= 0 && (v < b[h] || (v == b[h] && e < lane + 32 * h))) ++rank[h];
+    }
+    int *sorted = tile_fl;   // scratch until the tile list is built
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      if (b[h] >= 0) sorted[rank[h]] = b[h];
+    const int nvalid = __reduce_add_sync(0xffffffffu, (b[0] >= 0 ? 1 : 0) + (b[1] >= 0 ? 1 : 0));
+    __syncwarp();
+    if (lane == 0) {
+      int n = 0, ul[kMsaMaxTiles], fl[kMsaMaxTiles];
+      for (int i = 0; i < nvalid; ++i) {
+        const int blk = sorted[i];
+        // tile blk holds the block's positions from row `lead` on (bit 1)
+        if (n > 0 && ul[n - 1] == blk) fl[n - 1] |= 2;
+        else { ul[n] = blk; fl[n] = 2; ++n; }
+        // tile blk+1 holds its last `lead` positions in rows 0..lead-1 (bit 0)
+        if (lead > 0 && kMsaTile * (blk + 1) - lead <= pos) {
+          ul[n] = blk + 1;
+          fl[n] = 1;
+          ++n;
+        }
+      }
+      for (int i = 0; i < n; ++i) {
+        tile_u[i] = ul[i];
+        tile_fl[i] = fl[i];
+      }
+      *ntiles_sm = n;
+    }
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 3; ++s) {
+      mbar_init(kfull(s), 1);
+      mbar_init(vfull(s), 1);
+      mbar_init(kempty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(sfull(b), 1);
+      mbar_init(sempty(b), 4);   // one arrival per softmax warp
+      mbar_init(pfull(b), 4);
+      mbar_init(pempty(b), 1);
+    }
+    mbar_init(b_pvdone, 1);
+    mbar_init(b_qfull, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&p.tm_kv);
+    tma_prefetch_desc(&p.tm_q);
+  }
+  if (warp == 1) {
+    const int cols = 2 * NG + Hkv * NG;
+    tmem_alloc(smem_u32(tmem_slot), cols <= 32 ? 32 : cols <= 64 ? 64 : cols <= 128 ? 128 : cols <= 256 ? 256 : 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int ntiles = *ntiles_sm;
+  const int nsteps = ntiles * Hkv;
+  const int tiles_cols = 2 * NG + Hkv * NG;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(b_qfull, static_cast<uint32_t>(Hkv * QG));
+      for (int g = 0; g < Hkv; ++g)
+        for (int c = 0; c < 2; ++c)
+          tma_load_2d(sbase + lay.off_q + g * QG + c * NG * 128, &p.tm_q, c * 64, row * p.Hq + g * p.group, b_qfull);
+    }
+    const int nbox = kMsaTile / p.BH;
+    int issued = 0;
+    for (int t = 0; t < nsteps; ++t) {
+      const int ti = t / Hkv, g = t - ti * Hkv;
+      const int u = tile_u[ti];
+      const int st = t % S;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(kempty(st), ((t / S) & 1) ^ 1, abort_flag, p.err);
+      if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) break;
+      // lane b: box b of the tile (positions q0 .. q0+BH-1), loaded when it
+      // holds a position 0 .. pos and its page exists
+      int crow = -1;
+      if (lane < nbox) {
+        const int q0 = kMsaTile * u - lead + lane * p.BH;
+        if (q0 + p.BH - 1 >= 0 && q0 <= pos) {
+          const uint32_t slot = static_cast<uint32_t>(page_start - lead + kMsaTile * u + lane * p.BH);
+          const uint32_t pi = slot / static_cast<uint32_t>(p.P);
+          const int page = pi < static_cast<uint32_t>(npages) ? __ldg(p.pages + page_off + pi) : -1;
+          if (page < 0 || page >= p.num_pages) atomicOr(p.err, kErrBounds);
+          else crow = page * p.P + static_cast<int>(slot % static_cast<uint32_t>(p.P));
+        }
+      }
+      const uint32_t valid = __ballot_sync(0xffffffffu, crow >= 0);
+      const uint32_t bytes = __popc(valid) * p.BH * 128 * 2;
+      if (lane == 0) {
+        if (bytes) {
+          mbar_arrive_expect_tx(kfull(st), bytes);
+          mbar_arrive_expect_tx(vfull(st), bytes);
+        } else {
+          mbar_arrive(kfull(st));
+          mbar_arrive(vfull(st));
+        }
+      }
+      __syncwarp();
+      if (crow >= 0) {
+        const uint32_t kst = sbase + st * STAGE, vst = kst + KVB;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          tma_load_2d(kst + c * CH + lane * p.BH * 128, &p.tm_kv, g * 128 + c * 64, crow, kfull(st));
+          tma_load_2d(vst + c * CH + lane * p.BH * 128, &p.tm_kv, (Hkv + g) * 128 + c * 64, crow, vfull(st));
+        }
+      }
+      issued = t + 1;
+    }
+    // nothing of ours may still be landing when the CTA leaves: wait (bounded,
+    // whatever the abort flag says) for the loads of the last stages issued
+    if (lane == 0) {
+      volatile int no_abort = 0;
+      for (int t = max(0, issued - S); t < issued; ++t) {
+        mbar_wait(kfull(t % S), (t / S) & 1, &no_abort, p.err);
+        mbar_wait(vfull(t % S), (t / S) & 1, &no_abort, p.err);
+      }
+      mbar_wait(b_qfull, 0, &no_abort, p.err);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = mbar_wait(b_qfull, 0, abort_flag, p.err);
+      auto pv = [&](int t) -> bool {
+        const int st = t % S;
+        if (!mbar_wait(vfull(st), (t / S) & 1, abort_flag, p.err)) return false;
+        if (!mbar_wait(pfull(t & 1), (t >> 1) & 1, abort_flag, p.err)) return false;
+        tc_fence_after();
+        const int ti = t / Hkv, g = t - ti * Hkv;
+        const uint32_t vaddr = sbase + st * STAGE + KVB;
+        const uint32_t paddr = sbase + lay.off_p + (t & 1) * PB;
+#pragma unroll
+        for (int k = 0; k < kMsaTile / 16; ++k) {
+          // A = V^T (dims x tokens), read MN-major: 64-dim chunks CH apart,
+          // 8-token groups 1024 bytes apart; B = P^T, K-major
+          const uint64_t ad = smem_desc(vaddr + k * 16 * 128, CH, 1024, kSwizzle128);
+          const uint64_t bd = smem_desc(paddr + (k >> 2) * NG * 128 + (k & 3) * 32, 16, 1024, kSwizzle128);
+          mma_f16_ss(tmem_base + 2 * NG + g * NG, ad, bd, IDESC_PV, (ti > 0 || k > 0) ? 1u : 0u);
+        }
+        mma_commit(kempty(st));
+        mma_commit(pempty(t & 1));
+        mma_commit(b_pvdone);
+        return true;
+      };
+      for (int t = 0; t < nsteps && ok; ++t) {
+        const int st = t % S;
+        ok = mbar_wait(kfull(st), (t / S) & 1, abort_flag, p.err) &&
+             mbar_wait(sempty(t & 1), ((t >> 1) & 1) ^ 1, abort_flag, p.err);
+        if (!ok) break;
+        tc_fence_after();
+        const int ti = t / Hkv, g = t - ti * Hkv;
+        const uint32_t kaddr = sbase + st * STAGE;
+        const uint32_t qaddr = sbase + lay.off_q + g * QG;
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_f16_ss(tmem_base + (t & 1) * NG, smem_desc(kaddr + c * CH + k * 32, 16, 1024, kSwizzle128),
+                       smem_desc(qaddr + c * NG * 128 + k * 32, 16, 1024, kSwizzle128), IDESC_QK, (c | k) ? 1u : 0u);
+        mma_commit(sfull(t & 1));
+        if (t > 0) ok = pv(t - 1);   // PV of the previous step after this QK, so the two overlap the softmax
+      }
+      if (ok && nsteps > 0) pv(nsteps - 1);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int quad = warp & 3;
+    const int i = quad * 32 + lane;   // TMEM lane: token of S, dim of O
+    const int et = threadIdx.x - 64;
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    for (int k = et; k < Hkv * NG; k += 128) {
+      m_sm[k] = kMsaNegBig;
+      l_sm[k] = 0.f;
+    }
+    // every exit from the step loop is decided at a named barrier (an OR of
+    // the 128 threads' failures), so no softmax warp waits there alone
+    bool ok = !named_bar_any(1, 128, false);
+    bool carry = true;   // this warp's result of the previous step's last wait
+    for (int t = 0; t < nsteps && ok; ++t) {
+      const int ti = t / Hkv, g = t - ti * Hkv;
+      const int u = tile_u[ti], fl = tile_fl[ti];
+      const int q = kMsaTile * u - lead + i;
+      const bool valid = q >= 0 && q <= pos && ((i < lead) ? (fl & 1) : (fl & 2));
+      bool good = carry && __all_sync(0xffffffffu, mbar_wait(sfull(t & 1), (t >> 1) & 1, abort_flag, p.err));
+      tc_fence_after();
+      float s[NG];
+      if (good) {
+#pragma unroll
+        for (int c0 = 0; c0 < NG; c0 += 16)
+          tmem_ld16(tmem_base + lane_base + (t & 1) * NG + c0, *reinterpret_cast<float(*)[16]>(s + c0));
+        tmem_ld_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (good && lane == 0) mbar_arrive(sempty(t & 1));
+      // each head's largest logit of the tile (order keys; masked rows give 0)
+#pragma unroll
+      for (int h = 0; h < NG; ++h) {
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, valid ? score_key(s[h]) : 0u);
+        if (lane == 0) redmax[quad * NG + h] = mk;
+      }
+      if (named_bar_any(1, 128, !good)) {
+        ok = false;
+        break;
+      }
+      float alpha[NG], mnew[NG];
+      bool rescale = false;
+#pragma unroll
+      for (int h = 0; h < NG; ++h) {
+        const uint32_t k =
+            max(max(redmax[h], redmax[NG + h]), max(redmax[2 * NG + h], redmax[3 * NG + h]));
+        const float mold = m_sm[g * NG + h];
+        // (a tile always holds a kept position, so k is a real score)
+        const float tmax = key_score(k) * p.scale_log2;
+        mnew[h] = mold;
+        alpha[h] = 1.f;
+        if (tmax > mold + kMsaRescale) {
+          mnew[h] = tmax;
+          alpha[h] = exp2f(mold - tmax);
+          rescale = true;
+        }
+      }
+      // P (bf16) and the tile's per-head sums of what PV will add
+      float psum[NG];
+#pragma unroll
+      for (int h = 0; h < NG; ++h) {
+        const float e = valid ? exp2f(fmaf(s[h], p.scale_log2, -mnew[h])) : 0.f;
+        const __nv_bfloat16 pb = __float2bfloat16_rn(e);
+        s[h] = __bfloat162float(pb);
+        psum[h] = s[h];
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1)
+#pragma unroll
+        for (int h = 0; h < NG; ++h) psum[h] += __shfl_xor_sync(0xffffffffu, psum[h], o);
+      if (lane == 0)
+#pragma unroll
+        for (int h = 0; h < NG; ++h) redsum[quad * NG + h] = psum[h];
+      // P^T buffer (t & 1) is free once PV(t-2) completed
+      good = __all_sync(0xffffffffu, mbar_wait(pempty(t & 1), ((t >> 1) & 1) ^ 1, abort_flag, p.err));
+      if (good) {
+        const uint32_t pbase = sbase + lay.off_p + (t & 1) * PB + (i >> 6) * NG * 128;
+#pragma unroll
+        for (int h = 0; h < NG; ++h) {
+          const uint32_t a = pbase + h * 128 + ((((i & 63) >> 3) ^ (h & 7)) << 4) + ((i & 7) << 1);
+          const __nv_bfloat16 pb = __float2bfloat16_rn(s[h]);
+          asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"(*reinterpret_cast<const uint16_t *>(&pb)) : "memory");
+        }
+      }
+      // V rows of positions outside the kept blocks are zeroed once the tile
+      // has landed (a zero probability must not meet a stale value)
+      if (good && __any_sync(0xffffffffu, !valid)) {
+        const int st = t % S;
+        good = __all_sync(0xffffffffu, mbar_wait(vfull(st), (t / S) & 1, abort_flag, p.err));
+        if (good && !valid) {
+          const uint32_t vrow = sbase + st * STAGE + KVB + i * 128;
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              st_shared_v4(vrow + c * CH + k * 16, make_uint4(0u, 0u, 0u, 0u));
+        }
+      }
+      fence_proxy_async_smem();
+      if (named_bar_any(1, 128, !good)) {
+        ok = false;
+        break;
+      }
+      if (et < NG) {
+        const float ts = redsum[et] + redsum[NG + et] + redsum[2 * NG + et] + redsum[3 * NG + et];
+        l_sm[g * NG + et] = l_sm[g * NG + et] * alpha[et] + ts;
+      }
+      if (et == 0)
+#pragma unroll
+        for (int h = 0; h < NG; ++h) m_sm[g * NG + h] = mnew[h];
+      // O of this kv head is rescaled once PV(t-1) (and so every earlier PV
+      // into it) has completed; its first tile has no O yet
+      if (rescale && ti > 0) {
+        good = __all_sync(0xffffffffu, mbar_wait(b_pvdone, (t - 1) & 1, abort_flag, p.err));
+        tc_fence_after();
+        if (good) {
+#pragma unroll
+          for (int c0 = 0; c0 < NG; c0 += 16) {
+            float o[16];
+            tmem_ld16(tmem_base + lane_base + 2 * NG + g * NG + c0, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < 16; ++k) o[k] *= alpha[c0 + k];
+            tmem_st16(tmem_base + lane_base + 2 * NG + g * NG + c0, o);
+          }
+          tmem_st_wait();
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (good && lane == 0) mbar_arrive(pfull(t & 1));
+      carry = good;
+    }
+    if (ok && carry && nsteps > 0)
+      carry = __all_sync(0xffffffffu, mbar_wait(b_pvdone, (nsteps - 1) & 1, abort_flag, p.err));
+    tc_fence_after();
+    ok = !named_bar_any(1, 128, !(ok && carry));   // the last l values are in place
+    if (ok) {
+      for (int g = 0; g < Hkv; ++g) {
+#pragma unroll
+        for (int c0 = 0; c0 < NG; c0 += 16) {
+          float o[16];
+          tmem_ld16(tmem_base + lane_base + 2 * NG + g * NG + c0, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int h = c0 + k;
+            if (h >= p.group) continue;
+            const float l = l_sm[g * NG + h];
+            p.out[(static_cast<int64_t>(row) * p.Hq + g * p.group + h) * 128 + i] =
+                __float2bfloat16_rn(l > 0.f ? o[k] / l : 0.f);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1)
+    tmem_dealloc(tmem_base, tiles_cols <= 32 ? 32 : tiles_cols <= 64 ? 64 : tiles_cols <= 128 ? 128
+                                                 : tiles_cols <= 256 ? 256 : 512);
+}
+
+// ---------------------------------------------------------------------------
+// GQA attention over the selected blocks, CUDA cores (any shape)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(128) msa_attend_simt_kernel(
+    const int32_t *__restrict__ sel, const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ kv,
+    const int32_t *__restrict__ row_pos, const int32_t *__restrict__ row_page_off,
+    const int32_t *__restrict__ row_npages, const int32_t *__restrict__ row_page_start,
+    const int32_t *__restrict__ pages, __nv_bfloat16 *__restrict__ out, int *err, int Hq, int Hkv, int D, int bs,
+    int K, int P, int num_pages, float scale_log2) {
+  extern __shared__ float sm[];   // q [D], logits [K*bs], reduce [32]
+  float *qs = sm;
+  float *lg = sm + D;
+  float *red = lg + static_cast<int64_t>(K) * bs;
+  const int row = blockIdx.x / Hq, h = blockIdx.x % Hq;
+  const int g = h / (Hq / Hkv);
+  const int pos = row_pos[row];
+  if (pos < 0) return;
+  const int64_t row_elems = 2 * static_cast<int64_t>(Hkv) * D;
+  for (int d = threadIdx.x; d < D; d += blockDim.x)
+    qs[d] = __bfloat162float(q[(static_cast<int64_t>(row) * Hq + h) * D + d]);
+  __syncthreads();
+  const int32_t *sr = sel + static_cast<int64_t>(row) * K;
+  const int n = K * bs;
+  auto cache_row = [&](int e) -> int64_t {   // physical row of entry e, or -1
+    const int blk = sr[e / bs];
+    if (blk == -1) return -1;
+    if (blk < -1 || blk > pos / bs) {
+      atomicOr(err, kErrBounds);
+      return -1;
+    }
+    const int j = blk * bs + e % bs;
+    if (j > pos) return -1;
+    const int64_t slot = static_cast<int64_t>(row_page_start[row]) + j;
+    const int64_t pi = slot / P;
+    const int page = pi < row_npages[row] ? pages[row_page_off[row] + pi] : -1;
+    if (page < 0 || page >= num_pages) {
+      atomicOr(err, kErrBounds);
+      return -1;
+    }
+    return static_cast<int64_t>(page) * P + slot % P;
+  };
+  float mloc = -INFINITY;
+  for (int e = threadIdx.x; e < n; e += blockDim.x) {
+    const int64_t r = cache_row(e);
+    float x = -INFINITY;
+    if (r >= 0) {
+      const __nv_bfloat16 *k = kv + r * row_elems + static_cast<int64_t>(g) * D;
+      float a = 0.f;
+      for (int d = 0; d < D; ++d) a = fmaf(qs[d], __bfloat162float(k[d]), a);
+      x = a * scale_log2;
+    }
+    lg[e] = x;
+    mloc = fmaxf(mloc, x);
+  }
+  for (int o = 16; o; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x / 32] = mloc;
+  __syncthreads();
+  float m = -INFINITY;
+  for (int w = 0; w < static_cast<int>(blockDim.x / 32); ++w) m = fmaxf(m, red[w]);
+  __syncthreads();
+  float lloc = 0.f;
+  for (int e = threadIdx.x; e < n; e += blockDim.x) {
+    const float pe = lg[e] == -INFINITY ? 0.f : exp2f(lg[e] - m);
+    lg[e] = pe;
+    lloc += pe;
+  }
+  for (int o = 16; o; o >>= 1) lloc += __shfl_xor_sync(0xffffffffu, lloc, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x / 32] = lloc;
+  __syncthreads();
+  float lsum = 0.f;
+  for (int w = 0; w < static_cast<int>(blockDim.x / 32); ++w) lsum += red[w];
+  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    float acc = 0.f;
+    for (int e = 0; e < n; ++e) {
+      if (lg[e] == 0.f) continue;
+      const int64_t r = cache_row(e);
+      acc = fmaf(lg[e], __bfloat162float(kv[r * row_elems + static_cast<int64_t>(Hkv + g) * D + d]), acc);
+    }
+    out[(static_cast<int64_t>(row) * Hq + h) * D + d] = __float2bfloat16_rn(acc * inv);
+  }
+}
+
+template <int NG>
+cudaError_t run_msa_tc(const dsa_ctx *ctx, const dsa_plan_t *plan, const dsa_msa_shape_t &ms, const int32_t *sel,
+                       const void *q, const void *kv, float sm_scale, void *out, cudaStream_t s) {
+  MsaParams prm{};
+  const int BH = plan->box_rows;
+  const int P = ctx->cfg.page_size;
+  if (!encode_tiled_2d(&prm.tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void *>(kv),
+                       2 * static_cast<uint64_t>(ms.kv_heads) * 128, static_cast<uint64_t>(plan->cache_pages) * P,
+                       2 * static_cast<uint64_t>(ms.kv_heads) * 128 * 2, 64, BH, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if (!encode_tiled_2d(&prm.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void *>(q), 128,
+                       static_cast<uint64_t>(plan->T) * ms.q_heads, 256, 64, NG, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  prm.sel = sel;
+  prm.row_pos = plan->row_pos;
+  prm.row_page_off = plan->row_page_off;
+  prm.row_npages = plan->row_npages;
+  prm.row_page_start = plan->row_page_start;
+  prm.pages = plan->pages;
+  prm.out = static_cast<__nv_bfloat16 *>(out);
+  prm.err = ctx->err;
+  prm.Hq = ms.q_heads;
+  prm.Hkv = ms.kv_heads;
+  prm.group = ms.q_heads / ms.kv_heads;
+  prm.K = ms.topk_blocks;
+  prm.P = P;
+  prm.BH = BH;
+  prm.num_pages = plan->cache_pages;
+  prm.scale_log2 = sm_scale * kMsaLog2e;
+  prm.stages = MsaLayout(NG, 3, ms.kv_heads).bytes <= 227 * 1024 ? 3 : 2;
+  const int bytes = static_cast<int>(MsaLayout(NG, prm.stages, ms.kv_heads).bytes);
+  auto kern = msa_attend_tc_kernel<NG>;
+  // the limit is set to the largest layout this instance can have
+  static std::atomic<uint64_t> smem_limit_set{0};
+  if (cudaError_t e = ensure_smem_limit(kern, 227 * 1024, ctx->device, smem_limit_set); e != cudaSuccess) return e;
+  kern<<<plan->T, kMsaThreads, bytes, s>>>(prm);
+  return cudaGetLastError();
+}
+
+int msa_group_cols(int group) { return (group + 15) / 16 * 16; }
+
+}  // namespace
+
+bool msa_attend_tc_supported(const dsa_config_t &c, const dsa_msa_shape_t &ms, int box_rows) {
+  if (ms.block_size != kMsaTile || ms.head_dim != 128 || ms.kv_heads > kMsaMaxKvHeads) return false;
+  const int NG = msa_group_cols(ms.q_heads / ms.kv_heads);
+  if (NG != 16 && NG != 32 && NG != 64) return false;
+  if (2 * NG + ms.kv_heads * NG > 512) return false;
+  if (box_rows < 8 || c.page_size % box_rows != 0) return false;
+  return MsaLayout(NG, 2, ms.kv_heads).bytes <= 227 * 1024;
+}
+
+cudaError_t launch_msa_select(const dsa_ctx *ctx, const dsa_plan_t *plan, const dsa_msa_shape_t &ms,
+                              const float *scores, int32_t *sel, cudaStream_t s, int32_t *launches) {
+  const int smem = kSelMaxBlocks * 4;
+  static std::atomic<uint64_t> smem_limit_set{0};
+  if (cudaError_t e = ensure_smem_limit(msa_select_kernel, smem, ctx->device, smem_limit_set); e != cudaSuccess)
+    return e;
+  const int grid = std::min(plan->T, 4 * ctx->num_sms);
+  msa_select_kernel<<<std::max(1, grid), kSelThreads, smem, s>>>(scores, plan->row_score_off, plan->row_pos,
+                                                                  plan->T, ms.block_size, ms.topk_blocks, sel);
+  *launches += 1;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_msa_attend(const dsa_ctx *ctx, const dsa_plan_t *plan, const dsa_msa_shape_t &ms,
+                              const int32_t *sel, const void *q, const void *kv, float sm_scale, void *out,
+                              cudaStream_t s, int32_t *launches) {
+  cudaError_t e;
+  if (msa_attend_tc_supported(ctx->cfg, ms, plan->box_rows)) {
+    const int NG = msa_group_cols(ms.q_heads / ms.kv_heads);
+    if (NG == 16) e = run_msa_tc<16>(ctx, plan, ms, sel, q, kv, sm_scale, out, s);
+    else if (NG == 32) e = run_msa_tc<32>(ctx, plan, ms, sel, q, kv, sm_scale, out, s);
+    else e = run_msa_tc<64>(ctx, plan, ms, sel, q, kv, sm_scale, out, s);
+  } else {
+    const size_t sm = (static_cast<size_t>(ms.head_dim) + static_cast<size_t>(ms.topk_blocks) * ms.block_size + 32) *
+                      sizeof(float);
+    if (sm > 227 * 1024) return cudaErrorInvalidValue;
+    if (sm > 48 * 1024) {
+      e = cudaFuncSetAttribute(msa_attend_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(sm));
+      if (e != cudaSuccess) return e;
+    }
+    msa_attend_simt_kernel<<<plan->T * ms.q_heads, 128, sm, s>>>(
+        sel, static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(kv), plan->row_pos,
+        plan->row_page_off, plan->row_npages, plan->row_page_start, plan->pages, static_cast<__nv_bfloat16 *>(out),
+        ctx->err, ms.q_heads, ms.kv_heads, ms.head_dim, ms.block_size, ms.topk_blocks, ctx->cfg.page_size,
+        plan->cache_pages, sm_scale * kMsaLog2e);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) *launches += 1;
+  return e;
+}
+
+bool msa_select_supported(const dsa_plan_t *plan, const dsa_msa_shape_t &ms) {
+  return static_cast<int64_t>(plan->max_pos) / ms.block_size + 1 <= kSelMaxBlocks;
+}
+
+}  // namespace dsa
+
+// ----------------------------------------------------------------------------
+// C ABI
+// ----------------------------------------------------------------------------
+namespace {
+
+dsa_status msa_check(dsa_ctx_t *ctx, const dsa_plan_t *plan, const dsa_msa_shape_t *ms) {
+  if (!ctx || !plan || !ms || plan->ctx != ctx || ctx->device < 0) return DSA_ERR_INVALID_ARG;
+  if (ms->block_size <= 0 || ms->topk_blocks <= 0 || ms->q_heads <= 0 || ms->kv_heads <= 0 || ms->head_dim <= 0 ||
+      ms->reserved != 0 || ms->q_heads % ms->kv_heads != 0)
+    return DSA_ERR_INVALID_ARG;
+  if (ms->topk_blocks > dsa::kMsaMaxK || ms->head_dim % 8 != 0 || ms->head_dim > 1024) return DSA_ERR_UNSUPPORTED;
+  if (plan->capturable) return DSA_ERR_UNSUPPORTED;   // host plans only
+  if (cudaSetDevice(ctx->device) != cudaSuccess) return DSA_ERR_CUDA;
+  return DSA_OK;
+}
+
+dsa_status msa_status(dsa_ctx_t *ctx, cudaError_t e) {
+  if (e == cudaSuccess) return DSA_OK;
+  snprintf(ctx->last_cuda_error, sizeof(ctx->last_cuda_error), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+  return DSA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+dsa_status dsa_msa_select_blocks(dsa_ctx_t *ctx, const dsa_plan_t *plan, const dsa_msa_shape_t *shape,
+                                 const float *scores, int32_t *block_sel, dsa_stream_t stream) {
+  dsa_status st = msa_check(ctx, plan, shape);
+  if (st != DSA_OK) return st;
+  ctx->last_launches = 0;
+  if (!dsa::msa_select_supported(plan, *shape)) return DSA_ERR_UNSUPPORTED;
+  if (plan->T == 0) return DSA_OK;
+  if (!scores || !block_sel) return DSA_ERR_INVALID_ARG;
+  return msa_status(ctx, dsa::launch_msa_select(ctx, plan, *shape, scores, block_sel,
+                                                reinterpret_cast<cudaStream_t>(stream), &ctx->last_launches));
+}
+
+dsa_status dsa_msa_index_select(dsa_ctx_t *ctx, const dsa_plan_t *plan, const dsa_msa_shape_t *shape, const void *q,
+                                const float *w, const void *index_cache, int32_t *block_sel, dsa_stream_t stream) {
+  dsa_status st = msa_check(ctx, plan, shape);
+  if (st != DSA_OK) return st;
+  ctx->last_launches = 0;
+  if (!dsa::msa_select_supported(plan, *shape)) return DSA_ERR_UNSUPPORTED;
+  if (plan->T == 0) return DSA_OK;
+  if (!q || !w || !index_cache || !block_sel) return DSA_ERR_INVALID_ARG;
+  if (static_cast<size_t>(plan->num_scores) > ctx->scores_cap) return DSA_ERR_INVALID_ARG;   // plan of another size
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t n = 0;
+  cudaError_t e = dsa::launch_index_scores(ctx, plan, q, w, index_cache, ctx->scores, s, &n);
+  if (e == cudaSuccess) e = dsa::launch_msa_select(ctx, plan, *shape, ctx->scores, block_sel, s, &n);
+  ctx->last_launches = n;
+  return msa_status(ctx, e);
+}
+
+dsa_status dsa_msa_attend(dsa_ctx_t *ctx, const dsa_plan_t *plan, const dsa_msa_shape_t *shape,
+                          const int32_t *block_sel, const void *q, const void *kv_cache, float sm_scale, void *out,
+                          dsa_stream_t stream) {
+  dsa_status st = msa_check(ctx, plan, shape);
+  if (st != DSA_OK) return st;
+  ctx->last_launches = 0;
+  if (plan->T == 0) return DSA_OK;
+  if (!block_sel || !q || !kv_cache || !out) return DSA_ERR_INVALID_ARG;
+  if (!dsa::msa_attend_tc_supported(ctx->cfg, *shape, plan->box_rows) &&
+      (static_cast<size_t>(shape->head_dim) + static_cast<size_t>(shape->topk_blocks) * shape->block_size + 32) *
+              sizeof(float) >
+          227 * 1024)
+    return DSA_ERR_UNSUPPORTED;
+  return msa_status(ctx, dsa::launch_msa_attend(ctx, plan, *shape, block_sel, q, kv_cache, sm_scale, out,
+                                                reinterpret_cast<cudaStream_t>(stream), &ctx->last_launches));
+}
+
+int dsa_msa_attend_on_tensor_cores(const dsa_ctx_t *ctx, const dsa_plan_t *plan, const dsa_msa_shape_t *shape) {
+  if (!ctx || !plan || !shape || shape->kv_heads <= 0 || shape->q_heads % shape->kv_heads != 0) return 0;
+  return dsa::msa_attend_tc_supported(ctx->cfg, *shape, plan->box_rows) ? 1 : 0;
+}
+
+}  // extern "C"

@@ -45,7 +45,8 @@ EXPORTED = ["dsa_create", "dsa_destroy", "dsa_plan", "dsa_plan_destroy", "dsa_pl
             "dsa_last_launch_count", "dsa_status_str", "dsa_index_topk_static", "dsa_last_cuda_error",
             "dsa_quantize_store_keys", "dsa_quantize_store_latents", "dsa_attend_shared", "dsa_plan_capturable",
             "dsa_plan_update", "dsa_plan_read_counts", "dsa_quantize_q", "dsa_index_scores_fp8q",
-            "dsa_index_topk_fp8q", "dsa_selftest_wait_timeout"]
+            "dsa_index_topk_fp8q", "dsa_selftest_wait_timeout", "dsa_msa_select_blocks", "dsa_msa_index_select",
+            "dsa_msa_attend", "dsa_msa_attend_on_tensor_cores"]
 
 # dsa_device_span_t: q_len, ctx_start, page_start, page_off, num_pages, reserved (int32 each)
 DEVICE_SPAN_FIELDS = 6
@@ -68,6 +69,15 @@ class _Span(ctypes.Structure):
     _fields_ = [("request_id", ctypes.c_int64), ("q_start", ctypes.c_int32), ("q_len", ctypes.c_int32),
                 ("ctx_start", ctypes.c_int32), ("page_start", ctypes.c_int32), ("pages", ctypes.c_void_p),
                 ("num_pages", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class _MsaShape(ctypes.Structure):
+    _fields_ = [("block_size", ctypes.c_int32), ("topk_blocks", ctypes.c_int32), ("q_heads", ctypes.c_int32),
+                ("kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+def _msa_shape(ms) -> _MsaShape:
+    return _MsaShape(int(ms.block_size), int(ms.topk_blocks), int(ms.q_heads), int(ms.kv_heads), int(ms.head_dim), 0)
 
 
 class PlanInfo(ctypes.Structure):
@@ -118,6 +128,12 @@ def load() -> ctypes.CDLL:
     L.dsa_index_topk_fp8q.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
     L.dsa_get_error.argtypes = [vp, vp]
     L.dsa_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint64, vp, vp]
+    msp = ctypes.POINTER(_MsaShape)
+    L.dsa_msa_select_blocks.argtypes = [vp, vp, msp, vp, vp, vp]
+    L.dsa_msa_index_select.argtypes = [vp, vp, msp, vp, vp, vp, vp, vp]
+    L.dsa_msa_attend.argtypes = [vp, vp, msp, vp, vp, vp, ctypes.c_float, vp, vp]
+    L.dsa_msa_attend_on_tensor_cores.argtypes = [vp, vp, msp]
+    L.dsa_msa_attend_on_tensor_cores.restype = ctypes.c_int
     L.dsa_last_launch_count.argtypes = [vp]
     L.dsa_last_launch_count.restype = i32
     L.dsa_last_cuda_error.argtypes = [vp]
@@ -128,7 +144,7 @@ def load() -> ctypes.CDLL:
                  "dsa_index_scores", "dsa_topk_from_scores", "dsa_attend", "dsa_get_error", "dsa_quantize_store_keys",
                  "dsa_quantize_store_latents", "dsa_attend_shared", "dsa_plan_capturable", "dsa_plan_update",
                  "dsa_plan_read_counts", "dsa_quantize_q", "dsa_index_scores_fp8q", "dsa_index_topk_fp8q",
-                 "dsa_selftest_wait_timeout"):
+                 "dsa_selftest_wait_timeout", "dsa_msa_select_blocks", "dsa_msa_index_select", "dsa_msa_attend"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -328,6 +344,50 @@ class Context:
                                             _ptr(selection, d, (torch.int32,), "selection"), _stream(stream)),
                "dsa_index_topk_static", self.handle)
         return selection
+
+    # ------------------------------------------------------ block-sparse MSA
+    def msa_select_blocks(self, plan: Plan, msa, scores, block_sel=None, stream=None) -> torch.Tensor:
+        """dsa_msa_select_blocks: token scores -> (T, topk_blocks) int32 block ids."""
+        d = self.device
+        if block_sel is None:
+            block_sel = torch.empty(plan.num_rows, int(msa.topk_blocks), dtype=torch.int32, device=d)
+        ms = _msa_shape(msa)
+        _check(load().dsa_msa_select_blocks(self.handle, plan.handle, ctypes.byref(ms),
+                                            _ptr(scores, d, (torch.float32,), "scores"),
+                                            _ptr(block_sel, d, (torch.int32,), "block_sel"), _stream(stream)),
+               "dsa_msa_select_blocks", self.handle)
+        return block_sel
+
+    def msa_index_select(self, plan: Plan, msa, q, w, index_cache, block_sel=None, stream=None) -> torch.Tensor:
+        """dsa_msa_index_select: index scores (context scratch) + block selection."""
+        d = self.device
+        if block_sel is None:
+            block_sel = torch.empty(plan.num_rows, int(msa.topk_blocks), dtype=torch.int32, device=d)
+        ms = _msa_shape(msa)
+        _check(load().dsa_msa_index_select(self.handle, plan.handle, ctypes.byref(ms), _ptr(q, d, (torch.bfloat16,), "q"),
+                                           _ptr(w, d, (torch.float32,), "w"),
+                                           _ptr(index_cache, d, (torch.bfloat16, torch.uint8), "index_cache"),
+                                           _ptr(block_sel, d, (torch.int32,), "block_sel"), _stream(stream)),
+               "dsa_msa_index_select", self.handle)
+        return block_sel
+
+    def msa_attend(self, plan: Plan, msa, block_sel, q, kv_cache, sm_scale: float, out=None, stream=None):
+        """dsa_msa_attend: GQA attention over the kept blocks -> (T, q_heads, head_dim) bf16."""
+        d = self.device
+        if out is None:
+            out = torch.empty(plan.num_rows, int(msa.q_heads), int(msa.head_dim), dtype=torch.bfloat16, device=d)
+        ms = _msa_shape(msa)
+        _check(load().dsa_msa_attend(self.handle, plan.handle, ctypes.byref(ms),
+                                     _ptr(block_sel, d, (torch.int32,), "block_sel"),
+                                     _ptr(q, d, (torch.bfloat16,), "q"),
+                                     _ptr(kv_cache, d, (torch.bfloat16,), "kv_cache"), ctypes.c_float(sm_scale),
+                                     _ptr(out, d, (torch.bfloat16,), "out"), _stream(stream)),
+               "dsa_msa_attend", self.handle)
+        return out
+
+    def msa_attend_on_tensor_cores(self, plan: Plan, msa) -> bool:
+        ms = _msa_shape(msa)
+        return bool(load().dsa_msa_attend_on_tensor_cores(self.handle, plan.handle, ctypes.byref(ms)))
 
     def quantize_q(self, plan: Plan, q_bf16, codes=None, scales=None, stream=None):
         """dsa_quantize_q: the indexer query (T, 64, 128) bf16 -> (codes uint8 of the

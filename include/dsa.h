@@ -332,6 +332,59 @@ dsa_status dsa_plan_read_counts(const dsa_plan_t *plan, int32_t counts[8]);
  * DSA_ERR_CUDA. */
 dsa_status dsa_get_error(dsa_ctx_t *ctx, dsa_stream_t stream);
 
+/* ---- Block-sparse MSA -----------------------------------------------------
+ * LLMServingSim, "Sparse attention (DSA and block-sparse MSA)", table "Two
+ * shapes, three checkpoints", MiniMax-M3 column: each row keeps the top 16
+ * blocks of 128 tokens and attends over them with plain GQA; the index cache
+ * holds one bf16 vector per token.  The pages give no block-scoring formula;
+ * these calls implement the reading: a token's score is the DSA indexer score
+ * (dsa_index_scores over the context's index cache and shape), a block's
+ * score is the largest score among the positions the row sees, the selection
+ * is the causal top-k over blocks (ties to the lower block), and attention
+ * covers the positions <= the row's own in the kept blocks.
+ *
+ * Blocks are counted in request positions: block b of a request holds
+ * positions b*block_size .. (b+1)*block_size - 1.  The calls use the context's
+ * index format, index shape and page size and a HOST plan (dsa_plan; its topk
+ * and MLA fields are not read); capturable plans get DSA_ERR_UNSUPPORTED.
+ *
+ * dsa_msa_select_blocks: scores as from dsa_index_scores (each row's pos+1
+ *   scores at the plan's offsets) -> block_sel (T, topk_blocks) int32: the
+ *   kept block ids in ascending order, then -1 (rows that see at most
+ *   topk_blocks blocks keep them all).  DSA_ERR_UNSUPPORTED when a row has more
+ *   than 16,384 blocks or topk_blocks > 64.
+ * dsa_msa_index_select: dsa_index_scores into the context's scratch, then
+ *   dsa_msa_select_blocks.
+ * dsa_msa_attend: block_sel (T, topk_blocks) int32 (any order, -1 skipped; an
+ *   id outside 0 .. pos/block_size sets DSA_ERR_BOUNDS and is skipped);
+ *   q (T, q_heads, head_dim) bf16; kv_cache [pages][page_size][2 * kv_heads *
+ *   head_dim] bf16 per token: K of kv heads 0..kv_heads-1, then V of the same
+ *   heads; query head h reads kv head h / (q_heads / kv_heads);
+ *   out (T, q_heads, head_dim) bf16 = softmax((q . k_j) * sm_scale) . v_j over
+ *   the kept positions j, fp32 accumulation.  block_size 128 and head_dim 128
+ *   with a group of at most 64 query heads, at most 8 kv heads and a page size
+ *   that is a multiple of 8 run on the tensor cores
+ *   (dsa_msa_attend_on_tensor_cores); other shapes run a CUDA-core kernel.
+ * Device pointers, caller-owned.  DSA_ERR_INVALID_ARG for null pointers, a
+ * q_heads that is not a multiple of kv_heads or a nonzero reserved field. */
+typedef struct dsa_msa_shape {
+  int32_t block_size;    /* tokens per block (128 on the pages' MiniMax-M3 row) */
+  int32_t topk_blocks;   /* blocks kept per row (16), at most 64 */
+  int32_t q_heads;       /* query heads */
+  int32_t kv_heads;      /* key/value heads (GQA groups) */
+  int32_t head_dim;      /* per-head width of q, K and V */
+  int32_t reserved;      /* set to 0 */
+} dsa_msa_shape_t;
+dsa_status dsa_msa_select_blocks(dsa_ctx_t *ctx, const dsa_plan_t *plan, const dsa_msa_shape_t *shape,
+                                 const float *scores, int32_t *block_sel, dsa_stream_t stream);
+dsa_status dsa_msa_index_select(dsa_ctx_t *ctx, const dsa_plan_t *plan, const dsa_msa_shape_t *shape, const void *q,
+                                const float *w, const void *index_cache, int32_t *block_sel, dsa_stream_t stream);
+dsa_status dsa_msa_attend(dsa_ctx_t *ctx, const dsa_plan_t *plan, const dsa_msa_shape_t *shape,
+                          const int32_t *block_sel, const void *q, const void *kv_cache, float sm_scale, void *out,
+                          dsa_stream_t stream);
+/* 1 when dsa_msa_attend runs this shape on the tensor cores, else 0 (host-side query). */
+int dsa_msa_attend_on_tensor_cores(const dsa_ctx_t *ctx, const dsa_plan_t *plan, const dsa_msa_shape_t *shape);
+
 /* Drive the pipeline's bounded wait to its limit, for testing the failure
  * path (mstar IndexKeyStore.history: a failure is reported to the caller, not
  * fatal).  One CTA takes tensor memory, waits on an mbarrier that nothing

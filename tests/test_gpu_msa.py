@@ -1,0 +1,143 @@
+"""GPU parity for block-sparse MSA (LLMServingSim, "Sparse attention (DSA and
+block-sparse MSA)", MiniMax-M3 column): the CUDA block selection and GQA
+attention through the C ABI against the CPU oracle on the same seeded inputs,
+at small sizes (every row) and at the msa_decode workload's full size
+(sampled rows recomputed by the oracle)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from deepseek_sparse_attention_dsa_gb300 import dsa
+from deepseek_sparse_attention_dsa_gb300 import workloads as W
+from tests import harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from deepseek_sparse_attention_dsa_gb300 import build
+    build.build()
+
+
+def _inputs(wl, device="cpu"):
+    return (W.make_index_cache(wl, device=device), W.make_kv_cache(wl, device=device),
+            W.make_step_inputs(wl, device=device), W.make_msa_q(wl, device=device))
+
+
+def _run(wl, expect_tc=True, exact_selection=False):
+    ms = wl.msa
+    ic, kv, st, q = _inputs(wl)
+    ref = oracle.msa_run_all(wl, ic, kv, st, q)
+    ctx = dsa.Context(wl.shape, 0)
+    plan = ctx.plan(wl.spans, wl.num_pages)
+    assert ctx.msa_attend_on_tensor_cores(plan, ms) == expect_tc
+    icd, kvd, qd = ic.cuda(), kv.cuda(), q.cuda()
+    ctx.store_keys(plan, st.keys.cuda(), icd)
+    scores = ctx.index_scores(plan, st.q.cuda(), st.w.cuda(), icd)
+    sel = ctx.msa_select_blocks(plan, ms, scores)
+    sel2 = ctx.msa_index_select(plan, ms, st.q.cuda(), st.w.cuda(), icd)
+    out = ctx.msa_attend(plan, ms, sel, qd, kvd, ms.sm_scale)
+    ctx.get_error()
+    assert torch.equal(sel, sel2)
+    H.check_scores(scores.cpu().numpy()[:plan.num_scores], ref["scores"], ref["offsets"])
+    # the GPU's blocks against the oracle's, under the block scores the oracle computed
+    H.check_selection(sel.cpu().numpy(), ref["selection"], ref["block_scores"], ref["block_offsets"],
+                      ms.topk_blocks, exact=exact_selection)
+    # the selection of the oracle's own scores is the oracle's, exactly
+    sel_o = ctx.msa_select_blocks(plan, ms, torch.from_numpy(ref["scores"]).cuda())
+    ctx.get_error()
+    H.check_selection(sel_o.cpu().numpy(), ref["selection"], ref["block_scores"], ref["block_offsets"],
+                      ms.topk_blocks, exact=True)
+    # end to end: the oracle attends over the GPU's selection
+    ref_e2e = oracle.msa_attend(ms, wl.spans, wl.num_pages, sel.cpu().numpy(), q, kv)
+    H.check_attention(out.float().cpu().numpy(), ref_e2e)
+    # decoupled: the GPU attends over the oracle's selection (score-ordered)
+    out_o = ctx.msa_attend(plan, ms, torch.from_numpy(ref["selection"]).cuda(), qd, kvd, ms.sm_scale)
+    ctx.get_error()
+    H.check_attention(out_o.float().cpu().numpy(), ref["out"])
+    plan.close()
+    return ref
+
+
+def test_msa_small():
+    _run(W.msa_config("msa_small"))
+
+
+def test_msa_integer_index_inputs_select_exactly():
+    """Integer-valued index keys and queries make every token score exact, so
+    the block selection must be the oracle's set exactly, ties included."""
+    wl = W.msa_config("msa_small", seed=2101)
+    wl.dist = W.Distributions(w=("uniform", 0.0, 1.0 / 8), integer=True)
+    _run(wl, exact_selection=True)
+
+
+def test_msa_page_start_off_the_box_boundary():
+    """Token 0 at slots 5, 37 and 70: every block spans two tiles of the
+    attention; rows outside the kept blocks are masked and their V rows zeroed."""
+    _run(W.msa_config("msa_small", seed=2102, page_start=[5, 37, 70]))
+
+
+def test_msa_more_heads_per_group_and_one_kv_head():
+    """Other tensor-core instances: 32 query heads on one kv head (N = 32), 40
+    heads over 2 kv heads (a group of 20 padded to 32)."""
+    for qh, kh, seed in ((32, 1, 2103), (40, 2, 2104)):
+        wl = W.msa_config("msa_small", seed=seed)
+        wl.msa = W.MSAShape(topk_blocks=4, q_heads=qh, kv_heads=kh)
+        _run(wl)
+
+
+def test_msa_cuda_core_shapes():
+    """Shapes outside the tensor-core kernel (head_dim 64, blocks of 64) run the
+    CUDA-core kernel, checked the same way."""
+    wl = W.msa_config("msa_small", seed=2105)
+    wl.msa = W.MSAShape(block_size=64, topk_blocks=6, q_heads=8, kv_heads=2, head_dim=64,
+                        sm_scale=1.0 / np.sqrt(64.0))
+    _run(wl, expect_tc=False)
+
+
+def test_msa_decode_full_size_sampled_rows():
+    """msa_decode at full size (128 rows at 64K-128K, top 16 blocks of 128, 64
+    query heads over 4 kv heads): the whole step on the GPU in the bench's
+    launch configuration, 16 sampled rows recomputed by the oracle."""
+    wl = W.msa_config("msa_decode")
+    ms, sh = wl.msa, wl.shape
+    dev = torch.device("cuda", 0)
+    ic = W.make_index_cache(wl, device=dev)
+    kv = W.make_kv_cache(wl, device=dev)
+    st = W.make_step_inputs(wl, device=dev)
+    q = W.make_msa_q(wl, device=dev)
+    ctx = dsa.Context(sh, 0)
+    plan = ctx.plan(wl.spans, wl.num_pages)
+    assert ctx.msa_attend_on_tensor_cores(plan, ms)
+    ctx.store_keys(plan, st.keys, ic)
+    scores = ctx.index_scores(plan, st.q, st.w, ic)
+    sel = ctx.msa_select_blocks(plan, ms, scores)
+    out = ctx.msa_attend(plan, ms, sel, q, kv, ms.sm_scale)
+    ctx.get_error()
+    _, pos_all, _ = wl.row_table()
+    off_all = np.zeros(wl.num_rows + 1, np.int64)
+    np.cumsum(pos_all + 1, out=off_all[1:])
+    rng = np.random.default_rng(7)
+    for span_i in rng.choice(len(wl.spans), size=16, replace=False):
+        row = wl.spans[span_i].q_start
+        rw = wl.row_workload(int(span_i), 0)
+        ric = W.make_index_cache(rw)
+        rst = W.make_step_inputs(rw)
+        cache = oracle.store_keys(sh, rw.spans, rw.num_pages, rst.keys, ric)
+        sc, off = oracle.index_scores(sh, rw.spans, rw.num_pages, rst.q, rst.w, cache)
+        H.check_scores(scores[off_all[row]:off_all[row + 1]].cpu().numpy(), sc, off)
+        bsc, boff = oracle.msa_block_scores(ms, rw.spans, sc, off)
+        osel = oracle.msa_select(ms, rw.spans, bsc, boff)
+        g_sel = sel[row:row + 1].cpu().numpy()
+        H.check_selection(g_sel, osel, bsc, boff, ms.topk_blocks)
+        # attention over the GPU's blocks, recomputed from the rows they hold
+        p = int(pos_all[row])
+        toks = set()
+        for b in g_sel[0][g_sel[0] >= 0]:
+            toks.update(rw.spans[0].token_base + np.arange(b * ms.block_size, min((b + 1) * ms.block_size, p + 1)))
+        rkv = W.make_kv_cache(rw, tokens=toks)
+        rq = W.make_msa_q(rw)
+        ref = oracle.msa_attend(ms, rw.spans, rw.num_pages, g_sel, rq, rkv)
+        H.check_attention(out[row:row + 1].float().cpu().numpy(), ref)
