@@ -27,6 +27,10 @@ chunked_prefill and mixed_fp8) in the same process at the same steps and
 warm-up, reported under `prefill`: tokens/s, the stage split, and the
 indexer's and the attention's TFLOP/s as fractions of the measured dense bf16
 peak, with the clocks of that leg.
+Block-sparse MSA workloads (`--msa`, default msa_decode and msa_prefill) are
+timed the same way and reported under `msa`: store, index score, block
+selection and GQA attention over the kept blocks, with the attention's GB/s
+and TFLOP/s against the measured peaks.
 `--impl reference` times the CPU oracle (the only reference this method has)
 on a bounded sample of the same workload on the host cores.
 Multi-GPU (torchrun): independent replicas, one per rank (weak scaling).
@@ -256,6 +260,122 @@ def prefill_leg(args, name, rank, world, dev, flush):
            "gpu_launches": n_launch, "clocks": clk, "config": workload_config(name, wl)}
     plan.close()
     del ic, lc, st, scores, sel, out
+    torch.cuda.empty_cache()
+    return leg
+
+
+def msa_work(wl, block_sel=None):
+    """Algorithmic work of an MSA step.  Attention: every kept position read
+    once (K and V of all kv heads), q in, out back, the block ids; flops of
+    QK and PV over the kept positions.  Without a selection, the count assumes
+    each row keeps min(topk_blocks, its blocks) full blocks."""
+    sh, ms = wl.shape, wl.msa
+    _, pos, _ = wl.row_table()
+    vis = pos + 1
+    T = len(pos)
+    if block_sel is None:
+        kept = np.minimum(vis, ms.topk_blocks * ms.block_size)
+    else:
+        kept = np.zeros(T, np.int64)
+        for r in range(T):
+            b = block_sel[r][block_sel[r] >= 0].astype(np.int64)
+            kept[r] = int(np.clip(pos[r] + 1 - b * ms.block_size, 0, ms.block_size).sum())
+    idx_bytes = float(vis.sum()) * sh.index_row_bytes + T * (sh.index_heads * sh.index_dim * 2 + sh.index_heads * 4)
+    att_bytes = float(kept.sum()) * ms.kv_row_bytes + T * ms.q_heads * ms.head_dim * 2 * 2 + T * ms.topk_blocks * 4
+    return dict(rows=T, index_bytes=idx_bytes, attend_bytes=att_bytes,
+                step_bytes=idx_bytes + att_bytes + T * sh.index_row_bytes * 2,
+                index_flops=float(vis.sum()) * 2.0 * sh.index_heads * sh.index_dim,
+                attend_flops=float(kept.sum()) * 4.0 * ms.q_heads * ms.head_dim, kept=int(kept.sum()))
+
+
+def msa_leg(args, name, rank, world, dev, flush):
+    """A block-sparse MSA workload (store keys, index score, block selection,
+    GQA attention over the kept blocks) timed like the headline step."""
+    from deepseek_sparse_attention_dsa_gb300 import dsa
+    wl = W.msa_config(name, seed=2000 + W.MSA_CONFIG_NAMES.index(name) + 7919 * rank)
+    sh, ms = wl.shape, wl.msa
+    unit, decode = unit_of(wl)
+    ic = W.make_index_cache(wl, device=dev)
+    kv = W.make_kv_cache(wl, device=dev)
+    st = W.make_step_inputs(wl, device=dev)
+    q = W.make_msa_q(wl, device=dev)
+    ctx = dsa.Context(sh, dev.index)
+    plan = ctx.plan(wl.spans, wl.num_pages)
+    scores = torch.empty(max(1, plan.num_scores), dtype=torch.float32, device=dev)
+    bsel = torch.empty(plan.num_rows, ms.topk_blocks, dtype=torch.int32, device=dev)
+    out = torch.empty(plan.num_rows, ms.q_heads, ms.head_dim, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    launches = [0]
+
+    def step(record):
+        if record:
+            ev[0].record(stream)
+        ctx.store_keys(plan, st.keys, ic)
+        n = ctx.last_launch_count()
+        if record:
+            ev[1].record(stream)
+        ctx.index_scores(plan, st.q, st.w, ic, scores)
+        n += ctx.last_launch_count()
+        if record:
+            ev[2].record(stream)
+        ctx.msa_select_blocks(plan, ms, scores, bsel)
+        n += ctx.last_launch_count()
+        if record:
+            ev[3].record(stream)
+        ctx.msa_attend(plan, ms, bsel, q, kv, ms.sm_scale, out)
+        n += ctx.last_launch_count()
+        if record:
+            ev[4].record(stream)
+        launches[0] = n
+
+    for _ in range(args.warmup):
+        step(False)
+    ctx.get_error()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    stage = {"store": [], "index": [], "select": [], "attend": [], "step": []}
+    n_launch = 0
+    with ClockSampler(dev.index) as clk:
+        for _ in range(args.steps):
+            flush.zero_()
+            step(True)
+            n_launch += launches[0]
+            ev[4].synchronize()
+            for k, (a, b) in zip(("store", "index", "select", "attend", "step"),
+                                 ((0, 1), (1, 2), (2, 3), (3, 4), (0, 4))):
+                stage[k].append(ev[a].elapsed_time(ev[b]))
+    torch.cuda.synchronize(dev)
+    ctx.get_error()
+    total_ms = float(sum(stage["step"]))
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    work = msa_work(wl, bsel.cpu().numpy())
+    hbm, bf16, _, peak_kind = measured_peaks()
+    idx_ms = statistics.mean(stage["index"])
+    att_ms = statistics.mean(stage["attend"])
+    att_gbs = work["attend_bytes"] / (att_ms / 1e3) / 1e9
+    att_tf = work["attend_flops"] / (att_ms / 1e3) / 1e12
+    idx_gbs = work["index_bytes"] / (idx_ms / 1e3) / 1e9
+    leg = {"workload": name, "value": round(work["rows"] * world / (ms_step / 1e3), 2), "unit": unit,
+           "ms_per_step": round(ms_step, 4), "stages_ms": {k: round(statistics.mean(v), 4) for k, v in stage.items()},
+           "attend_kernel": "msa_attend_tc_kernel" if ctx.msa_attend_on_tensor_cores(plan, ms) else "msa_attend_simt_kernel",
+           "attend_gbs": round(att_gbs, 1), "attend_hbm_frac": round(att_gbs / hbm, 4),
+           "attend_tflops": round(att_tf, 2), "attend_tensor_frac": round(att_tf / bf16, 4),
+           "index_gbs": round(idx_gbs, 1), "index_hbm_frac": round(idx_gbs / hbm, 4),
+           "step_hbm_frac": round(work["step_bytes"] / (ms_step / 1e3) / 1e9 / hbm, 4),
+           "attend_bytes_per_step": work["attend_bytes"], "kept_positions": work["kept"],
+           "peaks": {"hbm_gbs": hbm, "bf16_tflops": bf16, "kind": peak_kind},
+           "gpu_launches": n_launch, "clocks": clk.summary(),
+           "config": dict(workload_config(name, wl), msa="top %d blocks of %d, GQA %d q / %d kv heads x %d"
+                          % (ms.topk_blocks, ms.block_size, ms.q_heads, ms.kv_heads, ms.head_dim))}
+    plan.close()
+    del ic, kv, st, q, scores, bsel, out
     torch.cuda.empty_cache()
     return leg
 
@@ -500,6 +620,8 @@ def run_ours(args, name, rank, world, local_rank):
     }
     if args.prefill and decode and not args.requests and not args.page_start:
         line["prefill"] = [prefill_leg(args, p, rank, world, dev, flush) for p in args.prefill.split(",") if p]
+    if args.msa and decode and not args.requests and not args.page_start:
+        line["msa"] = [msa_leg(args, m, rank, world, dev, flush) for m in args.msa.split(",") if m]
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_rows)
     return line
@@ -674,6 +796,8 @@ def main():
                     help="decode workloads: time the eager calls over a host plan instead of the captured step")
     ap.add_argument("--prefill", default="chunked_prefill,mixed_fp8",
                     help="decode workloads: prefill workloads timed in the same run (comma list; '' for none)")
+    ap.add_argument("--msa", default="msa_decode,msa_prefill",
+                    help="decode workloads: block-sparse MSA workloads timed in the same run (comma list; '' for none)")
     ap.add_argument("--page-start", type=int, default=0,
                     help="every request's token 0 at this slot of its first page (0 in the evaluation workloads)")
     ap.add_argument("--requests", type=int, default=0,

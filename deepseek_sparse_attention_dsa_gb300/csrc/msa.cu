@@ -22,9 +22,11 @@
 //     O^T_g[dim, head] += V[:, dim]^T . P^T[:, head]     (M = 128 dims, A = V read MN-major, B = P^T)
 // Warp 0 issues the TMA loads of a step's K and V boxes (the paged cache as
 // a 2-D tensor, 128-byte swizzle) into a ring of stages, warp 1 issues the
-// MMAs (QK of step t+1 before PV of step t), and four softmax warps
-// (thread = TMEM lane = token of S, dim of O) reduce each head's maximum with
-// redux.sync over order keys and its sum with shuffles, keep a per-head
+// MMAs (QK of step t+1 before PV of step t waits for its P), and eight
+// softmax warps, two per TMEM lane quadrant (thread = TMEM lane = token of S,
+// dim of O; each warp of a pair takes half of the heads), reduce each head's
+// maximum with redux.sync over order keys and its sum with halving shuffle
+// exchanges, keep a per-head
 // reference max that moves only when it grows by more than 2^8 (O is then
 // rescaled in TMEM), write P^T as bf16 in the 128-byte-swizzled K-major
 // layout, and normalise at the end.  Tiles start on the box boundary below
@@ -56,7 +58,8 @@ constexpr int kSelMaxBlocks = 16384;          // blocks per row held in shared m
 constexpr int kMsaMaxK = 64;                  // topk_blocks
 constexpr int kMsaTile = 128;                 // positions per tile (UMMA M)
 constexpr int kMsaMaxTiles = 2 * kMsaMaxK;
-constexpr int kMsaThreads = 192;              // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+constexpr int kMsaThreads = 320;              // warp 0 TMA, warp 1 MMA, warps 2-9 softmax (two per lane quadrant)
+constexpr int kMsaSoftThreads = 256;
 constexpr int kMsaMaxKvHeads = 8;
 
 __device__ __forceinline__ uint32_t score_key(float f) {
@@ -155,6 +158,41 @@ __global__ void __launch_bounds__(kSelThreads) msa_select_kernel(const float *__
 // ---------------------------------------------------------------------------
 // GQA attention over the selected blocks, tensor cores
 // ---------------------------------------------------------------------------
+// 2^x with the MUFU approximation (relative error ~2^-22; the results feed
+// bf16 probabilities and a lazily moved reference max).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Sums over the warp of N per-lane values (N = 16 or 32) by halving
+// exchanges: at each step a lane keeps half of its values and adds the
+// partner's copy of them, so N - 1 shuffles replace 5 N.  The lane ends with
+// the sum of value (lane >> (5 - log2 N)): N = 8, lanes 4h..4h+3 hold value
+// h; N = 16, lanes 2h and 2h+1; N = 32, lane h.
+template <int N>
+__device__ __forceinline__ float warp_sum_transpose(const float (&in)[N]) {
+  static_assert(N == 8 || N == 16 || N == 32, "values per lane");
+  float v[N];
+#pragma unroll
+  for (int k = 0; k < N; ++k) v[k] = in[k];
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int c = N, j = 4; c > 1; c >>= 1, --j) {
+    const bool up = (lane >> j) & 1;
+#pragma unroll
+    for (int k = 0; k < c / 2; ++k) {
+      const float send = up ? v[k] : v[k + c / 2];
+      const float keep = up ? v[k + c / 2] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 1 << j);
+    }
+  }
+#pragma unroll
+  for (int j = (N == 8 ? 1 : N == 16 ? 0 : -1); j >= 0; --j) v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1 << j);
+  return v[0];
+}
+
 struct MsaParams {
   CUtensorMap tm_kv;   // kv cache as [pages*P, 2*Hkv*128] bf16, box {64, BH}, 128-byte swizzle
   CUtensorMap tm_q;    // q as [T*Hq, 128] bf16, box {64, NG}, 128-byte swizzle
@@ -174,8 +212,8 @@ struct MsaLayout {
     off_q = stages * stage;
     off_p = off_q + Hkv * 2 * NG * 128;
     off_red = off_p + 2 * 2 * NG * 128;
-    off_ml = off_red + 2 * 4 * NG * 4;
-    off_tiles = off_ml + 2 * Hkv * NG * 4;
+    off_ml = off_red + 2 * 8 * NG * 4;          // [step parity][max keys | sums][NG][4 quads]
+    off_tiles = off_ml + 3 * Hkv * NG * 4;      // m [tile parity][Hkv][NG], l [Hkv][NG]
     off_bar = (off_tiles + 2 * kMsaMaxTiles * 4 + 7) / 8 * 8;
     off_misc = off_bar + 24 * 8;
     bytes = off_misc + 16 + 1024;   // + alignment slack
@@ -199,21 +237,22 @@ __global__ void __launch_bounds__(kMsaThreads, 1) msa_attend_tc_kernel(const __g
   const uint32_t bar0 = sbase + lay.off_bar;
   auto kfull = [&](int s) { return bar0 + 8u * s; };
   auto vfull = [&](int s) { return bar0 + 8u * (3 + s); };
-  auto kempty = [&](int s) { return bar0 + 8u * (6 + s); };
-  auto sfull = [&](int b) { return bar0 + 8u * (9 + b); };
-  auto sempty = [&](int b) { return bar0 + 8u * (11 + b); };
-  auto pfull = [&](int b) { return bar0 + 8u * (13 + b); };
-  auto pempty = [&](int b) { return bar0 + 8u * (15 + b); };
-  const uint32_t b_pvdone = bar0 + 8u * 17, b_qfull = bar0 + 8u * 18;
+  auto kempty = [&](int s) { return bar0 + 8u * (6 + s); };   // the stage's K half is free (its QK completed)
+  auto vempty = [&](int s) { return bar0 + 8u * (9 + s); };   // the stage's V half is free (its PV completed)
+  auto sfull = [&](int b) { return bar0 + 8u * (12 + b); };
+  auto sempty = [&](int b) { return bar0 + 8u * (14 + b); };
+  auto pfull = [&](int b) { return bar0 + 8u * (16 + b); };
+  auto pempty = [&](int b) { return bar0 + 8u * (18 + b); };
+  const uint32_t b_pvdone = bar0 + 8u * 20, b_qfull = bar0 + 8u * 21;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + lay.off_misc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + lay.off_misc + 4);
   int *ntiles_sm = reinterpret_cast<int *>(smem + lay.off_misc + 8);
   int32_t *tile_u = reinterpret_cast<int32_t *>(smem + lay.off_tiles);
   int32_t *tile_fl = tile_u + kMsaMaxTiles;
-  float *m_sm = reinterpret_cast<float *>(smem + lay.off_ml);
-  float *l_sm = m_sm + Hkv * NG;
-  uint32_t *redmax = reinterpret_cast<uint32_t *>(smem + lay.off_red);   // [4 quads][NG]
-  float *redsum = reinterpret_cast<float *>(smem + lay.off_red) + 4 * NG;  // [4 quads][NG]
+  float *m_sm = reinterpret_cast<float *>(smem + lay.off_ml);   // [tile parity][Hkv][NG]
+  float *l_sm = m_sm + 2 * Hkv * NG;                            // [Hkv][NG]
+  uint32_t *redmax = reinterpret_cast<uint32_t *>(smem + lay.off_red);       // [step parity] at stride 8*NG: [NG][4]
+  float *redsum = reinterpret_cast<float *>(smem + lay.off_red) + 4 * NG;    // the same, after the maxima
 
   const int warp = threadIdx.x / 32, lane = lane_id();
   const int row = blockIdx.x;
@@ -279,11 +318,12 @@ __global__ void __launch_bounds__(kMsaThreads, 1) msa_attend_tc_kernel(const __g
       mbar_init(kfull(s), 1);
       mbar_init(vfull(s), 1);
       mbar_init(kempty(s), 1);
+      mbar_init(vempty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(sfull(b), 1);
-      mbar_init(sempty(b), 4);   // one arrival per softmax warp
-      mbar_init(pfull(b), 4);
+      mbar_init(sempty(b), 8);   // one arrival per softmax warp
+      mbar_init(pfull(b), 8);
       mbar_init(pempty(b), 1);
     }
     mbar_init(b_pvdone, 1);
@@ -315,14 +355,11 @@ __global__ void __launch_bounds__(kMsaThreads, 1) msa_attend_tc_kernel(const __g
           tma_load_2d(sbase + lay.off_q + g * QG + c * NG * 128, &p.tm_q, c * 64, row * p.Hq + g * p.group, b_qfull);
     }
     const int nbox = kMsaTile / p.BH;
-    int issued = 0;
+    int issued_k = 0, issued_v = 0;
     for (int t = 0; t < nsteps; ++t) {
       const int ti = t / Hkv, g = t - ti * Hkv;
       const int u = tile_u[ti];
       const int st = t % S;
-      bool ok = true;
-      if (lane == 0) ok = mbar_wait(kempty(st), ((t / S) & 1) ^ 1, abort_flag, p.err);
-      if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) break;
       // lane b: box b of the tile (positions q0 .. q0+BH-1), loaded when it
       // holds a position 0 .. pos and its page exists
       int crow = -1;
@@ -338,34 +375,38 @@ __global__ void __launch_bounds__(kMsaThreads, 1) msa_attend_tc_kernel(const __g
       }
       const uint32_t valid = __ballot_sync(0xffffffffu, crow >= 0);
       const uint32_t bytes = __popc(valid) * p.BH * 128 * 2;
-      if (lane == 0) {
-        if (bytes) {
-          mbar_arrive_expect_tx(kfull(st), bytes);
-          mbar_arrive_expect_tx(vfull(st), bytes);
-        } else {
-          mbar_arrive(kfull(st));
-          mbar_arrive(vfull(st));
+      const uint32_t kst = sbase + st * STAGE, vst = kst + KVB;
+      // K once the stage's previous K has been read by its QK, V once its
+      // previous PV completed: the keys of a step run ahead of its values
+      bool ok = true;
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        const uint32_t full = half ? vfull(st) : kfull(st);
+        if (lane == 0) ok = mbar_wait(half ? vempty(st) : kempty(st), ((t / S) & 1) ^ 1, abort_flag, p.err);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        if (lane == 0) {
+          if (bytes) mbar_arrive_expect_tx(full, bytes);
+          else mbar_arrive(full);
         }
-      }
-      __syncwarp();
-      if (crow >= 0) {
-        const uint32_t kst = sbase + st * STAGE, vst = kst + KVB;
+        __syncwarp();
+        if (crow >= 0) {
+          const uint32_t dst = (half ? vst : kst) + lane * p.BH * 128;
+          const int x0 = (half * Hkv + g) * 128;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          tma_load_2d(kst + c * CH + lane * p.BH * 128, &p.tm_kv, g * 128 + c * 64, crow, kfull(st));
-          tma_load_2d(vst + c * CH + lane * p.BH * 128, &p.tm_kv, (Hkv + g) * 128 + c * 64, crow, vfull(st));
+          for (int c = 0; c < 2; ++c) tma_load_2d(dst + c * CH, &p.tm_kv, x0 + c * 64, crow, full);
         }
+        if (half) issued_v = t + 1;
+        else issued_k = t + 1;
       }
-      issued = t + 1;
+      if (!ok) break;
     }
     // nothing of ours may still be landing when the CTA leaves: wait (bounded,
     // whatever the abort flag says) for the loads of the last stages issued
     if (lane == 0) {
       volatile int no_abort = 0;
-      for (int t = max(0, issued - S); t < issued; ++t) {
-        mbar_wait(kfull(t % S), (t / S) & 1, &no_abort, p.err);
-        mbar_wait(vfull(t % S), (t / S) & 1, &no_abort, p.err);
-      }
+      for (int t = max(0, issued_k - S); t < issued_k; ++t) mbar_wait(kfull(t % S), (t / S) & 1, &no_abort, p.err);
+      for (int t = max(0, issued_v - S); t < issued_v; ++t) mbar_wait(vfull(t % S), (t / S) & 1, &no_abort, p.err);
       mbar_wait(b_qfull, 0, &no_abort, p.err);
     }
     __syncwarp();
@@ -373,11 +414,8 @@ __global__ void __launch_bounds__(kMsaThreads, 1) msa_attend_tc_kernel(const __g
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       bool ok = mbar_wait(b_qfull, 0, abort_flag, p.err);
-      auto pv = [&](int t) -> bool {
+      auto issue_pv = [&](int t) {
         const int st = t % S;
-        if (!mbar_wait(vfull(st), (t / S) & 1, abort_flag, p.err)) return false;
-        if (!mbar_wait(pfull(t & 1), (t >> 1) & 1, abort_flag, p.err)) return false;
-        tc_fence_after();
         const int ti = t / Hkv, g = t - ti * Hkv;
         const uint32_t vaddr = sbase + st * STAGE + KVB;
         const uint32_t paddr = sbase + lay.off_p + (t & 1) * PB;
@@ -389,17 +427,12 @@ __global__ void __launch_bounds__(kMsaThreads, 1) msa_attend_tc_kernel(const __g
           const uint64_t bd = smem_desc(paddr + (k >> 2) * NG * 128 + (k & 3) * 32, 16, 1024, kSwizzle128);
           mma_f16_ss(tmem_base + 2 * NG + g * NG, ad, bd, IDESC_PV, (ti > 0 || k > 0) ? 1u : 0u);
         }
-        mma_commit(kempty(st));
+        mma_commit(vempty(st));
         mma_commit(pempty(t & 1));
         mma_commit(b_pvdone);
-        return true;
       };
-      for (int t = 0; t < nsteps && ok; ++t) {
+      auto issue_qk = [&](int t) {
         const int st = t % S;
-        ok = mbar_wait(kfull(st), (t / S) & 1, abort_flag, p.err) &&
-             mbar_wait(sempty(t & 1), ((t >> 1) & 1) ^ 1, abort_flag, p.err);
-        if (!ok) break;
-        tc_fence_after();
         const int ti = t / Hkv, g = t - ti * Hkv;
         const uint32_t kaddr = sbase + st * STAGE;
         const uint32_t qaddr = sbase + lay.off_q + g * QG;
@@ -410,37 +443,91 @@ __global__ void __launch_bounds__(kMsaThreads, 1) msa_attend_tc_kernel(const __g
             mma_f16_ss(tmem_base + (t & 1) * NG, smem_desc(kaddr + c * CH + k * 32, 16, 1024, kSwizzle128),
                        smem_desc(qaddr + c * NG * 128 + k * 32, 16, 1024, kSwizzle128), IDESC_QK, (c | k) ? 1u : 0u);
         mma_commit(sfull(t & 1));
-        if (t > 0) ok = pv(t - 1);   // PV of the previous step after this QK, so the two overlap the softmax
+        mma_commit(kempty(st));
+      };
+      // a polling issuer: PV of the oldest softmaxed step or QK of the next
+      // step, whichever is ready, PV first (it frees a V half and a P buffer)
+      int nq = 0, np = 0;
+      uint32_t idle = 0;
+      uint64_t idle_since = 0;
+      while (ok && np < nsteps) {
+        bool progressed = false;
+        if (np < nq && mbar_test(pfull(np & 1), (np >> 1) & 1) && mbar_test(vfull(np % S), (np / S) & 1)) {
+          tc_fence_after();
+          issue_pv(np);
+          ++np;
+          progressed = true;
+        }
+        if (nq < nsteps && mbar_test(kfull(nq % S), (nq / S) & 1) &&
+            mbar_test(sempty(nq & 1), ((nq >> 1) & 1) ^ 1)) {
+          tc_fence_after();
+          issue_qk(nq);
+          ++nq;
+          progressed = true;
+        }
+        if (progressed) {
+          idle = 0;
+          idle_since = 0;
+        } else {
+          ++idle;
+          __nanosleep(32);
+          if ((idle & 255) == 0) {
+            if (*abort_flag) break;
+            if (idle_since == 0) {
+              idle_since = globaltimer();
+            } else if (globaltimer() - idle_since > kWaitLimitNs) {
+              *abort_flag = 1;
+              atomicOr(p.err, kErrTimeout);
+              break;
+            }
+          }
+        }
       }
-      if (ok && nsteps > 0) pv(nsteps - 1);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
+    // Eight warps, two per TMEM lane quadrant: warp half hf takes heads
+    // [hf * NG/2, (hf+1) * NG/2) of every step.  One named barrier per step:
+    // the per-quad maxima and sums are double-buffered by step parity, the
+    // reference maxima by tile parity, and each step's sums are folded into
+    // l one step later; every exit from the loop is decided at that barrier
+    // (an OR of the 256 threads' failures), so no softmax warp waits there
+    // alone.
+    constexpr int NH = NG / 2;            // heads per warp
     const int quad = warp & 3;
-    const int i = quad * 32 + lane;   // TMEM lane: token of S, dim of O
-    const int et = threadIdx.x - 64;
+    const int hf = (warp - 2) >> 2;
+    const int h0 = hf * NH;
+    const int i = quad * 32 + lane;       // TMEM lane: token of S, dim of O
+    const int et = threadIdx.x - 64;      // 0 .. 255
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    for (int k = et; k < Hkv * NG; k += 128) {
-      m_sm[k] = kMsaNegBig;
+    for (int k = et; k < Hkv * NG; k += kMsaSoftThreads) {
+      m_sm[k] = kMsaNegBig;            // reference maxima, tile parity 0
+      m_sm[Hkv * NG + k] = kMsaNegBig; // tile parity 1
       l_sm[k] = 0.f;
     }
-    // every exit from the step loop is decided at a named barrier (an OR of
-    // the 128 threads' failures), so no softmax warp waits there alone
-    bool ok = !named_bar_any(1, 128, false);
-    bool carry = true;   // this warp's result of the previous step's last wait
+    bool ok = !named_bar_any(1, kMsaSoftThreads, false);
+    bool carry = true;        // this warp's result of the previous step's last wait
+    float alpha_prev = 1.f;   // (et < NG) alpha of head et at the previous step
+    int g_prev = 0;
     for (int t = 0; t < nsteps && ok; ++t) {
       const int ti = t / Hkv, g = t - ti * Hkv;
       const int u = tile_u[ti], fl = tile_fl[ti];
       const int q = kMsaTile * u - lead + i;
       const bool valid = q >= 0 && q <= pos && ((i < lead) ? (fl & 1) : (fl & 2));
+      uint32_t *rmax = redmax + (t & 1) * 8 * NG;
+      float *rsum = redsum + (t & 1) * 8 * NG;
       bool good = carry && __all_sync(0xffffffffu, mbar_wait(sfull(t & 1), (t >> 1) & 1, abort_flag, p.err));
       tc_fence_after();
-      float s[NG];
+      float s[NH];
       if (good) {
+        if constexpr (NH == 8) {
+          tmem_ld8(tmem_base + lane_base + (t & 1) * NG + h0, s);
+        } else {
 #pragma unroll
-        for (int c0 = 0; c0 < NG; c0 += 16)
-          tmem_ld16(tmem_base + lane_base + (t & 1) * NG + c0, *reinterpret_cast<float(*)[16]>(s + c0));
+          for (int c0 = 0; c0 < NH; c0 += 16)
+            tmem_ld16(tmem_base + lane_base + (t & 1) * NG + h0 + c0, *reinterpret_cast<float(*)[16]>(s + c0));
+        }
         tmem_ld_wait();
       }
       tc_fence_before();
@@ -448,98 +535,117 @@ __global__ void __launch_bounds__(kMsaThreads, 1) msa_attend_tc_kernel(const __g
       if (good && lane == 0) mbar_arrive(sempty(t & 1));
       // each head's largest logit of the tile (order keys; masked rows give 0)
 #pragma unroll
-      for (int h = 0; h < NG; ++h) {
+      for (int h = 0; h < NH; ++h) {
         const uint32_t mk = __reduce_max_sync(0xffffffffu, valid ? score_key(s[h]) : 0u);
-        if (lane == 0) redmax[quad * NG + h] = mk;
+        if (lane == 0) rmax[(h0 + h) * 4 + quad] = mk;
       }
-      if (named_bar_any(1, 128, !good)) {
+      if (named_bar_any(1, kMsaSoftThreads, !good)) {
         ok = false;
         break;
       }
-      float alpha[NG], mnew[NG];
-      bool rescale = false;
-#pragma unroll
-      for (int h = 0; h < NG; ++h) {
-        const uint32_t k =
-            max(max(redmax[h], redmax[NG + h]), max(redmax[2 * NG + h], redmax[3 * NG + h]));
-        const float mold = m_sm[g * NG + h];
+      // the previous step's sums (its barrier has passed in every warp)
+      if (t > 0 && et < NG) {
+        const float4 ps = reinterpret_cast<const float4 *>(redsum + ((t - 1) & 1) * 8 * NG)[et];
+        l_sm[g_prev * NG + et] = l_sm[g_prev * NG + et] * alpha_prev + ((ps.x + ps.y) + (ps.z + ps.w));
+      }
+      const float *mold_sm = m_sm + ((ti & 1) ^ 1) * Hkv * NG + g * NG;   // written at the group's previous tile
+      float *mnew_sm = m_sm + (ti & 1) * Hkv * NG + g * NG;
+      // reference max of head h for this step (every thread that needs a
+      // head derives the same value from the same shared data)
+      auto head_max = [&](int h, float &alpha) -> float {
+        const uint4 k4 = reinterpret_cast<const uint4 *>(rmax)[h];
+        const uint32_t k = max(max(k4.x, k4.y), max(k4.z, k4.w));
+        const float mold = mold_sm[h];
         // (a tile always holds a kept position, so k is a real score)
         const float tmax = key_score(k) * p.scale_log2;
-        mnew[h] = mold;
-        alpha[h] = 1.f;
+        alpha = 1.f;
         if (tmax > mold + kMsaRescale) {
-          mnew[h] = tmax;
-          alpha[h] = exp2f(mold - tmax);
-          rescale = true;
+          alpha = fast_exp2(mold - tmax);
+          return tmax;
         }
+        return mold;
+      };
+      float alpha[NH], mnew[NH];
+      bool rescale = false;
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        mnew[h] = head_max(h0 + h, alpha[h]);
+        rescale = rescale || alpha[h] != 1.f;
+      }
+      if (et < NG) {
+        float a;
+        mnew_sm[et] = head_max(et, a);
+        alpha_prev = a;
+        g_prev = g;
       }
       // P (bf16) and the tile's per-head sums of what PV will add
-      float psum[NG];
 #pragma unroll
-      for (int h = 0; h < NG; ++h) {
-        const float e = valid ? exp2f(fmaf(s[h], p.scale_log2, -mnew[h])) : 0.f;
-        const __nv_bfloat16 pb = __float2bfloat16_rn(e);
-        s[h] = __bfloat162float(pb);
-        psum[h] = s[h];
+      for (int h = 0; h < NH; ++h) {
+        const float e = valid ? fast_exp2(fmaf(s[h], p.scale_log2, -mnew[h])) : 0.f;
+        s[h] = __bfloat162float(__float2bfloat16_rn(e));
       }
+      if constexpr (NH <= 16) {
+        const float sum = warp_sum_transpose<NH>(s);   // lane l holds head (l >> (5 - log2 NH))
+        constexpr int SHIFT = NH == 8 ? 2 : 1;
+        if ((lane & ((1 << SHIFT) - 1)) == 0) rsum[(h0 + (lane >> SHIFT)) * 4 + quad] = sum;
+      } else {
 #pragma unroll
-      for (int o = 16; o; o >>= 1)
-#pragma unroll
-        for (int h = 0; h < NG; ++h) psum[h] += __shfl_xor_sync(0xffffffffu, psum[h], o);
-      if (lane == 0)
-#pragma unroll
-        for (int h = 0; h < NG; ++h) redsum[quad * NG + h] = psum[h];
+        for (int c0 = 0; c0 < NH; c0 += 32) {
+          const float sum = warp_sum_transpose<32>(*reinterpret_cast<float(*)[32]>(s + c0));   // lane h: head h
+          rsum[(h0 + c0 + lane) * 4 + quad] = sum;
+        }
+      }
       // P^T buffer (t & 1) is free once PV(t-2) completed
       good = __all_sync(0xffffffffu, mbar_wait(pempty(t & 1), ((t >> 1) & 1) ^ 1, abort_flag, p.err));
       if (good) {
-        const uint32_t pbase = sbase + lay.off_p + (t & 1) * PB + (i >> 6) * NG * 128;
+        const uint32_t pbase = sbase + lay.off_p + (t & 1) * PB + (i >> 6) * NG * 128 + ((i & 7) << 1);
+        const uint32_t c8 = (i & 63) >> 3;
 #pragma unroll
-        for (int h = 0; h < NG; ++h) {
-          const uint32_t a = pbase + h * 128 + ((((i & 63) >> 3) ^ (h & 7)) << 4) + ((i & 7) << 1);
+        for (int h = 0; h < NH; ++h) {
+          const int hh = h0 + h;
+          const uint32_t a = pbase + hh * 128 + ((c8 ^ (hh & 7)) << 4);
           const __nv_bfloat16 pb = __float2bfloat16_rn(s[h]);
           asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"(*reinterpret_cast<const uint16_t *>(&pb)) : "memory");
         }
       }
       // V rows of positions outside the kept blocks are zeroed once the tile
-      // has landed (a zero probability must not meet a stale value)
+      // has landed (a zero probability must not meet a stale value); warp
+      // half hf zeroes 64-column chunk hf
       if (good && __any_sync(0xffffffffu, !valid)) {
         const int st = t % S;
         good = __all_sync(0xffffffffu, mbar_wait(vfull(st), (t / S) & 1, abort_flag, p.err));
         if (good && !valid) {
-          const uint32_t vrow = sbase + st * STAGE + KVB + i * 128;
+          const uint32_t vrow = sbase + st * STAGE + KVB + hf * CH + i * 128;
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              st_shared_v4(vrow + c * CH + k * 16, make_uint4(0u, 0u, 0u, 0u));
+          for (int k = 0; k < 8; ++k) st_shared_v4(vrow + k * 16, make_uint4(0u, 0u, 0u, 0u));
         }
       }
       fence_proxy_async_smem();
-      if (named_bar_any(1, 128, !good)) {
-        ok = false;
-        break;
-      }
-      if (et < NG) {
-        const float ts = redsum[et] + redsum[NG + et] + redsum[2 * NG + et] + redsum[3 * NG + et];
-        l_sm[g * NG + et] = l_sm[g * NG + et] * alpha[et] + ts;
-      }
-      if (et == 0)
-#pragma unroll
-        for (int h = 0; h < NG; ++h) m_sm[g * NG + h] = mnew[h];
-      // O of this kv head is rescaled once PV(t-1) (and so every earlier PV
-      // into it) has completed; its first tile has no O yet
-      if (rescale && ti > 0) {
+      // O of this kv head (this warp's head columns) is rescaled once PV(t-1)
+      // (and so every earlier PV into it) has completed; its first tile has
+      // no O yet
+      if (good && __any_sync(0xffffffffu, rescale) && ti > 0) {
         good = __all_sync(0xffffffffu, mbar_wait(b_pvdone, (t - 1) & 1, abort_flag, p.err));
         tc_fence_after();
         if (good) {
-#pragma unroll
-          for (int c0 = 0; c0 < NG; c0 += 16) {
-            float o[16];
-            tmem_ld16(tmem_base + lane_base + 2 * NG + g * NG + c0, o);
+          const uint32_t oaddr = tmem_base + lane_base + 2 * NG + g * NG + h0;
+          if constexpr (NH == 8) {
+            float o[8];
+            tmem_ld8(oaddr, o);
             tmem_ld_wait();
 #pragma unroll
-            for (int k = 0; k < 16; ++k) o[k] *= alpha[c0 + k];
-            tmem_st16(tmem_base + lane_base + 2 * NG + g * NG + c0, o);
+            for (int k = 0; k < 8; ++k) o[k] *= alpha[k];
+            tmem_st8(oaddr, o);
+          } else {
+#pragma unroll
+            for (int c0 = 0; c0 < NH; c0 += 16) {
+              float o[16];
+              tmem_ld16(oaddr + c0, o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int k = 0; k < 16; ++k) o[k] *= alpha[c0 + k];
+              tmem_st16(oaddr + c0, o);
+            }
           }
           tmem_st_wait();
         }
@@ -552,22 +658,30 @@ __global__ void __launch_bounds__(kMsaThreads, 1) msa_attend_tc_kernel(const __g
     if (ok && carry && nsteps > 0)
       carry = __all_sync(0xffffffffu, mbar_wait(b_pvdone, (nsteps - 1) & 1, abort_flag, p.err));
     tc_fence_after();
-    ok = !named_bar_any(1, 128, !(ok && carry));   // the last l values are in place
+    ok = !named_bar_any(1, kMsaSoftThreads, !(ok && carry));   // the last step's sums are in place
+    if (ok && nsteps > 0 && et < NG) {
+      const float4 ps = reinterpret_cast<const float4 *>(redsum + ((nsteps - 1) & 1) * 8 * NG)[et];
+      l_sm[g_prev * NG + et] = l_sm[g_prev * NG + et] * alpha_prev + ((ps.x + ps.y) + (ps.z + ps.w));
+    }
+    ok = !named_bar_any(1, kMsaSoftThreads, !ok);   // every l is final
     if (ok) {
       for (int g = 0; g < Hkv; ++g) {
+        const uint32_t oaddr = tmem_base + lane_base + 2 * NG + g * NG + h0;
+        float o[NH];
+        if constexpr (NH == 8) {
+          tmem_ld8(oaddr, o);
+        } else {
 #pragma unroll
-        for (int c0 = 0; c0 < NG; c0 += 16) {
-          float o[16];
-          tmem_ld16(tmem_base + lane_base + 2 * NG + g * NG + c0, o);
-          tmem_ld_wait();
+          for (int c0 = 0; c0 < NH; c0 += 16) tmem_ld16(oaddr + c0, *reinterpret_cast<float(*)[16]>(o + c0));
+        }
+        tmem_ld_wait();
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const int h = c0 + k;
-            if (h >= p.group) continue;
-            const float l = l_sm[g * NG + h];
-            p.out[(static_cast<int64_t>(row) * p.Hq + g * p.group + h) * 128 + i] =
-                __float2bfloat16_rn(l > 0.f ? o[k] / l : 0.f);
-          }
+        for (int k = 0; k < NH; ++k) {
+          const int h = h0 + k;
+          if (h >= p.group) continue;
+          const float l = l_sm[g * NG + h];
+          p.out[(static_cast<int64_t>(row) * p.Hq + g * p.group + h) * 128 + i] =
+              __float2bfloat16_rn(l > 0.f ? o[k] / l : 0.f);
         }
       }
     }
