@@ -212,7 +212,7 @@ struct MsaLayout {
     off_q = stages * stage;
     off_p = off_q + Hkv * 2 * NG * 128;
     off_red = off_p + 2 * 2 * NG * 128;
-    off_ml = off_red + 2 * 8 * NG * 4;          // [step parity][max keys | sums][NG][4 quads]
+    off_ml = off_red + 4 * 8 * NG * 4;          // [group][step parity][max keys | sums][NG][4 quads]
     off_tiles = off_ml + 3 * Hkv * NG * 4;      // m [tile parity][Hkv][NG], l [Hkv][NG]
     off_bar = (off_tiles + 2 * kMsaMaxTiles * 4 + 7) / 8 * 8;
     off_misc = off_bar + 24 * 8;
@@ -220,7 +220,7 @@ struct MsaLayout {
   }
 };
 
-template <int NG>
+template <int NG, int NGRP>
 __global__ void __launch_bounds__(kMsaThreads, 1) msa_attend_tc_kernel(const __grid_constant__ MsaParams p) {
   constexpr int CH = kMsaTile * 128;        // [128 rows][64 columns] bf16
   constexpr int KVB = 2 * CH;               // K (or V) of one kv head
@@ -322,8 +322,8 @@ __global__ void __launch_bounds__(kMsaThreads, 1) msa_attend_tc_kernel(const __g
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(sfull(b), 1);
-      mbar_init(sempty(b), 8);   // one arrival per softmax warp
-      mbar_init(pfull(b), 8);
+      mbar_init(sempty(b), 8 / NGRP);   // one arrival per softmax warp that takes the buffer's steps
+      mbar_init(pfull(b), 8 / NGRP);
       mbar_init(pempty(b), 1);
     }
     mbar_init(b_pvdone, 1);
@@ -487,36 +487,45 @@ __global__ void __launch_bounds__(kMsaThreads, 1) msa_attend_tc_kernel(const __g
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
-    // Eight warps, two per TMEM lane quadrant: warp half hf takes heads
-    // [hf * NG/2, (hf+1) * NG/2) of every step.  One named barrier per step:
-    // the per-quad maxima and sums are double-buffered by step parity, the
-    // reference maxima by tile parity, and each step's sums are folded into
-    // l one step later; every exit from the loop is decided at that barrier
-    // (an OR of the 256 threads' failures), so no softmax warp waits there
-    // alone.
-    constexpr int NH = NG / 2;            // heads per warp
+    // Eight warps, two per TMEM lane quadrant.  NGRP = 1: warp half hf takes
+    // heads [hf * NG/2, (hf+1) * NG/2) of every step.  NGRP = 2 (an even
+    // number of kv heads): warp half x takes every head of the steps
+    // t = x, x+2, ..., i.e. of the kv heads of parity x, so the two halves
+    // keep disjoint softmax state and their per-step latency chains overlap.
+    // One named barrier per step and group: the per-quad maxima and sums are
+    // double-buffered by the group's step parity, the reference maxima by
+    // tile parity, and each step's sums are folded into l at the group's next
+    // step; every exit from the loop is decided at that barrier (an OR of the
+    // group's failures), so no softmax warp waits there alone.
+    constexpr int NH = NG / (3 - NGRP);   // heads per warp: NG/2, or NG
+    constexpr int GTHREADS = kMsaSoftThreads / NGRP;
     const int quad = warp & 3;
     const int hf = (warp - 2) >> 2;
-    const int h0 = hf * NH;
+    const int grp = NGRP == 2 ? hf : 0;
+    const int h0 = NGRP == 2 ? 0 : hf * NH;
     const int i = quad * 32 + lane;       // TMEM lane: token of S, dim of O
     const int et = threadIdx.x - 64;      // 0 .. 255
+    const int gt = et - grp * GTHREADS;   // thread within the group
+    const uint32_t gbar = 1 + grp;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     for (int k = et; k < Hkv * NG; k += kMsaSoftThreads) {
       m_sm[k] = kMsaNegBig;            // reference maxima, tile parity 0
       m_sm[Hkv * NG + k] = kMsaNegBig; // tile parity 1
       l_sm[k] = 0.f;
     }
-    bool ok = !named_bar_any(1, kMsaSoftThreads, false);
+    bool ok = !named_bar_any(3, kMsaSoftThreads, false);
     bool carry = true;        // this warp's result of the previous step's last wait
-    float alpha_prev = 1.f;   // (et < NG) alpha of head et at the previous step
+    float alpha_prev = 1.f;   // (gt < NG) alpha of head gt at the group's previous step
     int g_prev = 0;
-    for (int t = 0; t < nsteps && ok; ++t) {
+    int t_last = -1;          // the group's last step
+    for (int t = grp; t < nsteps && ok; t += NGRP) {
+      const int lt = t / NGRP;            // the group's own step count
       const int ti = t / Hkv, g = t - ti * Hkv;
       const int u = tile_u[ti], fl = tile_fl[ti];
       const int q = kMsaTile * u - lead + i;
       const bool valid = q >= 0 && q <= pos && ((i < lead) ? (fl & 1) : (fl & 2));
-      uint32_t *rmax = redmax + (t & 1) * 8 * NG;
-      float *rsum = redsum + (t & 1) * 8 * NG;
+      uint32_t *rmax = redmax + (grp * 2 + (lt & 1)) * 8 * NG;
+      float *rsum = redsum + (grp * 2 + (lt & 1)) * 8 * NG;
       bool good = carry && __all_sync(0xffffffffu, mbar_wait(sfull(t & 1), (t >> 1) & 1, abort_flag, p.err));
       tc_fence_after();
       float s[NH];
@@ -539,14 +548,14 @@ __global__ void __launch_bounds__(kMsaThreads, 1) msa_attend_tc_kernel(const __g
         const uint32_t mk = __reduce_max_sync(0xffffffffu, valid ? score_key(s[h]) : 0u);
         if (lane == 0) rmax[(h0 + h) * 4 + quad] = mk;
       }
-      if (named_bar_any(1, kMsaSoftThreads, !good)) {
+      if (named_bar_any(gbar, GTHREADS, !good)) {
         ok = false;
         break;
       }
-      // the previous step's sums (its barrier has passed in every warp)
-      if (t > 0 && et < NG) {
-        const float4 ps = reinterpret_cast<const float4 *>(redsum + ((t - 1) & 1) * 8 * NG)[et];
-        l_sm[g_prev * NG + et] = l_sm[g_prev * NG + et] * alpha_prev + ((ps.x + ps.y) + (ps.z + ps.w));
+      // the group's previous step's sums (its barrier has passed in every warp of the group)
+      if (lt > 0 && gt < NG) {
+        const float4 ps = reinterpret_cast<const float4 *>(redsum + (grp * 2 + ((lt - 1) & 1)) * 8 * NG)[gt];
+        l_sm[g_prev * NG + gt] = l_sm[g_prev * NG + gt] * alpha_prev + ((ps.x + ps.y) + (ps.z + ps.w));
       }
       const float *mold_sm = m_sm + ((ti & 1) ^ 1) * Hkv * NG + g * NG;   // written at the group's previous tile
       float *mnew_sm = m_sm + (ti & 1) * Hkv * NG + g * NG;
@@ -572,12 +581,13 @@ __global__ void __launch_bounds__(kMsaThreads, 1) msa_attend_tc_kernel(const __g
         mnew[h] = head_max(h0 + h, alpha[h]);
         rescale = rescale || alpha[h] != 1.f;
       }
-      if (et < NG) {
+      if (gt < NG) {
         float a;
-        mnew_sm[et] = head_max(et, a);
+        mnew_sm[gt] = head_max(gt, a);
         alpha_prev = a;
         g_prev = g;
       }
+      t_last = t;
       // P (bf16) and the tile's per-head sums of what PV will add
 #pragma unroll
       for (int h = 0; h < NH; ++h) {
@@ -595,8 +605,10 @@ __global__ void __launch_bounds__(kMsaThreads, 1) msa_attend_tc_kernel(const __g
           rsum[(h0 + c0 + lane) * 4 + quad] = sum;
         }
       }
-      // P^T buffer (t & 1) is free once PV(t-2) completed
+      // P^T buffer (t & 1) is free once PV(t-2) completed (with NGRP = 2 that
+      // wait also orders the O rescale below after every earlier PV into O)
       good = __all_sync(0xffffffffu, mbar_wait(pempty(t & 1), ((t >> 1) & 1) ^ 1, abort_flag, p.err));
+      tc_fence_after();
       if (good) {
         const uint32_t pbase = sbase + lay.off_p + (t & 1) * PB + (i >> 6) * NG * 128 + ((i & 7) << 1);
         const uint32_t c8 = (i & 63) >> 3;
@@ -609,24 +621,31 @@ __global__ void __launch_bounds__(kMsaThreads, 1) msa_attend_tc_kernel(const __g
         }
       }
       // V rows of positions outside the kept blocks are zeroed once the tile
-      // has landed (a zero probability must not meet a stale value); warp
-      // half hf zeroes 64-column chunk hf
+      // has landed (a zero probability must not meet a stale value); with
+      // NGRP = 1, warp half hf zeroes 64-column chunk hf
       if (good && __any_sync(0xffffffffu, !valid)) {
         const int st = t % S;
         good = __all_sync(0xffffffffu, mbar_wait(vfull(st), (t / S) & 1, abort_flag, p.err));
         if (good && !valid) {
-          const uint32_t vrow = sbase + st * STAGE + KVB + hf * CH + i * 128;
 #pragma unroll
-          for (int k = 0; k < 8; ++k) st_shared_v4(vrow + k * 16, make_uint4(0u, 0u, 0u, 0u));
+          for (int c = 0; c < 2; ++c) {
+            if (NGRP == 1 && c != hf) continue;
+            const uint32_t vrow = sbase + st * STAGE + KVB + c * CH + i * 128;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) st_shared_v4(vrow + k * 16, make_uint4(0u, 0u, 0u, 0u));
+          }
         }
       }
       fence_proxy_async_smem();
-      // O of this kv head (this warp's head columns) is rescaled once PV(t-1)
-      // (and so every earlier PV into it) has completed; its first tile has
-      // no O yet
+      // O of this kv head (this warp's head columns) is rescaled once every
+      // earlier PV into it has completed (its first tile has no O yet).  With
+      // NGRP = 2 that is PV(t-2), already waited for above (PV(t-1) belongs
+      // to another kv head); with NGRP = 1 it is PV(t-1).
       if (good && __any_sync(0xffffffffu, rescale) && ti > 0) {
-        good = __all_sync(0xffffffffu, mbar_wait(b_pvdone, (t - 1) & 1, abort_flag, p.err));
-        tc_fence_after();
+        if (NGRP == 1) {
+          good = __all_sync(0xffffffffu, mbar_wait(b_pvdone, (t - 1) & 1, abort_flag, p.err));
+          tc_fence_after();
+        }
         if (good) {
           const uint32_t oaddr = tmem_base + lane_base + 2 * NG + g * NG + h0;
           if constexpr (NH == 8) {
@@ -655,17 +674,24 @@ __global__ void __launch_bounds__(kMsaThreads, 1) msa_attend_tc_kernel(const __g
       if (good && lane == 0) mbar_arrive(pfull(t & 1));
       carry = good;
     }
+    // every PV has completed before O is read: first the group's own last PV
+    // (the P buffer's barrier counts only that buffer's PVs, so its parity
+    // names that PV exactly), which leaves at most the very last PV of the
+    // row outstanding, then that one on the shared barrier (a parity wait on
+    // a barrier that could still be two phases short would pass early)
+    if (ok && carry && t_last >= 0)
+      carry = __all_sync(0xffffffffu, mbar_wait(pempty(t_last & 1), (t_last >> 1) & 1, abort_flag, p.err));
     if (ok && carry && nsteps > 0)
       carry = __all_sync(0xffffffffu, mbar_wait(b_pvdone, (nsteps - 1) & 1, abort_flag, p.err));
     tc_fence_after();
-    ok = !named_bar_any(1, kMsaSoftThreads, !(ok && carry));   // the last step's sums are in place
-    if (ok && nsteps > 0 && et < NG) {
-      const float4 ps = reinterpret_cast<const float4 *>(redsum + ((nsteps - 1) & 1) * 8 * NG)[et];
-      l_sm[g_prev * NG + et] = l_sm[g_prev * NG + et] * alpha_prev + ((ps.x + ps.y) + (ps.z + ps.w));
+    ok = !named_bar_any(gbar, GTHREADS, !(ok && carry));   // the group's last sums are in place
+    if (ok && t_last >= 0 && gt < NG) {
+      const float4 ps = reinterpret_cast<const float4 *>(redsum + (grp * 2 + ((t_last / NGRP) & 1)) * 8 * NG)[gt];
+      l_sm[g_prev * NG + gt] = l_sm[g_prev * NG + gt] * alpha_prev + ((ps.x + ps.y) + (ps.z + ps.w));
     }
-    ok = !named_bar_any(1, kMsaSoftThreads, !ok);   // every l is final
+    ok = !named_bar_any(gbar, GTHREADS, !ok);   // every l of the group's kv heads is final
     if (ok) {
-      for (int g = 0; g < Hkv; ++g) {
+      for (int g = grp; g < Hkv; g += NGRP) {
         const uint32_t oaddr = tmem_base + lane_base + 2 * NG + g * NG + h0;
         float o[NH];
         if constexpr (NH == 8) {
@@ -778,7 +804,7 @@ __global__ void __launch_bounds__(128) msa_attend_simt_kernel(
   }
 }
 
-template <int NG>
+template <int NG, int NGRP>
 cudaError_t run_msa_tc(const dsa_ctx *ctx, const dsa_plan_t *plan, const dsa_msa_shape_t &ms, const int32_t *sel,
                        const void *q, const void *kv, float sm_scale, void *out, cudaStream_t s) {
   MsaParams prm{};
@@ -809,7 +835,7 @@ cudaError_t run_msa_tc(const dsa_ctx *ctx, const dsa_plan_t *plan, const dsa_msa
   prm.scale_log2 = sm_scale * kMsaLog2e;
   prm.stages = MsaLayout(NG, 3, ms.kv_heads).bytes <= 227 * 1024 ? 3 : 2;
   const int bytes = static_cast<int>(MsaLayout(NG, prm.stages, ms.kv_heads).bytes);
-  auto kern = msa_attend_tc_kernel<NG>;
+  auto kern = msa_attend_tc_kernel<NG, NGRP>;
   // the limit is set to the largest layout this instance can have
   static std::atomic<uint64_t> smem_limit_set{0};
   if (cudaError_t e = ensure_smem_limit(kern, 227 * 1024, ctx->device, smem_limit_set); e != cudaSuccess) return e;
@@ -849,9 +875,13 @@ cudaError_t launch_msa_attend(const dsa_ctx *ctx, const dsa_plan_t *plan, const 
   cudaError_t e;
   if (msa_attend_tc_supported(ctx->cfg, ms, plan->box_rows)) {
     const int NG = msa_group_cols(ms.q_heads / ms.kv_heads);
-    if (NG == 16) e = run_msa_tc<16>(ctx, plan, ms, sel, q, kv, sm_scale, out, s);
-    else if (NG == 32) e = run_msa_tc<32>(ctx, plan, ms, sel, q, kv, sm_scale, out, s);
-    else e = run_msa_tc<64>(ctx, plan, ms, sel, q, kv, sm_scale, out, s);
+    // an even number of kv heads: two warp groups take alternate steps
+    const bool two = ms.kv_heads % 2 == 0;
+    if (NG == 16) e = two ? run_msa_tc<16, 2>(ctx, plan, ms, sel, q, kv, sm_scale, out, s)
+                          : run_msa_tc<16, 1>(ctx, plan, ms, sel, q, kv, sm_scale, out, s);
+    else if (NG == 32) e = two ? run_msa_tc<32, 2>(ctx, plan, ms, sel, q, kv, sm_scale, out, s)
+                               : run_msa_tc<32, 1>(ctx, plan, ms, sel, q, kv, sm_scale, out, s);
+    else e = run_msa_tc<64, 1>(ctx, plan, ms, sel, q, kv, sm_scale, out, s);
   } else {
     const size_t sm = (static_cast<size_t>(ms.head_dim) + static_cast<size_t>(ms.topk_blocks) * ms.block_size + 32) *
                       sizeof(float);
