@@ -288,11 +288,14 @@ def msa_work(wl, block_sel=None):
                 attend_flops=float(kept.sum()) * 4.0 * ms.q_heads * ms.head_dim, kept=int(kept.sum()))
 
 
-def msa_leg(args, name, rank, world, dev, flush):
+def msa_leg(args, name, rank, world, dev, flush, requests=0):
     """A block-sparse MSA workload (store keys, index score, block selection,
-    GQA attention over the kept blocks) timed like the headline step."""
+    GQA attention over the kept blocks) timed like the headline step;
+    `requests` keeps the first N requests (profiler captures)."""
     from deepseek_sparse_attention_dsa_gb300 import dsa
     wl = W.msa_config(name, seed=2000 + W.MSA_CONFIG_NAMES.index(name) + 7919 * rank)
+    if requests:
+        wl = wl.sub_workload(range(min(requests, len(wl.spans))))
     sh, ms = wl.shape, wl.msa
     unit, decode = unit_of(wl)
     ic = W.make_index_cache(wl, device=dev)
@@ -378,6 +381,27 @@ def msa_leg(args, name, rank, world, dev, flush):
     del ic, kv, st, q, scores, bsel, out
     torch.cuda.empty_cache()
     return leg
+
+
+def run_msa(args, name, rank, world, local_rank):
+    """`--workload msa_*`: the MSA step as the line itself (for profiler
+    captures and standalone runs; the headline stays long_decode)."""
+    from deepseek_sparse_attention_dsa_gb300 import build as lib_build
+    lib_build.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    leg = msa_leg(args, name, rank, world, dev, flush, args.requests)
+    hbm = leg["peaks"]["hbm_gbs"]
+    line = {"metric": METRIC, "value": leg["value"], "unit": leg["unit"], "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": leg["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded counter-based generator; no dataset or weights)",
+            "config": dict(leg["config"], requests_kept=args.requests or None),
+            "roofline": {"kernel": leg["attend_kernel"], "bound": "hbm", "achieved": leg["attend_gbs"], "peak": hbm,
+                         "unit": "GB/s", "frac": leg["attend_hbm_frac"], "traffic": None,
+                         "peak_kind": leg["peaks"]["kind"] + " (hbm_gbs)"},
+            "stages_ms": leg["stages_ms"], "gpu_launches": leg["gpu_launches"], "clocks": leg["clocks"], "msa": leg}
+    return line
 
 
 def run_ours(args, name, rank, world, local_rank):
@@ -788,7 +812,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="long_decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="long_decode", choices=sorted(WORKLOADS) + W.MSA_CONFIG_NAMES)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-rows", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -806,13 +830,18 @@ def main():
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
     rank, world, local_rank = rank_info()
     if args.impl == "reference":
+        if args.workload not in WORKLOADS:
+            ap.error("--impl reference times the DSA workloads (%s)" % ", ".join(sorted(WORKLOADS)))
         line = run_reference(args, args.workload, rank, world)
         if line is not None:
             print(json.dumps(line), flush=True)
         return
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-    line = run_ours(args, args.workload, rank, world, local_rank)
+    if args.workload in W.MSA_CONFIG_NAMES:
+        line = run_msa(args, args.workload, rank, world, local_rank)
+    else:
+        line = run_ours(args, args.workload, rank, world, local_rank)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
