@@ -29,8 +29,11 @@ indexer's and the attention's TFLOP/s as fractions of the measured dense bf16
 peak, with the clocks of that leg.
 Block-sparse MSA workloads (`--msa`, default msa_decode and msa_prefill) are
 timed the same way and reported under `msa`: store, index score, block
-selection and GQA attention over the kept blocks, with the attention's GB/s
-and TFLOP/s against the measured peaks.
+selection and GQA attention over the kept blocks.  Decode legs hold the
+indexer and the attention against the measured HBM copy rate (each key and
+kept row is read once); prefill legs hold the indexer against the dense bf16
+peak and report the attention's gather rate (kept rows re-read by the rows of
+one request come mostly from L2) beside its TFLOP/s.
 `--impl reference` times the CPU oracle (the only reference this method has)
 on a bounded sample of the same workload on the host cores.
 Multi-GPU (torchrun): independent replicas, one per rank (weak scaling).
@@ -304,11 +307,10 @@ def msa_leg(args, name, rank, world, dev, flush, requests=0):
     q = W.make_msa_q(wl, device=dev)
     ctx = dsa.Context(sh, dev.index)
     plan = ctx.plan(wl.spans, wl.num_pages)
-    scores = torch.empty(max(1, plan.num_scores), dtype=torch.float32, device=dev)
     bsel = torch.empty(plan.num_rows, ms.topk_blocks, dtype=torch.int32, device=dev)
     out = torch.empty(plan.num_rows, ms.q_heads, ms.head_dim, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     launches = [0]
 
     def step(record):
@@ -318,18 +320,16 @@ def msa_leg(args, name, rank, world, dev, flush, requests=0):
         n = ctx.last_launch_count()
         if record:
             ev[1].record(stream)
-        ctx.index_scores(plan, st.q, st.w, ic, scores)
+        # index score and block selection in one call (block maxima straight
+        # from the indexer's epilogue where the kernels allow it)
+        ctx.msa_index_select(plan, ms, st.q, st.w, ic, bsel)
         n += ctx.last_launch_count()
         if record:
             ev[2].record(stream)
-        ctx.msa_select_blocks(plan, ms, scores, bsel)
-        n += ctx.last_launch_count()
-        if record:
-            ev[3].record(stream)
         ctx.msa_attend(plan, ms, bsel, q, kv, ms.sm_scale, out)
         n += ctx.last_launch_count()
         if record:
-            ev[4].record(stream)
+            ev[3].record(stream)
         launches[0] = n
 
     for _ in range(args.warmup):
@@ -339,16 +339,15 @@ def msa_leg(args, name, rank, world, dev, flush, requests=0):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
-    stage = {"store": [], "index": [], "select": [], "attend": [], "step": []}
+    stage = {"store": [], "index_select": [], "attend": [], "step": []}
     n_launch = 0
     with ClockSampler(dev.index) as clk:
         for _ in range(args.steps):
             flush.zero_()
             step(True)
             n_launch += launches[0]
-            ev[4].synchronize()
-            for k, (a, b) in zip(("store", "index", "select", "attend", "step"),
-                                 ((0, 1), (1, 2), (2, 3), (3, 4), (0, 4))):
+            ev[3].synchronize()
+            for k, (a, b) in zip(("store", "index_select", "attend", "step"), ((0, 1), (1, 2), (2, 3), (0, 3))):
                 stage[k].append(ev[a].elapsed_time(ev[b]))
     torch.cuda.synchronize(dev)
     ctx.get_error()
@@ -360,25 +359,33 @@ def msa_leg(args, name, rank, world, dev, flush, requests=0):
     ms_step = total_ms / args.steps
     work = msa_work(wl, bsel.cpu().numpy())
     hbm, bf16, _, peak_kind = measured_peaks()
-    idx_ms = statistics.mean(stage["index"])
+    idx_ms = statistics.mean(stage["index_select"])   # the indexer with the block selection behind it
     att_ms = statistics.mean(stage["attend"])
     att_gbs = work["attend_bytes"] / (att_ms / 1e3) / 1e9
     att_tf = work["attend_flops"] / (att_ms / 1e3) / 1e12
     idx_gbs = work["index_bytes"] / (idx_ms / 1e3) / 1e9
+    idx_tf = work["index_flops"] / (idx_ms / 1e3) / 1e12
     leg = {"workload": name, "value": round(work["rows"] * world / (ms_step / 1e3), 2), "unit": unit,
            "ms_per_step": round(ms_step, 4), "stages_ms": {k: round(statistics.mean(v), 4) for k, v in stage.items()},
            "attend_kernel": "msa_attend_tc_kernel" if ctx.msa_attend_on_tensor_cores(plan, ms) else "msa_attend_simt_kernel",
-           "attend_gbs": round(att_gbs, 1), "attend_hbm_frac": round(att_gbs / hbm, 4),
            "attend_tflops": round(att_tf, 2), "attend_tensor_frac": round(att_tf / bf16, 4),
-           "index_gbs": round(idx_gbs, 1), "index_hbm_frac": round(idx_gbs / hbm, 4),
-           "step_hbm_frac": round(work["step_bytes"] / (ms_step / 1e3) / 1e9 / hbm, 4),
            "attend_bytes_per_step": work["attend_bytes"], "kept_positions": work["kept"],
            "peaks": {"hbm_gbs": hbm, "bf16_tflops": bf16, "kind": peak_kind},
            "gpu_launches": n_launch, "clocks": clk.summary(),
            "config": dict(workload_config(name, wl), msa="top %d blocks of %d, GQA %d q / %d kv heads x %d"
                           % (ms.topk_blocks, ms.block_size, ms.q_heads, ms.kv_heads, ms.head_dim))}
+    if decode:
+        leg.update(attend_gbs=round(att_gbs, 1), attend_hbm_frac=round(att_gbs / hbm, 4),
+                   index_gbs=round(idx_gbs, 1), index_hbm_frac=round(idx_gbs / hbm, 4),
+                   step_hbm_frac=round(work["step_bytes"] / (ms_step / 1e3) / 1e9 / hbm, 4))
+    else:
+        # prefill rows of a request re-read the same index keys and kept
+        # blocks (mostly from L2): the indexer is held against the tensor peak
+        # and the attention's byte rate is what it gathers into shared memory
+        leg.update(index_tflops=round(idx_tf, 2), index_frac=round(idx_tf / bf16, 4),
+                   attend_gather_gbs=round(att_gbs, 1))
     plan.close()
-    del ic, kv, st, q, scores, bsel, out
+    del ic, kv, st, q, bsel, out
     torch.cuda.empty_cache()
     return leg
 
@@ -392,14 +399,20 @@ def run_msa(args, name, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     leg = msa_leg(args, name, rank, world, dev, flush, args.requests)
-    hbm = leg["peaks"]["hbm_gbs"]
+    hbm, bf16 = leg["peaks"]["hbm_gbs"], leg["peaks"]["bf16_tflops"]
+    if "attend_hbm_frac" in leg:
+        roof = {"kernel": leg["attend_kernel"], "bound": "hbm", "achieved": leg["attend_gbs"], "peak": hbm,
+                "unit": "GB/s", "frac": leg["attend_hbm_frac"], "traffic": None,
+                "peak_kind": leg["peaks"]["kind"] + " (hbm_gbs)"}
+    else:
+        roof = {"kernel": leg["attend_kernel"], "bound": "tensor", "achieved": leg["attend_tflops"], "peak": bf16,
+                "unit": "TFLOP/s", "frac": leg["attend_tensor_frac"], "traffic": None,
+                "peak_kind": leg["peaks"]["kind"] + " (bf16_tflops burst)"}
     line = {"metric": METRIC, "value": leg["value"], "unit": leg["unit"], "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": leg["ms_per_step"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded counter-based generator; no dataset or weights)",
             "config": dict(leg["config"], requests_kept=args.requests or None),
-            "roofline": {"kernel": leg["attend_kernel"], "bound": "hbm", "achieved": leg["attend_gbs"], "peak": hbm,
-                         "unit": "GB/s", "frac": leg["attend_hbm_frac"], "traffic": None,
-                         "peak_kind": leg["peaks"]["kind"] + " (hbm_gbs)"},
+            "roofline": roof,
             "stages_ms": leg["stages_ms"], "gpu_launches": leg["gpu_launches"], "clocks": leg["clocks"], "msa": leg}
     return line
 

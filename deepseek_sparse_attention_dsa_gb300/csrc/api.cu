@@ -205,6 +205,7 @@ void dsa_destroy(dsa_ctx_t *ctx) {
     cudaFree(ctx->scores);
     cudaFree(ctx->opart);
     cudaFree(ctx->mlpart);
+    cudaFree(ctx->block_keys);
   }
   delete ctx;
 }

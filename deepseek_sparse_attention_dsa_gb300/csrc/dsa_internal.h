@@ -102,6 +102,27 @@ __host__ __device__ inline int64_t index_tiles_per_item(int64_t tiles, int cap) 
 // its tiles) plus the merge of the partials (about 0.15 tile periods per
 // row).  The host planner and the device planner share this function, so
 // both make the same units.
+// Order-preserving 32-bit key of a score (larger score, larger key; -0.0
+// ranks as +0.0).  Every score, -inf included, has a key above 0, so 0 can
+// stand for "no score".
+__host__ __device__ inline uint32_t score_order_key(float f) {
+  union {
+    float f;
+    uint32_t u;
+  } v{f};
+  uint32_t u = v.u;
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// First word of row r's block maxima in a packed block-key array: rows are
+// laid out by their score offsets, off / block + r, which keeps the rows'
+// ranges of pos / block + 1 words disjoint (the array needs
+// num_scores / block + rows + 1 words).
+__host__ __device__ inline int64_t block_key_base(int64_t score_off, int64_t row, int block) {
+  return score_off / block + row;
+}
+
 __host__ __device__ inline int attention_splits(int64_t T, int64_t topk, int num_sms) {
   const int64_t pairs = num_sms / 2 > 1 ? num_sms / 2 : 1;
   const int64_t full_tiles = (topk + kAttTile - 1) / kAttTile;
@@ -155,6 +176,8 @@ struct dsa_ctx {
   int32_t last_launches = 0;
   char last_cuda_error[160] = {0};  // name and text of the last CUDA error a call returned DSA_ERR_CUDA for
   float *static_scores = nullptr; // device address of the library's fixed score array (dsa_index_topk_static)
+  uint32_t *block_keys = nullptr; // MSA block maxima scratch (dsa_msa_index_select)
+  size_t block_keys_cap = 0;      // words
 };
 
 struct dsa_plan {
@@ -213,6 +236,15 @@ cudaError_t launch_store_keys(const dsa_ctx *ctx, const dsa_plan_t *plan, const 
                               cudaStream_t s, int32_t *launches);
 cudaError_t launch_index_scores(const dsa_ctx *ctx, const dsa_plan_t *plan, const void *q, const float *w,
                                 const void *cache, float *scores, cudaStream_t s, int32_t *launches);
+// The indexer with a block-maximum epilogue instead of the score store: for
+// every row r and block b of `block` positions, block_keys[block_key_base(r) + b]
+// is raised (atomicMax) to the largest score_order_key of the row's visible
+// scores in that block.  The words must start at zero.  Only the bf16
+// tensor-core kernels have this epilogue (index_block_keys_supported).
+cudaError_t launch_index_block_keys(const dsa_ctx *ctx, const dsa_plan_t *plan, const void *q, const float *w,
+                                    const void *cache, uint32_t *block_keys, int block, cudaStream_t s,
+                                    int32_t *launches);
+bool index_block_keys_supported(const dsa_ctx *ctx, const dsa_plan_t *plan);
 cudaError_t launch_topk(const dsa_ctx *ctx, const dsa_plan_t *plan, const float *scores, int32_t *sel,
                         cudaStream_t s, int32_t *launches);
 cudaError_t launch_plan_update(const dsa_ctx *ctx, dsa_plan_t *plan, const int32_t *num_spans,

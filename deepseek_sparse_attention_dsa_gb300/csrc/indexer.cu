@@ -21,6 +21,11 @@
 // CTA walks a tile-balanced contiguous range of the plan's work items; single-
 // row groups (decode) run two CTAs per SM.
 //
+// The MSA block selection runs the bf16 kernel with a block-maximum epilogue
+// instead of the score store: each epilogue warp reduces the order keys of
+// its 32 keys per block they touch (redux.sync) and raises the row's block
+// word with one atomicMax, so no token score is written or read back.
+//
 // The fp8 index format (132-byte keys) runs index_fp8_tc_kernel, the same
 // contraction behind a code -> bf16 conversion stage.  Shapes outside the
 // tensor-core instances run index_simt_kernel, one CUDA-core thread per key.
@@ -80,8 +85,10 @@ struct IdxParams {
   const int32_t *pages;
   const int64_t *row_score_off;
   float *scores;
+  uint32_t *block_keys;     // block maxima (the BMAX instances) instead of scores
   int *err;
   int P, BH, num_pages;
+  int block;                // positions per block of block_keys
 };
 
 // sum_h w[h] * relu(sign * v[h]) with the weights read four at a time from
@@ -103,7 +110,9 @@ __device__ __forceinline__ float weighted_relu_sum(const float *w, const float (
   return (a0 + a1) + (a2 + a3);
 }
 
-template <int HI, int DI, int G>
+// BMAX: the block-maximum epilogue (p.block_keys, p.block) in place of the
+// score store.
+template <int HI, int DI, int G, bool BMAX>
 __global__ void __launch_bounds__(kIdxThreads, 2) index_tc_kernel(const __grid_constant__ IdxParams p) {
   using C = IdxTraits<HI, DI, G>;
   extern __shared__ uint8_t smem_raw[];
@@ -306,7 +315,10 @@ __global__ void __launch_bounds__(kIdxThreads, 2) index_tc_kernel(const __grid_c
         for (int i = et; i < G * HI; i += 32 * kEpiWarps)
           wsm[i] = (i < nrows * HI) ? p.w[static_cast<int64_t>(g.row0) * HI + i] : 0.f;
 #pragma unroll
-        for (int gg = 0; gg < G; ++gg) soff[gg] = gg < nrows ? p.row_score_off[g.row0 + gg] : 0;
+        for (int gg = 0; gg < G; ++gg) {
+          soff[gg] = gg < nrows ? p.row_score_off[g.row0 + gg] : 0;
+          if constexpr (BMAX) soff[gg] = block_key_base(soff[gg], g.row0 + gg, p.block);
+        }
         named_bar_sync(1, 32 * kEpiWarps);
       }
       bool ok = true;
@@ -316,8 +328,10 @@ __global__ void __launch_bounds__(kIdxThreads, 2) index_tc_kernel(const __grid_c
         tc_fence_after();
         const int key = t * 128 + m - lead;   // < 0: a slot before the span's token 0
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * C::N;
+        float sv[G];
 #pragma unroll
         for (int gg = 0; gg < G; ++gg) {
+          sv[gg] = 0.f;
           if (gg < nrows) {
             float s = 0.f;
             if constexpr (HI >= 16) {
@@ -336,11 +350,60 @@ __global__ void __launch_bounds__(kIdxThreads, 2) index_tc_kernel(const __grid_c
                 for (int h = 0; h < 4; ++h) s = fmaf(wsm[gg * HI + h0 + h], fmaxf(v[h], 0.f), s);
               }
             }
-            if (key >= 0 && key <= pos0 + gg) p.scores[soff[gg] + key] = s;
+            if constexpr (!BMAX) {
+              if (key >= 0 && key <= pos0 + gg) p.scores[soff[gg] + key] = s;
+            } else {
+              sv[gg] = s;
+            }
           }
         }
         tc_fence_before();
-        mbar_arrive(aempty(acc));
+        mbar_arrive(aempty(acc));   // the accumulator is read: the next tile's MMAs may take it
+        if constexpr (BMAX) {
+          // block maxima of the warp's 32 consecutive keys: a butterfly max
+          // per row (the rows' shuffles interleave) and one atomic per row
+          // and block; a warp that straddles a block edge (a lead or a block
+          // size that is not a multiple of 32) takes one reduce per block
+          const int kfirst = t * 128 + quad * 32 - lead;   // the key of lane 0
+          const int klast = kfirst + 31;
+          if (klast >= 0) {
+            const int kmin = kfirst > 0 ? kfirst : 0;
+            const int b_hi = klast / p.block;
+            if (b_hi * p.block <= kmin) {   // one block (warp-uniform)
+              float mx[G];
+              uint32_t any[G];
+#pragma unroll
+              for (int gg = 0; gg < G; ++gg) {
+                const bool vis = gg < nrows && key >= 0 && key <= pos0 + gg;
+                mx[gg] = vis ? sv[gg] : -INFINITY;
+                any[gg] = __ballot_sync(0xffffffffu, vis);
+              }
+#pragma unroll
+              for (int o = 16; o; o >>= 1)
+#pragma unroll
+                for (int gg = 0; gg < G; ++gg) mx[gg] = fmaxf(mx[gg], __shfl_xor_sync(0xffffffffu, mx[gg], o));
+              if (lane == 0) {
+#pragma unroll
+                for (int gg = 0; gg < G; ++gg)
+                  if (any[gg]) atomicMax(p.block_keys + soff[gg] + b_hi, score_order_key(mx[gg]));
+              }
+            } else {
+              const int b_lo = kmin / p.block;
+#pragma unroll
+              for (int gg = 0; gg < G; ++gg) {
+                if (gg < nrows) {
+                  const bool vis = key >= 0 && key <= pos0 + gg;
+                  const uint32_t kk = vis ? score_order_key(sv[gg]) : 0u;
+                  for (int b = b_lo; b <= b_hi; ++b) {   // warp-uniform bounds
+                    const bool in = key >= b * p.block && key < (b + 1) * p.block;
+                    const uint32_t mk = __reduce_max_sync(0xffffffffu, in ? kk : 0u);
+                    if (lane == 0 && mk != 0u) atomicMax(p.block_keys + soff[gg] + b, mk);
+                  }
+                }
+              }
+            }
+          }
+        }
         acc ^= 1;
         if (acc == 0) aphase ^= 1;
       }
@@ -421,7 +484,8 @@ __global__ void __launch_bounds__(128) index_simt_kernel(const uint16_t *__restr
 
 template <int HI, int DI, int G>
 cudaError_t run_tc(const dsa_ctx *ctx, const dsa_plan_t *plan, const IdxSet &set, const void *q, const float *w,
-                   const void *cache, float *scores, cudaStream_t s, int BH) {
+                   const void *cache, float *scores, cudaStream_t s, int BH, uint32_t *block_keys = nullptr,
+                   int block = 0) {
   using C = IdxTraits<HI, DI, G>;
   IdxParams prm{};
   const dsa_config_t &c = ctx->cfg;
@@ -439,13 +503,17 @@ cudaError_t run_tc(const dsa_ctx *ctx, const dsa_plan_t *plan, const IdxSet &set
   prm.pages = plan->pages;
   prm.row_score_off = plan->row_score_off;
   prm.scores = scores;
+  prm.block_keys = block_keys;
+  prm.block = block;
   prm.err = ctx->err;
   prm.P = c.page_size;
   prm.BH = BH;
   prm.num_pages = plan->cache_pages;
-  auto kern = index_tc_kernel<HI, DI, G>;
-  static std::atomic<uint64_t> smem_limit_set{0};
-  if (cudaError_t e = ensure_smem_limit(kern, C::SMEM, ctx->device, smem_limit_set); e != cudaSuccess) return e;
+  auto kern = block_keys ? index_tc_kernel<HI, DI, G, true> : index_tc_kernel<HI, DI, G, false>;
+  static std::atomic<uint64_t> smem_limit_set[2] = {0, 0};
+  if (cudaError_t e = ensure_smem_limit(kern, C::SMEM, ctx->device, smem_limit_set[block_keys ? 1 : 0]);
+      e != cudaSuccess)
+    return e;
   kern<<<set.n_ctas, kIdxThreads, C::SMEM, s>>>(prm);
   return cudaGetLastError();
 }
@@ -928,6 +996,39 @@ cudaError_t launch_index_scores(const dsa_ctx *ctx, const dsa_plan_t *plan, cons
                                                      plan->capturable ? plan->counts + 1 : nullptr);
       e = cudaGetLastError();
     }
+    if (e != cudaSuccess) return e;
+    *launches += 1;
+  }
+  return cudaSuccess;
+}
+
+// The block-maximum epilogue pays off where the indexer streams keys (single-
+// row groups: the score writes and the selection's re-read are a real share
+// of the traffic).  Multi-row groups are bound by the epilogue's arithmetic,
+// where the extra cross-lane reduction costs more than the score stores it
+// saves, so plans with such groups keep the score path.
+bool index_block_keys_supported(const dsa_ctx *ctx, const dsa_plan_t *plan) {
+  const dsa_config_t &c = ctx->cfg;
+  if (c.index_fmt != DSA_INDEX_BF16 || plan->box_rows < 8 || plan->capturable) return false;
+  if (plan->idx[1].n_items > 0) return false;
+  return plan->idx[0].n_items == 0 || indexer_tc_supported(c, plan->idx[0].G);
+}
+
+cudaError_t launch_index_block_keys(const dsa_ctx *ctx, const dsa_plan_t *plan, const void *q, const float *w,
+                                    const void *cache, uint32_t *block_keys, int block, cudaStream_t s,
+                                    int32_t *launches) {
+  if (!index_block_keys_supported(ctx, plan) || block <= 0) return cudaErrorNotSupported;
+  const dsa_config_t &c = ctx->cfg;
+  const int BH = plan->box_rows;
+  for (int si = 0; si < 2; ++si) {
+    const IdxSet &set = plan->idx[si];
+    if (set.n_items == 0) continue;
+    uint32_t *bk = block_keys;
+    cudaError_t e;
+    if (c.index_heads == 64 && set.G == 1) e = run_tc<64, 128, 1>(ctx, plan, set, q, w, cache, nullptr, s, BH, bk, block);
+    else if (c.index_heads == 64) e = run_tc<64, 128, 4>(ctx, plan, set, q, w, cache, nullptr, s, BH, bk, block);
+    else if (set.G == 1) e = run_tc<4, 32, 1>(ctx, plan, set, q, w, cache, nullptr, s, BH, bk, block);
+    else e = run_tc<4, 32, 4>(ctx, plan, set, q, w, cache, nullptr, s, BH, bk, block);
     if (e != cudaSuccess) return e;
     *launches += 1;
   }

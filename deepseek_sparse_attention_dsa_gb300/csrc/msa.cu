@@ -12,9 +12,13 @@
 // positions <= the row's own in the kept blocks.
 //
 // msa_select_kernel: one CTA per row; warps take blocks and reduce their
-// scores to order-preserving 32-bit keys (redux.sync max), then topk_blocks
-// rounds of a block-wide argmax (ties to the lower block) pick the blocks,
-// written in ascending order with a -1 tail.
+// scores to order-preserving 32-bit keys (redux.sync max), or read the block
+// maxima the indexer's block-maximum epilogue left.  Rows of up to 256
+// blocks rank each block by counting the blocks that beat it; longer rows
+// take four 8-bit radix passes to find the topk_blocks-th largest key tau,
+// and two block scans over contiguous runs of blocks write every block above
+// tau and the lowest blocks equal to it (ties to the lower block), in
+// ascending order either way.
 //
 // msa_attend_tc_kernel (block_size 128, head_dim 128): one CTA per row walks
 // (tile, kv head) steps.  A tile is 128 positions, one UMMA M:
@@ -25,8 +29,8 @@
 // MMAs (QK of step t+1 before PV of step t waits for its P), and eight
 // softmax warps, two per TMEM lane quadrant (thread = TMEM lane = token of S,
 // dim of O; each warp of a pair takes half of the heads), reduce each head's
-// maximum with redux.sync over order keys and its sum with halving shuffle
-// exchanges, keep a per-head
+// maximum and sum with halving shuffle exchanges (one transposing pass per
+// reduction, not one butterfly per head), keep a per-head
 // reference max that moves only when it grows by more than 2^8 (O is then
 // rescaled in TMEM), write P^T as bf16 in the 128-byte-swizzled K-major
 // layout, and normalise at the end.  Tiles start on the box boundary below
@@ -55,6 +59,8 @@ constexpr float kMsaNegBig = -1.0e30f;
 
 constexpr int kSelThreads = 512;
 constexpr int kSelMaxBlocks = 16384;          // blocks per row held in shared memory
+constexpr int kSelRankBlocks = 256;           // rows with at most this many blocks rank by counting
+static_assert(kSelRankBlocks <= kSelThreads, "one block per thread when ranking by counting");
 constexpr int kMsaMaxK = 64;                  // topk_blocks
 constexpr int kMsaTile = 128;                 // positions per tile (UMMA M)
 constexpr int kMsaMaxTiles = 2 * kMsaMaxK;
@@ -62,11 +68,7 @@ constexpr int kMsaThreads = 320;              // warp 0 TMA, warp 1 MMA, warps 2
 constexpr int kMsaSoftThreads = 256;
 constexpr int kMsaMaxKvHeads = 8;
 
-__device__ __forceinline__ uint32_t score_key(float f) {
-  uint32_t u = __float_as_uint(f);
-  if (u == 0x80000000u) u = 0u;   // -0.0 ranks as +0.0
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
+__device__ __forceinline__ uint32_t score_key(float f) { return score_order_key(f); }
 __device__ __forceinline__ float key_score(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
@@ -74,23 +76,65 @@ __device__ __forceinline__ float key_score(uint32_t k) {
 // ---------------------------------------------------------------------------
 // block selection
 // ---------------------------------------------------------------------------
+// Exclusive prefix sum of one int per thread over the kSelThreads threads of
+// the block (ws: kSelThreads / 32 + 1 words; ends with a barrier, so ws is
+// free again on return).
+__device__ __forceinline__ int sel_block_scan(int v, int *ws, int warp, int lane) {
+  constexpr int kWarps = kSelThreads / 32;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) ws[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int t = lane < kWarps ? ws[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    if (lane < kWarps) ws[lane] = t - ws[lane];   // exclusive per-warp offsets
+  }
+  __syncthreads();
+  const int r = ws[warp] + x - v;
+  __syncthreads();
+  return r;
+}
+
+// `block_keys` non-null: the block maxima come ready from the indexer's
+// block-maximum epilogue (row r's at block_key_base), and `scores` is unused.
 __global__ void __launch_bounds__(kSelThreads) msa_select_kernel(const float *__restrict__ scores,
+                                                                 const uint32_t *__restrict__ block_keys,
                                                                  const int64_t *__restrict__ row_score_off,
                                                                  const int32_t *__restrict__ row_pos, int T, int bs,
                                                                  int K, int32_t *__restrict__ sel) {
-  extern __shared__ uint32_t bkey[];   // [kSelMaxBlocks] block keys; 0 = taken (below every finite score)
-  __shared__ unsigned long long wbest[kSelThreads / 32];
-  __shared__ int chosen[kMsaMaxK];
+  extern __shared__ uint32_t bkey[];   // [kSelMaxBlocks] block keys (every score's key is above 0)
+  __shared__ int hist[256];
+  __shared__ int scan_ws[kSelThreads / 32 + 1];
+  __shared__ uint32_t sel_prefix;
+  __shared__ int sel_kleft;
   constexpr int kWarps = kSelThreads / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int row = blockIdx.x; row < T; row += gridDim.x) {
     const int pos = row_pos[row];
     if (pos < 0) continue;   // padding row (uniform over the CTA)
     const int nblk = pos / bs + 1;
-    const float *s = scores + row_score_off[row];
+    if (nblk <= K) {   // every block is kept: nothing to rank
+      int32_t *out = sel + static_cast<int64_t>(row) * K;
+      for (int i = threadIdx.x; i < K; i += kSelThreads) out[i] = i < nblk ? i : -1;
+      continue;
+    }
+    if (block_keys) {
+      const uint32_t *bk = block_keys + block_key_base(row_score_off[row], row, bs);
+      for (int b = threadIdx.x; b < nblk; b += kSelThreads) bkey[b] = bk[b];
+    }
+    const float *s = block_keys ? nullptr : scores + row_score_off[row];
     // block maxima: warp w takes blocks w, w + kWarps, ...; four blocks per
     // pass keep their loads in flight together
-    for (int b0 = warp; b0 < nblk; b0 += 4 * kWarps) {
+    for (int b0 = block_keys ? nblk : warp; b0 < nblk; b0 += 4 * kWarps) {
       uint32_t m[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -110,48 +154,104 @@ __global__ void __launch_bounds__(kSelThreads) msa_select_kernel(const float *__
     }
     __syncthreads();
     int32_t *out = sel + static_cast<int64_t>(row) * K;
-    if (nblk <= K) {
-      for (int i = threadIdx.x; i < K; i += kSelThreads) out[i] = i < nblk ? i : -1;
-    } else {
-      // K rounds of argmax over (key, lower block first)
-      for (int k = 0; k < K; ++k) {
-        unsigned long long best = 0ull;
-        for (int i = threadIdx.x; i < nblk; i += kSelThreads) {
-          const unsigned long long v =
-              (static_cast<unsigned long long>(bkey[i]) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(i));
-          best = v > best ? v : best;
+    if (nblk <= kSelRankBlocks) {
+      // few blocks: thread i ranks block i by counting the blocks that beat
+      // it (a larger key, or the same key at a lower block), and one block
+      // scan gives the kept blocks their slots in block order
+      bool take = false;
+      if (static_cast<int>(threadIdx.x) < nblk) {
+        const uint32_t ki = bkey[threadIdx.x];
+        int rank = 0;
+        for (int j = 0; j < nblk; ++j) {
+          const uint32_t kj = bkey[j];
+          rank += (kj > ki || (kj == ki && j < static_cast<int>(threadIdx.x))) ? 1 : 0;
         }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) {
-          const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, o);
-          best = y > best ? y : best;
-        }
-        if (lane == 0) wbest[warp] = best;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-          unsigned long long b = 0ull;
-          for (int w = 0; w < kWarps; ++w) b = wbest[w] > b ? wbest[w] : b;
-          const int idx = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(b & 0xFFFFFFFFull));
-          chosen[k] = idx;
-          bkey[idx] = 0u;
-        }
-        __syncthreads();
+        take = rank < K;
       }
-      if (threadIdx.x == 0) {   // ascending block order
-        for (int a = 1; a < K; ++a) {
-          const int v = chosen[a];
-          int c = a - 1;
-          while (c >= 0 && chosen[c] > v) {
-            chosen[c + 1] = chosen[c];
-            --c;
+      const int slot = sel_block_scan(take ? 1 : 0, scan_ws, warp, lane);
+      if (take && slot < K) out[slot] = static_cast<int>(threadIdx.x);
+      continue;   // (the scan ended on a barrier: bkey is free for the next row)
+    }
+    // tau = the K-th largest key: four 8-bit radix passes from the top, each
+    // over the keys that share the digits found so far
+    uint32_t prefix = 0u, pmask = 0u;
+    int kleft = K;   // keys still to take among those matching prefix
+#pragma unroll 1
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int i = threadIdx.x; i < 256; i += kSelThreads) hist[i] = 0;
+      __syncthreads();
+      // (block maxima of one row share their leading digits: the lanes of a
+      // warp with the same digit add once, by their lowest lane)
+      for (int i0 = 0; i0 < nblk; i0 += kSelThreads) {
+        const int i = i0 + static_cast<int>(threadIdx.x);
+        const uint32_t k = i < nblk ? bkey[i] : 0u;
+        const bool act = i < nblk && (k & pmask) == prefix;
+        const uint32_t d = act ? (k >> shift) & 255u : 256u;
+        const uint32_t peers = __match_any_sync(0xffffffffu, d);
+        if (act && __ffs(peers) - 1 == lane) atomicAdd(&hist[d], __popc(peers));
+      }
+      __syncthreads();
+      if (warp == 0) {
+        // lane l holds digits 8l..8l+7; above[l] = keys with a digit of a higher lane
+        int c[8], tot = 0;
+#pragma unroll
+        for (int d = 0; d < 8; ++d) {
+          c[d] = hist[8 * lane + d];
+          tot += c[d];
+        }
+        // suffix sum over the lanes: incl = keys with a digit in this lane or above
+        int incl = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_down_sync(0xffffffffu, incl, o);
+          if (lane + o < 32) incl += y;
+        }
+        int acc = incl - tot;
+        if (acc < kleft && kleft <= incl) {
+#pragma unroll
+          for (int d = 7; d >= 0; --d) {
+            if (acc + c[d] >= kleft) {
+              sel_prefix = prefix | (static_cast<uint32_t>(8 * lane + d) << shift);
+              sel_kleft = kleft - acc;
+              break;
+            }
+            acc += c[d];
           }
-          chosen[c + 1] = v;
         }
       }
       __syncthreads();
-      for (int i = threadIdx.x; i < K; i += kSelThreads) out[i] = chosen[i];
+      prefix = sel_prefix;
+      kleft = sel_kleft;
+      pmask |= 255u << shift;
     }
-    __syncthreads();   // bkey and chosen are reused by the next row
+    // the chosen blocks: every key above tau, and the kleft lowest blocks
+    // whose key equals tau; each thread takes a contiguous run of blocks so
+    // two block scans give the tie ranks and the output slots in block order
+    const uint32_t tau = prefix;
+    const int per = (nblk + kSelThreads - 1) / kSelThreads;
+    const int c0 = min(nblk, threadIdx.x * per), c1 = min(nblk, c0 + per);
+    int n_eq = 0;
+    for (int i = c0; i < c1; ++i) n_eq += bkey[i] == tau;
+    int eq_before = sel_block_scan(n_eq, scan_ws, warp, lane);
+    int n_take = 0;
+    {
+      int e = eq_before;
+      for (int i = c0; i < c1; ++i) {
+        const uint32_t k = bkey[i];
+        if (k > tau) ++n_take;
+        else if (k == tau) n_take += (e++ < kleft);
+      }
+    }
+    const int slot0 = sel_block_scan(n_take, scan_ws, warp, lane);
+    {
+      int e = eq_before, o = slot0;
+      for (int i = c0; i < c1; ++i) {
+        const uint32_t k = bkey[i];
+        const bool take = k > tau || (k == tau && e++ < kleft);
+        if (take && o < K) out[o++] = i;
+      }
+    }
+    __syncthreads();   // bkey, hist and the scan words are reused by the next row
   }
 }
 
@@ -166,13 +266,19 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// Sums over the warp of N per-lane values (N = 16 or 32) by halving
-// exchanges: at each step a lane keeps half of its values and adds the
-// partner's copy of them, so N - 1 shuffles replace 5 N.  The lane ends with
-// the sum of value (lane >> (5 - log2 N)): N = 8, lanes 4h..4h+3 hold value
-// h; N = 16, lanes 2h and 2h+1; N = 32, lane h.
-template <int N>
-__device__ __forceinline__ float warp_sum_transpose(const float (&in)[N]) {
+// Reduces over the warp N per-lane values (N = 8, 16 or 32) by halving
+// exchanges: at each step a lane keeps half of its values and combines them
+// with the partner's copy, so N - 1 + (5 - log2 N) shuffles replace 5 N.  The
+// lane ends with the result for value (lane >> (5 - log2 N)): N = 8, lanes
+// 4h..4h+3 hold value h; N = 16, lanes 2h and 2h+1; N = 32, lane h.
+struct SumOp {
+  __device__ __forceinline__ float operator()(float a, float b) const { return a + b; }
+};
+struct MaxOp {
+  __device__ __forceinline__ float operator()(float a, float b) const { return fmaxf(a, b); }
+};
+template <int N, class Op>
+__device__ __forceinline__ float warp_reduce_transpose(const float (&in)[N], Op op) {
   static_assert(N == 8 || N == 16 || N == 32, "values per lane");
   float v[N];
 #pragma unroll
@@ -185,12 +291,16 @@ __device__ __forceinline__ float warp_sum_transpose(const float (&in)[N]) {
     for (int k = 0; k < c / 2; ++k) {
       const float send = up ? v[k] : v[k + c / 2];
       const float keep = up ? v[k + c / 2] : v[k];
-      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 1 << j);
+      v[k] = op(keep, __shfl_xor_sync(0xffffffffu, send, 1 << j));
     }
   }
 #pragma unroll
-  for (int j = (N == 8 ? 1 : N == 16 ? 0 : -1); j >= 0; --j) v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1 << j);
+  for (int j = (N == 8 ? 1 : N == 16 ? 0 : -1); j >= 0; --j) v[0] = op(v[0], __shfl_xor_sync(0xffffffffu, v[0], 1 << j));
   return v[0];
+}
+template <int N>
+__device__ __forceinline__ float warp_sum_transpose(const float (&in)[N]) {
+  return warp_reduce_transpose<N>(in, SumOp{});
 }
 
 struct MsaParams {
@@ -542,11 +652,23 @@ __global__ void __launch_bounds__(kMsaThreads, 1) msa_attend_tc_kernel(const __g
       tc_fence_before();
       __syncwarp();
       if (good && lane == 0) mbar_arrive(sempty(t & 1));
-      // each head's largest logit of the tile (order keys; masked rows give 0)
+      // each head's largest logit over this warp's 32 rows of the tile (as an
+      // order key; masked rows count as -inf), by the transposing reduction
+      {
+        float mx[NH];
 #pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        const uint32_t mk = __reduce_max_sync(0xffffffffu, valid ? score_key(s[h]) : 0u);
-        if (lane == 0) rmax[(h0 + h) * 4 + quad] = mk;
+        for (int h = 0; h < NH; ++h) mx[h] = valid ? s[h] : -INFINITY;
+        if constexpr (NH <= 16) {
+          const float m = warp_reduce_transpose<NH>(mx, MaxOp{});   // lane l holds head (l >> (5 - log2 NH))
+          constexpr int SHIFT = NH == 8 ? 2 : 1;
+          if ((lane & ((1 << SHIFT) - 1)) == 0) rmax[(h0 + (lane >> SHIFT)) * 4 + quad] = score_key(m);
+        } else {
+#pragma unroll
+          for (int c0 = 0; c0 < NH; c0 += 32) {
+            const float m = warp_reduce_transpose<32>(*reinterpret_cast<float(*)[32]>(mx + c0), MaxOp{});
+            rmax[(h0 + c0 + lane) * 4 + quad] = score_key(m);
+          }
+        }
       }
       if (named_bar_any(gbar, GTHREADS, !good)) {
         ok = false;
@@ -565,7 +687,8 @@ __global__ void __launch_bounds__(kMsaThreads, 1) msa_attend_tc_kernel(const __g
         const uint4 k4 = reinterpret_cast<const uint4 *>(rmax)[h];
         const uint32_t k = max(max(k4.x, k4.y), max(k4.z, k4.w));
         const float mold = mold_sm[h];
-        // (a tile always holds a kept position, so k is a real score)
+        // (a tile always holds a kept position, so k is a real score: a
+        // quadrant with none gives the key of -inf, below every score)
         const float tmax = key_score(k) * p.scale_log2;
         alpha = 1.f;
         if (tmax > mold + kMsaRescale) {
@@ -857,14 +980,24 @@ bool msa_attend_tc_supported(const dsa_config_t &c, const dsa_msa_shape_t &ms, i
 }
 
 cudaError_t launch_msa_select(const dsa_ctx *ctx, const dsa_plan_t *plan, const dsa_msa_shape_t &ms,
-                              const float *scores, int32_t *sel, cudaStream_t s, int32_t *launches) {
-  const int smem = kSelMaxBlocks * 4;
+                              const float *scores, const uint32_t *block_keys, int32_t *sel, cudaStream_t s,
+                              int32_t *launches) {
+  // shared memory for the plan's longest row only, so short rows (prefill)
+  // fit four CTAs per SM; the grid is what stays resident
+  const int max_blocks = static_cast<int>(static_cast<int64_t>(plan->max_pos) / ms.block_size + 1);
+  const int smem = std::min(kSelMaxBlocks, std::max(max_blocks, 32)) * 4;
   static std::atomic<uint64_t> smem_limit_set{0};
-  if (cudaError_t e = ensure_smem_limit(msa_select_kernel, smem, ctx->device, smem_limit_set); e != cudaSuccess)
+  if (cudaError_t e = ensure_smem_limit(msa_select_kernel, kSelMaxBlocks * 4, ctx->device, smem_limit_set);
+      e != cudaSuccess)
     return e;
-  const int grid = std::min(plan->T, 4 * ctx->num_sms);
-  msa_select_kernel<<<std::max(1, grid), kSelThreads, smem, s>>>(scores, plan->row_score_off, plan->row_pos,
-                                                                  plan->T, ms.block_size, ms.topk_blocks, sel);
+  int per_sm = 1;
+  if (cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, msa_select_kernel, kSelThreads, smem);
+      e != cudaSuccess)
+    return e;
+  const int grid = std::min(plan->T, std::max(1, per_sm) * ctx->num_sms);
+  msa_select_kernel<<<std::max(1, grid), kSelThreads, smem, s>>>(scores, block_keys, plan->row_score_off,
+                                                                  plan->row_pos, plan->T, ms.block_size,
+                                                                  ms.topk_blocks, sel);
   *launches += 1;
   return cudaGetLastError();
 }
@@ -942,7 +1075,7 @@ dsa_status dsa_msa_select_blocks(dsa_ctx_t *ctx, const dsa_plan_t *plan, const d
   if (!dsa::msa_select_supported(plan, *shape)) return DSA_ERR_UNSUPPORTED;
   if (plan->T == 0) return DSA_OK;
   if (!scores || !block_sel) return DSA_ERR_INVALID_ARG;
-  return msa_status(ctx, dsa::launch_msa_select(ctx, plan, *shape, scores, block_sel,
+  return msa_status(ctx, dsa::launch_msa_select(ctx, plan, *shape, scores, nullptr, block_sel,
                                                 reinterpret_cast<cudaStream_t>(stream), &ctx->last_launches));
 }
 
@@ -954,11 +1087,28 @@ dsa_status dsa_msa_index_select(dsa_ctx_t *ctx, const dsa_plan_t *plan, const ds
   if (!dsa::msa_select_supported(plan, *shape)) return DSA_ERR_UNSUPPORTED;
   if (plan->T == 0) return DSA_OK;
   if (!q || !w || !index_cache || !block_sel) return DSA_ERR_INVALID_ARG;
-  if (static_cast<size_t>(plan->num_scores) > ctx->scores_cap) return DSA_ERR_INVALID_ARG;   // plan of another size
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int32_t n = 0;
-  cudaError_t e = dsa::launch_index_scores(ctx, plan, q, w, index_cache, ctx->scores, s, &n);
-  if (e == cudaSuccess) e = dsa::launch_msa_select(ctx, plan, *shape, ctx->scores, block_sel, s, &n);
+  cudaError_t e;
+  if (dsa::index_block_keys_supported(ctx, plan)) {
+    // block maxima straight from the indexer's epilogue: no token scores
+    const size_t words = static_cast<size_t>(plan->num_scores / shape->block_size) + plan->T + 1;
+    if (words > ctx->block_keys_cap) {
+      cudaFree(ctx->block_keys);
+      ctx->block_keys = nullptr;
+      ctx->block_keys_cap = 0;
+      if (cudaMalloc(&ctx->block_keys, words * sizeof(uint32_t)) != cudaSuccess) return DSA_ERR_OOM;
+      ctx->block_keys_cap = words;
+    }
+    e = cudaMemsetAsync(ctx->block_keys, 0, words * sizeof(uint32_t), s);
+    if (e == cudaSuccess)
+      e = dsa::launch_index_block_keys(ctx, plan, q, w, index_cache, ctx->block_keys, shape->block_size, s, &n);
+    if (e == cudaSuccess) e = dsa::launch_msa_select(ctx, plan, *shape, nullptr, ctx->block_keys, block_sel, s, &n);
+  } else {
+    if (static_cast<size_t>(plan->num_scores) > ctx->scores_cap) return DSA_ERR_INVALID_ARG;   // plan of another size
+    e = dsa::launch_index_scores(ctx, plan, q, w, index_cache, ctx->scores, s, &n);
+    if (e == cudaSuccess) e = dsa::launch_msa_select(ctx, plan, *shape, ctx->scores, nullptr, block_sel, s, &n);
+  }
   ctx->last_launches = n;
   return msa_status(ctx, e);
 }

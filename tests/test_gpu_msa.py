@@ -88,6 +88,33 @@ def test_msa_more_heads_per_group_and_one_kv_head():
         _run(wl)
 
 
+@pytest.mark.parametrize("page_start,block_size", [(0, 128), ([5, 37, 70, 101], 128), ([3, 0, 63, 29], 64)])
+def test_msa_block_maxima_from_the_indexer_epilogue(page_start, block_size):
+    """Decode-only steps take the indexer's block-maximum epilogue (no token
+    scores): its selection equals the score path's exactly and matches the
+    oracle.  Token 0 off the 32-key boundary puts warps across block edges;
+    blocks of 64 put two blocks in one 128-key tile."""
+    sh = W.MSAShape(block_size=block_size, topk_blocks=6, q_heads=8, kv_heads=2,
+                    head_dim=128 if block_size == 128 else 64,
+                    sm_scale=1.0 / np.sqrt(128.0 if block_size == 128 else 64.0))
+    wl = W.build_workload("msa_fused", sh.index_shape(), [(1499, 1), (699, 1), (2999, 1), (130, 1)], 2106,
+                          W.Distributions(w=("uniform", 0.0, 1.0 / 8)), page_start=page_start)
+    wl.msa = sh
+    ic, kv, st, q = _inputs(wl)
+    ref = oracle.msa_run_all(wl, ic, kv, st, q)
+    ctx = dsa.Context(wl.shape, 0)
+    plan = ctx.plan(wl.spans, wl.num_pages)
+    icd = ic.cuda()
+    ctx.store_keys(plan, st.keys.cuda(), icd)
+    fused = ctx.msa_index_select(plan, sh, st.q.cuda(), st.w.cuda(), icd)
+    scores = ctx.index_scores(plan, st.q.cuda(), st.w.cuda(), icd)
+    via_scores = ctx.msa_select_blocks(plan, sh, scores)
+    ctx.get_error()
+    assert torch.equal(fused, via_scores)
+    H.check_selection(fused.cpu().numpy(), ref["selection"], ref["block_scores"], ref["block_offsets"],
+                      sh.topk_blocks)
+
+
 def test_msa_cuda_core_shapes():
     """Shapes outside the tensor-core kernel (head_dim 64, blocks of 64) run the
     CUDA-core kernel, checked the same way."""
@@ -97,11 +124,11 @@ def test_msa_cuda_core_shapes():
     _run(wl, expect_tc=False)
 
 
-def test_msa_decode_full_size_sampled_rows():
-    """msa_decode at full size (128 rows at 64K-128K, top 16 blocks of 128, 64
-    query heads over 4 kv heads): the whole step on the GPU in the bench's
-    launch configuration, 16 sampled rows recomputed by the oracle."""
-    wl = W.msa_config("msa_decode")
+def _full_size_sampled_rows(name, nsample, seed):
+    """The whole MSA step of `name` at full size on the GPU, in the bench's
+    launch configuration (the fused index-select call), with the score path
+    beside it; `nsample` sampled rows recomputed by the oracle."""
+    wl = W.msa_config(name)
     ms, sh = wl.msa, wl.shape
     dev = torch.device("cuda", 0)
     ic = W.make_index_cache(wl, device=dev)
@@ -112,17 +139,21 @@ def test_msa_decode_full_size_sampled_rows():
     plan = ctx.plan(wl.spans, wl.num_pages)
     assert ctx.msa_attend_on_tensor_cores(plan, ms)
     ctx.store_keys(plan, st.keys, ic)
+    sel = ctx.msa_index_select(plan, ms, st.q, st.w, ic)
     scores = ctx.index_scores(plan, st.q, st.w, ic)
-    sel = ctx.msa_select_blocks(plan, ms, scores)
+    sel_s = ctx.msa_select_blocks(plan, ms, scores)
     out = ctx.msa_attend(plan, ms, sel, q, kv, ms.sm_scale)
     ctx.get_error()
-    _, pos_all, _ = wl.row_table()
+    # block maxima from the indexer's epilogue select what the stored scores select
+    assert torch.equal(sel, sel_s)
+    span_of, pos_all, _ = wl.row_table()
     off_all = np.zeros(wl.num_rows + 1, np.int64)
     np.cumsum(pos_all + 1, out=off_all[1:])
-    rng = np.random.default_rng(7)
-    for span_i in rng.choice(len(wl.spans), size=16, replace=False):
-        row = wl.spans[span_i].q_start
-        rw = wl.row_workload(int(span_i), 0)
+    rng = np.random.default_rng(seed)
+    for row in rng.choice(wl.num_rows, size=nsample, replace=False):
+        row = int(row)
+        span_i = int(span_of[row])
+        rw = wl.row_workload(span_i, row - wl.spans[span_i].q_start)
         ric = W.make_index_cache(rw)
         rst = W.make_step_inputs(rw)
         cache = oracle.store_keys(sh, rw.spans, rw.num_pages, rst.keys, ric)
@@ -141,3 +172,16 @@ def test_msa_decode_full_size_sampled_rows():
         rq = W.make_msa_q(rw)
         ref = oracle.msa_attend(ms, rw.spans, rw.num_pages, g_sel, rq, rkv)
         H.check_attention(out[row:row + 1].float().cpu().numpy(), ref)
+
+
+def test_msa_decode_full_size_sampled_rows():
+    """msa_decode at full size (128 rows at 64K-128K, top 16 blocks of 128, 64
+    query heads over 4 kv heads): 16 sampled rows recomputed by the oracle."""
+    _full_size_sampled_rows("msa_decode", 16, 7)
+
+
+def test_msa_prefill_full_size_sampled_rows():
+    """msa_prefill at full size (one request, 8,192 new rows after 8,192
+    cached; multi-row indexer groups): 12 sampled rows recomputed by the
+    oracle."""
+    _full_size_sampled_rows("msa_prefill", 12, 8)
