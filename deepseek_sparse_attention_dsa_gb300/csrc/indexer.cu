@@ -21,10 +21,11 @@
 // CTA walks a tile-balanced contiguous range of the plan's work items; single-
 // row groups (decode) run two CTAs per SM.
 //
-// The MSA block selection runs the bf16 kernel with a block-maximum epilogue
-// instead of the score store: each epilogue warp reduces the order keys of
-// its 32 keys per block they touch (redux.sync) and raises the row's block
-// word with one atomicMax, so no token score is written or read back.
+// The MSA block selection of decode steps runs the bf16 kernel with a
+// block-maximum epilogue instead of the score store: each epilogue warp
+// reduces its 32 keys' scores per block they touch (a shuffle butterfly, the
+// rows of a group interleaved) and raises the row's block word with one
+// atomicMax of the order key, so no token score is written or read back.
 //
 // The fp8 index format (132-byte keys) runs index_fp8_tc_kernel, the same
 // contraction behind a code -> bf16 conversion stage.  Shapes outside the

@@ -41,6 +41,7 @@ namespace {
 // 512 threads, two per SM, when persistent CTAs take several rows each
 constexpr int kMaxWarps = 32;
 constexpr int kBatch = 16;            // independent loads in flight per thread
+constexpr int kScanBatch4 = 8;        // float4 loads in flight per thread in the candidate pass
 constexpr int kCandCap = 8192;        // candidate keys held in shared memory
 constexpr int kSampleMin = 4096;      // a strided sample holds kSampleMin .. 2*kSampleMin-1 keys
 constexpr int kBitmapWords = 8192;    // 262,144 positions
@@ -66,6 +67,10 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t u = __float_as_uint(f);
   if (u == 0x80000000u) u = 0u;  // -0.0 and +0.0 are the same score
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+// The score of an order key (+0.0 for the key of both zeros).
+__device__ __forceinline__ float key_to_score(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
 // Exclusive prefix sum over the block of one int per thread; *total gets the sum.
@@ -211,22 +216,69 @@ __device__ __forceinline__ void select_row(const float *__restrict__ scores, con
           for (int j = tid; j < m; j += kTopkThreads) visit(sm.sample[j]);
         },
         rank, sm, &unused);
-    // every key of the row at or above l0
-    for (int base = 0; base < n; base += kTopkThreads * kBatch) {
-      uint32_t k[kBatch];
+    // every key of the row at or above l0: the 16-byte-aligned body as
+    // float4 loads (kScanBatch4 per thread in flight), compared as floats
+    // against f0, the score whose key is l0 (order_key is monotone and maps
+    // -0.0 and +0.0 to one key, as >= does), each batch's candidates placed
+    // by one warp scan and one shared-memory atomic per warp; the unaligned
+    // head and the tail (< 4 keys each) by warp 0
+    const float f0 = key_to_score(l0);
+    const int a0 = min(n, static_cast<int>((4u - ((reinterpret_cast<uintptr_t>(s) >> 2) & 3u)) & 3u));
+    const int nb4 = (n - a0) >> 2;
+    const float4 *s4 = reinterpret_cast<const float4 *>(s + a0);
+    constexpr int kB4 = kScanBatch4;
+    for (int base = 0; base < nb4; base += kTopkThreads * kB4) {
+      float4 v[kB4];
 #pragma unroll
-      for (int j = 0; j < kBatch; ++j) {
-        const int i = base + j * kTopkThreads + tid;
-        k[j] = i < n ? order_key(__ldg(s + i)) : 0u;
+      for (int j = 0; j < kB4; ++j) {
+        const int i4 = base + j * kTopkThreads + tid;
+        v[j] = i4 < nb4 ? __ldg(s4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
+      // (past the row's end nothing counts, whatever f0 is)
+      const int nvalid4 = min(kB4, max(0, (nb4 - base - tid + kTopkThreads - 1) / kTopkThreads));
+      int cnt = 0;
 #pragma unroll
-      for (int j = 0; j < kBatch; ++j) {
-        const int i = base + j * kTopkThreads + tid;
-        const int c = warp_append(i < n && k[j] >= l0, &sm.n_cand);
-        if (c >= 0 && c < kCandCap) {
-          sm.ckey[c] = k[j];
-          sm.cpos[c] = i;
+      for (int j = 0; j < kB4; ++j)
+        if (j < nvalid4) cnt += (v[j].x >= f0) + (v[j].y >= f0) + (v[j].z >= f0) + (v[j].w >= f0);
+      if (__any_sync(0xffffffffu, cnt > 0)) {
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
         }
+        int wbase = 0;
+        if (lane == 31) wbase = atomicAdd(&sm.n_cand, incl);
+        int c = __shfl_sync(0xffffffffu, wbase, 31) + incl - cnt;
+        if (cnt > 0) {
+#pragma unroll
+          for (int j = 0; j < kB4; ++j) {
+            if (j >= nvalid4) break;
+            const float e4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              if (e4[e] >= f0) {
+                if (c < kCandCap) {
+                  sm.ckey[c] = order_key(e4[e]);
+                  sm.cpos[c] = a0 + 4 * (base + j * kTopkThreads + tid) + e;
+                }
+                ++c;
+              }
+            }
+          }
+        }
+      }
+    }
+    if (warp == 0) {
+      // head keys [0, a0) and tail keys [a0 + 4 nb4, n)
+      const int t0 = a0 + 4 * nb4;
+      const int i = lane < 4 ? lane : t0 + (lane - 4);
+      const bool in = lane < 4 ? lane < a0 : i < n;
+      const uint32_t key = in ? order_key(__ldg(s + i)) : 0u;
+      const int c = warp_append(in && key >= l0, &sm.n_cand);
+      if (c >= 0 && c < kCandCap) {
+        sm.ckey[c] = key;
+        sm.cpos[c] = i;
       }
     }
     __syncthreads();
