@@ -10,9 +10,10 @@
 // the data:
 //   1. candidates: a row with at most kCandCap keys takes all of them.  A
 //      longer row takes an evenly strided sample (4096..8191 keys) into shared
-//      memory, finds the sample key whose rank, scaled by the stride, lies a
-//      safe margin above topk, and keeps every key of the row at or above it
-//      (one pass over the row).  When that leaves fewer than topk keys or more
+//      memory, finds (to within a 2^10-key bin, below it) the sample key
+//      whose rank, scaled by the stride, lies a safe margin above topk, and
+//      keeps every key of the row at or above that bound (one pass over the
+//      row, float4 loads compared as floats).  When that leaves fewer than topk keys or more
 //      than kCandCap, the threshold is found by radix passes over the row in
 //      global memory instead.
 //   2. the k-th largest key tau and the number of tau ties to take (the
@@ -136,13 +137,15 @@ __device__ __forceinline__ int find_bin(const int *hist, int need, int *ws, int 
 // The rank-th largest key (rank >= 1) of the keys produced by `for_each`
 // (called as for_each(visit) with visit(key) for every key, by every thread
 // over its share), by three radix passes of 11, 11 and 10 bits.  *ties gets
-// how many keys equal to the result lie within the top `rank`.
-template <int NT, typename ForEach>
+// how many keys equal to the result lie within the top `rank`.  With
+// PASSES = 2 the result is the lower edge of the 2^10-key bin that holds it
+// (a bound at or below the rank-th key; *ties is then meaningless).
+template <int NT, int PASSES = 3, typename ForEach>
 __device__ __forceinline__ uint32_t radix_select(ForEach for_each, int rank, TopkSmem<NT> &sm, int *ties) {
   uint32_t prefix = 0, pmask = 0;
   int need = rank;
 #pragma unroll 1
-  for (int pass = 0; pass < 3; ++pass) {
+  for (int pass = 0; pass < PASSES; ++pass) {
     const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
     const int nbins = pass == 2 ? 1024 : 2048;
     for (int i = threadIdx.x; i < 2048; i += NT) sm.hist[i] = 0;
@@ -210,8 +213,10 @@ __device__ __forceinline__ void select_row(const float *__restrict__ scores, con
     const float ks = static_cast<float>(K) / static_cast<float>(stride);
     int rank = static_cast<int>(1.15f * ks + 3.f * sqrtf(ks)) + 8;
     rank = min(rank, m);
+    // (a threshold at or below that key is all the pass needs: the lower
+    // edge of its 2^10-key bin, two radix passes instead of three)
     int unused;
-    const uint32_t l0 = radix_select<NT>(
+    const uint32_t l0 = radix_select<NT, 2>(
         [&](auto visit) {
           for (int j = tid; j < m; j += kTopkThreads) visit(sm.sample[j]);
         },
