@@ -115,6 +115,35 @@ def test_msa_block_maxima_from_the_indexer_epilogue(page_start, block_size):
                       sh.topk_blocks)
 
 
+def test_msa_radix_selection_exact_on_integer_inputs():
+    """Rows of 260-550 blocks take the radix path of the block selection;
+    integer-valued index inputs on a 4 x 32 indexer make every token score
+    exact and small, so block maxima tie at the k-th block (two of the rows
+    drop a tie there) and the kept set must be the oracle's exactly (ties to
+    the lower block), through the indexer's block-maximum epilogue and
+    through stored scores alike."""
+    sh = W.MSAShape(topk_blocks=16, q_heads=8, kv_heads=2, index_heads=4, index_dim=32)
+    wl = W.build_workload("msa_radix", sh.index_shape(), [(33300, 1), (70000, 1), (47999, 1)], 2107,
+                          W.Distributions(w=("uniform", 0.0, 1.0 / 8), integer=True))
+    wl.msa = sh
+    ic, kv, st, q = _inputs(wl)
+    ref = oracle.msa_run_all(wl, ic, kv, st, q)
+    ctx = dsa.Context(wl.shape, 0)
+    plan = ctx.plan(wl.spans, wl.num_pages)
+    icd = ic.cuda()
+    ctx.store_keys(plan, st.keys.cuda(), icd)
+    fused = ctx.msa_index_select(plan, sh, st.q.cuda(), st.w.cuda(), icd)
+    scores = ctx.index_scores(plan, st.q.cuda(), st.w.cuda(), icd)
+    via_scores = ctx.msa_select_blocks(plan, sh, scores)
+    ctx.get_error()
+    assert torch.equal(fused, via_scores)
+    H.check_selection(fused.cpu().numpy(), ref["selection"], ref["block_scores"], ref["block_offsets"],
+                      sh.topk_blocks, exact=True)
+    out = ctx.msa_attend(plan, sh, fused, q.cuda(), kv.cuda(), sh.sm_scale)
+    ctx.get_error()
+    H.check_attention(out.float().cpu().numpy(), ref["out"])
+
+
 def test_msa_cuda_core_shapes():
     """Shapes outside the tensor-core kernel (head_dim 64, blocks of 64) run the
     CUDA-core kernel, checked the same way."""
