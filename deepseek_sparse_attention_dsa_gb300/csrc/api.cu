@@ -40,6 +40,8 @@ dsa_status supported_config(const dsa_config_t &c) {
   if (((c.kv_lora_rank + c.rope_dim) * 2) % 16 != 0) return DSA_ERR_UNSUPPORTED;
   if (c.kv_lora_rank % 8 != 0 || c.rope_dim % 8 != 0) return DSA_ERR_UNSUPPORTED;
   if (c.kv_lora_rank > 1024 || c.index_heads > 256 || c.heads > 1024) return DSA_ERR_UNSUPPORTED;
+  // the attention schedule cuts a row into at most kAttMaxPieces pieces
+  if (c.topk > 16384) return DSA_ERR_UNSUPPORTED;
   return DSA_OK;
 }
 
@@ -309,37 +311,52 @@ dsa_status dsa_plan(dsa_ctx_t *ctx, const dsa_span_t *spans, int32_t num_spans, 
   }
   plan->n_index_items = static_cast<int32_t>(n_index_items);
 
-  // ---- attention units: rows split over key ranges when there are few rows
+  // ---- attention: the rows' key tiles, in row order, cut into contiguous
+  // ranges, one per persistent two-CTA cluster; a row a cut crosses becomes
+  // one unit per piece, each with a partial slot, merged afterwards
   std::vector<AttUnit> units;
   std::vector<AttCombine> combines;
+  std::vector<AttCluster> clusters;
   {
     const int64_t K = c.topk;
-    const int splits = attention_splits(T, K, ctx->num_sms);
+    int64_t S = 0;
+    for (int32_t i = 0; i < num_spans; ++i)
+      for (int32_t r = 0; r < spans[i].q_len; ++r) S += att_row_tiles(static_cast<int64_t>(spans[i].ctx_start) + r, K);
+    int32_t ncl = 0;
+    int64_t per = 1;
+    att_cluster_split(S, ctx->num_sms, &ncl, &per);
+    clusters.assign(ncl, AttCluster{0, 0, 0, 0});
     int32_t slot = 0;
     int32_t row = 0;
+    int64_t off = 0;
     for (int32_t i = 0; i < num_spans; ++i) {
       const dsa_span_t &s = spans[i];
       for (int32_t r = 0; r < s.q_len; ++r, ++row) {
         const int64_t pos = s.ctx_start + r;
         const int64_t nsel = std::min<int64_t>(K, pos + 1);
-        const int64_t tiles = (nsel + kAttTile - 1) / kAttTile;
-        const int64_t sp = attention_row_units(pos, K, splits);
-        if (sp == 1) {
-          units.push_back(AttUnit{row, 0, static_cast<int32_t>(nsel), -1});
-        } else {
-          combines.push_back(AttCombine{row, slot, static_cast<int32_t>(sp), 0});
-          for (int64_t k = 0; k < sp; ++k) {
-            const int64_t t0 = tiles * k / sp, t1 = tiles * (k + 1) / sp;
-            units.push_back(AttUnit{row, static_cast<int32_t>(t0 * kAttTile),
-                                    static_cast<int32_t>(std::min<int64_t>(nsel, t1 * kAttTile)), slot++});
-          }
-          plan->splits_max = std::max<int32_t>(plan->splits_max, static_cast<int32_t>(sp));
+        const int64_t n = att_row_tiles(pos, K);
+        const int64_t c0 = off / per, c1 = (off + n - 1) / per;
+        const int32_t pieces = static_cast<int32_t>(c1 - c0 + 1);
+        if (pieces > 1) combines.push_back(AttCombine{row, slot, pieces, 0});
+        for (int64_t cl = c0; cl <= c1; ++cl) {
+          const int64_t a = std::max<int64_t>(off, cl * per), b = std::min<int64_t>(off + n, (cl + 1) * per);
+          if (a == cl * per) clusters[cl].u0 = static_cast<int32_t>(units.size());   // the cluster starts here
+          units.push_back(AttUnit{row, static_cast<int32_t>((a - off) * kAttTile),
+                                  static_cast<int32_t>(std::min<int64_t>(nsel, (b - off) * kAttTile)),
+                                  pieces > 1 ? slot++ : -1});
         }
+        plan->splits_max = std::max(plan->splits_max, pieces);
+        off += n;
       }
+    }
+    for (int32_t cl = 0; cl < ncl; ++cl) {
+      clusters[cl].u1 = cl + 1 < ncl ? clusters[cl + 1].u0 : static_cast<int32_t>(units.size());
+      clusters[cl].tiles = static_cast<int32_t>(std::min<int64_t>(per, S - cl * per));
     }
     plan->n_units = static_cast<int32_t>(units.size());
     plan->n_combine = static_cast<int32_t>(combines.size());
     plan->n_slots = slot;
+    plan->n_clusters = ncl;
   }
 
   // needs_selection: some row sees more than topk keys (mstar DSAPlan)
@@ -355,7 +372,8 @@ dsa_status dsa_plan(dsa_ctx_t *ctx, const dsa_span_t *spans, int32_t num_spans, 
     o_i[set] = lay.take<IdxItem>(items[set].size());
     o_c[set] = lay.take<int32_t>(cta_begin[set].size());
   }
-  const size_t o_u = lay.take<AttUnit>(units.size()), o_cb = lay.take<AttCombine>(combines.size());
+  const size_t o_u = lay.take<AttUnit>(units.size()), o_cb = lay.take<AttCombine>(combines.size()),
+               o_cl = lay.take<AttCluster>(clusters.size());
   const size_t bytes = std::max<size_t>(lay.bytes, 256);
   try {
     plan->host.assign(bytes, 0);
@@ -394,6 +412,7 @@ dsa_status dsa_plan(dsa_ctx_t *ctx, const dsa_span_t *spans, int32_t num_spans, 
     }
     if (!units.empty()) std::memcpy(h + o_u, units.data(), units.size() * sizeof(AttUnit));
     if (!combines.empty()) std::memcpy(h + o_cb, combines.data(), combines.size() * sizeof(AttCombine));
+    if (!clusters.empty()) std::memcpy(h + o_cl, clusters.data(), clusters.size() * sizeof(AttCluster));
   }
 
   if (is_host_only(ctx)) {
@@ -426,6 +445,7 @@ dsa_status dsa_plan(dsa_ctx_t *ctx, const dsa_span_t *spans, int32_t num_spans, 
   }
   plan->units = reinterpret_cast<AttUnit *>(d + o_u);
   plan->combine = reinterpret_cast<AttCombine *>(d + o_cb);
+  plan->clusters = reinterpret_cast<AttCluster *>(d + o_cl);
   *out = plan;
   return DSA_OK;
 }
@@ -457,9 +477,13 @@ dsa_status dsa_plan_capturable(dsa_ctx_t *ctx, int32_t max_rows, int32_t max_spa
   const dsa_config_t &c = ctx->cfg;
   // worst-case work for any update within the capacities
   const int64_t items_cap = max_scores / kIndexTile + 2 * static_cast<int64_t>(max_rows) + 1;
-  int64_t units_cap = 1;
-  for (int64_t t = 1; t <= max_rows; ++t)
-    units_cap = std::max<int64_t>(units_cap, t * attention_splits(t, c.topk, ctx->num_sms));
+  // attention: at most one cluster per two SMs; each cut between clusters
+  // adds one unit and at most one split row, and each split row's pieces are
+  // its cuts plus one
+  const int32_t clusters_cap = std::max(1, std::min(ctx->num_sms / 2, 1024));   // the device planner: one thread each
+  const int64_t units_cap = static_cast<int64_t>(max_rows) + clusters_cap;
+  const int32_t combine_cap = std::min(max_rows, clusters_cap);
+  const int32_t slots_cap = 2 * clusters_cap;
   if (items_cap > INT32_MAX / 2 || units_cap > INT32_MAX / 2) return DSA_ERR_INVALID_ARG;
   const int idx_cap = std::max(1, ctx->num_sms * indexer_ctas_per_sm(c, 1));
 
@@ -478,12 +502,13 @@ dsa_status dsa_plan_capturable(dsa_ctx_t *ctx, int32_t max_rows, int32_t max_spa
   plan->page_start_align = page_start_align;
   plan->box_rows = index_box_rows(c.page_size);
   plan->items_cap = static_cast<int32_t>(items_cap);
-  plan->combine_cap = max_rows;
+  plan->combine_cap = combine_cap;
   plan->n_units = static_cast<int32_t>(units_cap);
-  plan->n_combine = max_rows;
-  plan->n_slots = static_cast<int32_t>(units_cap);
+  plan->n_combine = combine_cap;
+  plan->n_slots = slots_cap;
+  plan->n_clusters = clusters_cap;
   plan->n_index_items = plan->items_cap;
-  plan->splits_max = 16;
+  plan->splits_max = clusters_cap;
   IdxSet &set = plan->idx[0];
   set.G = 1;
   set.n_groups = max_rows;
@@ -495,8 +520,8 @@ dsa_status dsa_plan_capturable(dsa_ctx_t *ctx, int32_t max_rows, int32_t max_spa
                o_np = lay.take<int32_t>(max_rows), o_ps = lay.take<int32_t>(max_rows),
                o_soff = lay.take<int64_t>(max_rows), o_g = lay.take<IdxGroup>(max_rows),
                o_i = lay.take<IdxItem>(items_cap), o_c = lay.take<int32_t>(idx_cap + 1),
-               o_u = lay.take<AttUnit>(units_cap), o_cb = lay.take<AttCombine>(max_rows), o_n = lay.take<int32_t>(8),
-               o_sp = lay.take<int8_t>(max_rows + 1);
+               o_u = lay.take<AttUnit>(units_cap), o_cb = lay.take<AttCombine>(combine_cap), o_n = lay.take<int32_t>(8),
+               o_cl = lay.take<AttCluster>(clusters_cap);
   auto fail = [&](dsa_status st) {
     dsa_plan_destroy(plan);
     return st;
@@ -507,10 +532,10 @@ dsa_status dsa_plan_capturable(dsa_ctx_t *ctx, int32_t max_rows, int32_t max_spa
   if (cudaMalloc(reinterpret_cast<void **>(&plan->dev), lay.bytes) != cudaSuccess ||
       cudaMalloc(reinterpret_cast<void **>(&plan->own_scores), static_cast<size_t>(max_scores) * sizeof(float)) !=
           cudaSuccess ||
-      cudaMalloc(reinterpret_cast<void **>(&plan->own_opart), static_cast<size_t>(units_cap) * hl * sizeof(float)) !=
+      cudaMalloc(reinterpret_cast<void **>(&plan->own_opart), static_cast<size_t>(slots_cap) * hl * sizeof(float)) !=
           cudaSuccess ||
       cudaMalloc(reinterpret_cast<void **>(&plan->own_mlpart),
-                 static_cast<size_t>(units_cap) * c.heads * 2 * sizeof(float)) != cudaSuccess)
+                 static_cast<size_t>(slots_cap) * c.heads * 2 * sizeof(float)) != cudaSuccess)
     return fail(DSA_ERR_OOM);
   char *d = plan->dev;
   plan->row_pos = reinterpret_cast<int32_t *>(d + o_pos);
@@ -524,15 +549,14 @@ dsa_status dsa_plan_capturable(dsa_ctx_t *ctx, int32_t max_rows, int32_t max_spa
   plan->units = reinterpret_cast<AttUnit *>(d + o_u);
   plan->combine = reinterpret_cast<AttCombine *>(d + o_cb);
   plan->counts = reinterpret_cast<int32_t *>(d + o_n);
-  plan->splits_by_rows = reinterpret_cast<int8_t *>(d + o_sp);
+  plan->clusters = reinterpret_cast<AttCluster *>(d + o_cl);
   // an empty plan until the first update: every row is padding, no work
   std::vector<char> h(lay.bytes, 0);
   std::fill_n(reinterpret_cast<int32_t *>(h.data() + o_pos), max_rows, -1);
   for (int64_t i = 0; i < items_cap; ++i) reinterpret_cast<IdxItem *>(h.data() + o_i)[i] = IdxItem{-1, 0, 0, 0};
   for (int64_t i = 0; i < units_cap; ++i) reinterpret_cast<AttUnit *>(h.data() + o_u)[i] = AttUnit{-1, 0, 0, -1};
-  for (int32_t i = 0; i < max_rows; ++i) reinterpret_cast<AttCombine *>(h.data() + o_cb)[i] = AttCombine{-1, 0, 0, 0};
-  for (int32_t t = 0; t <= max_rows; ++t)
-    reinterpret_cast<int8_t *>(h.data() + o_sp)[t] = static_cast<int8_t>(attention_splits(t, c.topk, ctx->num_sms));
+  for (int32_t i = 0; i < combine_cap; ++i) reinterpret_cast<AttCombine *>(h.data() + o_cb)[i] = AttCombine{-1, 0, 0, 0};
+  // (clusters start idle: zero-filled, u0 == u1)
   if (cudaMemcpy(plan->dev, h.data(), lay.bytes, cudaMemcpyHostToDevice) != cudaSuccess) return fail(DSA_ERR_CUDA);
   *out = plan;
   return DSA_OK;

@@ -103,8 +103,9 @@ struct AttTraits {
   static constexpr int OFF_K = OFF_QS + QS_CH * QCHUNK;
   static constexpr int OFF_X = OFF_K + STAGES * STAGE;   // x_in (two halves) then x_out (XOUT bytes)
   static constexpr int OFF_ROWS = OFF_X + XBYTES + XOUT;   // int32 [STAGES][TILE]
-  static constexpr int OFF_RED = OFF_ROWS + STAGES * TILE * 4;   // fp32 [2 tiles][2 halves][128] maxima, [2][128] sums
-  static constexpr int OFF_BAR = OFF_RED + (4 + 2) * 128 * 4;
+  // fp32 [2 tiles][2 halves][128] maxima, then [2 units][2 halves][128] sums
+  static constexpr int OFF_RED = OFF_ROWS + STAGES * TILE * 4;
+  static constexpr int OFF_BAR = OFF_RED + (4 + 4) * 128 * 4;
   static constexpr int NBAR = 24;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;
@@ -114,11 +115,6 @@ struct AttTraits {
   static_assert(QT_CH * 32 <= static_cast<int>(P_COL) && P_COL + TILE / 2 <= S_COL, "tensor memory: Q, P");
   static_assert(O_COL + HALF <= TMEM_COLS, "tensor memory: O");
   static_assert(QRBYTES <= OFF_K && STAGE % 1024 == 0, "alignment");
-  // the q_nope chunks bound for TMEM are staged in the stage buffers from
-  // QT_STAGE on, so the first tiles' gathers need not wait for the move
-  static constexpr int QT_STAGE = 2;
-  static constexpr int OFF_QT = OFF_K + QT_STAGE * STAGE;
-  static_assert(STAGES > QT_STAGE && QT_CH * QCHUNK <= (STAGES - QT_STAGE) * STAGE, "Q staging");
   static_assert(NBAR >= 16 + 2 * STAGES, "barriers");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
@@ -126,10 +122,12 @@ struct AttTraits {
 struct AttParams {
   CUtensorMap tm_qn;       // q_nope as [T*H, L] bf16, box {64, 128}, 128-byte swizzle
   CUtensorMap tm_qp;       // q_pe as [T*H, R] bf16, box {32, 128}, 64-byte swizzle
+  const __nv_bfloat16 *qn; // q_nope [T][H][L] (the chunks that go to tensor memory are read directly)
   const int32_t *sel;
   const uint8_t *latent;   // bf16 rows [L+R] or fp8 656-byte rows, [pages*P]
   const float *sink;
   const AttUnit *units;
+  const AttCluster *clusters;   // [grid / 2]
   const int32_t *row_pos, *row_page_off, *row_npages, *row_page_start, *pages;
   __nv_bfloat16 *out;      // [T][H][L]
   float *opart;            // [slots][H][L]
@@ -200,7 +198,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + C::OFF_BAR;
-  const uint32_t b_qsfull = bar0, b_qtfull = bar0 + 8, b_qtdone = bar0 + 16, b_pvdone = bar0 + 24;
+  // qsfull: a unit's rope and shared-memory q_nope columns landed (TMA);
+  // qkdone: a unit's last QK completed (its Q may be replaced); qtdone: the
+  // softmax warps wrote a unit's tensor-memory q_nope columns; pvdone: a PV
+  // completed; ofree: the softmax warps have read a unit's O out
+  const uint32_t b_qsfull = bar0, b_qkdone = bar0 + 8, b_qtdone = bar0 + 16, b_pvdone = bar0 + 24;
   auto kfull = [&](int s) { return bar0 + 8u * (4 + s); };
   auto kempty = [&](int s) { return bar0 + 8u * (4 + NS + s); };
   auto sfull = [&](int b) { return bar0 + 8u * (4 + 2 * NS + b); };
@@ -208,6 +210,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
   auto pfull = [&](int b) { return bar0 + 8u * (8 + 2 * NS + b); };
   auto xfull = [&](int b) { return bar0 + 8u * (10 + 2 * NS + b); };   // the partner's partial landed in x_in[b]
   auto xfree = [&](int b) { return bar0 + 8u * (12 + 2 * NS + b); };   // the partner has read our x_in[b] copy
+  const uint32_t b_ofree = bar0 + 8u * (14 + 2 * NS);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
   int32_t *rows_sm = reinterpret_cast<int32_t *>(smem + C::OFF_ROWS);
@@ -215,17 +218,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
   const int warp = threadIdx.x / 32, lane = lane_id();
   const uint32_t crank = cluster_rank();
   const uint32_t peer = crank ^ 1u;
-  const AttUnit unit = p.units[blockIdx.x >> 1];
-  const int row = unit.row;
-  if (row < 0) return;   // padding of a capturable plan: both CTAs of the pair leave before any cluster step
-  const int pos = p.row_pos[row];
-  const int nent = unit.k1 - unit.k0;
-  const int ntiles = (nent + T - 1) / T;
-  const int32_t *selrow = p.sel + static_cast<int64_t>(row) * p.K + unit.k0;
+  // this cluster's units: contiguous pieces of rows, `ntotal` key tiles in all
+  const AttCluster cl = p.clusters[blockIdx.x >> 1];
+  if (cl.u0 >= cl.u1) return;   // an idle cluster: both CTAs of the pair leave before any cluster step
+  const int ntotal = cl.tiles;
+  auto unit_tiles = [&](const AttUnit &u) { return (u.k1 - u.k0 + T - 1) / T; };
 
   if (threadIdx.x == 0) {
     mbar_init(b_qsfull, 1);
-    mbar_init(b_qtfull, 1);
+    mbar_init(b_qkdone, 1);
     mbar_init(b_qtdone, 8);   // softmax arrivals are one elected lane per warp (after __syncwarp)
     mbar_init(b_pvdone, 1);
     for (int s = 0; s < NS; ++s) {
@@ -241,6 +242,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
       mbar_init(xfull(b), 1);   // armed locally with the tile's bytes, filled by the partner's bulk copy
       mbar_init(xfree(b), 4);   // one arrival per partner softmax warp of half b
     }
+    mbar_init(b_ofree, 8);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -255,19 +257,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
 
   if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
+    // One polling loop over the cluster's tiles: PV of the oldest softmaxed
+    // tile or QK of the next, whichever is ready (PV first: it releases the
+    // stage and the P columns; QK only runs ahead).  A unit's first QK waits
+    // for its Q (rope and shared-memory columns by TMA, issued once the
+    // previous unit's QKs completed; tensor-memory columns from the softmax
+    // warps); its first PV waits until the previous unit's O has been read out.
     if (lane == 0) {
-      // rope columns of Q into shared memory; the q_nope columns (through the
-      // still idle stage buffers) for the softmax warps to move into TMEM
-      mbar_arrive_expect_tx(b_qsfull, C::QRBYTES + C::QS_CH * C::QCHUNK);
-      tma_load_2d(sbase + C::OFF_QR, &p.tm_qp, static_cast<int>(crank) * C::RH, row * p.H, b_qsfull);
-      for (int ch = C::QT_CH; ch < C::NPV; ++ch)
-        tma_load_2d(sbase + C::OFF_QS + (ch - C::QT_CH) * C::QCHUNK, &p.tm_qn,
-                    static_cast<int>(crank) * C::HALF + ch * 64, row * p.H, b_qsfull);
-      mbar_arrive_expect_tx(b_qtfull, C::QT_CH * C::QCHUNK);
-      for (int ch = 0; ch < C::QT_CH; ++ch)
-        tma_load_2d(sbase + C::OFF_QT + ch * C::QCHUNK, &p.tm_qn, static_cast<int>(crank) * C::HALF + ch * 64,
-                    row * p.H, b_qtfull);
-      bool ok = mbar_wait(b_qsfull, 0, abort_flag, p.err) && mbar_wait(b_qtdone, 0, abort_flag, p.err);
+      auto load_q = [&](int row) {
+        mbar_arrive_expect_tx(b_qsfull, C::QRBYTES + C::QS_CH * C::QCHUNK);
+        tma_load_2d(sbase + C::OFF_QR, &p.tm_qp, static_cast<int>(crank) * C::RH, row * p.H, b_qsfull);
+        for (int ch = C::QT_CH; ch < C::NPV; ++ch)
+          tma_load_2d(sbase + C::OFF_QS + (ch - C::QT_CH) * C::QCHUNK, &p.tm_qn,
+                      static_cast<int>(crank) * C::HALF + ch * 64, row * p.H, b_qsfull);
+      };
+      load_q(p.units[cl.u0].row);
       const uint32_t o_tmem = tmem_base + C::O_COL;
       // descriptors are built once; a K step of 16 columns adds 32 bytes (2
       // encoded), a stage adds STAGE / 16
@@ -277,30 +281,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
       const uint64_t krdesc0 = smem_desc(sbase + C::OFF_K + C::NPV * C::CHUNK, 16, 512, kSwizzle64);
       const uint64_t vdesc0 = smem_desc(sbase + C::OFF_K, C::CHUNK, 1024, kSwizzle128);
       constexpr uint64_t kStageStep = C::STAGE >> 4;
-      // issue PV of the oldest softmaxed tile or QK of the next tile, whichever
-      // is ready, PV first: it releases the stage and the P columns, while QK
-      // only runs ahead
-      int nq = 0, np = 0;
+      int nq = 0, np = 0;                                 // QKs / PVs issued, over the cluster's tiles
+      int uq = cl.u0, lq = 0, q_end = unit_tiles(p.units[cl.u0]);   // unit of the next QK, its index, its end
+      int lp = 0, p_start = 0, p_end = q_end;                       // the same for the next PV
+      int up = cl.u0;
+      bool q_ready = false, q_pending = false;   // Q of unit lq in place; a Q load waits for unit lq-1's QKs
+      bool ok = true;
       uint64_t idle_since = 0;
       uint32_t idle = 0;
-      while (ok && np < ntiles) {
+      while (ok && np < ntotal) {
         bool progressed = false;
-        if (np < nq && mbar_test(pfull(np & 1), (np >> 1) & 1)) {
+        if (np < nq && mbar_test(pfull(np & 1), (np >> 1) & 1) &&
+            (np != p_start || lp == 0 || mbar_test(b_ofree, (lp - 1) & 1))) {
           tc_fence_after();
           const int st = np % NS;
           const uint32_t p_tmem = tmem_base + C::P_COL;
 #pragma unroll
           for (int k = 0; k < T / 16; ++k)
             mma_f16_ts(o_tmem, p_tmem + k * 8, vdesc0 + st * kStageStep + (k * 16 * 128 >> 4), C::IDESC_PV,
-                       (np > 0 || k > 0) ? 1u : 0u);
+                       (np > p_start || k > 0) ? 1u : 0u);
           mma_commit(b_pvdone);
           mma_commit(kempty(st));
           ++np;
+          if (np == p_end && np < ntotal) {
+            ++up;
+            ++lp;
+            p_start = np;
+            p_end = np + unit_tiles(p.units[up]);
+          }
           progressed = true;
         }
-        if (nq < ntiles) {
+        if (q_pending && mbar_test(b_qkdone, (lq - 1) & 1)) {
+          load_q(p.units[uq].row);   // the previous unit's QKs have read the old Q
+          q_pending = false;
+          progressed = true;
+        }
+        if (nq < ntotal) {
+          if (!q_ready && !q_pending) q_ready = mbar_test(b_qsfull, lq & 1) && mbar_test(b_qtdone, lq & 1);
           const int st = nq % NS, sb = nq & 1;
-          if (mbar_test(kfull(st), (nq / NS) & 1) && mbar_test(sempty(sb), ((nq >> 1) & 1) ^ 1)) {
+          if (q_ready && mbar_test(kfull(st), (nq / NS) & 1) && mbar_test(sempty(sb), ((nq >> 1) & 1) ^ 1)) {
             fence_proxy_async_smem();   // the gathered tile feeds the tensor core
             tc_fence_after();
             const uint32_t s_tmem = tmem_base + C::S_COL + sb * T;
@@ -322,6 +341,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
               mma_f16_ss(s_tmem, qrdesc + 2 * k, krd + 2 * k, C::IDESC_QK, 1u);
             mma_commit(sfull(sb));
             ++nq;
+            if (nq == q_end) {
+              mma_commit(b_qkdone);   // the unit's QKs are issued: its Q may be replaced once they complete
+              if (nq < ntotal) {
+                ++uq;
+                ++lq;
+                q_end = nq + unit_tiles(p.units[uq]);
+                q_ready = false;
+                q_pending = true;
+              }
+            }
             progressed = true;
           }
         }
@@ -346,120 +375,133 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
     __syncwarp();
   } else if (warp < kSoftWarp0) {
     // ------------------------------------------------------------ producers
-    // Warps 1-2 resolve the tile's rows (key = 32 * (warp - 1) + lane); the
-    // selection entries of tile t+2 and the page ids of tile t+1 are loaded
-    // while tile t is issued.
+    // Warps 1-2 resolve a tile's rows (key = 32 * (warp - 1) + lane); the
+    // selection entries of tile t+2 and the page ids of tile t+1 of the unit
+    // are loaded while tile t is issued.  The stage ring runs on over the
+    // cluster's tiles, so the next unit's gathers start while the current
+    // unit finishes.
     const int pt = threadIdx.x - 32 * kProdWarp0;  // 0..223
-    const int page_off = p.row_page_off[row], npages = p.row_npages[row], page_start = p.row_page_start[row];
     const bool resolver = warp < kProdWarp0 + 2;
     const int rkey = (warp - kProdWarp0) * 32 + lane;
-    auto sel_at = [&](int t) -> int {
-      const int e = t * T + rkey;
-      return (resolver && t < ntiles && e < nent) ? selrow[e] : -1;
-    };
-    auto page_of = [&](int j) -> int {
-      if (j < 0 || j > pos) return -1;
-      const int64_t pi = (static_cast<int64_t>(page_start) + j) / p.P;
-      return pi < npages ? p.pages[page_off + pi] : -1;
-    };
-    auto phys = [&](int j, int pg) -> int32_t {   // -1: masked (zero-filled, its P is 0)
-      if (j == -1) return -1;
-      if (j < -1 || j > pos || pg < 0 || pg >= p.num_pages) {
-        atomicOr(p.err, kErrBounds);
-        return -1;
-      }
-      const int64_t slot = static_cast<int64_t>(page_start) + j;
-      return static_cast<int32_t>(static_cast<int64_t>(pg) * p.P + slot % p.P);
-    };
-    int j0 = sel_at(0), j1 = sel_at(1);
-    int pg0 = page_of(j0);
-    // Stage buffers QT_STAGE.. hold the q_nope columns of Q until the softmax
-    // warps have moved them into TMEM; the tiles before gather at once.
     // Every exit from the tile loop is decided at the named barrier (an OR
     // over the producers), so no producer is left waiting there alone.
-    bool ok = true;
-    for (int t = 0; t < ntiles; ++t) {
-      const int st = t % NS;
-      const int pg1 = page_of(j1);
-      const int j2 = sel_at(t + 2);
-      if (t == C::QT_STAGE && ok) ok = mbar_wait(b_qtdone, 0, abort_flag, p.err);
-      if (!FP8 && ok) ok = mbar_wait(kempty(st), ((t / NS) & 1) ^ 1, abort_flag, p.err);
-      int32_t *rows = rows_sm + st * T;
-      if (resolver && ok) rows[rkey] = phys(j0, pg0);
-      if (named_bar_any(2, kProdThreads, !ok)) break;
-      const uint32_t kst = sbase + C::OFF_K + st * C::STAGE;
-      if constexpr (!FP8) {
-        constexpr int ROWB = (L + R) * 2;
-        // piece q of a key: this CTA's q_nope columns, then its rope columns
-        for (int idx = pt; idx < T * C::PIECES; idx += kProdThreads) {
-          const int key = idx / C::PIECES, piece = idx - key * C::PIECES;
-          const int32_t prow = rows[key];
-          uint32_t dst;
-          int off;
-          if (piece < C::NPV * 8) {
-            dst = kst + (piece >> 3) * C::CHUNK + sw128_offset(key, piece & 7);
-            off = static_cast<int>(crank) * C::HALF * 2 + piece * 16;
-          } else {
-            dst = kst + C::NPV * C::CHUNK + sw64_offset(key, piece - C::NPV * 8);
-            off = L * 2 + static_cast<int>(crank) * C::RH * 2 + (piece - C::NPV * 8) * 16;
-          }
-          const uint8_t *src = p.latent + (prow >= 0 ? static_cast<int64_t>(prow) * ROWB + off : 0);
-          cp_async_16_zfill(dst, src, prow >= 0 ? 16u : 0u);
+    // (`ok` is this thread's; `stop` is decided at the barrier, the same in
+    // every producer, and alone ends the unit loop)
+    bool ok = true, stop = false;
+    int g = 0;   // the cluster's tile counter
+    for (int ui = cl.u0; ui < cl.u1 && !stop; ++ui) {
+      const AttUnit unit = p.units[ui];
+      const int row = unit.row;
+      const int pos = p.row_pos[row];
+      const int nent = unit.k1 - unit.k0;
+      const int ntiles = (nent + T - 1) / T;
+      const int32_t *selrow = p.sel + static_cast<int64_t>(row) * p.K + unit.k0;
+      const int page_off = p.row_page_off[row], npages = p.row_npages[row], page_start = p.row_page_start[row];
+      auto sel_at = [&](int t) -> int {
+        const int e = t * T + rkey;
+        return (resolver && t < ntiles && e < nent) ? selrow[e] : -1;
+      };
+      auto page_of = [&](int j) -> int {
+        if (j < 0 || j > pos) return -1;
+        const int64_t pi = (static_cast<int64_t>(page_start) + j) / p.P;
+        return pi < npages ? p.pages[page_off + pi] : -1;
+      };
+      auto phys = [&](int j, int pg) -> int32_t {   // -1: masked (zero-filled, its P is 0)
+        if (j == -1) return -1;
+        if (j < -1 || j > pos || pg < 0 || pg >= p.num_pages) {
+          atomicOr(p.err, kErrBounds);
+          return -1;
         }
-        cp_async_mbar_arrive(kfull(st));
-      } else {
-        // 656-byte rows [L e4m3 | L/128 fp32 scales | R bf16]: this CTA's
-        // codes (HALF/16 pieces) and rope half (4 pieces) are loaded into
-        // registers before the stage is known to be free, dequantised (code x
-        // scale, rounded to bf16) and stored as the bf16 tile.
-        constexpr int CPH = C::HALF / 16, RP = 4, PPK = CPH + RP;
-        constexpr int RB8 = L + 4 * (L / 128) + 2 * R;
-        constexpr int PER = (T * PPK + kProdThreads - 1) / kProdThreads;
-        uint4 raw[PER];
-        float scl[PER];
-#pragma unroll
-        for (int u = 0; u < PER; ++u) {
-          const int i = pt + u * kProdThreads;
-          raw[u] = make_uint4(0, 0, 0, 0);
-          scl[u] = 0.f;
-          if (i < T * PPK) {
-            const int key = i / PPK, k = i - key * PPK;
+        const int64_t slot = static_cast<int64_t>(page_start) + j;
+        return static_cast<int32_t>(static_cast<int64_t>(pg) * p.P + slot % p.P);
+      };
+      int j0 = sel_at(0), j1 = sel_at(1);
+      int pg0 = page_of(j0);
+      for (int t = 0; t < ntiles; ++t, ++g) {
+        const int st = g % NS;
+        const int pg1 = page_of(j1);
+        const int j2 = sel_at(t + 2);
+        if (!FP8 && ok) ok = mbar_wait(kempty(st), ((g / NS) & 1) ^ 1, abort_flag, p.err);
+        int32_t *rows = rows_sm + st * T;
+        if (resolver && ok) rows[rkey] = phys(j0, pg0);
+        if (named_bar_any(2, kProdThreads, !ok)) {
+          stop = true;
+          break;
+        }
+        const uint32_t kst = sbase + C::OFF_K + st * C::STAGE;
+        if constexpr (!FP8) {
+          constexpr int ROWB = (L + R) * 2;
+          // piece q of a key: this CTA's q_nope columns, then its rope columns
+          for (int idx = pt; idx < T * C::PIECES; idx += kProdThreads) {
+            const int key = idx / C::PIECES, piece = idx - key * C::PIECES;
             const int32_t prow = rows[key];
-            if (prow >= 0) {
-              const uint8_t *base = p.latent + static_cast<int64_t>(prow) * RB8;
-              if (k < CPH) {
-                raw[u] = __ldg(reinterpret_cast<const uint4 *>(base + static_cast<int>(crank) * C::HALF + 16 * k));
-                scl[u] = __ldg(reinterpret_cast<const float *>(base + L) + (static_cast<int>(crank) * C::HALF) / 128 +
-                               k / 8);
-              } else {
-                raw[u] = __ldg(reinterpret_cast<const uint4 *>(base + L + 4 * (L / 128) +
-                                                               static_cast<int>(crank) * C::RH * 2 + 16 * (k - CPH)));
+            uint32_t dst;
+            int off;
+            if (piece < C::NPV * 8) {
+              dst = kst + (piece >> 3) * C::CHUNK + sw128_offset(key, piece & 7);
+              off = static_cast<int>(crank) * C::HALF * 2 + piece * 16;
+            } else {
+              dst = kst + C::NPV * C::CHUNK + sw64_offset(key, piece - C::NPV * 8);
+              off = L * 2 + static_cast<int>(crank) * C::RH * 2 + (piece - C::NPV * 8) * 16;
+            }
+            const uint8_t *src = p.latent + (prow >= 0 ? static_cast<int64_t>(prow) * ROWB + off : 0);
+            cp_async_16_zfill(dst, src, prow >= 0 ? 16u : 0u);
+          }
+          cp_async_mbar_arrive(kfull(st));
+        } else {
+          // 656-byte rows [L e4m3 | L/128 fp32 scales | R bf16]: this CTA's
+          // codes (HALF/16 pieces) and rope half (4 pieces) are loaded into
+          // registers before the stage is known to be free, dequantised (code x
+          // scale, rounded to bf16) and stored as the bf16 tile.
+          constexpr int CPH = C::HALF / 16, RP = 4, PPK = CPH + RP;
+          constexpr int RB8 = L + 4 * (L / 128) + 2 * R;
+          constexpr int PER = (T * PPK + kProdThreads - 1) / kProdThreads;
+          uint4 raw[PER];
+          float scl[PER];
+#pragma unroll
+          for (int u = 0; u < PER; ++u) {
+            const int i = pt + u * kProdThreads;
+            raw[u] = make_uint4(0, 0, 0, 0);
+            scl[u] = 0.f;
+            if (i < T * PPK) {
+              const int key = i / PPK, k = i - key * PPK;
+              const int32_t prow = rows[key];
+              if (prow >= 0) {
+                const uint8_t *base = p.latent + static_cast<int64_t>(prow) * RB8;
+                if (k < CPH) {
+                  raw[u] = __ldg(reinterpret_cast<const uint4 *>(base + static_cast<int>(crank) * C::HALF + 16 * k));
+                  scl[u] = __ldg(reinterpret_cast<const float *>(base + L) + (static_cast<int>(crank) * C::HALF) / 128 +
+                                 k / 8);
+                } else {
+                  raw[u] = __ldg(reinterpret_cast<const uint4 *>(base + L + 4 * (L / 128) +
+                                                                 static_cast<int>(crank) * C::RH * 2 + 16 * (k - CPH)));
+                }
               }
             }
           }
-        }
-        ok = mbar_wait(kempty(st), ((t / NS) & 1) ^ 1, abort_flag, p.err);
+          ok = mbar_wait(kempty(st), ((g / NS) & 1) ^ 1, abort_flag, p.err);
 #pragma unroll
-        for (int u = 0; u < PER; ++u) {
-          const int i = pt + u * kProdThreads;
-          if (!ok || i >= T * PPK) continue;
-          const int key = i / PPK, k = i - key * PPK;
-          if (k < CPH) {
-            uint4 lo, hi;
-            e4m3x16_to_bf16(raw[u], scl[u], lo, hi);
-            const uint32_t chunk = kst + (k / 4) * C::CHUNK;
-            st_shared_v4(chunk + sw128_offset(key, (k % 4) * 2), lo);
-            st_shared_v4(chunk + sw128_offset(key, (k % 4) * 2 + 1), hi);
-          } else {
-            st_shared_v4(kst + C::NPV * C::CHUNK + sw64_offset(key, k - CPH), raw[u]);
+          for (int u = 0; u < PER; ++u) {
+            const int i = pt + u * kProdThreads;
+            if (!ok || i >= T * PPK) continue;
+            const int key = i / PPK, k = i - key * PPK;
+            if (k < CPH) {
+              uint4 lo, hi;
+              e4m3x16_to_bf16(raw[u], scl[u], lo, hi);
+              const uint32_t chunk = kst + (k / 4) * C::CHUNK;
+              st_shared_v4(chunk + sw128_offset(key, (k % 4) * 2), lo);
+              st_shared_v4(chunk + sw128_offset(key, (k % 4) * 2 + 1), hi);
+            } else {
+              st_shared_v4(kst + C::NPV * C::CHUNK + sw64_offset(key, k - CPH), raw[u]);
+            }
           }
+          fence_proxy_async_smem();
+          if (ok) mbar_arrive(kfull(st));
         }
-        fence_proxy_async_smem();
-        if (ok) mbar_arrive(kfull(st));
+        j0 = j1;
+        j1 = j2;
+        pg0 = pg1;
       }
-      j0 = j1;
-      j1 = j2;
-      pg0 = pg1;
     }
     cp_async_wait<0>();   // nothing in flight when the CTA leaves
   } else if (warp >= kSendWarp0) {
@@ -471,14 +513,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
     // once all four partner softmax warps have merged that half of tile u-1
     // (a bulk copy lands ~1 us sooner than the same bytes sent by st.async
     // from registers).  The S tile is released (sempty) once its values are
-    // in registers.
+    // in registers.  Tiles are counted over the cluster's units.
     const int quad = warp & 3;
     const int h = quad * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t slot = sbase + C::OFF_X + C::XBYTES + quad * (C::XOUT / 4);
     const uint32_t dst0 = map_to_cta(sbase + C::OFF_X, peer) + static_cast<uint32_t>(quad * 32) * 128;
     bool ok = true;
-    for (int u = 0; u < ntiles && ok; ++u) {
+    for (int u = 0; u < ntotal && ok; ++u) {
       const int b = u & 1;
       const uint32_t use = static_cast<uint32_t>(u >> 1);
       // warp-uniform, as the TMEM loads below are warp-collective
@@ -526,26 +568,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
     // of every tile (the half of x_in the partner sends for them) and output
     // columns [hf, hf+1) * HALF/2.  The pair shares each tile's maximum
     // through shared memory, so both take the same reference max, and adds
-    // its row sums at the end; every exit from the tile loop is decided at
-    // the pair's barrier (an OR of their failures).
+    // its row sums at the end of each unit; every exit from the tile loop is
+    // decided at the pair's barrier (an OR of their failures).  Per unit: the
+    // unit's tiles, then (once its last S has been read, so every QK of the
+    // unit has completed) the next unit's q_nope columns from global memory
+    // into tensor memory, then this unit's O read out and written.
     const int quad = warp & 3;
     const int hf = (warp - kSoftWarp0) >> 2;
     const int h = quad * 32 + lane;                      // head = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t pair_bar = 3 + quad;
-    float *red = reinterpret_cast<float *>(smem + C::OFF_RED);   // [t&1][hf][h] maxima, then [hf][h] sums
-    bool ok = __all_sync(0xffffffffu, mbar_wait(b_qtfull, 0, abort_flag, p.err));
-    if (ok) {
-      // this head's row of the q_nope columns: from the staged swizzled
-      // chunks into TMEM (bf16 pairs, lower column in the low half); the
-      // pair's warps take alternate chunks
+    float *red = reinterpret_cast<float *>(smem + C::OFF_RED);   // [t&1][hf][h] maxima, then [unit&1][hf][h] sums
+    // this head's row of the tensor-memory q_nope columns (bf16 pairs, lower
+    // column in the low half); the pair's warps take alternate chunks
+    auto move_q = [&](int row) {
+      const bool in = h < p.H;
 #pragma unroll 1
       for (int ch = hf; ch < C::QT_CH; ch += 2) {
-        const uint8_t *src = smem + C::OFF_QT + ch * C::QCHUNK + h * 128;
+        const uint4 *src = reinterpret_cast<const uint4 *>(
+            p.qn + (static_cast<int64_t>(row) * p.H + (in ? h : 0)) * L + static_cast<int>(crank) * C::HALF + ch * 64);
         uint32_t v[32];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const uint4 x = *reinterpret_cast<const uint4 *>(src + ((i ^ (h & 7)) << 4));
+          const uint4 x = in ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
           v[4 * i] = x.x;
           v[4 * i + 1] = x.y;
           v[4 * i + 2] = x.z;
@@ -554,187 +599,202 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
         tmem_st32(tmem_base + lane_base + ch * 32, v);
       }
       tmem_st_wait();
-    }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(b_qtdone);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_qtdone);
+    };
     constexpr int TH = T / 2;                            // keys of a tile per warp
-    float m_ref = kNegBig, l = 0.f;
-    int jn = hf * TH + lane < nent ? selrow[hf * TH + lane] : -1;
-    for (int t = 0; t < ntiles; ++t) {
-      const uint32_t vmask = __ballot_sync(0xffffffffu, jn >= 0 && jn <= pos);
-      if (t + 1 < ntiles) {
-        const int e = (t + 1) * T + hf * TH + lane;
-        jn = e < nent ? selrow[e] : -1;
-      }
-      const int sb = t & 1;
-      const uint32_t use = static_cast<uint32_t>(t >> 1);
-      if (h == 0) mbar_arrive_expect_tx(xfull(hf), C::XHALF);
-      bool good = ok && __all_sync(0xffffffffu, mbar_wait(sfull(sb), use & 1, abort_flag, p.err));
-      tc_fence_after();
-      float s[TH];
-      if (good) {
-#pragma unroll
-        for (int c0 = 0; c0 < TH; c0 += 16)
-          tmem_ld16(tmem_base + lane_base + C::S_COL + sb * T + hf * TH + c0,
-                    *reinterpret_cast<float(*)[16]>(s + c0));
-        tmem_ld_wait();
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (good && lane == 0) mbar_arrive(sempty(sb));   // our partial is in registers: the S tile can take QK of tile t+2
-      // full logits of this warp's keys: our partial + the partner's (x_in half hf)
-      good = good && __all_sync(0xffffffffu,
-                                mbar_wait<true>(xfull(hf), static_cast<uint32_t>(t) & 1, abort_flag, p.err));
-      float lmax = -INFINITY;
-      if (good) {
-        const float4 *xr = reinterpret_cast<const float4 *>(smem + C::OFF_X + hf * C::XHALF + h * 128);
-#pragma unroll
-        for (int c = 0; c < TH / 4; ++c) {
-          const float4 v = xr[c ^ (h & 7)];
-          // a + b == b + a in IEEE arithmetic: both CTAs get the same S
-          s[4 * c] += v.x;
-          s[4 * c + 1] += v.y;
-          s[4 * c + 2] += v.z;
-          s[4 * c + 3] += v.w;
+    move_q(p.units[cl.u0].row);
+    bool ok = true;
+    int g = 0;   // the cluster's tile counter
+    for (int ui = cl.u0, lu = 0; ui < cl.u1 && ok; ++ui, ++lu) {
+      const AttUnit unit = p.units[ui];
+      const int row = unit.row;
+      const int pos = p.row_pos[row];
+      const int nent = unit.k1 - unit.k0;
+      const int ntiles = (nent + T - 1) / T;
+      const int32_t *selrow = p.sel + static_cast<int64_t>(row) * p.K + unit.k0;
+      float m_ref = kNegBig, l = 0.f;
+      int jn = hf * TH + lane < nent ? selrow[hf * TH + lane] : -1;
+      for (int t = 0; t < ntiles; ++t, ++g) {
+        const uint32_t vmask = __ballot_sync(0xffffffffu, jn >= 0 && jn <= pos);
+        if (t + 1 < ntiles) {
+          const int e = (t + 1) * T + hf * TH + lane;
+          jn = e < nent ? selrow[e] : -1;
         }
-        // (scale_log2 > 0, so the max of the raw logits picks the same key)
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int i = 0; i < TH; ++i) {
-          s[i] = ((vmask >> i) & 1u) ? s[i] : -INFINITY;
-          mx[i & 3] = fmaxf(mx[i & 3], s[i]);
-        }
-        lmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      }
-      // this warp's rows of its x_in half have been read (a release arrive
-      // here costs more than it saves)
-      __syncwarp();
-      if (good && lane == 0) mbar_arrive_remote_relaxed(map_to_cta(xfree(hf), peer));
-      red[(sb * 2 + hf) * 128 + h] = lmax;
-      if (named_bar_any(pair_bar, 64, !good)) {   // both halves' maxima are in place
-        ok = false;
-        break;
-      }
-      // online softmax in base 2 with a lazily moved reference max
-      const float tmax = fmaxf(red[(sb * 2) * 128 + h], red[(sb * 2 + 1) * 128 + h]) * p.scale_log2;
-      float alpha = 1.f;
-      const bool rescale = tmax > m_ref + kRescaleThreshold;
-      if (rescale) {
-        alpha = fast_exp2(m_ref - tmax);
-        m_ref = tmax;
-      }
-      // P (bf16 pairs, lower key in the low half) for this warp's keys
-      float sm[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t packed[TH / 2];
-#pragma unroll
-      for (int i = 0; i < TH; i += 2) {
-        const __nv_bfloat162 pb = __floats2bfloat162_rn(fast_exp2(fmaf(s[i], p.scale_log2, -m_ref)),
-                                                        fast_exp2(fmaf(s[i + 1], p.scale_log2, -m_ref)));
-        const float2 pf = __bfloat1622float2(pb);
-        sm[(i >> 1) & 3] += pf.x + pf.y;
-        packed[i / 2] = *reinterpret_cast<const uint32_t *>(&pb);
-      }
-      l = l * alpha + ((sm[0] + sm[1]) + (sm[2] + sm[3]));
-      // PV of tile t-1 must be done before P is overwritten and before O is
-      // rescaled (PV of t-2 finished before PV of t-1 was issued); a failure
-      // here is seen at the next pair barrier
-      if (t > 0) {
-        good = __all_sync(0xffffffffu, mbar_wait(b_pvdone, (t - 1) & 1, abort_flag, p.err));
+        const int sb = g & 1;
+        const uint32_t use = static_cast<uint32_t>(g >> 1);
+        if (h == 0) mbar_arrive_expect_tx(xfull(hf), C::XHALF);
+        bool good = ok && __all_sync(0xffffffffu, mbar_wait(sfull(sb), use & 1, abort_flag, p.err));
         tc_fence_after();
-      }
-      // the O loads and stores are warp-collective: the warp rescales when any
-      // of its heads needs it (alpha is exactly 1 for the others)
-      if (good && t > 0 && __any_sync(0xffffffffu, rescale)) {
-#pragma unroll 1
-        for (int c0 = 0; c0 < C::HALF / 2; c0 += 16) {
-          float o[16];
-          tmem_ld16(tmem_base + lane_base + C::O_COL + hf * (C::HALF / 2) + c0, o);
-          tmem_ld_wait();
+        float s[TH];
+        if (good) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) o[i] *= alpha;
-          tmem_st16(tmem_base + lane_base + C::O_COL + hf * (C::HALF / 2) + c0, o);
+          for (int c0 = 0; c0 < TH; c0 += 16)
+            tmem_ld16(tmem_base + lane_base + C::S_COL + sb * T + hf * TH + c0,
+                      *reinterpret_cast<float(*)[16]>(s + c0));
+          tmem_ld_wait();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (good && lane == 0) mbar_arrive(sempty(sb));   // our partial is in registers: the S tile can take QK of tile g+2
+        // full logits of this warp's keys: our partial + the partner's (x_in half hf)
+        good = good && __all_sync(0xffffffffu,
+                                  mbar_wait<true>(xfull(hf), static_cast<uint32_t>(g) & 1, abort_flag, p.err));
+        float lmax = -INFINITY;
+        if (good) {
+          const float4 *xr = reinterpret_cast<const float4 *>(smem + C::OFF_X + hf * C::XHALF + h * 128);
+#pragma unroll
+          for (int c = 0; c < TH / 4; ++c) {
+            const float4 v = xr[c ^ (h & 7)];
+            // a + b == b + a in IEEE arithmetic: both CTAs get the same S
+            s[4 * c] += v.x;
+            s[4 * c + 1] += v.y;
+            s[4 * c + 2] += v.z;
+            s[4 * c + 3] += v.w;
+          }
+          // (scale_log2 > 0, so the max of the raw logits picks the same key)
+          float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int i = 0; i < TH; ++i) {
+            s[i] = ((vmask >> i) & 1u) ? s[i] : -INFINITY;
+            mx[i & 3] = fmaxf(mx[i & 3], s[i]);
+          }
+          lmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        }
+        // this warp's rows of its x_in half have been read (a release arrive
+        // here costs more than it saves)
+        __syncwarp();
+        if (good && lane == 0) mbar_arrive_remote_relaxed(map_to_cta(xfree(hf), peer));
+        red[(sb * 2 + hf) * 128 + h] = lmax;
+        if (named_bar_any(pair_bar, 64, !good)) {   // both halves' maxima are in place
+          ok = false;
+          break;
+        }
+        // online softmax in base 2 with a lazily moved reference max
+        const float tmax = fmaxf(red[(sb * 2) * 128 + h], red[(sb * 2 + 1) * 128 + h]) * p.scale_log2;
+        float alpha = 1.f;
+        const bool rescale = tmax > m_ref + kRescaleThreshold;
+        if (rescale) {
+          alpha = fast_exp2(m_ref - tmax);
+          m_ref = tmax;
+        }
+        // P (bf16 pairs, lower key in the low half) for this warp's keys
+        float sm[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t packed[TH / 2];
+#pragma unroll
+        for (int i = 0; i < TH; i += 2) {
+          const __nv_bfloat162 pb = __floats2bfloat162_rn(fast_exp2(fmaf(s[i], p.scale_log2, -m_ref)),
+                                                          fast_exp2(fmaf(s[i + 1], p.scale_log2, -m_ref)));
+          const float2 pf = __bfloat1622float2(pb);
+          sm[(i >> 1) & 3] += pf.x + pf.y;
+          packed[i / 2] = *reinterpret_cast<const uint32_t *>(&pb);
+        }
+        l = l * alpha + ((sm[0] + sm[1]) + (sm[2] + sm[3]));
+        // PV of tile g-1 (of this unit or the one before) must be done before
+        // P is overwritten, and before O is rescaled (PV of g-2 finished
+        // before PV of g-1 was issued); a failure here is seen at the next
+        // pair barrier
+        if (g > 0) {
+          good = __all_sync(0xffffffffu, mbar_wait(b_pvdone, (g - 1) & 1, abort_flag, p.err));
+          tc_fence_after();
+        }
+        // the O loads and stores are warp-collective: the warp rescales when
+        // any of its heads needs it (alpha is exactly 1 for the others); the
+        // unit's first tile has no O yet
+        if (good && t > 0 && __any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+          for (int c0 = 0; c0 < C::HALF / 2; c0 += 16) {
+            float o[16];
+            tmem_ld16(tmem_base + lane_base + C::O_COL + hf * (C::HALF / 2) + c0, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] *= alpha;
+            tmem_st16(tmem_base + lane_base + C::O_COL + hf * (C::HALF / 2) + c0, o);
+          }
+        }
+        if (good) {
+          tmem_st16(tmem_base + lane_base + C::P_COL + hf * (TH / 2), *reinterpret_cast<const float(*)[16]>(packed));
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (good && lane == 0) mbar_arrive(pfull(sb));
+        ok = good;
+      }
+      if (!ok) break;
+      // every QK of this unit has completed (its last S was read): the next
+      // unit's q_nope columns can replace this unit's in tensor memory
+      if (ui + 1 < cl.u1) move_q(p.units[ui + 1].row);
+      ok = __all_sync(0xffffffffu, mbar_wait(b_pvdone, (g - 1) & 1, abort_flag, p.err));   // this unit's last PV
+      tc_fence_after();
+      // the row sum is the two halves' sums (in a fixed order, the same in
+      // both CTAs); the sums alternate between two slots by unit.  The pair's
+      // barrier also makes `ok` the same in both warps, so they leave the
+      // unit loop together.
+      float *rsum = red + (4 + 2 * (lu & 1)) * 128;
+      rsum[hf * 128 + h] = l;
+      ok = !named_bar_any(pair_bar, 64, !ok);
+      l = rsum[h] + rsum[128 + h];
+      // (ok is warp-uniform and every lane takes its row out of TMEM, since the
+      // loads are warp-collective; only heads below H are stored)
+      const bool store = h < p.H;
+      if (ok) {
+        const int col0 = static_cast<int>(crank) * C::HALF + hf * (C::HALF / 2);
+        const uint32_t ocol = C::O_COL + hf * (C::HALF / 2);
+        if (unit.slot < 0) {
+          float f = 0.f;
+          if (p.sink && store) {
+            const float xs = p.sink[h] * kLog2e;
+            const float mf = fmaxf(m_ref, xs);
+            const float a = exp2f(m_ref - mf);
+            const float lf = l * a + exp2f(xs - mf);
+            f = lf > 0.f ? a / lf : 0.f;
+          } else {
+            f = l > 0.f ? 1.f / l : 0.f;
+          }
+          __nv_bfloat16 *dst = p.out + (static_cast<int64_t>(row) * p.H + h) * L + col0;
+#pragma unroll 1
+          for (int c0 = 0; c0 < C::HALF / 2; c0 += 16) {
+            float o[16];
+            __syncwarp();   // converged for the warp-collective load
+            tmem_ld16(tmem_base + lane_base + ocol + c0, o);
+            tmem_ld_wait();
+            if (!store) continue;
+            uint32_t w[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const __nv_bfloat162 b = __floats2bfloat162_rn(o[2 * i] * f, o[2 * i + 1] * f);
+              w[i] = *reinterpret_cast<const uint32_t *>(&b);
+            }
+            uint4 *d4 = reinterpret_cast<uint4 *>(dst + c0);
+            d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          }
+        } else {
+          float *dst = p.opart + (static_cast<int64_t>(unit.slot) * p.H + h) * L + col0;
+#pragma unroll 1
+          for (int c0 = 0; c0 < C::HALF / 2; c0 += 16) {
+            float o[16];
+            __syncwarp();   // converged for the warp-collective load
+            tmem_ld16(tmem_base + lane_base + ocol + c0, o);
+            tmem_ld_wait();
+            if (!store) continue;
+            float4 *d4 = reinterpret_cast<float4 *>(dst + c0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) d4[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+          }
+          if (crank == 0 && hf == 0 && store) {
+            float *ml = p.mlpart + (static_cast<int64_t>(unit.slot) * p.H + h) * 2;
+            ml[0] = m_ref;
+            ml[1] = l;
+          }
         }
       }
-      if (good) {
-        tmem_st16(tmem_base + lane_base + C::P_COL + hf * (TH / 2), *reinterpret_cast<const float(*)[16]>(packed));
-        tmem_st_wait();
-      }
+      // O is free for the next unit's first PV
       tc_fence_before();
       __syncwarp();
-      if (good && lane == 0) mbar_arrive(pfull(sb));
-      ok = good;
-    }
-    if (ok && ntiles > 0) ok = __all_sync(0xffffffffu, mbar_wait(b_pvdone, (ntiles - 1) & 1, abort_flag, p.err));
-    tc_fence_after();
-    // the row sum is the two halves' sums (in a fixed order, the same in both CTAs)
-    red[(4 + hf) * 128 + h] = l;
-    named_bar_sync(pair_bar, 64);
-    l = red[4 * 128 + h] + red[5 * 128 + h];
-    // (ok is warp-uniform and every lane takes its row out of TMEM, since the
-    // loads are warp-collective; only heads below H are stored)
-    const bool store = h < p.H;
-    if (ok) {
-      const int col0 = static_cast<int>(crank) * C::HALF + hf * (C::HALF / 2);
-      const uint32_t ocol = C::O_COL + hf * (C::HALF / 2);
-      if (unit.slot < 0) {
-        float f = 0.f;
-        if (p.sink && store) {
-          const float xs = p.sink[h] * kLog2e;
-          const float mf = fmaxf(m_ref, xs);
-          const float a = exp2f(m_ref - mf);
-          const float lf = l * a + exp2f(xs - mf);
-          f = lf > 0.f ? a / lf : 0.f;
-        } else {
-          f = l > 0.f ? 1.f / l : 0.f;
-        }
-        __nv_bfloat16 *dst = p.out + (static_cast<int64_t>(row) * p.H + h) * L + col0;
-#pragma unroll 1
-        for (int c0 = 0; c0 < C::HALF / 2; c0 += 16) {
-          float o[16];
-          __syncwarp();   // converged for the warp-collective load
-          if (ntiles > 0) {
-            tmem_ld16(tmem_base + lane_base + ocol + c0, o);
-            tmem_ld_wait();
-          } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) o[i] = 0.f;
-          }
-          if (!store) continue;
-          uint32_t w[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const __nv_bfloat162 b = __floats2bfloat162_rn(o[2 * i] * f, o[2 * i + 1] * f);
-            w[i] = *reinterpret_cast<const uint32_t *>(&b);
-          }
-          uint4 *d4 = reinterpret_cast<uint4 *>(dst + c0);
-          d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        }
-      } else {
-        float *dst = p.opart + (static_cast<int64_t>(unit.slot) * p.H + h) * L + col0;
-#pragma unroll 1
-        for (int c0 = 0; c0 < C::HALF / 2; c0 += 16) {
-          float o[16];
-          __syncwarp();   // converged for the warp-collective load
-          if (ntiles > 0) {
-            tmem_ld16(tmem_base + lane_base + ocol + c0, o);
-            tmem_ld_wait();
-          } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) o[i] = 0.f;
-          }
-          if (!store) continue;
-          float4 *d4 = reinterpret_cast<float4 *>(dst + c0);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) d4[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-        }
-        if (crank == 0 && hf == 0 && store) {
-          float *ml = p.mlpart + (static_cast<int64_t>(unit.slot) * p.H + h) * 2;
-          ml[0] = m_ref;
-          ml[1] = l;
-        }
-      }
+      if (lane == 0) mbar_arrive(b_ofree);
     }
   }
 
@@ -747,40 +807,65 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
 
 // ---------------------------------------------------------------------------
 // Merge of split rows: o = sum_s 2^(m_s - m) O_s / (sum_s 2^(m_s - m) l_s [+ 2^(sink - m)]).
-// One block per (row, head); threads over the latent columns.
+// A block takes kCombHeads heads of one merged row: one thread per head turns
+// the pieces' (m, l) into per-piece weights in shared memory, then the block
+// streams those heads' columns, four at a time (a float4 of each piece's
+// partial, then four bf16 out).
 // ---------------------------------------------------------------------------
-__device__ void combine_one(const AttCombine cb, int h, const float *__restrict__ opart,
-                            const float *__restrict__ mlpart, const float *__restrict__ sink, __nv_bfloat16 *out,
-                            int H, int L) {
-  if (cb.row < 0) return;   // padding of a capturable plan
-  float m = sink ? sink[h] * kLog2e : -INFINITY;
-  for (int s = 0; s < cb.nsplit; ++s) m = fmaxf(m, mlpart[((cb.first_slot + s) * static_cast<int64_t>(H) + h) * 2]);
-  float lsum = sink ? exp2f(sink[h] * kLog2e - m) : 0.f;
-  for (int s = 0; s < cb.nsplit; ++s) {
-    const float *ml = mlpart + ((cb.first_slot + s) * static_cast<int64_t>(H) + h) * 2;
-    lsum += exp2f(ml[0] - m) * ml[1];
-  }
-  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-  for (int d = threadIdx.x; d < L; d += blockDim.x) {
-    float acc = 0.f;
-    for (int s = 0; s < cb.nsplit; ++s) {
-      const int64_t base = (cb.first_slot + s) * static_cast<int64_t>(H) + h;
-      acc += exp2f(mlpart[base * 2] - m) * opart[base * L + d];
+constexpr int kCombHeads = 8;
+constexpr int kCombThreads = 256;
+
+__global__ void __launch_bounds__(kCombThreads) attend_combine_kernel(const AttCombine *__restrict__ combine,
+                                                                     const float *__restrict__ opart,
+                                                                     const float *__restrict__ mlpart,
+                                                                     const float *__restrict__ sink,
+                                                                     __nv_bfloat16 *out, int H, int L, int n_merge,
+                                                                     const int32_t *__restrict__ n_merge_dev) {
+  __shared__ float wsm[kCombHeads][kAttMaxPieces];
+  __shared__ float invl[kCombHeads];
+  // (merge, group of kCombHeads heads) pairs; a capturable plan's merge count is on the device
+  const int hb = (H + kCombHeads - 1) / kCombHeads;
+  const int n_work = (n_merge_dev ? *n_merge_dev : n_merge) * hb;
+  for (int w = blockIdx.x; w < n_work; w += gridDim.x) {
+    const AttCombine cb = combine[w / hb];
+    const int h0 = (w % hb) * kCombHeads;
+    if (cb.row < 0) continue;   // padding of a capturable plan (uniform over the block)
+    const int ns = cb.nsplit < kAttMaxPieces ? cb.nsplit : kAttMaxPieces;
+    __syncthreads();   // the previous item's weights have been used
+    if (threadIdx.x < kCombHeads && h0 + static_cast<int>(threadIdx.x) < H) {
+      const int h = h0 + threadIdx.x;
+      float m = sink ? sink[h] * kLog2e : -INFINITY;
+      for (int s = 0; s < ns; ++s) m = fmaxf(m, mlpart[((cb.first_slot + s) * static_cast<int64_t>(H) + h) * 2]);
+      float lsum = sink ? exp2f(sink[h] * kLog2e - m) : 0.f;
+      for (int s = 0; s < ns; ++s) {
+        const float *ml = mlpart + ((cb.first_slot + s) * static_cast<int64_t>(H) + h) * 2;
+        const float ws = exp2f(ml[0] - m);
+        wsm[threadIdx.x][s] = ws;
+        lsum += ws * ml[1];
+      }
+      invl[threadIdx.x] = lsum > 0.f ? 1.f / lsum : 0.f;
     }
-    out[(static_cast<int64_t>(cb.row) * H + h) * L + d] = __float2bfloat16_rn(acc * inv);
+    __syncthreads();
+    const int ngroups = kCombHeads * (L / 4);
+    for (int e = threadIdx.x; e < ngroups; e += kCombThreads) {
+      const int hh = e / (L / 4), d = (e - hh * (L / 4)) * 4;
+      const int h = h0 + hh;
+      if (h >= H) continue;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s = 0; s < ns; ++s) {
+        const float4 v = *reinterpret_cast<const float4 *>(opart + ((cb.first_slot + s) * static_cast<int64_t>(H) + h) * L + d);
+        const float ws = wsm[hh][s];
+        acc.x = fmaf(ws, v.x, acc.x);
+        acc.y = fmaf(ws, v.y, acc.y);
+        acc.z = fmaf(ws, v.z, acc.z);
+        acc.w = fmaf(ws, v.w, acc.w);
+      }
+      const float f = invl[hh];
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * f, acc.y * f), hi = __floats2bfloat162_rn(acc.z * f, acc.w * f);
+      *reinterpret_cast<uint2 *>(out + (static_cast<int64_t>(cb.row) * H + h) * L + d) =
+          make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
+    }
   }
-}
-
-
-__global__ void __launch_bounds__(128) attend_combine_kernel(const AttCombine *__restrict__ combine,
-                                                             const float *__restrict__ opart,
-                                                             const float *__restrict__ mlpart,
-                                                             const float *__restrict__ sink, __nv_bfloat16 *out,
-                                                             int H, int L, int n_merge,
-                                                             const int32_t *__restrict__ n_merge_dev) {
-  // (merge, head) pairs; a capturable plan's merge count is on the device
-  const int n_work = (n_merge_dev ? *n_merge_dev : n_merge) * H;
-  for (int w = blockIdx.x; w < n_work; w += gridDim.x) combine_one(combine[w / H], w % H, opart, mlpart, sink, out, H, L);
 }
 
 // ---------------------------------------------------------------------------
@@ -874,10 +959,12 @@ cudaError_t run_tc(const dsa_ctx *ctx, const dsa_plan_t *plan, const int32_t *se
   if (!encode_tiled_2d(&prm.tm_qp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void *>(q_pe), 64,
                        static_cast<uint64_t>(plan->T) * c.heads, 64 * 2, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
+  prm.qn = static_cast<const __nv_bfloat16 *>(q_nope);
   prm.sel = sel;
   prm.latent = static_cast<const uint8_t *>(latent);
   prm.sink = sink;
   prm.units = plan->units;
+  prm.clusters = plan->clusters;
   prm.row_pos = plan->row_pos;
   prm.row_page_off = plan->row_page_off;
   prm.row_npages = plan->row_npages;
@@ -895,7 +982,8 @@ cudaError_t run_tc(const dsa_ctx *ctx, const dsa_plan_t *plan, const int32_t *se
   auto kern = attend_tc_kernel<L, FP8>;
   static std::atomic<uint64_t> smem_limit_set{0};
   if (cudaError_t e = ensure_smem_limit(kern, Cfg::SMEM, ctx->device, smem_limit_set); e != cudaSuccess) return e;
-  kern<<<2 * plan->n_units, kAttThreads, Cfg::SMEM, s>>>(prm);
+  if (plan->n_clusters <= 0) return cudaSuccess;
+  kern<<<2 * plan->n_clusters, kAttThreads, Cfg::SMEM, s>>>(prm);
   return cudaGetLastError();
 }
 
@@ -926,11 +1014,12 @@ cudaError_t launch_attend(const dsa_ctx *ctx, const dsa_plan_t *plan, const int3
     if (plan->n_combine > 0) {
       // a capturable plan's merge count is known only on the device: a grid
       // that strides over its (merge, head) pairs
-      const int grid = plan->capturable ? std::min(plan->n_combine * c.heads, ctx->num_sms * 16)
-                                        : plan->n_combine * c.heads;
-      attend_combine_kernel<<<grid, 128, 0, s>>>(plan->combine, plan_opart(ctx, plan), plan_mlpart(ctx, plan), sink,
-                                                 static_cast<__nv_bfloat16 *>(out), c.heads, c.kv_lora_rank,
-                                                 plan->n_combine, plan->capturable ? plan->counts + 3 : nullptr);
+      const int hb = (c.heads + kCombHeads - 1) / kCombHeads;
+      const int grid = plan->capturable ? std::min(plan->n_combine * hb, ctx->num_sms * 8) : plan->n_combine * hb;
+      attend_combine_kernel<<<grid, kCombThreads, 0, s>>>(plan->combine, plan_opart(ctx, plan), plan_mlpart(ctx, plan),
+                                                          sink, static_cast<__nv_bfloat16 *>(out), c.heads,
+                                                          c.kv_lora_rank, plan->n_combine,
+                                                          plan->capturable ? plan->counts + 3 : nullptr);
       e = cudaGetLastError();
       if (e != cudaSuccess) return e;
       *launches += 1;

@@ -52,6 +52,15 @@ struct AttCombine {
   int32_t pad;
 };
 
+// The work of one persistent attention cluster: units [u0, u1), `tiles` key
+// tiles in all.  u0 == u1: an idle cluster (capturable plans' padding).
+struct AttCluster {
+  int32_t u0;
+  int32_t u1;
+  int32_t tiles;
+  int32_t pad;
+};
+
 constexpr int kIndexTile = 128;   // keys per indexer tile (UMMA M)
 constexpr int kAttTile = 64;      // keys per attention tile (UMMA N of QK)
 constexpr int kNoBox = -0x7fffffff - 1;   // index producers: a lane with no key box in the tile
@@ -96,12 +105,6 @@ __host__ __device__ inline int64_t index_tiles_per_item(int64_t tiles, int cap) 
   return t < 2 ? 2 : (t > 32 ? 32 : t);
 }
 
-// Key ranges per attention row for a step of T rows.  A row is one two-CTA
-// cluster and num_sms / 2 clusters run at a time; a row is split only when
-// that shortens waves x (a unit's fixed start-up, about ten tile periods, +
-// its tiles) plus the merge of the partials (about 0.15 tile periods per
-// row).  The host planner and the device planner share this function, so
-// both make the same units.
 // Order-preserving 32-bit key of a score (larger score, larger key; -0.0
 // ranks as +0.0).  Every score, -inf included, has a key above 0, so 0 can
 // stand for "no score".
@@ -123,31 +126,34 @@ __host__ __device__ inline int64_t block_key_base(int64_t score_off, int64_t row
   return score_off / block + row;
 }
 
-__host__ __device__ inline int attention_splits(int64_t T, int64_t topk, int num_sms) {
-  const int64_t pairs = num_sms / 2 > 1 ? num_sms / 2 : 1;
-  const int64_t full_tiles = (topk + kAttTile - 1) / kAttTile;
-  const int64_t sp_max = full_tiles / 2 > 1 ? full_tiles / 2 : 1;
-  int splits = 1;
-  if (T <= 0) return 1;
-  double best = 0.0;
-  for (int sp = 1; sp <= 16 && sp <= sp_max; ++sp) {
-    const int64_t waves = (T * sp + pairs - 1) / pairs;
-    const double est = static_cast<double>(waves) * (10.0 + static_cast<double>((full_tiles + sp - 1) / sp)) +
-                       (sp > 1 ? 0.15 * static_cast<double>(T) : 0.0);
-    if (sp == 1 || est < best) {
-      best = est;
-      splits = sp;
-    }
-  }
-  return splits;
+// Persistent attention schedule (the host planner and the device planner share
+// these functions, so both make the same units).  The step's rows, in order, are a sequence
+// of S key tiles (ceil(min(topk, pos+1) / kAttTile) per row).  It is cut
+// into n_clusters contiguous ranges of `per` tiles (the last one shorter), one
+// per two-CTA cluster; a row that a cut crosses becomes one unit per piece,
+// each writing a partial result that attend_combine_kernel merges.  Clusters
+// take at least kAttMinClusterTiles tiles, and there are at most one per two
+// SMs.
+constexpr int kAttMinClusterTiles = 16;
+// Ranges hold at least 8 tiles once S >= kAttMinClusterTiles (S / ceil(S / 16)),
+// so a row has at most ceil(tiles / 8) + 1 pieces: 33 at the largest topk
+// the library takes (16,384 keys, 256 tiles); the merge holds this many.
+constexpr int kAttMaxPieces = 64;
+
+__host__ __device__ inline void att_cluster_split(int64_t S, int num_sms, int32_t *n_clusters, int64_t *per) {
+  const int64_t cap = num_sms / 2 > 1 ? num_sms / 2 : 1;
+  int64_t n = (S + kAttMinClusterTiles - 1) / kAttMinClusterTiles;
+  n = n < 1 ? 1 : (n > cap ? cap : n);
+  int64_t q = (S + n - 1) / n;
+  if (q < 1) q = 1;
+  *per = q;
+  *n_clusters = static_cast<int32_t>(S > 0 ? (S + q - 1) / q : 0);
 }
 
-// Attention units of one row at position pos when rows split `splits` ways.
-__host__ __device__ inline int attention_row_units(int64_t pos, int64_t topk, int splits) {
+// Key tiles of a row at position pos (>= 0).
+__host__ __device__ inline int64_t att_row_tiles(int64_t pos, int64_t topk) {
   const int64_t nsel = pos + 1 < topk ? pos + 1 : topk;
-  const int64_t tiles = (nsel + kAttTile - 1) / kAttTile;
-  const int64_t sp = splits < tiles / 2 ? splits : tiles / 2;
-  return sp > 1 ? static_cast<int>(sp) : 1;
+  return (nsel + kAttTile - 1) / kAttTile;
 }
 
 // Indexer launch set: groups with the same row-group size.
@@ -195,6 +201,8 @@ struct dsa_plan {
   dsa::IdxSet idx[2];             // [0]: single-row groups, [1]: multi-row groups
   dsa::AttUnit *units = nullptr;
   int32_t n_units = 0, splits_max = 1;
+  dsa::AttCluster *clusters = nullptr;  // persistent attention clusters (the grid is two CTAs per entry)
+  int32_t n_clusters = 0;
   dsa::AttCombine *combine = nullptr;
   int32_t n_combine = 0, n_slots = 0;
   int32_t n_index_items = 0;
@@ -209,7 +217,6 @@ struct dsa_plan {
   int64_t page_ids = 0;                 // length of the page array of the last update
   float *own_scores = nullptr, *own_opart = nullptr, *own_mlpart = nullptr;
   int32_t *counts = nullptr;            // device [8], see dsa_plan_read_counts
-  int8_t *splits_by_rows = nullptr;     // device [T + 1]: the attention key split of a step of that many rows
 };
 
 namespace dsa {

@@ -44,7 +44,8 @@ struct PlanUpdateParams {
   int32_t *cta_begin;
   AttUnit *units;
   AttCombine *combine;
-  const int8_t *splits_by_rows;   // [max_rows + 1]: attention_splits(T, topk, num_sms)
+  AttCluster *clusters;           // [clusters_cap]
+  int32_t clusters_cap;
   int32_t *counts;
   int *err;
 };
@@ -176,21 +177,36 @@ __global__ void __launch_bounds__(kPlanThreads) plan_update_kernel(const PlanUpd
   int64_t sc = block_exclusive_scan(my_sc, &sc_total, sh);
   int64_t tile = block_exclusive_scan(my_tiles, &tiles_total, sh);
 
-  // ---- indexer items and attention units per row (the key split of a
-  // T-row step comes from the plan's table, made on the host with the host
-  // planner's own function)
+  // ---- indexer items and attention units per row.  The attention schedule
+  // cuts the rows' key tiles, in row order, into contiguous ranges, one per
+  // persistent cluster (att_cluster_split, the host planner's function); a
+  // row a cut crosses becomes one unit per piece, with partial slots and a
+  // merge.
   const int32_t tpi = static_cast<int32_t>(index_tiles_per_item(tiles_total, p.idx_cap));   // 2 .. 32
-  const int splits = p.splits_by_rows[T];
+  int64_t my_at = 0;
+#pragma unroll
+  for (int k = 0; k < kMaxRowsPerThread; ++k)
+    if (pos[k] >= 0) my_at += att_row_tiles(pos[k], p.topk);
+  int64_t at_total = 0;
+  const int64_t at_off0 = block_exclusive_scan(my_at, &at_total, sh);
+  int32_t ncl = 0;
+  int64_t per = 1;
+  att_cluster_split(at_total, p.num_sms, &ncl, &per);
   // counts packed two per scan: (items << 32 | units), (slots << 32 | merges)
   int64_t my_iu = 0, my_sm = 0;
+  {
+    int64_t off = at_off0;
 #pragma unroll
-  for (int k = 0; k < kMaxRowsPerThread; ++k) {
-    if (pos[k] < 0) continue;
-    const int32_t tiles = index_group_tiles(static_cast<int64_t>(pos[k]) + 1,
-                                            index_tile_lead(p.row_page_start[ra + k], p.box_rows));
-    const int u = attention_row_units(pos[k], p.topk, splits);
-    my_iu += (static_cast<int64_t>((tiles + tpi - 1) / tpi) << 32) + u;
-    my_sm += u > 1 ? ((static_cast<int64_t>(u) << 32) + 1) : 0;
+    for (int k = 0; k < kMaxRowsPerThread; ++k) {
+      if (pos[k] < 0) continue;
+      const int32_t tiles = index_group_tiles(static_cast<int64_t>(pos[k]) + 1,
+                                              index_tile_lead(p.row_page_start[ra + k], p.box_rows));
+      const int64_t n = att_row_tiles(pos[k], p.topk);
+      const int u = static_cast<int>((off + n - 1) / per - off / per + 1);
+      my_iu += (static_cast<int64_t>((tiles + tpi - 1) / tpi) << 32) + u;
+      my_sm += u > 1 ? ((static_cast<int64_t>(u) << 32) + 1) : 0;
+      off += n;
+    }
   }
   int64_t iu_total = 0, sm_total = 0;
   int64_t iu = block_exclusive_scan(my_iu, &iu_total, sh);
@@ -199,6 +215,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_update_kernel(const PlanUpd
   const int32_t n_slots = static_cast<int32_t>(sm_total >> 32), n_merge = static_cast<int32_t>(sm_total & 0xffffffff);
   // the plan's capacities bound these counts for every update the span checks
   // admit (see dsa_plan_capturable), so the writes below stay in bounds
+  int64_t at_off = at_off0;
 #pragma unroll
   for (int k = 0; k < kMaxRowsPerThread; ++k) {
     if (k >= rn) continue;
@@ -224,24 +241,25 @@ __global__ void __launch_bounds__(kPlanThreads) plan_update_kernel(const PlanUpd
     int32_t item = static_cast<int32_t>(iu >> 32);
     for (int32_t t0 = 0; t0 < tiles; t0 += tpi, ++item) p.items[item] = IdxItem{r, t0, min(tiles, t0 + tpi), 0};
     tile += tiles;
-    // attention: the whole row, or `u` key ranges with partial slots and a merge
+    // attention: one unit per piece of the row's tiles between cuts
     const int64_t nsel = min64(p.topk, static_cast<int64_t>(pos[k]) + 1);
-    const int64_t atiles = ceil_div(nsel, kAttTile);
-    const int u = attention_row_units(pos[k], p.topk, splits);
-    const int32_t unit = static_cast<int32_t>(iu & 0xffffffff);
-    if (u == 1) {
-      p.units[unit] = AttUnit{r, 0, static_cast<int32_t>(nsel), -1};
-    } else {
-      const int32_t slot = static_cast<int32_t>(smc >> 32);
-      p.combine[static_cast<int32_t>(smc & 0xffffffff)] = AttCombine{r, slot, u, 0};
-      for (int j = 0; j < u; ++j) {
-        const int64_t t0 = atiles * j / u, t1 = atiles * (j + 1) / u;
-        p.units[unit + j] = AttUnit{r, static_cast<int32_t>(t0 * kAttTile),
-                                    static_cast<int32_t>(min64(nsel, t1 * kAttTile)), slot + j};
-      }
-      smc += (static_cast<int64_t>(u) << 32) + 1;
+    const int64_t n = att_row_tiles(pos[k], p.topk);
+    const int64_t c0 = at_off / per, c1 = (at_off + n - 1) / per;
+    const int u = static_cast<int>(c1 - c0 + 1);
+    int32_t unit = static_cast<int32_t>(iu & 0xffffffff);
+    const int32_t slot = static_cast<int32_t>(smc >> 32);
+    if (u > 1) p.combine[static_cast<int32_t>(smc & 0xffffffff)] = AttCombine{r, slot, u, 0};
+    for (int64_t cl = c0; cl <= c1; ++cl, ++unit) {
+      const int64_t a = at_off > cl * per ? at_off : cl * per;
+      const int64_t b = at_off + n < (cl + 1) * per ? at_off + n : (cl + 1) * per;
+      if (a == cl * per) p.clusters[cl].u0 = unit;   // the cluster's first unit
+      p.units[unit] = AttUnit{r, static_cast<int32_t>((a - at_off) * kAttTile),
+                              static_cast<int32_t>(min64(nsel, (b - at_off) * kAttTile)),
+                              u > 1 ? slot + static_cast<int32_t>(cl - c0) : -1};
     }
+    if (u > 1) smc += (static_cast<int64_t>(u) << 32) + 1;
     iu += (static_cast<int64_t>((tiles + tpi - 1) / tpi) << 32) + u;
+    at_off += n;
   }
   if (tid == 0) {
     r_tile0[p.max_rows] = tiles_total;
@@ -250,7 +268,19 @@ __global__ void __launch_bounds__(kPlanThreads) plan_update_kernel(const PlanUpd
   // padding: units and merges past the step's counts exit at once
   for (int i = n_units + tid; i < p.units_cap; i += kPlanThreads) p.units[i] = AttUnit{-1, 0, 0, -1};
   for (int i = n_merge + tid; i < p.combine_cap; i += kPlanThreads) p.combine[i] = AttCombine{-1, 0, 0, 0};
-  __syncthreads();
+  __syncthreads();   // every cluster's first unit is written
+  // each cluster's unit range and tiles (thread = cluster; clusters_cap <=
+  // kPlanThreads); clusters past the schedule are idle
+  {
+    AttCluster e{0, 0, 0, 0};
+    if (tid < ncl) {
+      e.u0 = p.clusters[tid].u0;
+      e.u1 = tid + 1 < ncl ? p.clusters[tid + 1].u0 : n_units;
+      e.tiles = static_cast<int32_t>(min64(per, at_total - static_cast<int64_t>(tid) * per));
+    }
+    __syncthreads();   // every u0 is read before any entry is rewritten
+    if (tid < p.clusters_cap) p.clusters[tid] = e;
+  }
 
   // ---- per-CTA item ranges of the persistent indexer: CTA b starts at the
   // first item that begins at or after tile tiles_total * b / idx_cap.  Item
@@ -281,7 +311,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_update_kernel(const PlanUpd
     p.counts[3] = n_merge;
     p.counts[4] = n_slots;
     p.counts[5] = ok ? 1 : 0;
-    p.counts[6] = splits;
+    p.counts[6] = ncl;
     p.counts[7] = static_cast<int32_t>(min64(sc_total, INT32_MAX));
   }
 }
@@ -320,7 +350,8 @@ cudaError_t launch_plan_update(const dsa_ctx *ctx, dsa_plan_t *plan, const int32
   p.cta_begin = plan->idx[0].cta_begin;
   p.units = plan->units;
   p.combine = plan->combine;
-  p.splits_by_rows = plan->splits_by_rows;
+  p.clusters = plan->clusters;
+  p.clusters_cap = plan->n_clusters;
   p.counts = plan->counts;
   p.err = ctx->err;
   plan_update_kernel<<<1, kPlanThreads, plan_update_smem(plan->T, plan->max_spans), s>>>(p);

@@ -68,7 +68,7 @@ enum { DSA_INDEX_BF16 = 0, DSA_INDEX_FP8_132 = 1 };
 typedef struct dsa_config {
   int32_t index_heads;   /* indexer heads Hi (64 for DeepSeek-V3.2) */
   int32_t index_dim;     /* indexer head dim Di (128) */
-  int32_t topk;          /* positions kept per row (2048) */
+  int32_t topk;          /* positions kept per row (2048; at most 16384) */
   int32_t heads;         /* MLA query heads H (128) */
   int32_t kv_lora_rank;  /* latent width L (512); also the output width */
   int32_t rope_dim;      /* rope width R (64) */

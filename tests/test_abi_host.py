@@ -101,12 +101,18 @@ def test_plan_needs_selection_and_units(lib):
     assert not short.needs_selection
     long = ctx.plan([S(0, 1, K, pg[:33])], cache_pages=64)           # sees topk + 1
     assert long.needs_selection
-    # one decode row is split over several key ranges for occupancy; a full
-    # prefill batch is not
-    assert long.info.attend_splits_max > 1 and long.info.attend_units == long.info.attend_splits_max
+    # attention: the rows' key tiles (64 keys each), in order, are cut into
+    # contiguous ranges of ceil(S / n) tiles for n = min(76, ceil(S / 16))
+    # persistent clusters (152 SMs); a row crossed by a cut is one unit per
+    # piece.  One decode row of 32 tiles: two clusters of 16, two units.
+    assert long.info.attend_splits_max == 2 and long.info.attend_units == 2
     wl = W.config(2)
     big = ctx.plan(wl.spans, wl.num_pages)
-    assert big.info.attend_units == wl.num_rows and big.info.attend_splits_max == 1
+    tiles = 32 * wl.num_rows                  # every row selects 2048 keys
+    n = min(76, -(-tiles // 16))
+    per = -(-tiles // n)
+    cuts_inside_rows = sum(1 for c in range(1, n) if (c * per) % 32 != 0)
+    assert big.info.attend_units == wl.num_rows + cuts_inside_rows and big.info.attend_splits_max == 2
     assert big.num_scores == sum(range(8193, 16385))
 
 
