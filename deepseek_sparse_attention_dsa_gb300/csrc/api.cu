@@ -281,27 +281,24 @@ dsa_status dsa_plan(dsa_ctx_t *ctx, const dsa_span_t *spans, int32_t num_spans, 
     for (auto &g : groups[set]) tiles += g.ntiles;
     if (tiles == 0) continue;
     const int G = set ? Gm : 1;
-    const int cap = std::max(1, ctx->num_sms * indexer_ctas_per_sm(c, G));
-    // items of at most `tpi` tiles; CTAs take contiguous, tile-balanced item ranges
-    const int64_t tpi = index_tiles_per_item(tiles, cap);
-    std::vector<int64_t> prefix{0};
+    // CTAs take exactly balanced tile ranges (floor or ceil of tiles / CTAs);
+    // a group a range boundary crosses is one item per piece
+    const int n_ctas = static_cast<int>(std::min<int64_t>(tiles, std::max(1, ctx->num_sms * indexer_ctas_per_sm(c, G))));
+    cta_begin[set].assign(n_ctas + 1, 0);
+    int64_t off = 0;
     for (int32_t gi = 0; gi < static_cast<int32_t>(groups[set].size()); ++gi) {
       const IdxGroup &g = groups[set][gi];
-      for (int32_t t = 0; t < g.ntiles; t += static_cast<int32_t>(tpi)) {
-        IdxItem it{gi, t, std::min<int32_t>(g.ntiles, t + static_cast<int32_t>(tpi)), 0};
-        items[set].push_back(it);
-        prefix.push_back(prefix.back() + (it.tile1 - it.tile0));
+      if (g.ntiles <= 0) continue;
+      const int64_t b0 = index_cta_of_tile(off, tiles, n_ctas), b1 = index_cta_of_tile(off + g.ntiles - 1, tiles, n_ctas);
+      for (int64_t b = b0; b <= b1; ++b) {
+        const int64_t a = std::max<int64_t>(off, index_cta_start(b, tiles, n_ctas));
+        const int64_t e = std::min<int64_t>(off + g.ntiles, index_cta_start(b + 1, tiles, n_ctas));
+        if (a == index_cta_start(b, tiles, n_ctas)) cta_begin[set][b] = static_cast<int32_t>(items[set].size());
+        items[set].push_back(IdxItem{gi, static_cast<int32_t>(a - off), static_cast<int32_t>(e - off), 0});
       }
+      off += g.ntiles;
     }
     const int n_items = static_cast<int>(items[set].size());
-    const int n_ctas = std::min(n_items, cap);
-    cta_begin[set].resize(n_ctas + 1);
-    size_t k = 0;
-    for (int b = 0; b <= n_ctas; ++b) {
-      const int64_t target = tiles * b / n_ctas;
-      while (k < prefix.size() - 1 && prefix[k] < target) ++k;
-      cta_begin[set][b] = static_cast<int32_t>(k);
-    }
     cta_begin[set][n_ctas] = n_items;
     plan->idx[set].G = G;
     plan->idx[set].n_groups = static_cast<int>(groups[set].size());
@@ -476,7 +473,11 @@ dsa_status dsa_plan_capturable(dsa_ctx_t *ctx, int32_t max_rows, int32_t max_spa
     return DSA_ERR_INVALID_ARG;
   const dsa_config_t &c = ctx->cfg;
   // worst-case work for any update within the capacities
-  const int64_t items_cap = max_scores / kIndexTile + 2 * static_cast<int64_t>(max_rows) + 1;
+  // indexer items: one per row plus one per CTA boundary inside a row, and
+  // the CTAs are at most the key tiles (max_scores / 128 + 2 per row)
+  const int idx_ctas = std::max(1, ctx->num_sms * indexer_ctas_per_sm(c, 1));
+  const int64_t items_cap =
+      static_cast<int64_t>(max_rows) + std::min<int64_t>(idx_ctas, max_scores / kIndexTile + 2 * static_cast<int64_t>(max_rows)) + 1;
   // attention: at most one cluster per two SMs; each cut between clusters
   // adds one unit and at most one split row, and each split row's pieces are
   // its cuts plus one
@@ -485,7 +486,7 @@ dsa_status dsa_plan_capturable(dsa_ctx_t *ctx, int32_t max_rows, int32_t max_spa
   const int32_t combine_cap = std::min(max_rows, clusters_cap);
   const int32_t slots_cap = 2 * clusters_cap;
   if (items_cap > INT32_MAX / 2 || units_cap > INT32_MAX / 2) return DSA_ERR_INVALID_ARG;
-  const int idx_cap = std::max(1, ctx->num_sms * indexer_ctas_per_sm(c, 1));
+  const int idx_cap = idx_ctas;
 
   dsa_plan_t *plan = new (std::nothrow) dsa_plan_t();
   if (!plan) return DSA_ERR_OOM;

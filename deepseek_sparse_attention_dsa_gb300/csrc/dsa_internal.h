@@ -99,10 +99,17 @@ cudaError_t ensure_smem_limit(Kernel kern, int bytes, int device, std::atomic<ui
   return e;
 }
 
-// Tiles per indexer work item for `tiles` tiles over `cap` persistent CTAs.
-__host__ __device__ inline int64_t index_tiles_per_item(int64_t tiles, int cap) {
-  const int64_t t = tiles / (static_cast<int64_t>(cap) * 8);
-  return t < 2 ? 2 : (t > 32 ? 32 : t);
+// The persistent indexer's split of a launch set's `total` key tiles (its
+// groups' tiles in order) over `cap` CTAs: CTA b takes tiles
+// [index_cta_start(b), index_cta_start(b + 1)), ceil(total * b / cap), so
+// every CTA has floor or ceil of total / cap tiles and tile t belongs to CTA
+// floor(t * cap / total).  A group a boundary crosses is one work item per
+// piece.  The host planner and the device planner share these functions.
+__host__ __device__ inline int64_t index_cta_start(int64_t b, int64_t total, int cap) {
+  return (total * b + cap - 1) / cap;
+}
+__host__ __device__ inline int64_t index_cta_of_tile(int64_t t, int64_t total, int cap) {
+  return t * cap / total;
 }
 
 // Order-preserving 32-bit key of a score (larger score, larger key; -0.0

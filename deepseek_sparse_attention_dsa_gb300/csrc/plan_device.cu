@@ -12,10 +12,10 @@
 // step get position -1 and attention units / merges past its counts row -1,
 // so their work exits at once; the counts themselves stay on the device.
 //
-// One CTA of 1024 threads.  The spans and the per-row offsets live in shared
-// memory; each thread takes a contiguous run of spans or rows (at most
-// kMaxRowsPerThread), and block-wide exclusive scans give the offsets, so the
-// planner is a handful of passes with no chain of global-memory round trips.
+// One CTA of 1024 threads.  The spans live in shared memory; each thread
+// takes a contiguous run of spans or rows (at most kMaxRowsPerThread), and
+// block-wide exclusive scans give the offsets, so the planner is a handful of
+// passes with no chain of global-memory round trips.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -79,17 +79,13 @@ __device__ int64_t block_exclusive_scan(int64_t v, int64_t *total, int64_t *sh) 
   return before;
 }
 
-__device__ __forceinline__ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_update_kernel(const PlanUpdateParams p) {
   extern __shared__ uint8_t smem_raw[];
-  // shared memory: per row [max_rows + 1] int64 tile offsets and int32 item
-  // offsets, then per span [max_spans + 1] first rows and [max_spans] ctx_start,
-  // page_off, num_pages, page_start
-  int64_t *r_tile0 = reinterpret_cast<int64_t *>(smem_raw);
-  int32_t *r_item0 = reinterpret_cast<int32_t *>(r_tile0 + p.max_rows + 1);
-  int32_t *s_q0 = r_item0 + p.max_rows + 1;
+  // shared memory: per span [max_spans + 1] first rows and [max_spans]
+  // ctx_start, page_off, num_pages, page_start
+  int32_t *s_q0 = reinterpret_cast<int32_t *>(smem_raw);
   int32_t *s_ctx = s_q0 + p.max_spans + 1;
   int32_t *s_poff = s_ctx + p.max_spans;
   int32_t *s_np = s_poff + p.max_spans;
@@ -182,7 +178,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_update_kernel(const PlanUpd
   // persistent cluster (att_cluster_split, the host planner's function); a
   // row a cut crosses becomes one unit per piece, with partial slots and a
   // merge.
-  const int32_t tpi = static_cast<int32_t>(index_tiles_per_item(tiles_total, p.idx_cap));   // 2 .. 32
+  // the indexer's tiles are split over n_cta CTAs exactly (index_cta_start,
+  // the host planner's function); a row a CTA boundary crosses is one item
+  // per piece
+  const int32_t n_cta = static_cast<int32_t>(min64(tiles_total, p.idx_cap));
+  auto idx_pieces = [&](int64_t off, int64_t n) -> int {
+    return static_cast<int>(index_cta_of_tile(off + n - 1, tiles_total, n_cta) - index_cta_of_tile(off, tiles_total, n_cta) + 1);
+  };
   int64_t my_at = 0;
 #pragma unroll
   for (int k = 0; k < kMaxRowsPerThread; ++k)
@@ -195,7 +197,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_update_kernel(const PlanUpd
   // counts packed two per scan: (items << 32 | units), (slots << 32 | merges)
   int64_t my_iu = 0, my_sm = 0;
   {
-    int64_t off = at_off0;
+    int64_t off = at_off0, ioff = tile;
 #pragma unroll
     for (int k = 0; k < kMaxRowsPerThread; ++k) {
       if (pos[k] < 0) continue;
@@ -203,9 +205,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_update_kernel(const PlanUpd
                                               index_tile_lead(p.row_page_start[ra + k], p.box_rows));
       const int64_t n = att_row_tiles(pos[k], p.topk);
       const int u = static_cast<int>((off + n - 1) / per - off / per + 1);
-      my_iu += (static_cast<int64_t>((tiles + tpi - 1) / tpi) << 32) + u;
+      my_iu += (static_cast<int64_t>(idx_pieces(ioff, tiles)) << 32) + u;
       my_sm += u > 1 ? ((static_cast<int64_t>(u) << 32) + 1) : 0;
       off += n;
+      ioff += tiles;
     }
   }
   int64_t iu_total = 0, sm_total = 0;
@@ -221,8 +224,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_update_kernel(const PlanUpd
     if (k >= rn) continue;
     const int r = ra + k;
     p.row_score_off[r] = sc;
-    r_tile0[r] = tile;
-    r_item0[r] = static_cast<int32_t>(iu >> 32);
     if (pos[k] < 0) continue;
     sc += static_cast<int64_t>(pos[k]) + 1;
     const int32_t lead = index_tile_lead(p.row_page_start[r], p.box_rows);
@@ -239,7 +240,18 @@ __global__ void __launch_bounds__(kPlanThreads) plan_update_kernel(const PlanUpd
     g.lead = lead;
     p.groups[r] = g;
     int32_t item = static_cast<int32_t>(iu >> 32);
-    for (int32_t t0 = 0; t0 < tiles; t0 += tpi, ++item) p.items[item] = IdxItem{r, t0, min(tiles, t0 + tpi), 0};
+    {
+      const int64_t b0 = index_cta_of_tile(tile, tiles_total, n_cta), b1 = index_cta_of_tile(tile + tiles - 1, tiles_total, n_cta);
+      for (int64_t b = b0; b <= b1; ++b, ++item) {
+        const int64_t cs = index_cta_start(b, tiles_total, n_cta);
+        const int64_t a = tile > cs ? tile : cs;
+        const int64_t ce = index_cta_start(b + 1, tiles_total, n_cta);
+        const int64_t e = tile + tiles < ce ? tile + tiles : ce;
+        if (a == cs) p.cta_begin[b] = item;   // the CTA's first item
+        p.items[item] = IdxItem{r, static_cast<int32_t>(a - tile), static_cast<int32_t>(e - tile), 0};
+      }
+    }
+    const int32_t n_idx_pieces = idx_pieces(tile, tiles);
     tile += tiles;
     // attention: one unit per piece of the row's tiles between cuts
     const int64_t nsel = min64(p.topk, static_cast<int64_t>(pos[k]) + 1);
@@ -258,12 +270,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_update_kernel(const PlanUpd
                               u > 1 ? slot + static_cast<int32_t>(cl - c0) : -1};
     }
     if (u > 1) smc += (static_cast<int64_t>(u) << 32) + 1;
-    iu += (static_cast<int64_t>((tiles + tpi - 1) / tpi) << 32) + u;
+    iu += (static_cast<int64_t>(n_idx_pieces) << 32) + u;
     at_off += n;
-  }
-  if (tid == 0) {
-    r_tile0[p.max_rows] = tiles_total;
-    r_item0[p.max_rows] = n_items;
   }
   // padding: units and merges past the step's counts exit at once
   for (int i = n_units + tid; i < p.units_cap; i += kPlanThreads) p.units[i] = AttUnit{-1, 0, 0, -1};
@@ -282,28 +290,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_update_kernel(const PlanUpd
     if (tid < p.clusters_cap) p.clusters[tid] = e;
   }
 
-  // ---- per-CTA item ranges of the persistent indexer: CTA b starts at the
-  // first item that begins at or after tile tiles_total * b / idx_cap.  Item
-  // starts grow along the rows, so the search runs over rows: the first row
-  // whose last item starts at or after the target, then the item inside it.
-  for (int b = tid; b <= p.idx_cap; b += kPlanThreads) {
-    int32_t k = n_items;
-    if (b < p.idx_cap) {
-      const int64_t target = tiles_total * b / p.idx_cap;
-      int lo = 0, hi = static_cast<int>(T);   // first row in [0, T) whose last item starts at or after target
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        const int64_t last = r_tile0[mid] + static_cast<int64_t>(r_item0[mid + 1] - r_item0[mid] - 1) * tpi;
-        if (last < target) lo = mid + 1;
-        else hi = mid;
-      }
-      if (lo < T) {
-        const int32_t d = static_cast<int32_t>(target > r_tile0[lo] ? target - r_tile0[lo] : 0);   // < the row's tiles
-        k = r_item0[lo] + (d + tpi - 1) / tpi;
-      }
-    }
-    p.cta_begin[b] = k;
-  }
+  // ---- CTAs past the split (n_cta <= b <= idx_cap) start at the end
+  for (int b = n_cta + tid; b <= p.idx_cap; b += kPlanThreads) p.cta_begin[b] = n_items;
   if (tid == 0) {
     p.counts[0] = static_cast<int32_t>(T);
     p.counts[1] = n_items;
@@ -318,9 +306,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_update_kernel(const PlanUpd
 
 }  // namespace
 
-static size_t plan_update_smem(int32_t max_rows, int32_t max_spans) {
-  return static_cast<size_t>(max_rows + 1) * (sizeof(int64_t) + sizeof(int32_t)) +
-         static_cast<size_t>(max_spans + 1) * sizeof(int32_t) + static_cast<size_t>(max_spans) * 4 * sizeof(int32_t);
+static size_t plan_update_smem(int32_t /*max_rows*/, int32_t max_spans) {
+  return static_cast<size_t>(max_spans + 1) * sizeof(int32_t) + static_cast<size_t>(max_spans) * 4 * sizeof(int32_t);
 }
 
 cudaError_t launch_plan_update(const dsa_ctx *ctx, dsa_plan_t *plan, const int32_t *num_spans,
