@@ -50,33 +50,48 @@ struct PlanUpdateParams {
   int *err;
 };
 
-// Exclusive scan of one value per thread over the block.  Returns the sum of
-// the values of the lower threads; *total = the sum over all threads.
-__device__ int64_t block_exclusive_scan(int64_t v, int64_t *total, int64_t *sh) {
+// Exclusive scans of N values per thread over the block, in one pass (three
+// barriers for all N): v[i] becomes the sum of the lower threads' v[i] and
+// total[i] the sum over all threads.  sh holds 32 x N values.
+template <int N>
+__device__ void block_exclusive_scan(int64_t (&v)[N], int64_t (&total)[N], int64_t *sh) {
   static_assert(kPlanThreads == 32 * 32, "one scan level over 32 warps");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int64_t x = v;
+  int64_t x[N];
+#pragma unroll
+  for (int i = 0; i < N; ++i) x[i] = v[i];
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, x[i], o);
+      if (lane >= o) x[i] += y;
+    }
   }
-  if (lane == 31) sh[warp] = x;
+  if (lane == 31) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) sh[i * 32 + warp] = x[i];
+  }
   __syncthreads();
   if (warp == 0) {
-    int64_t t = sh[lane];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int64_t y = __shfl_up_sync(0xffffffffu, t, o);
-      if (lane >= o) t += y;
+    for (int i = 0; i < N; ++i) {
+      int64_t t = sh[i * 32 + lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, t, o);
+        if (lane >= o) t += y;
+      }
+      sh[i * 32 + lane] = t;
     }
-    sh[lane] = t;
   }
   __syncthreads();
-  const int64_t before = (warp > 0 ? sh[warp - 1] : 0) + x - v;
-  *total = sh[31];
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    v[i] = (warp > 0 ? sh[i * 32 + warp - 1] : 0) + x[i] - v[i];
+    total[i] = sh[i * 32 + 31];
+  }
   __syncthreads();   // sh is free for the next scan
-  return before;
 }
 
 __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
@@ -90,15 +105,19 @@ __global__ void __launch_bounds__(kPlanThreads) plan_update_kernel(const PlanUpd
   int32_t *s_poff = s_ctx + p.max_spans;
   int32_t *s_np = s_poff + p.max_spans;
   int32_t *s_ps = s_np + p.max_spans;
-  __shared__ int64_t sh[32];
+  __shared__ int64_t sh[32 * 3];
   const int tid = threadIdx.x;
 
-  // ---- spans into shared memory, validity, rows and scores
+  // ---- spans into shared memory, validity, rows and scores (the first span
+  // of each thread is loaded together with the count: the span array holds
+  // max_spans entries whatever the count says)
+  dsa_device_span_t s0{};
+  if (tid < p.max_spans) s0 = p.spans[tid];
   int n = *p.num_spans;
   bool ok = n >= 0 && n <= p.max_spans;
   if (!ok) n = 0;
   for (int i = tid; i < n; i += kPlanThreads) {
-    const dsa_device_span_t s = p.spans[i];
+    const dsa_device_span_t s = i == tid ? s0 : p.spans[i];
     const int64_t end = static_cast<int64_t>(s.ctx_start) + s.q_len;   // tokens 0 .. end-1
     const bool v = s.q_len >= 1 && s.ctx_start >= 0 && s.page_start >= 0 && s.page_start % p.align == 0 &&
                    s.num_pages >= 0 && s.page_off >= 0 && s.reserved == 0 &&
@@ -120,9 +139,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_update_kernel(const PlanUpd
     my_rows += q;
     my_scores += (2 * c + 1 + q) * q / 2;   // rows at positions c .. c+q-1 score pos+1 keys each
   }
-  int64_t T = 0, total_scores = 0;
-  const int64_t row0 = block_exclusive_scan(my_rows, &T, sh);
-  block_exclusive_scan(my_scores, &total_scores, sh);
+  int64_t sv[2] = {my_rows, my_scores}, st[2];
+  block_exclusive_scan<2>(sv, st, sh);
+  const int64_t row0 = sv[0];
+  int64_t T = st[0];
+  const int64_t total_scores = st[1];
   if (T > p.max_rows || total_scores > p.max_scores) ok = false;   // uniform: totals are block-wide
   if (!ok) {
     n = 0;
@@ -169,9 +190,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_update_kernel(const PlanUpd
     p.row_npages[r] = np;
     p.row_page_start[r] = ps;
   }
-  int64_t sc_total = 0, tiles_total = 0;
-  int64_t sc = block_exclusive_scan(my_sc, &sc_total, sh);
-  int64_t tile = block_exclusive_scan(my_tiles, &tiles_total, sh);
+  // (score offsets, indexer tiles and attention tiles in one scan)
+  int64_t my_at = 0;
+#pragma unroll
+  for (int k = 0; k < kMaxRowsPerThread; ++k)
+    if (pos[k] >= 0) my_at += att_row_tiles(pos[k], p.topk);
+  int64_t rv[3] = {my_sc, my_tiles, my_at}, rt[3];
+  block_exclusive_scan<3>(rv, rt, sh);
+  int64_t sc = rv[0], tile = rv[1];
+  const int64_t sc_total = rt[0], tiles_total = rt[1];
+  const int64_t at_off0 = rv[2], at_total = rt[2];
 
   // ---- indexer items and attention units per row.  The attention schedule
   // cuts the rows' key tiles, in row order, into contiguous ranges, one per
@@ -185,12 +213,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_update_kernel(const PlanUpd
   auto idx_pieces = [&](int64_t off, int64_t n) -> int {
     return static_cast<int>(index_cta_of_tile(off + n - 1, tiles_total, n_cta) - index_cta_of_tile(off, tiles_total, n_cta) + 1);
   };
-  int64_t my_at = 0;
-#pragma unroll
-  for (int k = 0; k < kMaxRowsPerThread; ++k)
-    if (pos[k] >= 0) my_at += att_row_tiles(pos[k], p.topk);
-  int64_t at_total = 0;
-  const int64_t at_off0 = block_exclusive_scan(my_at, &at_total, sh);
   int32_t ncl = 0;
   int64_t per = 1;
   att_cluster_split(at_total, p.num_sms, &ncl, &per);
@@ -211,9 +233,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_update_kernel(const PlanUpd
       ioff += tiles;
     }
   }
-  int64_t iu_total = 0, sm_total = 0;
-  int64_t iu = block_exclusive_scan(my_iu, &iu_total, sh);
-  int64_t smc = block_exclusive_scan(my_sm, &sm_total, sh);
+  int64_t uv[2] = {my_iu, my_sm}, ut[2];
+  block_exclusive_scan<2>(uv, ut, sh);
+  int64_t iu = uv[0], smc = uv[1];
+  const int64_t iu_total = ut[0], sm_total = ut[1];
   const int32_t n_items = static_cast<int32_t>(iu_total >> 32), n_units = static_cast<int32_t>(iu_total & 0xffffffff);
   const int32_t n_slots = static_cast<int32_t>(sm_total >> 32), n_merge = static_cast<int32_t>(sm_total & 0xffffffff);
   // the plan's capacities bound these counts for every update the span checks

@@ -273,7 +273,8 @@ dsa_status dsa_index_topk_fp8q(dsa_ctx_t *ctx, const dsa_plan_t *plan, const voi
  * and starts empty.  dsa_plan_update recomputes it ON THE DEVICE, enqueued
  * on `stream`, from spans in device memory:
  *   num_spans  device int32 scalar, 0 .. max_spans;
- *   spans      device dsa_device_span_t[max_spans] (the first num_spans read);
+ *   spans      device dsa_device_span_t[max_spans] (all max_spans entries are
+ *              read; the first num_spans are used);
  *   pages      device int32 page ids; span s uses pages[page_off ..
  *              page_off + num_pages); num_page_ids is the array's length.
  * The rows are the spans' rows in order (row 0 = span 0's first row).  The
