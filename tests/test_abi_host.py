@@ -155,3 +155,47 @@ def test_indexer_stays_on_tensor_cores_for_any_page_start(lib):
     small_pages = W.DSAShape(**dict(W.DEEPSEEK, page_size=4))
     plan = _host_ctx(small_pages).plan([S(0, 1, 10, np.arange(3, dtype=np.int32), page_start=1)], cache_pages=3)
     assert plan.info.index_box_rows == 4 and not plan.index_tensor_cores
+
+
+def _att_schedule(positions, topk, num_sms=152):
+    """The persistent attention schedule, written out: the rows' key tiles (64
+    keys each) in row order are cut into n = min(SMs / 2, ceil(S / 16))
+    contiguous ranges of ceil(S / n) tiles (n recomputed from that length); a
+    row a cut crosses is one unit per piece.  Returns (units, largest pieces
+    per row)."""
+    tiles = [-(-min(topk, p + 1) // 64) for p in positions]
+    S = sum(tiles)
+    n = max(1, min(num_sms // 2, -(-S // 16)))
+    per = max(1, -(-S // n))
+    units, most, off = 0, 0, 0
+    for t in tiles:
+        pieces = (off + t - 1) // per - off // per + 1
+        units += pieces
+        most = max(most, pieces)
+        off += t
+    return units, most
+
+
+@pytest.mark.parametrize("rows", [
+    [0],                          # one tile
+    [2047],                       # one full row: two clusters of 16 tiles
+    [70000] * 16,                 # 16 decode rows: 32 clusters of 16 tiles, every row cut once
+    [100000] * 128,               # long decode: 76 clusters of 54 tiles
+    list(range(0, 640, 1)),       # 640 short rows of 1..10 tiles
+    [5000] * 3 + list(range(2047, 2047 + 40)),   # decode rows and a chunk
+])
+def test_attention_schedule_units(lib, rows):
+    """The plan's attention units follow the persistent schedule's definition
+    (written out here): every row a range boundary crosses is one unit per
+    piece."""
+    ctx = _host_ctx()
+    K = W.DEEPSEEK["topk"]
+    pg = np.arange(2048, dtype=np.int32)
+    spans, q = [], 0
+    for p in rows:
+        npg = (p + 1 + 63) // 64
+        spans.append(S(q, 1, p, pg[:npg]))
+        q += 1
+    plan = ctx.plan(spans, cache_pages=2048)
+    units, most = _att_schedule(rows, K)
+    assert plan.info.attend_units == units and plan.info.attend_splits_max == most
