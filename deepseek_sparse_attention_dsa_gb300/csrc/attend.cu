@@ -15,9 +15,10 @@
 //   * 7 producer warps gather the CTA's 576 bytes of each latent row through
 //     the page table (cp.async into 128- and 64-byte swizzled tiles;
 //     completion lands on an mbarrier; the selection entries and page ids of
-//     the next tiles are already in flight).  fp8 latents (656-byte rows) are
-//     loaded into registers, dequantised (code x the scale of its 128-column
-//     group, rounded to bf16) and stored as the same bf16 tiles;
+//     the next tiles are already in flight).  For fp8 latents (656-byte
+//     rows) the codes and scales are loaded into registers, dequantised (code
+//     x the scale of its 128-column group, rounded to bf16) and stored as the
+//     same bf16 tiles, and the rope columns (bf16 already) come by cp.async;
 //   * one thread issues the partial logits S_c = Q[:, cols_c] . C[:, cols_c]^T
 //     (M = 128 heads, N = 64 keys, fp32 in TMEM; the q_nope columns of this
 //     CTA live in tensor memory as the A operand, the rope columns in shared
@@ -230,7 +231,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
     mbar_init(b_qtdone, 8);   // softmax arrivals are one elected lane per warp (after __syncwarp)
     mbar_init(b_pvdone, 1);
     for (int s = 0; s < NS; ++s) {
-      mbar_init(kfull(s), kProdThreads);
+      mbar_init(kfull(s), FP8 ? 2 * kProdThreads : kProdThreads);   // fp8: stores and rope copies
       mbar_init(kempty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -450,12 +451,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
           cp_async_mbar_arrive(kfull(st));
         } else {
           // 656-byte rows [L e4m3 | L/128 fp32 scales | R bf16]: this CTA's
-          // codes (HALF/16 pieces) and rope half (4 pieces) are loaded into
-          // registers before the stage is known to be free, dequantised (code x
-          // scale, rounded to bf16) and stored as the bf16 tile.
-          constexpr int CPH = C::HALF / 16, RP = 4, PPK = CPH + RP;
+          // codes (CPH 16-byte pieces a key) and their scales are loaded into
+          // registers before the stage is known to be free, dequantised (code
+          // x scale, rounded to bf16) and stored as the bf16 tile.  The rope
+          // half (RP pieces, already bf16) is copied straight into the stage
+          // by cp.async once it is free: the full barrier then counts each
+          // producer twice (its stores, its copies).  Register loads are what
+          // holds a producer up (every barrier, fence and release arrive
+          // waits for them), so only the pieces that need arithmetic take
+          // that path.
+          constexpr int CPH = C::HALF / 16, RP = 4;
           constexpr int RB8 = L + 4 * (L / 128) + 2 * R;
-          constexpr int PER = (T * PPK + kProdThreads - 1) / kProdThreads;
+          constexpr int PER = (T * CPH + kProdThreads - 1) / kProdThreads;
           uint4 raw[PER];
           float scl[PER];
 #pragma unroll
@@ -463,37 +470,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
             const int i = pt + u * kProdThreads;
             raw[u] = make_uint4(0, 0, 0, 0);
             scl[u] = 0.f;
-            if (i < T * PPK) {
-              const int key = i / PPK, k = i - key * PPK;
+            if (i < T * CPH) {
+              const int key = i / CPH, k = i - key * CPH;
               const int32_t prow = rows[key];
               if (prow >= 0) {
                 const uint8_t *base = p.latent + static_cast<int64_t>(prow) * RB8;
-                if (k < CPH) {
-                  raw[u] = __ldg(reinterpret_cast<const uint4 *>(base + static_cast<int>(crank) * C::HALF + 16 * k));
-                  scl[u] = __ldg(reinterpret_cast<const float *>(base + L) + (static_cast<int>(crank) * C::HALF) / 128 +
-                                 k / 8);
-                } else {
-                  raw[u] = __ldg(reinterpret_cast<const uint4 *>(base + L + 4 * (L / 128) +
-                                                                 static_cast<int>(crank) * C::RH * 2 + 16 * (k - CPH)));
-                }
+                raw[u] = __ldg(reinterpret_cast<const uint4 *>(base + static_cast<int>(crank) * C::HALF + 16 * k));
+                scl[u] = __ldg(reinterpret_cast<const float *>(base + L) + (static_cast<int>(crank) * C::HALF) / 128 +
+                               k / 8);
               }
             }
           }
           ok = mbar_wait(kempty(st), ((g / NS) & 1) ^ 1, abort_flag, p.err);
+          if (ok) {
+            for (int idx = pt; idx < T * RP; idx += kProdThreads) {
+              const int key = idx / RP, piece = idx - key * RP;
+              const int32_t prow = rows[key];
+              const uint8_t *src = p.latent + (prow >= 0 ? static_cast<int64_t>(prow) * RB8 + L + 4 * (L / 128) +
+                                                               static_cast<int>(crank) * C::RH * 2 + 16 * piece
+                                                         : 0);
+              cp_async_16_zfill(kst + C::NPV * C::CHUNK + sw64_offset(key, piece), src, prow >= 0 ? 16u : 0u);
+            }
+            cp_async_mbar_arrive(kfull(st));
+          }
 #pragma unroll
           for (int u = 0; u < PER; ++u) {
             const int i = pt + u * kProdThreads;
-            if (!ok || i >= T * PPK) continue;
-            const int key = i / PPK, k = i - key * PPK;
-            if (k < CPH) {
-              uint4 lo, hi;
-              e4m3x16_to_bf16(raw[u], scl[u], lo, hi);
-              const uint32_t chunk = kst + (k / 4) * C::CHUNK;
-              st_shared_v4(chunk + sw128_offset(key, (k % 4) * 2), lo);
-              st_shared_v4(chunk + sw128_offset(key, (k % 4) * 2 + 1), hi);
-            } else {
-              st_shared_v4(kst + C::NPV * C::CHUNK + sw64_offset(key, k - CPH), raw[u]);
-            }
+            if (!ok || i >= T * CPH) continue;
+            const int key = i / CPH, k = i - key * CPH;
+            // a piece is two 16-byte bf16 units of its key's 128-byte row;
+            // pieces in odd chunks store their upper unit first, so that
+            // the eight pieces of a store phase cover eight different units
+            const int par = (k >> 2) & 1;
+            uint4 r = raw[u];
+            if (par) r = make_uint4(r.z, r.w, r.x, r.y);
+            uint4 first, second;
+            e4m3x16_to_bf16(r, scl[u], first, second);
+            const uint32_t chunk = kst + (k / 4) * C::CHUNK;
+            st_shared_v4(chunk + sw128_offset(key, (k % 4) * 2 + par), first);
+            st_shared_v4(chunk + sw128_offset(key, (k % 4) * 2 + (par ^ 1)), second);
           }
           fence_proxy_async_smem();
           if (ok) mbar_arrive(kfull(st));
