@@ -733,14 +733,19 @@ __global__ void __launch_bounds__(kFp8Threads, 1) index_fp8_tc_kernel(const __gr
           if (bytes) mbar_arrive_expect_tx(c8full(s8), bytes);
           else mbar_arrive(c8full(s8));
         }
-        for (int b = 0; b < nbox; ++b) {
+        {
+          // the codes and the scales of every box from their own lanes (a
+          // box has >= 8 rows, so 2 * nbox <= 32)
+          const int b = lane >> 1;
           const int page = __shfl_sync(0xffffffffu, mypage, b);
           const int slot = __shfl_sync(0xffffffffu, myslot, b);
-          if (lane == 0 && page >= 0) {
-            tma_load_3d(sbase + C::OFF_C8 + s8 * C::CODE_BYTES + b * p.BH * 128, &p.tm_codes, 0, slot, page,
-                        c8full(s8));
-            tma_load_2d(sbase + C::OFF_SC8 + s8 * C::SC8_BYTES + b * sc_stride * 4, &p.tm_scales, slot, page,
-                        c8full(s8));
+          if (b < nbox && page >= 0) {
+            if ((lane & 1) == 0)
+              tma_load_3d(sbase + C::OFF_C8 + s8 * C::CODE_BYTES + b * p.BH * 128, &p.tm_codes, 0, slot, page,
+                          c8full(s8));
+            else
+              tma_load_2d(sbase + C::OFF_SC8 + s8 * C::SC8_BYTES + b * sc_stride * 4, &p.tm_scales, slot, page,
+                          c8full(s8));
           }
         }
         if (++s8 == C::S8) {
