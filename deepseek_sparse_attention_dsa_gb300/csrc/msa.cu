@@ -20,20 +20,24 @@
 // tau and the lowest blocks equal to it (ties to the lower block), in
 // ascending order either way.
 //
-// msa_attend_tc_kernel (block_size 128, head_dim 128): one CTA per row walks
-// (tile, kv head) steps.  A tile is 128 positions, one UMMA M:
+// msa_attend_tc_kernel (block_size 128, head_dim 128): a persistent grid, one
+// CTA per SM walking its rows (every grid-th row) as a run of (tile, kv head)
+// steps.  A tile is 128 positions, one UMMA M:
 //     S^T[token, head] = K[token, :] . Q_g[head, :]      (M = 128 tokens, N = group heads padded to 16)
 //     O^T_g[dim, head] += V[:, dim]^T . P^T[:, head]     (M = 128 dims, A = V read MN-major, B = P^T)
-// Warp 0 issues the TMA loads of a step's K and V boxes (the paged cache as
-// a 2-D tensor, 128-byte swizzle) into a ring of stages, warp 1 issues the
-// MMAs (QK of step t+1 before PV of step t waits for its P), and eight
+// Warp 10 builds each row's tile list (kept blocks in ascending order) up to
+// two rows ahead, warp 0 issues the TMA loads of a step's K and V boxes (the
+// paged cache as a 2-D tensor, 128-byte swizzle) into a ring of stages that
+// runs on across rows, warp 1 issues the MMAs (QK of step t+1 before PV of
+// step t waits for its P; the next row's QKs start while the current row
+// drains), and eight
 // softmax warps, two per TMEM lane quadrant (thread = TMEM lane = token of S,
 // dim of O; each warp of a pair takes half of the heads), reduce each head's
 // maximum and sum with halving shuffle exchanges (one transposing pass per
 // reduction, not one butterfly per head), keep a per-head
 // reference max that moves only when it grows by more than 2^8 (O is then
 // rescaled in TMEM), write P^T as bf16 in the 128-byte-swizzled K-major
-// layout, and normalise at the end.  Tiles start on the box boundary below
+// layout, and normalise a row's output at the start of their next row.  Tiles start on the box boundary below
 // the span's page_start (as the indexer's key tiles do): with page_start a
 // multiple of the box height a tile is exactly one block, otherwise a block
 // spans two tiles and rows outside the kept blocks are masked (their V rows
@@ -64,7 +68,8 @@ static_assert(kSelRankBlocks <= kSelThreads, "one block per thread when ranking 
 constexpr int kMsaMaxK = 64;                  // topk_blocks
 constexpr int kMsaTile = 128;                 // positions per tile (UMMA M)
 constexpr int kMsaMaxTiles = 2 * kMsaMaxK;
-constexpr int kMsaThreads = 320;              // warp 0 TMA, warp 1 MMA, warps 2-9 softmax (two per lane quadrant)
+constexpr int kMsaThreads = 352;              // warp 0 TMA, warp 1 MMA, warps 2-9 softmax (two per lane quadrant), warp 10 tile lists
+constexpr int kMsaListWarp = 10;
 constexpr int kMsaSoftThreads = 256;
 constexpr int kMsaMaxKvHeads = 8;
 
@@ -310,9 +315,11 @@ struct MsaParams {
   const int32_t *row_pos, *row_page_off, *row_npages, *row_page_start, *pages;
   __nv_bfloat16 *out;  // [T][Hq][128]
   int *err;
-  int Hq, Hkv, group, K, P, BH, num_pages, stages;
+  int T, Hq, Hkv, group, K, P, BH, num_pages, stages;
   float scale_log2;    // sm_scale * log2(e)
 };
+
+constexpr int kMsaBars = 28;
 
 // Shared-memory layout of one CTA (bytes from a 1024-aligned base).
 struct MsaLayout {
@@ -323,13 +330,107 @@ struct MsaLayout {
     off_p = off_q + Hkv * 2 * NG * 128;
     off_red = off_p + 2 * 2 * NG * 128;
     off_ml = off_red + 4 * 8 * NG * 4;          // [group][step parity][max keys | sums][NG][4 quads]
-    off_tiles = off_ml + 3 * Hkv * NG * 4;      // m [tile parity][Hkv][NG], l [Hkv][NG]
-    off_bar = (off_tiles + 2 * kMsaMaxTiles * 4 + 7) / 8 * 8;
-    off_misc = off_bar + 24 * 8;
+    off_tiles = off_ml + 4 * Hkv * NG * 4;      // m [tile parity][Hkv][NG], l [row parity][Hkv][NG]
+    off_bar = (off_tiles + 2 * 2 * kMsaMaxTiles * 4 + 7) / 8 * 8;   // [row parity][tile | flags][kMsaMaxTiles]
+    off_misc = off_bar + kMsaBars * 8;
     bytes = off_misc + 16 + 1024;   // + alignment slack
   }
 };
 
+// The tile list of one row, built by a warp (every lane returns its length):
+// the kept blocks in ascending order (rank placement: the selection may come
+// in any order), each block's tile and, when the span's token 0 is off the
+// box boundary, the tile holding the block's last `lead` positions.  tu and
+// tf hold kMsaMaxTiles entries; the sorted blocks pass through tf's upper
+// half (list entry n <= 2 i + 1 is written after sorted block i is read).
+__device__ __forceinline__ int msa_row_tiles(const int32_t *sr, int K, int pos, int lead, int32_t *tu, int32_t *tf,
+                                             int *err) {
+  const int lane = threadIdx.x & 31;
+  const int last = pos / kMsaTile;
+  int b[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int e = lane + 32 * h;
+    int v = e < K ? sr[e] : -1;
+    if (v < -1 || v > last) {
+      atomicOr(err, kErrBounds);
+      v = -1;
+    }
+    b[h] = v;
+  }
+  int rank[2] = {0, 0};
+  for (int e = 0; e < 64; ++e) {
+    const int v = __shfl_sync(0xffffffffu, b[e >> 5], e & 31);
+    if (v < 0) continue;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      if (b[h] >= 0 && (v < b[h] || (v == b[h] && e < lane + 32 * h))) ++rank[h];
+  }
+  int32_t *sorted = tf + kMsaMaxK;
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+    if (b[h] >= 0) sorted[rank[h]] = b[h];
+  const int nvalid = __reduce_add_sync(0xffffffffu, (b[0] >= 0 ? 1 : 0) + (b[1] >= 0 ? 1 : 0));
+  __syncwarp();
+  int n = 0;
+  if (lane == 0) {
+    for (int i = 0; i < nvalid; ++i) {
+      const int blk = sorted[i];
+      // tile blk holds the block's positions from row `lead` on (bit 1)
+      if (n > 0 && tu[n - 1] == blk) tf[n - 1] |= 2;
+      else { tu[n] = blk; tf[n] = 2; ++n; }
+      // tile blk+1 holds its last `lead` positions in rows 0..lead-1 (bit 0)
+      if (lead > 0 && kMsaTile * (blk + 1) - lead <= pos) {
+        tu[n] = blk + 1;
+        tf[n] = 1;
+        ++n;
+      }
+    }
+  }
+  n = __shfl_sync(0xffffffffu, n, 0);
+  __syncwarp();
+  return n;
+}
+
+// O / l of one row into its output, by one softmax warp (thread = dim i):
+// for the kv heads g = grp, grp + NGRP, ... the warp's NH heads from h0 on.
+// ocol is this lane quadrant's tensor-memory address of the row's O for kv
+// head 0, head h0; l_row the row's sums [Hkv][NG].
+template <int NG, int NGRP, int NH>
+__device__ __forceinline__ void msa_write_out(uint32_t ocol, const float *l_row, int Hkv, int grp, int h0, int group,
+                                              __nv_bfloat16 *out_row, int i) {
+  constexpr int CW = NH < 16 ? NH : 16;   // heads per tensor-memory load
+  for (int g = grp; g < Hkv; g += NGRP) {
+#pragma unroll
+    for (int c0 = 0; c0 < NH; c0 += CW) {
+      float o[CW];
+      if constexpr (CW == 8) tmem_ld8(ocol + g * NG + c0, o);
+      else tmem_ld16(ocol + g * NG + c0, o);
+      tmem_ld_wait();
+#pragma unroll
+      for (int k = 0; k < CW; ++k) {
+        const int h = h0 + c0 + k;
+        if (h >= group) continue;
+        const float l = l_row[g * NG + h];
+        out_row[(g * group + h) * 128 + i] = __float2bfloat16_rn(l > 0.f ? o[k] / l : 0.f);
+      }
+    }
+  }
+}
+
+// A persistent grid: CTA b takes rows b, b + grid, b + 2 grid, ... (padding
+// rows of a capturable plan, pos < 0, are skipped by every role alike).  The
+// stage ring, the S and P buffers and their barriers run on across rows
+// (barrier parities follow the CTA's global step count), so the next row's
+// loads and QKs start while the current row drains.  Each row's tile list is
+// built by the producer into one of two buffers (row parity) and released by
+// the MMA thread and the softmax warps once they are past the row; the row's
+// Q is reloaded once the previous row's last QK has completed.  A row's
+// output is written by its softmax warps at the start of their next row,
+// while that row's first QK is on its way (its sums l are double-buffered by
+// row parity; O has one buffer: a row's first PV into a kv head's columns
+// needs a P that the warps owning that head write only after reading the
+// previous row's O out).
 template <int NG, int NGRP>
 __global__ void __launch_bounds__(kMsaThreads, 1) msa_attend_tc_kernel(const __grid_constant__ MsaParams p) {
   constexpr int CH = kMsaTile * 128;        // [128 rows][64 columns] bf16
@@ -353,75 +454,31 @@ __global__ void __launch_bounds__(kMsaThreads, 1) msa_attend_tc_kernel(const __g
   auto sempty = [&](int b) { return bar0 + 8u * (14 + b); };
   auto pfull = [&](int b) { return bar0 + 8u * (16 + b); };
   auto pempty = [&](int b) { return bar0 + 8u * (18 + b); };
-  const uint32_t b_pvdone = bar0 + 8u * 20, b_qfull = bar0 + 8u * 21;
+  const uint32_t b_pvdone = bar0 + 8u * 20, b_qfull = bar0 + 8u * 21, b_qempty = bar0 + 8u * 22;
+  auto tfull = [&](int b) { return bar0 + 8u * (23 + b); };    // tile list b written
+  auto tempty = [&](int b) { return bar0 + 8u * (25 + b); };   // tile list b read by every consumer
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + lay.off_misc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + lay.off_misc + 4);
-  int *ntiles_sm = reinterpret_cast<int *>(smem + lay.off_misc + 8);
-  int32_t *tile_u = reinterpret_cast<int32_t *>(smem + lay.off_tiles);
-  int32_t *tile_fl = tile_u + kMsaMaxTiles;
+  int *ntiles_sm = reinterpret_cast<int *>(smem + lay.off_misc + 8);   // [row parity]
+  int32_t *tiles_sm = reinterpret_cast<int32_t *>(smem + lay.off_tiles);
+  auto tile_u = [&](int b) { return tiles_sm + b * 2 * kMsaMaxTiles; };
+  auto tile_fl = [&](int b) { return tiles_sm + b * 2 * kMsaMaxTiles + kMsaMaxTiles; };
   float *m_sm = reinterpret_cast<float *>(smem + lay.off_ml);   // [tile parity][Hkv][NG]
-  float *l_sm = m_sm + 2 * Hkv * NG;                            // [Hkv][NG]
+  float *l_sm = m_sm + 2 * Hkv * NG;                            // [row parity][Hkv][NG]
   uint32_t *redmax = reinterpret_cast<uint32_t *>(smem + lay.off_red);       // [step parity] at stride 8*NG: [NG][4]
   float *redsum = reinterpret_cast<float *>(smem + lay.off_red) + 4 * NG;    // the same, after the maxima
 
   const int warp = threadIdx.x / 32, lane = lane_id();
-  const int row = blockIdx.x;
-  const int pos = p.row_pos[row];
-  if (pos < 0) return;   // padding row of a capturable plan: the whole CTA leaves before any barrier
-  const int page_start = p.row_page_start[row], page_off = p.row_page_off[row], npages = p.row_npages[row];
-  const int lead = page_start % p.BH;
+  const int row0 = blockIdx.x, rstride = gridDim.x;
 
-  if (warp == 0) {
-    // ---- the row's tiles: kept blocks in ascending order (rank placement,
-    // the selection may come in any order), each block's tile and, when
-    // page_start is off the box boundary, the tile holding its tail
-    const int32_t *sr = p.sel + static_cast<int64_t>(row) * p.K;
-    const int last = pos / kMsaTile;
-    int b[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int e = lane + 32 * h;
-      int v = e < p.K ? sr[e] : -1;
-      if (v < -1 || v > last) {
-        atomicOr(p.err, kErrBounds);
-        v = -1;
-      }
-      b[h] = v;
-    }
-    int rank[2] = {0, 0};
-    for (int e = 0; e < 64; ++e) {
-      const int v = __shfl_sync(0xffffffffu, b[e >> 5], e & 31);
-      if (v < 0) continue;
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-        if (b[h] >= 0 && (v < b[h] || (v == b[h] && e < lane + 32 * h))) ++rank[h];
-    }
-    int *sorted = tile_fl;   // scratch until the tile list is built
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-      if (b[h] >= 0) sorted[rank[h]] = b[h];
-    const int nvalid = __reduce_add_sync(0xffffffffu, (b[0] >= 0 ? 1 : 0) + (b[1] >= 0 ? 1 : 0));
-    __syncwarp();
-    if (lane == 0) {
-      int n = 0, ul[kMsaMaxTiles], fl[kMsaMaxTiles];
-      for (int i = 0; i < nvalid; ++i) {
-        const int blk = sorted[i];
-        // tile blk holds the block's positions from row `lead` on (bit 1)
-        if (n > 0 && ul[n - 1] == blk) fl[n - 1] |= 2;
-        else { ul[n] = blk; fl[n] = 2; ++n; }
-        // tile blk+1 holds its last `lead` positions in rows 0..lead-1 (bit 0)
-        if (lead > 0 && kMsaTile * (blk + 1) - lead <= pos) {
-          ul[n] = blk + 1;
-          fl[n] = 1;
-          ++n;
-        }
-      }
-      for (int i = 0; i < n; ++i) {
-        tile_u[i] = ul[i];
-        tile_fl[i] = fl[i];
-      }
-      *ntiles_sm = n;
-    }
+  // the first row's tile list is built while the barriers and tensor memory
+  // are set up (published on its barrier by thread 0 after the setup)
+  int first = row0;
+  while (first < p.T && p.row_pos[first] < 0) first += rstride;
+  if (warp == kMsaListWarp && first < p.T) {
+    const int n = msa_row_tiles(p.sel + static_cast<int64_t>(first) * p.K, p.K, p.row_pos[first],
+                                p.row_page_start[first] % p.BH, tile_u(0), tile_fl(0), p.err);
+    if (lane == 0) ntiles_sm[0] = n;
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < 3; ++s) {
@@ -435,81 +492,126 @@ __global__ void __launch_bounds__(kMsaThreads, 1) msa_attend_tc_kernel(const __g
       mbar_init(sempty(b), 8 / NGRP);   // one arrival per softmax warp that takes the buffer's steps
       mbar_init(pfull(b), 8 / NGRP);
       mbar_init(pempty(b), 1);
+      mbar_init(tfull(b), 1);
+      mbar_init(tempty(b), 2 + 8);      // the producer, the MMA thread and one lane per softmax warp
     }
     mbar_init(b_pvdone, 1);
     mbar_init(b_qfull, 1);
+    mbar_init(b_qempty, 1);
     *abort_flag = 0;
     fence_mbar_init();
+    if (first < p.T) mbar_arrive(tfull(0));
     tma_prefetch_desc(&p.tm_kv);
     tma_prefetch_desc(&p.tm_q);
   }
+  const int tiles_cols = 2 * NG + Hkv * NG;
   if (warp == 1) {
-    const int cols = 2 * NG + Hkv * NG;
-    tmem_alloc(smem_u32(tmem_slot), cols <= 32 ? 32 : cols <= 64 ? 64 : cols <= 128 ? 128 : cols <= 256 ? 256 : 512);
+    tmem_alloc(smem_u32(tmem_slot), tiles_cols <= 32 ? 32 : tiles_cols <= 64 ? 64 : tiles_cols <= 128 ? 128
+                                    : tiles_cols <= 256 ? 256 : 512);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int ntiles = *ntiles_sm;
-  const int nsteps = ntiles * Hkv;
-  const int tiles_cols = 2 * NG + Hkv * NG;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      mbar_arrive_expect_tx(b_qfull, static_cast<uint32_t>(Hkv * QG));
-      for (int g = 0; g < Hkv; ++g)
-        for (int c = 0; c < 2; ++c)
-          tma_load_2d(sbase + lay.off_q + g * QG + c * NG * 128, &p.tm_q, c * 64, row * p.Hq + g * p.group, b_qfull);
-    }
     const int nbox = kMsaTile / p.BH;
-    int issued_k = 0, issued_v = 0;
-    for (int t = 0; t < nsteps; ++t) {
-      const int ti = t / Hkv, g = t - ti * Hkv;
-      const int u = tile_u[ti];
-      const int st = t % S;
-      // lane b: box b of the tile (positions q0 .. q0+BH-1), loaded when it
-      // holds a position 0 .. pos and its page exists
-      int crow = -1;
-      if (lane < nbox) {
-        const int q0 = kMsaTile * u - lead + lane * p.BH;
-        if (q0 + p.BH - 1 >= 0 && q0 <= pos) {
-          const uint32_t slot = static_cast<uint32_t>(page_start - lead + kMsaTile * u + lane * p.BH);
-          const uint32_t pi = slot / static_cast<uint32_t>(p.P);
-          const int page = pi < static_cast<uint32_t>(npages) ? __ldg(p.pages + page_off + pi) : -1;
-          if (page < 0 || page >= p.num_pages) atomicOr(p.err, kErrBounds);
-          else crow = page * p.P + static_cast<int>(slot % static_cast<uint32_t>(p.P));
-        }
-      }
-      const uint32_t valid = __ballot_sync(0xffffffffu, crow >= 0);
-      const uint32_t bytes = __popc(valid) * p.BH * 128 * 2;
-      const uint32_t kst = sbase + st * STAGE, vst = kst + KVB;
-      // K once the stage's previous K has been read by its QK, V once its
-      // previous PV completed: the keys of a step run ahead of its values
-      bool ok = true;
-#pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        const uint32_t full = half ? vfull(st) : kfull(st);
-        if (lane == 0) ok = mbar_wait(half ? vempty(st) : kempty(st), ((t / S) & 1) ^ 1, abort_flag, p.err);
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
-        if (lane == 0) {
-          if (bytes) mbar_arrive_expect_tx(full, bytes);
-          else mbar_arrive(full);
-        }
-        __syncwarp();
-        if (crow >= 0) {
-          const uint32_t dst = (half ? vst : kst) + lane * p.BH * 128;
-          const int x0 = (half * Hkv + g) * 128;
-#pragma unroll
-          for (int c = 0; c < 2; ++c) tma_load_2d(dst + c * CH, &p.tm_kv, x0 + c * 64, crow, full);
-        }
-        if (half) issued_v = t + 1;
-        else issued_k = t + 1;
-      }
+    int issued_k = 0, issued_v = 0;   // global steps whose K / V loads went out
+    int gbase = 0;                    // global step of the row's first step
+    int j = 0;                        // rows taken so far
+    int nq = 0;                       // rows whose Q was loaded
+    bool ok = true;
+    for (int row = row0; row < p.T && ok; row += rstride) {
+      const int pos = p.row_pos[row];
+      if (pos < 0) continue;
+      const int page_start = p.row_page_start[row], page_off = p.row_page_off[row], npages = p.row_npages[row];
+      const int lead = page_start % p.BH;
+      const int buf = j & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(tfull(buf), (j >> 1) & 1, abort_flag, p.err));
+      ++j;
       if (!ok) break;
+      const int32_t *tu = tile_u(buf);
+      const int nsteps = ntiles_sm[buf] * Hkv;
+      bool qdone = false;
+      if (nsteps > 0 && nq == 0) {   // the first row's Q goes out ahead of its keys
+        if (lane == 0) {
+          mbar_arrive_expect_tx(b_qfull, static_cast<uint32_t>(Hkv * QG));
+          for (int gg = 0; gg < Hkv; ++gg)
+            for (int c = 0; c < 2; ++c)
+              tma_load_2d(sbase + lay.off_q + gg * QG + c * NG * 128, &p.tm_q, c * 64, row * p.Hq + gg * p.group,
+                          b_qfull);
+        }
+        ++nq;
+        qdone = true;
+      }
+      for (int ls = 0; ls < nsteps && ok; ++ls) {
+        const int t = gbase + ls;
+        const int ti = ls / Hkv, g = ls - ti * Hkv;
+        const int u = tu[ti];
+        const int st = t % S;
+        // lane b: box b of the tile (positions q0 .. q0+BH-1), loaded when it
+        // holds a position 0 .. pos and its page exists
+        int crow = -1;
+        if (lane < nbox) {
+          const int q0 = kMsaTile * u - lead + lane * p.BH;
+          if (q0 + p.BH - 1 >= 0 && q0 <= pos) {
+            const uint32_t slot = static_cast<uint32_t>(page_start - lead + kMsaTile * u + lane * p.BH);
+            const uint32_t pi = slot / static_cast<uint32_t>(p.P);
+            const int page = pi < static_cast<uint32_t>(npages) ? __ldg(p.pages + page_off + pi) : -1;
+            if (page < 0 || page >= p.num_pages) atomicOr(p.err, kErrBounds);
+            else crow = page * p.P + static_cast<int>(slot % static_cast<uint32_t>(p.P));
+          }
+        }
+        const uint32_t valid = __ballot_sync(0xffffffffu, crow >= 0);
+        const uint32_t bytes = __popc(valid) * p.BH * 128 * 2;
+        const uint32_t kst = sbase + st * STAGE, vst = kst + KVB;
+        // K once the stage's previous K has been read by its QK, V once its
+        // previous PV completed: the keys of a step run ahead of its values
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          const uint32_t full = half ? vfull(st) : kfull(st);
+          if (lane == 0) ok = mbar_wait(half ? vempty(st) : kempty(st), ((t / S) & 1) ^ 1, abort_flag, p.err);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) break;
+          if (lane == 0) {
+            if (bytes) mbar_arrive_expect_tx(full, bytes);
+            else mbar_arrive(full);
+          }
+          __syncwarp();
+          if (crow >= 0) {
+            const uint32_t dst = (half ? vst : kst) + lane * p.BH * 128;
+            const int x0 = (half * Hkv + g) * 128;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) tma_load_2d(dst + c * CH, &p.tm_kv, x0 + c * 64, crow, full);
+          }
+          if (half) {
+            issued_v = t + 1;
+          } else {
+            issued_k = t + 1;
+            if (ls == 0 && !qdone) {
+              // the row's Q, once the previous row's last QK has completed
+              if (lane == 0) {
+                if (nq > 0) ok = mbar_wait(b_qempty, (nq - 1) & 1, abort_flag, p.err);
+                if (ok) {
+                  mbar_arrive_expect_tx(b_qfull, static_cast<uint32_t>(Hkv * QG));
+                  for (int gg = 0; gg < Hkv; ++gg)
+                    for (int c = 0; c < 2; ++c)
+                      tma_load_2d(sbase + lay.off_q + gg * QG + c * NG * 128, &p.tm_q, c * 64,
+                                  row * p.Hq + gg * p.group, b_qfull);
+                }
+              }
+              ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+              ++nq;
+              if (!ok) break;
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty(buf));   // the row's list is no longer read here
+      gbase += nsteps;
     }
     // nothing of ours may still be landing when the CTA leaves: wait (bounded,
     // whatever the abort flag says) for the loads of the last stages issued
@@ -517,16 +619,14 @@ __global__ void __launch_bounds__(kMsaThreads, 1) msa_attend_tc_kernel(const __g
       volatile int no_abort = 0;
       for (int t = max(0, issued_k - S); t < issued_k; ++t) mbar_wait(kfull(t % S), (t / S) & 1, &no_abort, p.err);
       for (int t = max(0, issued_v - S); t < issued_v; ++t) mbar_wait(vfull(t % S), (t / S) & 1, &no_abort, p.err);
-      mbar_wait(b_qfull, 0, &no_abort, p.err);
+      if (nq > 0) mbar_wait(b_qfull, (nq - 1) & 1, &no_abort, p.err);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      bool ok = mbar_wait(b_qfull, 0, abort_flag, p.err);
-      auto issue_pv = [&](int t) {
+      auto issue_pv = [&](int t, int g, bool accumulate) {
         const int st = t % S;
-        const int ti = t / Hkv, g = t - ti * Hkv;
         const uint32_t vaddr = sbase + st * STAGE + KVB;
         const uint32_t paddr = sbase + lay.off_p + (t & 1) * PB;
 #pragma unroll
@@ -535,15 +635,14 @@ __global__ void __launch_bounds__(kMsaThreads, 1) msa_attend_tc_kernel(const __g
           // 8-token groups 1024 bytes apart; B = P^T, K-major
           const uint64_t ad = smem_desc(vaddr + k * 16 * 128, CH, 1024, kSwizzle128);
           const uint64_t bd = smem_desc(paddr + (k >> 2) * NG * 128 + (k & 3) * 32, 16, 1024, kSwizzle128);
-          mma_f16_ss(tmem_base + 2 * NG + g * NG, ad, bd, IDESC_PV, (ti > 0 || k > 0) ? 1u : 0u);
+          mma_f16_ss(tmem_base + 2 * NG + g * NG, ad, bd, IDESC_PV, (accumulate || k > 0) ? 1u : 0u);
         }
         mma_commit(vempty(st));
         mma_commit(pempty(t & 1));
         mma_commit(b_pvdone);
       };
-      auto issue_qk = [&](int t) {
+      auto issue_qk = [&](int t, int g) {
         const int st = t % S;
-        const int ti = t / Hkv, g = t - ti * Hkv;
         const uint32_t kaddr = sbase + st * STAGE;
         const uint32_t qaddr = sbase + lay.off_q + g * QG;
 #pragma unroll
@@ -555,25 +654,78 @@ __global__ void __launch_bounds__(kMsaThreads, 1) msa_attend_tc_kernel(const __g
         mma_commit(sfull(t & 1));
         mma_commit(kempty(st));
       };
-      // a polling issuer: PV of the oldest softmaxed step or QK of the next
-      // step, whichever is ready, PV first (it frees a V half and a P buffer)
-      int nq = 0, np = 0;
+      auto next_row = [&](int r) {
+        while (r < p.T && p.row_pos[r] < 0) r += rstride;
+        return r;
+      };
+      // Two cursors over the CTA's global steps, QK ahead and PV behind it.
+      // A cursor's row ends at a global step (q_end, p_end) known once the
+      // row's step count has been read from its tile list (the QK cursor
+      // waits for the list's barrier; `seen` lists so far; the PV cursor reads
+      // the count after that, and the list stays put until this thread has
+      // released it).  The ready tests compare steps only; row changes are
+      // taken when a cursor stands at its row's end.
+      int rq = next_row(row0), jq = 0, qrows = 0;
+      int rp = rq, jp = 0;
+      int seen = 0, nq = 0, np = 0;
+      int q_end = 0, p_end = 0, p_row0 = 0;   // (q_end, p_end: 0 until a row is known)
+      int gq = 0, gp = 0;                     // kv head of the next QK / PV
+      bool q_known = false, p_known = false, qready = false;
+      bool ok = true;
       uint32_t idle = 0;
       uint64_t idle_since = 0;
-      while (ok && np < nsteps) {
+      // a polling issuer: PV of the oldest softmaxed step or QK of the next
+      // step, whichever is ready, PV first (it frees a V half and a P buffer)
+      while (ok && rp < p.T) {
         bool progressed = false;
-        if (np < nq && mbar_test(pfull(np & 1), (np >> 1) & 1) && mbar_test(vfull(np % S), (np / S) & 1)) {
+        if (np < p_end && np < nq && mbar_test(pfull(np & 1), (np >> 1) & 1) && mbar_test(vfull(np % S), (np / S) & 1)) {
           tc_fence_after();
-          issue_pv(np);
+          issue_pv(np, gp, np - p_row0 >= Hkv);
           ++np;
+          gp = gp + 1 == Hkv ? 0 : gp + 1;
           progressed = true;
         }
-        if (nq < nsteps && mbar_test(kfull(nq % S), (nq / S) & 1) &&
+        if (nq < q_end && qready && mbar_test(kfull(nq % S), (nq / S) & 1) &&
             mbar_test(sempty(nq & 1), ((nq >> 1) & 1) ^ 1)) {
           tc_fence_after();
-          issue_qk(nq);
+          issue_qk(nq, gq);
           ++nq;
+          gq = gq + 1 == Hkv ? 0 : gq + 1;
+          if (nq == q_end) {
+            mma_commit(b_qempty);   // the row's Q may be replaced once its last QK completes
+            ++qrows;
+          }
           progressed = true;
+        }
+        if (!(q_known && nq < q_end) || !qready || !p_known || np == p_end) {
+          // row changes
+          if (q_known && nq == q_end) {
+            rq = next_row(rq + rstride);
+            ++jq;
+            q_known = false;
+            qready = false;
+          }
+          if (!q_known && rq < p.T && mbar_test(tfull(jq & 1), (jq >> 1) & 1)) {
+            q_end = nq + ntiles_sm[jq & 1] * Hkv;
+            gq = 0;
+            ++seen;
+            q_known = true;
+            progressed = true;
+          }
+          if (q_known && !qready && nq < q_end) qready = mbar_test(b_qfull, qrows & 1);
+          if (!p_known && jp < seen) {
+            p_row0 = np;
+            p_end = np + ntiles_sm[jp & 1] * Hkv;
+            gp = 0;
+            p_known = true;
+          }
+          if (p_known && np == p_end) {
+            mbar_arrive(tempty(jp & 1));
+            rp = next_row(rp + rstride);
+            ++jp;
+            p_known = false;
+            progressed = true;
+          }
         }
         if (progressed) {
           idle = 0;
@@ -595,6 +747,26 @@ __global__ void __launch_bounds__(kMsaThreads, 1) msa_attend_tc_kernel(const __g
       }
     }
     __syncwarp();
+  } else if (warp == kMsaListWarp) {
+    // ------------------------------------------------------------ tile lists
+    // The lists of the CTA's rows after the first, each into its row-parity
+    // buffer once every consumer has released that buffer's previous row:
+    // built up to two rows ahead, off the producer's path.
+    int j = 1;
+    for (int row = first + rstride; row < p.T; row += rstride) {
+      const int pos = p.row_pos[row];
+      if (pos < 0) continue;
+      const int buf = j & 1;
+      if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(tempty(buf), ((j >> 1) & 1) ^ 1, abort_flag, p.err))) break;
+      ++j;
+      const int n = msa_row_tiles(p.sel + static_cast<int64_t>(row) * p.K, p.K, pos, p.row_page_start[row] % p.BH,
+                                  tile_u(buf), tile_fl(buf), p.err);
+      if (lane == 0) {
+        ntiles_sm[buf] = n;
+        mbar_arrive(tfull(buf));
+      }
+      __syncwarp();
+    }
   } else {
     // ------------------------------------------------------------ softmax
     // Eight warps, two per TMEM lane quadrant.  NGRP = 1: warp half hf takes
@@ -618,222 +790,255 @@ __global__ void __launch_bounds__(kMsaThreads, 1) msa_attend_tc_kernel(const __g
     const int gt = et - grp * GTHREADS;   // thread within the group
     const uint32_t gbar = 1 + grp;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    for (int k = et; k < Hkv * NG; k += kMsaSoftThreads) {
-      m_sm[k] = kMsaNegBig;            // reference maxima, tile parity 0
-      m_sm[Hkv * NG + k] = kMsaNegBig; // tile parity 1
-      l_sm[k] = 0.f;
-    }
-    bool ok = !named_bar_any(3, kMsaSoftThreads, false);
-    bool carry = true;        // this warp's result of the previous step's last wait
-    float alpha_prev = 1.f;   // (gt < NG) alpha of head gt at the group's previous step
-    int g_prev = 0;
-    int t_last = -1;          // the group's last step
-    for (int t = grp; t < nsteps && ok; t += NGRP) {
-      const int lt = t / NGRP;            // the group's own step count
-      const int ti = t / Hkv, g = t - ti * Hkv;
-      const int u = tile_u[ti], fl = tile_fl[ti];
-      const int q = kMsaTile * u - lead + i;
-      const bool valid = q >= 0 && q <= pos && ((i < lead) ? (fl & 1) : (fl & 2));
-      uint32_t *rmax = redmax + (grp * 2 + (lt & 1)) * 8 * NG;
-      float *rsum = redsum + (grp * 2 + (lt & 1)) * 8 * NG;
-      bool good = carry && __all_sync(0xffffffffu, mbar_wait(sfull(t & 1), (t >> 1) & 1, abort_flag, p.err));
+    bool ok = true;
+    int j = 0, gbase = 0;
+    // the row whose output is still to be written (at the next row's start,
+    // overlapping that row's first QK): its row, its l buffer and the
+    // group's last step in it
+    const uint32_t ocol = tmem_base + lane_base + 2 * NG + h0;   // O of kv head 0, this warp's heads
+    int pend_row = -1, pend_buf = 0, pend_tlast = -1;
+    auto flush = [&](bool wait_pv) {   // writes the pending row's output
+      bool pg = true;
+      if (wait_pv && pend_tlast >= 0) pg = __all_sync(0xffffffffu, mbar_wait(pempty(pend_tlast & 1), (pend_tlast >> 1) & 1, abort_flag, p.err));
       tc_fence_after();
-      float s[NH];
-      if (good) {
-        if constexpr (NH == 8) {
-          tmem_ld8(tmem_base + lane_base + (t & 1) * NG + h0, s);
-        } else {
-#pragma unroll
-          for (int c0 = 0; c0 < NH; c0 += 16)
-            tmem_ld16(tmem_base + lane_base + (t & 1) * NG + h0 + c0, *reinterpret_cast<float(*)[16]>(s + c0));
-        }
-        tmem_ld_wait();
-      }
+      if (pg)
+        msa_write_out<NG, NGRP, NH>(ocol, l_sm + pend_buf * Hkv * NG, Hkv, grp, h0, p.group,
+                                    p.out + static_cast<int64_t>(pend_row) * p.Hq * 128, i);
       tc_fence_before();
-      __syncwarp();
-      if (good && lane == 0) mbar_arrive(sempty(t & 1));
-      // each head's largest logit over this warp's 32 rows of the tile (as an
-      // order key; masked rows count as -inf), by the transposing reduction
-      {
-        float mx[NH];
-#pragma unroll
-        for (int h = 0; h < NH; ++h) mx[h] = valid ? s[h] : -INFINITY;
-        if constexpr (NH <= 16) {
-          const float m = warp_reduce_transpose<NH>(mx, MaxOp{});   // lane l holds head (l >> (5 - log2 NH))
-          constexpr int SHIFT = NH == 8 ? 2 : 1;
-          if ((lane & ((1 << SHIFT) - 1)) == 0) rmax[(h0 + (lane >> SHIFT)) * 4 + quad] = score_key(m);
-        } else {
-#pragma unroll
-          for (int c0 = 0; c0 < NH; c0 += 32) {
-            const float m = warp_reduce_transpose<32>(*reinterpret_cast<float(*)[32]>(mx + c0), MaxOp{});
-            rmax[(h0 + c0 + lane) * 4 + quad] = score_key(m);
-          }
-        }
+      pend_row = -1;
+      return pg;
+    };
+    // the next row's position and first slot are loaded a row ahead
+    int pos_n = row0 < p.T ? p.row_pos[row0] : -1, ps_n = row0 < p.T ? p.row_page_start[row0] : 0;
+    auto prefetch = [&](int r) {
+      if (r < p.T) {
+        pos_n = p.row_pos[r];
+        ps_n = p.row_page_start[r];
+      }
+    };
+    for (int row = row0; row < p.T && ok; row += rstride) {
+      const int pos = pos_n, lead = ps_n % p.BH;
+      if (pos < 0) {
+        prefetch(row + rstride);
+        continue;
+      }
+      const int buf = j & 1;
+      bool good = __all_sync(0xffffffffu, mbar_wait(tfull(buf), (j >> 1) & 1, abort_flag, p.err));
+      ++j;
+      const int nsteps = (good ? ntiles_sm[buf] : 0) * Hkv;
+      const int32_t *tu = tile_u(buf), *tf = tile_fl(buf);
+      float *l_row = l_sm + buf * Hkv * NG;
+      // the group's softmax state starts afresh (every reader of the previous
+      // row's passed the barrier that ended that row)
+      for (int k = gt; k < Hkv * NG; k += GTHREADS) {
+        if ((k / NG) % NGRP != grp) continue;
+        m_sm[k] = kMsaNegBig;            // reference maxima, tile parity 0
+        m_sm[Hkv * NG + k] = kMsaNegBig; // tile parity 1
+        l_row[k] = 0.f;
       }
       if (named_bar_any(gbar, GTHREADS, !good)) {
         ok = false;
         break;
       }
-      // the group's previous step's sums (its barrier has passed in every warp of the group)
-      if (lt > 0 && gt < NG) {
-        const float4 ps = reinterpret_cast<const float4 *>(redsum + (grp * 2 + ((lt - 1) & 1)) * 8 * NG)[gt];
-        l_sm[g_prev * NG + gt] = l_sm[g_prev * NG + gt] * alpha_prev + ((ps.x + ps.y) + (ps.z + ps.w));
-      }
-      const float *mold_sm = m_sm + ((ti & 1) ^ 1) * Hkv * NG + g * NG;   // written at the group's previous tile
-      float *mnew_sm = m_sm + (ti & 1) * Hkv * NG + g * NG;
-      // reference max of head h for this step (every thread that needs a
-      // head derives the same value from the same shared data)
-      auto head_max = [&](int h, float &alpha) -> float {
-        const uint4 k4 = reinterpret_cast<const uint4 *>(rmax)[h];
-        const uint32_t k = max(max(k4.x, k4.y), max(k4.z, k4.w));
-        const float mold = mold_sm[h];
-        // (a tile always holds a kept position, so k is a real score: a
-        // quadrant with none gives the key of -inf, below every score)
-        const float tmax = key_score(k) * p.scale_log2;
-        alpha = 1.f;
-        if (tmax > mold + kMsaRescale) {
-          alpha = fast_exp2(mold - tmax);
-          return tmax;
-        }
-        return mold;
-      };
-      float alpha[NH], mnew[NH];
-      bool rescale = false;
-#pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        mnew[h] = head_max(h0 + h, alpha[h]);
-        rescale = rescale || alpha[h] != 1.f;
-      }
-      if (gt < NG) {
-        float a;
-        mnew_sm[gt] = head_max(gt, a);
-        alpha_prev = a;
-        g_prev = g;
-      }
-      t_last = t;
-      // P (bf16) and the tile's per-head sums of what PV will add
-#pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        const float e = valid ? fast_exp2(fmaf(s[h], p.scale_log2, -mnew[h])) : 0.f;
-        s[h] = __bfloat162float(__float2bfloat16_rn(e));
-      }
-      if constexpr (NH <= 16) {
-        const float sum = warp_sum_transpose<NH>(s);   // lane l holds head (l >> (5 - log2 NH))
-        constexpr int SHIFT = NH == 8 ? 2 : 1;
-        if ((lane & ((1 << SHIFT) - 1)) == 0) rsum[(h0 + (lane >> SHIFT)) * 4 + quad] = sum;
-      } else {
-#pragma unroll
-        for (int c0 = 0; c0 < NH; c0 += 32) {
-          const float sum = warp_sum_transpose<32>(*reinterpret_cast<float(*)[32]>(s + c0));   // lane h: head h
-          rsum[(h0 + c0 + lane) * 4 + quad] = sum;
-        }
-      }
-      // P^T buffer (t & 1) is free once PV(t-2) completed (with NGRP = 2 that
-      // wait also orders the O rescale below after every earlier PV into O)
-      good = __all_sync(0xffffffffu, mbar_wait(pempty(t & 1), ((t >> 1) & 1) ^ 1, abort_flag, p.err));
-      tc_fence_after();
-      if (good) {
-        const uint32_t pbase = sbase + lay.off_p + (t & 1) * PB + (i >> 6) * NG * 128 + ((i & 7) << 1);
-        const uint32_t c8 = (i & 63) >> 3;
-#pragma unroll
-        for (int h = 0; h < NH; ++h) {
-          const int hh = h0 + h;
-          const uint32_t a = pbase + hh * 128 + ((c8 ^ (hh & 7)) << 4);
-          const __nv_bfloat16 pb = __float2bfloat16_rn(s[h]);
-          asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"(*reinterpret_cast<const uint16_t *>(&pb)) : "memory");
-        }
-      }
-      // V rows of positions outside the kept blocks are zeroed once the tile
-      // has landed (a zero probability must not meet a stale value); with
-      // NGRP = 1, warp half hf zeroes 64-column chunk hf
-      if (good && __any_sync(0xffffffffu, !valid)) {
-        const int st = t % S;
-        good = __all_sync(0xffffffffu, mbar_wait(vfull(st), (t / S) & 1, abort_flag, p.err));
-        if (good && !valid) {
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            if (NGRP == 1 && c != hf) continue;
-            const uint32_t vrow = sbase + st * STAGE + KVB + c * CH + i * 128;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) st_shared_v4(vrow + k * 16, make_uint4(0u, 0u, 0u, 0u));
-          }
-        }
-      }
-      fence_proxy_async_smem();
-      // O of this kv head (this warp's head columns) is rescaled once every
-      // earlier PV into it has completed (its first tile has no O yet).  With
-      // NGRP = 2 that is PV(t-2), already waited for above (PV(t-1) belongs
-      // to another kv head); with NGRP = 1 it is PV(t-1).
-      if (good && __any_sync(0xffffffffu, rescale) && ti > 0) {
-        if (NGRP == 1) {
-          good = __all_sync(0xffffffffu, mbar_wait(b_pvdone, (t - 1) & 1, abort_flag, p.err));
-          tc_fence_after();
-        }
+      // (loaded after the barrier: a load still in flight holds its thread
+      // at the next one)
+      prefetch(row + rstride);
+      // the previous row's output, while this row's first QK is on its way:
+      // its last PV first (no P of this row is written yet, so the wait on
+      // that PV's P buffer names it exactly)
+      if (pend_row >= 0) ok = flush(true);
+      bool carry = true;        // this warp's result of the previous step's last wait
+      float alpha_prev = 1.f;   // (gt < NG) alpha of head gt at the group's previous step of the row
+      int g_prev = 0;
+      int t_last = -1;          // the group's last step of the row
+      for (int ls = grp, lr = 0; ls < nsteps && ok; ls += NGRP, ++lr) {
+        const int t = gbase + ls;           // global step (gbase is even when NGRP = 2)
+        const int lt = t / NGRP;            // the group's own step count
+        const int ti = ls / Hkv, g = ls - ti * Hkv;
+        const int u = tu[ti], fl = tf[ti];
+        const int q = kMsaTile * u - lead + i;
+        const bool valid = q >= 0 && q <= pos && ((i < lead) ? (fl & 1) : (fl & 2));
+        uint32_t *rmax = redmax + (grp * 2 + (lt & 1)) * 8 * NG;
+        float *rsum = redsum + (grp * 2 + (lt & 1)) * 8 * NG;
+        good = carry && __all_sync(0xffffffffu, mbar_wait(sfull(t & 1), (t >> 1) & 1, abort_flag, p.err));
+        tc_fence_after();
+        float s[NH];
         if (good) {
-          const uint32_t oaddr = tmem_base + lane_base + 2 * NG + g * NG + h0;
           if constexpr (NH == 8) {
-            float o[8];
-            tmem_ld8(oaddr, o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int k = 0; k < 8; ++k) o[k] *= alpha[k];
-            tmem_st8(oaddr, o);
+            tmem_ld8(tmem_base + lane_base + (t & 1) * NG + h0, s);
           } else {
 #pragma unroll
-            for (int c0 = 0; c0 < NH; c0 += 16) {
-              float o[16];
-              tmem_ld16(oaddr + c0, o);
-              tmem_ld_wait();
+            for (int c0 = 0; c0 < NH; c0 += 16)
+              tmem_ld16(tmem_base + lane_base + (t & 1) * NG + h0 + c0, *reinterpret_cast<float(*)[16]>(s + c0));
+          }
+          tmem_ld_wait();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (good && lane == 0) mbar_arrive(sempty(t & 1));
+        // each head's largest logit over this warp's 32 rows of the tile (as an
+        // order key; masked rows count as -inf), by the transposing reduction
+        {
+          float mx[NH];
 #pragma unroll
-              for (int k = 0; k < 16; ++k) o[k] *= alpha[c0 + k];
-              tmem_st16(oaddr + c0, o);
+          for (int h = 0; h < NH; ++h) mx[h] = valid ? s[h] : -INFINITY;
+          if constexpr (NH <= 16) {
+            const float m = warp_reduce_transpose<NH>(mx, MaxOp{});   // lane l holds head (l >> (5 - log2 NH))
+            constexpr int SHIFT = NH == 8 ? 2 : 1;
+            if ((lane & ((1 << SHIFT) - 1)) == 0) rmax[(h0 + (lane >> SHIFT)) * 4 + quad] = score_key(m);
+          } else {
+#pragma unroll
+            for (int c0 = 0; c0 < NH; c0 += 32) {
+              const float m = warp_reduce_transpose<32>(*reinterpret_cast<float(*)[32]>(mx + c0), MaxOp{});
+              rmax[(h0 + c0 + lane) * 4 + quad] = score_key(m);
             }
           }
-          tmem_st_wait();
         }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (good && lane == 0) mbar_arrive(pfull(t & 1));
-      carry = good;
-    }
-    // every PV has completed before O is read: first the group's own last PV
-    // (the P buffer's barrier counts only that buffer's PVs, so its parity
-    // names that PV exactly), which leaves at most the very last PV of the
-    // row outstanding, then that one on the shared barrier (a parity wait on
-    // a barrier that could still be two phases short would pass early)
-    if (ok && carry && t_last >= 0)
-      carry = __all_sync(0xffffffffu, mbar_wait(pempty(t_last & 1), (t_last >> 1) & 1, abort_flag, p.err));
-    if (ok && carry && nsteps > 0)
-      carry = __all_sync(0xffffffffu, mbar_wait(b_pvdone, (nsteps - 1) & 1, abort_flag, p.err));
-    tc_fence_after();
-    ok = !named_bar_any(gbar, GTHREADS, !(ok && carry));   // the group's last sums are in place
-    if (ok && t_last >= 0 && gt < NG) {
-      const float4 ps = reinterpret_cast<const float4 *>(redsum + (grp * 2 + ((t_last / NGRP) & 1)) * 8 * NG)[gt];
-      l_sm[g_prev * NG + gt] = l_sm[g_prev * NG + gt] * alpha_prev + ((ps.x + ps.y) + (ps.z + ps.w));
-    }
-    ok = !named_bar_any(gbar, GTHREADS, !ok);   // every l of the group's kv heads is final
-    if (ok) {
-      for (int g = grp; g < Hkv; g += NGRP) {
-        const uint32_t oaddr = tmem_base + lane_base + 2 * NG + g * NG + h0;
-        float o[NH];
-        if constexpr (NH == 8) {
-          tmem_ld8(oaddr, o);
+        if (named_bar_any(gbar, GTHREADS, !good)) {
+          ok = false;
+          break;
+        }
+        // the group's previous step's sums (its barrier has passed in every warp of the group)
+        if (lr > 0 && gt < NG) {
+          const float4 ps = reinterpret_cast<const float4 *>(redsum + (grp * 2 + ((lt - 1) & 1)) * 8 * NG)[gt];
+          l_row[g_prev * NG + gt] = l_row[g_prev * NG + gt] * alpha_prev + ((ps.x + ps.y) + (ps.z + ps.w));
+        }
+        const float *mold_sm = m_sm + ((ti & 1) ^ 1) * Hkv * NG + g * NG;   // written at the group's previous tile
+        float *mnew_sm = m_sm + (ti & 1) * Hkv * NG + g * NG;
+        // reference max of head h for this step (every thread that needs a
+        // head derives the same value from the same shared data)
+        auto head_max = [&](int h, float &alpha) -> float {
+          const uint4 k4 = reinterpret_cast<const uint4 *>(rmax)[h];
+          const uint32_t k = max(max(k4.x, k4.y), max(k4.z, k4.w));
+          const float mold = mold_sm[h];
+          // (a tile always holds a kept position, so k is a real score: a
+          // quadrant with none gives the key of -inf, below every score)
+          const float tmax = key_score(k) * p.scale_log2;
+          alpha = 1.f;
+          if (tmax > mold + kMsaRescale) {
+            alpha = fast_exp2(mold - tmax);
+            return tmax;
+          }
+          return mold;
+        };
+        float alpha[NH], mnew[NH];
+        bool rescale = false;
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          mnew[h] = head_max(h0 + h, alpha[h]);
+          rescale = rescale || alpha[h] != 1.f;
+        }
+        if (gt < NG) {
+          float a;
+          mnew_sm[gt] = head_max(gt, a);
+          alpha_prev = a;
+          g_prev = g;
+        }
+        t_last = t;
+        // P (bf16) and the tile's per-head sums of what PV will add
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          const float e = valid ? fast_exp2(fmaf(s[h], p.scale_log2, -mnew[h])) : 0.f;
+          s[h] = __bfloat162float(__float2bfloat16_rn(e));
+        }
+        if constexpr (NH <= 16) {
+          const float sum = warp_sum_transpose<NH>(s);   // lane l holds head (l >> (5 - log2 NH))
+          constexpr int SHIFT = NH == 8 ? 2 : 1;
+          if ((lane & ((1 << SHIFT) - 1)) == 0) rsum[(h0 + (lane >> SHIFT)) * 4 + quad] = sum;
         } else {
 #pragma unroll
-          for (int c0 = 0; c0 < NH; c0 += 16) tmem_ld16(oaddr + c0, *reinterpret_cast<float(*)[16]>(o + c0));
+          for (int c0 = 0; c0 < NH; c0 += 32) {
+            const float sum = warp_sum_transpose<32>(*reinterpret_cast<float(*)[32]>(s + c0));   // lane h: head h
+            rsum[(h0 + c0 + lane) * 4 + quad] = sum;
+          }
         }
-        tmem_ld_wait();
+        // P^T buffer (t & 1) is free once PV(t-2) completed (with NGRP = 2 that
+        // wait also orders the O rescale below after every earlier PV into O)
+        good = __all_sync(0xffffffffu, mbar_wait(pempty(t & 1), ((t >> 1) & 1) ^ 1, abort_flag, p.err));
+        tc_fence_after();
+        if (good) {
+          const uint32_t pbase = sbase + lay.off_p + (t & 1) * PB + (i >> 6) * NG * 128 + ((i & 7) << 1);
+          const uint32_t c8 = (i & 63) >> 3;
 #pragma unroll
-        for (int k = 0; k < NH; ++k) {
-          const int h = h0 + k;
-          if (h >= p.group) continue;
-          const float l = l_sm[g * NG + h];
-          p.out[(static_cast<int64_t>(row) * p.Hq + g * p.group + h) * 128 + i] =
-              __float2bfloat16_rn(l > 0.f ? o[k] / l : 0.f);
+          for (int h = 0; h < NH; ++h) {
+            const int hh = h0 + h;
+            const uint32_t a = pbase + hh * 128 + ((c8 ^ (hh & 7)) << 4);
+            const __nv_bfloat16 pb = __float2bfloat16_rn(s[h]);
+            asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"(*reinterpret_cast<const uint16_t *>(&pb)) : "memory");
+          }
         }
+        // V rows of positions outside the kept blocks are zeroed once the tile
+        // has landed (a zero probability must not meet a stale value); with
+        // NGRP = 1, warp half hf zeroes 64-column chunk hf
+        if (good && __any_sync(0xffffffffu, !valid)) {
+          const int st = t % S;
+          good = __all_sync(0xffffffffu, mbar_wait(vfull(st), (t / S) & 1, abort_flag, p.err));
+          if (good && !valid) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              if (NGRP == 1 && c != hf) continue;
+              const uint32_t vrow = sbase + st * STAGE + KVB + c * CH + i * 128;
+#pragma unroll
+              for (int k = 0; k < 8; ++k) st_shared_v4(vrow + k * 16, make_uint4(0u, 0u, 0u, 0u));
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        // O of this kv head (this warp's head columns) is rescaled once every
+        // earlier PV into it has completed (its first tile has no O yet).  With
+        // NGRP = 2 that is PV(t-2), already waited for above (PV(t-1) belongs
+        // to another kv head); with NGRP = 1 it is PV(t-1) (the wait above has
+        // PV(t-2) complete, so the parity wait cannot pass two phases short).
+        if (good && __any_sync(0xffffffffu, rescale) && ti > 0) {
+          if (NGRP == 1) {
+            good = __all_sync(0xffffffffu, mbar_wait(b_pvdone, (t - 1) & 1, abort_flag, p.err));
+            tc_fence_after();
+          }
+          if (good) {
+            const uint32_t oaddr = ocol + g * NG;
+            if constexpr (NH == 8) {
+              float o[8];
+              tmem_ld8(oaddr, o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int k = 0; k < 8; ++k) o[k] *= alpha[k];
+              tmem_st8(oaddr, o);
+            } else {
+#pragma unroll
+              for (int c0 = 0; c0 < NH; c0 += 16) {
+                float o[16];
+                tmem_ld16(oaddr + c0, o);
+                tmem_ld_wait();
+#pragma unroll
+                for (int k = 0; k < 16; ++k) o[k] *= alpha[c0 + k];
+                tmem_st16(oaddr + c0, o);
+              }
+            }
+            tmem_st_wait();
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (good && lane == 0) mbar_arrive(pfull(t & 1));
+        carry = good;
       }
+      // the row's last sums into l; its output is written at the start of the
+      // next row (or after the last one)
+      ok = !named_bar_any(gbar, GTHREADS, !(ok && carry));   // the group's last sums are in place
+      if (ok && t_last >= 0 && gt < NG) {
+        const float4 ps = reinterpret_cast<const float4 *>(redsum + (grp * 2 + ((t_last / NGRP) & 1)) * 8 * NG)[gt];
+        l_row[g_prev * NG + gt] = l_row[g_prev * NG + gt] * alpha_prev + ((ps.x + ps.y) + (ps.z + ps.w));
+      }
+      pend_row = row;
+      pend_buf = buf;
+      pend_tlast = t_last;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty(buf));
+      gbase += nsteps;
     }
+    // the CTA's last row (its sums were folded before the group's last barrier)
+    ok = !named_bar_any(gbar, GTHREADS, !ok);
+    if (ok && pend_row >= 0) flush(true);
   }
 
   tc_fence_before();
@@ -948,6 +1153,7 @@ cudaError_t run_msa_tc(const dsa_ctx *ctx, const dsa_plan_t *plan, const dsa_msa
   prm.pages = plan->pages;
   prm.out = static_cast<__nv_bfloat16 *>(out);
   prm.err = ctx->err;
+  prm.T = plan->T;
   prm.Hq = ms.q_heads;
   prm.Hkv = ms.kv_heads;
   prm.group = ms.q_heads / ms.kv_heads;
@@ -962,7 +1168,8 @@ cudaError_t run_msa_tc(const dsa_ctx *ctx, const dsa_plan_t *plan, const dsa_msa
   // the limit is set to the largest layout this instance can have
   static std::atomic<uint64_t> smem_limit_set{0};
   if (cudaError_t e = ensure_smem_limit(kern, 227 * 1024, ctx->device, smem_limit_set); e != cudaSuccess) return e;
-  kern<<<plan->T, kMsaThreads, bytes, s>>>(prm);
+  // persistent: one CTA per SM (the layout fills shared memory), rows strided over the grid
+  kern<<<std::min(plan->T, std::max(1, ctx->num_sms)), kMsaThreads, bytes, s>>>(prm);
   return cudaGetLastError();
 }
 

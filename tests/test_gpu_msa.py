@@ -88,6 +88,25 @@ def test_msa_more_heads_per_group_and_one_kv_head():
         _run(wl)
 
 
+@pytest.mark.parametrize("q_heads,kv_heads,page_start",
+                         [(8, 2, 0), (32, 1, [13, 0, 70, 101, 3]), (16, 4, [5, 37, 0, 64, 0]),
+                          (40, 2, [0, 9, 0, 0, 77])])
+def test_msa_rows_walked_by_persistent_ctas(q_heads, kv_heads, page_start):
+    """541 rows, more than the SMs: each CTA of the persistent grid walks three
+    or four rows (its two tile-list buffers reused, the next row's Q and
+    loads overlapping the current row's tail, each row's output written
+    during the next row when two O buffers fit, at the row's end otherwise),
+    with one or two softmax groups (odd and even kv head counts), rows of a
+    single tile (one step per group) and token 0 on and off the box
+    boundary; every row against the oracle."""
+    ms = W.MSAShape(topk_blocks=4, q_heads=q_heads, kv_heads=kv_heads)
+    reqs = [(600, 200), (900, 150), (1499, 1), (300, 60), (0, 130)]
+    wl = W.build_workload("msa_rows", ms.index_shape(), reqs, 2110 + kv_heads,
+                          W.Distributions(w=("uniform", 0.0, 1.0 / 8)), page_start=page_start)
+    wl.msa = ms
+    _run(wl)
+
+
 @pytest.mark.parametrize("page_start,block_size", [(0, 128), ([5, 37, 70, 101], 128), ([3, 0, 63, 29], 64)])
 def test_msa_block_maxima_from_the_indexer_epilogue(page_start, block_size):
     """Decode-only steps take the indexer's block-maximum epilogue (no token
