@@ -5,11 +5,15 @@
 //
 // CTAs select one row at a time: 1024 threads with a row each when a step
 // has at most one row per SM, else 512-thread CTAs, two per SM, taking rows
-// in turn.  Scores are mapped to order-preserving 32-bit keys (-0.0
+// in turn, or, for many rows of at most kShortRow keys, 256-thread CTAs, four
+// per SM, with a quarter of the shared memory (candidate, sample and bitmap
+// capacities halved or quartered): a row's phases are latency-bound, so more
+// rows in flight per SM is what shortens the step.  Scores are mapped to order-preserving 32-bit keys (-0.0
 // ranks as +0.0).  The selection is exact; only the amount of work depends on
 // the data:
 //   1. candidates: a row with at most kCandCap keys takes all of them.  A
-//      longer row takes an evenly strided sample (4096..8191 keys) into shared
+//      longer row takes an evenly strided sample (kSampleMin..2 kSampleMin-1
+//      keys: 4096 for 512 threads and up, 1024 for 256) into shared
 //      memory, finds (to within a 2^10-key bin, below it) the sample key
 //      whose rank, scaled by the stride, lies a safe margin above topk, and
 //      keeps every key of the row at or above that bound (one pass over the
@@ -39,24 +43,33 @@ namespace dsa {
 namespace {
 
 // CTA sizes: 1024 threads, one CTA per SM, when every row has its own CTA;
-// 512 threads, two per SM, when persistent CTAs take several rows each
+// 512 threads, two per SM, when persistent CTAs take several rows each; 256
+// threads, four per SM, for many rows of at most kShortRow keys
 constexpr int kMaxWarps = 32;
 constexpr int kBatch = 16;            // independent loads in flight per thread
 constexpr int kScanBatch4 = 8;        // float4 loads in flight per thread in the candidate pass
-constexpr int kCandCap = 8192;        // candidate keys held in shared memory
-constexpr int kSampleMin = 4096;      // a strided sample holds kSampleMin .. 2*kSampleMin-1 keys
-constexpr int kBitmapWords = 8192;    // 262,144 positions
 constexpr int kTieCap = 2048;         // tau ties ranked by position in shared memory
+constexpr int kShortRow = 32768;      // longest row the 256-thread CTAs take
+// Shared-memory capacities by CTA size: candidate keys held, the strided
+// sample's minimum (it holds kSampleMin .. 2*kSampleMin-1 keys) and the
+// position bitmap's words.  At 256 threads a row of up to kShortRow keys
+// leaves ~1.15 topk + 3 sigma candidates (<= 3.4K at topk 2048) under the cap.
+template <int NT>
+struct TopkCaps {
+  static constexpr int kCandCap = NT >= 512 ? 8192 : 4096;
+  static constexpr int kSampleMin = NT >= 512 ? 4096 : 1024;
+  static constexpr int kBitmapWords = NT >= 512 ? 8192 : 2048;   // 262,144 or 65,536 positions
+};
 
 template <int NT>
 struct TopkSmem {
   static constexpr int kWarps = NT / 32;
   union {
-    uint32_t sample[2 * kSampleMin];
-    uint32_t bits[kBitmapWords];
+    uint32_t sample[2 * TopkCaps<NT>::kSampleMin];
+    uint32_t bits[TopkCaps<NT>::kBitmapWords];
   };
-  uint32_t ckey[kCandCap];
-  int32_t cpos[kCandCap];
+  uint32_t ckey[TopkCaps<NT>::kCandCap];
+  int32_t cpos[TopkCaps<NT>::kCandCap];
   int hist[2048];                     // radix histograms; tie positions during output
   int ws[kWarps];
   int res[2];
@@ -183,6 +196,9 @@ __device__ __forceinline__ void select_row(const float *__restrict__ scores, con
                                            int row, TopkSmem<NT> &sm) {
   constexpr int kTopkThreads = NT;
   constexpr int kTopkWarps = NT / 32;
+  constexpr int kCandCap = TopkCaps<NT>::kCandCap;
+  constexpr int kSampleMin = TopkCaps<NT>::kSampleMin;
+  constexpr int kBitmapWords = TopkCaps<NT>::kBitmapWords;
   const int n = row_pos[row] + 1;
   int32_t *out = sel + static_cast<int64_t>(row) * K;
   if (n <= K) {
@@ -458,10 +474,14 @@ cudaError_t run_topk(int device, const float *scores, const int64_t *row_score_o
 cudaError_t launch_topk(const dsa_ctx *ctx, const dsa_plan_t *plan, const float *scores, int32_t *sel,
                         cudaStream_t s, int32_t *launches) {
   // up to one row per SM: 1024-thread CTAs, one row each; more rows: 512-thread
-  // CTAs, two per SM, each taking rows in turn
+  // CTAs, two per SM, each taking rows in turn; many rows (more than two per
+  // SM) of at most kShortRow keys: 256-thread CTAs, four per SM
   cudaError_t e;
   if (plan->T <= ctx->num_sms)
     e = run_topk<1024>(ctx->device, scores, plan->row_score_off, plan->row_pos, plan->T, ctx->cfg.topk, sel, std::max(1, plan->T), s);
+  else if (plan->T > 2 * ctx->num_sms && static_cast<int64_t>(plan->max_pos) + 1 <= kShortRow)
+    e = run_topk<256>(ctx->device, scores, plan->row_score_off, plan->row_pos, plan->T, ctx->cfg.topk, sel,
+                      std::min(plan->T, 4 * ctx->num_sms), s);
   else
     e = run_topk<512>(ctx->device, scores, plan->row_score_off, plan->row_pos, plan->T, ctx->cfg.topk, sel,
                       std::min(plan->T, 2 * ctx->num_sms), s);

@@ -220,6 +220,45 @@ def test_topk_many_rows_per_cta():
     H.check_selection(g, ref, sc, off, sh.topk, exact=True)
 
 
+def test_topk_many_short_rows_four_ctas_per_sm():
+    """More rows than two per SM, none longer than 32,768 keys: the selection
+    runs 256-thread CTAs, four per SM, with the smaller shared-memory
+    capacities (4,096 candidates, a 1,024-key sample, a 65,536-position
+    bitmap).  Rows of every path: fewer keys than topk, every key a candidate,
+    a strided sample, a sample the data fools, and threshold ties below, equal
+    to and above what the tie ranking holds."""
+    sh = W.DSAShape(**W.DEEPSEEK)
+    rng = np.random.default_rng(17)
+    rows = []
+    rows += [rng.standard_normal(int(n)).astype(np.float32) for n in rng.integers(100, 2048, size=20)]
+    rows += [rng.standard_normal(int(n)).astype(np.float32) for n in rng.integers(2049, 4096, size=120)]
+    rows += [rng.standard_normal(int(n)).astype(np.float32) for n in rng.integers(4097, 32768, size=200)]
+    rows.append(rng.standard_normal(32768).astype(np.float32))
+    for _ in range(8):
+        fool = (rng.random(30000) * 10 + 1).astype(np.float32)
+        fool[:: 30000 // 1024] = 0.0                                              # the sample sees only zeros
+        rows.append(fool)
+    for n_tie, n_top in ((3000, 1000), (1500, 1000), (1048, 1000)) * 4:        # ties > cap, <= cap, == need
+        r = (rng.random(20000) * 0.5).astype(np.float32)
+        idx = rng.permutation(20000)
+        r[idx[:n_top]] = (2.0 + rng.random(n_top)).astype(np.float32)
+        r[idx[n_top:n_top + n_tie]] = 1.0
+        rows.append(r)
+    order = rng.permutation(len(rows))
+    rows = [rows[i] for i in order]
+    assert len(rows) > 2 * 152 and max(len(r) for r in rows) <= 32768
+    wl = W.build_workload("topk_short", sh, [(len(r) - 1, 1) for r in rows], seed=18)
+    off = np.zeros(len(rows) + 1, np.int64)
+    off[1:] = np.cumsum([len(r) for r in rows])
+    sc = np.concatenate(rows)
+    ref = oracle.topk(sh, wl.spans, sc, off)
+    ctx = dsa.Context(sh, 0)
+    plan = ctx.plan(wl.spans, wl.num_pages)
+    g = ctx.topk_from_scores(plan, torch.from_numpy(sc).cuda()).cpu().numpy()
+    ctx.get_error()
+    H.check_selection(g, ref, sc, off, sh.topk, exact=True)
+
+
 def test_quantize_on_store_bit_exact():
     """bf16 rows quantised into the 132-byte index rows and 656-byte latent rows
     give the oracle's bytes exactly (scales, codes, ties to even, saturation,
