@@ -830,7 +830,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
 constexpr int kCombHeads = 8;
 constexpr int kCombThreads = 256;
 
-__global__ void __launch_bounds__(kCombThreads) attend_combine_kernel(const AttCombine *__restrict__ combine,
+__global__ void __launch_bounds__(kCombThreads, 4) attend_combine_kernel(const AttCombine *__restrict__ combine,
                                                                      const float *__restrict__ opart,
                                                                      const float *__restrict__ mlpart,
                                                                      const float *__restrict__ sink,
@@ -846,6 +846,55 @@ __global__ void __launch_bounds__(kCombThreads) attend_combine_kernel(const AttC
     const int h0 = (w % hb) * kCombHeads;
     if (cb.row < 0) continue;   // padding of a capturable plan (uniform over the block)
     const int ns = cb.nsplit < kAttMaxPieces ? cb.nsplit : kAttMaxPieces;
+    if (ns == 2) {
+      // a row split in two (the usual case): every thread derives its heads'
+      // weights itself, and its loads (both pieces' O and (max, sum) of two
+      // float4 groups at a time) go out together
+      const int L4 = L / 4, total = kCombHeads * L4;
+      const float *o0 = opart + static_cast<int64_t>(cb.first_slot) * H * L;
+      const float *o1 = o0 + static_cast<int64_t>(H) * L;
+      const float2 *ml0 = reinterpret_cast<const float2 *>(mlpart) + static_cast<int64_t>(cb.first_slot) * H;
+      const float2 *ml1 = ml0 + H;
+      for (int e0 = threadIdx.x; e0 < total; e0 += 2 * kCombThreads) {
+        float4 a[2], b[2];
+        float2 ma[2], mb[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int e = e0 + k * kCombThreads;
+          const int hh = e / L4, d = (e - hh * L4) * 4, h = h0 + hh;
+          if (e < total && h < H) {
+            a[k] = *reinterpret_cast<const float4 *>(o0 + static_cast<int64_t>(h) * L + d);
+            b[k] = *reinterpret_cast<const float4 *>(o1 + static_cast<int64_t>(h) * L + d);
+            ma[k] = ml0[h];
+            mb[k] = ml1[h];
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int e = e0 + k * kCombThreads;
+          const int hh = e / L4, d = (e - hh * L4) * 4, h = h0 + hh;
+          if (e >= total || h >= H) continue;
+          float m = sink ? sink[h] * kLog2e : -INFINITY;
+          m = fmaxf(m, ma[k].x);
+          m = fmaxf(m, mb[k].x);
+          const float wa = exp2f(ma[k].x - m), wb = exp2f(mb[k].x - m);
+          float lsum = sink ? exp2f(sink[h] * kLog2e - m) : 0.f;
+          lsum = fmaf(wa, ma[k].y, lsum);
+          lsum = fmaf(wb, mb[k].y, lsum);
+          const float f = lsum > 0.f ? 1.f / lsum : 0.f;
+          float4 acc;
+          acc.x = fmaf(wb, b[k].x, wa * a[k].x);
+          acc.y = fmaf(wb, b[k].y, wa * a[k].y);
+          acc.z = fmaf(wb, b[k].z, wa * a[k].z);
+          acc.w = fmaf(wb, b[k].w, wa * a[k].w);
+          const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * f, acc.y * f),
+                               hi = __floats2bfloat162_rn(acc.z * f, acc.w * f);
+          *reinterpret_cast<uint2 *>(out + (static_cast<int64_t>(cb.row) * H + h) * L + d) =
+              make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
+        }
+      }
+      continue;
+    }
     __syncthreads();   // the previous item's weights have been used
     if (threadIdx.x < kCombHeads && h0 + static_cast<int>(threadIdx.x) < H) {
       const int h = h0 + threadIdx.x;
