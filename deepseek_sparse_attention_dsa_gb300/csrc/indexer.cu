@@ -94,20 +94,33 @@ struct IdxParams {
 
 // sum_h w[h] * relu(sign * v[h]) with the weights read four at a time from
 // shared memory (one broadcast load per four heads) and four independent
-// accumulators (the FMA latency is not a chain over all heads).
+// accumulators (the FMA latency is not a chain over all heads), held as two
+// pairs for the packed fp32 FMA (fma.rn.f32x2: each lane is the same IEEE
+// fma as fmaf, so the sum is unchanged, in half the instructions).
+__device__ __forceinline__ uint64_t pack_f2(float x, float y) {
+  uint64_t u;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(u) : "f"(x), "f"(y));
+  return u;
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
 template <int HI>
 __device__ __forceinline__ float weighted_relu_sum(const float *w, const float (&v)[HI], float sign) {
   static_assert(HI % 4 == 0, "heads");
   const float4 *w4 = reinterpret_cast<const float4 *>(w);
-  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  uint64_t a01 = 0, a23 = 0;   // (+0, +0) pairs
 #pragma unroll
   for (int h = 0; h < HI; h += 4) {
     const float4 ww = w4[h / 4];
-    a0 = fmaf(ww.x, fmaxf(sign * v[h], 0.f), a0);
-    a1 = fmaf(ww.y, fmaxf(sign * v[h + 1], 0.f), a1);
-    a2 = fmaf(ww.z, fmaxf(sign * v[h + 2], 0.f), a2);
-    a3 = fmaf(ww.w, fmaxf(sign * v[h + 3], 0.f), a3);
+    a01 = ffma2(pack_f2(ww.x, ww.y), pack_f2(fmaxf(sign * v[h], 0.f), fmaxf(sign * v[h + 1], 0.f)), a01);
+    a23 = ffma2(pack_f2(ww.z, ww.w), pack_f2(fmaxf(sign * v[h + 2], 0.f), fmaxf(sign * v[h + 3], 0.f)), a23);
   }
+  float a0, a1, a2, a3;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(a01));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a2), "=f"(a3) : "l"(a23));
   return (a0 + a1) + (a2 + a3);
 }
 
