@@ -663,10 +663,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
           for (int c = 0; c < TH / 4; ++c) {
             const float4 v = xr[c ^ (h & 7)];
             // a + b == b + a in IEEE arithmetic: both CTAs get the same S
-            s[4 * c] += v.x;
-            s[4 * c + 1] += v.y;
-            s[4 * c + 2] += v.z;
-            s[4 * c + 3] += v.w;
+            f2_unpack(f2_add(f2_pack(s[4 * c], s[4 * c + 1]), f2_pack(v.x, v.y)), s[4 * c], s[4 * c + 1]);
+            f2_unpack(f2_add(f2_pack(s[4 * c + 2], s[4 * c + 3]), f2_pack(v.z, v.w)), s[4 * c + 2], s[4 * c + 3]);
           }
           // (scale_log2 > 0, so the max of the raw logits picks the same key)
           float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -694,17 +692,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
           alpha = fast_exp2(m_ref - tmax);
           m_ref = tmax;
         }
-        // P (bf16 pairs, lower key in the low half) for this warp's keys
-        float sm[4] = {0.f, 0.f, 0.f, 0.f};
+        // P (bf16 pairs, lower key in the low half) for this warp's keys; the
+        // row sum of the rounded P in four partial sums (key pair k into sum
+        // k mod 4), held as two pairs for the packed adds
+        uint64_t sm01 = 0, sm23 = 0;
         uint32_t packed[TH / 2];
+        const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nm2 = f2_pack(-m_ref, -m_ref);
 #pragma unroll
-        for (int i = 0; i < TH; i += 2) {
-          const __nv_bfloat162 pb = __floats2bfloat162_rn(fast_exp2(fmaf(s[i], p.scale_log2, -m_ref)),
-                                                          fast_exp2(fmaf(s[i + 1], p.scale_log2, -m_ref)));
-          const float2 pf = __bfloat1622float2(pb);
-          sm[(i >> 1) & 3] += pf.x + pf.y;
-          packed[i / 2] = *reinterpret_cast<const uint32_t *>(&pb);
+        for (int i = 0; i < TH; i += 8) {
+          float x[8];
+#pragma unroll
+          for (int j = 0; j < 8; j += 2) f2_unpack(f2_fma(f2_pack(s[i + j], s[i + j + 1]), sc2, nm2), x[j], x[j + 1]);
+          float2 pf[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const __nv_bfloat162 pb = __floats2bfloat162_rn(fast_exp2(x[2 * j]), fast_exp2(x[2 * j + 1]));
+            pf[j] = __bfloat1622float2(pb);
+            packed[i / 2 + j] = *reinterpret_cast<const uint32_t *>(&pb);
+          }
+          sm01 = f2_add(sm01, f2_add(f2_pack(pf[0].x, pf[1].x), f2_pack(pf[0].y, pf[1].y)));
+          sm23 = f2_add(sm23, f2_add(f2_pack(pf[2].x, pf[3].x), f2_pack(pf[2].y, pf[3].y)));
         }
+        float sm[4];
+        f2_unpack(sm01, sm[0], sm[1]);
+        f2_unpack(sm23, sm[2], sm[3]);
         l = l * alpha + ((sm[0] + sm[1]) + (sm[2] + sm[3]));
         // PV of tile g-1 (of this unit or the one before) must be done before
         // P is overwritten, and before O is rescaled (PV of g-2 finished
@@ -724,7 +735,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
             tmem_ld16(tmem_base + lane_base + C::O_COL + hf * (C::HALF / 2) + c0, o);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) o[i] *= alpha;
+            for (int i = 0; i < 16; i += 2)
+              f2_unpack(f2_mul(f2_pack(o[i], o[i + 1]), f2_pack(alpha, alpha)), o[i], o[i + 1]);
             tmem_st16(tmem_base + lane_base + C::O_COL + hf * (C::HALF / 2) + c0, o);
           }
         }

@@ -97,16 +97,6 @@ struct IdxParams {
 // accumulators (the FMA latency is not a chain over all heads), held as two
 // pairs for the packed fp32 FMA (fma.rn.f32x2: each lane is the same IEEE
 // fma as fmaf, so the sum is unchanged, in half the instructions).
-__device__ __forceinline__ uint64_t pack_f2(float x, float y) {
-  uint64_t u;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(u) : "f"(x), "f"(y));
-  return u;
-}
-__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
 template <int HI>
 __device__ __forceinline__ float weighted_relu_sum(const float *w, const float (&v)[HI], float sign) {
   static_assert(HI % 4 == 0, "heads");
@@ -115,12 +105,12 @@ __device__ __forceinline__ float weighted_relu_sum(const float *w, const float (
 #pragma unroll
   for (int h = 0; h < HI; h += 4) {
     const float4 ww = w4[h / 4];
-    a01 = ffma2(pack_f2(ww.x, ww.y), pack_f2(fmaxf(sign * v[h], 0.f), fmaxf(sign * v[h + 1], 0.f)), a01);
-    a23 = ffma2(pack_f2(ww.z, ww.w), pack_f2(fmaxf(sign * v[h + 2], 0.f), fmaxf(sign * v[h + 3], 0.f)), a23);
+    a01 = f2_fma(f2_pack(ww.x, ww.y), f2_pack(fmaxf(sign * v[h], 0.f), fmaxf(sign * v[h + 1], 0.f)), a01);
+    a23 = f2_fma(f2_pack(ww.z, ww.w), f2_pack(fmaxf(sign * v[h + 2], 0.f), fmaxf(sign * v[h + 3], 0.f)), a23);
   }
   float a0, a1, a2, a3;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(a01));
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a2), "=f"(a3) : "l"(a23));
+  f2_unpack(a01, a0, a1);
+  f2_unpack(a23, a2, a3);
   return (a0 + a1) + (a2 + a3);
 }
 
@@ -224,6 +214,11 @@ __global__ void __launch_bounds__(kIdxThreads, 2) index_tc_kernel(const __grid_c
       };
       int la0 = box_page(item.tile0), la1 = box_page(item.tile0 + 1), la2 = box_page(item.tile0 + 2),
           la3 = box_page(item.tile0 + 3);
+      // single-row (decode) score launches stream each key once: the keys go
+      // into L2 evict-first, so the scores (stored evict-last) are still there
+      // when the top-k reads them back; row groups re-read their keys
+      constexpr bool kHint = G == 1 && !BMAX;
+      const uint64_t kpol = kHint ? l2_policy_evict_first() : 0;
       for (int t = item.tile0; t < item.tile1; ++t) {
         const int nkeys = min(128, nrows_total - t * 128);
         const int nbox = (nkeys + p.BH - 1) / p.BH;
@@ -248,9 +243,11 @@ __global__ void __launch_bounds__(kIdxThreads, 2) index_tc_kernel(const __grid_c
           // box has >= 8 rows, so nbox * NCH <= 32)
           const int b = lane / C::NCH, c = lane % C::NCH;
           const int row = __shfl_sync(0xffffffffu, myrow, b & 31);
-          if (b < nbox && row >= 0)
-            tma_load_2d(sbase + C::OFF_K + stage * C::KT_BYTES + c * 128 * C::ROWB + b * p.BH * C::ROWB,
-                        &p.tm_keys, c * C::CH, row, kfull(stage));
+          const uint32_t dst = sbase + C::OFF_K + stage * C::KT_BYTES + c * 128 * C::ROWB + b * p.BH * C::ROWB;
+          if (b < nbox && row >= 0) {
+            if constexpr (kHint) tma_load_2d_hint(dst, &p.tm_keys, c * C::CH, row, kfull(stage), kpol);
+            else tma_load_2d(dst, &p.tm_keys, c * C::CH, row, kfull(stage));
+          }
         }
         if (++stage == C::STAGES) {
           stage = 0;
@@ -335,6 +332,7 @@ __global__ void __launch_bounds__(kIdxThreads, 2) index_tc_kernel(const __grid_c
         }
         named_bar_sync(1, 32 * kEpiWarps);
       }
+      const uint64_t spol = (G == 1 && !BMAX) ? l2_policy_evict_last() : 0;
       bool ok = true;
       for (int t = item.tile0; t < item.tile1; ++t) {
         // warp-uniform, as the TMEM loads below are warp-collective
@@ -365,7 +363,10 @@ __global__ void __launch_bounds__(kIdxThreads, 2) index_tc_kernel(const __grid_c
               }
             }
             if constexpr (!BMAX) {
-              if (key >= 0 && key <= pos0 + gg) p.scores[soff[gg] + key] = s;
+              if (key >= 0 && key <= pos0 + gg) {
+                if constexpr (G == 1) st_global_hint(p.scores + soff[gg] + key, s, spol);
+                else p.scores[soff[gg] + key] = s;
+              }
             } else {
               sv[gg] = s;
             }

@@ -143,6 +143,32 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm,
       "l"(tm), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
 }
+// L2 eviction-priority policies for the cache-hinted forms below (the whole
+// access, fraction 1.0): evict_first for a stream read once, evict_last for
+// data the next kernel of the step reads back.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// tma_load_2d with an L2 cache policy.
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap *tm, int32_t x, int32_t y,
+                                                 uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+      "{%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(tm), "r"(x), "r"(y), "r"(bar), "l"(pol)
+      : "memory");
+}
+// A 4-byte global store with an L2 cache policy.
+__device__ __forceinline__ void st_global_hint(float *ptr, float v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(ptr), "f"(v), "l"(pol) : "memory");
+}
 // Non-blocking test of an mbarrier phase.
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -155,6 +181,34 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// ----------------------------------------------------------------- packed fp32
+// Two floats in one 64-bit register for the paired fp32 instructions
+// (add/mul/fma .f32x2): each lane is the same IEEE round-to-nearest operation
+// as its scalar form, so results are unchanged, in half the instructions.
+__device__ __forceinline__ uint64_t f2_pack(float x, float y) {
+  uint64_t u;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(u) : "f"(x), "f"(y));
+  return u;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t u, float &x, float &y) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(u));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 // ----------------------------------------------------------------- cp.async
 // 16-byte copy that reads `src_bytes` (0 or 16) bytes and zero-fills the rest.
 __device__ __forceinline__ void cp_async_16_zfill(uint32_t dst, const void *src, uint32_t src_bytes) {
