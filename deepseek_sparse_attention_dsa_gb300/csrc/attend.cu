@@ -432,21 +432,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
         const uint32_t kst = sbase + C::OFF_K + st * C::STAGE;
         if constexpr (!FP8) {
           constexpr int ROWB = (L + R) * 2;
-          // piece q of a key: this CTA's q_nope columns, then its rope columns
-          for (int idx = pt; idx < T * C::PIECES; idx += kProdThreads) {
-            const int key = idx / C::PIECES, piece = idx - key * C::PIECES;
-            const int32_t prow = rows[key];
-            uint32_t dst;
-            int off;
-            if (piece < C::NPV * 8) {
-              dst = kst + (piece >> 3) * C::CHUNK + sw128_offset(key, piece & 7);
-              off = static_cast<int>(crank) * C::HALF * 2 + piece * 16;
-            } else {
-              dst = kst + C::NPV * C::CHUNK + sw64_offset(key, piece - C::NPV * 8);
-              off = L * 2 + static_cast<int>(crank) * C::RH * 2 + (piece - C::NPV * 8) * 16;
+          // piece q of a key: this CTA's q_nope columns, then its rope columns.
+          // Producer thread pt takes pieces pt, pt + 224, ...; the (key, piece)
+          // pair advances by (224 / PIECES, 224 % PIECES) with a carry.
+          constexpr int NIT = (T * C::PIECES + kProdThreads - 1) / kProdThreads;
+          constexpr int DK = kProdThreads / C::PIECES, DP = kProdThreads % C::PIECES;
+          int key = pt / C::PIECES, piece = pt - key * C::PIECES;
+          const int off_nope = static_cast<int>(crank) * C::HALF * 2;
+          const int off_rope = L * 2 + static_cast<int>(crank) * C::RH * 2 - C::NPV * 8 * 16;
+#pragma unroll
+          for (int u = 0; u < NIT; ++u) {
+            if (u + 1 < NIT || key < T) {
+              const int32_t prow = rows[key];
+              const bool rope = piece >= C::NPV * 8;
+              const uint32_t dst = rope ? kst + C::NPV * C::CHUNK + sw64_offset(key, piece - C::NPV * 8)
+                                        : kst + (piece >> 3) * C::CHUNK + sw128_offset(key, piece & 7);
+              const int off = (rope ? off_rope : off_nope) + piece * 16;
+              const uint8_t *src = p.latent + (prow >= 0 ? static_cast<int64_t>(prow) * ROWB + off : 0);
+              cp_async_16_zfill(dst, src, prow >= 0 ? 16u : 0u);
             }
-            const uint8_t *src = p.latent + (prow >= 0 ? static_cast<int64_t>(prow) * ROWB + off : 0);
-            cp_async_16_zfill(dst, src, prow >= 0 ? 16u : 0u);
+            piece += DP;
+            key += DK;
+            if (piece >= C::PIECES) {
+              piece -= C::PIECES;
+              ++key;
+            }
           }
           cp_async_mbar_arrive(kfull(st));
         } else {
