@@ -703,8 +703,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
           m_ref = tmax;
         }
         // P (bf16 pairs, lower key in the low half) for this warp's keys; the
-        // row sum of the rounded P in four partial sums (key pair k into sum
-        // k mod 4), held as two pairs for the packed adds
+        // row sum takes the fp32 probabilities before their bf16 rounding (no
+        // conversion back per key), in four partial sums (key pair k into
+        // sum k mod 4) held as two pairs for the packed adds
         uint64_t sm01 = 0, sm23 = 0;
         uint32_t packed[TH / 2];
         const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nm2 = f2_pack(-m_ref, -m_ref);
@@ -716,8 +717,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1)
           float2 pf[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const __nv_bfloat162 pb = __floats2bfloat162_rn(fast_exp2(x[2 * j]), fast_exp2(x[2 * j + 1]));
-            pf[j] = __bfloat1622float2(pb);
+            pf[j] = make_float2(fast_exp2(x[2 * j]), fast_exp2(x[2 * j + 1]));
+            const __nv_bfloat162 pb = __floats2bfloat162_rn(pf[j].x, pf[j].y);
             packed[i / 2 + j] = *reinterpret_cast<const uint32_t *>(&pb);
           }
           sm01 = f2_add(sm01, f2_add(f2_pack(pf[0].x, pf[1].x), f2_pack(pf[0].y, pf[1].y)));
